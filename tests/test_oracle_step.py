@@ -1,0 +1,276 @@
+"""Pins of the oracle's whole parallel-draft step (CPU only).
+
+* K = 1 reduces to ordinary next-token (EAGLE) drafting: an independently
+  written one-step drafter below, fed the shifted prompt pairing of "P-EAGLE:
+  parallel speculative decoding in vLLM" (Parallel drafting), gives the same
+  logits.
+* For K > 1 the same independent drafter, fed the NTP row and K-1 rows of
+  (h_shared, emb(mask)) at the next positions, gives the same logits: the MTP
+  placeholders of the same section.
+* Appending draft positions leaves earlier positions unchanged (causal mask).
+* All MASK slots carry identical inputs.
+* Batch order and physical block numbering do not matter.
+* The per-stream RMSNorm of "Attention Drift" (Observation 2) makes the step
+  invariant to the scale of each captured stream.
+* In bf16 mode every stored intermediate is a bf16 value.
+"""
+
+import dataclasses
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+from oracle import pe_oracle as O
+from speculative_drafting_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _setup(name, **over):
+    wl = W.get(name, **over)
+    b = W.make_batch(wl)
+    w = W.make_weights(wl)
+    kc, vc = W.make_kv_cache(wl, b["num_blocks"])
+    return wl, b, w, kc, vc
+
+
+# --------------------------------------------------------------------------
+# an independent plain drafter: explicit input rows -> logits (fp64, no rounding)
+
+
+def _f64(a, dt):
+    if dt == "bf16":
+        return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.asarray(a, np.float64)
+
+
+def _norm(v, g, eps):
+    d = v.shape[-1]
+    return v * g / np.sqrt(np.linalg.norm(v) ** 2 / d + eps)
+
+
+def _rot(x, p, theta):
+    # rotary embedding as a complex rotation of (x_i, x_{i+hd/2})
+    hd = x.shape[-1]
+    h = hd // 2
+    z = (x[:h] + 1j * x[h:]) * np.exp(1j * p * theta ** (-np.arange(0, hd, 2) / hd))
+    return np.concatenate([z.real, z.imag])
+
+
+def plain_drafter(dm, w, rows, prior_k, prior_v):
+    """rows: list of (streams[3][d], emb[d], position).  prior_k/v: dict
+    position -> [G][hd] for cached positions.  Every row attends to every key
+    at a position <= its own.  Returns logits [len(rows)][V]."""
+    dt = dm.dtype
+    P = {k: _f64(v, dt) for k, v in w.items()}
+    H, G, hd = dm.n_heads, dm.n_kv_heads, dm.head_dim
+    xs, keys, vals = [], dict(prior_k), dict(prior_v)
+    qs = []
+    for streams, e, p in rows:
+        inp = np.concatenate([_norm(streams[s], P["gamma_stream"][s], dm.eps) for s in range(3)] + [e])
+        x = P["w_fc"].dot(inp)
+        u = x if dm.post_norm else _norm(x, P["gamma_in"], dm.eps)
+        qkv = P["w_qkv"].dot(u)
+        q = np.stack([_rot(qkv[h * hd:(h + 1) * hd], p, dm.rope_theta) for h in range(H)])
+        kk = np.stack([_rot(qkv[(H + g) * hd:(H + g + 1) * hd], p, dm.rope_theta) for g in range(G)])
+        vv = np.stack([qkv[(H + G + g) * hd:(H + G + g + 1) * hd] for g in range(G)])
+        keys[p], vals[p] = kk, vv
+        xs.append(x)
+        qs.append(q)
+    out = []
+    for (streams, e, p), x, q in zip(rows, xs, qs):
+        ps = sorted(t for t in keys if t <= p)
+        Kt = np.stack([keys[t] for t in ps])
+        Vt = np.stack([vals[t] for t in ps])
+        o = []
+        for h in range(H):
+            g = h * G // H
+            pr = scipy.special.softmax(Kt[:, g, :].dot(q[h]) / np.sqrt(hd))
+            o.append(pr.dot(Vt[:, g, :]))
+        att = P["w_o"].dot(np.concatenate(o))
+
+        def mlp(m):
+            gate = P["w_gate"].dot(m)
+            return P["w_down"].dot(gate * scipy.special.expit(gate) * P["w_up"].dot(m))
+
+        if dm.post_norm:
+            a = _norm(x + att, P["gamma_post"], dm.eps)
+            z = _norm(a + mlp(a), P["gamma_final"], dm.eps)
+        else:
+            a = x + att
+            y = a + mlp(_norm(a, P["gamma_post"], dm.eps))
+            z = _norm(y, P["gamma_final"], dm.eps)
+        out.append(P["w_lm"].dot(z))
+    return np.stack(out)
+
+
+def _prior(b, kc, vc, dm, r):
+    c = int(b["prev_pos"][b["qsl"][r]])
+    pk, pv = {}, {}
+    for p in range(c):
+        blk = b["block_table"][r][p // dm.block_size]
+        pk[p] = _f64(kc[blk, :, p % dm.block_size, :], dm.dtype)
+        pv[p] = _f64(vc[blk, :, p % dm.block_size, :], dm.dtype)
+    return pk, pv
+
+
+def _explicit_rows(dm, b, w, r):
+    """The pages' input construction for request r, written out directly."""
+    dt = dm.dtype
+    q0, q1 = int(b["qsl"][r]), int(b["qsl"][r + 1])
+    a = int(b["accepted"][r])
+    emb = _f64(w["emb"], dt)
+    H = _f64(b["H_tgt"], dt)
+    rows = []
+    for j in range(a + 1):
+        nxt = int(b["bonus"][r]) if j == a else int(b["prev_tok"][q0 + j + 1])
+        rows.append((H[q0 + j], emb[nxt], int(b["prev_pos"][q0 + j])))
+    hs = np.stack([_f64(w["h_shared"], dt)] * 3)
+    p0 = int(b["prev_pos"][q0 + a])
+    for m in range(1, dm.K):
+        rows.append((hs, _f64(w["emb_mask"], dt), p0 + m))
+    return rows
+
+
+@pytest.mark.parametrize("post_norm", [False, True])
+def test_k1_reduces_to_next_token_drafting(post_norm):
+    wl, b, w, kc, vc = _setup("tiny_fp32", K=1, post_norm=post_norm)
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    for r in range(wl.batch):
+        rows = _explicit_rows(wl.dims, b, w, r)
+        assert len(rows) == int(b["accepted"][r]) + 1
+        ref = plain_drafter(wl.dims, w, rows, *_prior(b, kc, vc, wl.dims, r))
+        np.testing.assert_allclose(res["req"][r]["logits"][0], ref[-1], rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("post_norm", [False, True])
+def test_mask_rows_match_independent_drafter(post_norm):
+    wl, b, w, kc, vc = _setup("tiny_fp32", post_norm=post_norm)
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    for r in range(wl.batch):
+        rows = _explicit_rows(wl.dims, b, w, r)
+        ref = plain_drafter(wl.dims, w, rows, *_prior(b, kc, vc, wl.dims, r))
+        np.testing.assert_allclose(res["req"][r]["logits"], ref[-wl.dims.K:], rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("name", ["small_prenorm", "small_postnorm_hd128"])
+def test_appending_draft_positions_leaves_earlier_ones_unchanged(name):
+    wl, b, w, kc, vc = _setup(name)
+    K = wl.dims.K
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    # two more draft positions: the block table must cover them
+    wl2 = dataclasses.replace(wl, dims=dataclasses.replace(wl.dims, K=K + 2))
+    b2 = W.make_batch(wl2)
+    assert np.array_equal(b2["prev_tok"], b["prev_tok"])
+    kc2, vc2 = W.make_kv_cache(wl2, b2["num_blocks"])
+    # give the second cache the same prior context, position by position
+    bs = wl.dims.block_size
+    for r in range(wl.batch):
+        for p in range(int(b["prev_pos"][b["qsl"][r]])):
+            blk1 = b["block_table"][r][p // bs]
+            blk2 = b2["block_table"][r][p // bs]
+            kc2[blk2, :, p % bs] = kc[blk1, :, p % bs]
+            vc2[blk2, :, p % bs] = vc[blk1, :, p % bs]
+    res2 = O.draft_step(wl2.dims, w, b2, kc2, vc2)
+    for r in range(wl.batch):
+        np.testing.assert_array_equal(res2["req"][r]["z"][:K], res["req"][r]["z"])
+        np.testing.assert_allclose(res2["req"][r]["logits"][:K], res["req"][r]["logits"], rtol=0, atol=1e-12)
+
+
+def test_all_mask_slots_carry_identical_inputs():
+    wl, b, w, kc, vc = _setup("small_prenorm")
+    meta, G, E, A = O.prepare_inputs(wl.dims, w, b)
+    mrows = np.nonzero(meta["is_masked"])[0]
+    assert len(mrows) == wl.batch * (wl.dims.K - 1)
+    for o in mrows[1:]:
+        assert np.array_equal(A[o], A[mrows[0]])
+        assert np.array_equal(G[o], G[mrows[0]])
+    # and the hidden part is h_shared in all three stream slots
+    hs = O.bf16_decode(w["h_shared"])
+    for s in range(3):
+        assert np.array_equal(G[mrows[0], s], hs)
+
+
+def test_batch_order_does_not_matter():
+    wl, b, w, kc, vc = _setup("small_prenorm")
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    perm = [2, 0, 1]
+    n = np.diff(b["qsl"])
+    b2 = dict(b)
+    b2["qsl"] = np.concatenate([[0], np.cumsum(n[perm])]).astype(np.int32)
+    for key in ("prev_tok", "prev_pos", "H_tgt"):
+        b2[key] = np.concatenate([b[key][b["qsl"][r]:b["qsl"][r + 1]] for r in perm])
+    for key in ("accepted", "bonus", "block_table"):
+        b2[key] = b[key][perm]
+    res2 = O.draft_step(wl.dims, w, b2, kc, vc)
+    for i, r in enumerate(perm):
+        np.testing.assert_array_equal(res2["req"][i]["logits"], res["req"][r]["logits"])
+
+
+def test_block_numbering_does_not_matter():
+    wl, b, w, kc, vc = _setup("small_postnorm_hd128")
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    g = np.random.default_rng(9)
+    pi = g.permutation(b["num_blocks"])
+    b2 = dict(b)
+    t = b["block_table"].copy()
+    t[t >= 0] = pi[t[t >= 0]]
+    b2["block_table"] = t
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[pi], vc2[pi] = kc, vc
+    res2 = O.draft_step(wl.dims, w, b2, kc2, vc2)
+    for r in range(wl.batch):
+        np.testing.assert_array_equal(res2["req"][r]["logits"], res["req"][r]["logits"])
+        np.testing.assert_array_equal(res2["req"][r]["slot"] // wl.dims.block_size,
+                                      pi[res["req"][r]["slot"] // wl.dims.block_size])
+
+
+def test_per_stream_scale_invariance():
+    wl, b, w, kc, vc = _setup("tiny_fp32", eps=0.0)
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    b2 = dict(b)
+    b2["H_tgt"] = b["H_tgt"] * np.array([7.0, 0.01, 300.0], np.float32)[None, :, None]
+    res2 = O.draft_step(wl.dims, w, b2, kc, vc)
+    for r in range(wl.batch):
+        np.testing.assert_allclose(res2["req"][r]["A"], res["req"][r]["A"], rtol=1e-6, atol=1e-7)
+        np.testing.assert_allclose(res2["req"][r]["logits"], res["req"][r]["logits"], rtol=0, atol=1e-6)
+
+
+def test_bf16_mode_stores_bf16_values_and_tracks_fp64():
+    wl, b, w, kc, vc = _setup("small_prenorm")
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    # the same data with no rounding anywhere
+    w64 = {k: O.bf16_decode(v).astype(np.float32) for k, v in w.items()}
+    b64 = dict(b)
+    b64["H_tgt"] = O.bf16_decode(b["H_tgt"]).astype(np.float32)
+    dm64 = dataclasses.replace(wl.dims, dtype="f32")
+    res64 = O.draft_step(dm64, w64, b64, O.bf16_decode(kc).astype(np.float32),
+                         O.bf16_decode(vc).astype(np.float32))
+    for r in range(wl.batch):
+        rr = res["req"][r]
+        for key in ("A", "x", "u", "k", "v", "q", "attn", "a", "z"):
+            assert np.array_equal(O.bf16_round(rr[key]), rr[key]), key
+        diff = np.abs(rr["logits"] - res64["req"][r]["logits"]).max()
+        assert diff < 0.05, diff
+
+
+def test_table1_stream_rms_equalised_by_per_stream_norm():
+    # Attention Drift, Table 1: verifier stream RMS (h_low, h_mid, h_high) per model
+    rows = []
+    with open(os.path.join(GOLDEN, "attention_drift_table1_rms.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                name, lo, mid, hi = line.rsplit(None, 3)
+                rows.append((name, float(lo), float(mid), float(hi)))
+    assert len(rows) == 5
+    g = np.random.default_rng(10)
+    d = 4096
+    for name, *r in rows:
+        Gs = np.stack([g.standard_normal(d) * s for s in r])[None]
+        before = O.rms(Gs[0])
+        A = O.drafter_input(Gs, np.zeros((1, d)), np.ones((3, d)), 1e-6, "f32")
+        after = [O.rms(A[0, s * d:(s + 1) * d]) for s in range(3)]
+        np.testing.assert_allclose(before, r, rtol=0.05)
+        np.testing.assert_allclose(after, 1.0, atol=2e-3)
