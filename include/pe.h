@@ -1,0 +1,209 @@
+/*
+ * pe.h -- C-ABI of the P-EAGLE parallel-draft step on one GB300 (sm_103a).
+ *
+ * One parallel-draft step turns the previous verify batch of a ragged set of
+ * requests into K draft tokens per request with a single drafter forward pass.
+ * The calls below follow the problem statement of "P-EAGLE: parallel
+ * speculative decoding in vLLM":
+ *   pe_prepare_inputs  the fused batch-metadata build ("Fused Triton kernel":
+ *                      copy previous token ids and positions, insert the bonus
+ *                      token, fill the parallel-draft slots with the MASK id,
+ *                      emit the rejected-token mask, the masked-token mask and
+ *                      the hidden-state map; rejected tokens map to
+ *                      PADDING_SLOT_ID = -1 per "KV cache and CUDA graphs"),
+ *                      the hidden-state copy / h_shared broadcast
+ *                      ("Hidden-state management") and the drafter input, which
+ *                      applies an RMSNorm to each captured target stream
+ *                      ("Attention Drift", section 4.1, Observation 2) and
+ *                      concatenates them with the token embedding.
+ *   pe_draft_step      the drafter pass ("Parallel drafting": all positions go
+ *                      through the layer at once): fc projection, one decoder
+ *                      layer (QKV, RoPE, paged KV write, paged attention over
+ *                      the context plus earlier draft positions, SwiGLU MLP,
+ *                      pre-norm or post-norm residuals) and the final norm.
+ *   pe_argmax          the LM head fused with a per-row greedy argmax.
+ *
+ * Conventions for every call
+ *   - All tensor arguments are DEVICE pointers owned by the caller; the library
+ *     never frees or keeps them past the call (weights excepted: pe_create
+ *     borrows them for the handle's lifetime).  Layouts are dense row-major.
+ *   - Floating tensors have the handle's dtype: float (PE_DTYPE_F32) or bf16
+ *     bit patterns (PE_DTYPE_BF16), except where a signature says float.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on it: no allocation, no host
+ *     synchronisation, no stream creation, so a step can be captured in a CUDA
+ *     graph.  Host-side sizes (B, T_in, ...) are baked into a capture.
+ *   - `ws` is a caller-allocated device workspace of at least
+ *     pe_workspace_bytes() bytes, 256-byte aligned; one workspace must not be
+ *     used by two calls that may run concurrently.
+ *   - Return value: PE_OK, or an error code below.  PE_ERR_ARG / PE_ERR_UNSUPPORTED
+ *     are detected on the host before anything is enqueued.  PE_ERR_CUDA means
+ *     a launch failed (cudaGetLastError).  Problems that only the device can see
+ *     (an out-of-range accepted count, block id or token id, an exhausted bounded
+ *     wait) do not fault: the kernel clamps or skips the access and ORs a bit
+ *     into the status word in `ws`; read it with pe_read_status after the work.
+ *   - No exception crosses this interface.
+ */
+#ifndef PE_H
+#define PE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define PE_OK 0
+#define PE_ERR_ARG 1          /* null pointer, bad size, workspace too small */
+#define PE_ERR_UNSUPPORTED 2  /* dims outside what the kernels handle */
+#define PE_ERR_CUDA 3         /* a CUDA runtime call or launch failed */
+#define PE_ERR_DEVICE_INPUT 4 /* pe_read_status: the status word has input bits */
+#define PE_ERR_TIMEOUT 5      /* pe_read_status: a bounded device wait gave up */
+
+/* device status word bits (pe_read_status) */
+#define PE_ST_ACCEPTED_RANGE 0x1u /* a_r outside [0, n_r-1] (clamped) or n_r < 1 */
+#define PE_ST_BLOCK_RANGE 0x2u    /* position past the block table, block id outside
+                                     [0, num_blocks) or negative position: slot -1,
+                                     the key is skipped by attention */
+#define PE_ST_TOKEN_RANGE 0x4u    /* token id outside [0, V): embedding row 0 is used */
+#define PE_ST_TIMEOUT 0x10u       /* a bounded wait inside a kernel expired */
+
+/* padding slot of rejected rows ("KV cache and CUDA graphs") */
+#define PE_PADDING_SLOT_ID (-1)
+
+enum { PE_DTYPE_F32 = 0, PE_DTYPE_BF16 = 1 };
+
+/* Drafter and step dimensions.  Supported: n_streams == 3; d, inter, vocab,
+ * head_dim multiples of 8; n_heads a multiple of n_kv_heads; head_dim in
+ * {16, 32, 64, 128} (bf16 needs 64 or 128); 1 <= K <= 16; block_size >= 1;
+ * n_heads / n_kv_heads * K <= 128 for bf16. */
+typedef struct pe_dims {
+  int32_t d;          /* drafter hidden size (and each captured stream's width) */
+  int32_t n_streams;  /* captured target streams: h_low, h_mid, h_high (3) */
+  int32_t n_heads;    /* H, query heads */
+  int32_t n_kv_heads; /* G, KV heads; query head h reads KV head h / (H/G) */
+  int32_t head_dim;   /* hd */
+  int32_t inter;      /* I, SwiGLU intermediate size */
+  int32_t vocab;      /* V */
+  int32_t K;          /* draft depth: K draft tokens per request */
+  int32_t block_size; /* bs, tokens per paged-KV block */
+  int32_t mask_id;    /* MASK token id written into the parallel-draft slots */
+  int32_t post_norm;  /* 0: pre-norm layer; 1: post-norm layer */
+  int32_t dtype;      /* PE_DTYPE_F32 or PE_DTYPE_BF16 */
+  float eps;          /* RMSNorm epsilon */
+  float rope_theta;   /* RoPE base */
+} pe_dims;
+
+/* Drafter parameters: device pointers, borrowed for the handle's lifetime. */
+typedef struct pe_weights {
+  const void* emb;          /* [V][d] token embedding */
+  const void* emb_mask;     /* [d] learned emb(mask) for the MASK slots */
+  const void* h_shared;     /* [d] learned shared hidden state for the MASK slots,
+                               placed in all three stream slots */
+  const void* gamma_stream; /* [3][d] RMSNorm gains of the captured streams */
+  const void* w_fc;         /* [d][4d] fc: [h_low | h_mid | h_high | emb] -> d */
+  const void* gamma_in;     /* [d] pre-norm: norm before QKV (unused post-norm) */
+  const void* w_qkv;        /* [(H+2G)*hd][d]: H q heads, then G k, then G v heads */
+  const void* w_o;          /* [d][H*hd] */
+  const void* gamma_post;   /* [d] pre-norm: MLP input norm; post-norm: norm after
+                               the attention residual */
+  const void* w_gate;       /* [I][d] */
+  const void* w_up;         /* [I][d] */
+  const void* w_down;       /* [d][I] */
+  const void* gamma_final;  /* [d] pre-norm: final norm; post-norm: norm after the
+                               MLP residual */
+  const void* w_lm;         /* [V][d] LM head */
+} pe_weights;
+
+/* Drafter-batch metadata: caller-owned device buffers written by
+ * pe_prepare_inputs and read by pe_draft_step.  T_out = T_in + B*(K-1).
+ * Request r's output rows are out_qsl[r] .. out_qsl[r+1]-1: its n_r copied rows
+ * (row j pairs the hidden state of input row j with the next token, the bonus
+ * token at j = a_r; rows past a_r are rejected) followed by K-1 MASK rows at
+ * positions prev_pos[a_r] + 1 .. + K-1. */
+typedef struct pe_meta {
+  int32_t* out_qsl;     /* [B+1] output row offsets */
+  int32_t* tok;         /* [T_out] drafter input token */
+  int64_t* pos;         /* [T_out] position */
+  uint8_t* is_rejected; /* [T_out] 1 for rejected rows */
+  uint8_t* is_masked;   /* [T_out] 1 for MASK rows */
+  int32_t* hidden_src;  /* [T_out] input row of the hidden state, -1 = h_shared */
+  int64_t* slot;        /* [T_out] KV slot, PE_PADDING_SLOT_ID for rejected rows */
+  int32_t* valid_qsl;   /* [B+1] exclusive scan of a_r + K */
+  int32_t* valid_rows;  /* [T_out] output rows that are not rejected, in order;
+                           -1 past n_valid */
+  int32_t* n_valid;     /* [1] number of non-rejected rows */
+  int32_t* sample_idx;  /* [B*K] output row predicting draft k of request r (r*K+k) */
+  int32_t* seq_len;     /* [B] cache positions visible after the step: prev_pos[a_r]+K */
+} pe_meta;
+
+typedef struct pe_handle pe_handle;
+
+/* Create a handle for one drafter.  Validates dims (PE_ERR_UNSUPPORTED) and
+ * pointers (PE_ERR_ARG), selects the kernels and encodes the TMA descriptors of
+ * the weight matrices.  Uses the current CUDA device; *out is NULL on error. */
+int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out);
+
+/* Destroy a handle (NULL is ignored).  Does not touch the weights. */
+void pe_destroy(pe_handle* h);
+
+/* Workspace bytes that cover every call with at most max_batch requests,
+ * max_rows_in previous verify rows in total and block tables of at most
+ * max_blocks_per_seq entries per request.  0 on bad arguments. */
+size_t pe_workspace_bytes(const pe_handle* h, int max_batch, int max_rows_in,
+                          int max_blocks_per_seq);
+
+/* Steps (1)-(3): batch metadata, hidden-state map and drafter input.
+ *   qsl[B+1]        int32, input row offsets of the previous verify batch
+ *   prev_tok[T_in]  int32 token ids;  prev_pos[T_in] int64 positions
+ *   accepted[B]     int32 a_r, accepted drafts, 0 <= a_r <= n_r - 1
+ *   bonus[B]        int32 bonus (correction) token b_r
+ *   block_table[B][max_blocks] int32 physical KV block ids; num_blocks bounds them
+ *   H_tgt[T_in][3][d] captured target hidden states (h_low, h_mid, h_high)
+ *   meta            output metadata buffers (all fields required)
+ *   G_out  [T_out][3][d]  nullable: hidden-state map; MASK rows get h_shared
+ *   E_out  [T_out][d]     nullable: embedding rows; MASK rows get emb(mask)
+ *   A_out  [T_out][4d]    nullable: drafter input of the non-rejected rows in
+ *                         valid_rows order (row i <-> valid_rows[i]):
+ *                         [RMSNorm(h_low), RMSNorm(h_mid), RMSNorm(h_high), emb]
+ * Clears the status word in ws, then ORs in any input problem it finds. */
+int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl,
+                      const int32_t* prev_tok, const int64_t* prev_pos,
+                      const int32_t* accepted, const int32_t* bonus,
+                      const int32_t* block_table, int max_blocks, int num_blocks,
+                      const void* H_tgt, const pe_meta* meta, void* G_out, void* E_out,
+                      void* A_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Step (4): the drafter layer for the batch prepared by pe_prepare_inputs.
+ *   A         [T_out][4d] drafter input from pe_prepare_inputs (A_out)
+ *   k_cache, v_cache  [num_blocks][G][block_size][hd] paged KV caches; this
+ *             step's non-rejected rows are written at meta->slot (never at -1),
+ *             then attention reads them back
+ *   z_out     [B*K][d] normalised final hidden state of the K sample rows of each
+ *             request (row r*K + k predicts draft token k+1 of request r)
+ * block_table / max_blocks / num_blocks as passed to pe_prepare_inputs. */
+int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void* A,
+                  const int32_t* block_table, int max_blocks, int num_blocks,
+                  void* k_cache, void* v_cache, void* z_out, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/* Step (5): LM head fused with argmax.  draft_tokens[n] = argmax_v z[n] . w_lm[v]
+ * (lowest index on ties; fp32 logits).  logits [n_rows][V] float is nullable:
+ * when given, the fp32 logits are stored too. */
+int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, float* logits,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* Copy the device status word from ws into *status (synchronises `stream`);
+ * clear it when `clear` is non-zero.  Returns PE_OK when no bit is set,
+ * PE_ERR_TIMEOUT when PE_ST_TIMEOUT is set, else PE_ERR_DEVICE_INPUT. */
+int pe_read_status(const pe_handle* h, void* ws, uint32_t* status, int clear, void* stream);
+
+/* Static text for a return code. */
+const char* pe_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PE_H */

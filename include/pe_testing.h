@@ -1,0 +1,40 @@
+/*
+ * pe_testing.h -- unit-test hook of libpe: one drafter projection in isolation.
+ *
+ * Not part of the parallel-draft step.  It runs exactly the kernel the step runs
+ * for one of the drafter's projections (tcgen05 GEMM for bf16, SIMT GEMM for
+ * fp32) so tests can check that kernel alone against a matrix product.  Same
+ * conventions as pe.h: device pointers owned by the caller, asynchronous on
+ * `stream`, no allocation.
+ */
+#ifndef PE_TESTING_H
+#define PE_TESTING_H
+
+#include "pe.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  PE_PROJ_FC = 0,     /* X [n][4d]   . w_fc^T   -> float [n][d]        */
+  PE_PROJ_QKV = 1,    /* X [n][d]    . w_qkv^T  -> float [n][(H+2G)hd] */
+  PE_PROJ_O = 2,      /* X [n][H hd] . w_o^T    -> float [n][d]        */
+  PE_PROJ_SWIGLU = 3, /* silu(X w_gate^T) * (X w_up^T) -> dtype [n][I] */
+  PE_PROJ_DOWN = 4,   /* X [n][I]    . w_down^T -> float [n][d]        */
+  PE_PROJ_LM = 5      /* X [n][d]    . w_lm^T   -> float [n][V]        */
+};
+
+/* Workspace bytes pe_test_projection needs for n_rows rows (0 on bad input). */
+size_t pe_test_projection_workspace(const pe_handle* h, int which, int n_rows);
+
+/* Run projection `which` over n_rows rows of X (the handle's dtype, row-major).
+ * Returns PE_ERR_ARG / PE_ERR_UNSUPPORTED on bad input, PE_ERR_CUDA on a launch
+ * failure.  The status word is the first 4 bytes of ws (pe_read_status). */
+int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void* out, void* ws,
+                       size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PE_TESTING_H */

@@ -1,0 +1,573 @@
+// C-ABI of the P-EAGLE parallel-draft step: handle, workspace layout and the
+// three step calls (include/pe.h documents every argument).
+//
+// All work is enqueued on the caller's stream; nothing here allocates device
+// memory, synchronises the host or creates streams, except pe_read_status, which
+// synchronises the stream to read the status word back.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "pe_internal.h"
+#include "pe_prep.h"
+#include "pe_testing.h"
+
+using namespace pe;
+
+struct pe_handle {
+  pe_dims d;
+  pe_weights w;
+  int num_sms;
+  CUtensorMap m_fc, m_qkv, m_o, m_gate, m_up, m_down, m_lm;
+  double inv_freq[64];
+};
+
+namespace {
+
+enum GemmId { G_FC = 0, G_QKV, G_O, G_GATEUP, G_DOWN, G_LM, G_COUNT };
+
+size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+size_t esize(const pe_handle* h) { return h->d.dtype == PE_DTYPE_BF16 ? 2 : 4; }
+bool is_bf16(const pe_handle* h) { return h->d.dtype == PE_DTYPE_BF16; }
+
+struct GemmShape {
+  int M, K, dual;
+};
+
+GemmShape gemm_shape(const pe_handle* h, int id) {
+  const pe_dims& d = h->d;
+  switch (id) {
+    case G_FC: return {d.d, 4 * d.d, 0};
+    case G_QKV: return {(d.n_heads + 2 * d.n_kv_heads) * d.head_dim, d.d, 0};
+    case G_O: return {d.d, d.n_heads * d.head_dim, 0};
+    case G_GATEUP: return {d.inter, d.d, 1};
+    case G_DOWN: return {d.d, d.inter, 0};
+    default: return {d.vocab, d.d, 0};
+  }
+}
+
+TcPlan plan_of(const pe_handle* h, int id, int N) {
+  const GemmShape s = gemm_shape(h, id);
+  return plan_gemm_tc(s.M, s.K, N, s.dual, h->num_sms, true);
+}
+
+// Largest split-K partial buffer and counter count over every N <= N_max.
+// Within one count of N tiles the split count is fixed and the bytes grow with
+// N, so the top of each range is enough.
+void gemm_scratch_bound(const pe_handle* h, int id, int N_max, size_t& partial, int& counters) {
+  partial = 0;
+  counters = 0;
+  if (!is_bf16(h) || N_max <= 0) return;
+  const int nt_max = (N_max + 255) / 256;
+  for (int nt = 1; nt <= nt_max; ++nt) {
+    const TcPlan p = plan_of(h, id, std::min(256 * nt, N_max));
+    partial = std::max(partial, p.partial_bytes);
+    counters = std::max(counters, p.n_counters);
+  }
+}
+
+// Attention split partials, bounded over every batch size <= B (the split count
+// rises as the batch shrinks).
+size_t attn_scratch_bound(const pe_handle* h, int B, int max_blocks) {
+  if (!is_bf16(h)) return 0;
+  const pe_dims& d = h->d;
+  size_t best = 0;
+  const long Lmax = static_cast<long>(max_blocks) * d.block_size;
+  const long chunks = std::max<long>(1, (Lmax + 63) / 64);
+  for (int b = 1; b <= B; ++b) {
+    const long heads = static_cast<long>(b) * d.n_kv_heads;
+    long ns = (2L * h->num_sms + heads - 1) / heads;
+    ns = std::max<long>(1, std::min(ns, chunks));
+    best = std::max(best, attention_scratch_bytes(b, d.K, d.n_heads, d.head_dim, static_cast<int>(ns)));
+  }
+  return best;
+}
+
+struct Layout {
+  size_t status, counters, x, u, qkv, q_s, x_s, attn, r1, a, m, hm, y, amax, partial, attn_part;
+  size_t total;
+  int counter_off[G_COUNT];
+  int n_counters;
+};
+
+// Workspace layout of a step with B requests, T_in verify rows and block tables
+// of max_blocks entries.  Each region is sized by a bound that only grows with
+// (B, T_in, max_blocks), so a workspace sized for the maxima fits every call.
+Layout layout_of(const pe_handle* h, int B, int T_in, int max_blocks) {
+  const pe_dims& d = h->d;
+  const size_t e = esize(h);
+  const int T_out = T_in + B * (d.K - 1);
+  const int NS = B * d.K;
+  const int Hd = d.n_heads * d.head_dim;
+  const int QKV = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = al256(off + bytes);
+    return o;
+  };
+  L.status = take(256);
+  const int Ns[G_COUNT] = {T_out, T_out, NS, NS, NS, NS};
+  size_t part = 0;
+  int nc = 0;
+  for (int g = 0; g < G_COUNT; ++g) {
+    size_t p;
+    int c;
+    gemm_scratch_bound(h, g, Ns[g], p, c);
+    part = std::max(part, p);
+    L.counter_off[g] = nc;
+    nc += c;
+  }
+  L.n_counters = nc;
+  L.counters = take(static_cast<size_t>(std::max(nc, 1)) * sizeof(int));
+  L.x = take(static_cast<size_t>(T_out) * d.d * e);
+  L.u = take(static_cast<size_t>(T_out) * d.d * e);
+  L.qkv = take(static_cast<size_t>(T_out) * QKV * sizeof(float));
+  L.q_s = take(static_cast<size_t>(NS) * Hd * e);
+  L.x_s = take(static_cast<size_t>(NS) * d.d * e);
+  L.attn = take(static_cast<size_t>(NS) * Hd * e);
+  L.r1 = take(static_cast<size_t>(NS) * d.d * e);
+  L.a = take(static_cast<size_t>(NS) * d.d * e);
+  L.m = take(static_cast<size_t>(NS) * d.d * e);
+  L.hm = take(static_cast<size_t>(NS) * d.inter * e);
+  L.y = take(static_cast<size_t>(NS) * d.d * e);
+  L.amax = take(static_cast<size_t>(NS) * sizeof(unsigned long long));
+  L.partial = take(part);
+  L.attn_part = take(attn_scratch_bound(h, B, max_blocks));
+  L.total = off;
+  return L;
+}
+
+// Workspace of pe_argmax for n_rows rows.
+Layout layout_argmax(const pe_handle* h, int n_rows) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = al256(off + bytes);
+    return o;
+  };
+  L.status = take(256);
+  size_t part;
+  int nc;
+  gemm_scratch_bound(h, G_LM, n_rows, part, nc);
+  L.counter_off[G_LM] = 0;
+  L.n_counters = nc;
+  L.counters = take(static_cast<size_t>(std::max(nc, 1)) * sizeof(int));
+  L.amax = take(static_cast<size_t>(n_rows) * sizeof(unsigned long long));
+  L.partial = take(part);
+  L.total = off;
+  return L;
+}
+
+// Workspace of one projection (test hook) over n_rows rows.
+Layout layout_projection(const pe_handle* h, int which, int n_rows) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = al256(off + bytes);
+    return o;
+  };
+  L.status = take(256);
+  size_t part;
+  int nc;
+  gemm_scratch_bound(h, which, n_rows, part, nc);
+  L.counter_off[which] = 0;
+  L.n_counters = nc;
+  L.counters = take(static_cast<size_t>(std::max(nc, 1)) * sizeof(int));
+  L.partial = take(part);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int check_meta(const pe_meta* m) {
+  if (!m || !m->out_qsl || !m->tok || !m->pos || !m->is_rejected || !m->is_masked ||
+      !m->hidden_src || !m->slot || !m->valid_qsl || !m->valid_rows || !m->n_valid ||
+      !m->sample_idx || !m->seq_len)
+    return PE_ERR_ARG;
+  return PE_OK;
+}
+
+// One projection of the step, on the tensor cores (bf16) or SIMT (fp32).
+int run_gemm(pe_handle* h, int id, const void* X, int N_cap, const int* n_rows_dev,
+             const Epilogue& epi, void* ws, const Layout& L, cudaStream_t st) {
+  const GemmShape s = gemm_shape(h, id);
+  if (!is_bf16(h)) {
+    const pe_weights& w = h->w;
+    const void* W = id == G_FC ? w.w_fc : id == G_QKV ? w.w_qkv : id == G_O ? w.w_o
+                  : id == G_GATEUP ? w.w_gate : id == G_DOWN ? w.w_down : w.w_lm;
+    const void* W2 = id == G_GATEUP ? w.w_up : nullptr;
+    return launch_gemm_f32(static_cast<const float*>(W), static_cast<const float*>(W2),
+                           static_cast<const float*>(X), s.M, s.K, N_cap, n_rows_dev, epi, st);
+  }
+  const TcPlan p = plan_of(h, id, N_cap);
+  const CUtensorMap* mA = id == G_FC ? &h->m_fc : id == G_QKV ? &h->m_qkv : id == G_O ? &h->m_o
+                        : id == G_GATEUP ? &h->m_gate : id == G_DOWN ? &h->m_down : &h->m_lm;
+  const CUtensorMap* mA2 = id == G_GATEUP ? &h->m_up : nullptr;
+  return launch_gemm_tc(p, mA, mA2, X, n_rows_dev, epi, at<float>(ws, L.partial),
+                        at<int>(ws, L.counters) + L.counter_off[id], at<uint32_t>(ws, L.status), st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out) {
+  if (!out) return PE_ERR_ARG;
+  *out = nullptr;
+  if (!dims || !w) return PE_ERR_ARG;
+  const pe_dims& d = *dims;
+  const bool bf = d.dtype == PE_DTYPE_BF16;
+  if (d.dtype != PE_DTYPE_BF16 && d.dtype != PE_DTYPE_F32) return PE_ERR_UNSUPPORTED;
+  if (d.n_streams != 3 || d.d <= 0 || d.d % 8 || d.inter <= 0 || d.inter % 8 || d.vocab <= 0 ||
+      d.vocab % 8 || d.n_heads <= 0 || d.n_kv_heads <= 0 || d.n_heads % d.n_kv_heads ||
+      d.head_dim <= 0 || d.head_dim % 8 || d.head_dim > 128 || d.K < 1 || d.K > 64 ||
+      d.block_size < 1 || !(d.eps >= 0.f) || !(d.rope_theta > 0.f))
+    return PE_ERR_UNSUPPORTED;
+  if (bf && ((d.head_dim != 64 && d.head_dim != 128) ||
+             d.K * (d.n_heads / d.n_kv_heads) > 128))
+    return PE_ERR_UNSUPPORTED;
+  const void* req[] = {w->emb,    w->emb_mask, w->h_shared, w->gamma_stream, w->w_fc,
+                       w->w_qkv,  w->w_o,      w->gamma_post, w->w_gate,   w->w_up,
+                       w->w_down, w->gamma_final, w->w_lm};
+  for (const void* p : req)
+    if (!p || !aligned16(p)) return PE_ERR_ARG;
+  if (!d.post_norm && (!w->gamma_in || !aligned16(w->gamma_in))) return PE_ERR_ARG;
+  pe_handle* h = new (std::nothrow) pe_handle;
+  if (!h) return PE_ERR_ARG;
+  std::memset(h, 0, sizeof(*h));
+  h->d = d;
+  h->w = *w;
+  h->num_sms = num_sms_of_current_device();
+  if (h->num_sms <= 0) {
+    delete h;
+    return PE_ERR_CUDA;
+  }
+  for (int i = 0; i < d.head_dim / 2; ++i)
+    h->inv_freq[i] = std::pow(static_cast<double>(d.rope_theta),
+                              -2.0 * static_cast<double>(i) / static_cast<double>(d.head_dim));
+  if (bf) {
+    const int QKV = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
+    bool ok = encode_tmap_bf16(&h->m_fc, w->w_fc, d.d, 4ull * d.d, 128) &&
+              encode_tmap_bf16(&h->m_qkv, w->w_qkv, QKV, d.d, 128) &&
+              encode_tmap_bf16(&h->m_o, w->w_o, d.d, static_cast<uint64_t>(d.n_heads) * d.head_dim, 128) &&
+              encode_tmap_bf16(&h->m_gate, w->w_gate, d.inter, d.d, 128) &&
+              encode_tmap_bf16(&h->m_up, w->w_up, d.inter, d.d, 128) &&
+              encode_tmap_bf16(&h->m_down, w->w_down, d.d, d.inter, 128) &&
+              encode_tmap_bf16(&h->m_lm, w->w_lm, d.vocab, d.d, 128);
+    if (!ok) {
+      delete h;
+      return PE_ERR_CUDA;
+    }
+  }
+  *out = h;
+  return PE_OK;
+}
+
+void pe_destroy(pe_handle* h) { delete h; }
+
+size_t pe_workspace_bytes(const pe_handle* h, int max_batch, int max_rows_in,
+                          int max_blocks_per_seq) {
+  if (!h || max_batch < 1 || max_rows_in < 1 || max_blocks_per_seq < 1) return 0;
+  const Layout a = layout_of(h, max_batch, max_rows_in, max_blocks_per_seq);
+  const Layout b = layout_argmax(h, max_batch * h->d.K);
+  return std::max(a.total, b.total);
+}
+
+int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl, const int32_t* prev_tok,
+                      const int64_t* prev_pos, const int32_t* accepted, const int32_t* bonus,
+                      const int32_t* block_table, int max_blocks, int num_blocks,
+                      const void* H_tgt, const pe_meta* meta, void* G_out, void* E_out,
+                      void* A_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!h || B < 1 || T_in < B || max_blocks < 1 || num_blocks < 1 || !qsl || !prev_tok ||
+      !prev_pos || !accepted || !bonus || !block_table || !H_tgt || !ws)
+    return PE_ERR_ARG;
+  if (check_meta(meta) != PE_OK) return PE_ERR_ARG;
+  if (ws_bytes < 256 || !aligned16(ws) || !aligned16(H_tgt)) return PE_ERR_ARG;
+  if ((G_out && !aligned16(G_out)) || (E_out && !aligned16(E_out)) || (A_out && !aligned16(A_out)))
+    return PE_ERR_ARG;
+  const pe_dims& d = h->d;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* status = at<uint32_t>(ws, 0);
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return PE_ERR_CUDA;
+  MetaLaunch ml;
+  ml.B = B;
+  ml.T_in = T_in;
+  ml.K = d.K;
+  ml.mask_id = d.mask_id;
+  ml.bs = d.block_size;
+  ml.max_blocks = max_blocks;
+  ml.num_blocks = num_blocks;
+  ml.vocab = d.vocab;
+  ml.qsl = qsl;
+  ml.prev_tok = prev_tok;
+  ml.prev_pos = prev_pos;
+  ml.accepted = accepted;
+  ml.bonus = bonus;
+  ml.block_table = block_table;
+  ml.meta = *meta;
+  ml.status = status;
+  int rc = launch_meta(ml, st);
+  if (rc != PE_OK) return rc;
+  const int T_out = T_in + B * (d.K - 1);
+  if (G_out || E_out) {
+    GatherArgs g{};
+    g.T_out = T_out;
+    g.T_in = T_in;
+    g.d = d.d;
+    g.vocab = d.vocab;
+    g.hidden_src = meta->hidden_src;
+    g.tok = meta->tok;
+    g.is_masked = meta->is_masked;
+    g.H_tgt = H_tgt;
+    g.h_shared = h->w.h_shared;
+    g.emb = h->w.emb;
+    g.emb_mask = h->w.emb_mask;
+    g.G = G_out;
+    g.E = E_out;
+    g.status = status;
+    rc = launch_gather(g, d.dtype, h->num_sms, st);
+    if (rc != PE_OK) return rc;
+  }
+  if (A_out) {
+    InputArgs ia{};
+    ia.T_out = T_out;
+    ia.T_in = T_in;
+    ia.d = d.d;
+    ia.vocab = d.vocab;
+    ia.eps = d.eps;
+    ia.n_valid = meta->n_valid;
+    ia.valid_rows = meta->valid_rows;
+    ia.hidden_src = meta->hidden_src;
+    ia.tok = meta->tok;
+    ia.is_masked = meta->is_masked;
+    ia.H_tgt = H_tgt;
+    ia.h_shared = h->w.h_shared;
+    ia.emb = h->w.emb;
+    ia.emb_mask = h->w.emb_mask;
+    ia.gamma_stream = h->w.gamma_stream;
+    ia.A = A_out;
+    ia.status = status;
+    rc = launch_input(ia, d.dtype, st);
+    if (rc != PE_OK) return rc;
+  }
+  return PE_OK;
+}
+
+int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void* A,
+                  const int32_t* block_table, int max_blocks, int num_blocks, void* k_cache,
+                  void* v_cache, void* z_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!h || B < 1 || T_in < B || max_blocks < 1 || num_blocks < 1 || !A || !block_table ||
+      !k_cache || !v_cache || !z_out || !ws)
+    return PE_ERR_ARG;
+  if (check_meta(meta) != PE_OK) return PE_ERR_ARG;
+  if (!aligned16(A) || !aligned16(z_out) || !aligned16(ws)) return PE_ERR_ARG;
+  const pe_dims& d = h->d;
+  const Layout L = layout_of(h, B, T_in, max_blocks);
+  if (ws_bytes < L.total) return PE_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T_out = T_in + B * (d.K - 1);
+  const int NS = B * d.K;
+  const int Hd = d.n_heads * d.head_dim;
+  const int QKV = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  const int dt = d.dtype;
+  if (L.n_counters > 0 &&
+      cudaMemsetAsync(at<int>(ws, L.counters), 0, L.n_counters * sizeof(int), st) != cudaSuccess)
+    return PE_ERR_CUDA;
+  void* x = at<void>(ws, L.x);
+  void* u = d.post_norm ? x : at<void>(ws, L.u);
+  void* qkv = at<void>(ws, L.qkv);
+  void* q_s = at<void>(ws, L.q_s);
+  void* x_s = at<void>(ws, L.x_s);
+  void* attn = at<void>(ws, L.attn);
+  void* r1 = at<void>(ws, L.r1);
+  void* a = at<void>(ws, L.a);
+  void* m = at<void>(ws, L.m);
+  void* hm = at<void>(ws, L.hm);
+  void* y = at<void>(ws, L.y);
+  int rc;
+  // fc: x = A W_fc^T over the non-rejected rows
+  Epilogue e;
+  e.mode = EPI_STORE;
+  e.out = x;
+  e.ld_out = d.d;
+  if ((rc = run_gemm(h, G_FC, A, T_out, meta->n_valid, e, ws, L, st)) != PE_OK) return rc;
+  // pre-norm: u = RMSNorm(x; gamma_in)
+  if (!d.post_norm &&
+      (rc = launch_rmsnorm(x, d.d, h->w.gamma_in, u, d.d, d.d, d.eps, T_out, meta->n_valid, dt,
+                           st)) != PE_OK)
+    return rc;
+  // QKV (fp32, RoPE follows)
+  e = Epilogue();
+  e.mode = EPI_STORE_F32;
+  e.out = qkv;
+  e.ld_out = QKV;
+  if ((rc = run_gemm(h, G_QKV, u, T_out, meta->n_valid, e, ws, L, st)) != PE_OK) return rc;
+  // RoPE, KV write at the non-rejected slots, sample-row q and residual rows
+  RopeArgs ra{};
+  ra.T_out = T_out;
+  ra.B = B;
+  ra.K = d.K;
+  ra.H = d.n_heads;
+  ra.G = d.n_kv_heads;
+  ra.hd = d.head_dim;
+  ra.d = d.d;
+  ra.bs = d.block_size;
+  ra.num_blocks = num_blocks;
+  ra.qkv = static_cast<const float*>(qkv);
+  ra.x = x;
+  ra.n_valid = meta->n_valid;
+  ra.valid_rows = meta->valid_rows;
+  ra.valid_qsl = meta->valid_qsl;
+  ra.pos = meta->pos;
+  ra.slot = meta->slot;
+  ra.k_cache = k_cache;
+  ra.v_cache = v_cache;
+  ra.q_s = q_s;
+  ra.x_s = x_s;
+  std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
+  ra.status = status;
+  if ((rc = launch_rope_kv(ra, dt, st)) != PE_OK) return rc;
+  // paged attention of the sample rows
+  AttnArgs aa{};
+  aa.B = B;
+  aa.K = d.K;
+  aa.H = d.n_heads;
+  aa.G = d.n_kv_heads;
+  aa.hd = d.head_dim;
+  aa.bs = d.block_size;
+  aa.max_blocks = max_blocks;
+  aa.num_blocks = num_blocks;
+  plan_attention(B, d.n_kv_heads, d.K, d.n_heads, d.head_dim, max_blocks, d.block_size,
+                 h->num_sms, aa.n_splits, aa.split_len);
+  aa.q = q_s;
+  aa.k_cache = k_cache;
+  aa.v_cache = v_cache;
+  aa.block_table = block_table;
+  aa.seq_len = meta->seq_len;
+  aa.part_o = at<float>(ws, L.attn_part);
+  aa.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + L.attn_part +
+                                        al256(static_cast<size_t>(aa.n_splits) * NS * d.n_heads *
+                                              d.head_dim * sizeof(float)));
+  aa.out = attn;
+  aa.status = status;
+  if ((rc = launch_attention(aa, dt, st)) != PE_OK) return rc;
+  // O projection + residual
+  e = Epilogue();
+  e.mode = EPI_RESID;
+  e.out = d.post_norm ? r1 : a;
+  e.ld_out = d.d;
+  e.resid = x_s;
+  e.ld_resid = d.d;
+  if ((rc = run_gemm(h, G_O, attn, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
+  // post-norm: a = RMSNorm(r1; gamma_post); pre-norm: m = RMSNorm(a; gamma_post)
+  if (d.post_norm) {
+    if ((rc = launch_rmsnorm(r1, d.d, h->w.gamma_post, a, d.d, d.d, d.eps, NS, nullptr, dt, st)) != PE_OK)
+      return rc;
+  } else {
+    if ((rc = launch_rmsnorm(a, d.d, h->w.gamma_post, m, d.d, d.d, d.eps, NS, nullptr, dt, st)) != PE_OK)
+      return rc;
+  }
+  // SwiGLU: hm = silu(gate) * up
+  e = Epilogue();
+  e.mode = EPI_SWIGLU;
+  e.out = hm;
+  e.ld_out = d.inter;
+  if ((rc = run_gemm(h, G_GATEUP, d.post_norm ? a : m, NS, nullptr, e, ws, L, st)) != PE_OK)
+    return rc;
+  // down projection + residual
+  e = Epilogue();
+  e.mode = EPI_RESID;
+  e.out = y;
+  e.ld_out = d.d;
+  e.resid = a;
+  e.ld_resid = d.d;
+  if ((rc = run_gemm(h, G_DOWN, hm, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
+  // z = RMSNorm(y; gamma_final)
+  (void)Hd;
+  return launch_rmsnorm(y, d.d, h->w.gamma_final, z_out, d.d, d.d, d.eps, NS, nullptr, dt, st);
+}
+
+int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, float* logits,
+              void* ws, size_t ws_bytes, void* stream) {
+  if (!h || !z || n_rows < 1 || !draft_tokens || !ws) return PE_ERR_ARG;
+  if (!aligned16(z) || !aligned16(ws)) return PE_ERR_ARG;
+  const Layout L = layout_argmax(h, n_rows);
+  if (ws_bytes < L.total) return PE_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned long long* keys = at<unsigned long long>(ws, L.amax);
+  if (cudaMemsetAsync(keys, 0, static_cast<size_t>(n_rows) * sizeof(unsigned long long), st) !=
+      cudaSuccess)
+    return PE_ERR_CUDA;
+  if (L.n_counters > 0 &&
+      cudaMemsetAsync(at<int>(ws, L.counters), 0, L.n_counters * sizeof(int), st) != cudaSuccess)
+    return PE_ERR_CUDA;
+  Epilogue e;
+  e.mode = EPI_ARGMAX;
+  e.amax = keys;
+  e.logits = logits;
+  e.ld_logits = h->d.vocab;
+  int rc = run_gemm(h, G_LM, z, n_rows, nullptr, e, ws, L, st);
+  if (rc != PE_OK) return rc;
+  return launch_argmax_finalize(keys, n_rows, draft_tokens, st);
+}
+
+size_t pe_test_projection_workspace(const pe_handle* h, int which, int n_rows) {
+  if (!h || which < 0 || which >= G_COUNT || n_rows < 1) return 0;
+  return layout_projection(h, which, n_rows).total;
+}
+
+int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void* out, void* ws,
+                       size_t ws_bytes, void* stream) {
+  if (!h || which < 0 || which >= G_COUNT || n_rows < 1 || !X || !out || !ws) return PE_ERR_ARG;
+  if (!aligned16(X) || !aligned16(ws)) return PE_ERR_ARG;
+  const Layout L = layout_projection(h, which, n_rows);
+  if (ws_bytes < L.total) return PE_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (L.n_counters > 0 &&
+      cudaMemsetAsync(at<int>(ws, L.counters), 0, L.n_counters * sizeof(int), st) != cudaSuccess)
+    return PE_ERR_CUDA;
+  Epilogue e;
+  e.mode = which == G_GATEUP ? EPI_SWIGLU : EPI_STORE_F32;
+  e.out = out;
+  e.ld_out = gemm_shape(h, which).M;
+  return run_gemm(h, which, X, n_rows, nullptr, e, ws, L, st);
+}
+
+int pe_read_status(const pe_handle* h, void* ws, uint32_t* status, int clear, void* stream) {
+  if (!h || !ws || !status) return PE_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return PE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PE_ERR_CUDA;
+  if (clear && cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return PE_ERR_CUDA;
+  *status = v;
+  if (v & PE_ST_TIMEOUT) return PE_ERR_TIMEOUT;
+  return v ? PE_ERR_DEVICE_INPUT : PE_OK;
+}
+
+const char* pe_status_string(int code) {
+  switch (code) {
+    case PE_OK: return "ok";
+    case PE_ERR_ARG: return "invalid argument (null pointer, size, alignment or workspace too small)";
+    case PE_ERR_UNSUPPORTED: return "unsupported dimensions";
+    case PE_ERR_CUDA: return "CUDA runtime or launch error";
+    case PE_ERR_DEVICE_INPUT: return "the device found out-of-range inputs (see the status bits)";
+    case PE_ERR_TIMEOUT: return "a bounded device wait expired";
+    default: return "unknown status code";
+  }
+}
+
+}  // extern "C"

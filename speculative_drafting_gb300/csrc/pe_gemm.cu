@@ -1,0 +1,573 @@
+// Drafter projections: D[t][f] = sum_k X[t][k] * W[f][k] with a fused epilogue.
+//
+// bf16: a persistent tcgen05 kernel.  The weight matrix is the MMA's M side
+// (128 output features per tile) and the token rows are its N side (16..256
+// per tile), so a decode-sized batch still fills the 128-row tensor-core tile
+// and the weights stream through shared memory exactly once per N tile.  Warp 0
+// issues TMA loads (128-byte swizzle, weights marked evict-first, tokens
+// evict-last) into a ring of shared-memory stages; one thread of warp 1 issues
+// tcgen05.mma into a TMEM accumulator; warps 2-5 read the accumulator with
+// tcgen05.ld and run the epilogue.  Small-N projections split K across CTAs so
+// every SM streams weights; the last CTA of a tile sums the fp32 partials in a
+// fixed order (deterministic) and runs the epilogue.
+//
+// fp32: a plain shared-memory-tiled SIMT kernel with the same epilogues (fp32
+// FMA; TF32 would not meet a 1e-5 logit tolerance).
+#include <algorithm>
+#include <cstdio>
+
+#include "pe_common.cuh"
+#include "pe_internal.h"
+
+namespace pe {
+
+constexpr int kBM = 128;  // weight rows per tile (MMA M)
+constexpr int kBK = 64;   // reduction elements per k-block: one 128-byte swizzle row
+constexpr int kMaxStages = 8;
+constexpr int kTcThreads = 192;
+constexpr uint32_t kABytes = kBM * kBK * 2;
+
+struct TcArgs {
+  int M, K, N_cap, dual;
+  int BN, n_tiles, m_tiles, k_splits, kb_per_split, num_kb, stages;
+  uint32_t tmem_cols;
+  const int* n_rows_dev;
+  Epilogue epi;
+  float* partial;  // [k_splits][N_cap][n_acc][M]
+  int* counters;   // [m_tiles * n_tiles]
+  uint32_t* status;
+};
+
+// ------------------------------------------------------------------ epilogue math
+
+template <typename T>
+PE_DEV void epi_store_elem(const Epilogue& e, int f, int t, float v, float v2) {
+  switch (e.mode) {
+    case EPI_STORE:
+      static_cast<T*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] = Elem<T>::from_f(v);
+      break;
+    case EPI_STORE_F32:
+      static_cast<float*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] = v;
+      break;
+    case EPI_RESID: {
+      const float r =
+          Elem<T>::to_f(static_cast<const T*>(e.resid)[static_cast<size_t>(t) * e.ld_resid + f]);
+      static_cast<T*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] = Elem<T>::from_f(v + r);
+      break;
+    }
+    case EPI_SWIGLU: {
+      const float s = v / (1.0f + expf(-v));
+      static_cast<T*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] = Elem<T>::from_f(s * v2);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+PE_DEV unsigned long long warp_max_u64(unsigned long long k) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
+    k = other > k ? other : k;
+  }
+  return k;
+}
+
+// Epilogue of 16 token columns j0..j0+15 for feature f (this thread's TMEM lane).
+// Called by all 128 epilogue threads together (ARGMAX uses named barrier 1).
+PE_DEV void tc_epilogue16(const TcArgs& p, int f, int j0, const float* v, const float* v2,
+                          int n_rows, unsigned long long (*red)[16], int ew, int et) {
+  const Epilogue& e = p.epi;
+  const bool fok = f < p.M;
+  if (e.mode != EPI_ARGMAX) {
+    if (!fok) return;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (j0 + i < n_rows) epi_store_elem<bf16>(e, f, j0 + i, v[i], v2 ? v2[i] : 0.f);
+    return;
+  }
+  if (e.logits && fok) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (j0 + i < n_rows) e.logits[static_cast<size_t>(j0 + i) * e.ld_logits + f] = v[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const unsigned long long k = warp_max_u64(fok ? argmax_key(v[i], f) : 0ull);
+    if ((threadIdx.x & 31) == 0) red[ew][i] = k;
+  }
+  named_bar_sync(1, 128);
+  if (et < 16 && j0 + et < n_rows) {
+    unsigned long long k = red[0][et];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) k = red[w][et] > k ? red[w][et] : k;
+    if (k) atomicMax(&e.amax[j0 + et], k);
+  }
+  named_bar_sync(1, 128);
+}
+
+// ------------------------------------------------------------------ tcgen05 kernel
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
+                   const __grid_constant__ CUtensorMap mapB, const TcArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t tfull_bar, tempty_bar, final_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh, n_rows_sh, last_sh;
+  __shared__ unsigned long long red_sh[4][16];
+  __shared__ int ep_ok[2][4];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int nA = p.dual ? 2 : 1;
+  const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * 128u;
+  const uint32_t stage_bytes = kABytes * nA + b_bytes;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&tfull_bar, 1);
+    mbar_init(&tempty_bar, 128);
+    mbar_init(&final_bar, 1);
+    abort_sh = 0;
+    int n = p.N_cap;
+    if (p.n_rows_dev) {
+      const int v = *p.n_rows_dev;
+      n = v < 0 ? 0 : (v < n ? v : n);
+    }
+    n_rows_sh = n;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&mapA);
+    if (p.dual) prefetch_tmap(&mapA2);
+    prefetch_tmap(&mapB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = tmem_base_sh;
+  const int n_rows = n_rows_sh;
+  const int total = p.m_tiles * p.n_tiles * p.k_splits;
+  volatile int* abort_flag = &abort_sh;
+  auto fail = [&]() {
+    abort_sh = 1;
+    set_status(p.status, PE_ST_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;  // per-stage: ever armed / parity of last arm
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const int n = t % p.n_tiles, rest = t / p.n_tiles;
+        const int ks = rest % p.k_splits, m = rest / p.k_splits;
+        if (n * p.BN >= n_rows) continue;
+        const int kb0 = ks * p.kb_per_split;
+        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            fail();
+            break;
+          }
+          uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes;
+          mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
+          tma_load_2d(sa, &mapA, &full_bar[stage], kb * kBK, m * kBM, pol_w);
+          if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], kb * kBK, m * kBM, pol_w);
+          tma_load_2d(sa + kABytes * nA, &mapB, &full_bar[stage], kb * kBK, n * p.BN, pol_x);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let copies already in flight land before the CTA's shared memory goes away
+        for (int s = 0; s < p.stages; ++s)
+          if (armed & (1u << s)) {
+            int dummy = 0;
+            mbar_wait(&full_bar[s], (armed_parity >> s) & 1u, &dummy);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (one thread)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, p.BN);
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const int n = t % p.n_tiles, rest = t / p.n_tiles;
+        const int ks = rest % p.k_splits;
+        if (n * p.BN >= n_rows) continue;
+        const int kb0 = ks * p.kb_per_split;
+        const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+        if (!mbar_wait(&tempty_bar, acc_phase ^ 1u, abort_flag)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
+          const uint64_t adesc = sw128_kmajor_desc(sa);
+          const uint64_t a2desc = sw128_kmajor_desc(sa + kABytes);
+          const uint64_t bdesc = sw128_kmajor_desc(sa + kABytes * nA);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // advance 16 elements (32 bytes) along K inside the swizzle row
+            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+            umma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, acc);
+            if (p.dual)
+              umma_bf16(tmem_base + static_cast<uint32_t>(p.BN), a2desc + 2 * kk, bdesc + 2 * kk,
+                        idesc, acc);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar);
+        acc_phase ^= 1u;
+      }
+      // every MMA issued by this thread has finished before TMEM is released
+      umma_commit(&final_bar);
+      int dummy = 0;
+      mbar_wait(&final_bar, 0, &dummy);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    const int et = threadIdx.x - 64;
+    uint32_t acc_phase = 0;
+    const int nacc = nA;
+    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      const int n = t % p.n_tiles, rest = t / p.n_tiles;
+      const int ks = rest % p.k_splits, m = rest / p.k_splits;
+      if (n * p.BN >= n_rows) continue;
+      // the four epilogue warps decide together whether to go on, so none of
+      // them can be left waiting at a named barrier the others skipped
+      const bool ok = mbar_wait(&tfull_bar, acc_phase, abort_flag);
+      if (lane == 0) ep_ok[acc_phase][ew] = ok ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!(ep_ok[acc_phase][0] && ep_ok[acc_phase][1] && ep_ok[acc_phase][2] &&
+            ep_ok[acc_phase][3])) {
+        fail();
+        break;
+      }
+      tc_fence_after();
+      const int f = m * kBM + q * 32 + lane;
+      const int jt = n * p.BN;
+      const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      if (p.k_splits == 1) {
+        for (int c = 0; c < p.BN; c += 16) {
+          float v[16], v2[16];
+          tmem_ld16(tl + c, v);
+          if (p.dual) tmem_ld16(tl + p.BN + c, v2);
+          tc_epilogue16(p, f, jt + c, v, p.dual ? v2 : nullptr, n_rows, red_sh, ew, et);
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar);
+      } else {
+        for (int c = 0; c < p.BN; c += 16) {
+          float v[16], v2[16];
+          tmem_ld16(tl + c, v);
+          if (p.dual) tmem_ld16(tl + p.BN + c, v2);
+          if (f < p.M) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = jt + c + i;
+              if (j < n_rows) {
+                const size_t base = (static_cast<size_t>(ks) * p.N_cap + j) * nacc;
+                p.partial[base * p.M + f] = v[i];
+                if (p.dual) p.partial[(base + 1) * p.M + f] = v2[i];
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar);
+        // the last split of this (m, n) tile sums the partials in split order
+        __threadfence();
+        named_bar_sync(1, 128);
+        const int tile_mn = m * p.n_tiles + n;
+        if (et == 0) last_sh = (atomicAdd(&p.counters[tile_mn], 1) == p.k_splits - 1);
+        named_bar_sync(1, 128);
+        if (last_sh) {
+          __threadfence();
+          for (int c = 0; c < p.BN; c += 16) {
+            float v[16], v2[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              v[i] = 0.f;
+              v2[i] = 0.f;
+            }
+            if (f < p.M) {
+              for (int s = 0; s < p.k_splits; ++s) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const int j = jt + c + i;
+                  if (j < n_rows) {
+                    const size_t base = (static_cast<size_t>(s) * p.N_cap + j) * nacc;
+                    v[i] += __ldcg(&p.partial[base * p.M + f]);
+                    if (p.dual) v2[i] += __ldcg(&p.partial[(base + 1) * p.M + f]);
+                  }
+                }
+              }
+            }
+            tc_epilogue16(p, f, jt + c, v, p.dual ? v2 : nullptr, n_rows, red_sh, ew, et);
+          }
+          if (et == 0) p.counters[tile_mn] = 0;
+        }
+      }
+      acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+// ------------------------------------------------------------------ host: plan + launch
+
+TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int num_sms, bool allow_split) {
+  TcPlan pl{};
+  pl.M = M;
+  pl.K = K;
+  pl.N_cap = N_cap < 1 ? 1 : N_cap;
+  pl.dual = dual;
+  const int nt = (pl.N_cap + 255) / 256;
+  int bn = (pl.N_cap + nt - 1) / nt;
+  bn = (bn + 15) / 16 * 16;
+  pl.BN = bn < 16 ? 16 : bn;
+  pl.n_tiles = nt;
+  pl.m_tiles = (M + kBM - 1) / kBM;
+  pl.num_kb = (K + kBK - 1) / kBK;
+  const int base = pl.m_tiles * pl.n_tiles;
+  int best = 1;
+  if (allow_split && base < num_sms) {
+    double best_cost = 1e30;
+    for (int s = 1; s <= 64; ++s) {
+      const int kbs = (pl.num_kb + s - 1) / s;
+      if (s > 1 && kbs < 4) break;
+      const int ss = (pl.num_kb + kbs - 1) / kbs;
+      const long tiles = static_cast<long>(base) * ss;
+      const long waves = (tiles + num_sms - 1) / num_sms;
+      const double cost = static_cast<double>(waves) * kbs + (ss > 1 ? 2.0 : 0.0);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best = ss;
+      }
+    }
+  }
+  pl.kb_per_split = (pl.num_kb + best - 1) / best;
+  pl.k_splits = (pl.num_kb + pl.kb_per_split - 1) / pl.kb_per_split;
+  const int nA = dual ? 2 : 1;
+  const size_t stage_bytes = static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128;
+  int stages = static_cast<int>((200u * 1024u) / stage_bytes);
+  pl.stages = std::max(2, std::min(kMaxStages, stages));
+  pl.smem_bytes = pl.stages * stage_bytes + 1024;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(pl.BN * nA)) cols <<= 1;
+  pl.tmem_cols = static_cast<int>(cols);
+  const long total = static_cast<long>(base) * pl.k_splits;
+  pl.grid = static_cast<int>(std::min<long>(total, num_sms));
+  pl.partial_bytes = 0;
+  if (pl.k_splits > 1) {
+    pl.partial_bytes = static_cast<size_t>(pl.k_splits) * pl.N_cap * nA * M * sizeof(float);
+    pl.partial_bytes = (pl.partial_bytes + 255) / 256 * 256;
+  }
+  pl.n_counters = base;
+  return pl;
+}
+
+int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap* mapA2,
+                   const void* X, const int* n_rows_dev, const Epilogue& epi, float* partial,
+                   int* counters, uint32_t* status, cudaStream_t st) {
+  if (pl.dual && !mapA2) return PE_ERR_ARG;
+  if (pl.k_splits > 1 && (!partial || !counters)) return PE_ERR_ARG;
+  CUtensorMap mapB;
+  if (!encode_tmap_bf16(&mapB, X, static_cast<uint64_t>(pl.N_cap), static_cast<uint64_t>(pl.K),
+                        static_cast<uint32_t>(pl.BN)))
+    return PE_ERR_CUDA;
+  TcArgs a{};
+  a.M = pl.M;
+  a.K = pl.K;
+  a.N_cap = pl.N_cap;
+  a.dual = pl.dual;
+  a.BN = pl.BN;
+  a.n_tiles = pl.n_tiles;
+  a.m_tiles = pl.m_tiles;
+  a.k_splits = pl.k_splits;
+  a.kb_per_split = pl.kb_per_split;
+  a.num_kb = pl.num_kb;
+  a.stages = pl.stages;
+  a.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
+  a.n_rows_dev = n_rows_dev;
+  a.epi = epi;
+  a.status = status;
+  a.partial = partial;
+  a.counters = counters;
+  if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(pl.smem_bytes)) != cudaSuccess)
+    return PE_ERR_CUDA;
+  gemm_tc_kernel<<<pl.grid, kTcThreads, pl.smem_bytes, st>>>(*mapA, pl.dual ? *mapA2 : *mapA,
+                                                              mapB, a);
+  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ fp32 SIMT kernel
+
+constexpr int kSt = 64;  // tile edge (features x tokens)
+constexpr int kSk = 16;  // reduction chunk
+
+__global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ W,
+                                                       const float* __restrict__ W2,
+                                                       const float* __restrict__ X, int M, int K,
+                                                       int N_cap, const int* n_rows_dev,
+                                                       Epilogue e) {
+  __shared__ float Ws[kSk][kSt + 1];
+  __shared__ float W2s[kSk][kSt + 1];
+  __shared__ float Xs[kSk][kSt + 1];
+  int n_rows = N_cap;
+  if (n_rows_dev) n_rows = min(max(*n_rows_dev, 0), N_cap);
+  const int f0 = blockIdx.x * kSt, t0 = blockIdx.y * kSt;
+  if (t0 >= n_rows) return;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const bool dual = W2 != nullptr;
+  float acc[4][4] = {}, acc2[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += kSk) {
+    for (int i = threadIdx.x; i < kSt * kSk; i += 256) {
+      const int r = i / kSk, kk = i % kSk;
+      const int f = f0 + r, t = t0 + r, k = k0 + kk;
+      Ws[kk][r] = (f < M && k < K) ? W[static_cast<size_t>(f) * K + k] : 0.f;
+      if (dual) W2s[kk][r] = (f < M && k < K) ? W2[static_cast<size_t>(f) * K + k] : 0.f;
+      Xs[kk][r] = (t < n_rows && k < K) ? X[static_cast<size_t>(t) * K + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kSk; ++kk) {
+      float wv[4], w2v[4], xv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        wv[i] = Ws[kk][tx * 4 + i];
+        w2v[i] = dual ? W2s[kk][tx * 4 + i] : 0.f;
+        xv[i] = Xs[kk][ty * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = fmaf(wv[i], xv[j], acc[i][j]);
+          acc2[i][j] = fmaf(w2v[i], xv[j], acc2[i][j]);
+        }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int t = t0 + ty * 4 + j;
+    if (t >= n_rows) continue;
+    if (e.mode == EPI_ARGMAX) {
+      unsigned long long best = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int f = f0 + tx * 4 + i;
+        if (f >= M) continue;
+        if (e.logits) e.logits[static_cast<size_t>(t) * e.ld_logits + f] = acc[i][j];
+        const unsigned long long k = argmax_key(acc[i][j], f);
+        best = k > best ? k : best;
+      }
+      if (best) atomicMax(&e.amax[t], best);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int f = f0 + tx * 4 + i;
+        if (f < M) epi_store_elem<float>(e, f, t, acc[i][j], acc2[i][j]);
+      }
+    }
+  }
+}
+
+int launch_gemm_f32(const float* W, const float* W2, const float* X, int M, int K, int N_cap,
+                    const int* n_rows_dev, const Epilogue& epi, cudaStream_t st) {
+  if (N_cap <= 0 || M <= 0) return PE_OK;
+  dim3 grid((M + kSt - 1) / kSt, (N_cap + kSt - 1) / kSt);
+  gemm_f32_kernel<<<grid, 256, 0, st>>>(W, W2, X, M, K, N_cap, n_rows_dev, epi);
+  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool encode_tmap_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !ptr || rows == 0 || cols == 0 || (cols % 8) != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms_of_current_device() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace pe

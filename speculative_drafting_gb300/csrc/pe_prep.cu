@@ -1,0 +1,390 @@
+// Steps (1)-(3) of the parallel-draft step: batch metadata, hidden-state map
+// and drafter input ("P-EAGLE: parallel speculative decoding in vLLM": Fused
+// Triton kernel, Hidden-state management, KV cache and CUDA graphs;
+// "Attention Drift" section 4.1, Observation 2).
+//
+// Every index read from user data is range-checked: out-of-range values are
+// clamped or skipped and reported in the status word, never dereferenced.
+#include "pe_common.cuh"
+#include "pe_prep.h"
+
+namespace pe {
+
+// ------------------------------------------------------------------ (1) metadata
+
+struct MetaArgs {
+  int B, T_in, T_out, K, mask_id, bs, max_blocks, num_blocks, vocab;
+  const int32_t* qsl;
+  const int32_t* prev_tok;
+  const int64_t* prev_pos;
+  const int32_t* accepted;
+  const int32_t* bonus;
+  const int32_t* block_table;
+  pe_meta m;
+  uint32_t* status;
+};
+
+// Per-request row counts, with the input checks (identical in both passes).
+PE_DEV void request_counts(const MetaArgs& a, int r, int& n, int& acc, bool& bad) {
+  int q0 = a.qsl[r], q1 = a.qsl[r + 1];
+  bad = false;
+  if (q0 < 0 || q1 > a.T_in || q1 < q0) {
+    bad = true;
+    q0 = min(max(q0, 0), a.T_in);
+    q1 = min(max(q1, q0), a.T_in);
+  }
+  n = q1 - q0;
+  acc = a.accepted[r];
+  if (n < 1 || acc < 0 || acc > n - 1) {
+    bad = true;
+    acc = min(max(acc, 0), max(n - 1, 0));
+  }
+}
+
+// Cache slot of position p of request r through its block table; -1 (flagged)
+// when the position or the block id is out of range.
+PE_DEV int64_t slot_of(const MetaArgs& a, int r, int64_t p) {
+  if (p < 0 || p / a.bs >= a.max_blocks) {
+    set_status(a.status, PE_ST_BLOCK_RANGE);
+    return PE_PADDING_SLOT_ID;
+  }
+  const int blk = a.block_table[static_cast<size_t>(r) * a.max_blocks + p / a.bs];
+  if (blk < 0 || blk >= a.num_blocks) {
+    set_status(a.status, PE_ST_BLOCK_RANGE);
+    return PE_PADDING_SLOT_ID;
+  }
+  return static_cast<int64_t>(blk) * a.bs + p % a.bs;
+}
+
+// One CTA.  Pass 1: exclusive block scans (warp shuffles + one shared-memory
+// level) of n_r + K - 1 (output rows) and a_r + K (non-rejected rows) over the
+// requests.  Pass 2: one warp per request writes its rows.
+__global__ void __launch_bounds__(1024) meta_kernel(const MetaArgs a) {
+  __shared__ int wsum_o[32], wsum_v[32];
+  __shared__ int carry_o, carry_v;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = blockDim.x >> 5;
+  if (tid == 0) {
+    carry_o = 0;
+    carry_v = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int r = base + tid;
+    int lo = 0, lv = 0;
+    if (r < a.B) {
+      int n, acc;
+      bool bad;
+      request_counts(a, r, n, acc, bad);
+      if (bad) set_status(a.status, PE_ST_ACCEPTED_RANGE);
+      lo = n + a.K - 1;
+      lv = (n >= 1 ? acc + 1 : 0) + a.K - 1;
+    }
+    int xo = lo, xv = lv;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int to = __shfl_up_sync(0xffffffffu, xo, off);
+      const int tv = __shfl_up_sync(0xffffffffu, xv, off);
+      if (lane >= off) {
+        xo += to;
+        xv += tv;
+      }
+    }
+    if (lane == 31) {
+      wsum_o[warp] = xo;
+      wsum_v[warp] = xv;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int so = lane < nw ? wsum_o[lane] : 0;
+      int sv = lane < nw ? wsum_v[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int to = __shfl_up_sync(0xffffffffu, so, off);
+        const int tv = __shfl_up_sync(0xffffffffu, sv, off);
+        if (lane >= off) {
+          so += to;
+          sv += tv;
+        }
+      }
+      if (lane < nw) {
+        wsum_o[lane] = so;  // inclusive prefix of warp totals
+        wsum_v[lane] = sv;
+      }
+    }
+    __syncthreads();
+    const int pre_o = carry_o + (warp ? wsum_o[warp - 1] : 0) + xo - lo;
+    const int pre_v = carry_v + (warp ? wsum_v[warp - 1] : 0) + xv - lv;
+    if (r < a.B) {
+      a.m.out_qsl[r] = pre_o;
+      a.m.valid_qsl[r] = pre_v;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      carry_o += wsum_o[nw - 1];
+      carry_v += wsum_v[nw - 1];
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.m.out_qsl[a.B] = carry_o;
+    a.m.valid_qsl[a.B] = carry_v;
+    *a.m.n_valid = min(carry_v, a.T_out);
+    if (carry_o != a.T_out) set_status(a.status, PE_ST_ACCEPTED_RANGE);
+  }
+  __syncthreads();
+
+  // pass 2: rows of request r
+  for (int r = warp; r < a.B; r += nw) {
+    int n, acc;
+    bool bad;
+    request_counts(a, r, n, acc, bad);
+    const int q0 = min(max(a.qsl[r], 0), a.T_in);
+    const int o0 = a.m.out_qsl[r];
+    const int v0 = a.m.valid_qsl[r];
+    const int b = a.bonus[r];
+    if (b < 0 || b >= a.vocab) set_status(a.status, PE_ST_TOKEN_RANGE);
+    const int i_ntp = min(q0 + acc, a.T_in - 1);
+    const int64_t p0 = a.prev_pos[i_ntp];
+    const int rows = n + a.K - 1;
+    for (int j = lane; j < rows; j += 32) {
+      const int o = o0 + j;
+      if (o < 0 || o >= a.T_out) {
+        set_status(a.status, PE_ST_ACCEPTED_RANGE);
+        continue;
+      }
+      int tok, hsrc, vi = -1;
+      int64_t pos, slot;
+      uint8_t rej = 0, msk = 0;
+      if (j < n) {
+        const int i = q0 + j;
+        tok = (j == acc || j == n - 1) ? b : a.prev_tok[i + 1];
+        if (j != acc && j != n - 1 && (tok < 0 || tok >= a.vocab))
+          set_status(a.status, PE_ST_TOKEN_RANGE);
+        pos = a.prev_pos[i];
+        hsrc = i;
+        if (j > acc) {
+          rej = 1;
+          slot = PE_PADDING_SLOT_ID;
+        } else {
+          slot = slot_of(a, r, pos);
+          vi = v0 + j;
+        }
+        if (j == acc) a.m.sample_idx[static_cast<size_t>(r) * a.K] = o;
+      } else {
+        const int mm = j - n + 1;  // 1..K-1
+        tok = a.mask_id;
+        pos = p0 + mm;
+        hsrc = -1;
+        msk = 1;
+        slot = slot_of(a, r, pos);
+        vi = v0 + acc + mm;
+        a.m.sample_idx[static_cast<size_t>(r) * a.K + mm] = o;
+      }
+      a.m.tok[o] = tok;
+      a.m.pos[o] = pos;
+      a.m.is_rejected[o] = rej;
+      a.m.is_masked[o] = msk;
+      a.m.hidden_src[o] = hsrc;
+      a.m.slot[o] = slot;
+      if (vi >= 0) {
+        if (vi < a.T_out)
+          a.m.valid_rows[vi] = o;
+        else
+          set_status(a.status, PE_ST_ACCEPTED_RANGE);
+      }
+    }
+    if (lane == 0) a.m.seq_len[r] = static_cast<int32_t>(p0 + a.K);
+  }
+  // rows past the non-rejected count
+  const int nv = *a.m.n_valid;
+  for (int i = nv + tid; i < a.T_out; i += blockDim.x) a.m.valid_rows[i] = -1;
+}
+
+int launch_meta(const MetaLaunch& L, cudaStream_t st) {
+  MetaArgs a;
+  a.B = L.B;
+  a.T_in = L.T_in;
+  a.T_out = L.T_in + L.B * (L.K - 1);
+  a.K = L.K;
+  a.mask_id = L.mask_id;
+  a.bs = L.bs;
+  a.max_blocks = L.max_blocks;
+  a.num_blocks = L.num_blocks;
+  a.vocab = L.vocab;
+  a.qsl = L.qsl;
+  a.prev_tok = L.prev_tok;
+  a.prev_pos = L.prev_pos;
+  a.accepted = L.accepted;
+  a.bonus = L.bonus;
+  a.block_table = L.block_table;
+  a.m = L.meta;
+  a.status = L.status;
+  int threads = 32;
+  while (threads < L.B && threads < 1024) threads <<= 1;
+  if (threads < 128) threads = 128;
+  meta_kernel<<<1, threads, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ (2) hidden-state map
+
+// G[o][s][:] = H_tgt[hidden_src[o]][s][:] or h_shared; E[o][:] = emb[tok[o]] or
+// emb_mask.  Grid-stride over 16-byte vectors; 4 loads in flight per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
+  constexpr int V = Elem<T>::kVec;
+  const int vd = a.d / V;             // vectors per stream row
+  const long nG = a.G ? static_cast<long>(a.T_out) * 3 * vd : 0;
+  const long nE = a.E ? static_cast<long>(a.T_out) * vd : 0;
+  const long total = nG + nE;
+  const long stride = static_cast<long>(gridDim.x) * blockDim.x;
+  const uint4* H = static_cast<const uint4*>(a.H_tgt);
+  const uint4* hs = static_cast<const uint4*>(a.h_shared);
+  const uint4* emb = static_cast<const uint4*>(a.emb);
+  const uint4* em = static_cast<const uint4*>(a.emb_mask);
+  for (long base = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+       base += 4 * stride) {
+    uint4 val[4];
+    long dst[4];
+    bool isG[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long idx = base + u * stride;
+      dst[u] = -1;
+      if (idx >= total) continue;
+      if (idx < nG) {
+        const long o = idx / (3 * vd);
+        const int rem = static_cast<int>(idx - o * 3 * vd);
+        const int src = a.hidden_src[o];
+        if (src >= 0 && src < a.T_in)
+          val[u] = H[static_cast<long>(src) * 3 * vd + rem];
+        else if (src < 0)
+          val[u] = hs[rem % vd];
+        else {
+          set_status(a.status, PE_ST_ACCEPTED_RANGE);
+          val[u] = make_uint4(0, 0, 0, 0);
+        }
+        dst[u] = idx;
+        isG[u] = true;
+      } else {
+        const long e = idx - nG;
+        const long o = e / vd;
+        const int rem = static_cast<int>(e - o * vd);
+        if (a.is_masked[o]) {
+          val[u] = em[rem];
+        } else {
+          int t = a.tok[o];
+          if (t < 0 || t >= a.vocab) {
+            set_status(a.status, PE_ST_TOKEN_RANGE);
+            t = 0;
+          }
+          val[u] = emb[static_cast<long>(t) * vd + rem];
+        }
+        dst[u] = e;
+        isG[u] = false;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (dst[u] < 0) continue;
+      if (isG[u])
+        static_cast<uint4*>(a.G)[dst[u]] = val[u];
+      else
+        static_cast<uint4*>(a.E)[dst[u]] = val[u];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ (3) drafter input
+
+// A[v] = [RMSNorm(G0) g0, RMSNorm(G1) g1, RMSNorm(G2) g2, E] for non-rejected row
+// v (output row valid_rows[v]), straight from H_tgt / h_shared / the embedding.
+// blockIdx.x = v, blockIdx.y = segment (0..2 streams, 3 embedding).
+template <typename T>
+__global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
+  __shared__ float red[32];
+  constexpr int V = Elem<T>::kVec;
+  const int v = blockIdx.x, seg = blockIdx.y;
+  const int nv = min(max(*a.n_valid, 0), a.T_out);
+  if (v >= nv) return;
+  const int o = a.valid_rows[v];
+  if (o < 0 || o >= a.T_out) {
+    if (threadIdx.x == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
+    return;
+  }
+  const int vd = a.d / V;
+  uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.A) + static_cast<size_t>(v) * 4 * a.d +
+                                        static_cast<size_t>(seg) * a.d);
+  if (seg == 3) {
+    const uint4* src;
+    if (a.is_masked[o]) {
+      src = static_cast<const uint4*>(a.emb_mask);
+    } else {
+      int t = a.tok[o];
+      if (t < 0 || t >= a.vocab) {
+        if (threadIdx.x == 0) set_status(a.status, PE_ST_TOKEN_RANGE);
+        t = 0;
+      }
+      src = static_cast<const uint4*>(a.emb) + static_cast<size_t>(t) * vd;
+    }
+    for (int i = threadIdx.x; i < vd; i += blockDim.x) out[i] = src[i];
+    return;
+  }
+  const int hsrc = a.hidden_src[o];
+  const uint4* src;
+  if (hsrc < 0) {
+    src = static_cast<const uint4*>(a.h_shared);
+  } else if (hsrc < a.T_in) {
+    src = static_cast<const uint4*>(a.H_tgt) + (static_cast<size_t>(hsrc) * 3 + seg) * vd;
+  } else {
+    if (threadIdx.x == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
+    src = static_cast<const uint4*>(a.h_shared);
+  }
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < vd; i += blockDim.x) {
+    float f[V];
+    unpack16<T>(src[i], f);
+#pragma unroll
+    for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(a.d) + a.eps);
+  const uint4* gam = static_cast<const uint4*>(a.gamma_stream) + static_cast<size_t>(seg) * vd;
+  for (int i = threadIdx.x; i < vd; i += blockDim.x) {
+    float f[V], g[V];
+    unpack16<T>(src[i], f);
+    unpack16<T>(gam[i], g);
+#pragma unroll
+    for (int k = 0; k < V; ++k) f[k] = f[k] * inv * g[k];
+    out[i] = pack16<T>(f);
+  }
+}
+
+template <typename T>
+int launch_gather_t(const GatherArgs& a, int num_sms, cudaStream_t st) {
+  const int vd = a.d / Elem<T>::kVec;
+  const long total = static_cast<long>(a.T_out) * vd * ((a.G ? 3 : 0) + (a.E ? 1 : 0));
+  if (total == 0) return PE_OK;
+  long blocks = (total + 4L * 256 - 1) / (4L * 256);
+  blocks = blocks < 4L * num_sms ? blocks : 4L * num_sms;
+  gather_kernel<T><<<static_cast<int>(blocks), 256, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+}
+
+int launch_gather(const GatherArgs& a, int dtype, int num_sms, cudaStream_t st) {
+  return dtype == PE_DTYPE_BF16 ? launch_gather_t<bf16>(a, num_sms, st)
+                                : launch_gather_t<float>(a, num_sms, st);
+}
+
+int launch_input(const InputArgs& a, int dtype, cudaStream_t st) {
+  if (a.T_out <= 0) return PE_OK;
+  dim3 grid(a.T_out, 4);
+  if (dtype == PE_DTYPE_BF16)
+    input_kernel<bf16><<<grid, 128, 0, st>>>(a);
+  else
+    input_kernel<float><<<grid, 128, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+}
+
+}  // namespace pe

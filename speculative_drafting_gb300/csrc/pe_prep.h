@@ -1,0 +1,103 @@
+// Launch interfaces of the non-GEMM kernels (host side).
+#pragma once
+
+#include "pe_internal.h"
+
+namespace pe {
+
+// ---------------------------------------------------------------- (1) metadata
+struct MetaLaunch {
+  int B, T_in, K, mask_id, bs, max_blocks, num_blocks, vocab;
+  const int32_t* qsl;
+  const int32_t* prev_tok;
+  const int64_t* prev_pos;
+  const int32_t* accepted;
+  const int32_t* bonus;
+  const int32_t* block_table;
+  pe_meta meta;
+  uint32_t* status;
+};
+int launch_meta(const MetaLaunch& L, cudaStream_t st);
+
+// ---------------------------------------------------------------- (2) hidden-state map
+struct GatherArgs {
+  int T_out, T_in, d, vocab;
+  const int32_t* hidden_src;
+  const int32_t* tok;
+  const uint8_t* is_masked;
+  const void* H_tgt;
+  const void* h_shared;
+  const void* emb;
+  const void* emb_mask;
+  void* G;  // nullable
+  void* E;  // nullable
+  uint32_t* status;
+};
+int launch_gather(const GatherArgs& a, int dtype, int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- (3) drafter input
+struct InputArgs {
+  int T_out, T_in, d, vocab;
+  float eps;
+  const int32_t* n_valid;
+  const int32_t* valid_rows;
+  const int32_t* hidden_src;
+  const int32_t* tok;
+  const uint8_t* is_masked;
+  const void* H_tgt;
+  const void* h_shared;
+  const void* emb;
+  const void* emb_mask;
+  const void* gamma_stream;
+  void* A;
+  uint32_t* status;
+};
+int launch_input(const InputArgs& a, int dtype, cudaStream_t st);
+
+// ---------------------------------------------------------------- row RMSNorm
+// out[i] = x[i] * gamma / sqrt(mean(x[i]^2) + eps) for rows i < n_rows.
+int launch_rmsnorm(const void* x, int ld_x, const void* gamma, void* out, int ld_out, int d,
+                   float eps, int rows_cap, const int* n_rows_dev, int dtype, cudaStream_t st);
+
+// ---------------------------------------------------------------- RoPE + KV write
+struct RopeArgs {
+  int T_out, B, K, H, G, hd, d, bs, num_blocks;
+  const float* qkv;  // [T_out][(H+2G)hd] fp32, non-rejected rows in valid_rows order
+  const void* x;     // [T_out][d] fc output (same order)
+  const int32_t* n_valid;
+  const int32_t* valid_rows;
+  const int32_t* valid_qsl;
+  const int64_t* pos;
+  const int64_t* slot;
+  void* k_cache;
+  void* v_cache;
+  void* q_s;  // [B*K][H][hd] queries of the sample rows
+  void* x_s;  // [B*K][d] fc output of the sample rows (residual)
+  double inv_freq[64];
+  uint32_t* status;
+};
+int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+  int B, K, H, G, hd, bs, max_blocks, num_blocks;
+  int n_splits, split_len;
+  const void* q;  // [B*K][H][hd]
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* seq_len;
+  float* part_o;   // [n_splits][B*K][H][hd]     (bf16 path)
+  float* part_ml;  // [n_splits][B*K][H][2]      (bf16 path)
+  void* out;       // [B*K][H*hd]
+  uint32_t* status;
+};
+void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, int num_sms,
+                    int& n_splits, int& split_len);
+size_t attention_scratch_bytes(int B, int K, int H, int hd, int n_splits);
+int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st);
+
+// ---------------------------------------------------------------- argmax keys -> ids
+int launch_argmax_finalize(const unsigned long long* keys, int n, int32_t* out, cudaStream_t st);
+
+}  // namespace pe

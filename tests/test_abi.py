@@ -1,0 +1,59 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every function the
+headers declare; host-side argument checks answer without touching a GPU."""
+
+import ctypes
+import shutil
+
+import pytest
+
+from speculative_drafting_gb300 import binding, build
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not __import__("os").path.exists(
+    "/usr/local/cuda/bin/nvcc"), reason="needs nvcc to build libpe.so")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = binding.declared_functions(binding.HEADER) + binding.declared_functions(binding.TESTING_HEADER)
+    assert {"pe_create", "pe_destroy", "pe_workspace_bytes", "pe_prepare_inputs", "pe_draft_step",
+            "pe_argmax", "pe_read_status", "pe_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(0, 7):
+        assert isinstance(binding.status_string(code), str)
+    assert binding.status_string(0) == "ok"
+
+
+def test_host_argument_checks(lib):
+    h = ctypes.c_void_p()
+    w = binding.PeWeights()
+    good = binding.PeDims(d=64, n_streams=3, n_heads=4, n_kv_heads=2, head_dim=16, inter=128, vocab=512,
+                          K=4, block_size=4, mask_id=0, post_norm=0, dtype=binding.PE_DTYPE_F32,
+                          eps=1e-6, rope_theta=1e4)
+    # null handle output / null dims / null weights
+    assert lib.pe_create(ctypes.byref(good), ctypes.byref(w), None) == binding.PE_ERR_ARG
+    assert lib.pe_create(None, ctypes.byref(w), ctypes.byref(h)) == binding.PE_ERR_ARG
+    assert lib.pe_create(ctypes.byref(good), ctypes.byref(w), ctypes.byref(h)) == binding.PE_ERR_ARG
+    assert not h.value
+    # unsupported dims are refused before any device call
+    for field, value in (("n_streams", 2), ("d", 60), ("head_dim", 256), ("n_kv_heads", 3), ("K", 0),
+                         ("dtype", 7)):
+        bad = binding.PeDims.from_buffer_copy(good)
+        setattr(bad, field, value)
+        assert lib.pe_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(h)) == \
+            binding.PE_ERR_UNSUPPORTED, field
+    bf = binding.PeDims.from_buffer_copy(good)
+    bf.dtype = binding.PE_DTYPE_BF16  # bf16 attention needs head_dim 64 or 128
+    assert lib.pe_create(ctypes.byref(bf), ctypes.byref(w), ctypes.byref(h)) == binding.PE_ERR_UNSUPPORTED
+    assert lib.pe_workspace_bytes(None, 1, 1, 1) == 0
+    assert lib.pe_prepare_inputs(None, 1, 1, *([None] * 6), 1, 1, None, None, None, None, None, None,
+                                 0, None) == binding.PE_ERR_ARG
+    assert lib.pe_argmax(None, None, 1, None, None, None, 0, None) == binding.PE_ERR_ARG

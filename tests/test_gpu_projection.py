@@ -1,0 +1,59 @@
+"""The step's projection kernel (tcgen05 GEMM for bf16, SIMT for fp32) alone,
+against a float64 matrix product of the same bf16 operands."""
+
+import numpy as np
+import pytest
+
+from oracle import pe_oracle as O
+from parity import cuda_or_skip, f64, host, setup
+from speculative_drafting_gb300 import runner
+
+pytestmark = pytest.mark.gpu
+
+PROJ = {"fc": 0, "qkv": 1, "o": 2, "swiglu": 3, "down": 4, "lm": 5}
+
+
+def _shape(dm, which):
+    H = dm.n_heads * dm.head_dim
+    return {"fc": (dm.d, 4 * dm.d, "w_fc"), "qkv": (dm.qkv_rows, dm.d, "w_qkv"), "o": (dm.d, H, "w_o"),
+            "swiglu": (dm.inter, dm.d, "w_gate"), "down": (dm.d, dm.inter, "w_down"),
+            "lm": (dm.vocab, dm.d, "w_lm")}[which]
+
+
+@pytest.mark.parametrize("name", ["small_prenorm", "small_postnorm_hd128", "tiny_fp32"])
+@pytest.mark.parametrize("which", list(PROJ))
+@pytest.mark.parametrize("n", [1, 7, 16, 100, 300])
+def test_projection_matches_matmul(name, which, n):
+    torch = cuda_or_skip()
+    wl, b, w, kc, vc, r = setup(name, want_logits=False, kv=False)
+    dm = wl.dims
+    M, Kd, wname = _shape(dm, which)
+    g = np.random.default_rng(n * 31 + PROJ[which])
+    X = g.standard_normal((n, Kd)).astype(np.float32)
+    if dm.dtype == "bf16":
+        from speculative_drafting_gb300.workloads import f32_to_bf16_bits
+        Xh = f32_to_bf16_bits(X)
+    else:
+        Xh = X
+    Xd = runner.to_device(Xh, dm.dtype)
+    out_dt = (torch.bfloat16 if dm.dtype == "bf16" else torch.float32) if which == "swiglu" else torch.float32
+    out = torch.full((n, M), float("nan"), dtype=out_dt, device="cuda")
+    ws = r.drafter.test_projection(PROJ[which], Xd, n, out)
+    torch.cuda.synchronize()
+    st, _ = r.drafter.read_status(ws)
+    assert st == 0, hex(st)
+    x64 = f64(Xh, dm.dtype)
+    if which == "swiglu":
+        ref = O.bf16_round(O.silu(O.linear(x64, f64(w["w_gate"], dm.dtype))) *
+                           O.linear(x64, f64(w["w_up"], dm.dtype))) if dm.dtype == "bf16" else \
+            O.silu(O.linear(x64, f64(w["w_gate"], dm.dtype))) * O.linear(x64, f64(w["w_up"], dm.dtype))
+        got = f64(host(out), dm.dtype)
+        tol = 2 ** -7 * np.abs(ref) + 1e-6 if dm.dtype == "bf16" else 1e-5 * (1 + np.abs(ref))
+    else:
+        ref = O.linear(x64, f64(w[wname], dm.dtype))
+        got = host(out).astype(np.float64)
+        # fp32 accumulation of K products of magnitude ~|x||w|
+        tol = 1e-5 * np.sqrt(Kd) * 0.02 * 4 + 1e-5 * np.abs(ref)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref)
+    assert np.all(err <= tol), f"max err {err.max():.3g}"

@@ -1,0 +1,93 @@
+"""GPU parity of the whole parallel-draft step (pe_prepare_inputs ->
+pe_draft_step -> pe_argmax) against the CPU oracle on every row, at sizes the
+oracle finishes in seconds: every projection spans several 128-row tiles and a
+ragged tail, contexts cross block boundaries, one request starts from an empty
+context."""
+
+import numpy as np
+import pytest
+
+from oracle import pe_oracle as O
+from parity import (LOGIT_TOL, check_close_bf16, check_logits_and_draft, check_meta, cuda_or_skip, f64,
+                    host, setup)
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    ("tiny_fp32", {}),
+    ("tiny_fp32", {"post_norm": True}),
+    ("tiny_fp32", {"K": 1}),
+    ("small_prenorm", {}),
+    ("small_prenorm", {"accepted": (5, 0, 3)}),
+    ("small_postnorm_hd128", {}),
+    ("small_postnorm_hd128", {"post_norm": False, "accepted": (0, 2, 0, 8)}),
+    ("small_prenorm", {"K": 1}),
+    ("small_prenorm", {"batch": 12, "n_prev": 6, "ctx": ("uniform", 0, 700), "seed": 3}),
+]
+
+
+def _check_kv(wl, b, kc0, vc0, r, res):
+    """Written slots hold the oracle's k / v; every other slot is untouched."""
+    dt = wl.dims.dtype
+    bs = wl.dims.block_size
+    kc, vc = host(r.k_cache), host(r.v_cache)
+    written = np.zeros(kc.shape[0] * bs, dtype=bool)
+    for rr, out in res["req"].items():
+        slots = out["slot"]
+        assert (slots >= 0).all()
+        written[slots] = True
+        got_k = f64(kc[slots // bs, :, slots % bs, :], dt)
+        got_v = f64(vc[slots // bs, :, slots % bs, :], dt)
+        if dt == "bf16":
+            check_close_bf16(got_k, out["k"], "k cache", max_ulps=1, min_exact=0.99)
+            check_close_bf16(got_v, out["v"], "v cache", max_ulps=1, min_exact=0.99)
+        else:
+            np.testing.assert_allclose(got_k, out["k"], rtol=1e-5, atol=1e-6)
+            np.testing.assert_allclose(got_v, out["v"], rtol=1e-5, atol=1e-6)
+    w2 = written.reshape(kc.shape[0], bs)
+    untouched = ~w2
+    np.testing.assert_array_equal(kc.transpose(0, 2, 1, 3)[untouched], kc0.transpose(0, 2, 1, 3)[untouched])
+    np.testing.assert_array_equal(vc.transpose(0, 2, 1, 3)[untouched], vc0.transpose(0, 2, 1, 3)[untouched])
+
+
+@pytest.mark.parametrize("name,over", CASES)
+def test_step_matches_oracle(name, over):
+    torch = cuda_or_skip()
+    wl, b, w, kc, vc, r = setup(name, **over)
+    r.run()
+    torch.cuda.synchronize()
+    st, rc = r.status()
+    assert st == 0, hex(st)
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    check_meta(r, res["meta"])
+    K = wl.dims.K
+    dt = wl.dims.dtype
+    z = f64(host(r.z), dt)
+    logits = host(r.logits)
+    draft = host(r.draft)
+    for rr, out in res["req"].items():
+        sl = slice(rr * K, (rr + 1) * K)
+        if dt == "bf16":
+            assert np.abs(z[sl] - out["z"]).max() <= 0.05
+        else:
+            np.testing.assert_allclose(z[sl], out["z"], rtol=1e-5, atol=1e-5)
+        check_logits_and_draft(dt, logits[sl], draft[sl], out["logits"], where=f"request {rr}")
+    _check_kv(wl, b, kc, vc, r, res)
+
+
+def test_step_is_repeatable_and_graph_capturable():
+    torch = cuda_or_skip()
+    wl, b, w, kc, vc, r = setup("small_prenorm")
+    r.run()
+    torch.cuda.synchronize()
+    first = host(r.logits).copy()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        r.run(stream=s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(r.logits), first)
+    assert r.status()[0] == 0
