@@ -1,0 +1,378 @@
+"""Benchmark of the P-EAGLE parallel-draft step on GB300.
+
+One step = the whole hot path over one synthetic batch: pe_prepare_inputs
+(metadata, drafter input) -> pe_draft_step (fc, decoder layer with paged
+attention, final norm) -> pe_argmax (LM head + greedy argmax).  The step is
+captured as CUDA graphs (the way a serving engine runs the drafter) and timed
+with CUDA events on its stream, max over ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line.  --impl reference times the CPU oracle (the only
+reference this build has) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_drafting_gb300 import workloads as W  # noqa: E402
+
+METRIC = "parallel-draft step latency (us) and draft tokens/s at K=7; HBM GB/s %peak"
+UNIT = "draft tokens/s"
+DEFAULT_WORKLOAD = "gptoss_b1_k7"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------------------- algorithmic bytes
+
+
+def lm_head_bytes(dm, n_rows):
+    """Bytes the LM head must move: W_lm once, the z rows, the fp32 argmax keys."""
+    return dm.vocab * dm.d * 2 + n_rows * dm.d * 2 + n_rows * 8
+
+
+def step_bytes(dm, batch):
+    """Bytes the whole step must move: every weight once, the KV it reads and writes,
+    the captured hidden states and the embedding rows."""
+    d, I, V = dm.d, dm.inter, dm.vocab
+    w = (4 * d * d + dm.qkv_rows * d + d * dm.n_heads * dm.head_dim + 3 * I * d + V * d) * 2
+    B, K = batch["B"], dm.K
+    acc = batch["accepted"]
+    pos0 = batch["prev_pos"][batch["qsl"][:-1] + acc]
+    kv_read = int(np.sum(pos0 + K)) * dm.n_kv_heads * dm.head_dim * 2 * 2
+    n_valid = int(np.sum(acc + K))
+    kv_write = n_valid * dm.n_kv_heads * dm.head_dim * 2 * 2
+    hid = batch["T_in"] * 3 * d * 2 + n_valid * d * 2
+    return w + kv_read + kv_write + hid
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+
+def oracle_sample(wl, batch, w, kc, vc, budget_s=20.0):
+    """Time the oracle (as it stands) on whole requests of the workload until the
+    budget is spent (at least one request).  Returns (draft tokens/s, sample text, threads)."""
+    from oracle import pe_oracle as O
+
+    t0 = time.perf_counter()
+    done = 0
+    for r in range(wl.batch):
+        O.draft_step(wl.dims, w, batch, kc, vc, requests=[r])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    try:
+        from threadpoolctl import threadpool_info
+
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        threads = os.cpu_count() or 1
+    sample = f"{done} of {wl.batch} requests of {wl.name} (full layer + LM head per request), {dt:.1f} s"
+    return done * wl.dims.K / dt, sample, threads
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = W.get(args.workload)
+    batch = W.make_batch(wl)
+    w = W.make_weights(wl)
+    kc, vc = W.make_kv_cache(wl, batch["num_blocks"])
+    # each step: the oracle on whole requests of the workload, bounded in time;
+    # the whole run stops after a few minutes
+    per = []
+    t_all = time.perf_counter()
+    threads, sample = 1, ""
+    for _ in range(max(1, args.steps)):
+        v, sample, threads = oracle_sample(wl, batch, w, kc, vc, budget_s=10.0)
+        per.append(v)
+        if time.perf_counter() - t_all > 150:
+            break
+    value = statistics.median(per)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": len(per), "warmup": 0, "ms_per_step": 1000.0 * wl.batch * wl.dims.K / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "global_batch": wl.batch, "K": wl.dims.K,
+                       "description": wl.description},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from speculative_drafting_gb300 import build, runner
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    wl = W.get(args.workload)
+    wl_rank = W.get(args.workload, seed=wl.seed + rank)  # each rank drafts its own batch
+    batch = W.make_batch(wl_rank)
+    w = W.make_weights(wl)
+    kc, vc = W.make_kv_cache(wl_rank, batch["num_blocks"])
+    r = runner.StepRunner(wl, batch, w, kc, vc)
+    dm = wl.dims
+    B, K = batch["B"], dm.K
+    n_rows = B * K
+    stream = torch.cuda.Stream()
+    # eager warm-up, then capture: graph 1 = prepare + drafter layer, graph 2 = LM head + argmax
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            r.run(stream=stream)
+    stream.synchronize()
+    st, _ = r.status()
+    if st:
+        raise RuntimeError(f"device status {st:#x} on the benchmark batch")
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=stream):
+        r.prepare(stream=stream)
+        r.step(stream=stream)
+    with torch.cuda.graph(g2, stream=stream):
+        r.argmax(stream=stream)
+    launches_per_step = (2 + (11 if not dm.post_norm else 10) + 2)
+
+    def one_step():
+        g1.replay()
+        g2.replay()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            one_step()
+    stream.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            g1.replay()
+            ev[i][1].record(stream)
+            g2.replay()
+            ev[i][2].record(stream)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    lm_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    step_ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    # eager (no graph) step time, for reference
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e = max(10, args.steps // 4)
+        e0.record(stream)
+        for _ in range(n_e):
+            r.run(stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / n_e
+
+    # end to end through the C-ABI with host buffers: H2D of the step inputs from
+    # pinned memory, the step, D2H of the draft tokens, every step
+    host_in = {k: torch.from_numpy(np.ascontiguousarray(batch[k])).pin_memory()
+               for k in ("qsl", "prev_tok", "prev_pos", "accepted", "bonus", "block_table")}
+    hid = batch["H_tgt"]
+    host_in["H_tgt"] = (torch.from_numpy(hid.view(np.int16)).pin_memory() if dm.dtype == "bf16"
+                        else torch.from_numpy(hid).pin_memory())
+    dev_view = {k: (r.inp[k].view(torch.int16) if k == "H_tgt" and dm.dtype == "bf16" else r.inp[k])
+                for k in host_in}
+    out_host = torch.empty(n_rows, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = out_host.numel() * 4
+    n_e2e = max(10, args.steps // 2)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for k, t in host_in.items():
+                dev_view[k].copy_(t, non_blocking=True)
+            one_step()
+            out_host.copy_(r.draft, non_blocking=True)
+        stream.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            for k, t in host_in.items():
+                dev_view[k].copy_(t, non_blocking=True)
+            one_step()
+            out_host.copy_(r.draft, non_blocking=True)
+        a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / n_e2e
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    st, _ = r.status()
+    if st:
+        raise RuntimeError(f"device status {st:#x} after timing")
+
+    peaks, src = measured_peaks()
+    lm_avg_s = statistics.mean(lm_ms) / 1e3
+    lm_bytes = lm_head_bytes(dm, n_rows)
+    achieved = lm_bytes / lm_avg_s / 1e9
+    total_tokens = n_rows * world
+    value = total_tokens / (step_ms / 1e3)
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            v, sample, threads = oracle_sample(wl_rank, batch, w, kc, vc, budget_s=20.0)
+            cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+        sb = step_bytes(dm, batch)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "step_latency_us": step_ms * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if
+            dm.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "global_batch": B * world, "K": K,
+                       "description": wl.description, "cuda_graph": True,
+                       "l2": "inputs larger than L2: 1.41 GB of weights stream through every step"
+                       if wl.name.startswith("gptoss") else "inputs larger than L2 (weights + KV)",
+                       "parallelism": f"replica x{world} (independent requests per GPU)"},
+            "eager_ms_per_step": eager_ms,
+            "step_hbm": {"algorithmic_bytes": sb, "achieved_gbs": sb / (step_ms / 1e3) / 1e9,
+                         "frac": sb / (step_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+            "clocks": clk,
+            "e2e": {"value": total_tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * args.steps,
+            "roofline": {"kernel": "gemm_tc_kernel (LM head + argmax epilogue)", "bound": "hbm",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": src, "algorithmic_bytes": lm_bytes,
+                         "avg_launch_us": lm_avg_s * 1e6},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

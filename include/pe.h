@@ -75,10 +75,10 @@ extern "C" {
 
 enum { PE_DTYPE_F32 = 0, PE_DTYPE_BF16 = 1 };
 
-/* Drafter and step dimensions.  Supported: n_streams == 3; d, inter, vocab,
- * head_dim multiples of 8; n_heads a multiple of n_kv_heads; head_dim in
- * {16, 32, 64, 128} (bf16 needs 64 or 128); 1 <= K <= 16; block_size >= 1;
- * n_heads / n_kv_heads * K <= 128 for bf16. */
+/* Drafter and step dimensions.  Supported: n_streams == 3; d, inter and
+ * head_dim multiples of 8 (16-byte rows); n_heads a multiple of n_kv_heads;
+ * head_dim <= 128 (bf16 needs 64 or 128); 1 <= K <= 64; block_size >= 1;
+ * K * n_heads / n_kv_heads <= 128 for bf16. */
 typedef struct pe_dims {
   int32_t d;          /* drafter hidden size (and each captured stream's width) */
   int32_t n_streams;  /* captured target streams: h_low, h_mid, h_high (3) */

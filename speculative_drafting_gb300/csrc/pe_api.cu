@@ -78,7 +78,7 @@ size_t attn_scratch_bound(const pe_handle* h, int B, int max_blocks) {
   for (int b = 1; b <= B; ++b) {
     const long heads = static_cast<long>(b) * d.n_kv_heads;
     long ns = (2L * h->num_sms + heads - 1) / heads;
-    ns = std::max<long>(1, std::min(ns, chunks));
+    ns = std::max<long>(1, std::min(std::min(ns, chunks), 128L));
     best = std::max(best, attention_scratch_bytes(b, d.K, d.n_heads, d.head_dim, static_cast<int>(ns)));
   }
   return best;
@@ -230,7 +230,7 @@ int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out) {
   const bool bf = d.dtype == PE_DTYPE_BF16;
   if (d.dtype != PE_DTYPE_BF16 && d.dtype != PE_DTYPE_F32) return PE_ERR_UNSUPPORTED;
   if (d.n_streams != 3 || d.d <= 0 || d.d % 8 || d.inter <= 0 || d.inter % 8 || d.vocab <= 0 ||
-      d.vocab % 8 || d.n_heads <= 0 || d.n_kv_heads <= 0 || d.n_heads % d.n_kv_heads ||
+      d.n_heads <= 0 || d.n_kv_heads <= 0 || d.n_heads % d.n_kv_heads ||
       d.head_dim <= 0 || d.head_dim % 8 || d.head_dim > 128 || d.K < 1 || d.K > 64 ||
       d.block_size < 1 || !(d.eps >= 0.f) || !(d.rope_theta > 0.f))
     return PE_ERR_UNSUPPORTED;

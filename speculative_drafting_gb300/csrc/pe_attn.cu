@@ -23,6 +23,7 @@ namespace pe {
 constexpr int kKC = 64;      // keys per chunk
 constexpr int kStages = 3;   // cp.async ring depth
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxSplits = 128;  // key splits per (request, KV head)
 
 template <int HD>
 __global__ void __launch_bounds__(256) attn_mma_kernel(const AttnArgs a) {
@@ -247,25 +248,35 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const AttnArgs a) {
   }
 }
 
-// out[s][h*hd + d] = sum_j 2^(m_j - M) o_j[d] / sum_j 2^(m_j - M) l_j
+// out[s][h*hd + d] = sum_j 2^(m_j - M) o_j[d] / sum_j 2^(m_j - M) l_j.
+// Warp 0 turns the (m_j, l_j) of the splits into weights once; then every
+// thread sums its dimensions over the splits.
 template <typename T>
 __global__ void attn_combine_kernel(const AttnArgs a) {
+  __shared__ float w_sh[kMaxSplits];
+  __shared__ float inv_sh;
   const size_t sh = blockIdx.x;  // (sample, head)
   const size_t n_sh = static_cast<size_t>(a.B) * a.K * a.H;
-  float M = -INFINITY;
-  for (int j = 0; j < a.n_splits; ++j) M = fmaxf(M, a.part_ml[(j * n_sh + sh) * 2]);
-  float den = 0.f;
-  for (int j = 0; j < a.n_splits; ++j) {
-    const float m = a.part_ml[(j * n_sh + sh) * 2];
-    if (m != -INFINITY) den += exp2f(m - M) * a.part_ml[(j * n_sh + sh) * 2 + 1];
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float M = -INFINITY;
+    for (int j = lane; j < a.n_splits; j += 32) M = fmaxf(M, a.part_ml[(j * n_sh + sh) * 2]);
+    M = warp_max(M);
+    float den = 0.f;
+    for (int j = lane; j < a.n_splits; j += 32) {
+      const float m = a.part_ml[(j * n_sh + sh) * 2];
+      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+      w_sh[j] = w;
+      den += w * a.part_ml[(j * n_sh + sh) * 2 + 1];
+    }
+    den = warp_sum(den);
+    if (lane == 0) inv_sh = den > 0.f ? 1.f / den : 0.f;
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
+  __syncthreads();
+  const float inv = inv_sh;
   for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
     float acc = 0.f;
-    for (int j = 0; j < a.n_splits; ++j) {
-      const float m = a.part_ml[(j * n_sh + sh) * 2];
-      if (m != -INFINITY) acc += exp2f(m - M) * a.part_o[(j * n_sh + sh) * a.hd + d];
-    }
+    for (int j = 0; j < a.n_splits; ++j) acc += w_sh[j] * a.part_o[(j * n_sh + sh) * a.hd + d];
     static_cast<T*>(a.out)[sh * a.hd + d] = Elem<T>::from_f(acc * inv);
   }
 }
@@ -345,7 +356,7 @@ void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, 
   const long target = 2L * std::max(num_sms, 1);
   const long heads = std::max<long>(1, static_cast<long>(B) * G);
   long ns = (target + heads - 1) / heads;
-  ns = std::max<long>(1, std::min(ns, chunks));
+  ns = std::max<long>(1, std::min(std::min(ns, chunks), static_cast<long>(kMaxSplits)));
   const long chunks_per = (chunks + ns - 1) / ns;
   split_len = static_cast<int>(chunks_per * kKC);
   n_splits = static_cast<int>((Lmax + split_len - 1) / split_len);
@@ -371,13 +382,13 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
   const int warps = (rows + 15) / 16;
   const dim3 grid(a.n_splits, a.G, a.B);
   const size_t smem = static_cast<size_t>(kStages) * 2 * kKC * a.hd * 2;
+  // one attribute value for every launch (the largest head size's ring)
+  const int smem_max = kStages * 2 * kKC * 128 * 2;
   if (a.hd == 64) {
-    cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
+    cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     attn_mma_kernel<64><<<grid, warps * 32, smem, st>>>(a);
   } else if (a.hd == 128) {
-    cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
+    cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     attn_mma_kernel<128><<<grid, warps * 32, smem, st>>>(a);
   } else {
     return PE_ERR_UNSUPPORTED;

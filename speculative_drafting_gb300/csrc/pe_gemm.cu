@@ -23,13 +23,14 @@ namespace pe {
 
 constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBK = 64;   // reduction elements per k-block: one 128-byte swizzle row
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
+constexpr size_t kSmemBudget = 212 * 1024;  // dynamic shared memory for the stage ring
 constexpr int kTcThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;
 
 struct TcArgs {
   int M, K, N_cap, dual;
-  int BN, n_tiles, m_tiles, k_splits, kb_per_split, num_kb, stages;
+  int BN, n_tiles, m_tiles, k_splits, kb_per_split, num_kb, stages, acc_bufs;
   uint32_t tmem_cols;
   const int* n_rows_dev;
   Epilogue epi;
@@ -109,13 +110,41 @@ PE_DEV void tc_epilogue16(const TcArgs& p, int f, int j0, const float* v, const 
 
 // ------------------------------------------------------------------ tcgen05 kernel
 
+// Sum of the fp32 split partials of 16 token columns of feature f, in split
+// order (deterministic).  Four splits' loads are issued before they are added.
+PE_DEV void sum_partials16(const TcArgs& p, int acc, int f, int j0, int n_rows, float* v) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = 0.f;
+  if (f >= p.M) return;
+  const int nacc = p.dual ? 2 : 1;
+  auto at = [&](int s, int j) -> const float* {
+    return p.partial + ((static_cast<size_t>(s) * p.N_cap + j) * nacc + acc) * p.M + f;
+  };
+  int s = 0;
+  for (; s + 4 <= p.k_splits; s += 4) {
+    float t[4][16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) t[u][i] = (j0 + i < n_rows) ? __ldcg(at(s + u, j0 + i)) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] += t[u][i];
+  }
+  for (; s < p.k_splits; ++s)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (j0 + i < n_rows) v[i] += __ldcg(at(s, j0 + i));
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
                    const __grid_constant__ CUtensorMap mapB, const TcArgs p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t tfull_bar, tempty_bar, final_bar;
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, n_rows_sh, last_sh;
   __shared__ unsigned long long red_sh[4][16];
@@ -127,14 +156,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nA = p.dual ? 2 : 1;
   const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * 128u;
   const uint32_t stage_bytes = kABytes * nA + b_bytes;
+  // accumulator buffers in TMEM: two when they fit, so the MMA of the next tile
+  // runs while the epilogue drains this one
+  const int nbuf = p.acc_bufs;
+  const uint32_t buf_cols = static_cast<uint32_t>(p.BN * nA);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&tfull_bar, 1);
-    mbar_init(&tempty_bar, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 128);
+    }
     mbar_init(&final_bar, 1);
     abort_sh = 0;
     int n = p.N_cap;
@@ -174,7 +209,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_parity = 0;  // per-stage: ever armed / parity of last arm
+      uint32_t armed = 0, armed_parity = 0;  // per stage: ever armed / parity of the last arm
       for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
         const int n = t % p.n_tiles, rest = t / p.n_tiles;
         const int ks = rest % p.k_splits, m = rest / p.k_splits;
@@ -212,19 +247,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------- MMA issuer (one thread)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBM, p.BN);
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int stage = 0, it = 0;
+      uint32_t phase = 0, acc_phase[2] = {0u, 0u};
       for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
         const int n = t % p.n_tiles, rest = t / p.n_tiles;
         const int ks = rest % p.k_splits;
         if (n * p.BN >= n_rows) continue;
+        const int b = it % nbuf;
+        ++it;
         const int kb0 = ks * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-        if (!mbar_wait(&tempty_bar, acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait(&tempty_bar[b], acc_phase[b] ^ 1u, abort_flag)) {
           fail();
           break;
         }
         tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(b) * buf_cols;
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
@@ -241,10 +279,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // advance 16 elements (32 bytes) along K inside the swizzle row
             const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-            umma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, acc);
+            umma_bf16(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, acc);
             if (p.dual)
-              umma_bf16(tmem_base + static_cast<uint32_t>(p.BN), a2desc + 2 * kk, bdesc + 2 * kk,
-                        idesc, acc);
+              umma_bf16(d0 + static_cast<uint32_t>(p.BN), a2desc + 2 * kk, bdesc + 2 * kk, idesc,
+                        acc);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == p.stages) {
@@ -253,8 +291,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(&tfull_bar);
-        acc_phase ^= 1u;
+        umma_commit(&tfull_bar[b]);
+        acc_phase[b] ^= 1u;
       }
       // every MMA issued by this thread has finished before TMEM is released
       umma_commit(&final_bar);
@@ -266,35 +304,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;
     const int ew = warp - 2;
     const int et = threadIdx.x - 64;
-    uint32_t acc_phase = 0;
-    const int nacc = nA;
+    uint32_t acc_phase[2] = {0u, 0u};
+    int it = 0;
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
       const int n = t % p.n_tiles, rest = t / p.n_tiles;
       const int ks = rest % p.k_splits, m = rest / p.k_splits;
       if (n * p.BN >= n_rows) continue;
+      const int b = it % nbuf;
+      const int par = it & 1;
+      ++it;
       // the four epilogue warps decide together whether to go on, so none of
       // them can be left waiting at a named barrier the others skipped
-      const bool ok = mbar_wait(&tfull_bar, acc_phase, abort_flag);
-      if (lane == 0) ep_ok[acc_phase][ew] = ok ? 1 : 0;
+      const bool ok = mbar_wait(&tfull_bar[b], acc_phase[b], abort_flag);
+      if (lane == 0) ep_ok[par][ew] = ok ? 1 : 0;
       named_bar_sync(1, 128);
-      if (!(ep_ok[acc_phase][0] && ep_ok[acc_phase][1] && ep_ok[acc_phase][2] &&
-            ep_ok[acc_phase][3])) {
+      if (!(ep_ok[par][0] && ep_ok[par][1] && ep_ok[par][2] && ep_ok[par][3])) {
         fail();
         break;
       }
+      acc_phase[b] ^= 1u;
       tc_fence_after();
       const int f = m * kBM + q * 32 + lane;
       const int jt = n * p.BN;
-      const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t tl = tmem_base + static_cast<uint32_t>(b) * buf_cols +
+                          (static_cast<uint32_t>(q * 32) << 16);
       if (p.k_splits == 1) {
         for (int c = 0; c < p.BN; c += 16) {
           float v[16], v2[16];
           tmem_ld16(tl + c, v);
           if (p.dual) tmem_ld16(tl + p.BN + c, v2);
+          if (c + 16 >= p.BN) {
+            // last TMEM read of this buffer: hand it back before the stores
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[b]);
+          }
           tc_epilogue16(p, f, jt + c, v, p.dual ? v2 : nullptr, n_rows, red_sh, ew, et);
         }
-        tc_fence_before();
-        mbar_arrive(&tempty_bar);
       } else {
         for (int c = 0; c < p.BN; c += 16) {
           float v[16], v2[16];
@@ -305,7 +350,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int i = 0; i < 16; ++i) {
               const int j = jt + c + i;
               if (j < n_rows) {
-                const size_t base = (static_cast<size_t>(ks) * p.N_cap + j) * nacc;
+                const size_t base = (static_cast<size_t>(ks) * p.N_cap + j) * nA;
                 p.partial[base * p.M + f] = v[i];
                 if (p.dual) p.partial[(base + 1) * p.M + f] = v2[i];
               }
@@ -313,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&tempty_bar);
+        mbar_arrive(&tempty_bar[b]);
         // the last split of this (m, n) tile sums the partials in split order
         __threadfence();
         named_bar_sync(1, 128);
@@ -324,30 +369,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __threadfence();
           for (int c = 0; c < p.BN; c += 16) {
             float v[16], v2[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              v[i] = 0.f;
-              v2[i] = 0.f;
-            }
-            if (f < p.M) {
-              for (int s = 0; s < p.k_splits; ++s) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const int j = jt + c + i;
-                  if (j < n_rows) {
-                    const size_t base = (static_cast<size_t>(s) * p.N_cap + j) * nacc;
-                    v[i] += __ldcg(&p.partial[base * p.M + f]);
-                    if (p.dual) v2[i] += __ldcg(&p.partial[(base + 1) * p.M + f]);
-                  }
-                }
-              }
-            }
+            sum_partials16(p, 0, f, jt + c, n_rows, v);
+            if (p.dual) sum_partials16(p, 1, f, jt + c, n_rows, v2);
             tc_epilogue16(p, f, jt + c, v, p.dual ? v2 : nullptr, n_rows, red_sh, ew, et);
           }
           if (et == 0) p.counters[tile_mn] = 0;
         }
       }
-      acc_phase ^= 1u;
     }
   }
 
@@ -368,6 +396,7 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int num_sms, bool allow_s
   pl.K = K;
   pl.N_cap = N_cap < 1 ? 1 : N_cap;
   pl.dual = dual;
+  const int nA = dual ? 2 : 1;
   const int nt = (pl.N_cap + 255) / 256;
   int bn = (pl.N_cap + nt - 1) / nt;
   bn = (bn + 15) / 16 * 16;
@@ -378,6 +407,8 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int num_sms, bool allow_s
   const int base = pl.m_tiles * pl.n_tiles;
   int best = 1;
   if (allow_split && base < num_sms) {
+    // time ~ k-blocks streamed by the busiest SM + the serial part of the split
+    // reduction (about half a k-block per split, four partial loads in flight)
     double best_cost = 1e30;
     for (int s = 1; s <= 64; ++s) {
       const int kbs = (pl.num_kb + s - 1) / s;
@@ -385,7 +416,7 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int num_sms, bool allow_s
       const int ss = (pl.num_kb + kbs - 1) / kbs;
       const long tiles = static_cast<long>(base) * ss;
       const long waves = (tiles + num_sms - 1) / num_sms;
-      const double cost = static_cast<double>(waves) * kbs + (ss > 1 ? 2.0 : 0.0);
+      const double cost = static_cast<double>(waves) * kbs + (ss > 1 ? 2.0 + 0.5 * ss : 0.0);
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best = ss;
@@ -394,13 +425,13 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int num_sms, bool allow_s
   }
   pl.kb_per_split = (pl.num_kb + best - 1) / best;
   pl.k_splits = (pl.num_kb + pl.kb_per_split - 1) / pl.kb_per_split;
-  const int nA = dual ? 2 : 1;
   const size_t stage_bytes = static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128;
-  int stages = static_cast<int>((200u * 1024u) / stage_bytes);
+  const int stages = static_cast<int>((kSmemBudget) / stage_bytes);
   pl.stages = std::max(2, std::min(kMaxStages, stages));
   pl.smem_bytes = pl.stages * stage_bytes + 1024;
+  pl.acc_bufs = (2 * pl.BN * nA <= 512) ? 2 : 1;
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(pl.BN * nA)) cols <<= 1;
+  while (cols < static_cast<uint32_t>(pl.acc_bufs * pl.BN * nA)) cols <<= 1;
   pl.tmem_cols = static_cast<int>(cols);
   const long total = static_cast<long>(base) * pl.k_splits;
   pl.grid = static_cast<int>(std::min<long>(total, num_sms));
@@ -434,14 +465,17 @@ int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap*
   a.kb_per_split = pl.kb_per_split;
   a.num_kb = pl.num_kb;
   a.stages = pl.stages;
+  a.acc_bufs = pl.acc_bufs;
   a.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
   a.n_rows_dev = n_rows_dev;
   a.epi = epi;
   a.status = status;
   a.partial = partial;
   a.counters = counters;
+  // one attribute value (the largest any plan uses) for every launch, so kernels
+  // captured into a graph stay launchable whatever order they replay in
   if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(pl.smem_bytes)) != cudaSuccess)
+                           static_cast<int>(kSmemBudget + 1024)) != cudaSuccess)
     return PE_ERR_CUDA;
   gemm_tc_kernel<<<pl.grid, kTcThreads, pl.smem_bytes, st>>>(*mapA, pl.dual ? *mapA2 : *mapA,
                                                               mapB, a);

@@ -36,6 +36,7 @@ struct Epilogue {
 struct TcPlan {
   int M, K, N_cap, dual;
   int BN, n_tiles, m_tiles, num_kb, k_splits, kb_per_split, stages, grid, tmem_cols;
+  int acc_bufs;  // TMEM accumulator buffers (2 = the next tile's MMA overlaps the epilogue)
   size_t smem_bytes;
   size_t partial_bytes;  // split-K fp32 partials (0 without split)
   int n_counters;        // tile counters (m_tiles * n_tiles)

@@ -89,9 +89,14 @@ def bf16_ulps(a, b):
 
 
 def check_close_bf16(got, ref, what, max_ulps=1, min_exact=0.99):
-    """Stored bf16 values: nearly all bit-equal, the rest within max_ulps."""
+    """Stored bf16 values: nearly all bit-equal, the rest within max_ulps of the
+    bf16 spacing at the larger of the value and the tensor's RMS (a value that
+    comes out of a cancellation carries the error of the terms it came from)."""
+    scale = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
     u = bf16_ulps(got, ref)
-    exact = float(np.mean(u == 0))
-    assert u.max() <= max_ulps, f"{what}: max {u.max():.3g} ulps"
+    u_scale = np.abs(got - ref) / (2.0 ** -8 * max(scale, 1e-30))
+    err = np.minimum(u, u_scale)
+    exact = float(np.mean(got == ref))
+    assert err.max() <= max_ulps, f"{what}: max {err.max():.3g} ulps"
     assert exact >= min_exact, f"{what}: only {exact:.4f} bit-exact"
     return exact

@@ -55,10 +55,12 @@ def test_prepare_inputs_matches_oracle(name, over):
 def test_status_flags_bad_inputs_without_faulting():
     torch = cuda_or_skip()
     wl, b, w, kc, vc, r = setup("small_prenorm", want_logits=False, kv=False)
-    # accepted count past the verify rows, a block id out of range, a token past V
+    # accepted count past the verify rows, a block id out of range where request
+    # 0's NTP row writes, a bonus token past V
     r.inp["accepted"][1] = 99
-    r.inp["block_table"][0, 0] = b["num_blocks"] + 5
-    r.inp["prev_tok"][1] = wl.dims.vocab + 3
+    p_ntp = int(b["prev_pos"][b["qsl"][0] + b["accepted"][0]])
+    r.inp["block_table"][0, p_ntp // wl.dims.block_size] = b["num_blocks"] + 5
+    r.inp["bonus"][0] = wl.dims.vocab + 3
     r.prepare()
     torch.cuda.synchronize()
     st, rc = r.status()

@@ -39,8 +39,8 @@ def _check_kv(wl, b, kc0, vc0, r, res):
         got_k = f64(kc[slots // bs, :, slots % bs, :], dt)
         got_v = f64(vc[slots // bs, :, slots % bs, :], dt)
         if dt == "bf16":
-            check_close_bf16(got_k, out["k"], "k cache", max_ulps=1, min_exact=0.99)
-            check_close_bf16(got_v, out["v"], "v cache", max_ulps=1, min_exact=0.99)
+            check_close_bf16(got_k, out["k"], "k cache", max_ulps=1, min_exact=0.95)
+            check_close_bf16(got_v, out["v"], "v cache", max_ulps=1, min_exact=0.95)
         else:
             np.testing.assert_allclose(got_k, out["k"], rtol=1e-5, atol=1e-6)
             np.testing.assert_allclose(got_v, out["v"], rtol=1e-5, atol=1e-6)
