@@ -8,7 +8,7 @@
 // warp.  Keys stream through shared memory in chunks of 64 (cp.async, 3 stages,
 // 16-byte chunks XOR-swizzled by row so ldmatrix is conflict-free); S = Q K^T and
 // O += P V run on warp-level bf16 mma.sync with fp32 accumulators and an online
-// softmax in the exp2 domain.  Each split writes unnormalised partials; a combine
+// softmax in the exp2 domain (P enters the second product as a hi + lo bf16 pair).  Each split writes unnormalised partials; a combine
 // kernel merges the splits (flash-decoding style).
 //
 // fp32: one CTA per (sample row, query head), SIMT dot products, online softmax.
@@ -203,14 +203,16 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const AttnArgs a) {
       o[i][2] *= al_b;
       o[i][3] *= al_b;
     }
-    // O += P V: 4 k-steps of 16 keys, HD/8 n-tiles of 8 dims
+    // O += P V: 4 k-steps of 16 keys, HD/8 n-tiles of 8 dims.  P is carried as
+    // a bf16 pair hi + lo (two MMAs), about 16 significant bits, so the weights
+    // are not rounded to 8 bits before they meet V.
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      uint32_t ph[4], pl[4];
+      split_bf16x2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+      split_bf16x2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+      split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+      split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
 #pragma unroll
       for (int nd = 0; nd < HD / 8; nd += 2) {
         const int mat = lane >> 3;
@@ -218,8 +220,10 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const AttnArgs a) {
         const int ch = nd + (mat >> 1);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(vs_base + key * ROWB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(o[nd], pa, b0, b1);
-        mma_bf16_16816(o[nd + 1], pa, b2, b3);
+        mma_bf16_16816(o[nd], ph, b0, b1);
+        mma_bf16_16816(o[nd], pl, b0, b1);
+        mma_bf16_16816(o[nd + 1], ph, b2, b3);
+        mma_bf16_16816(o[nd + 1], pl, b2, b3);
       }
     }
   }

@@ -313,6 +313,16 @@ PE_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// (a, b) -> bf16 pair hi = round(a, b) and lo = round((a, b) - hi): hi + lo
+// carries about 16 significant bits of each value.
+PE_DEV void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 l =
+      __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 PE_DEV void cp_async16(uint32_t smem_addr, const void* gptr, bool valid) {
   const int n = valid ? 16 : 0;  // 0 source bytes: the destination is zero-filled
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr), "l"(gptr),
