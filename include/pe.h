@@ -195,6 +195,26 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
 int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, float* logits,
               void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free pe_argmax.  The pages have no counterpart: this is an
+ * interface addition for callers that cannot allocate device memory at all,
+ * such as a serving engine that has already reserved every byte for weights and
+ * KV cache and hands a plugin only a stream, code that runs while another
+ * component is capturing a CUDA graph (a cudaMalloc there would break the
+ * capture), or a runtime bound to a fixed memory plan.
+ * Same arguments and results as pe_argmax, without the workspace: its scratch
+ * (one 64-bit argmax key per row) lives in a static device array of
+ * PE_NOALLOC_MAX_ROWS entries (32 KiB) that every GPU loading this library holds
+ * until the process exits.  n_rows above PE_NOALLOC_MAX_ROWS returns PE_ERR_ARG.
+ * The call performs no cudaMalloc / cudaFree; it never splits the LM head over
+ * K (no partial sums to keep).  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current, so make it
+ * before any stream capture.  All calls on a device share the array: each call
+ * clears the keys it uses, and calls that overlap on the GPU race.  No status
+ * word is kept, so device-side problems are not reported. */
+#define PE_NOALLOC_MAX_ROWS 4096
+int pe_argmax_noalloc(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens,
+                      float* logits, void* stream);
+
 /* Copy the device status word from ws into *status (synchronises `stream`);
  * clear it when `clear` is non-zero.  Returns PE_OK when no bit is set,
  * PE_ERR_TIMEOUT when PE_ST_TIMEOUT is set, else PE_ERR_DEVICE_INPUT. */

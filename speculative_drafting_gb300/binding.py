@@ -96,6 +96,8 @@ def load(path: str | None = None):
     lib.pe_read_status.restype = _i32
     lib.pe_status_string.argtypes = [_i32]
     lib.pe_status_string.restype = ctypes.c_char_p
+    lib.pe_argmax_noalloc.argtypes = [_vp, _vp, _i32, _vp, _vp, _vp]
+    lib.pe_argmax_noalloc.restype = _i32
     lib.pe_test_projection_workspace.argtypes = [_vp, _i32, _i32]
     lib.pe_test_projection_workspace.restype = _sz
     lib.pe_test_projection.argtypes = [_vp, _i32, _vp, _i32, _vp, _vp, _sz, _vp]
@@ -224,6 +226,12 @@ class Drafter:
         rc = self.lib.pe_argmax(self.h, _ptr(z), n_rows, _ptr(draft_tokens), _ptr(logits), _ptr(ws),
                                 ws.numel(), _stream(stream))
         _check(rc, "pe_argmax")
+
+    def argmax_noalloc(self, z, n_rows, draft_tokens, logits=None, stream=None):
+        """pe_argmax without a workspace (its scratch is a static device array)."""
+        rc = self.lib.pe_argmax_noalloc(self.h, _ptr(z), n_rows, _ptr(draft_tokens), _ptr(logits),
+                                        _stream(stream))
+        _check(rc, "pe_argmax_noalloc")
 
     def test_projection(self, which, X, n_rows, out, stream=None):
         """One drafter projection through the step's GEMM kernel (pe_testing.h)."""

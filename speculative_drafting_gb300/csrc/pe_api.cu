@@ -571,3 +571,11 @@ const char* pe_status_string(int code) {
 }
 
 }  // extern "C"
+
+// Read-only views of a handle for other translation units of the library.
+namespace pe {
+const pe_dims* handle_dims(const pe_handle* h) { return &h->d; }
+const CUtensorMap* handle_lm_map(const pe_handle* h) { return &h->m_lm; }
+int handle_num_sms(const pe_handle* h) { return h->num_sms; }
+const void* handle_w_lm(const pe_handle* h) { return h->w.w_lm; }
+}  // namespace pe

@@ -64,4 +64,10 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t
 
 int num_sms_of_current_device();
 
+// Read-only views of a handle (defined beside the handle).
+const pe_dims* handle_dims(const pe_handle* h);
+const CUtensorMap* handle_lm_map(const pe_handle* h);
+int handle_num_sms(const pe_handle* h);
+const void* handle_w_lm(const pe_handle* h);
+
 }  // namespace pe
