@@ -34,8 +34,12 @@
  *     synchronisation, no stream creation, so a step can be captured in a CUDA
  *     graph.  Host-side sizes (B, T_in, ...) are baked into a capture.
  *   - `ws` is a caller-allocated device workspace of at least
- *     pe_workspace_bytes() bytes, 256-byte aligned; one workspace must not be
+ *     pe_workspace_bytes() bytes, 256-byte aligned.  One workspace must not be
  *     used by two calls that may run concurrently.
+ *   - Kernels are launched with programmatic stream serialisation: each one may
+ *     start its independent prologue (and pull its weights into L2) while the
+ *     previous kernel on the stream finishes, and waits for it before reading
+ *     its results.
  *   - Return value: PE_OK, or an error code below.  PE_ERR_ARG / PE_ERR_UNSUPPORTED
  *     are detected on the host before anything is enqueued.  PE_ERR_CUDA means
  *     a launch failed (cudaGetLastError).  Problems that only the device can see

@@ -42,9 +42,13 @@ Readings where the pages are silent (each one is listed in the design notes):
     z = RMSNorm(a + MLP(a); gamma_final), no further norm.
   * MLP is SwiGLU: down(silu(gate(m)) * up(m)), silu(t) = t / (1 + e^-t).
   * Greedy draft: argmax of the logits, lowest index on ties.
-  * bf16 mode: a value is rounded to bf16 (nearest, ties to even) wherever the
-    step hands it to the next stage: A, x, u, q/k/v after RoPE, the attention
-    output, the residual sums, the normalised rows, the SwiGLU product, z.
+  * bf16 mode (weights, KV cache and tensor-core operands in bf16):
+      - rounded to bf16 (nearest, ties to even): the drafter input A, q/k/v
+        after RoPE (the cache dtype), the attention output, z;
+      - carried as a bf16 pair hi + lo (hi = bf16(v), lo = bf16(v - hi), about
+        16 significant bits): the projection operands u (QKV input), the MLP
+        input (a post-norm, m pre-norm) and the SwiGLU product h;
+      - not rounded (fp32 on the GPU): the fc output x and the residual sums.
     Logits stay unrounded.  fp32 mode rounds nothing (fp64 throughout).
 
 Pins: every function here is checked in tests/test_oracle_*.py against closed
@@ -90,8 +94,18 @@ def decode(arr, dtype):
     return np.asarray(arr, dtype=np.float64)
 
 
+def bf16_pair_round(x):
+    """Value of a bf16 pair hi + lo holding x: hi = bf16(x), lo = bf16(x - hi)."""
+    hi = bf16_round(x)
+    return hi + bf16_round(np.asarray(x, dtype=np.float64) - hi)
+
+
 def _rounder(dtype):
     return bf16_round if dtype == "bf16" else (lambda v: np.asarray(v, dtype=np.float64))
+
+
+def _pair_rounder(dtype):
+    return bf16_pair_round if dtype == "bf16" else (lambda v: np.asarray(v, dtype=np.float64))
 
 
 # ---------------------------------------------------------------------------
@@ -291,7 +305,7 @@ def silu(t):
 
 
 def swiglu_mlp(m, w_gate, w_up, w_down, R):
-    """down(silu(gate(m)) * up(m)); the product is a stored intermediate."""
+    """down(silu(gate(m)) * up(m)); the product h is stored through R."""
     h = R(silu(linear(m, w_gate)) * linear(m, w_up))
     return linear(h, w_down)
 
@@ -359,6 +373,7 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
     """
     dt = dims.dtype
     R = _rounder(dt)
+    R2 = _pair_rounder(dt)
     P = _Params(w, dt)
     K, H, G_, hd = dims.K, dims.n_heads, dims.n_kv_heads, dims.head_dim
     meta = prepare_metadata(batch["qsl"], batch["prev_tok"], batch["prev_pos"],
@@ -383,8 +398,8 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
                           for o in rows])
         A = drafter_input(Grows, Erows, gam_s, dims.eps, dt)
         # (4) fc, input norm, QKV with RoPE, KV write
-        x = R(linear(A, P["w_fc"]))
-        u = x if dims.post_norm else R(rmsnorm(x, P["gamma_in"], dims.eps))
+        x = linear(A, P["w_fc"])
+        u = R2(x) if dims.post_norm else R2(rmsnorm(x, P["gamma_in"], dims.eps))
         qkv = linear(u, P["w_qkv"])
         pos = meta["pos"][rows]
         q = qkv[:, : H * hd].reshape(-1, H, hd)
@@ -414,13 +429,13 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
         xs = x[s_loc]
         o_proj = linear(attn, P["w_o"])
         if dims.post_norm:
-            a = R(rmsnorm(R(xs + o_proj), P["gamma_post"], dims.eps))
-            y = R(a + swiglu_mlp(a, P["w_gate"], P["w_up"], P["w_down"], R))
+            a = R2(rmsnorm(xs + o_proj, P["gamma_post"], dims.eps))
+            y = a + swiglu_mlp(a, P["w_gate"], P["w_up"], P["w_down"], R2)
             z = R(rmsnorm(y, P["gamma_final"], dims.eps))
         else:
-            a = R(xs + o_proj)
-            m = R(rmsnorm(a, P["gamma_post"], dims.eps))
-            y = R(a + swiglu_mlp(m, P["w_gate"], P["w_up"], P["w_down"], R))
+            a = xs + o_proj
+            m = R2(rmsnorm(a, P["gamma_post"], dims.eps))
+            y = a + swiglu_mlp(m, P["w_gate"], P["w_up"], P["w_down"], R2)
             z = R(rmsnorm(y, P["gamma_final"], dims.eps))
         res = dict(rows=rows, A=A, x=x, u=u, k=k, v=v, slot=meta["slot"][rows],
                    q=q[s_loc], attn=attn, a=a, z=z)

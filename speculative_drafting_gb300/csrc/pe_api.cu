@@ -47,24 +47,11 @@ GemmShape gemm_shape(const pe_handle* h, int id) {
   }
 }
 
-TcPlan plan_of(const pe_handle* h, int id, int N) {
+// The LM head never splits K: its argmax epilogue needs whole sums, and its
+// vocabulary gives plenty of tiles.
+TcPlan plan_of(const pe_handle* h, int id, int N, bool bpair) {
   const GemmShape s = gemm_shape(h, id);
-  return plan_gemm_tc(s.M, s.K, N, s.dual, h->num_sms, true);
-}
-
-// Largest split-K partial buffer and counter count over every N <= N_max.
-// Within one count of N tiles the split count is fixed and the bytes grow with
-// N, so the top of each range is enough.
-void gemm_scratch_bound(const pe_handle* h, int id, int N_max, size_t& partial, int& counters) {
-  partial = 0;
-  counters = 0;
-  if (!is_bf16(h) || N_max <= 0) return;
-  const int nt_max = (N_max + 255) / 256;
-  for (int nt = 1; nt <= nt_max; ++nt) {
-    const TcPlan p = plan_of(h, id, std::min(256 * nt, N_max));
-    partial = std::max(partial, p.partial_bytes);
-    counters = std::max(counters, p.n_counters);
-  }
+  return plan_gemm_tc(s.M, s.K, N, s.dual, bpair ? 1 : 0, h->num_sms, id != G_LM);
 }
 
 // Attention split partials, bounded over every batch size <= B (the split count
@@ -85,10 +72,12 @@ size_t attn_scratch_bound(const pe_handle* h, int B, int max_blocks) {
 }
 
 struct Layout {
-  size_t status, counters, x, u, qkv, q_s, x_s, attn, r1, a, m, hm, y, amax, partial, attn_part;
+  // x: fc output (fp32); u / u_lo: QKV operand (bf16 pair; fp32 in fp32 mode);
+  // qkv (fp32); q_s; x_s: residual rows (fp32); attn; r: attention residual sum
+  // (fp32); a / a_lo / a_f: MLP operand pair and its fp32 value; h / h_lo:
+  // SwiGLU product pair; y: MLP residual sum (fp32); amax: argmax keys
+  size_t status, x, u, u_lo, qkv, q_s, x_s, attn, r, a, a_lo, a_f, h, h_lo, y, amax, attn_part;
   size_t total;
-  int counter_off[G_COUNT];
-  int n_counters;
 };
 
 // Workspace layout of a step with B requests, T_in verify rows and block tables
@@ -109,32 +98,22 @@ Layout layout_of(const pe_handle* h, int B, int T_in, int max_blocks) {
     return o;
   };
   L.status = take(256);
-  const int Ns[G_COUNT] = {T_out, T_out, NS, NS, NS, NS};
-  size_t part = 0;
-  int nc = 0;
-  for (int g = 0; g < G_COUNT; ++g) {
-    size_t p;
-    int c;
-    gemm_scratch_bound(h, g, Ns[g], p, c);
-    part = std::max(part, p);
-    L.counter_off[g] = nc;
-    nc += c;
-  }
-  L.n_counters = nc;
-  L.counters = take(static_cast<size_t>(std::max(nc, 1)) * sizeof(int));
-  L.x = take(static_cast<size_t>(T_out) * d.d * e);
-  L.u = take(static_cast<size_t>(T_out) * d.d * e);
-  L.qkv = take(static_cast<size_t>(T_out) * QKV * sizeof(float));
+  const size_t f4 = sizeof(float);
+  L.x = take(static_cast<size_t>(T_out) * d.d * f4);
+  L.u = take(static_cast<size_t>(T_out) * d.d * f4);
+  L.u_lo = take(static_cast<size_t>(T_out) * d.d * e);
+  L.qkv = take(static_cast<size_t>(T_out) * QKV * f4);
   L.q_s = take(static_cast<size_t>(NS) * Hd * e);
-  L.x_s = take(static_cast<size_t>(NS) * d.d * e);
+  L.x_s = take(static_cast<size_t>(NS) * d.d * f4);
   L.attn = take(static_cast<size_t>(NS) * Hd * e);
-  L.r1 = take(static_cast<size_t>(NS) * d.d * e);
-  L.a = take(static_cast<size_t>(NS) * d.d * e);
-  L.m = take(static_cast<size_t>(NS) * d.d * e);
-  L.hm = take(static_cast<size_t>(NS) * d.inter * e);
-  L.y = take(static_cast<size_t>(NS) * d.d * e);
+  L.r = take(static_cast<size_t>(NS) * d.d * f4);
+  L.a = take(static_cast<size_t>(NS) * d.d * f4);
+  L.a_lo = take(static_cast<size_t>(NS) * d.d * e);
+  L.a_f = take(static_cast<size_t>(NS) * d.d * f4);
+  L.h = take(static_cast<size_t>(NS) * d.inter * f4);
+  L.h_lo = take(static_cast<size_t>(NS) * d.inter * e);
+  L.y = take(static_cast<size_t>(NS) * d.d * f4);
   L.amax = take(static_cast<size_t>(NS) * sizeof(unsigned long long));
-  L.partial = take(part);
   L.attn_part = take(attn_scratch_bound(h, B, max_blocks));
   L.total = off;
   return L;
@@ -150,14 +129,7 @@ Layout layout_argmax(const pe_handle* h, int n_rows) {
     return o;
   };
   L.status = take(256);
-  size_t part;
-  int nc;
-  gemm_scratch_bound(h, G_LM, n_rows, part, nc);
-  L.counter_off[G_LM] = 0;
-  L.n_counters = nc;
-  L.counters = take(static_cast<size_t>(std::max(nc, 1)) * sizeof(int));
   L.amax = take(static_cast<size_t>(n_rows) * sizeof(unsigned long long));
-  L.partial = take(part);
   L.total = off;
   return L;
 }
@@ -172,13 +144,8 @@ Layout layout_projection(const pe_handle* h, int which, int n_rows) {
     return o;
   };
   L.status = take(256);
-  size_t part;
-  int nc;
-  gemm_scratch_bound(h, which, n_rows, part, nc);
-  L.counter_off[which] = 0;
-  L.n_counters = nc;
-  L.counters = take(static_cast<size_t>(std::max(nc, 1)) * sizeof(int));
-  L.partial = take(part);
+  (void)which;
+  (void)n_rows;
   L.total = off;
   return L;
 }
@@ -199,8 +166,10 @@ int check_meta(const pe_meta* m) {
 }
 
 // One projection of the step, on the tensor cores (bf16) or SIMT (fp32).
-int run_gemm(pe_handle* h, int id, const void* X, int N_cap, const int* n_rows_dev,
-             const Epilogue& epi, void* ws, const Layout& L, cudaStream_t st) {
+// X_lo: the low half of a bf16-pair operand (bf16 only; nullable).
+int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
+             const int* n_rows_dev, const Epilogue& epi, void* ws, const Layout& L,
+             cudaStream_t st) {
   const GemmShape s = gemm_shape(h, id);
   if (!is_bf16(h)) {
     const pe_weights& w = h->w;
@@ -210,12 +179,11 @@ int run_gemm(pe_handle* h, int id, const void* X, int N_cap, const int* n_rows_d
     return launch_gemm_f32(static_cast<const float*>(W), static_cast<const float*>(W2),
                            static_cast<const float*>(X), s.M, s.K, N_cap, n_rows_dev, epi, st);
   }
-  const TcPlan p = plan_of(h, id, N_cap);
+  const TcPlan p = plan_of(h, id, N_cap, X_lo != nullptr);
   const CUtensorMap* mA = id == G_FC ? &h->m_fc : id == G_QKV ? &h->m_qkv : id == G_O ? &h->m_o
                         : id == G_GATEUP ? &h->m_gate : id == G_DOWN ? &h->m_down : &h->m_lm;
   const CUtensorMap* mA2 = id == G_GATEUP ? &h->m_up : nullptr;
-  return launch_gemm_tc(p, mA, mA2, X, n_rows_dev, epi, at<float>(ws, L.partial),
-                        at<int>(ws, L.counters) + L.counter_off[id], at<uint32_t>(ws, L.status), st);
+  return launch_gemm_tc(p, mA, mA2, X, X_lo, n_rows_dev, epi, at<uint32_t>(ws, L.status), st);
 }
 
 }  // namespace
@@ -298,8 +266,7 @@ int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl, const i
     return PE_ERR_ARG;
   const pe_dims& d = h->d;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint32_t* status = at<uint32_t>(ws, 0);
-  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return PE_ERR_CUDA;
+  uint32_t* status = at<uint32_t>(ws, 0);  // cleared by the metadata kernel
   MetaLaunch ml;
   ml.B = B;
   ml.T_in = T_in;
@@ -382,38 +349,55 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   const int QKV = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
   uint32_t* status = at<uint32_t>(ws, L.status);
   const int dt = d.dtype;
-  if (L.n_counters > 0 &&
-      cudaMemsetAsync(at<int>(ws, L.counters), 0, L.n_counters * sizeof(int), st) != cudaSuccess)
-    return PE_ERR_CUDA;
-  void* x = at<void>(ws, L.x);
-  void* u = d.post_norm ? x : at<void>(ws, L.u);
-  void* qkv = at<void>(ws, L.qkv);
+  const bool bf = dt == PE_DTYPE_BF16;
+  float* x = at<float>(ws, L.x);
+  void* u = at<void>(ws, L.u);
+  bf16_t* u_lo = bf ? at<bf16_t>(ws, L.u_lo) : nullptr;
+  float* qkv = at<float>(ws, L.qkv);
   void* q_s = at<void>(ws, L.q_s);
-  void* x_s = at<void>(ws, L.x_s);
+  float* x_s = at<float>(ws, L.x_s);
   void* attn = at<void>(ws, L.attn);
-  void* r1 = at<void>(ws, L.r1);
+  float* r = at<float>(ws, L.r);
   void* a = at<void>(ws, L.a);
-  void* m = at<void>(ws, L.m);
-  void* hm = at<void>(ws, L.hm);
-  void* y = at<void>(ws, L.y);
+  bf16_t* a_lo = bf ? at<bf16_t>(ws, L.a_lo) : nullptr;
+  float* a_f = at<float>(ws, L.a_f);
+  void* hm = at<void>(ws, L.h);
+  bf16_t* h_lo = bf ? at<bf16_t>(ws, L.h_lo) : nullptr;
+  float* y = at<float>(ws, L.y);
   int rc;
-  // fc: x = A W_fc^T over the non-rejected rows
+  auto norm = [&](const float* in, const void* gamma, int apply, void* out, bf16_t* out_lo,
+                  float* out_f32, int rows, const int* n_rows_dev) {
+    RowNormArgs n{};
+    n.x = in;
+    n.ld_x = d.d;
+    n.gamma = gamma;
+    n.apply_norm = apply;
+    n.out = out;
+    n.out_lo = out_lo;
+    n.out_f32 = out_f32;
+    n.ld_out = d.d;
+    n.d = d.d;
+    n.eps = d.eps;
+    n.rows_cap = rows;
+    n.n_rows_dev = n_rows_dev;
+    return launch_rownorm(n, dt, st);
+  };
+  // fc: x = A W_fc^T over the non-rejected rows (fp32)
   Epilogue e;
-  e.mode = EPI_STORE;
+  e.mode = EPI_STORE_F32;
   e.out = x;
   e.ld_out = d.d;
-  if ((rc = run_gemm(h, G_FC, A, T_out, meta->n_valid, e, ws, L, st)) != PE_OK) return rc;
-  // pre-norm: u = RMSNorm(x; gamma_in)
-  if (!d.post_norm &&
-      (rc = launch_rmsnorm(x, d.d, h->w.gamma_in, u, d.d, d.d, d.eps, T_out, meta->n_valid, dt,
-                           st)) != PE_OK)
+  if ((rc = run_gemm(h, G_FC, A, nullptr, T_out, meta->n_valid, e, ws, L, st)) != PE_OK) return rc;
+  // QKV operand u: RMSNorm(x; gamma_in) (pre-norm) or x (post-norm), as a bf16 pair
+  if ((rc = norm(x, h->w.gamma_in, d.post_norm ? 0 : 1, u, u_lo, nullptr, T_out, meta->n_valid)) !=
+      PE_OK)
     return rc;
   // QKV (fp32, RoPE follows)
   e = Epilogue();
   e.mode = EPI_STORE_F32;
   e.out = qkv;
   e.ld_out = QKV;
-  if ((rc = run_gemm(h, G_QKV, u, T_out, meta->n_valid, e, ws, L, st)) != PE_OK) return rc;
+  if ((rc = run_gemm(h, G_QKV, u, u_lo, T_out, meta->n_valid, e, ws, L, st)) != PE_OK) return rc;
   // RoPE, KV write at the non-rejected slots, sample-row q and residual rows
   RopeArgs ra{};
   ra.T_out = T_out;
@@ -425,7 +409,7 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   ra.d = d.d;
   ra.bs = d.block_size;
   ra.num_blocks = num_blocks;
-  ra.qkv = static_cast<const float*>(qkv);
+  ra.qkv = qkv;
   ra.x = x;
   ra.n_valid = meta->n_valid;
   ra.valid_rows = meta->valid_rows;
@@ -463,40 +447,39 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   aa.out = attn;
   aa.status = status;
   if ((rc = launch_attention(aa, dt, st)) != PE_OK) return rc;
-  // O projection + residual
+  // O projection + residual: r = x_s + attn W_o^T (fp32)
   e = Epilogue();
-  e.mode = EPI_RESID;
-  e.out = d.post_norm ? r1 : a;
+  e.mode = EPI_RESID_F32;
+  e.out = r;
   e.ld_out = d.d;
   e.resid = x_s;
   e.ld_resid = d.d;
-  if ((rc = run_gemm(h, G_O, attn, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
-  // post-norm: a = RMSNorm(r1; gamma_post); pre-norm: m = RMSNorm(a; gamma_post)
-  if (d.post_norm) {
-    if ((rc = launch_rmsnorm(r1, d.d, h->w.gamma_post, a, d.d, d.d, d.eps, NS, nullptr, dt, st)) != PE_OK)
-      return rc;
-  } else {
-    if ((rc = launch_rmsnorm(a, d.d, h->w.gamma_post, m, d.d, d.d, d.eps, NS, nullptr, dt, st)) != PE_OK)
-      return rc;
-  }
-  // SwiGLU: hm = silu(gate) * up
-  e = Epilogue();
-  e.mode = EPI_SWIGLU;
-  e.out = hm;
-  e.ld_out = d.inter;
-  if ((rc = run_gemm(h, G_GATEUP, d.post_norm ? a : m, NS, nullptr, e, ws, L, st)) != PE_OK)
+  if ((rc = run_gemm(h, G_O, attn, nullptr, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
+  // MLP operand: post-norm a = RMSNorm(r; gamma_post), which is also the MLP
+  // residual (kept as the fp32 value of the pair); pre-norm m = RMSNorm(r), the
+  // residual being r itself
+  if ((rc = norm(r, h->w.gamma_post, 1, a, a_lo, d.post_norm ? a_f : nullptr, NS, nullptr)) !=
+      PE_OK)
     return rc;
-  // down projection + residual
+  const float* mlp_resid = d.post_norm ? (bf ? a_f : static_cast<const float*>(a)) : r;
+  // SwiGLU: h = silu(gate) * up (a bf16 pair in bf16 mode)
   e = Epilogue();
-  e.mode = EPI_RESID;
+  e.mode = bf ? EPI_SWIGLU_PAIR : EPI_SWIGLU;
+  e.out = hm;
+  e.out2 = h_lo;
+  e.ld_out = d.inter;
+  if ((rc = run_gemm(h, G_GATEUP, a, a_lo, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
+  // down projection + residual (fp32)
+  e = Epilogue();
+  e.mode = EPI_RESID_F32;
   e.out = y;
   e.ld_out = d.d;
-  e.resid = a;
+  e.resid = mlp_resid;
   e.ld_resid = d.d;
-  if ((rc = run_gemm(h, G_DOWN, hm, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
-  // z = RMSNorm(y; gamma_final)
+  if ((rc = run_gemm(h, G_DOWN, hm, h_lo, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
+  // z = RMSNorm(y; gamma_final), the LM head operand
   (void)Hd;
-  return launch_rmsnorm(y, d.d, h->w.gamma_final, z_out, d.d, d.d, d.eps, NS, nullptr, dt, st);
+  return norm(y, h->w.gamma_final, 1, z_out, nullptr, nullptr, NS, nullptr);
 }
 
 int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, float* logits,
@@ -510,15 +493,12 @@ int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, fl
   if (cudaMemsetAsync(keys, 0, static_cast<size_t>(n_rows) * sizeof(unsigned long long), st) !=
       cudaSuccess)
     return PE_ERR_CUDA;
-  if (L.n_counters > 0 &&
-      cudaMemsetAsync(at<int>(ws, L.counters), 0, L.n_counters * sizeof(int), st) != cudaSuccess)
-    return PE_ERR_CUDA;
   Epilogue e;
   e.mode = EPI_ARGMAX;
   e.amax = keys;
   e.logits = logits;
   e.ld_logits = h->d.vocab;
-  int rc = run_gemm(h, G_LM, z, n_rows, nullptr, e, ws, L, st);
+  int rc = run_gemm(h, G_LM, z, nullptr, n_rows, nullptr, e, ws, L, st);
   if (rc != PE_OK) return rc;
   return launch_argmax_finalize(keys, n_rows, draft_tokens, st);
 }
@@ -535,14 +515,11 @@ int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void*
   const Layout L = layout_projection(h, which, n_rows);
   if (ws_bytes < L.total) return PE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (L.n_counters > 0 &&
-      cudaMemsetAsync(at<int>(ws, L.counters), 0, L.n_counters * sizeof(int), st) != cudaSuccess)
-    return PE_ERR_CUDA;
   Epilogue e;
   e.mode = which == G_GATEUP ? EPI_SWIGLU : EPI_STORE_F32;
   e.out = out;
   e.ld_out = gemm_shape(h, which).M;
-  return run_gemm(h, which, X, n_rows, nullptr, e, ws, L, st);
+  return run_gemm(h, which, X, nullptr, n_rows, nullptr, e, ws, L, st);
 }
 
 int pe_read_status(const pe_handle* h, void* ws, uint32_t* status, int clear, void* stream) {

@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const AttnArgs a) {
   constexpr int CH = HD / 8;         // 16-byte chunks per key row
   constexpr int TILE = kKC * ROWB;   // one K or V chunk
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_trigger();
+  pdl_wait();
   const int split = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int HG = a.H / a.G;
   const int rows = a.K * HG;
@@ -259,6 +261,8 @@ template <typename T>
 __global__ void attn_combine_kernel(const AttnArgs a) {
   __shared__ float w_sh[kMaxSplits];
   __shared__ float inv_sh;
+  pdl_trigger();
+  pdl_wait();
   const size_t sh = blockIdx.x;  // (sample, head)
   const size_t n_sh = static_cast<size_t>(a.B) * a.K * a.H;
   if (threadIdx.x < 32) {
@@ -288,6 +292,8 @@ __global__ void attn_combine_kernel(const AttnArgs a) {
 // fp32: one CTA (4 warps) per (sample row, query head)
 __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
   __shared__ float wm[4], wl[4], wacc[4][128];
+  pdl_trigger();
+  pdl_wait();
   const int s = blockIdx.x, h = blockIdx.y;
   const int r = s / a.K, k = s % a.K;
   const int g = h / (a.H / a.G);
@@ -379,8 +385,9 @@ size_t attention_scratch_bytes(int B, int K, int H, int hd, int n_splits) {
 int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
   if (a.B <= 0) return PE_OK;
   if (dtype != PE_DTYPE_BF16) {
-    attn_f32_kernel<<<dim3(a.B * a.K, a.H), 128, 0, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+    return launch_pdl(attn_f32_kernel, dim3(a.B * a.K, a.H), dim3(128), 0, st, a) == cudaSuccess
+               ? PE_OK
+               : PE_ERR_CUDA;
   }
   const int rows = a.K * (a.H / a.G);
   const int warps = (rows + 15) / 16;
@@ -390,16 +397,20 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
   const int smem_max = kStages * 2 * kKC * 128 * 2;
   if (a.hd == 64) {
     cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-    attn_mma_kernel<64><<<grid, warps * 32, smem, st>>>(a);
+    if (launch_pdl(attn_mma_kernel<64>, grid, dim3(warps * 32), smem, st, a) != cudaSuccess)
+      return PE_ERR_CUDA;
   } else if (a.hd == 128) {
     cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-    attn_mma_kernel<128><<<grid, warps * 32, smem, st>>>(a);
+    if (launch_pdl(attn_mma_kernel<128>, grid, dim3(warps * 32), smem, st, a) != cudaSuccess)
+      return PE_ERR_CUDA;
   } else {
     return PE_ERR_UNSUPPORTED;
   }
   if (cudaGetLastError() != cudaSuccess) return PE_ERR_CUDA;
-  attn_combine_kernel<bf16><<<a.B * a.K * a.H, std::min(a.hd, 128), 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+  return launch_pdl(attn_combine_kernel<bf16>, dim3(a.B * a.K * a.H), dim3(std::min(a.hd, 128)), 0,
+                    st, a) == cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
 }
 
 }  // namespace pe

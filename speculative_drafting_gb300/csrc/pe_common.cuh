@@ -74,6 +74,37 @@ PE_DEV uint4 pack16<bf16>(const float* f) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the step is launched with programmatic stream serialisation:
+// it lets the next kernel be scheduled as soon as it starts (pdl_trigger) and
+// waits for the previous kernel's completion and memory (pdl_wait) before it
+// reads anything that kernel wrote.  Without the launch attribute both are
+// no-ops.
+
+PE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+PE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kernel` on `st` with programmatic stream serialisation.
+template <typename... Exp, typename... Act>
+inline cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Act&&... args) {
+  // Every kernel of the step asks for the largest shared-memory carveout, so
+  // consecutive kernels never make an SM drain to change its L1/shared split.
+  cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+}
+
 // ---------------------------------------------------------------- small utilities
 
 PE_DEV void set_status(uint32_t* st, uint32_t bits) {
@@ -186,6 +217,14 @@ PE_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, i
       : "memory");
 }
 
+// Prefetch one tensor-map box into L2 (no shared memory, no barrier).
+PE_DEV void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 PE_DEV uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -279,6 +318,31 @@ PE_DEV void tmem_ld16(uint32_t taddr, float* v) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------- thread-block clusters
+
+PE_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of every CTA of the cluster: release this CTA's shared-memory
+// writes, then wait until every CTA of the cluster has arrived.
+PE_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Load a float from the shared memory of CTA `rank` of this cluster, at the
+// same offset as the local address `local`.
+PE_DEV float ld_dsmem_f32(uint32_t local, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
 }
 
 PE_DEV void named_bar_sync(int id, int nthreads) {

@@ -8,13 +8,16 @@
 // evict-last) into a ring of shared-memory stages; one thread of warp 1 issues
 // tcgen05.mma into a TMEM accumulator; warps 2-5 read the accumulator with
 // tcgen05.ld and run the epilogue.  Small-N projections split K across CTAs so
-// every SM streams weights; the last CTA of a tile sums the fp32 partials in a
-// fixed order (deterministic) and runs the epilogue.
+// every SM streams weights: the splits of a tile form a thread-block cluster
+// and add their fp32 partial tiles through distributed shared memory, in rank
+// order (deterministic), before the epilogue.
 //
 // fp32: a plain shared-memory-tiled SIMT kernel with the same epilogues (fp32
 // FMA; TF32 would not meet a 1e-5 logit tolerance).
 #include <algorithm>
 #include <cstdio>
+#include <map>
+#include <mutex>
 
 #include "pe_common.cuh"
 #include "pe_internal.h"
@@ -25,17 +28,17 @@ constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBK = 64;   // reduction elements per k-block: one 128-byte swizzle row
 constexpr int kMaxStages = 12;
 constexpr size_t kSmemBudget = 212 * 1024;  // dynamic shared memory for the stage ring
+constexpr int kPrefetchKb = 16;             // k-blocks of weights pulled into L2 early
+constexpr int kMaxClusterSplits = 8;        // portable cluster size
 constexpr int kTcThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;
 
 struct TcArgs {
-  int M, K, N_cap, dual;
+  int M, K, N_cap, dual, bpair;
   int BN, n_tiles, m_tiles, k_splits, kb_per_split, num_kb, stages, acc_bufs;
   uint32_t tmem_cols;
   const int* n_rows_dev;
   Epilogue epi;
-  float* partial;  // [k_splits][N_cap][n_acc][M]
-  int* counters;   // [m_tiles * n_tiles]
   uint32_t* status;
 };
 
@@ -50,15 +53,21 @@ PE_DEV void epi_store_elem(const Epilogue& e, int f, int t, float v, float v2) {
     case EPI_STORE_F32:
       static_cast<float*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] = v;
       break;
-    case EPI_RESID: {
-      const float r =
-          Elem<T>::to_f(static_cast<const T*>(e.resid)[static_cast<size_t>(t) * e.ld_resid + f]);
-      static_cast<T*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] = Elem<T>::from_f(v + r);
+    case EPI_RESID_F32:
+      static_cast<float*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] =
+          v + e.resid[static_cast<size_t>(t) * e.ld_resid + f];
       break;
-    }
     case EPI_SWIGLU: {
       const float s = v / (1.0f + expf(-v));
       static_cast<T*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] = Elem<T>::from_f(s * v2);
+      break;
+    }
+    case EPI_SWIGLU_PAIR: {
+      const float h = v / (1.0f + expf(-v)) * v2;
+      const bf16 hi = __float2bfloat16_rn(h);
+      const size_t o = static_cast<size_t>(t) * e.ld_out + f;
+      static_cast<bf16*>(e.out)[o] = hi;
+      static_cast<bf16*>(e.out2)[o] = __float2bfloat16_rn(h - __bfloat162float(hi));
       break;
     }
     default:
@@ -109,44 +118,50 @@ PE_DEV void tc_epilogue16(const TcArgs& p, int f, int j0, const float* v, const 
 }
 
 // ------------------------------------------------------------------ tcgen05 kernel
+//
+// Two schedules share the kernel:
+//  * k_splits == 1: persistent.  CTA b takes tiles b, b + grid, ... over
+//    (m, n) tiles; two TMEM accumulators (when they fit) let the MMA of the
+//    next tile run while the epilogue drains the current one.
+//  * k_splits > 1: the splits of one (m, n) tile are one thread-block cluster
+//    (rank = split).  Each CTA streams its share of K, parks its fp32 partial
+//    tile in its own shared memory (the stage ring is idle by then), and after a
+//    cluster barrier every CTA sums, over the cluster's ranks in rank order
+//    (deterministic), the columns j with j % k_splits == rank, read through
+//    distributed shared memory, and runs the epilogue on them.
 
-// Sum of the fp32 split partials of 16 token columns of feature f, in split
-// order (deterministic).  Four splits' loads are issued before they are added.
-PE_DEV void sum_partials16(const TcArgs& p, int acc, int f, int j0, int n_rows, float* v) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = 0.f;
-  if (f >= p.M) return;
-  const int nacc = p.dual ? 2 : 1;
-  auto at = [&](int s, int j) -> const float* {
-    return p.partial + ((static_cast<size_t>(s) * p.N_cap + j) * nacc + acc) * p.M + f;
-  };
-  int s = 0;
-  for (; s + 4 <= p.k_splits; s += 4) {
-    float t[4][16];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int i = 0; i < 16; ++i) t[u][i] = (j0 + i < n_rows) ? __ldcg(at(s + u, j0 + i)) : 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] += t[u][i];
+struct TileRef {
+  int m, n, ks;
+};
+
+// The tile a CTA works on at its it-th turn; false when it has no more.
+PE_DEV bool next_tile(const TcArgs& p, int it, TileRef& t) {
+  if (p.k_splits > 1) {
+    if (it > 0) return false;
+    const int tile = blockIdx.x / p.k_splits;
+    t.ks = blockIdx.x % p.k_splits;
+    t.n = tile % p.n_tiles;
+    t.m = tile / p.n_tiles;
+    return t.m < p.m_tiles;
   }
-  for (; s < p.k_splits; ++s)
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (j0 + i < n_rows) v[i] += __ldcg(at(s, j0 + i));
+  const int tile = blockIdx.x + it * gridDim.x;
+  if (tile >= p.m_tiles * p.n_tiles) return false;
+  t.ks = 0;
+  t.n = tile % p.n_tiles;
+  t.m = tile / p.n_tiles;
+  return true;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
-                   const __grid_constant__ CUtensorMap mapB, const TcArgs p) {
+                   const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapB2,
+                   const TcArgs p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
   __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_sh, n_rows_sh, last_sh;
+  __shared__ int abort_sh, n_rows_sh;
   __shared__ unsigned long long red_sh[4][16];
   __shared__ int ep_ok[2][4];
 
@@ -154,12 +169,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int nA = p.dual ? 2 : 1;
+  const int nB = p.bpair ? 2 : 1;
   const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * 128u;
-  const uint32_t stage_bytes = kABytes * nA + b_bytes;
-  // accumulator buffers in TMEM: two when they fit, so the MMA of the next tile
-  // runs while the epilogue drains this one
+  const uint32_t stage_bytes = kABytes * nA + b_bytes * nB;
   const int nbuf = p.acc_bufs;
   const uint32_t buf_cols = static_cast<uint32_t>(p.BN * nA);
+  const bool clustered = p.k_splits > 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -172,22 +187,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(&final_bar, 1);
     abort_sh = 0;
-    int n = p.N_cap;
-    if (p.n_rows_dev) {
-      const int v = *p.n_rows_dev;
-      n = v < 0 ? 0 : (v < n ? v : n);
-    }
-    n_rows_sh = n;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&mapA);
     if (p.dual) prefetch_tmap(&mapA2);
     prefetch_tmap(&mapB);
+    if (p.bpair) prefetch_tmap(&mapB2);
+    // The weights do not depend on the previous kernel: start pulling this
+    // CTA's first tile into L2 while that kernel finishes.
+    TileRef t;
+    if (next_tile(p, 0, t)) {
+      const int kb0 = t.ks * p.kb_per_split;
+      const int kb1 = min(min(p.num_kb, kb0 + p.kb_per_split), kb0 + kPrefetchKb);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        tma_prefetch_l2_2d(&mapA, kb * kBK, t.m * kBM);
+        if (p.dual) tma_prefetch_l2_2d(&mapA2, kb * kBK, t.m * kBM);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, p.tmem_cols);
     tmem_relinquish();
+  }
+  // the token rows, the row count and the epilogue's inputs come from earlier kernels
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    int n = p.N_cap;
+    if (p.n_rows_dev) {
+      const int v = *p.n_rows_dev;
+      n = v < 0 ? 0 : (v < n ? v : n);
+    }
+    n_rows_sh = n;
   }
   tc_fence_before();
   __syncthreads();
@@ -195,12 +227,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const uint32_t tmem_base = tmem_base_sh;
   const int n_rows = n_rows_sh;
-  const int total = p.m_tiles * p.n_tiles * p.k_splits;
   volatile int* abort_flag = &abort_sh;
   auto fail = [&]() {
     abort_sh = 1;
     set_status(p.status, PE_ST_TIMEOUT);
   };
+  // cluster mode: this CTA's partial tile, [acc][column][128 features] fp32,
+  // parked at the start of the (by then idle) stage ring
+  float* part = reinterpret_cast<float*>(smem);
 
   if (warp == 0) {
     // ---------------- TMA producer
@@ -210,11 +244,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;  // per stage: ever armed / parity of the last arm
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-        const int n = t % p.n_tiles, rest = t / p.n_tiles;
-        const int ks = rest % p.k_splits, m = rest / p.k_splits;
-        if (n * p.BN >= n_rows) continue;
-        const int kb0 = ks * p.kb_per_split;
+      TileRef t;
+      for (int it = 0; next_tile(p, it, t) && !*abort_flag; ++it) {
+        if (t.n * p.BN >= n_rows) continue;
+        const int kb0 = t.ks * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
@@ -223,9 +256,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes;
           mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
-          tma_load_2d(sa, &mapA, &full_bar[stage], kb * kBK, m * kBM, pol_w);
-          if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], kb * kBK, m * kBM, pol_w);
-          tma_load_2d(sa + kABytes * nA, &mapB, &full_bar[stage], kb * kBK, n * p.BN, pol_x);
+          tma_load_2d(sa, &mapA, &full_bar[stage], kb * kBK, t.m * kBM, pol_w);
+          if (p.dual)
+            tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], kb * kBK, t.m * kBM, pol_w);
+          tma_load_2d(sa + kABytes * nA, &mapB, &full_bar[stage], kb * kBK, t.n * p.BN, pol_x);
+          if (p.bpair)
+            tma_load_2d(sa + kABytes * nA + b_bytes, &mapB2, &full_bar[stage], kb * kBK,
+                        t.n * p.BN, pol_x);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == p.stages) {
@@ -247,15 +284,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------- MMA issuer (one thread)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBM, p.BN);
-      int stage = 0, it = 0;
+      int stage = 0, cnt = 0;
       uint32_t phase = 0, acc_phase[2] = {0u, 0u};
-      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-        const int n = t % p.n_tiles, rest = t / p.n_tiles;
-        const int ks = rest % p.k_splits;
-        if (n * p.BN >= n_rows) continue;
-        const int b = it % nbuf;
-        ++it;
-        const int kb0 = ks * p.kb_per_split;
+      TileRef t;
+      for (int it = 0; next_tile(p, it, t) && !*abort_flag; ++it) {
+        if (t.n * p.BN >= n_rows) continue;
+        const int b = cnt % nbuf;
+        ++cnt;
+        const int kb0 = t.ks * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         if (!mbar_wait(&tempty_bar[b], acc_phase[b] ^ 1u, abort_flag)) {
           fail();
@@ -275,14 +311,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint64_t adesc = sw128_kmajor_desc(sa);
           const uint64_t a2desc = sw128_kmajor_desc(sa + kABytes);
           const uint64_t bdesc = sw128_kmajor_desc(sa + kABytes * nA);
+          const uint64_t b2desc = sw128_kmajor_desc(sa + kABytes * nA + b_bytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // advance 16 elements (32 bytes) along K inside the swizzle row
             const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
             umma_bf16(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, acc);
-            if (p.dual)
-              umma_bf16(d0 + static_cast<uint32_t>(p.BN), a2desc + 2 * kk, bdesc + 2 * kk, idesc,
-                        acc);
+            if (p.bpair) umma_bf16(d0, adesc + 2 * kk, b2desc + 2 * kk, idesc, 1u);
+            if (p.dual) {
+              const uint32_t d1 = d0 + static_cast<uint32_t>(p.BN);
+              umma_bf16(d1, a2desc + 2 * kk, bdesc + 2 * kk, idesc, acc);
+              if (p.bpair) umma_bf16(d1, a2desc + 2 * kk, b2desc + 2 * kk, idesc, 1u);
+            }
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == p.stages) {
@@ -304,15 +344,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;
     const int ew = warp - 2;
     const int et = threadIdx.x - 64;
+    const int fl = q * 32 + lane;  // this thread's feature within the tile
     uint32_t acc_phase[2] = {0u, 0u};
-    int it = 0;
-    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-      const int n = t % p.n_tiles, rest = t / p.n_tiles;
-      const int ks = rest % p.k_splits, m = rest / p.k_splits;
-      if (n * p.BN >= n_rows) continue;
-      const int b = it % nbuf;
-      const int par = it & 1;
-      ++it;
+    int cnt = 0;
+    TileRef t;
+    for (int it = 0; next_tile(p, it, t) && !*abort_flag; ++it) {
+      if (t.n * p.BN >= n_rows) continue;
+      const int b = cnt % nbuf;
+      const int par = cnt & 1;
+      ++cnt;
       // the four epilogue warps decide together whether to go on, so none of
       // them can be left waiting at a named barrier the others skipped
       const bool ok = mbar_wait(&tfull_bar[b], acc_phase[b], abort_flag);
@@ -324,11 +364,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       acc_phase[b] ^= 1u;
       tc_fence_after();
-      const int f = m * kBM + q * 32 + lane;
-      const int jt = n * p.BN;
+      const int f = t.m * kBM + fl;
+      const int jt = t.n * p.BN;
       const uint32_t tl = tmem_base + static_cast<uint32_t>(b) * buf_cols +
                           (static_cast<uint32_t>(q * 32) << 16);
-      if (p.k_splits == 1) {
+      if (!clustered) {
         for (int c = 0; c < p.BN; c += 16) {
           float v[16], v2[16];
           tmem_ld16(tl + c, v);
@@ -341,42 +381,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_epilogue16(p, f, jt + c, v, p.dual ? v2 : nullptr, n_rows, red_sh, ew, et);
         }
       } else {
+        // park the partial tile: part[a][j][fl] (consecutive features, conflict-free)
         for (int c = 0; c < p.BN; c += 16) {
-          float v[16], v2[16];
+          float v[16];
           tmem_ld16(tl + c, v);
-          if (p.dual) tmem_ld16(tl + p.BN + c, v2);
-          if (f < p.M) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int j = jt + c + i;
-              if (j < n_rows) {
-                const size_t base = (static_cast<size_t>(ks) * p.N_cap + j) * nA;
-                p.partial[base * p.M + f] = v[i];
-                if (p.dual) p.partial[(base + 1) * p.M + f] = v2[i];
-              }
-            }
+          for (int i = 0; i < 16; ++i) part[(c + i) * kBM + fl] = v[i];
+          if (p.dual) {
+            tmem_ld16(tl + p.BN + c, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) part[(p.BN + c + i) * kBM + fl] = v[i];
           }
         }
         tc_fence_before();
-        mbar_arrive(&tempty_bar[b]);
-        // the last split of this (m, n) tile sums the partials in split order
-        __threadfence();
-        named_bar_sync(1, 128);
-        const int tile_mn = m * p.n_tiles + n;
-        if (et == 0) last_sh = (atomicAdd(&p.counters[tile_mn], 1) == p.k_splits - 1);
-        named_bar_sync(1, 128);
-        if (last_sh) {
-          __threadfence();
-          for (int c = 0; c < p.BN; c += 16) {
-            float v[16], v2[16];
-            sum_partials16(p, 0, f, jt + c, n_rows, v);
-            if (p.dual) sum_partials16(p, 1, f, jt + c, n_rows, v2);
-            tc_epilogue16(p, f, jt + c, v, p.dual ? v2 : nullptr, n_rows, red_sh, ew, et);
+      }
+    }
+  }
+
+  if (clustered) {
+    // every CTA of the cluster has parked its partial (a CTA that gave up on a
+    // wait leaves its partial unwritten; its status bit reports the problem) ...
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 2 && !*abort_flag) {
+      const int fl = (warp & 3) * 32 + lane;
+      TileRef t;
+      if (next_tile(p, 0, t) && t.n * p.BN < n_rows) {
+        const int f = t.m * kBM + fl;
+        const int jt = t.n * p.BN;
+        const uint32_t rank = cluster_ctarank();
+        const uint32_t base = smem_u32(part);
+        for (int j = static_cast<int>(rank); j < p.BN; j += p.k_splits) {
+          if (jt + j >= n_rows) break;
+          float v = 0.f, v2 = 0.f;
+          for (int r = 0; r < p.k_splits; ++r) {
+            v += ld_dsmem_f32(base + static_cast<uint32_t>((j * kBM + fl) * 4), r);
+            if (p.dual)
+              v2 += ld_dsmem_f32(base + static_cast<uint32_t>(((p.BN + j) * kBM + fl) * 4), r);
           }
-          if (et == 0) p.counters[tile_mn] = 0;
+          if (f < p.M) epi_store_elem<bf16>(p.epi, f, jt + j, v, v2);
         }
       }
     }
+    // ... and no CTA leaves while another may still read its shared memory
+    __syncwarp();
+    cluster_sync_all();
   }
 
   tc_fence_before();
@@ -390,74 +439,107 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ------------------------------------------------------------------ host: plan + launch
 
-TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int num_sms, bool allow_split) {
+// How many clusters of `cs` CTAs with `smem` bytes each can be resident at once.
+static int max_active_clusters(int cs, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<int, size_t>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(cs, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(kSmemBudget + 1024));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs * 64);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)gemm_tc_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+
+TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split) {
   TcPlan pl{};
   pl.M = M;
   pl.K = K;
   pl.N_cap = N_cap < 1 ? 1 : N_cap;
   pl.dual = dual;
+  pl.bpair = bpair;
   const int nA = dual ? 2 : 1;
-  const int nt = (pl.N_cap + 255) / 256;
-  int bn = (pl.N_cap + nt - 1) / nt;
-  bn = (bn + 15) / 16 * 16;
-  pl.BN = bn < 16 ? 16 : bn;
-  pl.n_tiles = nt;
+  const int nB = bpair ? 2 : 1;
+  // token tile: at most 256 rows, and narrow enough that three stages fit
+  int nt = (pl.N_cap + 255) / 256;
+  size_t stage_bytes = 0;
+  for (;; ++nt) {
+    int bn = (pl.N_cap + nt - 1) / nt;
+    bn = (bn + 15) / 16 * 16;
+    pl.BN = bn < 16 ? 16 : bn;
+    stage_bytes = static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128 * nB;
+    if (kSmemBudget / stage_bytes >= 3 || pl.BN <= 64) break;
+  }
+  pl.n_tiles = (pl.N_cap + pl.BN - 1) / pl.BN;
   pl.m_tiles = (M + kBM - 1) / kBM;
   pl.num_kb = (K + kBK - 1) / kBK;
-  const int base = pl.m_tiles * pl.n_tiles;
-  int best = 1;
-  if (allow_split && base < num_sms) {
-    // time ~ k-blocks streamed by the busiest SM + the serial part of the split
-    // reduction (about half a k-block per split, four partial loads in flight)
-    double best_cost = 1e30;
-    for (int s = 1; s <= 64; ++s) {
-      const int kbs = (pl.num_kb + s - 1) / s;
-      if (s > 1 && kbs < 4) break;
-      const int ss = (pl.num_kb + kbs - 1) / kbs;
-      const long tiles = static_cast<long>(base) * ss;
-      const long waves = (tiles + num_sms - 1) / num_sms;
-      const double cost = static_cast<double>(waves) * kbs + (ss > 1 ? 2.0 + 0.5 * ss : 0.0);
-      if (cost < best_cost - 1e-9) {
-        best_cost = cost;
-        best = ss;
-      }
-    }
-  }
-  pl.kb_per_split = (pl.num_kb + best - 1) / best;
-  pl.k_splits = (pl.num_kb + pl.kb_per_split - 1) / pl.kb_per_split;
-  const size_t stage_bytes = static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128;
-  const int stages = static_cast<int>((kSmemBudget) / stage_bytes);
+  const int stages = static_cast<int>(kSmemBudget / stage_bytes);
   pl.stages = std::max(2, std::min(kMaxStages, stages));
   pl.smem_bytes = pl.stages * stage_bytes + 1024;
-  pl.acc_bufs = (2 * pl.BN * nA <= 512) ? 2 : 1;
+  const int base = pl.m_tiles * pl.n_tiles;
+  // split K across a cluster when one wave of plain tiles leaves SMs idle: the
+  // splits of a tile must all be resident at once, their partial tile must fit
+  // in the stage ring, and at least 4 k-blocks go to each split
+  int s = 1;
+  if (allow_split && base < num_sms) {
+    s = std::min(kMaxClusterSplits, num_sms / base);
+    s = std::min(s, pl.num_kb / 4);
+    const size_t part_bytes = static_cast<size_t>(nA) * pl.BN * kBM * sizeof(float);
+    if (part_bytes > pl.stages * stage_bytes) s = 1;
+    while (s > 1 && max_active_clusters(s, pl.smem_bytes) * s < base * s) --s;
+    if (s < 2) s = 1;
+  }
+  pl.kb_per_split = (pl.num_kb + s - 1) / s;
+  pl.k_splits = (pl.num_kb + pl.kb_per_split - 1) / pl.kb_per_split;
+  pl.acc_bufs = (pl.k_splits == 1 && 2 * pl.BN * nA <= 512) ? 2 : 1;
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(pl.acc_bufs * pl.BN * nA)) cols <<= 1;
   pl.tmem_cols = static_cast<int>(cols);
-  const long total = static_cast<long>(base) * pl.k_splits;
-  pl.grid = static_cast<int>(std::min<long>(total, num_sms));
-  pl.partial_bytes = 0;
-  if (pl.k_splits > 1) {
-    pl.partial_bytes = static_cast<size_t>(pl.k_splits) * pl.N_cap * nA * M * sizeof(float);
-    pl.partial_bytes = (pl.partial_bytes + 255) / 256 * 256;
-  }
-  pl.n_counters = base;
+  pl.grid = pl.k_splits > 1 ? base * pl.k_splits : std::min(base, num_sms);
   return pl;
 }
 
 int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap* mapA2,
-                   const void* X, const int* n_rows_dev, const Epilogue& epi, float* partial,
-                   int* counters, uint32_t* status, cudaStream_t st) {
+                   const void* X, const void* X_lo, const int* n_rows_dev, const Epilogue& epi,
+                   uint32_t* status, cudaStream_t st) {
   if (pl.dual && !mapA2) return PE_ERR_ARG;
-  if (pl.k_splits > 1 && (!partial || !counters)) return PE_ERR_ARG;
-  CUtensorMap mapB;
+  if (pl.bpair && !X_lo) return PE_ERR_ARG;
+  if (pl.k_splits > 1 && epi.mode == EPI_ARGMAX) return PE_ERR_ARG;
+  CUtensorMap mapB, mapB2;
   if (!encode_tmap_bf16(&mapB, X, static_cast<uint64_t>(pl.N_cap), static_cast<uint64_t>(pl.K),
                         static_cast<uint32_t>(pl.BN)))
     return PE_ERR_CUDA;
+  if (pl.bpair) {
+    if (!encode_tmap_bf16(&mapB2, X_lo, static_cast<uint64_t>(pl.N_cap),
+                          static_cast<uint64_t>(pl.K), static_cast<uint32_t>(pl.BN)))
+      return PE_ERR_CUDA;
+  } else {
+    mapB2 = mapB;
+  }
   TcArgs a{};
   a.M = pl.M;
   a.K = pl.K;
   a.N_cap = pl.N_cap;
   a.dual = pl.dual;
+  a.bpair = pl.bpair;
   a.BN = pl.BN;
   a.n_tiles = pl.n_tiles;
   a.m_tiles = pl.m_tiles;
@@ -470,16 +552,31 @@ int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap*
   a.n_rows_dev = n_rows_dev;
   a.epi = epi;
   a.status = status;
-  a.partial = partial;
-  a.counters = counters;
   // one attribute value (the largest any plan uses) for every launch, so kernels
   // captured into a graph stay launchable whatever order they replay in
   if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemBudget + 1024)) != cudaSuccess)
     return PE_ERR_CUDA;
-  gemm_tc_kernel<<<pl.grid, kTcThreads, pl.smem_bytes, st>>>(*mapA, pl.dual ? *mapA2 : *mapA,
-                                                              mapB, a);
-  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+  cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = pl.smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = pl.k_splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pl.k_splits > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *mapA, pl.dual ? *mapA2 : *mapA, mapB, mapB2, a) ==
+                 cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ fp32 SIMT kernel
@@ -495,6 +592,8 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__
   __shared__ float Ws[kSk][kSt + 1];
   __shared__ float W2s[kSk][kSt + 1];
   __shared__ float Xs[kSk][kSt + 1];
+  pdl_trigger();
+  pdl_wait();
   int n_rows = N_cap;
   if (n_rows_dev) n_rows = min(max(*n_rows_dev, 0), N_cap);
   const int f0 = blockIdx.x * kSt, t0 = blockIdx.y * kSt;
@@ -559,8 +658,10 @@ int launch_gemm_f32(const float* W, const float* W2, const float* X, int M, int 
                     const int* n_rows_dev, const Epilogue& epi, cudaStream_t st) {
   if (N_cap <= 0 || M <= 0) return PE_OK;
   dim3 grid((M + kSt - 1) / kSt, (N_cap + kSt - 1) / kSt);
-  gemm_f32_kernel<<<grid, 256, 0, st>>>(W, W2, X, M, K, N_cap, n_rows_dev, epi);
-  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+  return launch_pdl(gemm_f32_kernel, grid, dim3(256), 0, st, W, W2, X, M, K, N_cap, n_rows_dev,
+                    epi) == cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ tensor maps

@@ -14,18 +14,20 @@ namespace pe {
 // Every drafter projection is D[t][f] = sum_k X[t][k] * W[f][k] (X: token rows,
 // W: [out][in] weight rows); the epilogue decides what is stored.
 enum EpiMode {
-  EPI_STORE = 0,      // out[t][f] = D                       (element type of the step)
-  EPI_STORE_F32 = 1,  // out[t][f] = D                       (float)
-  EPI_RESID = 2,      // out[t][f] = D + resid[t][f]
-  EPI_SWIGLU = 3,     // out[t][f] = silu(D_gate) * D_up     (two weight matrices)
-  EPI_ARGMAX = 4,     // amax[t] = max over f of key(D, f); optional fp32 logits
+  EPI_STORE = 0,        // out[t][f] = D                      (element type of the step)
+  EPI_STORE_F32 = 1,    // out[t][f] = D                      (float)
+  EPI_RESID_F32 = 2,    // out[t][f] = D + resid[t][f]        (float, float residual)
+  EPI_SWIGLU = 3,       // out[t][f] = silu(D_gate) * D_up    (element type of the step)
+  EPI_SWIGLU_PAIR = 4,  // the same product as a bf16 pair: out = hi, out2 = lo
+  EPI_ARGMAX = 5,       // amax[t] = max over f of key(D, f); optional fp32 logits
 };
 
 struct Epilogue {
   int mode = EPI_STORE;
   void* out = nullptr;
+  void* out2 = nullptr;
   int ld_out = 0;
-  const void* resid = nullptr;
+  const float* resid = nullptr;
   int ld_resid = 0;
   unsigned long long* amax = nullptr;
   float* logits = nullptr;
@@ -34,23 +36,23 @@ struct Epilogue {
 
 // ------------------------------------------------------------------ tcgen05 GEMM (bf16)
 struct TcPlan {
-  int M, K, N_cap, dual;
+  int M, K, N_cap, dual, bpair;
   int BN, n_tiles, m_tiles, num_kb, k_splits, kb_per_split, stages, grid, tmem_cols;
   int acc_bufs;  // TMEM accumulator buffers (2 = the next tile's MMA overlaps the epilogue)
   size_t smem_bytes;
-  size_t partial_bytes;  // split-K fp32 partials (0 without split)
-  int n_counters;        // tile counters (m_tiles * n_tiles)
 };
 
-TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int num_sms, bool allow_split);
+// dual: two weight matrices (gate and up) with two accumulators.  bpair: the
+// token rows come as a bf16 pair (hi, lo) whose products add into one accumulator.
+TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split);
 
 // mapA / mapA2: weight tensor maps (box 64 x 128, 128-byte swizzle).  X: token
 // rows [N_cap][K] bf16 (row stride K).  n_rows_dev: live token rows on device
-// (nullable: all N_cap).  partial: plan.partial_bytes of split-K scratch;
-// counters: plan.n_counters ints, zero on entry (left zero on normal exit).
+// (nullable: all N_cap).  A split plan launches clusters of k_splits CTAs and
+// needs no global scratch; EPI_ARGMAX requires an unsplit plan.
 int launch_gemm_tc(const TcPlan& plan, const CUtensorMap* mapA, const CUtensorMap* mapA2,
-                   const void* X, const int* n_rows_dev, const Epilogue& epi, float* partial,
-                   int* counters, uint32_t* status, cudaStream_t st);
+                   const void* X, const void* X_lo, const int* n_rows_dev, const Epilogue& epi,
+                   uint32_t* status, cudaStream_t st);
 
 // ------------------------------------------------------------------ fp32 SIMT GEMM
 int launch_gemm_f32(const float* W, const float* W2, const float* X, int M, int K, int N_cap,

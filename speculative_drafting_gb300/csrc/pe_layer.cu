@@ -1,5 +1,5 @@
-// Row RMSNorm, rotary embedding with the paged KV write, and the argmax
-// finalisation of the drafter layer.
+// Row RMSNorm (fp32 rows in; bf16, bf16-pair or fp32 out), rotary embedding
+// with the paged KV write, and the argmax finalisation of the drafter layer.
 //
 // RoPE is the rotate-half form: the pair (x_i, x_{i+hd/2}) turns by the angle
 // pos * theta^(-2i/hd).  The angle is formed and reduced modulo 2*pi in double
@@ -14,54 +14,68 @@
 
 namespace pe {
 
+// One CTA per row of an fp32 input: y = x * gamma / sqrt(mean(x^2) + eps) (or
+// y = x when apply_norm is 0), stored as any of: the step's element type (out,
+// rounded to nearest), the rest of a bf16 pair (out_lo = bf16(y - out)), and the
+// fp32 value of what was stored (out + out_lo, or y).
 template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const T* __restrict__ x, int ld_x,
-                                                      const T* __restrict__ gamma,
-                                                      T* __restrict__ out, int ld_out, int d,
-                                                      float eps, int rows_cap,
-                                                      const int* n_rows_dev) {
+__global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
   __shared__ float red[32];
-  constexpr int V = Elem<T>::kVec;
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x;
-  int n = rows_cap;
-  if (n_rows_dev) n = min(max(*n_rows_dev, 0), rows_cap);
+  int n = a.rows_cap;
+  if (a.n_rows_dev) n = min(max(*a.n_rows_dev, 0), a.rows_cap);
   if (row >= n) return;
-  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * ld_x);
-  const uint4* gam = reinterpret_cast<const uint4*>(gamma);
-  uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * ld_out);
-  const int vd = d / V;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < vd; i += blockDim.x) {
-    float f[V];
-    unpack16<T>(src[i], f);
-#pragma unroll
-    for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
+  const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(row) * a.ld_x);
+  const int v4 = a.d / 4;
+  float inv = 1.0f;
+  if (a.apply_norm) {
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < v4; i += blockDim.x) {
+      const float4 f = src[i];
+      ss = fmaf(f.x, f.x, ss);
+      ss = fmaf(f.y, f.y, ss);
+      ss = fmaf(f.z, f.z, ss);
+      ss = fmaf(f.w, f.w, ss);
+    }
+    ss = block_sum(ss, red);
+    inv = 1.0f / sqrtf(ss / static_cast<float>(a.d) + a.eps);
   }
-  ss = block_sum(ss, red);
-  const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
-  for (int i = threadIdx.x; i < vd; i += blockDim.x) {
-    float f[V], g[V];
-    unpack16<T>(src[i], f);
-    unpack16<T>(gam[i], g);
+  const T* gam = static_cast<const T*>(a.gamma);
+  T* out = static_cast<T*>(a.out);
+  const size_t ro = static_cast<size_t>(row) * a.ld_out;
+  for (int i = threadIdx.x; i < v4; i += blockDim.x) {
+    const float4 f4 = src[i];
+    const float f[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
-    for (int k = 0; k < V; ++k) f[k] = f[k] * inv * g[k];
-    dst[i] = pack16<T>(f);
+    for (int k = 0; k < 4; ++k) {
+      const int c = 4 * i + k;
+      const float y = a.apply_norm ? f[k] * inv * Elem<T>::to_f(gam[c]) : f[k];
+      float stored = y;
+      if (out) {
+        const T hi = Elem<T>::from_f(y);
+        out[ro + c] = hi;
+        stored = Elem<T>::to_f(hi);
+        if (a.out_lo) {
+          const bf16 lo = __float2bfloat16_rn(y - stored);
+          a.out_lo[ro + c] = lo;
+          stored += __bfloat162float(lo);
+        }
+      }
+      if (a.out_f32) a.out_f32[ro + c] = stored;
+    }
   }
 }
 
-int launch_rmsnorm(const void* x, int ld_x, const void* gamma, void* out, int ld_out, int d,
-                   float eps, int rows_cap, const int* n_rows_dev, int dtype, cudaStream_t st) {
-  if (rows_cap <= 0) return PE_OK;
-  const int threads = d >= 2048 ? 256 : 128;
-  if (dtype == PE_DTYPE_BF16)
-    rmsnorm_kernel<bf16><<<rows_cap, threads, 0, st>>>(
-        static_cast<const bf16*>(x), ld_x, static_cast<const bf16*>(gamma),
-        static_cast<bf16*>(out), ld_out, d, eps, rows_cap, n_rows_dev);
-  else
-    rmsnorm_kernel<float><<<rows_cap, threads, 0, st>>>(
-        static_cast<const float*>(x), ld_x, static_cast<const float*>(gamma),
-        static_cast<float*>(out), ld_out, d, eps, rows_cap, n_rows_dev);
-  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+int launch_rownorm(const RowNormArgs& a, int dtype, cudaStream_t st) {
+  if (a.rows_cap <= 0) return PE_OK;
+  const int threads = a.d >= 2048 ? 256 : 128;
+  const cudaError_t e =
+      dtype == PE_DTYPE_BF16
+          ? launch_pdl(rownorm_kernel<bf16>, dim3(a.rows_cap), dim3(threads), 0, st, a)
+          : launch_pdl(rownorm_kernel<float>, dim3(a.rows_cap), dim3(threads), 0, st, a);
+  return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ RoPE + KV write
@@ -72,6 +86,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
   __shared__ float cs[64], sn[64];
   __shared__ int samp_sh;
+  pdl_trigger();
+  pdl_wait();
   const int v = blockIdx.x;
   const int nv = min(max(*a.n_valid, 0), a.T_out);
   if (v >= nv) return;
@@ -139,27 +155,27 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
     }
   }
   if (s_idx >= 0) {
-    constexpr int V = Elem<T>::kVec;
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) +
-                                                      static_cast<size_t>(v) * a.d);
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.x_s) + static_cast<size_t>(s_idx) * a.d);
-    for (int i = threadIdx.x; i < a.d / V; i += blockDim.x) dst[i] = src[i];
+    // the fc output of the sample rows is the attention residual (fp32)
+    const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(v) * a.d);
+    float4* dst = reinterpret_cast<float4*>(a.x_s + static_cast<size_t>(s_idx) * a.d);
+    for (int i = threadIdx.x; i < a.d / 4; i += blockDim.x) dst[i] = src[i];
   }
 }
 
 int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st) {
   if (a.T_out <= 0) return PE_OK;
-  if (dtype == PE_DTYPE_BF16)
-    rope_kv_kernel<bf16><<<a.T_out, 256, 0, st>>>(a);
-  else
-    rope_kv_kernel<float><<<a.T_out, 256, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+  const cudaError_t e =
+      dtype == PE_DTYPE_BF16 ? launch_pdl(rope_kv_kernel<bf16>, dim3(a.T_out), dim3(256), 0, st, a)
+                             : launch_pdl(rope_kv_kernel<float>, dim3(a.T_out), dim3(256), 0, st, a);
+  return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ argmax keys -> ids
 
 __global__ void argmax_finalize_kernel(const unsigned long long* __restrict__ keys, int n,
                                        int32_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const unsigned long long k = keys[i];
@@ -168,8 +184,10 @@ __global__ void argmax_finalize_kernel(const unsigned long long* __restrict__ ke
 
 int launch_argmax_finalize(const unsigned long long* keys, int n, int32_t* out, cudaStream_t st) {
   if (n <= 0) return PE_OK;
-  argmax_finalize_kernel<<<(n + 255) / 256, 256, 0, st>>>(keys, n, out);
-  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+  return launch_pdl(argmax_finalize_kernel, dim3((n + 255) / 256), dim3(256), 0, st, keys, n, out) ==
+                 cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
 }
 
 }  // namespace pe

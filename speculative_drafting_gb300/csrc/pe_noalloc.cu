@@ -68,8 +68,8 @@ extern "C" int pe_argmax_noalloc(pe_handle* h, const void* z, int n_rows, int32_
   e.ld_logits = d.vocab;
   if (d.dtype == PE_DTYPE_BF16) {
     // no split over K: a split would need partial sums the array does not hold
-    const TcPlan p = plan_gemm_tc(d.vocab, d.d, n_rows, 0, handle_num_sms(h), false);
-    rc = launch_gemm_tc(p, handle_lm_map(h), nullptr, z, nullptr, e, nullptr, nullptr, nullptr, st);
+    const TcPlan p = plan_gemm_tc(d.vocab, d.d, n_rows, 0, 0, handle_num_sms(h), false);
+    rc = launch_gemm_tc(p, handle_lm_map(h), nullptr, z, nullptr, nullptr, e, nullptr, st);
   } else {
     rc = launch_gemm_f32(static_cast<const float*>(handle_w_lm(h)), nullptr,
                          static_cast<const float*>(z), d.vocab, d.d, n_rows, nullptr, e, st);

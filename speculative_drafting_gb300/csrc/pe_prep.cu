@@ -64,9 +64,12 @@ __global__ void __launch_bounds__(1024) meta_kernel(const MetaArgs a) {
   __shared__ int carry_o, carry_v;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nw = blockDim.x >> 5;
+  pdl_trigger();
+  pdl_wait();
   if (tid == 0) {
     carry_o = 0;
     carry_v = 0;
+    if (a.status) *a.status = 0;  // a step starts with a clean status word
   }
   __syncthreads();
   for (int base = 0; base < a.B; base += blockDim.x) {
@@ -223,8 +226,8 @@ int launch_meta(const MetaLaunch& L, cudaStream_t st) {
   int threads = 32;
   while (threads < L.B && threads < 1024) threads <<= 1;
   if (threads < 128) threads = 128;
-  meta_kernel<<<1, threads, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+  return launch_pdl(meta_kernel, dim3(1), dim3(threads), 0, st, a) == cudaSuccess ? PE_OK
+                                                                                : PE_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ (2) hidden-state map
@@ -233,6 +236,8 @@ int launch_meta(const MetaLaunch& L, cudaStream_t st) {
 // emb_mask.  Grid-stride over 16-byte vectors; 4 loads in flight per thread.
 template <typename T>
 __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int V = Elem<T>::kVec;
   const int vd = a.d / V;             // vectors per stream row
   const long nG = a.G ? static_cast<long>(a.T_out) * 3 * vd : 0;
@@ -304,6 +309,8 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
 template <typename T>
 __global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   constexpr int V = Elem<T>::kVec;
   const int v = blockIdx.x, seg = blockIdx.y;
   const int nv = min(max(*a.n_valid, 0), a.T_out);
@@ -368,8 +375,10 @@ int launch_gather_t(const GatherArgs& a, int num_sms, cudaStream_t st) {
   if (total == 0) return PE_OK;
   long blocks = (total + 4L * 256 - 1) / (4L * 256);
   blocks = blocks < 4L * num_sms ? blocks : 4L * num_sms;
-  gather_kernel<T><<<static_cast<int>(blocks), 256, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+  return launch_pdl(gather_kernel<T>, dim3(static_cast<int>(blocks)), dim3(256), 0, st, a) ==
+                 cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
 }
 
 int launch_gather(const GatherArgs& a, int dtype, int num_sms, cudaStream_t st) {
@@ -380,11 +389,10 @@ int launch_gather(const GatherArgs& a, int dtype, int num_sms, cudaStream_t st) 
 int launch_input(const InputArgs& a, int dtype, cudaStream_t st) {
   if (a.T_out <= 0) return PE_OK;
   dim3 grid(a.T_out, 4);
-  if (dtype == PE_DTYPE_BF16)
-    input_kernel<bf16><<<grid, 128, 0, st>>>(a);
-  else
-    input_kernel<float><<<grid, 128, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+  const cudaError_t e = dtype == PE_DTYPE_BF16
+                            ? launch_pdl(input_kernel<bf16>, grid, dim3(128), 0, st, a)
+                            : launch_pdl(input_kernel<float>, grid, dim3(128), 0, st, a);
+  return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 
 }  // namespace pe

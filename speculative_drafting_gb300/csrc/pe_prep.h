@@ -1,9 +1,13 @@
 // Launch interfaces of the non-GEMM kernels (host side).
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "pe_internal.h"
 
 namespace pe {
+
+typedef __nv_bfloat16 bf16_t;
 
 // ---------------------------------------------------------------- (1) metadata
 struct MetaLaunch {
@@ -55,15 +59,29 @@ struct InputArgs {
 int launch_input(const InputArgs& a, int dtype, cudaStream_t st);
 
 // ---------------------------------------------------------------- row RMSNorm
-// out[i] = x[i] * gamma / sqrt(mean(x[i]^2) + eps) for rows i < n_rows.
-int launch_rmsnorm(const void* x, int ld_x, const void* gamma, void* out, int ld_out, int d,
-                   float eps, int rows_cap, const int* n_rows_dev, int dtype, cudaStream_t st);
+// y[i] = x[i] * gamma / sqrt(mean(x[i]^2) + eps) (apply_norm) or x[i], for rows
+// i < n_rows of an fp32 input, stored as: out (step dtype), out_lo (bf16 rest of
+// a pair, nullable), out_f32 (fp32 value of what was stored, nullable).
+struct RowNormArgs {
+  const float* x;
+  int ld_x;
+  const void* gamma;
+  int apply_norm;
+  void* out;
+  bf16_t* out_lo;
+  float* out_f32;
+  int ld_out, d;
+  float eps;
+  int rows_cap;
+  const int* n_rows_dev;
+};
+int launch_rownorm(const RowNormArgs& a, int dtype, cudaStream_t st);
 
 // ---------------------------------------------------------------- RoPE + KV write
 struct RopeArgs {
   int T_out, B, K, H, G, hd, d, bs, num_blocks;
   const float* qkv;  // [T_out][(H+2G)hd] fp32, non-rejected rows in valid_rows order
-  const void* x;     // [T_out][d] fc output (same order)
+  const float* x;    // [T_out][d] fc output, fp32 (same order)
   const int32_t* n_valid;
   const int32_t* valid_rows;
   const int32_t* valid_qsl;
@@ -71,8 +89,8 @@ struct RopeArgs {
   const int64_t* slot;
   void* k_cache;
   void* v_cache;
-  void* q_s;  // [B*K][H][hd] queries of the sample rows
-  void* x_s;  // [B*K][d] fc output of the sample rows (residual)
+  void* q_s;    // [B*K][H][hd] queries of the sample rows
+  float* x_s;  // [B*K][d] fc output of the sample rows (residual, fp32)
   double inv_freq[64];
   uint32_t* status;
 };

@@ -67,6 +67,7 @@ def check_logits_and_draft(dtype, got_logits, got_draft, ref_logits, where=""):
     """Logit tolerance, then argmax agreement outside the tie window."""
     tol = LOGIT_TOL[dtype]
     diff = np.abs(got_logits.astype(np.float64) - ref_logits)
+    print(f"[parity] {where}: logits max-abs {diff.max():.3g} (tolerance {tol})")
     assert diff.max() <= tol, f"{where} logits max-abs {diff.max():.3g} > {tol}"
     top2 = np.sort(ref_logits, axis=-1)[:, -2:]
     gap = top2[:, 1] - top2[:, 0]

@@ -250,8 +250,11 @@ def test_bf16_mode_stores_bf16_values_and_tracks_fp64():
                          O.bf16_decode(vc).astype(np.float32))
     for r in range(wl.batch):
         rr = res["req"][r]
-        for key in ("A", "x", "u", "k", "v", "q", "attn", "a", "z"):
+        for key in ("A", "k", "v", "q", "attn", "z"):
             assert np.array_equal(O.bf16_round(rr[key]), rr[key]), key
+        # the projection operands are bf16 pairs: not bf16 values, but pair values
+        assert not np.array_equal(O.bf16_round(rr["u"]), rr["u"])
+        assert np.array_equal(O.bf16_pair_round(rr["u"]), rr["u"])
         diff = np.abs(rr["logits"] - res64["req"][r]["logits"]).max()
         assert diff < 0.05, diff
 
