@@ -47,11 +47,9 @@ GemmShape gemm_shape(const pe_handle* h, int id) {
   }
 }
 
-// The LM head never splits K: its argmax epilogue needs whole sums, and its
-// vocabulary gives plenty of tiles.
 TcPlan plan_of(const pe_handle* h, int id, int N, bool bpair) {
   const GemmShape s = gemm_shape(h, id);
-  return plan_gemm_tc(s.M, s.K, N, s.dual, bpair ? 1 : 0, h->num_sms, id != G_LM);
+  return plan_gemm_tc(s.M, s.K, N, s.dual, bpair ? 1 : 0, h->num_sms, true);
 }
 
 // Attention split partials, bounded over every batch size <= B (the split count
@@ -60,13 +58,11 @@ size_t attn_scratch_bound(const pe_handle* h, int B, int max_blocks) {
   if (!is_bf16(h)) return 0;
   const pe_dims& d = h->d;
   size_t best = 0;
-  const long Lmax = static_cast<long>(max_blocks) * d.block_size;
-  const long chunks = std::max<long>(1, (Lmax + 63) / 64);
+  // the split count only grows with the block-table width, so the width given
+  // bounds every narrower call; the batch size is walked
   for (int b = 1; b <= B; ++b) {
-    const long heads = static_cast<long>(b) * d.n_kv_heads;
-    long ns = (2L * h->num_sms + heads - 1) / heads;
-    ns = std::max<long>(1, std::min(std::min(ns, chunks), 128L));
-    best = std::max(best, attention_scratch_bytes(b, d.K, d.n_heads, d.head_dim, static_cast<int>(ns)));
+    const int ns = attention_split_count(b, d.n_kv_heads, max_blocks, d.block_size, h->num_sms);
+    best = std::max(best, attention_scratch_bytes(b, d.K, d.n_heads, d.head_dim, ns));
   }
   return best;
 }
@@ -266,7 +262,8 @@ int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl, const i
     return PE_ERR_ARG;
   const pe_dims& d = h->d;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint32_t* status = at<uint32_t>(ws, 0);  // cleared by the metadata kernel
+  uint32_t* status = at<uint32_t>(ws, 0);
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return PE_ERR_CUDA;
   MetaLaunch ml;
   ml.B = B;
   ml.T_in = T_in;

@@ -20,13 +20,20 @@
 
 namespace pe {
 
-constexpr int kKC = 64;      // keys per chunk
-constexpr int kStages = 3;   // cp.async ring depth
+constexpr int kKC = 64;  // keys per chunk
+// cp.async ring depth: three chunks for hd 64; two for hd 128, whose 32 KB
+// chunks would otherwise hold an SM to two CTAs
+template <int HD>
+__host__ __device__ constexpr int ring_stages() {
+  return HD >= 128 ? 2 : 3;
+}
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxSplits = 128;  // key splits per (request, KV head)
+constexpr int kMaxSplits = 128;       // key splits per (request, KV head)
+constexpr long kMaxSplitKeys = 2048;  // keys per split, at most
 
 template <int HD>
 __global__ void __launch_bounds__(256) attn_mma_kernel(const AttnArgs a) {
+  constexpr int kStages = ring_stages<HD>();
   constexpr int ROWB = HD * 2;       // bytes per key row in shared memory
   constexpr int CH = HD / 8;         // 16-byte chunks per key row
   constexpr int TILE = kKC * ROWB;   // one K or V chunk
@@ -283,9 +290,17 @@ __global__ void attn_combine_kernel(const AttnArgs a) {
   __syncthreads();
   const float inv = inv_sh;
   for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < a.n_splits; ++j) acc += w_sh[j] * a.part_o[(j * n_sh + sh) * a.hd + d];
-    static_cast<T*>(a.out)[sh * a.hd + d] = Elem<T>::from_f(acc * inv);
+    // eight independent accumulators keep eight split loads in flight
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int j = 0;
+    for (; j + 8 <= a.n_splits; j += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        acc[u] += w_sh[j + u] * a.part_o[((j + u) * n_sh + sh) * a.hd + d];
+    }
+    for (; j < a.n_splits; ++j) acc[0] += w_sh[j] * a.part_o[(j * n_sh + sh) * a.hd + d];
+    const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    static_cast<T*>(a.out)[sh * a.hd + d] = Elem<T>::from_f(sum * inv);
   }
 }
 
@@ -356,6 +371,19 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
   }
 }
 
+// Key splits per (request, KV head): enough CTAs for two per SM, and no split
+// longer than kMaxSplitKeys keys (long contexts of a large batch would
+// otherwise leave a few CTAs streaming the longest contexts alone).
+int attention_split_count(int B, int G, int max_blocks, int bs, int num_sms) {
+  const long Lmax = static_cast<long>(max_blocks) * bs;
+  const long chunks = std::max<long>(1, (Lmax + kKC - 1) / kKC);
+  const long heads = std::max<long>(1, static_cast<long>(B) * G);
+  long ns = (2L * std::max(num_sms, 1) + heads - 1) / heads;
+  ns = std::max(ns, (Lmax + kMaxSplitKeys - 1) / kMaxSplitKeys);
+  ns = std::max<long>(1, std::min(std::min(ns, chunks), static_cast<long>(kMaxSplits)));
+  return static_cast<int>(ns);
+}
+
 void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, int num_sms,
                     int& n_splits, int& split_len) {
   (void)K;
@@ -363,10 +391,7 @@ void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, 
   (void)hd;
   const long Lmax = static_cast<long>(max_blocks) * bs;
   const long chunks = std::max<long>(1, (Lmax + kKC - 1) / kKC);
-  const long target = 2L * std::max(num_sms, 1);
-  const long heads = std::max<long>(1, static_cast<long>(B) * G);
-  long ns = (target + heads - 1) / heads;
-  ns = std::max<long>(1, std::min(std::min(ns, chunks), static_cast<long>(kMaxSplits)));
+  const long ns = attention_split_count(B, G, max_blocks, bs, num_sms);
   const long chunks_per = (chunks + ns - 1) / ns;
   split_len = static_cast<int>(chunks_per * kKC);
   n_splits = static_cast<int>((Lmax + split_len - 1) / split_len);
@@ -392,9 +417,10 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
   const int rows = a.K * (a.H / a.G);
   const int warps = (rows + 15) / 16;
   const dim3 grid(a.n_splits, a.G, a.B);
-  const size_t smem = static_cast<size_t>(kStages) * 2 * kKC * a.hd * 2;
-  // one attribute value for every launch (the largest head size's ring)
-  const int smem_max = kStages * 2 * kKC * 128 * 2;
+  const int stages = a.hd >= 128 ? ring_stages<128>() : ring_stages<64>();
+  const size_t smem = static_cast<size_t>(stages) * 2 * kKC * a.hd * 2;
+  // one attribute value for every launch (the largest ring)
+  const int smem_max = 3 * 2 * kKC * 128 * 2;
   if (a.hd == 64) {
     cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (launch_pdl(attn_mma_kernel<64>, grid, dim3(warps * 32), smem, st, a) != cudaSuccess)

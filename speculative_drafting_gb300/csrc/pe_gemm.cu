@@ -30,12 +30,19 @@ constexpr int kMaxStages = 12;
 constexpr size_t kSmemBudget = 212 * 1024;  // dynamic shared memory for the stage ring
 constexpr int kPrefetchKb = 16;             // k-blocks of weights pulled into L2 early
 constexpr int kMaxClusterSplits = 8;        // portable cluster size
+// Narrow token tiles stream weights: two 64-element K atoms per stage put the
+// two 128-byte halves of each weight row's 256 bytes on the bus back to back
+// (measured: LM head at B=1 259 us instead of 303 us).  Wide tiles keep one atom
+// so that enough stages stay in flight.
+constexpr int kNarrowBN = 64;
 constexpr int kTcThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;
 
 struct TcArgs {
   int M, K, N_cap, dual, bpair;
+  int tile_base, tile_count;  // the (m, n) tiles of this launch
   int BN, n_tiles, m_tiles, k_splits, kb_per_split, num_kb, stages, acc_bufs;
+  int atoms;  // 64-element K atoms per stage (a k-block is atoms * 64 elements)
   uint32_t tmem_cols;
   const int* n_rows_dev;
   Epilogue epi;
@@ -138,14 +145,17 @@ struct TileRef {
 PE_DEV bool next_tile(const TcArgs& p, int it, TileRef& t) {
   if (p.k_splits > 1) {
     if (it > 0) return false;
-    const int tile = blockIdx.x / p.k_splits;
+    const int local = blockIdx.x / p.k_splits;
+    if (local >= p.tile_count) return false;
+    const int tile = p.tile_base + local;
     t.ks = blockIdx.x % p.k_splits;
     t.n = tile % p.n_tiles;
     t.m = tile / p.n_tiles;
     return t.m < p.m_tiles;
   }
-  const int tile = blockIdx.x + it * gridDim.x;
-  if (tile >= p.m_tiles * p.n_tiles) return false;
+  const int local = blockIdx.x + it * gridDim.x;
+  if (local >= p.tile_count) return false;
+  const int tile = p.tile_base + local;
   t.ks = 0;
   t.n = tile % p.n_tiles;
   t.m = tile / p.n_tiles;
@@ -171,7 +181,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nA = p.dual ? 2 : 1;
   const int nB = p.bpair ? 2 : 1;
   const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * 128u;
-  const uint32_t stage_bytes = kABytes * nA + b_bytes * nB;
+  const uint32_t atom_bytes = kABytes * nA + b_bytes * nB;
+  const uint32_t stage_bytes = atom_bytes * p.atoms;
+  const int kbk = kBK * p.atoms;  // elements of K per k-block
   const int nbuf = p.acc_bufs;
   const uint32_t buf_cols = static_cast<uint32_t>(p.BN * nA);
   const bool clustered = p.k_splits > 1;
@@ -199,11 +211,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     TileRef t;
     if (next_tile(p, 0, t)) {
       const int kb0 = t.ks * p.kb_per_split;
-      const int kb1 = min(min(p.num_kb, kb0 + p.kb_per_split), kb0 + kPrefetchKb);
-      for (int kb = kb0; kb < kb1; ++kb) {
-        tma_prefetch_l2_2d(&mapA, kb * kBK, t.m * kBM);
-        if (p.dual) tma_prefetch_l2_2d(&mapA2, kb * kBK, t.m * kBM);
-      }
+      const int kb1 = min(min(p.num_kb, kb0 + p.kb_per_split), kb0 + kPrefetchKb / p.atoms);
+      for (int kb = kb0; kb < kb1; ++kb)
+        for (int at = 0; at < p.atoms; ++at) {
+          tma_prefetch_l2_2d(&mapA, kb * kbk + at * kBK, t.m * kBM);
+          if (p.dual) tma_prefetch_l2_2d(&mapA2, kb * kbk + at * kBK, t.m * kBM);
+        }
     }
   }
   if (warp == 1) {
@@ -254,15 +267,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             fail();
             break;
           }
-          uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes;
           mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
-          tma_load_2d(sa, &mapA, &full_bar[stage], kb * kBK, t.m * kBM, pol_w);
-          if (p.dual)
-            tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], kb * kBK, t.m * kBM, pol_w);
-          tma_load_2d(sa + kABytes * nA, &mapB, &full_bar[stage], kb * kBK, t.n * p.BN, pol_x);
-          if (p.bpair)
-            tma_load_2d(sa + kABytes * nA + b_bytes, &mapB2, &full_bar[stage], kb * kBK,
-                        t.n * p.BN, pol_x);
+          // the atoms of one row follow each other in memory: their boxes go out
+          // back to back, A first (the weights dominate the traffic)
+          for (int at = 0; at < p.atoms; ++at) {
+            uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes;
+            const int x = kb * kbk + at * kBK;
+            tma_load_2d(sa, &mapA, &full_bar[stage], x, t.m * kBM, pol_w);
+            if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], x, t.m * kBM, pol_w);
+          }
+          for (int at = 0; at < p.atoms; ++at) {
+            uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes;
+            const int x = kb * kbk + at * kBK;
+            tma_load_2d(sa + kABytes * nA, &mapB, &full_bar[stage], x, t.n * p.BN, pol_x);
+            if (p.bpair)
+              tma_load_2d(sa + kABytes * nA + b_bytes, &mapB2, &full_bar[stage], x, t.n * p.BN,
+                          pol_x);
+          }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == p.stages) {
@@ -307,7 +328,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
+          for (int at = 0; at < p.atoms; ++at) {
+          const uint32_t sa =
+              smem_u32(smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes);
           const uint64_t adesc = sw128_kmajor_desc(sa);
           const uint64_t a2desc = sw128_kmajor_desc(sa + kABytes);
           const uint64_t bdesc = sw128_kmajor_desc(sa + kABytes * nA);
@@ -315,7 +338,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // advance 16 elements (32 bytes) along K inside the swizzle row
-            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+            const uint32_t acc = (kb > kb0 || at > 0 || kk > 0) ? 1u : 0u;
             umma_bf16(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, acc);
             if (p.bpair) umma_bf16(d0, adesc + 2 * kk, b2desc + 2 * kk, idesc, 1u);
             if (p.dual) {
@@ -323,6 +346,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               umma_bf16(d1, a2desc + 2 * kk, bdesc + 2 * kk, idesc, acc);
               if (p.bpair) umma_bf16(d1, a2desc + 2 * kk, b2desc + 2 * kk, idesc, 1u);
             }
+          }
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == p.stages) {
@@ -411,15 +435,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int jt = t.n * p.BN;
         const uint32_t rank = cluster_ctarank();
         const uint32_t base = smem_u32(part);
+        const int ew = warp - 2, et = threadIdx.x - 64;
         for (int j = static_cast<int>(rank); j < p.BN; j += p.k_splits) {
-          if (jt + j >= n_rows) break;
+          if (jt + j >= n_rows) break;  // uniform over the epilogue warps
           float v = 0.f, v2 = 0.f;
           for (int r = 0; r < p.k_splits; ++r) {
             v += ld_dsmem_f32(base + static_cast<uint32_t>((j * kBM + fl) * 4), r);
             if (p.dual)
               v2 += ld_dsmem_f32(base + static_cast<uint32_t>(((p.BN + j) * kBM + fl) * 4), r);
           }
-          if (f < p.M) epi_store_elem<bf16>(p.epi, f, jt + j, v, v2);
+          if (p.epi.mode == EPI_ARGMAX) {
+            // max over this tile's 128 features of token jt + j
+            if (p.epi.logits && f < p.M)
+              p.epi.logits[static_cast<size_t>(jt + j) * p.epi.ld_logits + f] = v;
+            const unsigned long long k = warp_max_u64(f < p.M ? argmax_key(v, f) : 0ull);
+            if (lane == 0) red_sh[ew][0] = k;
+            named_bar_sync(1, 128);
+            if (et == 0) {
+              unsigned long long kk = red_sh[0][0];
+              for (int w2 = 1; w2 < 4; ++w2) kk = red_sh[w2][0] > kk ? red_sh[w2][0] : kk;
+              if (kk) atomicMax(&p.epi.amax[jt + j], kk);
+            }
+            named_bar_sync(1, 128);
+          } else if (f < p.M) {
+            epi_store_elem<bf16>(p.epi, f, jt + j, v, v2);
+          }
         }
       }
     }
@@ -485,12 +525,14 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
     int bn = (pl.N_cap + nt - 1) / nt;
     bn = (bn + 15) / 16 * 16;
     pl.BN = bn < 16 ? 16 : bn;
-    stage_bytes = static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128 * nB;
+    pl.atoms = pl.BN <= kNarrowBN ? 2 : 1;
+    stage_bytes = (static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128 * nB) *
+                  pl.atoms;
     if (kSmemBudget / stage_bytes >= 3 || pl.BN <= 64) break;
   }
   pl.n_tiles = (pl.N_cap + pl.BN - 1) / pl.BN;
   pl.m_tiles = (M + kBM - 1) / kBM;
-  pl.num_kb = (K + kBK - 1) / kBK;
+  pl.num_kb = (K + kBK * pl.atoms - 1) / (kBK * pl.atoms);
   const int stages = static_cast<int>(kSmemBudget / stage_bytes);
   pl.stages = std::max(2, std::min(kMaxStages, stages));
   pl.smem_bytes = pl.stages * stage_bytes + 1024;
@@ -501,7 +543,7 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   int s = 1;
   if (allow_split && base < num_sms) {
     s = std::min(kMaxClusterSplits, num_sms / base);
-    s = std::min(s, pl.num_kb / 4);
+    s = std::min(s, pl.num_kb * pl.atoms / 4);
     const size_t part_bytes = static_cast<size_t>(nA) * pl.BN * kBM * sizeof(float);
     if (part_bytes > pl.stages * stage_bytes) s = 1;
     while (s > 1 && max_active_clusters(s, pl.smem_bytes) * s < base * s) --s;
@@ -514,7 +556,73 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   while (cols < static_cast<uint32_t>(pl.acc_bufs * pl.BN * nA)) cols <<= 1;
   pl.tmem_cols = static_cast<int>(cols);
   pl.grid = pl.k_splits > 1 ? base * pl.k_splits : std::min(base, num_sms);
+  pl.main_tiles = base;
+  pl.tail_splits = 1;
+  pl.tail_kb_per_split = pl.num_kb;
+  if (pl.k_splits == 1 && base > num_sms) {
+    // Several rounds of persistent tiles: a partial last round leaves SMs idle
+    // while a few CTAs finish one more tile.  Run the full rounds persistent and
+    // the remaining tiles as clusters that split them over K.
+    const int rem = base % num_sms;
+    int ts = rem ? std::min(kMaxClusterSplits, num_sms / rem) : 1;
+    ts = std::min(ts, pl.num_kb * pl.atoms / 4);
+    const size_t part_bytes = static_cast<size_t>(nA) * pl.BN * kBM * sizeof(float);
+    if (part_bytes > pl.stages * stage_bytes) ts = 1;
+    while (ts > 1 && max_active_clusters(ts, pl.smem_bytes) < rem) --ts;
+    if (ts >= 2) {
+      pl.main_tiles = base - rem;
+      pl.tail_kb_per_split = (pl.num_kb + ts - 1) / ts;
+      pl.tail_splits = (pl.num_kb + pl.tail_kb_per_split - 1) / pl.tail_kb_per_split;
+    }
+  }
   return pl;
+}
+
+// One launch over tiles [tile_base, tile_base + tile_count) with k_splits splits
+// of kb_per_split k-blocks each (k_splits > 1: clusters of k_splits CTAs).
+static int launch_one(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap* mapA2,
+                      const CUtensorMap& mapB, const CUtensorMap& mapB2, const int* n_rows_dev,
+                      const Epilogue& epi, uint32_t* status, cudaStream_t st, int tile_base,
+                      int tile_count, int k_splits, int kb_per_split, int grid) {
+  TcArgs a{};
+  a.M = pl.M;
+  a.K = pl.K;
+  a.N_cap = pl.N_cap;
+  a.dual = pl.dual;
+  a.bpair = pl.bpair;
+  a.tile_base = tile_base;
+  a.tile_count = tile_count;
+  a.BN = pl.BN;
+  a.n_tiles = pl.n_tiles;
+  a.m_tiles = pl.m_tiles;
+  a.k_splits = k_splits;
+  a.kb_per_split = kb_per_split;
+  a.num_kb = pl.num_kb;
+  a.atoms = pl.atoms;
+  a.stages = pl.stages;
+  a.acc_bufs = k_splits == 1 ? pl.acc_bufs : 1;
+  a.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
+  a.n_rows_dev = n_rows_dev;
+  a.epi = epi;
+  a.status = status;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = pl.smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = k_splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = k_splits > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *mapA, pl.dual ? *mapA2 : *mapA, mapB, mapB2, a) ==
+                 cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
 }
 
 int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap* mapA2,
@@ -522,7 +630,6 @@ int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap*
                    uint32_t* status, cudaStream_t st) {
   if (pl.dual && !mapA2) return PE_ERR_ARG;
   if (pl.bpair && !X_lo) return PE_ERR_ARG;
-  if (pl.k_splits > 1 && epi.mode == EPI_ARGMAX) return PE_ERR_ARG;
   CUtensorMap mapB, mapB2;
   if (!encode_tmap_bf16(&mapB, X, static_cast<uint64_t>(pl.N_cap), static_cast<uint64_t>(pl.K),
                         static_cast<uint32_t>(pl.BN)))
@@ -534,24 +641,6 @@ int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap*
   } else {
     mapB2 = mapB;
   }
-  TcArgs a{};
-  a.M = pl.M;
-  a.K = pl.K;
-  a.N_cap = pl.N_cap;
-  a.dual = pl.dual;
-  a.bpair = pl.bpair;
-  a.BN = pl.BN;
-  a.n_tiles = pl.n_tiles;
-  a.m_tiles = pl.m_tiles;
-  a.k_splits = pl.k_splits;
-  a.kb_per_split = pl.kb_per_split;
-  a.num_kb = pl.num_kb;
-  a.stages = pl.stages;
-  a.acc_bufs = pl.acc_bufs;
-  a.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
-  a.n_rows_dev = n_rows_dev;
-  a.epi = epi;
-  a.status = status;
   // one attribute value (the largest any plan uses) for every launch, so kernels
   // captured into a graph stay launchable whatever order they replay in
   if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -559,24 +648,16 @@ int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap*
     return PE_ERR_CUDA;
   cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                        cudaSharedmemCarveoutMaxShared);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.grid);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = pl.smem_bytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = pl.k_splits;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pl.k_splits > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *mapA, pl.dual ? *mapA2 : *mapA, mapB, mapB2, a) ==
-                 cudaSuccess
-             ? PE_OK
-             : PE_ERR_CUDA;
+  const int base = pl.m_tiles * pl.n_tiles;
+  if (pl.k_splits > 1)
+    return launch_one(pl, mapA, mapA2, mapB, mapB2, n_rows_dev, epi, status, st, 0, base,
+                      pl.k_splits, pl.kb_per_split, pl.grid);
+  int rc = launch_one(pl, mapA, mapA2, mapB, mapB2, n_rows_dev, epi, status, st, 0, pl.main_tiles,
+                      1, pl.num_kb, std::min(pl.main_tiles, pl.grid));
+  if (rc != PE_OK || pl.main_tiles == base) return rc;
+  const int tail = base - pl.main_tiles;
+  return launch_one(pl, mapA, mapA2, mapB, mapB2, n_rows_dev, epi, status, st, pl.main_tiles, tail,
+                    pl.tail_splits, pl.tail_kb_per_split, tail * pl.tail_splits);
 }
 
 // ------------------------------------------------------------------ fp32 SIMT kernel

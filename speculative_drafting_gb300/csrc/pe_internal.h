@@ -38,8 +38,12 @@ struct Epilogue {
 struct TcPlan {
   int M, K, N_cap, dual, bpair;
   int BN, n_tiles, m_tiles, num_kb, k_splits, kb_per_split, stages, grid, tmem_cols;
+  int atoms;  // 64-element K atoms per stage
   int acc_bufs;  // TMEM accumulator buffers (2 = the next tile's MMA overlaps the epilogue)
   size_t smem_bytes;
+  // unsplit plans with several rounds of tiles: the first main_tiles run
+  // persistent, the rest as clusters of tail_splits CTAs splitting K
+  int main_tiles, tail_splits, tail_kb_per_split;
 };
 
 // dual: two weight matrices (gate and up) with two accumulators.  bpair: the
@@ -49,7 +53,7 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
 // mapA / mapA2: weight tensor maps (box 64 x 128, 128-byte swizzle).  X: token
 // rows [N_cap][K] bf16 (row stride K).  n_rows_dev: live token rows on device
 // (nullable: all N_cap).  A split plan launches clusters of k_splits CTAs and
-// needs no global scratch; EPI_ARGMAX requires an unsplit plan.
+// needs no global scratch.
 int launch_gemm_tc(const TcPlan& plan, const CUtensorMap* mapA, const CUtensorMap* mapA2,
                    const void* X, const void* X_lo, const int* n_rows_dev, const Epilogue& epi,
                    uint32_t* status, cudaStream_t st);

@@ -56,20 +56,22 @@ PE_DEV int64_t slot_of(const MetaArgs& a, int r, int64_t p) {
   return static_cast<int64_t>(blk) * a.bs + p % a.bs;
 }
 
-// One CTA.  Pass 1: exclusive block scans (warp shuffles + one shared-memory
-// level) of n_r + K - 1 (output rows) and a_r + K (non-rejected rows) over the
-// requests.  Pass 2: one warp per request writes its rows.
-__global__ void __launch_bounds__(1024) meta_kernel(const MetaArgs a) {
+// Pass 1 (every CTA): exclusive block scans (warp shuffles + one shared-memory
+// level) of n_r + K - 1 (output rows) and a_r + K (non-rejected rows) over all
+// requests; the requests are few, so each CTA redoes the scan instead of
+// waiting for another CTA.  Pass 2: CTA c writes the rows of requests
+// [c*R, (c+1)*R), one warp per request (R = warps per CTA).
+__global__ void __launch_bounds__(256) meta_kernel(const MetaArgs a) {
   __shared__ int wsum_o[32], wsum_v[32];
   __shared__ int carry_o, carry_v;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nw = blockDim.x >> 5;
+  const int r_begin = blockIdx.x * nw, r_end = min(a.B, r_begin + nw);
   pdl_trigger();
   pdl_wait();
   if (tid == 0) {
     carry_o = 0;
     carry_v = 0;
-    if (a.status) *a.status = 0;  // a step starts with a clean status word
   }
   __syncthreads();
   for (int base = 0; base < a.B; base += blockDim.x) {
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(1024) meta_kernel(const MetaArgs a) {
       int n, acc;
       bool bad;
       request_counts(a, r, n, acc, bad);
-      if (bad) set_status(a.status, PE_ST_ACCEPTED_RANGE);
+      if (bad && r >= r_begin && r < r_end) set_status(a.status, PE_ST_ACCEPTED_RANGE);
       lo = n + a.K - 1;
       lv = (n >= 1 ? acc + 1 : 0) + a.K - 1;
     }
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(1024) meta_kernel(const MetaArgs a) {
     __syncthreads();
     const int pre_o = carry_o + (warp ? wsum_o[warp - 1] : 0) + xo - lo;
     const int pre_v = carry_v + (warp ? wsum_v[warp - 1] : 0) + xv - lv;
-    if (r < a.B) {
+    if (r < a.B && (r >= r_begin && r < r_end)) {
       a.m.out_qsl[r] = pre_o;
       a.m.valid_qsl[r] = pre_v;
     }
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(1024) meta_kernel(const MetaArgs a) {
     }
     __syncthreads();
   }
-  if (tid == 0) {
+  if (tid == 0 && blockIdx.x == 0) {
     a.m.out_qsl[a.B] = carry_o;
     a.m.valid_qsl[a.B] = carry_v;
     *a.m.n_valid = min(carry_v, a.T_out);
@@ -137,8 +139,9 @@ __global__ void __launch_bounds__(1024) meta_kernel(const MetaArgs a) {
   }
   __syncthreads();
 
-  // pass 2: rows of request r
-  for (int r = warp; r < a.B; r += nw) {
+  // pass 2: rows of request r (this CTA's own requests; their offsets were
+  // written by this CTA above)
+  for (int r = r_begin + warp; r < r_end; r += nw) {
     int n, acc;
     bool bad;
     request_counts(a, r, n, acc, bad);
@@ -199,9 +202,10 @@ __global__ void __launch_bounds__(1024) meta_kernel(const MetaArgs a) {
     }
     if (lane == 0) a.m.seq_len[r] = static_cast<int32_t>(p0 + a.K);
   }
-  // rows past the non-rejected count
-  const int nv = *a.m.n_valid;
-  for (int i = nv + tid; i < a.T_out; i += blockDim.x) a.m.valid_rows[i] = -1;
+  // rows past the non-rejected count (every CTA knows the total)
+  const int nv = min(carry_v, a.T_out);
+  for (int i = nv + blockIdx.x * blockDim.x + tid; i < a.T_out; i += gridDim.x * blockDim.x)
+    a.m.valid_rows[i] = -1;
 }
 
 int launch_meta(const MetaLaunch& L, cudaStream_t st) {
@@ -223,11 +227,11 @@ int launch_meta(const MetaLaunch& L, cudaStream_t st) {
   a.block_table = L.block_table;
   a.m = L.meta;
   a.status = L.status;
-  int threads = 32;
-  while (threads < L.B && threads < 1024) threads <<= 1;
-  if (threads < 128) threads = 128;
-  return launch_pdl(meta_kernel, dim3(1), dim3(threads), 0, st, a) == cudaSuccess ? PE_OK
-                                                                                : PE_ERR_CUDA;
+  // 8 warps per CTA, one request per warp in pass 2
+  const int threads = 256;
+  const int grid = (L.B + threads / 32 - 1) / (threads / 32);
+  return launch_pdl(meta_kernel, dim3(grid), dim3(threads), 0, st, a) == cudaSuccess ? PE_OK
+                                                                                  : PE_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ (2) hidden-state map

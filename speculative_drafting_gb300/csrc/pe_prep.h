@@ -110,6 +110,7 @@ struct AttnArgs {
   void* out;       // [B*K][H*hd]
   uint32_t* status;
 };
+int attention_split_count(int B, int G, int max_blocks, int bs, int num_sms);
 void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, int num_sms,
                     int& n_splits, int& split_len);
 size_t attention_scratch_bytes(int B, int K, int H, int hd, int n_splits);
