@@ -4,11 +4,12 @@
 // once; draft position k sees every cache position up to its own).
 //
 // bf16: one CTA per (request, KV head, key split).  Its query tile is the K
-// sample rows x the H/G query heads that share the KV head (GQA), 16 rows per
-// warp.  Keys stream through shared memory in chunks of 64 (cp.async, 3 stages,
-// 16-byte chunks XOR-swizzled by row so ldmatrix is conflict-free); S = Q K^T and
-// O += P V run on warp-level bf16 mma.sync with fp32 accumulators and an online
-// softmax in the exp2 domain (P enters the second product as a hi + lo bf16 pair).  Each split writes unnormalised partials; a combine
+// sample rows x the H/G query heads that share the KV head (GQA).  A producer
+// warp streams the KV blocks with TMA (one block-table lookup per 16 keys) into
+// a 3-chunk ring; compute warps own 16 query rows and half of every 64-key
+// chunk; S = Q K^T and O += P V run on warp-level bf16 mma.sync with fp32
+// accumulators and an online softmax in the exp2 domain (P enters the second
+// product as a hi + lo bf16 pair).  Each split writes unnormalised partials; a combine
 // kernel merges the splits (flash-decoding style).
 //
 // fp32: one CTA per (sample row, query head), SIMT dot products, online softmax.
@@ -20,31 +21,79 @@
 
 namespace pe {
 
-constexpr int kKC = 64;  // keys per chunk
-// cp.async ring depth: three chunks for hd 64; two for hd 128, whose 32 KB
-// chunks would otherwise hold an SM to two CTAs
-template <int HD>
-__host__ __device__ constexpr int ring_stages() {
-  return HD >= 128 ? 2 : 3;
-}
+constexpr int kKC = 64;               // keys per chunk
+constexpr int kStages = 3;            // KV chunks in flight per CTA
+constexpr int kMaxComputeWarps = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplits = 128;       // key splits per (request, KV head)
 constexpr long kMaxSplitKeys = 2048;  // keys per split, at most
 
-template <int HD>
-__global__ void __launch_bounds__(256) attn_mma_kernel(const AttnArgs a) {
-  constexpr int kStages = ring_stages<HD>();
-  constexpr int ROWB = HD * 2;       // bytes per key row in shared memory
-  constexpr int CH = HD / 8;         // 16-byte chunks per key row
-  constexpr int TILE = kKC * ROWB;   // one K or V chunk
-  extern __shared__ __align__(128) uint8_t smem[];
-  pdl_trigger();
-  pdl_wait();
+// Thread roles of the bf16 attention CTA: compute warps 0..cw-1 (row warp
+// w % rw, key group w / rw), then one producer warp.
+struct AttnShape {
+  int rw;  // warps over the query rows (16 rows each)
+  int kg;  // key groups: each handles 64 / kg keys of every chunk
+  int cw;  // compute warps = rw * kg
+};
+
+__host__ __device__ inline AttnShape attn_shape(int rows) {
+  AttnShape s;
+  s.rw = (rows + 15) / 16;
+  s.kg = s.rw <= kMaxComputeWarps / 2 ? 2 : 1;
+  s.cw = s.rw * s.kg;
+  return s;
+}
+
+// One CTA per (key split, KV head, request).  The producer warp walks the
+// split's 64-key chunks: per 16-key group it looks the block up once and loads
+// the K and V rows of this KV head with TMA (128-byte swizzle, 64 elements of
+// the head dim per box) into a ring of kStages chunks.  Each compute warp owns
+// 16 query rows and one key group; S = Q K^T and O += P V run on mma.sync with
+// fp32 accumulators and an online softmax in the exp2 domain; P enters P V as a
+// hi + lo bf16 pair.  At the end the key groups' states merge in shared memory
+// and the CTA writes unnormalised partials for the combine kernel.
+template <int HD, int KG>
+__global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1))
+    attn_tma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                    const AttnArgs a) {
+  constexpr int HALVES = HD / 64;        // 128-byte swizzle atoms per key row
+  constexpr int GROUP_BYTES = 16 * 128;  // one box: 16 keys x 64 dims
+  constexpr int TILE = kKC * HD * 2;     // one K (or V) chunk
+  constexpr int STAGE = 2 * TILE;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ uint32_t mask_sh[kStages];
+  __shared__ int abort_sh;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
   const int split = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int HG = a.H / a.G;
   const int rows = a.K * HG;
+  const AttnShape sh = attn_shape(rows);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
+  const int n_compute = sh.cw * 32;
+
+  // stale shared memory must be finite: a masked key still multiplies its V row by 0
+  for (int i = threadIdx.x; i < kStages * STAGE / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], sh.cw);
+    }
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == sh.cw && lane == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+  }
+  pdl_trigger();
+  pdl_wait();
+  fence_proxy_async();  // the zeroed ring is visible to the TMA writes that follow
+  __syncthreads();
 
   int L = a.seq_len[r];
   const int Lmax = a.max_blocks * a.bs;
@@ -55,210 +104,249 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const AttnArgs a) {
   const int P0 = L - a.K;  // position of the first draft query (the NTP row)
   const int t0 = split * a.split_len;
   const int t1 = min(L, t0 + a.split_len);
+  const int n_chunks = t1 > t0 ? (t1 - t0 + kKC - 1) / kKC : 0;
   const size_t n_samp = static_cast<size_t>(a.B) * a.K;
+  volatile int* abort_flag = &abort_sh;
 
-  // rows handled by this thread: ra = 16*warp + gq, rb = ra + 8
-  const int ra = warp * 16 + gq, rb = ra + 8;
-  auto row_sample = [&](int row) { return static_cast<size_t>(r) * a.K + row / HG; };
-  auto row_head = [&](int row) { return g * HG + row % HG; };
-
-  if (t0 >= t1) {
-    for (int hf = 0; hf < 2; ++hf) {
-      const int rr = hf ? rb : ra;
-      if (rr >= rows) continue;
-      const size_t idx = (static_cast<size_t>(split) * n_samp + row_sample(rr)) * a.H + row_head(rr);
-      if (tq == 0) {
-        a.part_ml[idx * 2] = -INFINITY;
-        a.part_ml[idx * 2 + 1] = 0.f;
-      }
-      for (int d = tq * 2; d < HD; d += 8) {
-        a.part_o[idx * HD + d] = 0.f;
-        a.part_o[idx * HD + d + 1] = 0.f;
-      }
-    }
-    return;
-  }
-
-  // Q fragments (A operand of m16n8k16, row-major), zero for padding rows
-  uint32_t qf[HD / 16][4];
-  {
-    const bf16* q = static_cast<const bf16*>(a.q);
-    auto qrow = [&](int row) -> const bf16* {
-      return row < rows ? q + (row_sample(row) * a.H + row_head(row)) * HD : nullptr;
-    };
-    const bf16* qa = qrow(ra);
-    const bf16* qb = qrow(rb);
-#pragma unroll
-    for (int ks = 0; ks < HD / 16; ++ks) {
-      const int c0 = ks * 16 + tq * 2;
-      qf[ks][0] = qa ? *reinterpret_cast<const uint32_t*>(qa + c0) : 0u;
-      qf[ks][1] = qb ? *reinterpret_cast<const uint32_t*>(qb + c0) : 0u;
-      qf[ks][2] = qa ? *reinterpret_cast<const uint32_t*>(qa + c0 + 8) : 0u;
-      qf[ks][3] = qb ? *reinterpret_cast<const uint32_t*>(qb + c0 + 8) : 0u;
-    }
-  }
-  const int lim_a = P0 + (ra < rows ? ra / HG : 0);
-  const int lim_b = P0 + (rb < rows ? rb / HG : 0);
-
-  const bf16* kc = static_cast<const bf16*>(a.k_cache);
-  const bf16* vc = static_cast<const bf16*>(a.v_cache);
-  const uint32_t sbase = smem_u32(smem);
-  const int n_chunks = (t1 - t0 + kKC - 1) / kKC;
-
-  auto load_chunk = [&](int c, int stage) {
-    const uint32_t kdst = sbase + stage * 2 * TILE;
-    const uint32_t vdst = kdst + TILE;
-    for (int idx = threadIdx.x; idx < kKC * CH; idx += blockDim.x) {
-      const int key = idx / CH, ch = idx - key * CH;
-      const int t = t0 + c * kKC + key;
-      bool ok = t < t1;
-      size_t off = 0;
-      if (ok) {
-        const int blk = a.block_table[static_cast<size_t>(r) * a.max_blocks + t / a.bs];
-        if (blk < 0 || blk >= a.num_blocks) {
-          set_status(a.status, PE_ST_BLOCK_RANGE);
-          ok = false;
-        } else {
-          off = ((static_cast<size_t>(blk) * a.G + g) * a.bs + t % a.bs) * HD + ch * 8;
+  if (warp == sh.cw) {
+    // ---------------- producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int c = 0; c < n_chunks && !*abort_flag; ++c) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+          abort_sh = 1;
+          set_status(a.status, PE_ST_TIMEOUT);
+          break;
+        }
+        uint32_t mask = 0;
+        int row[4];
+        for (int q = 0; q < 4; ++q) {
+          const int t = t0 + c * kKC + q * 16;
+          row[q] = 0;
+          if (t >= t1) continue;
+          const int blk = a.block_table[static_cast<size_t>(r) * a.max_blocks + t / a.bs];
+          if (blk < 0 || blk >= a.num_blocks) {
+            set_status(a.status, PE_ST_BLOCK_RANGE);
+            continue;
+          }
+          row[q] = (blk * a.G + g) * a.bs + t % a.bs;
+          mask |= 1u << q;
+        }
+        mask_sh[stage] = mask;
+        mbar_arrive_expect_tx(&full_bar[stage],
+                              static_cast<uint32_t>(__popc(mask)) * 2u * HALVES * GROUP_BYTES);
+        uint8_t* kd = ring + stage * STAGE;
+        uint8_t* vd = kd + TILE;
+        for (int q = 0; q < 4; ++q) {
+          if (!(mask & (1u << q))) continue;
+          for (int hh = 0; hh < HALVES; ++hh) {
+            const int off = hh * (kKC * 128) + q * GROUP_BYTES;
+            tma_load_2d(kd + off, &kmap, &full_bar[stage], hh * 64, row[q], policy_evict_first());
+            tma_load_2d(vd + off, &vmap, &full_bar[stage], hh * 64, row[q], policy_evict_first());
+          }
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      const uint32_t so = key * ROWB + ((ch ^ (key & 7)) << 4);
-      cp_async16(kdst + so, kc + off, ok);
-      cp_async16(vdst + so, vc + off, ok);
     }
-  };
-
-  float o[HD / 8][4];
-#pragma unroll
-  for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-  const float sc = kLog2e / sqrtf(static_cast<float>(HD));
-
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < n_chunks) load_chunk(s, s);
-    cp_async_commit();
-  }
-
-  for (int c = 0; c < n_chunks; ++c) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
+  } else {
+    // ---------------- compute warps
+    const int rw = warp % sh.rw, kgi = warp / sh.rw;
+    constexpr int KEYS = kKC / KG;  // keys of each chunk this warp handles (64 or 32)
+    constexpr int NT = KEYS / 8;    // 8-key n-tiles
+    const int kofs = kgi * KEYS;
+    const int ra = rw * 16 + gq, rb = ra + 8;
+    auto row_sample = [&](int rr) { return static_cast<size_t>(r) * a.K + rr / HG; };
+    auto row_head = [&](int rr) { return g * HG + rr % HG; };
+    uint32_t qf[HD / 16][4];
     {
-      const int nc = c + kStages - 1;
-      if (nc < n_chunks) load_chunk(nc, nc % kStages);
-      cp_async_commit();
-    }
-    const uint32_t ks_base = sbase + (c % kStages) * 2 * TILE;
-    const uint32_t vs_base = ks_base + TILE;
-
-    // S = Q K^T over 64 keys: 8 n-tiles of 8 keys
-    float s[8][4];
+      const bf16* q = static_cast<const bf16*>(a.q);
+      const bf16* qa = ra < rows ? q + (row_sample(ra) * a.H + row_head(ra)) * HD : nullptr;
+      const bf16* qb = rb < rows ? q + (row_sample(rb) * a.H + row_head(rb)) * HD : nullptr;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < HD / 16; ++ks) {
-#pragma unroll
-      for (int nt = 0; nt < 8; nt += 2) {
-        const int mat = lane >> 3;
-        const int key = nt * 8 + (mat >> 1) * 8 + (lane & 7);
-        const int ch = ks * 2 + (mat & 1);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(ks_base + key * ROWB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(s[nt], qf[ks], b0, b1);
-        mma_bf16_16816(s[nt + 1], qf[ks], b2, b3);
+      for (int ks = 0; ks < HD / 16; ++ks) {
+        const int c0 = ks * 16 + tq * 2;
+        qf[ks][0] = qa ? *reinterpret_cast<const uint32_t*>(qa + c0) : 0u;
+        qf[ks][1] = qb ? *reinterpret_cast<const uint32_t*>(qb + c0) : 0u;
+        qf[ks][2] = qa ? *reinterpret_cast<const uint32_t*>(qa + c0 + 8) : 0u;
+        qf[ks][3] = qb ? *reinterpret_cast<const uint32_t*>(qb + c0 + 8) : 0u;
       }
     }
-    // scale, causal / range mask, online softmax (rows ra: s[.][0..1], rb: s[.][2..3])
-    const int kbase = t0 + c * kKC;
-    float mx_a = -INFINITY, mx_b = -INFINITY;
+    const int lim_a = P0 + (ra < rows ? ra / HG : 0);
+    const int lim_b = P0 + (rb < rows ? rb / HG : 0);
+    float o[HD / 8][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+    const float sc = kLog2e / sqrtf(static_cast<float>(HD));
+    // shared-memory address of 16-byte unit ch (0 .. HD/8-1) of chunk key kk
+    auto kv_addr = [&](uint32_t base, int kk, int ch) {
+      return base + (ch >> 3) * (kKC * 128) + kk * 128 + (((ch & 7) ^ (kk & 7)) << 4);
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+        abort_sh = 1;
+        set_status(a.status, PE_ST_TIMEOUT);
+        break;
+      }
+      const uint32_t mask = mask_sh[stage];
+      const uint32_t kb = smem_u32(ring + stage * STAGE);
+      const uint32_t vb = kb + TILE;
+      // S = Q K^T over this warp's keys: KEYS/8 n-tiles of 8 keys
+      float s[NT][4];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = kbase + nt * 8 + tq * 2 + e;
-        const bool valid = t < t1;
-        s[nt][e] = (valid && t <= lim_a) ? s[nt][e] * sc : -INFINITY;
-        s[nt][2 + e] = (valid && t <= lim_b) ? s[nt][2 + e] * sc : -INFINITY;
-        mx_a = fmaxf(mx_a, s[nt][e]);
-        mx_b = fmaxf(mx_b, s[nt][2 + e]);
+      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < HD / 16; ++ks) {
+#pragma unroll
+        for (int nt = 0; nt < NT; nt += 2) {
+          const int mat = lane >> 3;
+          const int kk = kofs + nt * 8 + (mat >> 1) * 8 + (lane & 7);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(kv_addr(kb, kk, ks * 2 + (mat & 1)), b0, b1, b2, b3);
+          mma_bf16_16816(s[nt], qf[ks], b0, b1);
+          mma_bf16_16816(s[nt + 1], qf[ks], b2, b3);
+        }
+      }
+      // mask (range, invalid blocks, causal limit), online softmax
+      const int kbase = t0 + c * kKC + kofs;
+      float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = kbase + nt * 8 + tq * 2 + e;
+          const bool ok = t < t1 && ((mask >> ((kofs + nt * 8) >> 4)) & 1u);
+          s[nt][e] = (ok && t <= lim_a) ? s[nt][e] * sc : -INFINITY;
+          s[nt][2 + e] = (ok && t <= lim_b) ? s[nt][2 + e] * sc : -INFINITY;
+          mx_a = fmaxf(mx_a, s[nt][e]);
+          mx_b = fmaxf(mx_b, s[nt][2 + e]);
+        }
+      }
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+      const float al_a = (mn_a == -INFINITY) ? 1.f : exp2f(m_a - mn_a);
+      const float al_b = (mn_b == -INFINITY) ? 1.f : exp2f(m_b - mn_b);
+      m_a = mn_a;
+      m_b = mn_b;
+      float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          s[nt][e] = (mn_a == -INFINITY) ? 0.f : exp2f(s[nt][e] - mn_a);
+          s[nt][2 + e] = (mn_b == -INFINITY) ? 0.f : exp2f(s[nt][2 + e] - mn_b);
+          ps_a += s[nt][e];
+          ps_b += s[nt][2 + e];
+        }
+      }
+      l_a = l_a * al_a + ps_a;
+      l_b = l_b * al_b + ps_b;
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) {
+        o[i][0] *= al_a;
+        o[i][1] *= al_a;
+        o[i][2] *= al_b;
+        o[i][3] *= al_b;
+      }
+      // O += P V over this warp's keys, 16 keys per k-step
+#pragma unroll
+      for (int kk = 0; kk < NT / 2; ++kk) {
+        uint32_t ph[4], pl[4];
+        split_bf16x2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+        split_bf16x2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+        split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+        split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+#pragma unroll
+        for (int nd = 0; nd < HD / 8; nd += 2) {
+          const int mat = lane >> 3;
+          const int key = kofs + kk * 16 + (mat & 1) * 8 + (lane & 7);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(kv_addr(vb, key, nd + (mat >> 1)), b0, b1, b2, b3);
+          mma_bf16_16816(o[nd], ph, b0, b1);
+          mma_bf16_16816(o[nd], pl, b0, b1);
+          mma_bf16_16816(o[nd + 1], ph, b2, b3);
+          mma_bf16_16816(o[nd + 1], pl, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[stage]);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-    const float al_a = (mn_a == -INFINITY) ? 1.f : exp2f(m_a - mn_a);
-    const float al_b = (mn_b == -INFINITY) ? 1.f : exp2f(m_b - mn_b);
-    m_a = mn_a;
-    m_b = mn_b;
-    float ps_a = 0.f, ps_b = 0.f;
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    // merge the key groups through the (now idle) ring: group 1 parks, group 0 merges
+    float* mo = reinterpret_cast<float*>(ring);            // [row][HD]
+    float* mml = mo + static_cast<size_t>(sh.rw) * 16 * HD;  // [row][2]
+    named_bar_sync(1, n_compute);
+    if (KG == 2 && kgi == 1) {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+      for (int hf = 0; hf < 2; ++hf) {
+        const int rl = rw * 16 + gq + hf * 8;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        s[nt][e] = (mn_a == -INFINITY) ? 0.f : exp2f(s[nt][e] - mn_a);
-        s[nt][2 + e] = (mn_b == -INFINITY) ? 0.f : exp2f(s[nt][2 + e] - mn_b);
-        ps_a += s[nt][e];
-        ps_b += s[nt][2 + e];
+        for (int nd = 0; nd < HD / 8; ++nd) {
+          const int d = nd * 8 + tq * 2;
+          mo[rl * HD + d] = o[nd][hf * 2];
+          mo[rl * HD + d + 1] = o[nd][hf * 2 + 1];
+        }
+        if (tq == 0) {
+          mml[rl * 2] = hf ? m_b : m_a;
+          mml[rl * 2 + 1] = hf ? l_b : l_a;
+        }
       }
     }
-    l_a = l_a * al_a + ps_a;
-    l_b = l_b * al_b + ps_b;
+    named_bar_sync(1, n_compute);
+    if (kgi == 0) {
 #pragma unroll
-    for (int i = 0; i < HD / 8; ++i) {
-      o[i][0] *= al_a;
-      o[i][1] *= al_a;
-      o[i][2] *= al_b;
-      o[i][3] *= al_b;
-    }
-    // O += P V: 4 k-steps of 16 keys, HD/8 n-tiles of 8 dims.  P is carried as
-    // a bf16 pair hi + lo (two MMAs), about 16 significant bits, so the weights
-    // are not rounded to 8 bits before they meet V.
+      for (int hf = 0; hf < 2; ++hf) {
+        const int rr = hf ? rb : ra;
+        float m = hf ? m_b : m_a, l = hf ? l_b : l_a;
+        float w0 = 1.f, w1 = 0.f;
+        const int rl = rw * 16 + gq + hf * 8;
+        if (KG == 2) {
+          const float m1 = mml[rl * 2], l1 = mml[rl * 2 + 1];
+          const float M = fmaxf(m, m1);
+          w0 = (m == -INFINITY) ? 0.f : exp2f(m - M);
+          w1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - M);
+          l = l * w0 + l1 * w1;
+          m = M;
+        }
+        if (rr >= rows) continue;
+        const size_t idx =
+            (static_cast<size_t>(split) * n_samp + row_sample(rr)) * a.H + row_head(rr);
+        float* po = a.part_o + idx * HD;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t ph[4], pl[4];
-      split_bf16x2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
-      split_bf16x2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
-      split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
-      split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
-#pragma unroll
-      for (int nd = 0; nd < HD / 8; nd += 2) {
-        const int mat = lane >> 3;
-        const int key = kk * 16 + (mat & 1) * 8 + (lane & 7);
-        const int ch = nd + (mat >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(vs_base + key * ROWB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(o[nd], ph, b0, b1);
-        mma_bf16_16816(o[nd], pl, b0, b1);
-        mma_bf16_16816(o[nd + 1], ph, b2, b3);
-        mma_bf16_16816(o[nd + 1], pl, b2, b3);
+        for (int nd = 0; nd < HD / 8; ++nd) {
+          const int d = nd * 8 + tq * 2;
+          float v0 = o[nd][hf * 2] * w0, v1 = o[nd][hf * 2 + 1] * w0;
+          if (KG == 2) {
+            v0 += mo[rl * HD + d] * w1;
+            v1 += mo[rl * HD + d + 1] * w1;
+          }
+          *reinterpret_cast<float2*>(po + d) = make_float2(v0, v1);
+        }
+        if (tq == 0) {
+          a.part_ml[idx * 2] = m;
+          a.part_ml[idx * 2 + 1] = l;
+        }
       }
     }
   }
-  cp_async_wait<0>();
-
-  // quad-reduce the row sums and write this split's partials
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int rr = half ? rb : ra;
-    if (rr >= rows) continue;
-    const size_t idx = (static_cast<size_t>(split) * n_samp + row_sample(rr)) * a.H + row_head(rr);
-    float* po = a.part_o + idx * HD;
-#pragma unroll
-    for (int nd = 0; nd < HD / 8; ++nd) {
-      const int d = nd * 8 + tq * 2;
-      *reinterpret_cast<float2*>(po + d) = make_float2(o[nd][half * 2], o[nd][half * 2 + 1]);
-    }
-    if (tq == 0) {
-      a.part_ml[idx * 2] = half ? m_b : m_a;
-      a.part_ml[idx * 2 + 1] = half ? l_b : l_a;
-    }
-  }
+  // the producer may still be waiting for an empty slot only after an abort
+  __syncthreads();
 }
 
 // out[s][h*hd + d] = sum_j 2^(m_j - M) o_j[d] / sum_j 2^(m_j - M) l_j.
@@ -415,24 +503,27 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
                : PE_ERR_CUDA;
   }
   const int rows = a.K * (a.H / a.G);
-  const int warps = (rows + 15) / 16;
+  const AttnShape sh = attn_shape(rows);
   const dim3 grid(a.n_splits, a.G, a.B);
-  const int stages = a.hd >= 128 ? ring_stages<128>() : ring_stages<64>();
-  const size_t smem = static_cast<size_t>(stages) * 2 * kKC * a.hd * 2;
-  // one attribute value for every launch (the largest ring)
-  const int smem_max = 3 * 2 * kKC * 128 * 2;
-  if (a.hd == 64) {
-    cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-    if (launch_pdl(attn_mma_kernel<64>, grid, dim3(warps * 32), smem, st, a) != cudaSuccess)
-      return PE_ERR_CUDA;
-  } else if (a.hd == 128) {
-    cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-    if (launch_pdl(attn_mma_kernel<128>, grid, dim3(warps * 32), smem, st, a) != cudaSuccess)
-      return PE_ERR_CUDA;
-  } else {
+  const size_t smem = static_cast<size_t>(kStages) * 2 * kKC * a.hd * 2 + 1024;
+  // TMA views of the caches: rows = (block, KV head, offset), 64-element boxes
+  // of 16 rows; a 16-key group never crosses a block (block size % 16 == 0)
+  CUtensorMap kmap, vmap;
+  const uint64_t nrows = static_cast<uint64_t>(a.num_blocks) * a.G * a.bs;
+  if (!encode_tmap_bf16(&kmap, a.k_cache, nrows, a.hd, 16) ||
+      !encode_tmap_bf16(&vmap, a.v_cache, nrows, a.hd, 16))
+    return PE_ERR_CUDA;
+  const int smem_max = kStages * 2 * kKC * 128 * 2 + 1024;
+  const dim3 block(32 * (sh.cw + 1));
+  void (*kern)(CUtensorMap, CUtensorMap, AttnArgs) = nullptr;
+  if (a.hd == 64)
+    kern = sh.kg == 2 ? attn_tma_kernel<64, 2> : attn_tma_kernel<64, 1>;
+  else if (a.hd == 128)
+    kern = sh.kg == 2 ? attn_tma_kernel<128, 2> : attn_tma_kernel<128, 1>;
+  else
     return PE_ERR_UNSUPPORTED;
-  }
-  if (cudaGetLastError() != cudaSuccess) return PE_ERR_CUDA;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+  if (launch_pdl(kern, grid, block, smem, st, kmap, vmap, a) != cudaSuccess) return PE_ERR_CUDA;
   return launch_pdl(attn_combine_kernel<bf16>, dim3(a.B * a.K * a.H), dim3(std::min(a.hd, 128)), 0,
                     st, a) == cudaSuccess
              ? PE_OK
