@@ -26,7 +26,9 @@
  * Conventions for every call
  *   - All tensor arguments are DEVICE pointers owned by the caller; the library
  *     never frees or keeps them past the call (weights excepted: pe_create
- *     borrows them for the handle's lifetime).  Layouts are dense row-major.
+ *     borrows them for the handle's lifetime; for bf16 it reads the seven
+ *     projection matrices once, into its own tile-packed copy, so later
+ *     writes to those seven are not seen).  Layouts are dense row-major.
  *   - Floating tensors have the handle's dtype: float (PE_DTYPE_F32) or bf16
  *     bit patterns (PE_DTYPE_BF16), except where a signature says float.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
@@ -100,7 +102,12 @@ typedef struct pe_dims {
   float rope_theta;   /* RoPE base */
 } pe_dims;
 
-/* Drafter parameters: device pointers, borrowed for the handle's lifetime. */
+/* Drafter parameters: device pointers, borrowed for the handle's lifetime.
+ * emb, emb_mask, h_shared and gamma_stream are required.  The layer's parameters
+ * (w_fc, w_qkv, w_o, gamma_post, w_gate, w_up, w_down, gamma_final, w_lm, and
+ * gamma_in for a pre-norm layer) come all together or all NULL: with none, the
+ * handle serves pe_prepare_inputs only and the layer's calls (pe_draft_step,
+ * pe_argmax, pe_argmax_noalloc) return PE_ERR_ARG.  Some but not all: PE_ERR_ARG. */
 typedef struct pe_weights {
   const void* emb;          /* [V][d] token embedding */
   const void* emb_mask;     /* [d] learned emb(mask) for the MASK slots */
@@ -147,10 +154,16 @@ typedef struct pe_handle pe_handle;
 
 /* Create a handle for one drafter.  Validates dims (PE_ERR_UNSUPPORTED) and
  * pointers (PE_ERR_ARG), selects the kernels and encodes the TMA descriptors of
- * the weight matrices.  Uses the current CUDA device; *out is NULL on error. */
+ * the weight matrices.  bf16: allocates device memory for a copy of w_fc,
+ * w_qkv, w_o, w_gate, w_up, w_down and w_lm in tile order (blocks of 128 rows x
+ * 64 columns, each one contiguous 16 KB run, zero-padded to whole blocks), then
+ * synchronises the device and fills it; pe_destroy frees it.  This is the only
+ * call that allocates device memory or synchronises.  Uses the current CUDA
+ * device; *out is NULL on error (PE_ERR_CUDA: allocation or packing failed). */
 int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out);
 
-/* Destroy a handle (NULL is ignored).  Does not touch the weights. */
+/* Destroy a handle (NULL is ignored): frees its packed weight copy, never the
+ * caller's weights.  No work that uses the handle may still be in flight. */
 void pe_destroy(pe_handle* h);
 
 /* Workspace bytes that cover every call with at most max_batch requests,

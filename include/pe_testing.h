@@ -22,7 +22,12 @@ enum {
   PE_PROJ_O = 2,      /* X [n][H hd] . w_o^T    -> float [n][d]        */
   PE_PROJ_SWIGLU = 3, /* silu(X w_gate^T) * (X w_up^T) -> dtype [n][I] */
   PE_PROJ_DOWN = 4,   /* X [n][I]    . w_down^T -> float [n][d]        */
-  PE_PROJ_LM = 5      /* X [n][d]    . w_lm^T   -> float [n][V]        */
+  PE_PROJ_LM = 5,     /* X [n][d]    . w_lm^T   -> float [n][V]        */
+  /* flags OR'ed into `which` */
+  PE_PROJ_PERSISTENT = 0x100, /* never split K over a cluster: the persistent
+                                 schedule with its tail split */
+  PE_PROJ_PAIR = 0x200        /* bf16 only: X holds n rows of high parts followed
+                                 by n rows of low parts; the operand is hi + lo */
 };
 
 /* Workspace bytes pe_test_projection needs for n_rows rows (0 on bad input). */

@@ -21,6 +21,8 @@ struct pe_handle {
   int num_sms;
   CUtensorMap m_fc, m_qkv, m_o, m_gate, m_up, m_down, m_lm;
   double inv_freq[64];
+  void* packed;  // owned: tile-packed copies of the seven projection weights (bf16)
+  bool has_layer;  // false: metadata / drafter-input handle without layer weights
 };
 
 namespace {
@@ -47,9 +49,9 @@ GemmShape gemm_shape(const pe_handle* h, int id) {
   }
 }
 
-TcPlan plan_of(const pe_handle* h, int id, int N, bool bpair) {
+TcPlan plan_of(const pe_handle* h, int id, int N, bool bpair, bool allow_split = true) {
   const GemmShape s = gemm_shape(h, id);
-  return plan_gemm_tc(s.M, s.K, N, s.dual, bpair ? 1 : 0, h->num_sms, true);
+  return plan_gemm_tc(s.M, s.K, N, s.dual, bpair ? 1 : 0, h->num_sms, allow_split);
 }
 
 // Attention split partials, bounded over every batch size <= B (the split count
@@ -165,7 +167,7 @@ int check_meta(const pe_meta* m) {
 // X_lo: the low half of a bf16-pair operand (bf16 only; nullable).
 int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
              const int* n_rows_dev, const Epilogue& epi, void* ws, const Layout& L,
-             cudaStream_t st) {
+             cudaStream_t st, bool allow_split = true) {
   const GemmShape s = gemm_shape(h, id);
   if (!is_bf16(h)) {
     const pe_weights& w = h->w;
@@ -175,7 +177,7 @@ int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
     return launch_gemm_f32(static_cast<const float*>(W), static_cast<const float*>(W2),
                            static_cast<const float*>(X), s.M, s.K, N_cap, n_rows_dev, epi, st);
   }
-  const TcPlan p = plan_of(h, id, N_cap, X_lo != nullptr);
+  const TcPlan p = plan_of(h, id, N_cap, X_lo != nullptr, allow_split);
   const CUtensorMap* mA = id == G_FC ? &h->m_fc : id == G_QKV ? &h->m_qkv : id == G_O ? &h->m_o
                         : id == G_GATEUP ? &h->m_gate : id == G_DOWN ? &h->m_down : &h->m_lm;
   const CUtensorMap* mA2 = id == G_GATEUP ? &h->m_up : nullptr;
@@ -201,17 +203,27 @@ int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out) {
   if (bf && ((d.head_dim != 64 && d.head_dim != 128) ||
              d.K * (d.n_heads / d.n_kv_heads) > 128))
     return PE_ERR_UNSUPPORTED;
-  const void* req[] = {w->emb,    w->emb_mask, w->h_shared, w->gamma_stream, w->w_fc,
-                       w->w_qkv,  w->w_o,      w->gamma_post, w->w_gate,   w->w_up,
-                       w->w_down, w->gamma_final, w->w_lm};
+  const void* req[] = {w->emb, w->emb_mask, w->h_shared, w->gamma_stream};
   for (const void* p : req)
     if (!p || !aligned16(p)) return PE_ERR_ARG;
-  if (!d.post_norm && (!w->gamma_in || !aligned16(w->gamma_in))) return PE_ERR_ARG;
+  // the layer's parameters: all of them, or none (a preparation-only handle)
+  const void* layer[] = {w->w_fc,   w->w_qkv, w->w_o,    w->gamma_post, w->w_gate,
+                         w->w_up,   w->w_down, w->gamma_final, w->w_lm};
+  int n_layer = 0;
+  for (const void* p : layer) {
+    if (p && !aligned16(p)) return PE_ERR_ARG;
+    n_layer += p ? 1 : 0;
+  }
+  const int n_all = static_cast<int>(sizeof(layer) / sizeof(layer[0]));
+  if (n_layer != 0 && n_layer != n_all) return PE_ERR_ARG;
+  const bool has_layer = n_layer == n_all;
+  if (has_layer && !d.post_norm && (!w->gamma_in || !aligned16(w->gamma_in))) return PE_ERR_ARG;
   pe_handle* h = new (std::nothrow) pe_handle;
   if (!h) return PE_ERR_ARG;
   std::memset(h, 0, sizeof(*h));
   h->d = d;
   h->w = *w;
+  h->has_layer = has_layer;
   h->num_sms = num_sms_of_current_device();
   if (h->num_sms <= 0) {
     delete h;
@@ -220,16 +232,46 @@ int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out) {
   for (int i = 0; i < d.head_dim / 2; ++i)
     h->inv_freq[i] = std::pow(static_cast<double>(d.rope_theta),
                               -2.0 * static_cast<double>(i) / static_cast<double>(d.head_dim));
-  if (bf) {
+  if (bf && has_layer) {
     const int QKV = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
-    bool ok = encode_tmap_bf16(&h->m_fc, w->w_fc, d.d, 4ull * d.d, 128) &&
-              encode_tmap_bf16(&h->m_qkv, w->w_qkv, QKV, d.d, 128) &&
-              encode_tmap_bf16(&h->m_o, w->w_o, d.d, static_cast<uint64_t>(d.n_heads) * d.head_dim, 128) &&
-              encode_tmap_bf16(&h->m_gate, w->w_gate, d.inter, d.d, 128) &&
-              encode_tmap_bf16(&h->m_up, w->w_up, d.inter, d.d, 128) &&
-              encode_tmap_bf16(&h->m_down, w->w_down, d.d, d.inter, 128) &&
-              encode_tmap_bf16(&h->m_lm, w->w_lm, d.vocab, d.d, 128);
+    const int HD = d.n_heads * d.head_dim;
+    struct {
+      CUtensorMap* map;
+      const void* W;
+      int M, K;
+    } mats[] = {{&h->m_fc, w->w_fc, d.d, 4 * d.d},     {&h->m_qkv, w->w_qkv, QKV, d.d},
+                {&h->m_o, w->w_o, d.d, HD},             {&h->m_gate, w->w_gate, d.inter, d.d},
+                {&h->m_up, w->w_up, d.inter, d.d},      {&h->m_down, w->w_down, d.d, d.inter},
+                {&h->m_lm, w->w_lm, d.vocab, d.d}};
+    bool ok = true;
+    if (gemm_weights_packed()) {
+      // one allocation, each copy 256-byte aligned; packed on a private stream
+      // once every earlier write of the weights, on any stream, has finished
+      size_t off[7], total = 0;
+      for (int i = 0; i < 7; ++i) {
+        off[i] = total;
+        total += al256(packed_weight_bytes(mats[i].M, mats[i].K));
+      }
+      cudaStream_t s = nullptr;
+      ok = cudaDeviceSynchronize() == cudaSuccess && cudaMalloc(&h->packed, total) == cudaSuccess &&
+           cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess;
+      for (int i = 0; ok && i < 7; ++i) {
+        void* P = static_cast<char*>(h->packed) + off[i];
+        ok = pack_weight(mats[i].W, mats[i].M, mats[i].K, P, s) == PE_OK &&
+             encode_packed_weight_map(mats[i].map, P, mats[i].M, mats[i].K);
+      }
+      if (s) {
+        ok = cudaStreamSynchronize(s) == cudaSuccess && ok;
+        cudaStreamDestroy(s);
+      }
+    } else {
+      for (auto& m : mats)
+        ok = ok && encode_tmap_bf16(m.map, m.W, static_cast<uint64_t>(m.M),
+                                    static_cast<uint64_t>(m.K), 128);
+    }
     if (!ok) {
+      cudaGetLastError();
+      if (h->packed) cudaFree(h->packed);
       delete h;
       return PE_ERR_CUDA;
     }
@@ -238,7 +280,11 @@ int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out) {
   return PE_OK;
 }
 
-void pe_destroy(pe_handle* h) { delete h; }
+void pe_destroy(pe_handle* h) {
+  if (!h) return;
+  if (h->packed) cudaFree(h->packed);
+  delete h;
+}
 
 size_t pe_workspace_bytes(const pe_handle* h, int max_batch, int max_rows_in,
                           int max_blocks_per_seq) {
@@ -331,8 +377,8 @@ int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl, const i
 int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void* A,
                   const int32_t* block_table, int max_blocks, int num_blocks, void* k_cache,
                   void* v_cache, void* z_out, void* ws, size_t ws_bytes, void* stream) {
-  if (!h || B < 1 || T_in < B || max_blocks < 1 || num_blocks < 1 || !A || !block_table ||
-      !k_cache || !v_cache || !z_out || !ws)
+  if (!h || !h->has_layer || B < 1 || T_in < B || max_blocks < 1 || num_blocks < 1 || !A ||
+      !block_table || !k_cache || !v_cache || !z_out || !ws)
     return PE_ERR_ARG;
   if (check_meta(meta) != PE_OK) return PE_ERR_ARG;
   if (!aligned16(A) || !aligned16(z_out) || !aligned16(ws)) return PE_ERR_ARG;
@@ -481,7 +527,7 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
 
 int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, float* logits,
               void* ws, size_t ws_bytes, void* stream) {
-  if (!h || !z || n_rows < 1 || !draft_tokens || !ws) return PE_ERR_ARG;
+  if (!h || !h->has_layer || !z || n_rows < 1 || !draft_tokens || !ws) return PE_ERR_ARG;
   if (!aligned16(z) || !aligned16(ws)) return PE_ERR_ARG;
   const Layout L = layout_argmax(h, n_rows);
   if (ws_bytes < L.total) return PE_ERR_ARG;
@@ -501,22 +547,33 @@ int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, fl
 }
 
 size_t pe_test_projection_workspace(const pe_handle* h, int which, int n_rows) {
+  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR);
   if (!h || which < 0 || which >= G_COUNT || n_rows < 1) return 0;
   return layout_projection(h, which, n_rows).total;
 }
 
 int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void* out, void* ws,
                        size_t ws_bytes, void* stream) {
-  if (!h || which < 0 || which >= G_COUNT || n_rows < 1 || !X || !out || !ws) return PE_ERR_ARG;
+  const bool persistent = (which & PE_PROJ_PERSISTENT) != 0;
+  const bool pair = (which & PE_PROJ_PAIR) != 0;
+  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR);
+  if (!h || !h->has_layer || which < 0 || which >= G_COUNT || n_rows < 1 || !X || !out || !ws)
+    return PE_ERR_ARG;
   if (!aligned16(X) || !aligned16(ws)) return PE_ERR_ARG;
+  if (pair && !is_bf16(h)) return PE_ERR_UNSUPPORTED;
   const Layout L = layout_projection(h, which, n_rows);
   if (ws_bytes < L.total) return PE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const GemmShape s = gemm_shape(h, which);
   Epilogue e;
   e.mode = which == G_GATEUP ? EPI_SWIGLU : EPI_STORE_F32;
   e.out = out;
-  e.ld_out = gemm_shape(h, which).M;
-  return run_gemm(h, which, X, nullptr, n_rows, nullptr, e, ws, L, st);
+  e.ld_out = s.M;
+  const void* X_lo =
+      pair ? static_cast<const void*>(static_cast<const bf16_t*>(X) +
+                                      static_cast<size_t>(n_rows) * s.K)
+           : nullptr;
+  return run_gemm(h, which, X, X_lo, n_rows, nullptr, e, ws, L, st, !persistent);
 }
 
 int pe_read_status(const pe_handle* h, void* ws, uint32_t* status, int clear, void* stream) {
@@ -552,4 +609,5 @@ const pe_dims* handle_dims(const pe_handle* h) { return &h->d; }
 const CUtensorMap* handle_lm_map(const pe_handle* h) { return &h->m_lm; }
 int handle_num_sms(const pe_handle* h) { return h->num_sms; }
 const void* handle_w_lm(const pe_handle* h) { return h->w.w_lm; }
+bool handle_has_layer(const pe_handle* h) { return h->has_layer; }
 }  // namespace pe

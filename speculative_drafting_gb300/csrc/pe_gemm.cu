@@ -30,11 +30,36 @@ constexpr int kMaxStages = 12;
 constexpr size_t kSmemBudget = 212 * 1024;  // dynamic shared memory for the stage ring
 constexpr int kPrefetchKb = 16;             // k-blocks of weights pulled into L2 early
 constexpr int kMaxClusterSplits = 8;        // portable cluster size
+// Weights in tile order (one contiguous 16 KB block per weight box) or row-major
+// (measured, LM head at B=1 with two CTAs per SM: 188 us packed, 192 us not).
+#ifndef PE_PACKED_WEIGHTS
+#define PE_PACKED_WEIGHTS 1
+#endif
+constexpr bool kPackedWeights = PE_PACKED_WEIGHTS != 0;
 // Narrow token tiles stream weights: two 64-element K atoms per stage put the
 // two 128-byte halves of each weight row's 256 bytes on the bus back to back
 // (measured: LM head at B=1 259 us instead of 303 us).  Wide tiles keep one atom
 // so that enough stages stay in flight.
 constexpr int kNarrowBN = 64;
+// Narrow token tiles run several CTAs per SM, each with its share of the SM's
+// shared memory: one CTA's loads keep only part of the SM's share of DRAM
+// bandwidth busy, whatever its ring depth (measured, LM head of 201088 x 2880 at
+// 8 tokens: 5 or 3 stages per CTA both 275 us; two CTAs of 3 stages 196 us,
+// three of 3 one-atom stages 188 us).  A long stream of tiles takes three per
+// SM; shorter GEMMs (split over K in clusters) do better with two.
+#ifndef PE_NARROW_CTAS_PER_SM
+#define PE_NARROW_CTAS_PER_SM 2
+#endif
+#ifndef PE_STREAM_CTAS_PER_SM
+#define PE_STREAM_CTAS_PER_SM 3
+#endif
+constexpr int kNarrowCtasPerSm = PE_NARROW_CTAS_PER_SM;
+constexpr int kStreamCtasPerSm = PE_STREAM_CTAS_PER_SM;
+// shared memory of an SM that its CTAs can have (228 KB less 1 KB)
+constexpr size_t kSmemPerSm = 227 * 1024;
+// per CTA beside its ring: the system's 1 KB, the static barriers and
+// reduction buffers (under 1 KB), the ring's 1 KB alignment slack, and a margin
+constexpr size_t kCtaSmemOverhead = 5 * 1024;
 constexpr int kTcThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;
 
@@ -43,6 +68,8 @@ struct TcArgs {
   int tile_base, tile_count;  // the (m, n) tiles of this launch
   int BN, n_tiles, m_tiles, k_splits, kb_per_split, num_kb, stages, acc_bufs;
   int atoms;  // 64-element K atoms per stage (a k-block is atoms * 64 elements)
+  int packed;   // weights tile-packed: box (m, atom) at row (m * k_atoms + atom) * 128
+  int k_atoms;  // 64-element atoms per weight row (packed)
   uint32_t tmem_cols;
   const int* n_rows_dev;
   Epilogue epi;
@@ -141,6 +168,20 @@ struct TileRef {
   int m, n, ks;
 };
 
+// Tensor-map coordinates of the weight box of tile row m at reduction offset x
+// (a multiple of 64).  Packed weights: past K the box lies beyond the last
+// block, so TMA fills it with zeros as it does past K of a row-major weight.
+PE_DEV void weight_box(const TcArgs& p, int m, int x, int& cx, int& cy) {
+  if (p.packed) {
+    const int a = x / kBK;
+    cx = 0;
+    cy = (a < p.k_atoms ? m * p.k_atoms + a : p.m_tiles * p.k_atoms) * kBM;
+  } else {
+    cx = x;
+    cy = m * kBM;
+  }
+}
+
 // The tile a CTA works on at its it-th turn; false when it has no more.
 PE_DEV bool next_tile(const TcArgs& p, int it, TileRef& t) {
   if (p.k_splits > 1) {
@@ -162,7 +203,10 @@ PE_DEV bool next_tile(const TcArgs& p, int it, TileRef& t) {
   return true;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+// OCC: CTAs per SM the instance is launched for (each instance keeps its own
+// fixed shared-memory limit, so graph replays of either stay launchable).
+template <int OCC>
+__global__ void __launch_bounds__(kTcThreads, OCC)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
                    const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapB2,
                    const TcArgs p) {
@@ -214,8 +258,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int kb1 = min(min(p.num_kb, kb0 + p.kb_per_split), kb0 + kPrefetchKb / p.atoms);
       for (int kb = kb0; kb < kb1; ++kb)
         for (int at = 0; at < p.atoms; ++at) {
-          tma_prefetch_l2_2d(&mapA, kb * kbk + at * kBK, t.m * kBM);
-          if (p.dual) tma_prefetch_l2_2d(&mapA2, kb * kbk + at * kBK, t.m * kBM);
+          if (kb * kbk + at * kBK >= p.K) break;
+          int cx, cy;
+          weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
+          tma_prefetch_l2_2d(&mapA, cx, cy);
+          if (p.dual) tma_prefetch_l2_2d(&mapA2, cx, cy);
         }
     }
   }
@@ -272,9 +319,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // back to back, A first (the weights dominate the traffic)
           for (int at = 0; at < p.atoms; ++at) {
             uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes;
-            const int x = kb * kbk + at * kBK;
-            tma_load_2d(sa, &mapA, &full_bar[stage], x, t.m * kBM, pol_w);
-            if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], x, t.m * kBM, pol_w);
+            int cx, cy;
+            weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
+            tma_load_2d(sa, &mapA, &full_bar[stage], cx, cy, pol_w);
+            if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], cx, cy, pol_w);
           }
           for (int at = 0; at < p.atoms; ++at) {
             uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes;
@@ -479,16 +527,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ------------------------------------------------------------------ host: plan + launch
 
-// How many clusters of `cs` CTAs with `smem` bytes each can be resident at once.
-static int max_active_clusters(int cs, size_t smem) {
+static_assert(kNarrowCtasPerSm >= 1 && kNarrowCtasPerSm <= 3, "CTAs per SM");
+static_assert(kStreamCtasPerSm >= 1 && kStreamCtasPerSm <= 3, "CTAs per SM");
+using TcKernelFn = decltype(&gemm_tc_kernel<1>);
+
+// The instance for `occ` CTAs per SM.
+static TcKernelFn tc_kernel(int occ) {
+  return occ >= 3 ? gemm_tc_kernel<3> : occ == 2 ? gemm_tc_kernel<2> : gemm_tc_kernel<1>;
+}
+
+// Dynamic shared memory limit of an instance: its largest ring plus the 1 KB
+// alignment slack.  The limit, not a launch's own size, decides how many CTAs
+// of the function the SM takes, so it is what makes `occ` CTAs fit.
+static size_t tc_max_dyn_smem(int occ) {
+  return occ > 1 ? kSmemPerSm / occ - kCtaSmemOverhead + 1024 : kSmemBudget + 1024;
+}
+
+// Set an instance's attributes: the same values at every launch.
+static cudaError_t tc_prepare(int occ) {
+  const TcKernelFn k = tc_kernel(occ);
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(tc_max_dyn_smem(occ)));
+  cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
+// How many clusters of `cs` CTAs of the `occ` instance with `smem` bytes each
+// can be resident at once.
+static int max_active_clusters(int occ, int cs, size_t smem) {
   static std::mutex mu;
-  static std::map<std::pair<int, size_t>, int> cache;
+  static std::map<std::pair<std::pair<int, int>, size_t>, int> cache;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_pair(cs, smem);
+  const auto key = std::make_pair(std::make_pair(occ, cs), smem);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(kSmemBudget + 1024));
+  tc_prepare(occ);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs * 64);
   cfg.blockDim = dim3(kTcThreads);
@@ -501,7 +575,7 @@ static int max_active_clusters(int cs, size_t smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, (void*)gemm_tc_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)tc_kernel(occ), &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -532,10 +606,38 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   }
   pl.n_tiles = (pl.N_cap + pl.BN - 1) / pl.BN;
   pl.m_tiles = (M + kBM - 1) / kBM;
+  // CTAs per SM: narrow tiles share each SM among several CTAs of at least two
+  // stages each (fewer atoms per stage where that is what fits); a stream of at
+  // least two full rounds of tiles takes the most
+  int occ = 1;
+  size_t budget = kSmemBudget;
+  if (pl.BN <= kNarrowBN) {
+    const int want = pl.m_tiles * pl.n_tiles >= 2 * kStreamCtasPerSm * num_sms ? kStreamCtasPerSm
+                                                                                : kNarrowCtasPerSm;
+    const size_t b = tc_max_dyn_smem(want) - 1024;
+    int atoms = pl.atoms;
+    size_t sb = stage_bytes;
+    while (atoms > 1 && b / sb < 2) {
+      atoms /= 2;
+      sb = (static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128 * nB) * atoms;
+    }
+    if (want > 1 && b / sb >= 2) {
+      occ = want;
+      budget = b;
+      pl.atoms = atoms;
+      stage_bytes = sb;
+    }
+  }
   pl.num_kb = (K + kBK * pl.atoms - 1) / (kBK * pl.atoms);
-  const int stages = static_cast<int>(kSmemBudget / stage_bytes);
+  const int stages = static_cast<int>(budget / stage_bytes);
   pl.stages = std::max(2, std::min(kMaxStages, stages));
   pl.smem_bytes = pl.stages * stage_bytes + 1024;
+  // (the occupancy query answers 1 for this kernel at any size, though the SM
+  // does run two such CTAs side by side: the fit is the arithmetic above, and
+  // no CTA outside a cluster waits for another, so it is only a speed matter)
+  pl.ctas_per_sm = occ;
+  // the resident CTAs of one wave; every "SM" count below is in these slots
+  num_sms *= occ;
   const int base = pl.m_tiles * pl.n_tiles;
   // split K across a cluster when one wave of plain tiles leaves SMs idle: the
   // splits of a tile must all be resident at once, their partial tile must fit
@@ -546,15 +648,20 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
     s = std::min(s, pl.num_kb * pl.atoms / 4);
     const size_t part_bytes = static_cast<size_t>(nA) * pl.BN * kBM * sizeof(float);
     if (part_bytes > pl.stages * stage_bytes) s = 1;
-    while (s > 1 && max_active_clusters(s, pl.smem_bytes) * s < base * s) --s;
+    while (s > 1 && max_active_clusters(occ, s, pl.smem_bytes) * s < base * s) --s;
     if (s < 2) s = 1;
   }
   pl.kb_per_split = (pl.num_kb + s - 1) / s;
   pl.k_splits = (pl.num_kb + pl.kb_per_split - 1) / pl.kb_per_split;
   pl.acc_bufs = (pl.k_splits == 1 && 2 * pl.BN * nA <= 512) ? 2 : 1;
-  uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(pl.acc_bufs * pl.BN * nA)) cols <<= 1;
-  pl.tmem_cols = static_cast<int>(cols);
+  // TMEM columns: a power of two >= 32; the CTAs sharing an SM share its 512
+  auto tmem_cols_for = [&](int bufs) {
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(bufs * pl.BN * nA)) c <<= 1;
+    return static_cast<int>(c);
+  };
+  if (tmem_cols_for(pl.acc_bufs) * occ > 512) pl.acc_bufs = 1;
+  pl.tmem_cols = tmem_cols_for(pl.acc_bufs);
   pl.grid = pl.k_splits > 1 ? base * pl.k_splits : std::min(base, num_sms);
   pl.main_tiles = base;
   pl.tail_splits = 1;
@@ -568,7 +675,7 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
     ts = std::min(ts, pl.num_kb * pl.atoms / 4);
     const size_t part_bytes = static_cast<size_t>(nA) * pl.BN * kBM * sizeof(float);
     if (part_bytes > pl.stages * stage_bytes) ts = 1;
-    while (ts > 1 && max_active_clusters(ts, pl.smem_bytes) < rem) --ts;
+    while (ts > 1 && max_active_clusters(occ, ts, pl.smem_bytes) < rem) --ts;
     if (ts >= 2) {
       pl.main_tiles = base - rem;
       pl.tail_kb_per_split = (pl.num_kb + ts - 1) / ts;
@@ -596,6 +703,8 @@ static int launch_one(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorM
   a.n_tiles = pl.n_tiles;
   a.m_tiles = pl.m_tiles;
   a.k_splits = k_splits;
+  a.packed = kPackedWeights ? 1 : 0;
+  a.k_atoms = (pl.K + kBK - 1) / kBK;
   a.kb_per_split = kb_per_split;
   a.num_kb = pl.num_kb;
   a.atoms = pl.atoms;
@@ -619,7 +728,8 @@ static int launch_one(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorM
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = k_splits > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *mapA, pl.dual ? *mapA2 : *mapA, mapB, mapB2, a) ==
+  return cudaLaunchKernelEx(&cfg, tc_kernel(pl.ctas_per_sm), *mapA, pl.dual ? *mapA2 : *mapA, mapB,
+                            mapB2, a) ==
                  cudaSuccess
              ? PE_OK
              : PE_ERR_CUDA;
@@ -630,24 +740,21 @@ int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap*
                    uint32_t* status, cudaStream_t st) {
   if (pl.dual && !mapA2) return PE_ERR_ARG;
   if (pl.bpair && !X_lo) return PE_ERR_ARG;
+  const uint32_t b_box = static_cast<uint32_t>(pl.BN);
   CUtensorMap mapB, mapB2;
   if (!encode_tmap_bf16(&mapB, X, static_cast<uint64_t>(pl.N_cap), static_cast<uint64_t>(pl.K),
-                        static_cast<uint32_t>(pl.BN)))
+                        b_box))
     return PE_ERR_CUDA;
   if (pl.bpair) {
     if (!encode_tmap_bf16(&mapB2, X_lo, static_cast<uint64_t>(pl.N_cap),
-                          static_cast<uint64_t>(pl.K), static_cast<uint32_t>(pl.BN)))
+                          static_cast<uint64_t>(pl.K), b_box))
       return PE_ERR_CUDA;
   } else {
     mapB2 = mapB;
   }
-  // one attribute value (the largest any plan uses) for every launch, so kernels
-  // captured into a graph stay launchable whatever order they replay in
-  if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBudget + 1024)) != cudaSuccess)
-    return PE_ERR_CUDA;
-  cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                       cudaSharedmemCarveoutMaxShared);
+  // one attribute value per instance for every launch, so kernels captured
+  // into a graph stay launchable whatever order they replay in
+  if (tc_prepare(pl.ctas_per_sm) != cudaSuccess) return PE_ERR_CUDA;
   const int base = pl.m_tiles * pl.n_tiles;
   if (pl.k_splits > 1)
     return launch_one(pl, mapA, mapA2, mapB, mapB2, n_rows_dev, epi, status, st, 0, base,
@@ -778,6 +885,52 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// ------------------------------------------------------------------ tile-packed weights
+
+size_t packed_weight_bytes(int M, int K) {
+  const size_t mt = static_cast<size_t>((M + kBM - 1) / kBM);
+  const size_t ka = static_cast<size_t>((K + kBK - 1) / kBK);
+  return mt * ka * kABytes;
+}
+
+// One thread per 16-byte chunk of the packed copy: chunk c of row r of block
+// (m, a) holds W[128m + r][64a + 8c .. 64a + 8c + 7] (zeros past M or K; K is a
+// multiple of 8, so a chunk is all in or all out).
+__global__ void pack_weight_kernel(const uint4* __restrict__ W, int M, int K, int k_atoms,
+                                   size_t n_chunks, uint4* __restrict__ P) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n_chunks;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i & 7);
+    const size_t rowi = i >> 3;  // row of the packed [blocks * 128][64] view
+    const int r = static_cast<int>(rowi % kBM);
+    const size_t blk = rowi / kBM;
+    const int a = static_cast<int>(blk % k_atoms);
+    const int m = static_cast<int>(blk / k_atoms);
+    const int f = m * kBM + r;
+    const int k = a * kBK + c * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (f < M && k < K) v = W[(static_cast<size_t>(f) * K + k) / 8];
+    P[i] = v;
+  }
+}
+
+int pack_weight(const void* W, int M, int K, void* P, cudaStream_t st) {
+  if (!W || !P || M <= 0 || K <= 0 || K % 8) return PE_ERR_ARG;
+  const size_t n_chunks = packed_weight_bytes(M, K) / 16;
+  const int k_atoms = (K + kBK - 1) / kBK;
+  const size_t blocks = std::min<size_t>((n_chunks + 255) / 256, 152u * 16u);
+  pack_weight_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<const uint4*>(W), M, K, k_atoms, n_chunks, static_cast<uint4*>(P));
+  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+}
+
+bool encode_packed_weight_map(CUtensorMap* map, const void* P, int M, int K) {
+  const uint64_t rows = packed_weight_bytes(M, K) / 128;
+  return encode_tmap_bf16(map, P, rows, 64, static_cast<uint32_t>(kBM));
+}
+
+bool gemm_weights_packed() { return kPackedWeights; }
 
 int num_sms_of_current_device() {
   int dev = 0, n = 0;

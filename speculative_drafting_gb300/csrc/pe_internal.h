@@ -40,6 +40,7 @@ struct TcPlan {
   int BN, n_tiles, m_tiles, num_kb, k_splits, kb_per_split, stages, grid, tmem_cols;
   int atoms;  // 64-element K atoms per stage
   int acc_bufs;  // TMEM accumulator buffers (2 = the next tile's MMA overlaps the epilogue)
+  int ctas_per_sm;  // resident CTAs per SM the plan is sized for
   size_t smem_bytes;
   // unsplit plans with several rounds of tiles: the first main_tiles run
   // persistent, the rest as clusters of tail_splits CTAs splitting K
@@ -68,6 +69,20 @@ int launch_gemm_f32(const float* W, const float* W2, const float* X, int M, int 
 bool encode_tmap_bf16(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);
 
+// ------------------------------------------------------------------ tile-packed weights
+// A weight W [M][K] (bf16, row-major) copied into the order the GEMM reads it:
+// tile (m, a) = rows 128m..128m+127 x columns 64a..64a+63 is one contiguous
+// 16 KB block of 128 rows of 128 bytes; blocks run over a (K) within m.  Rows
+// past M and columns past K are zero.  Each weight box the GEMM loads is then
+// one contiguous stretch of DRAM rather than 128 stretches of 128 bytes spread
+// over the matrix (the weights of a narrow step are streamed once, at DRAM speed).
+size_t packed_weight_bytes(int M, int K);
+int pack_weight(const void* W, int M, int K, void* P, cudaStream_t st);
+// tensor map over a packed weight: [m_tiles * k_atoms * 128 rows][64], box 128 x 64
+bool encode_packed_weight_map(CUtensorMap* map, const void* P, int M, int K);
+// whether the GEMM takes its weights packed (the handle packs them when true)
+bool gemm_weights_packed();
+
 int num_sms_of_current_device();
 
 // Read-only views of a handle (defined beside the handle).
@@ -75,5 +90,6 @@ const pe_dims* handle_dims(const pe_handle* h);
 const CUtensorMap* handle_lm_map(const pe_handle* h);
 int handle_num_sms(const pe_handle* h);
 const void* handle_w_lm(const pe_handle* h);
+bool handle_has_layer(const pe_handle* h);
 
 }  // namespace pe

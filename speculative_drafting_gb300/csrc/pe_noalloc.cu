@@ -49,7 +49,7 @@ int scratch_address(void** out) {
 extern "C" int pe_argmax_noalloc(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens,
                                  float* logits, void* stream) {
   using namespace pe;
-  if (!h || !z || !draft_tokens || n_rows < 1) return PE_ERR_ARG;
+  if (!h || !handle_has_layer(h) || !z || !draft_tokens || n_rows < 1) return PE_ERR_ARG;
   if (n_rows > PE_NOALLOC_MAX_ROWS) return PE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(z) & 15u) != 0) return PE_ERR_ARG;
   void* base = nullptr;

@@ -50,15 +50,8 @@ class StepRunner:
                     ("qsl", "prev_tok", "prev_pos", "accepted", "bonus", "block_table", "H_tgt")}
         self.drafter = binding.Drafter(wl.dims, self.w) if wl.has_drafter else None
         if self.drafter is None:
-            # metadata + preparation only: a handle still needs every weight pointer
-            d = wl.dims
-            edt = torch.bfloat16 if dt == "bf16" else torch.float32
-            dummy = torch.zeros(64, dtype=edt, device=device)
-            full = dict(self.w)
-            for k in binding.WEIGHT_FIELDS:
-                full.setdefault(k, dummy)
-            self._dummy = dummy
-            self.drafter = binding.Drafter(d, full)
+            # metadata + preparation only: the layer's weights are left out (NULL)
+            self.drafter = binding.Drafter(wl.dims, self.w)
         self.meta = binding.Meta(self.B, self.T_in, K, device)
         edt = torch.bfloat16 if dt == "bf16" else torch.float32
         d = wl.dims.d

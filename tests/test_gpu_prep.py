@@ -72,3 +72,24 @@ def test_status_flags_bad_inputs_without_faulting():
     r2.prepare()
     torch.cuda.synchronize()
     assert r2.status()[0] == 0
+
+
+def test_preparation_only_handle_refuses_layer_calls():
+    """A handle made without the layer's weights (they are NULL) prepares inputs
+    and refuses the layer's calls on the host, before anything is enqueued."""
+    torch = cuda_or_skip()
+    from speculative_drafting_gb300 import binding
+    wl, b, w, kc, vc, r = setup("meta_prep_b64", want_logits=False, kv=False)
+    assert "w_lm" not in r.drafter.weights
+    z = torch.zeros(8, wl.dims.d, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(8, dtype=torch.int32, device="cuda")
+    with pytest.raises(binding.PeError) as e:
+        r.drafter.argmax_noalloc(z, 8, out)
+    assert e.value.code == binding.PE_ERR_ARG
+    with pytest.raises(binding.PeError) as e:
+        r.drafter.test_projection(5, z, 8, torch.zeros(8, 4, device="cuda"))
+    assert e.value.code == binding.PE_ERR_ARG
+    r.prepare()
+    torch.cuda.synchronize()
+    st, _ = r.status()
+    assert st == 0

@@ -57,3 +57,50 @@ def test_projection_matches_matmul(name, which, n):
     assert np.all(np.isfinite(got))
     err = np.abs(got - ref)
     assert np.all(err <= tol), f"max err {err.max():.3g}"
+
+
+# PE_PROJ_PERSISTENT / PE_PROJ_PAIR (pe_testing.h)
+PERSISTENT, PAIR = 0x100, 0x200
+
+
+@pytest.mark.parametrize("name", ["small_prenorm", "small_postnorm_hd128"])
+@pytest.mark.parametrize("which", list(PROJ))
+@pytest.mark.parametrize("n", [100, 256, 300, 513])
+@pytest.mark.parametrize("flags", [PERSISTENT, PAIR, PERSISTENT | PAIR])
+def test_projection_schedules_and_pairs(name, which, n, flags):
+    """The persistent schedule (several CTAs per SM for narrow token tiles, the
+    ragged last round split over K) and bf16-pair operands, against the float64
+    product of the operand the kernel was given."""
+    torch = cuda_or_skip()
+    wl, b, w, kc, vc, r = setup(name, want_logits=False, kv=False)
+    dm = wl.dims
+    M, Kd, wname = _shape(dm, which)
+    from speculative_drafting_gb300.workloads import f32_to_bf16_bits
+    g = np.random.default_rng(n * 37 + PROJ[which] + flags)
+    X = g.standard_normal((n, Kd)).astype(np.float32)
+    hi = f32_to_bf16_bits(X)
+    x64 = f64(hi, "bf16")
+    Xh = hi
+    if flags & PAIR:
+        lo = f32_to_bf16_bits((X.astype(np.float64) - x64).astype(np.float32))
+        x64 = x64 + f64(lo, "bf16")
+        Xh = np.concatenate([hi, lo], axis=0)
+    Xd = runner.to_device(Xh, "bf16")
+    out_dt = torch.bfloat16 if which == "swiglu" else torch.float32
+    out = torch.full((n, M), float("nan"), dtype=out_dt, device="cuda")
+    ws = r.drafter.test_projection(PROJ[which] | flags, Xd, n, out)
+    torch.cuda.synchronize()
+    st, _ = r.drafter.read_status(ws)
+    assert st == 0, hex(st)
+    if which == "swiglu":
+        ref = O.bf16_round(O.silu(O.linear(x64, f64(w["w_gate"], "bf16"))) *
+                           O.linear(x64, f64(w["w_up"], "bf16")))
+        got = f64(host(out), "bf16")
+        tol = 2 ** -7 * np.abs(ref) + 1e-6
+    else:
+        ref = O.linear(x64, f64(w[wname], "bf16"))
+        got = host(out).astype(np.float64)
+        tol = 1e-5 * np.sqrt(Kd) * 0.02 * 4 + 1e-5 * np.abs(ref)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref)
+    assert np.all(err <= tol), f"max err {err.max():.3g}"
