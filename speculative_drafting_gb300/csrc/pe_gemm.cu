@@ -554,7 +554,9 @@ static cudaError_t tc_prepare(int occ) {
 }
 
 // How many clusters of `cs` CTAs of the `occ` instance with `smem` bytes each
-// can be resident at once.
+// can be resident at once.  The query places one CTA of this kernel per SM (as
+// the per-SM query does); `occ` such placements side by side fit as well, so
+// its answer times `occ` is a lower bound on what the SMs hold.
 static int max_active_clusters(int occ, int cs, size_t smem) {
   static std::mutex mu;
   static std::map<std::pair<std::pair<int, int>, size_t>, int> cache;
@@ -579,8 +581,8 @@ static int max_active_clusters(int occ, int cs, size_t smem) {
     cudaGetLastError();
     n = 0;
   }
-  cache[key] = n;
-  return n;
+  cache[key] = n * occ;
+  return n * occ;
 }
 
 TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split) {
