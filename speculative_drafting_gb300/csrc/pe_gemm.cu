@@ -486,11 +486,25 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
         const int ew = warp - 2, et = threadIdx.x - 64;
         for (int j = static_cast<int>(rank); j < p.BN; j += p.k_splits) {
           if (jt + j >= n_rows) break;  // uniform over the epilogue warps
+          // all the splits' loads go out before the first add (they are
+          // independent); the sum still runs in rank order
+          float pv[kMaxClusterSplits], pv2[kMaxClusterSplits];
+          const uint32_t o1 = base + static_cast<uint32_t>((j * kBM + fl) * 4);
+          const uint32_t o2 = base + static_cast<uint32_t>(((p.BN + j) * kBM + fl) * 4);
+#pragma unroll
+          for (int r = 0; r < kMaxClusterSplits; ++r) {
+            if (r < p.k_splits) {
+              pv[r] = ld_dsmem_f32(o1, r);
+              pv2[r] = p.dual ? ld_dsmem_f32(o2, r) : 0.f;
+            }
+          }
           float v = 0.f, v2 = 0.f;
-          for (int r = 0; r < p.k_splits; ++r) {
-            v += ld_dsmem_f32(base + static_cast<uint32_t>((j * kBM + fl) * 4), r);
-            if (p.dual)
-              v2 += ld_dsmem_f32(base + static_cast<uint32_t>(((p.BN + j) * kBM + fl) * 4), r);
+#pragma unroll
+          for (int r = 0; r < kMaxClusterSplits; ++r) {
+            if (r < p.k_splits) {
+              v += pv[r];
+              v2 += pv2[r];
+            }
           }
           if (p.epi.mode == EPI_ARGMAX) {
             // max over this tile's 128 features of token jt + j
