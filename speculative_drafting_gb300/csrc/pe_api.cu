@@ -533,9 +533,7 @@ int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, fl
   if (ws_bytes < L.total) return PE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned long long* keys = at<unsigned long long>(ws, L.amax);
-  if (cudaMemsetAsync(keys, 0, static_cast<size_t>(n_rows) * sizeof(unsigned long long), st) !=
-      cudaSuccess)
-    return PE_ERR_CUDA;
+  if (launch_zero_keys(keys, n_rows, st) != PE_OK) return PE_ERR_CUDA;
   Epilogue e;
   e.mode = EPI_ARGMAX;
   e.amax = keys;

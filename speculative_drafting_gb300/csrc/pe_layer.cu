@@ -9,6 +9,8 @@
 // KV write: non-rejected rows store k (after RoPE) and v at their slot; rejected
 // rows never reach this kernel (their slot is PADDING_SLOT_ID = -1, "P-EAGLE:
 // parallel speculative decoding in vLLM", KV cache and CUDA graphs).
+#include <algorithm>
+
 #include "pe_common.cuh"
 #include "pe_prep.h"
 
@@ -170,7 +172,25 @@ int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st) {
   return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 
-// ------------------------------------------------------------------ argmax keys -> ids
+// ------------------------------------------------------------------ argmax keys
+
+// A memset node would end the chain of programmatic launches; this kernel keeps
+// it, so the LM-head GEMM after it sets up and pulls its first weights into L2
+// while the kernels before finish.
+__global__ void zero_keys_kernel(unsigned long long* __restrict__ keys, int n) {
+  pdl_trigger();
+  pdl_wait();  // the previous argmax finalisation may still be reading them
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) keys[i] = 0ull;
+}
+
+int launch_zero_keys(unsigned long long* keys, int n, cudaStream_t st) {
+  if (n <= 0) return PE_OK;
+  const int blocks = std::min((n + 255) / 256, 64);
+  return launch_pdl(zero_keys_kernel, dim3(blocks), dim3(256), 0, st, keys, n) == cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
+}
+
 
 __global__ void argmax_finalize_kernel(const unsigned long long* __restrict__ keys, int n,
                                        int32_t* __restrict__ out) {

@@ -57,9 +57,7 @@ extern "C" int pe_argmax_noalloc(pe_handle* h, const void* z, int n_rows, int32_
   if (rc != PE_OK) return rc;
   unsigned long long* keys = static_cast<unsigned long long*>(base);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(keys, 0, static_cast<size_t>(n_rows) * sizeof(unsigned long long), st) !=
-      cudaSuccess)
-    return PE_ERR_CUDA;
+  if (launch_zero_keys(keys, n_rows, st) != PE_OK) return PE_ERR_CUDA;
   const pe_dims& d = *handle_dims(h);
   Epilogue e;
   e.mode = EPI_ARGMAX;

@@ -116,7 +116,10 @@ void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, 
 size_t attention_scratch_bytes(int B, int K, int H, int hd, int n_splits);
 int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st);
 
-// ---------------------------------------------------------------- argmax keys -> ids
+// ---------------------------------------------------------------- argmax keys
+// keys[0..n) = 0 (a kernel, so the LM head that follows can start early)
+int launch_zero_keys(unsigned long long* keys, int n, cudaStream_t st);
+// keys -> ids
 int launch_argmax_finalize(const unsigned long long* keys, int n, int32_t* out, cudaStream_t st);
 
 }  // namespace pe
