@@ -28,7 +28,11 @@ constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBK = 64;   // reduction elements per k-block: one 128-byte swizzle row
 constexpr int kMaxStages = 12;
 constexpr size_t kSmemBudget = 212 * 1024;  // dynamic shared memory for the stage ring
-constexpr int kPrefetchKb = 16;             // k-blocks of weights pulled into L2 early
+// k-blocks of weights a CTA pulls into L2 before its dependency wait.  Kept
+// small: the SM's TMA unit works the prefetches off before the CTA's own loads,
+// and deep prefetches delayed them (measured, step at B=1: 16 k-blocks 328 us,
+// 4: 303 us, 2: 301 us, none: 306 us).
+constexpr int kPrefetchKb = 2;
 constexpr int kMaxClusterSplits = 8;        // portable cluster size
 // Weights in tile order (one contiguous 16 KB block per weight box) or row-major
 // (measured, LM head at B=1 with two CTAs per SM: 188 us packed, 192 us not).
