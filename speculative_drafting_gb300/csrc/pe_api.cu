@@ -477,7 +477,7 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   aa.max_blocks = max_blocks;
   aa.num_blocks = num_blocks;
   plan_attention(B, d.n_kv_heads, d.K, d.n_heads, d.head_dim, max_blocks, d.block_size,
-                 h->num_sms, aa.n_splits, aa.split_len);
+                 h->num_sms, aa.n_splits, aa.split_len, aa.cluster);
   aa.q = q_s;
   aa.k_cache = k_cache;
   aa.v_cache = v_cache;

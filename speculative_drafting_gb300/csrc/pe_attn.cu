@@ -9,8 +9,10 @@
 // a 3-chunk ring; compute warps own 16 query rows and half of every 64-key
 // chunk; S = Q K^T and O += P V run on warp-level bf16 mma.sync with fp32
 // accumulators and an online softmax in the exp2 domain (P enters the second
-// product as a hi + lo bf16 pair).  Each split writes unnormalised partials; a combine
-// kernel merges the splits (flash-decoding style).
+// product as a hi + lo bf16 pair).  Each split leaves an unnormalised partial
+// (flash-decoding style).  While the splits of a (request, KV head) fit one
+// thread-block cluster they merge there, through distributed shared memory;
+// otherwise the partials go to global memory and a combine kernel merges them.
 //
 // fp32: one CTA per (sample row, query head), SIMT dot products, online softmax.
 #include <algorithm>
@@ -27,6 +29,12 @@ constexpr int kMaxComputeWarps = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplits = 128;       // key splits per (request, KV head)
 constexpr long kMaxSplitKeys = 2048;  // keys per split, at most
+// Cluster mode: the splits of one (request, KV head) are one thread-block
+// cluster (non-portable size up to 16) and merge in distributed shared memory.
+// Chosen while its splits stay at most kClusterSplitKeys keys long, or at most
+// a quarter longer than the splits the global-memory merge would use.
+constexpr int kMaxAttnCluster = 16;
+constexpr long kClusterSplitKeys = 1024;
 
 // Thread roles of the bf16 attention CTA: compute warps 0..cw-1 (row warp
 // w % rw, key group w / rw), then one producer warp.
@@ -109,42 +117,59 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1))
   volatile int* abort_flag = &abort_sh;
 
   if (warp == sh.cw) {
-    // ---------------- producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int c = 0; c < n_chunks && !*abort_flag; ++c) {
-        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
-          abort_sh = 1;
-          set_status(a.status, PE_ST_TIMEOUT);
-          break;
-        }
-        uint32_t mask = 0;
-        int row[4];
-        for (int q = 0; q < 4; ++q) {
-          const int t = t0 + c * kKC + q * 16;
-          row[q] = 0;
-          if (t >= t1) continue;
+    // ---------------- producer warp: its lanes look up the KV rows of 32
+    // 16-key groups (8 chunks) at once; lane 0 issues the loads
+    int stage = 0;
+    uint32_t phase = 0;
+    bool go = true;
+    for (int cb = 0; cb < n_chunks && go; cb += 8) {
+      int rowv = -1;  // this lane's group: cache row of its first key, -1 = none
+      {
+        const int t = t0 + (cb * 4 + lane) * 16;
+        if (t < t1) {
           const int blk = a.block_table[static_cast<size_t>(r) * a.max_blocks + t / a.bs];
-          if (blk < 0 || blk >= a.num_blocks) {
+          if (blk < 0 || blk >= a.num_blocks)
             set_status(a.status, PE_ST_BLOCK_RANGE);
-            continue;
-          }
-          row[q] = (blk * a.G + g) * a.bs + t % a.bs;
-          mask |= 1u << q;
+          else
+            rowv = (blk * a.G + g) * a.bs + t % a.bs;
         }
-        mask_sh[stage] = mask;
-        mbar_arrive_expect_tx(&full_bar[stage],
-                              static_cast<uint32_t>(__popc(mask)) * 2u * HALVES * GROUP_BYTES);
-        uint8_t* kd = ring + stage * STAGE;
-        uint8_t* vd = kd + TILE;
+      }
+      const int c_end = min(n_chunks, cb + 8);
+      for (int c = cb; c < c_end; ++c) {
+        int row[4];
+        uint32_t mask = 0;
+#pragma unroll
         for (int q = 0; q < 4; ++q) {
-          if (!(mask & (1u << q))) continue;
-          for (int hh = 0; hh < HALVES; ++hh) {
-            const int off = hh * (kKC * 128) + q * GROUP_BYTES;
-            tma_load_2d(kd + off, &kmap, &full_bar[stage], hh * 64, row[q], policy_evict_first());
-            tma_load_2d(vd + off, &vmap, &full_bar[stage], hh * 64, row[q], policy_evict_first());
+          row[q] = __shfl_sync(0xffffffffu, rowv, (c - cb) * 4 + q);
+          if (row[q] >= 0) mask |= 1u << q;
+        }
+        int ok = 1;
+        if (lane == 0) {
+          if (*abort_flag || !mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            abort_sh = 1;
+            set_status(a.status, PE_ST_TIMEOUT);
+            ok = 0;
+          } else {
+            mask_sh[stage] = mask;
+            mbar_arrive_expect_tx(&full_bar[stage],
+                                  static_cast<uint32_t>(__popc(mask)) * 2u * HALVES * GROUP_BYTES);
+            uint8_t* kd = ring + stage * STAGE;
+            uint8_t* vd = kd + TILE;
+            for (int q = 0; q < 4; ++q) {
+              if (!(mask & (1u << q))) continue;
+              for (int hh = 0; hh < HALVES; ++hh) {
+                const int off = hh * (kKC * 128) + q * GROUP_BYTES;
+                tma_load_2d(kd + off, &kmap, &full_bar[stage], hh * 64, row[q],
+                            policy_evict_first());
+                tma_load_2d(vd + off, &vmap, &full_bar[stage], hh * 64, row[q],
+                            policy_evict_first());
+              }
+            }
           }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          go = false;
+          break;
         }
         if (++stage == kStages) {
           stage = 0;
@@ -310,9 +335,11 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1))
     }
     named_bar_sync(1, n_compute);
     if (kgi == 0) {
+      // merged (m, l) of rows ra, rb (all four lanes of a row read the parked
+      // group-1 values before any lane overwrites them below)
+      float mh[2], lh[2], w0h[2], w1h[2];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int rr = hf ? rb : ra;
         float m = hf ? m_b : m_a, l = hf ? l_b : l_a;
         float w0 = 1.f, w1 = 0.f;
         const int rl = rw * 16 + gq + hf * 8;
@@ -324,29 +351,102 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1))
           l = l * w0 + l1 * w1;
           m = M;
         }
-        if (rr >= rows) continue;
-        const size_t idx =
-            (static_cast<size_t>(split) * n_samp + row_sample(rr)) * a.H + row_head(rr);
-        float* po = a.part_o + idx * HD;
+        mh[hf] = m;
+        lh[hf] = l;
+        w0h[hf] = w0;
+        w1h[hf] = w1;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int rr = hf ? rb : ra;
+        const int rl = rw * 16 + gq + hf * 8;
+        // cluster: this split's partial replaces the parked values in place
+        // (each element is read and written by the same lane); else global
+        float* po = mo + rl * HD;
+        float* pml = mml + rl * 2;
+        if (!a.cluster) {
+          if (rr >= rows) continue;
+          const size_t idx =
+              (static_cast<size_t>(split) * n_samp + row_sample(rr)) * a.H + row_head(rr);
+          po = a.part_o + idx * HD;
+          pml = a.part_ml + idx * 2;
+        }
 #pragma unroll
         for (int nd = 0; nd < HD / 8; ++nd) {
           const int d = nd * 8 + tq * 2;
-          float v0 = o[nd][hf * 2] * w0, v1 = o[nd][hf * 2 + 1] * w0;
+          float v0 = o[nd][hf * 2] * w0h[hf], v1 = o[nd][hf * 2 + 1] * w0h[hf];
           if (KG == 2) {
-            v0 += mo[rl * HD + d] * w1;
-            v1 += mo[rl * HD + d + 1] * w1;
+            v0 += mo[rl * HD + d] * w1h[hf];
+            v1 += mo[rl * HD + d + 1] * w1h[hf];
           }
           *reinterpret_cast<float2*>(po + d) = make_float2(v0, v1);
         }
         if (tq == 0) {
-          a.part_ml[idx * 2] = m;
-          a.part_ml[idx * 2 + 1] = l;
+          pml[0] = mh[hf];
+          pml[1] = lh[hf];
         }
       }
     }
   }
   // the producer may still be waiting for an empty slot only after an abort
   __syncthreads();
+  if (!a.cluster) return;
+
+  // ---------------- merge of the splits inside the cluster
+  // Every split's partial sits at the start of its ring: o [row][HD] (fp32,
+  // unnormalised), then (m, l) per row.  CTA `rank` merges rows rank, rank + S,
+  // ...: out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j.
+  cluster_sync_all();
+  {
+    const int S = static_cast<int>(gridDim.x);
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int nw = static_cast<int>(blockDim.x >> 5);
+    const uint32_t o_base = smem_u32(ring);
+    const uint32_t ml_base = o_base + static_cast<uint32_t>(sh.rw * 16 * HD * 4);
+    constexpr int DPL = HD / 32;  // dims per lane
+    for (int i = warp;; i += nw) {
+      const int rr = rank + i * S;
+      if (rr >= rows) break;
+      float mj = -INFINITY, lj = 0.f;
+      if (lane < S) {
+        mj = ld_dsmem_f32(ml_base + static_cast<uint32_t>(rr * 2) * 4u, lane);
+        lj = ld_dsmem_f32(ml_base + static_cast<uint32_t>(rr * 2 + 1) * 4u, lane);
+      }
+      const float M = warp_max(mj);
+      const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+      const float den = warp_sum(wj * lj);
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      float acc[DPL];
+#pragma unroll
+      for (int q = 0; q < DPL; ++q) acc[q] = 0.f;
+      for (int j0 = 0; j0 < S; j0 += 4) {
+        // four splits' loads in flight before their adds (in split order)
+        float v[4][DPL];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int q = 0; q < DPL; ++q)
+            v[u][q] = (j0 + u < S) ? ld_dsmem_f32(o_base + static_cast<uint32_t>(rr * HD + lane + 32 * q) * 4u,
+                                                  static_cast<uint32_t>(j0 + u))
+                                   : 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wj, (j0 + u) & 31);
+          if (j0 + u < S)
+#pragma unroll
+            for (int q = 0; q < DPL; ++q) acc[q] += w * v[u][q];
+        }
+      }
+      const size_t samp = static_cast<size_t>(r) * a.K + rr / HG;
+      const int head = g * HG + rr % HG;
+      bf16* out = static_cast<bf16*>(a.out) + (samp * a.H + head) * HD;
+#pragma unroll
+      for (int q = 0; q < DPL; ++q) out[lane + 32 * q] = __float2bfloat16_rn(acc[q] * inv);
+    }
+  }
+  // no CTA leaves while another may still read its shared memory
+  cluster_sync_all();
 }
 
 // out[s][h*hd + d] = sum_j 2^(m_j - M) o_j[d] / sum_j 2^(m_j - M) l_j.
@@ -473,15 +573,24 @@ int attention_split_count(int B, int G, int max_blocks, int bs, int num_sms) {
 }
 
 void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, int num_sms,
-                    int& n_splits, int& split_len) {
+                    int& n_splits, int& split_len, int& cluster) {
   (void)K;
   (void)H;
   (void)hd;
   const long Lmax = static_cast<long>(max_blocks) * bs;
   const long chunks = std::max<long>(1, (Lmax + kKC - 1) / kKC);
   const long ns = attention_split_count(B, G, max_blocks, bs, num_sms);
-  const long chunks_per = (chunks + ns - 1) / ns;
-  split_len = static_cast<int>(chunks_per * kKC);
+  // as many splits as one cluster takes, if each stays short enough
+  const long nc = std::min<long>(ns, kMaxAttnCluster);
+  const long len_c = (chunks + nc - 1) / nc * kKC;
+  const long len_g = (chunks + ns - 1) / ns * kKC;
+  if (len_c <= std::max(kClusterSplitKeys, len_g + len_g / 4)) {
+    cluster = 1;
+    split_len = static_cast<int>(len_c);
+  } else {
+    cluster = 0;
+    split_len = static_cast<int>(len_g);
+  }
   n_splits = static_cast<int>((Lmax + split_len - 1) / split_len);
   if (n_splits < 1) n_splits = 1;
 }
@@ -523,9 +632,40 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
   else
     return PE_ERR_UNSUPPORTED;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-  if (launch_pdl(kern, grid, block, smem, st, kmap, vmap, a) != cudaSuccess) return PE_ERR_CUDA;
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+  if (a.cluster) {
+    // one cluster per (request, KV head): the splits merge in shared memory
+    if (a.n_splits > kMaxAttnCluster) return PE_ERR_UNSUPPORTED;
+    if (a.n_splits > 8)
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(a.n_splits);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    int n_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&n_clusters, (void*)kern, &cfg) == cudaSuccess &&
+        n_clusters > 0)
+      return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a) == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+    cudaGetLastError();
+    // the SMs cannot hold such a cluster: the same splits through global memory
+    // (the workspace holds partials for at least this many splits)
+  }
+  AttnArgs ag = a;
+  ag.cluster = 0;
+  if (launch_pdl(kern, grid, block, smem, st, kmap, vmap, ag) != cudaSuccess) return PE_ERR_CUDA;
   return launch_pdl(attn_combine_kernel<bf16>, dim3(a.B * a.K * a.H), dim3(std::min(a.hd, 128)), 0,
-                    st, a) == cudaSuccess
+                    st, ag) == cudaSuccess
              ? PE_OK
              : PE_ERR_CUDA;
 }

@@ -100,6 +100,10 @@ int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st);
 struct AttnArgs {
   int B, K, H, G, hd, bs, max_blocks, num_blocks;
   int n_splits, split_len;
+  // 1: the n_splits CTAs of one (request, KV head) are a thread-block cluster
+  // and merge their partials in distributed shared memory (part_o / part_ml and
+  // the combine kernel unused); 0: partials in global memory + combine kernel
+  int cluster;
   const void* q;  // [B*K][H][hd]
   const void* k_cache;
   const void* v_cache;
@@ -112,7 +116,7 @@ struct AttnArgs {
 };
 int attention_split_count(int B, int G, int max_blocks, int bs, int num_sms);
 void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, int num_sms,
-                    int& n_splits, int& split_len);
+                    int& n_splits, int& split_len, int& cluster);
 size_t attention_scratch_bytes(int B, int K, int H, int hd, int n_splits);
 int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st);
 
