@@ -26,8 +26,12 @@ enum {
   /* flags OR'ed into `which` */
   PE_PROJ_PERSISTENT = 0x100, /* never split K over a cluster: the persistent
                                  schedule with its tail split */
-  PE_PROJ_PAIR = 0x200        /* bf16 only: X holds n rows of high parts followed
+  PE_PROJ_PAIR = 0x200,       /* bf16 only: X holds n rows of high parts followed
                                  by n rows of low parts; the operand is hi + lo */
+  PE_PROJ_PARTIAL = 0x400     /* not with PE_PROJ_SWIGLU: each K split stores its
+                                 partial sum, out = float [16][n][M] (split k at
+                                 out + k*n*M; tiles past the split count are left
+                                 as they were); the result is their sum */
 };
 
 /* Workspace bytes pe_test_projection needs for n_rows rows (0 on bad input). */

@@ -49,9 +49,28 @@ GemmShape gemm_shape(const pe_handle* h, int id) {
   }
 }
 
-TcPlan plan_of(const pe_handle* h, int id, int N, bool bpair, bool allow_split = true) {
+TcPlan plan_of(const pe_handle* h, int id, int N, bool bpair, bool allow_split = true,
+               bool partial = false) {
   const GemmShape s = gemm_shape(h, id);
-  return plan_gemm_tc(s.M, s.K, N, s.dual, bpair ? 1 : 0, h->num_sms, allow_split);
+  return plan_gemm_tc(s.M, s.K, N, s.dual, bpair ? 1 : 0, h->num_sms, allow_split, partial);
+}
+
+// The projections whose K splits store partial sums (EPI_PARTIAL_F32) for the
+// kernel after them to add, and whether their token operand is a bf16 pair.
+bool partial_gemm(int id) { return id == G_FC || id == G_QKV || id == G_O || id == G_DOWN; }
+bool pair_operand(int id) { return id == G_QKV || id == G_GATEUP || id == G_DOWN; }
+
+// Bytes of partial sums projection `id` stores over any N <= N_max token rows
+// (the split count rises as N falls, so every N is walked).
+size_t partial_bytes_bound(const pe_handle* h, int id, int N_max) {
+  const GemmShape s = gemm_shape(h, id);
+  if (!is_bf16(h)) return static_cast<size_t>(N_max) * s.M * sizeof(float);
+  size_t best = 0;
+  for (int n = 1; n <= N_max; ++n) {
+    const TcPlan p = plan_of(h, id, n, pair_operand(id), true, true);
+    best = std::max(best, static_cast<size_t>(p.k_splits) * n * s.M * sizeof(float));
+  }
+  return best;
 }
 
 // Attention split partials, bounded over every batch size <= B (the split count
@@ -71,10 +90,12 @@ size_t attn_scratch_bound(const pe_handle* h, int B, int max_blocks) {
 
 struct Layout {
   // x: fc output (fp32); u / u_lo: QKV operand (bf16 pair; fp32 in fp32 mode);
-  // qkv (fp32); q_s; x_s: residual rows (fp32); attn; r: attention residual sum
-  // (fp32); a / a_lo / a_f: MLP operand pair and its fp32 value; h / h_lo:
-  // SwiGLU product pair; y: MLP residual sum (fp32); amax: argmax keys
-  size_t status, x, u, u_lo, qkv, q_s, x_s, attn, r, a, a_lo, a_f, h, h_lo, y, amax, attn_part;
+  // q_s; x_s: residual rows (fp32); attn; r: attention residual sum (fp32);
+  // a / a_lo / a_f: MLP operand pair and its fp32 value; h / h_lo: SwiGLU
+  // product pair; part: the split partial sums of fc, QKV, O and down (one at
+  // a time: each is read by the next kernel before the next projection stores);
+  // amax: argmax keys
+  size_t status, x, u, u_lo, q_s, x_s, attn, r, a, a_lo, a_f, h, h_lo, part, amax, attn_part;
   size_t total;
 };
 
@@ -100,7 +121,6 @@ Layout layout_of(const pe_handle* h, int B, int T_in, int max_blocks) {
   L.x = take(static_cast<size_t>(T_out) * d.d * f4);
   L.u = take(static_cast<size_t>(T_out) * d.d * f4);
   L.u_lo = take(static_cast<size_t>(T_out) * d.d * e);
-  L.qkv = take(static_cast<size_t>(T_out) * QKV * f4);
   L.q_s = take(static_cast<size_t>(NS) * Hd * e);
   L.x_s = take(static_cast<size_t>(NS) * d.d * f4);
   L.attn = take(static_cast<size_t>(NS) * Hd * e);
@@ -110,7 +130,11 @@ Layout layout_of(const pe_handle* h, int B, int T_in, int max_blocks) {
   L.a_f = take(static_cast<size_t>(NS) * d.d * f4);
   L.h = take(static_cast<size_t>(NS) * d.inter * f4);
   L.h_lo = take(static_cast<size_t>(NS) * d.inter * e);
-  L.y = take(static_cast<size_t>(NS) * d.d * f4);
+  L.part = take(std::max(std::max(partial_bytes_bound(h, G_FC, T_out),
+                                  partial_bytes_bound(h, G_QKV, T_out)),
+                         std::max(partial_bytes_bound(h, G_O, NS),
+                                  partial_bytes_bound(h, G_DOWN, NS))));
+  (void)QKV;
   L.amax = take(static_cast<size_t>(NS) * sizeof(unsigned long long));
   L.attn_part = take(attn_scratch_bound(h, B, max_blocks));
   L.total = off;
@@ -165,10 +189,13 @@ int check_meta(const pe_meta* m) {
 
 // One projection of the step, on the tensor cores (bf16) or SIMT (fp32).
 // X_lo: the low half of a bf16-pair operand (bf16 only; nullable).
+// epi.mode EPI_PARTIAL_F32: *n_parts receives the number of partial tiles stored.
 int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
              const int* n_rows_dev, const Epilogue& epi, void* ws, const Layout& L,
-             cudaStream_t st, bool allow_split = true) {
+             cudaStream_t st, bool allow_split = true, int* n_parts = nullptr) {
   const GemmShape s = gemm_shape(h, id);
+  const bool partial = epi.mode == EPI_PARTIAL_F32;
+  if (n_parts) *n_parts = 1;
   if (!is_bf16(h)) {
     const pe_weights& w = h->w;
     const void* W = id == G_FC ? w.w_fc : id == G_QKV ? w.w_qkv : id == G_O ? w.w_o
@@ -177,7 +204,8 @@ int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
     return launch_gemm_f32(static_cast<const float*>(W), static_cast<const float*>(W2),
                            static_cast<const float*>(X), s.M, s.K, N_cap, n_rows_dev, epi, st);
   }
-  const TcPlan p = plan_of(h, id, N_cap, X_lo != nullptr, allow_split);
+  const TcPlan p = plan_of(h, id, N_cap, X_lo != nullptr, allow_split, partial);
+  if (n_parts) *n_parts = p.k_splits;
   const CUtensorMap* mA = id == G_FC ? &h->m_fc : id == G_QKV ? &h->m_qkv : id == G_O ? &h->m_o
                         : id == G_GATEUP ? &h->m_gate : id == G_DOWN ? &h->m_down : &h->m_lm;
   const CUtensorMap* mA2 = id == G_GATEUP ? &h->m_up : nullptr;
@@ -396,7 +424,7 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   float* x = at<float>(ws, L.x);
   void* u = at<void>(ws, L.u);
   bf16_t* u_lo = bf ? at<bf16_t>(ws, L.u_lo) : nullptr;
-  float* qkv = at<float>(ws, L.qkv);
+  float* part = at<float>(ws, L.part);
   void* q_s = at<void>(ws, L.q_s);
   float* x_s = at<float>(ws, L.x_s);
   void* attn = at<void>(ws, L.attn);
@@ -406,13 +434,20 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   float* a_f = at<float>(ws, L.a_f);
   void* hm = at<void>(ws, L.h);
   bf16_t* h_lo = bf ? at<bf16_t>(ws, L.h_lo) : nullptr;
-  float* y = at<float>(ws, L.y);
   int rc;
-  auto norm = [&](const float* in, const void* gamma, int apply, void* out, bf16_t* out_lo,
+  // a row norm over the sum of a projection's n_parts partial tiles (plus an
+  // optional fp32 residual); sum_out (nullable) receives that fp32 sum
+  auto norm = [&](const float* parts, int n_parts, size_t part_stride, const float* resid,
+                  float* sum_out, const void* gamma, int apply, void* out, bf16_t* out_lo,
                   float* out_f32, int rows, const int* n_rows_dev) {
     RowNormArgs n{};
-    n.x = in;
+    n.x = parts;
     n.ld_x = d.d;
+    n.n_parts = n_parts;
+    n.part_stride = part_stride;
+    n.resid = resid;
+    n.ld_resid = d.d;
+    n.sum_out = sum_out;
     n.gamma = gamma;
     n.apply_norm = apply;
     n.out = out;
@@ -425,22 +460,31 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
     n.n_rows_dev = n_rows_dev;
     return launch_rownorm(n, dt, st);
   };
+  // each projection below but gate/up stores the partial sums of its K splits;
+  // the kernel after it adds them (in split order) as it reads them
+  auto partial_epi = [&](int rows, int M) {
+    Epilogue ep;
+    ep.mode = EPI_PARTIAL_F32;
+    ep.out = part;
+    ep.ld_out = M;
+    ep.part_stride = static_cast<size_t>(rows) * M;
+    return ep;
+  };
+  int np = 1;
   // fc: x = A W_fc^T over the non-rejected rows (fp32)
-  Epilogue e;
-  e.mode = EPI_STORE_F32;
-  e.out = x;
-  e.ld_out = d.d;
-  if ((rc = run_gemm(h, G_FC, A, nullptr, T_out, meta->n_valid, e, ws, L, st)) != PE_OK) return rc;
-  // QKV operand u: RMSNorm(x; gamma_in) (pre-norm) or x (post-norm), as a bf16 pair
-  if ((rc = norm(x, h->w.gamma_in, d.post_norm ? 0 : 1, u, u_lo, nullptr, T_out, meta->n_valid)) !=
+  Epilogue e = partial_epi(T_out, d.d);
+  if ((rc = run_gemm(h, G_FC, A, nullptr, T_out, meta->n_valid, e, ws, L, st, true, &np)) !=
       PE_OK)
     return rc;
-  // QKV (fp32, RoPE follows)
-  e = Epilogue();
-  e.mode = EPI_STORE_F32;
-  e.out = qkv;
-  e.ld_out = QKV;
-  if ((rc = run_gemm(h, G_QKV, u, u_lo, T_out, meta->n_valid, e, ws, L, st)) != PE_OK) return rc;
+  // x (kept in fp32 for the residual) and the QKV operand u: RMSNorm(x; gamma_in)
+  // (pre-norm) or x (post-norm), as a bf16 pair
+  if ((rc = norm(part, np, e.part_stride, nullptr, x, h->w.gamma_in, d.post_norm ? 0 : 1, u, u_lo,
+                 nullptr, T_out, meta->n_valid)) != PE_OK)
+    return rc;
+  // QKV (partial sums; RoPE adds them)
+  e = partial_epi(T_out, QKV);
+  if ((rc = run_gemm(h, G_QKV, u, u_lo, T_out, meta->n_valid, e, ws, L, st, true, &np)) != PE_OK)
+    return rc;
   // RoPE, KV write at the non-rejected slots, sample-row q and residual rows
   RopeArgs ra{};
   ra.T_out = T_out;
@@ -452,7 +496,9 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   ra.d = d.d;
   ra.bs = d.block_size;
   ra.num_blocks = num_blocks;
-  ra.qkv = qkv;
+  ra.qkv = part;
+  ra.n_parts = np;
+  ra.part_stride = e.part_stride;
   ra.x = x;
   ra.n_valid = meta->n_valid;
   ra.valid_rows = meta->valid_rows;
@@ -490,19 +536,15 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   aa.out = attn;
   aa.status = status;
   if ((rc = launch_attention(aa, dt, st)) != PE_OK) return rc;
-  // O projection + residual: r = x_s + attn W_o^T (fp32)
-  e = Epilogue();
-  e.mode = EPI_RESID_F32;
-  e.out = r;
-  e.ld_out = d.d;
-  e.resid = x_s;
-  e.ld_resid = d.d;
-  if ((rc = run_gemm(h, G_O, attn, nullptr, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
-  // MLP operand: post-norm a = RMSNorm(r; gamma_post), which is also the MLP
-  // residual (kept as the fp32 value of the pair); pre-norm m = RMSNorm(r), the
-  // residual being r itself
-  if ((rc = norm(r, h->w.gamma_post, 1, a, a_lo, d.post_norm ? a_f : nullptr, NS, nullptr)) !=
-      PE_OK)
+  // O projection (partial sums)
+  e = partial_epi(NS, d.d);
+  if ((rc = run_gemm(h, G_O, attn, nullptr, NS, nullptr, e, ws, L, st, true, &np)) != PE_OK)
+    return rc;
+  // r = x_s + attn W_o^T, and the MLP operand: post-norm a = RMSNorm(r;
+  // gamma_post), which is also the MLP residual (kept as the fp32 value of the
+  // pair); pre-norm m = RMSNorm(r), the residual being r itself
+  if ((rc = norm(part, np, e.part_stride, x_s, d.post_norm ? nullptr : r, h->w.gamma_post, 1, a,
+                 a_lo, d.post_norm ? a_f : nullptr, NS, nullptr)) != PE_OK)
     return rc;
   const float* mlp_resid = d.post_norm ? (bf ? a_f : static_cast<const float*>(a)) : r;
   // SwiGLU: h = silu(gate) * up (a bf16 pair in bf16 mode)
@@ -512,17 +554,14 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   e.out2 = h_lo;
   e.ld_out = d.inter;
   if ((rc = run_gemm(h, G_GATEUP, a, a_lo, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
-  // down projection + residual (fp32)
-  e = Epilogue();
-  e.mode = EPI_RESID_F32;
-  e.out = y;
-  e.ld_out = d.d;
-  e.resid = mlp_resid;
-  e.ld_resid = d.d;
-  if ((rc = run_gemm(h, G_DOWN, hm, h_lo, NS, nullptr, e, ws, L, st)) != PE_OK) return rc;
-  // z = RMSNorm(y; gamma_final), the LM head operand
+  // down projection (partial sums)
+  e = partial_epi(NS, d.d);
+  if ((rc = run_gemm(h, G_DOWN, hm, h_lo, NS, nullptr, e, ws, L, st, true, &np)) != PE_OK)
+    return rc;
+  // z = RMSNorm(y; gamma_final) with y = residual + h W_down^T: the LM head operand
   (void)Hd;
-  return norm(y, h->w.gamma_final, 1, z_out, nullptr, nullptr, NS, nullptr);
+  return norm(part, np, e.part_stride, mlp_resid, nullptr, h->w.gamma_final, 1, z_out, nullptr,
+              nullptr, NS, nullptr);
 }
 
 int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, float* logits,
@@ -545,7 +584,7 @@ int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, fl
 }
 
 size_t pe_test_projection_workspace(const pe_handle* h, int which, int n_rows) {
-  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR);
+  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR | PE_PROJ_PARTIAL);
   if (!h || which < 0 || which >= G_COUNT || n_rows < 1) return 0;
   return layout_projection(h, which, n_rows).total;
 }
@@ -554,7 +593,9 @@ int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void*
                        size_t ws_bytes, void* stream) {
   const bool persistent = (which & PE_PROJ_PERSISTENT) != 0;
   const bool pair = (which & PE_PROJ_PAIR) != 0;
-  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR);
+  const bool partial = (which & PE_PROJ_PARTIAL) != 0;
+  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR | PE_PROJ_PARTIAL);
+  if (partial && which == G_GATEUP) return PE_ERR_ARG;
   if (!h || !h->has_layer || which < 0 || which >= G_COUNT || n_rows < 1 || !X || !out || !ws)
     return PE_ERR_ARG;
   if (!aligned16(X) || !aligned16(ws)) return PE_ERR_ARG;
@@ -564,9 +605,10 @@ int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const GemmShape s = gemm_shape(h, which);
   Epilogue e;
-  e.mode = which == G_GATEUP ? EPI_SWIGLU : EPI_STORE_F32;
+  e.mode = which == G_GATEUP ? EPI_SWIGLU : partial ? EPI_PARTIAL_F32 : EPI_STORE_F32;
   e.out = out;
   e.ld_out = s.M;
+  e.part_stride = static_cast<size_t>(n_rows) * s.M;
   const void* X_lo =
       pair ? static_cast<const void*>(static_cast<const bf16_t*>(X) +
                                       static_cast<size_t>(n_rows) * s.K)

@@ -34,6 +34,8 @@ constexpr size_t kSmemBudget = 212 * 1024;  // dynamic shared memory for the sta
 // 4: 303 us, 2: 301 us, none: 306 us).
 constexpr int kPrefetchKb = 2;
 constexpr int kMaxClusterSplits = 8;        // portable cluster size
+constexpr int kMaxPartialSplits = 16;       // splits storing their own partial sums
+static_assert(kMaxPartialSplits <= 16, "the projection test hook holds 16 partial tiles");
 // Weights in tile order (one contiguous 16 KB block per weight box) or row-major
 // (measured, LM head at B=1 with two CTAs per SM: 188 us packed, 192 us not).
 #ifndef PE_PACKED_WEIGHTS
@@ -89,6 +91,7 @@ PE_DEV void epi_store_elem(const Epilogue& e, int f, int t, float v, float v2) {
       static_cast<T*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] = Elem<T>::from_f(v);
       break;
     case EPI_STORE_F32:
+    case EPI_PARTIAL_F32:  // (out already points at this split's partial tile)
       static_cast<float*>(e.out)[static_cast<size_t>(t) * e.ld_out + f] = v;
       break;
     case EPI_RESID_F32:
@@ -124,9 +127,9 @@ PE_DEV unsigned long long warp_max_u64(unsigned long long k) {
 
 // Epilogue of 16 token columns j0..j0+15 for feature f (this thread's TMEM lane).
 // Called by all 128 epilogue threads together (ARGMAX uses named barrier 1).
-PE_DEV void tc_epilogue16(const TcArgs& p, int f, int j0, const float* v, const float* v2,
-                          int n_rows, unsigned long long (*red)[16], int ew, int et) {
-  const Epilogue& e = p.epi;
+PE_DEV void tc_epilogue16(const TcArgs& p, const Epilogue& e, int f, int j0, const float* v,
+                          const float* v2, int n_rows, unsigned long long (*red)[16], int ew,
+                          int et) {
   const bool fok = f < p.M;
   if (e.mode != EPI_ARGMAX) {
     if (!fok) return;
@@ -207,6 +210,14 @@ PE_DEV bool next_tile(const TcArgs& p, int it, TileRef& t) {
   return true;
 }
 
+// A tile whose token rows all lie past the live row count is skipped, except a
+// CTA's first tile when it is the token tile 0: its weights start loading
+// before the row count is known, so every role works through it (its epilogue
+// stores nothing past the live rows).
+PE_DEV bool tile_skipped(const TcArgs& p, const TileRef& t, int it, int n_rows) {
+  return t.n * p.BN >= n_rows && !(it == 0 && t.n == 0);
+}
+
 // OCC: CTAs per SM the instance is launched for (each instance keeps its own
 // fixed shared-memory limit, so graph replays of either stay launchable).
 template <int OCC>
@@ -234,7 +245,8 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
   const int kbk = kBK * p.atoms;  // elements of K per k-block
   const int nbuf = p.acc_bufs;
   const uint32_t buf_cols = static_cast<uint32_t>(p.BN * nA);
-  const bool clustered = p.k_splits > 1;
+  // K splits reduce inside a cluster, unless each stores its own partial
+  const bool clustered = p.k_splits > 1 && p.epi.mode != EPI_PARTIAL_F32;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -249,25 +261,45 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
     abort_sh = 0;
     fence_barrier_init();
   }
+  // weight boxes of the first tile's first stages, already loading (thread 0)
+  int pre = 0;
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&mapA);
     if (p.dual) prefetch_tmap(&mapA2);
     prefetch_tmap(&mapB);
     if (p.bpair) prefetch_tmap(&mapB2);
-    // The weights do not depend on the previous kernel: start pulling this
-    // CTA's first tile into L2 while that kernel finishes.
+    // The weights do not depend on the previous kernel.  Token tile 0: load the
+    // weight boxes of the first stages into the ring now, while that kernel
+    // finishes (the token boxes follow after the dependency wait).  Otherwise
+    // pull the first k-blocks into L2.
     TileRef t;
     if (next_tile(p, 0, t)) {
       const int kb0 = t.ks * p.kb_per_split;
-      const int kb1 = min(min(p.num_kb, kb0 + p.kb_per_split), kb0 + kPrefetchKb / p.atoms);
-      for (int kb = kb0; kb < kb1; ++kb)
-        for (int at = 0; at < p.atoms; ++at) {
-          if (kb * kbk + at * kBK >= p.K) break;
-          int cx, cy;
-          weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
-          tma_prefetch_l2_2d(&mapA, cx, cy);
-          if (p.dual) tma_prefetch_l2_2d(&mapA2, cx, cy);
+      const int nkb = min(p.num_kb, kb0 + p.kb_per_split) - kb0;
+      if (t.n == 0) {
+        const uint64_t pol_w = policy_evict_first();
+        pre = min(nkb, p.stages);
+        for (int s = 0; s < pre; ++s) {
+          mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+          for (int at = 0; at < p.atoms; ++at) {
+            uint8_t* sa = smem + static_cast<size_t>(s) * stage_bytes + at * atom_bytes;
+            int cx, cy;
+            weight_box(p, t.m, (kb0 + s) * kbk + at * kBK, cx, cy);
+            tma_load_2d(sa, &mapA, &full_bar[s], cx, cy, pol_w);
+            if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[s], cx, cy, pol_w);
+          }
         }
+      } else {
+        const int kb1 = min(kb0 + nkb, kb0 + kPrefetchKb / p.atoms);
+        for (int kb = kb0; kb < kb1; ++kb)
+          for (int at = 0; at < p.atoms; ++at) {
+            if (kb * kbk + at * kBK >= p.K) break;
+            int cx, cy;
+            weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
+            tma_prefetch_l2_2d(&mapA, cx, cy);
+            if (p.dual) tma_prefetch_l2_2d(&mapA2, cx, cy);
+          }
+      }
     }
   }
   if (warp == 1) {
@@ -307,37 +339,48 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
       const uint64_t pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0, armed_parity = 0;  // per stage: ever armed / parity of the last arm
+      // per stage: ever armed / parity of the last arm; stages 0..pre-1 were
+      // armed (phase 0) with their weight boxes before the dependency wait
+      uint32_t armed = (1u << pre) - 1u, armed_parity = 0;
+      uint32_t pending_b = armed;  // ... whose token boxes are still to be issued
+      auto issue_b = [&](int s, int kb, int tn) {
+        for (int at = 0; at < p.atoms; ++at) {
+          uint8_t* sa = smem + static_cast<size_t>(s) * stage_bytes + at * atom_bytes;
+          const int x = kb * kbk + at * kBK;
+          tma_load_2d(sa + kABytes * nA, &mapB, &full_bar[s], x, tn * p.BN, pol_x);
+          if (p.bpair)
+            tma_load_2d(sa + kABytes * nA + b_bytes, &mapB2, &full_bar[s], x, tn * p.BN, pol_x);
+        }
+      };
       TileRef t;
       for (int it = 0; next_tile(p, it, t) && !*abort_flag; ++it) {
-        if (t.n * p.BN >= n_rows) continue;
+        if (tile_skipped(p, t, it, n_rows)) continue;
         const int kb0 = t.ks * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
-            fail();
-            break;
+          if (it == 0 && kb - kb0 < pre) {
+            // weights already on their way into this stage
+            issue_b(stage, kb, t.n);
+            pending_b &= ~(1u << stage);
+          } else {
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+              fail();
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
+            // the atoms of one row follow each other in memory: their boxes go
+            // out back to back, A first (the weights dominate the traffic)
+            for (int at = 0; at < p.atoms; ++at) {
+              uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes;
+              int cx, cy;
+              weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
+              tma_load_2d(sa, &mapA, &full_bar[stage], cx, cy, pol_w);
+              if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], cx, cy, pol_w);
+            }
+            issue_b(stage, kb, t.n);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           }
-          mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
-          // the atoms of one row follow each other in memory: their boxes go out
-          // back to back, A first (the weights dominate the traffic)
-          for (int at = 0; at < p.atoms; ++at) {
-            uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes;
-            int cx, cy;
-            weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
-            tma_load_2d(sa, &mapA, &full_bar[stage], cx, cy, pol_w);
-            if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], cx, cy, pol_w);
-          }
-          for (int at = 0; at < p.atoms; ++at) {
-            uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes;
-            const int x = kb * kbk + at * kBK;
-            tma_load_2d(sa + kABytes * nA, &mapB, &full_bar[stage], x, t.n * p.BN, pol_x);
-            if (p.bpair)
-              tma_load_2d(sa + kABytes * nA + b_bytes, &mapB2, &full_bar[stage], x, t.n * p.BN,
-                          pol_x);
-          }
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
@@ -345,6 +388,11 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
         }
       }
       if (*abort_flag) {
+        // stages armed before the wait but left without their token boxes get
+        // them now, so that their barriers complete
+        if (pending_b && next_tile(p, 0, t))
+          for (int s = 0; s < p.stages; ++s)
+            if (pending_b & (1u << s)) issue_b(s, t.ks * p.kb_per_split + s, t.n);
         // let copies already in flight land before the CTA's shared memory goes away
         for (int s = 0; s < p.stages; ++s)
           if (armed & (1u << s)) {
@@ -361,7 +409,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
       uint32_t phase = 0, acc_phase[2] = {0u, 0u};
       TileRef t;
       for (int it = 0; next_tile(p, it, t) && !*abort_flag; ++it) {
-        if (t.n * p.BN >= n_rows) continue;
+        if (tile_skipped(p, t, it, n_rows)) continue;
         const int b = cnt % nbuf;
         ++cnt;
         const int kb0 = t.ks * p.kb_per_split;
@@ -425,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
     int cnt = 0;
     TileRef t;
     for (int it = 0; next_tile(p, it, t) && !*abort_flag; ++it) {
-      if (t.n * p.BN >= n_rows) continue;
+      if (tile_skipped(p, t, it, n_rows)) continue;
       const int b = cnt % nbuf;
       const int par = cnt & 1;
       ++cnt;
@@ -445,6 +493,9 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
       const uint32_t tl = tmem_base + static_cast<uint32_t>(b) * buf_cols +
                           (static_cast<uint32_t>(q * 32) << 16);
       if (!clustered) {
+        Epilogue ep = p.epi;
+        if (ep.mode == EPI_PARTIAL_F32)
+          ep.out = static_cast<float*>(ep.out) + static_cast<size_t>(t.ks) * ep.part_stride;
         for (int c = 0; c < p.BN; c += 16) {
           float v[16], v2[16];
           tmem_ld16(tl + c, v);
@@ -454,7 +505,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
             tc_fence_before();
             mbar_arrive(&tempty_bar[b]);
           }
-          tc_epilogue16(p, f, jt + c, v, p.dual ? v2 : nullptr, n_rows, red_sh, ew, et);
+          tc_epilogue16(p, ep, f, jt + c, v, p.dual ? v2 : nullptr, n_rows, red_sh, ew, et);
         }
       } else {
         // park the partial tile: part[a][j][fl] (consecutive features, conflict-free)
@@ -482,7 +533,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
     if (warp >= 2 && !*abort_flag) {
       const int fl = (warp & 3) * 32 + lane;
       TileRef t;
-      if (next_tile(p, 0, t) && t.n * p.BN < n_rows) {
+      if (next_tile(p, 0, t) && !tile_skipped(p, t, 0, n_rows)) {
         const int f = t.m * kBM + fl;
         const int jt = t.n * p.BN;
         const uint32_t rank = cluster_ctarank();
@@ -603,7 +654,8 @@ static int max_active_clusters(int occ, int cs, size_t smem) {
   return n * occ;
 }
 
-TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split) {
+TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split,
+                    bool partial) {
   TcPlan pl{};
   pl.M = M;
   pl.K = K;
@@ -663,7 +715,12 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   // splits of a tile must all be resident at once, their partial tile must fit
   // in the stage ring, and at least 4 k-blocks go to each split
   int s = 1;
-  if (allow_split && base < num_sms) {
+  if (allow_split && base < num_sms && partial) {
+    // each split stores its own partial sum: as many as fill the CTA slots
+    s = std::min(kMaxPartialSplits, num_sms / base);
+    s = std::min(s, pl.num_kb * pl.atoms / 4);
+    if (s < 2) s = 1;
+  } else if (allow_split && base < num_sms) {
     s = std::min(kMaxClusterSplits, num_sms / base);
     s = std::min(s, pl.num_kb * pl.atoms / 4);
     const size_t part_bytes = static_cast<size_t>(nA) * pl.BN * kBM * sizeof(float);
@@ -686,7 +743,7 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   pl.main_tiles = base;
   pl.tail_splits = 1;
   pl.tail_kb_per_split = pl.num_kb;
-  if (pl.k_splits == 1 && base > num_sms) {
+  if (pl.k_splits == 1 && base > num_sms && !partial) {
     // Several rounds of persistent tiles: a partial last round leaves SMs idle
     // while a few CTAs finish one more tile.  Run the full rounds persistent and
     // the remaining tiles as clusters that split them over K.
@@ -747,7 +804,7 @@ static int launch_one(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorM
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = k_splits > 1 ? 2 : 1;
+  cfg.numAttrs = (k_splits > 1 && epi.mode != EPI_PARTIAL_F32) ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, tc_kernel(pl.ctas_per_sm), *mapA, pl.dual ? *mapA2 : *mapA, mapB,
                             mapB2, a) ==
                  cudaSuccess

@@ -20,6 +20,9 @@ enum EpiMode {
   EPI_SWIGLU = 3,       // out[t][f] = silu(D_gate) * D_up    (element type of the step)
   EPI_SWIGLU_PAIR = 4,  // the same product as a bf16 pair: out = hi, out2 = lo
   EPI_ARGMAX = 5,       // amax[t] = max over f of key(D, f); optional fp32 logits
+  // split k of a K-split GEMM stores its partial sum: out[k * part_stride +
+  // t * ld_out + f] (float); the consumer adds the splits in order 0, 1, ...
+  EPI_PARTIAL_F32 = 6,
 };
 
 struct Epilogue {
@@ -32,6 +35,7 @@ struct Epilogue {
   unsigned long long* amax = nullptr;
   float* logits = nullptr;
   int ld_logits = 0;
+  size_t part_stride = 0;  // EPI_PARTIAL_F32: floats between splits' partial tiles
 };
 
 // ------------------------------------------------------------------ tcgen05 GEMM (bf16)
@@ -47,9 +51,12 @@ struct TcPlan {
   int main_tiles, tail_splits, tail_kb_per_split;
 };
 
+// partial: the epilogue is EPI_PARTIAL_F32, so splits of K need no cluster (each
+// stores its own partial) and the split count is free of cluster limits.
 // dual: two weight matrices (gate and up) with two accumulators.  bpair: the
 // token rows come as a bf16 pair (hi, lo) whose products add into one accumulator.
-TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split);
+TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split,
+                    bool partial = false);
 
 // mapA / mapA2: weight tensor maps (box 64 x 128, 128-byte swizzle).  X: token
 // rows [N_cap][K] bf16 (row stride K).  n_rows_dev: live token rows on device

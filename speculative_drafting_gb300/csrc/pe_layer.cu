@@ -16,57 +16,110 @@
 
 namespace pe {
 
-// One CTA per row of an fp32 input: y = x * gamma / sqrt(mean(x^2) + eps) (or
-// y = x when apply_norm is 0), stored as any of: the step's element type (out,
-// rounded to nearest), the rest of a bf16 pair (out_lo = bf16(y - out)), and the
-// fp32 value of what was stored (out + out_lo, or y).
+// One CTA per row: x = (sum of the partial tiles, in order) + resid, then
+// y = x * gamma / sqrt(mean(x^2) + eps) (or y = x when apply_norm is 0), stored
+// as any of: the step's element type (out, rounded to nearest), the rest of a
+// bf16 pair (out_lo = bf16(y - out)), and the fp32 value of what was stored
+// (out + out_lo, or y); sum_out receives x.  The row stays in registers between
+// the sum of squares and the output pass (up to kRowCache float4 per thread).
+constexpr int kRowCache = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
   __shared__ float red[32];
   pdl_trigger();
+  const int v4 = a.d / 4;
+  // the gains are weights, independent of the kernels before: read them now
+  const T* gam = static_cast<const T*>(a.gamma);
+  float gc[kRowCache][4];
+#pragma unroll
+  for (int c = 0; c < kRowCache; ++c) {
+    const int i = threadIdx.x + c * blockDim.x;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) gc[c][k] = (a.apply_norm && i < v4) ? Elem<T>::to_f(gam[4 * i + k]) : 1.f;
+  }
   pdl_wait();
   const int row = blockIdx.x;
   int n = a.rows_cap;
   if (a.n_rows_dev) n = min(max(*a.n_rows_dev, 0), a.rows_cap);
   if (row >= n) return;
-  const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(row) * a.ld_x);
-  const int v4 = a.d / 4;
+  const size_t ro = static_cast<size_t>(row) * a.ld_x;
+  auto load = [&](int i) {
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < a.n_parts; ++k) {
+      const float4 p = reinterpret_cast<const float4*>(a.x + k * a.part_stride + ro)[i];
+      s.x += p.x;
+      s.y += p.y;
+      s.z += p.z;
+      s.w += p.w;
+    }
+    if (a.resid) {
+      const float4 r =
+          reinterpret_cast<const float4*>(a.resid + static_cast<size_t>(row) * a.ld_resid)[i];
+      s.x += r.x;
+      s.y += r.y;
+      s.z += r.z;
+      s.w += r.w;
+    }
+    if (a.sum_out) reinterpret_cast<float4*>(a.sum_out + ro)[i] = s;
+    return s;
+  };
+  float4 xc[kRowCache];
+  float ss = 0.f;
+  auto acc_ss = [&](const float4& f) {
+    ss = fmaf(f.x, f.x, ss);
+    ss = fmaf(f.y, f.y, ss);
+    ss = fmaf(f.z, f.z, ss);
+    ss = fmaf(f.w, f.w, ss);
+  };
+#pragma unroll
+  for (int c = 0; c < kRowCache; ++c) {
+    const int i = threadIdx.x + c * blockDim.x;
+    if (i < v4) {
+      xc[c] = load(i);
+      acc_ss(xc[c]);
+    }
+  }
+  for (int i = threadIdx.x + kRowCache * blockDim.x; i < v4; i += blockDim.x) acc_ss(load(i));
   float inv = 1.0f;
   if (a.apply_norm) {
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < v4; i += blockDim.x) {
-      const float4 f = src[i];
-      ss = fmaf(f.x, f.x, ss);
-      ss = fmaf(f.y, f.y, ss);
-      ss = fmaf(f.z, f.z, ss);
-      ss = fmaf(f.w, f.w, ss);
-    }
     ss = block_sum(ss, red);
     inv = 1.0f / sqrtf(ss / static_cast<float>(a.d) + a.eps);
   }
-  const T* gam = static_cast<const T*>(a.gamma);
   T* out = static_cast<T*>(a.out);
-  const size_t ro = static_cast<size_t>(row) * a.ld_out;
-  for (int i = threadIdx.x; i < v4; i += blockDim.x) {
-    const float4 f4 = src[i];
+  const size_t oo = static_cast<size_t>(row) * a.ld_out;
+  auto emit = [&](int i, const float4& f4, const float* g) {
     const float f[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int c = 4 * i + k;
-      const float y = a.apply_norm ? f[k] * inv * Elem<T>::to_f(gam[c]) : f[k];
+      const float y = a.apply_norm ? f[k] * inv * g[k] : f[k];
       float stored = y;
       if (out) {
         const T hi = Elem<T>::from_f(y);
-        out[ro + c] = hi;
+        out[oo + c] = hi;
         stored = Elem<T>::to_f(hi);
         if (a.out_lo) {
           const bf16 lo = __float2bfloat16_rn(y - stored);
-          a.out_lo[ro + c] = lo;
+          a.out_lo[oo + c] = lo;
           stored += __bfloat162float(lo);
         }
       }
-      if (a.out_f32) a.out_f32[ro + c] = stored;
+      if (a.out_f32) a.out_f32[oo + c] = stored;
     }
+  };
+#pragma unroll
+  for (int c = 0; c < kRowCache; ++c) {
+    const int i = threadIdx.x + c * blockDim.x;
+    if (i < v4) emit(i, xc[c], gc[c]);
+  }
+  for (int i = threadIdx.x + kRowCache * blockDim.x; i < v4; i += blockDim.x) {
+    // rows wider than the register cache: the sum again (sum_out is rewritten
+    // with the same value)
+    float g[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) g[k] = a.apply_norm ? Elem<T>::to_f(gam[4 * i + k]) : 1.f;
+    emit(i, load(i), g);
   }
 }
 
@@ -126,7 +179,13 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
   __syncthreads();
   const int s_idx = samp_sh;
   const int QKV = (a.H + 2 * a.G) * a.hd;
-  const float* row = a.qkv + static_cast<size_t>(v) * QKV;
+  // element x of this row of the QKV projection: the sum of its partial tiles
+  const float* row0 = a.qkv + static_cast<size_t>(v) * QKV;
+  auto qkv_at = [&](int x) {
+    float acc = 0.f;
+    for (int k = 0; k < a.n_parts; ++k) acc += row0[k * a.part_stride + x];
+    return acc;
+  };
   const bool slot_ok = slot >= 0 && slot < static_cast<int64_t>(a.num_blocks) * a.bs;
   if (!slot_ok && slot != PE_PADDING_SLOT_ID && threadIdx.x == 0)
     set_status(a.status, PE_ST_BLOCK_RANGE);
@@ -134,7 +193,7 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
   // rotated q (sample rows) and k (all rows)
   for (int e = threadIdx.x; e < (a.H + a.G) * half; e += blockDim.x) {
     const int hh = e / half, i = e - hh * half;
-    const float x1 = row[hh * a.hd + i], x2 = row[hh * a.hd + i + half];
+    const float x1 = qkv_at(hh * a.hd + i), x2 = qkv_at(hh * a.hd + i + half);
     const float y1 = x1 * cs[i] - x2 * sn[i];
     const float y2 = x2 * cs[i] + x1 * sn[i];
     if (hh < a.H) {
@@ -153,7 +212,7 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
     for (int e = threadIdx.x; e < a.G * a.hd; e += blockDim.x) {
       const int g = e / a.hd, i = e - g * a.hd;
       T* vc = static_cast<T*>(a.v_cache) + ((blk * a.G + g) * a.bs + off) * a.hd;
-      vc[i] = Elem<T>::from_f(row[(a.H + a.G) * a.hd + e]);
+      vc[i] = Elem<T>::from_f(qkv_at((a.H + a.G) * a.hd + e));
     }
   }
   if (s_idx >= 0) {

@@ -60,11 +60,17 @@ int launch_input(const InputArgs& a, int dtype, cudaStream_t st);
 
 // ---------------------------------------------------------------- row RMSNorm
 // y[i] = x[i] * gamma / sqrt(mean(x[i]^2) + eps) (apply_norm) or x[i], for rows
-// i < n_rows of an fp32 input, stored as: out (step dtype), out_lo (bf16 rest of
-// a pair, nullable), out_f32 (fp32 value of what was stored, nullable).
+// i < n_rows, where x = (sum of n_parts partial tiles, in order) + resid, stored
+// as: out (step dtype), out_lo (bf16 rest of a pair, nullable), out_f32 (fp32
+// value of what was stored, nullable); sum_out (nullable) receives x itself.
 struct RowNormArgs {
-  const float* x;
+  const float* x;  // partial k of row i at x[k * part_stride + i * ld_x]
   int ld_x;
+  int n_parts;
+  size_t part_stride;
+  const float* resid;  // nullable, [rows][ld_resid]
+  int ld_resid;
+  float* sum_out;  // nullable, [rows][ld_x]
   const void* gamma;
   int apply_norm;
   void* out;
@@ -80,7 +86,10 @@ int launch_rownorm(const RowNormArgs& a, int dtype, cudaStream_t st);
 // ---------------------------------------------------------------- RoPE + KV write
 struct RopeArgs {
   int T_out, B, K, H, G, hd, d, bs, num_blocks;
-  const float* qkv;  // [T_out][(H+2G)hd] fp32, non-rejected rows in valid_rows order
+  const float* qkv;  // n_parts partial tiles of [T_out][(H+2G)hd] fp32, part_stride
+                     // apart; non-rejected rows in valid_rows order
+  int n_parts;
+  size_t part_stride;
   const float* x;    // [T_out][d] fc output, fp32 (same order)
   const int32_t* n_valid;
   const int32_t* valid_rows;

@@ -104,3 +104,47 @@ def test_projection_schedules_and_pairs(name, which, n, flags):
     assert np.all(np.isfinite(got))
     err = np.abs(got - ref)
     assert np.all(err <= tol), f"max err {err.max():.3g}"
+
+
+PARTIAL = 0x400  # PE_PROJ_PARTIAL (pe_testing.h)
+
+
+@pytest.mark.parametrize("name", ["small_prenorm", "small_postnorm_hd128", "tiny_fp32"])
+@pytest.mark.parametrize("which", ["fc", "qkv", "o", "down", "lm"])
+@pytest.mark.parametrize("n", [1, 7, 16, 100, 300])
+@pytest.mark.parametrize("pair", [False, True])
+def test_projection_partial_sums(name, which, n, pair):
+    """K splits that store their own partial sums: the tiles add up to the
+    float64 product (tiles past the split count stay zero)."""
+    torch = cuda_or_skip()
+    wl, b, w, kc, vc, r = setup(name, want_logits=False, kv=False)
+    dm = wl.dims
+    if pair and dm.dtype != "bf16":
+        pytest.skip("pair operands are bf16 only")
+    M, Kd, wname = _shape(dm, which)
+    g = np.random.default_rng(n * 41 + PROJ[which] + 7 * pair)
+    X = g.standard_normal((n, Kd)).astype(np.float32)
+    if dm.dtype == "bf16":
+        from speculative_drafting_gb300.workloads import f32_to_bf16_bits
+        hi = f32_to_bf16_bits(X)
+        x64 = f64(hi, "bf16")
+        Xh = hi
+        if pair:
+            lo = f32_to_bf16_bits((X.astype(np.float64) - x64).astype(np.float32))
+            x64 = x64 + f64(lo, "bf16")
+            Xh = np.concatenate([hi, lo], axis=0)
+    else:
+        Xh, x64 = X, X.astype(np.float64)
+    Xd = runner.to_device(Xh, dm.dtype)
+    out = torch.zeros((16, n, M), dtype=torch.float32, device="cuda")
+    ws = r.drafter.test_projection(PROJ[which] | PARTIAL | (PAIR if pair else 0), Xd, n, out)
+    torch.cuda.synchronize()
+    st, _ = r.drafter.read_status(ws)
+    assert st == 0, hex(st)
+    ref = O.linear(x64, f64(w[wname], dm.dtype))
+    parts = host(out).astype(np.float64)
+    got = parts.sum(axis=0)
+    tol = 1e-5 * np.sqrt(Kd) * 0.02 * 4 + 1e-5 * np.abs(ref)
+    assert np.all(np.isfinite(parts))
+    err = np.abs(got - ref)
+    assert np.all(err <= tol), f"max err {err.max():.3g}"
