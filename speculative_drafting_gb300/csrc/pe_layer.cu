@@ -135,8 +135,12 @@ int launch_rownorm(const RowNormArgs& a, int dtype, cudaStream_t st) {
 
 // ------------------------------------------------------------------ RoPE + KV write
 
-// One CTA per non-rejected row v.  The row is a sample row when it is one of
-// the last K non-rejected rows of its request (NTP row + MASK rows).
+// CTAs (v, y): non-rejected row v, the y-th of kRopeCtasPerRow slices of its
+// heads (every element sums the QKV partial tiles, so a row is spread over
+// several CTAs).  The row is a sample row when it is one of the last K
+// non-rejected rows of its request (NTP row + MASK rows).
+constexpr int kRopeCtasPerRow = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
   __shared__ float cs[64], sn[64];
@@ -179,6 +183,8 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
   __syncthreads();
   const int s_idx = samp_sh;
   const int QKV = (a.H + 2 * a.G) * a.hd;
+  const int tid = blockIdx.y * blockDim.x + threadIdx.x;  // thread within the row
+  const int nthr = gridDim.y * blockDim.x;
   // element x of this row of the QKV projection: the sum of its partial tiles
   const float* row0 = a.qkv + static_cast<size_t>(v) * QKV;
   auto qkv_at = [&](int x) {
@@ -191,7 +197,7 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
     set_status(a.status, PE_ST_BLOCK_RANGE);
   const int64_t blk = slot_ok ? slot / a.bs : 0, off = slot_ok ? slot % a.bs : 0;
   // rotated q (sample rows) and k (all rows)
-  for (int e = threadIdx.x; e < (a.H + a.G) * half; e += blockDim.x) {
+  for (int e = tid; e < (a.H + a.G) * half; e += nthr) {
     const int hh = e / half, i = e - hh * half;
     const float x1 = qkv_at(hh * a.hd + i), x2 = qkv_at(hh * a.hd + i + half);
     const float y1 = x1 * cs[i] - x2 * sn[i];
@@ -209,7 +215,7 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
     }
   }
   if (slot_ok) {
-    for (int e = threadIdx.x; e < a.G * a.hd; e += blockDim.x) {
+    for (int e = tid; e < a.G * a.hd; e += nthr) {
       const int g = e / a.hd, i = e - g * a.hd;
       T* vc = static_cast<T*>(a.v_cache) + ((blk * a.G + g) * a.bs + off) * a.hd;
       vc[i] = Elem<T>::from_f(qkv_at((a.H + a.G) * a.hd + e));
@@ -219,15 +225,16 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
     // the fc output of the sample rows is the attention residual (fp32)
     const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(v) * a.d);
     float4* dst = reinterpret_cast<float4*>(a.x_s + static_cast<size_t>(s_idx) * a.d);
-    for (int i = threadIdx.x; i < a.d / 4; i += blockDim.x) dst[i] = src[i];
+    for (int i = tid; i < a.d / 4; i += nthr) dst[i] = src[i];
   }
 }
 
 int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st) {
   if (a.T_out <= 0) return PE_OK;
   const cudaError_t e =
-      dtype == PE_DTYPE_BF16 ? launch_pdl(rope_kv_kernel<bf16>, dim3(a.T_out), dim3(256), 0, st, a)
-                             : launch_pdl(rope_kv_kernel<float>, dim3(a.T_out), dim3(256), 0, st, a);
+      dtype == PE_DTYPE_BF16
+          ? launch_pdl(rope_kv_kernel<bf16>, dim3(a.T_out, kRopeCtasPerRow), dim3(256), 0, st, a)
+          : launch_pdl(rope_kv_kernel<float>, dim3(a.T_out, kRopeCtasPerRow), dim3(256), 0, st, a);
   return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 
