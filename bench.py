@@ -17,8 +17,10 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -64,6 +66,24 @@ def measured_peaks():
 
 
 # ----------------------------------------------------------------------------- algorithmic bytes
+
+
+def profiled_traffic(workload):
+    """DRAM bytes (read + write) of the LM head per step from the committed ncu
+    summary, while the GEMM sources are the ones it was captured with; else None."""
+    if workload != "gptoss_b1_k7":
+        return None
+    try:
+        text = open(os.path.join(ROOT, "profiles", "lm_head_gemm_gptoss_b1_k7.md")).read()
+        vals = dict(re.findall(r"^\s*(traffic_bytes_per_step|source_sha256|sources):\s*(\S.*)$",
+                               text, re.M))
+        digests = "".join(hashlib.sha256(open(os.path.join(ROOT, f), "rb").read()).hexdigest()
+                          for f in vals["sources"].split())
+        if hashlib.sha256(digests.encode()).hexdigest() != vals["source_sha256"].strip():
+            return None
+        return int(vals["traffic_bytes_per_step"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def lm_head_bytes(dm, n_rows):
@@ -375,7 +395,8 @@ def run_ours(args, rank, world, local):
                              else None),
             "roofline": {"kernel": "gemm_tc_kernel (LM head + argmax epilogue)", "bound": "hbm",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic(wl.name),
                          "peak_source": src, "algorithmic_bytes": lm_bytes,
                          "avg_launch_us": lm_avg_s * 1e6},
             "cpu_baseline": cpu,
