@@ -57,18 +57,24 @@ TcPlan plan_of(const pe_handle* h, int id, int N, bool bpair, bool allow_split =
 
 // The projections whose K splits store partial sums (EPI_PARTIAL_F32) for the
 // kernel after them to add, and whether their token operand is a bf16 pair.
-bool partial_gemm(int id) { return id == G_FC || id == G_QKV || id == G_O || id == G_DOWN; }
+// With PE_PARTIAL_SUMS 0 they reduce their splits in a cluster and store the sum.
+#ifndef PE_PARTIAL_SUMS
+#define PE_PARTIAL_SUMS 1
+#endif
+bool partial_gemm(int id) {
+  return PE_PARTIAL_SUMS && (id == G_FC || id == G_QKV || id == G_O || id == G_DOWN);
+}
 bool pair_operand(int id) { return id == G_QKV || id == G_GATEUP || id == G_DOWN; }
 
 // Bytes of partial sums projection `id` stores over any N <= N_max token rows
 // (the split count rises as N falls, so every N is walked).
 size_t partial_bytes_bound(const pe_handle* h, int id, int N_max) {
   const GemmShape s = gemm_shape(h, id);
-  if (!is_bf16(h)) return static_cast<size_t>(N_max) * s.M * sizeof(float);
+  if (!is_bf16(h) || !partial_gemm(id)) return static_cast<size_t>(N_max) * s.M * sizeof(float);
   size_t best = 0;
   for (int n = 1; n <= N_max; ++n) {
     const TcPlan p = plan_of(h, id, n, pair_operand(id), true, true);
-    best = std::max(best, static_cast<size_t>(p.k_splits) * n * s.M * sizeof(float));
+    best = std::max(best, static_cast<size_t>(p.partial ? p.k_splits : 1) * n * s.M * sizeof(float));
   }
   return best;
 }
@@ -205,11 +211,13 @@ int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
                            static_cast<const float*>(X), s.M, s.K, N_cap, n_rows_dev, epi, st);
   }
   const TcPlan p = plan_of(h, id, N_cap, X_lo != nullptr, allow_split, partial);
-  if (n_parts) *n_parts = p.k_splits;
+  if (n_parts) *n_parts = p.partial ? p.k_splits : 1;
+  Epilogue ep = epi;
+  if (partial && !p.partial) ep.mode = EPI_STORE_F32;  // the splits reduce in a cluster
   const CUtensorMap* mA = id == G_FC ? &h->m_fc : id == G_QKV ? &h->m_qkv : id == G_O ? &h->m_o
                         : id == G_GATEUP ? &h->m_gate : id == G_DOWN ? &h->m_down : &h->m_lm;
   const CUtensorMap* mA2 = id == G_GATEUP ? &h->m_up : nullptr;
-  return launch_gemm_tc(p, mA, mA2, X, X_lo, n_rows_dev, epi, at<uint32_t>(ws, L.status), st);
+  return launch_gemm_tc(p, mA, mA2, X, X_lo, n_rows_dev, ep, at<uint32_t>(ws, L.status), st);
 }
 
 }  // namespace
@@ -464,7 +472,7 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   // the kernel after it adds them (in split order) as it reads them
   auto partial_epi = [&](int rows, int M) {
     Epilogue ep;
-    ep.mode = EPI_PARTIAL_F32;
+    ep.mode = PE_PARTIAL_SUMS ? EPI_PARTIAL_F32 : EPI_STORE_F32;
     ep.out = part;
     ep.ld_out = M;
     ep.part_stride = static_cast<size_t>(rows) * M;

@@ -31,8 +31,11 @@ constexpr int kMaxSplits = 128;       // key splits per (request, KV head)
 constexpr long kMaxSplitKeys = 2048;  // keys per split, at most
 // Cluster mode: the splits of one (request, KV head) are one thread-block
 // cluster (non-portable size up to 16) and merge in distributed shared memory.
-// Chosen while its splits stay at most kClusterSplitKeys keys long, or at most
-// a quarter longer than the splits the global-memory merge would use.
+// Chosen while the whole grid is one wave (two CTAs per SM) and its splits stay
+// at most kClusterSplitKeys keys long, or at most a quarter longer than the
+// splits the global-memory merge would use.  With several waves a cluster's
+// CTAs would hold their SMs while waiting for the cluster's slowest split
+// (measured at B=64: +163 us, at B=32 with 32K contexts: +102 us).
 constexpr int kMaxAttnCluster = 16;
 constexpr long kClusterSplitKeys = 1024;
 
@@ -60,8 +63,12 @@ __host__ __device__ inline AttnShape attn_shape(int rows) {
 // fp32 accumulators and an online softmax in the exp2 domain; P enters P V as a
 // hi + lo bf16 pair.  At the end the key groups' states merge in shared memory
 // and the CTA writes unnormalised partials for the combine kernel.
-template <int HD, int KG>
-__global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1))
+// MINB = 2 (hd = 64): registers capped so that two CTAs share an SM, for grids
+// of several waves (one CTA's 3-chunk ring does not keep an SM's share of DRAM
+// busy; measured at B=64: step 1756 -> 1570 us).  A grid of one wave keeps the
+// uncapped registers (no spills).  hd = 128 fits two CTAs by shared memory.
+template <int HD, int KG, int MINB>
+__global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
     attn_tma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const AttnArgs a) {
   constexpr int HALVES = HD / 64;        // 128-byte swizzle atoms per key row
@@ -313,23 +320,29 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1))
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-    // merge the key groups through the (now idle) ring: group 1 parks, group 0 merges
-    float* mo = reinterpret_cast<float*>(ring);            // [row][HD]
-    float* mml = mo + static_cast<size_t>(sh.rw) * 16 * HD;  // [row][2]
+    // merge the key groups through the (now idle) ring: groups 1..KG-1 park their
+    // state in regions 0..KG-2 ([row][HD] each, then (m, l) per row), group 0
+    // merges; the merged partial then takes region 0's place
+    constexpr int NREG = KG > 1 ? KG - 1 : 1;
+    const int rows_pad = sh.rw * 16;
+    float* mo = reinterpret_cast<float*>(ring);
+    float* mml = mo + static_cast<size_t>(NREG) * rows_pad * HD;
     named_bar_sync(1, n_compute);
-    if (KG == 2 && kgi == 1) {
+    if (KG > 1 && kgi >= 1) {
+      float* po = mo + static_cast<size_t>(kgi - 1) * rows_pad * HD;
+      float* pml = mml + static_cast<size_t>(kgi - 1) * rows_pad * 2;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int rl = rw * 16 + gq + hf * 8;
 #pragma unroll
         for (int nd = 0; nd < HD / 8; ++nd) {
           const int d = nd * 8 + tq * 2;
-          mo[rl * HD + d] = o[nd][hf * 2];
-          mo[rl * HD + d + 1] = o[nd][hf * 2 + 1];
+          po[rl * HD + d] = o[nd][hf * 2];
+          po[rl * HD + d + 1] = o[nd][hf * 2 + 1];
         }
         if (tq == 0) {
-          mml[rl * 2] = hf ? m_b : m_a;
-          mml[rl * 2 + 1] = hf ? l_b : l_a;
+          pml[rl * 2] = hf ? m_b : m_a;
+          pml[rl * 2 + 1] = hf ? l_b : l_a;
         }
       }
     }
@@ -337,24 +350,32 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1))
     if (kgi == 0) {
       // merged (m, l) of rows ra, rb (all four lanes of a row read the parked
       // group-1 values before any lane overwrites them below)
-      float mh[2], lh[2], w0h[2], w1h[2];
+      float mh[2], lh[2], w0h[2], wgh[2][NREG];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float m = hf ? m_b : m_a, l = hf ? l_b : l_a;
-        float w0 = 1.f, w1 = 0.f;
+        float w0 = 1.f;
         const int rl = rw * 16 + gq + hf * 8;
-        if (KG == 2) {
-          const float m1 = mml[rl * 2], l1 = mml[rl * 2 + 1];
-          const float M = fmaxf(m, m1);
+#pragma unroll
+        for (int g2 = 0; g2 < NREG; ++g2) wgh[hf][g2] = 0.f;
+        if (KG > 1) {
+          float M = m;
+#pragma unroll
+          for (int g2 = 0; g2 < KG - 1; ++g2) M = fmaxf(M, mml[(g2 * rows_pad + rl) * 2]);
           w0 = (m == -INFINITY) ? 0.f : exp2f(m - M);
-          w1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - M);
-          l = l * w0 + l1 * w1;
+          l *= w0;
+#pragma unroll
+          for (int g2 = 0; g2 < KG - 1; ++g2) {
+            const float mg = mml[(g2 * rows_pad + rl) * 2];
+            const float wg = (mg == -INFINITY) ? 0.f : exp2f(mg - M);
+            l += mml[(g2 * rows_pad + rl) * 2 + 1] * wg;
+            wgh[hf][g2] = wg;
+          }
           m = M;
         }
         mh[hf] = m;
         lh[hf] = l;
         w0h[hf] = w0;
-        w1h[hf] = w1;
       }
       __syncwarp();
 #pragma unroll
@@ -376,9 +397,11 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1))
         for (int nd = 0; nd < HD / 8; ++nd) {
           const int d = nd * 8 + tq * 2;
           float v0 = o[nd][hf * 2] * w0h[hf], v1 = o[nd][hf * 2 + 1] * w0h[hf];
-          if (KG == 2) {
-            v0 += mo[rl * HD + d] * w1h[hf];
-            v1 += mo[rl * HD + d + 1] * w1h[hf];
+#pragma unroll
+          for (int g2 = 0; g2 < KG - 1; ++g2) {
+            const float* pg = mo + static_cast<size_t>(g2) * rows_pad * HD + rl * HD;
+            v0 += pg[d] * wgh[hf][g2];
+            v1 += pg[d + 1] * wgh[hf][g2];
           }
           *reinterpret_cast<float2*>(po + d) = make_float2(v0, v1);
         }
@@ -403,7 +426,8 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1))
     const int rank = static_cast<int>(cluster_ctarank());
     const int nw = static_cast<int>(blockDim.x >> 5);
     const uint32_t o_base = smem_u32(ring);
-    const uint32_t ml_base = o_base + static_cast<uint32_t>(sh.rw * 16 * HD * 4);
+    constexpr int NREG_C = KG > 1 ? KG - 1 : 1;
+    const uint32_t ml_base = o_base + static_cast<uint32_t>(NREG_C * sh.rw * 16 * HD * 4);
     constexpr int DPL = HD / 32;  // dims per lane
     for (int i = warp;; i += nw) {
       const int rr = rank + i * S;
@@ -584,7 +608,8 @@ void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, 
   const long nc = std::min<long>(ns, kMaxAttnCluster);
   const long len_c = (chunks + nc - 1) / nc * kKC;
   const long len_g = (chunks + ns - 1) / ns * kKC;
-  if (len_c <= std::max(kClusterSplitKeys, len_g + len_g / 4)) {
+  const long grid_c = static_cast<long>(B) * G * ((Lmax + len_c - 1) / len_c);
+  if (grid_c <= 2L * num_sms && len_c <= std::max(kClusterSplitKeys, len_g + len_g / 4)) {
     cluster = 1;
     split_len = static_cast<int>(len_c);
   } else {
@@ -625,10 +650,16 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
   const int smem_max = kStages * 2 * kKC * 128 * 2 + 1024;
   const dim3 block(32 * (sh.cw + 1));
   void (*kern)(CUtensorMap, CUtensorMap, AttnArgs) = nullptr;
+  // several waves of CTAs: the register-capped instance (two CTAs per SM)
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool waves = static_cast<long>(grid.x) * grid.y * grid.z > sms;
   if (a.hd == 64)
-    kern = sh.kg == 2 ? attn_tma_kernel<64, 2> : attn_tma_kernel<64, 1>;
+    kern = sh.kg == 2 ? (waves ? attn_tma_kernel<64, 2, 2> : attn_tma_kernel<64, 2, 1>)
+                      : (waves ? attn_tma_kernel<64, 1, 2> : attn_tma_kernel<64, 1, 1>);
   else if (a.hd == 128)
-    kern = sh.kg == 2 ? attn_tma_kernel<128, 2> : attn_tma_kernel<128, 1>;
+    kern = sh.kg == 2 ? attn_tma_kernel<128, 2, 1> : attn_tma_kernel<128, 1, 1>;
   else
     return PE_ERR_UNSUPPORTED;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);

@@ -34,7 +34,16 @@ constexpr size_t kSmemBudget = 212 * 1024;  // dynamic shared memory for the sta
 // 4: 303 us, 2: 301 us, none: 306 us).
 constexpr int kPrefetchKb = 2;
 constexpr int kMaxClusterSplits = 8;        // portable cluster size
-constexpr int kMaxPartialSplits = 16;       // splits storing their own partial sums
+#ifndef PE_MAX_PARTIAL_SPLITS
+#define PE_MAX_PARTIAL_SPLITS 16
+#endif
+constexpr int kMaxPartialSplits = PE_MAX_PARTIAL_SPLITS;  // splits storing their own partials
+// Weight boxes of the first stages issued before the dependency wait (1), or
+// only the first k-blocks pulled into L2 (0).  Measured slightly slower at
+// every workload (2-6 us per step), so off.
+#ifndef PE_EARLY_WEIGHTS
+#define PE_EARLY_WEIGHTS 0
+#endif
 static_assert(kMaxPartialSplits <= 16, "the projection test hook holds 16 partial tiles");
 // Weights in tile order (one contiguous 16 KB block per weight box) or row-major
 // (measured, LM head at B=1 with two CTAs per SM: 188 us packed, 192 us not).
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
     if (next_tile(p, 0, t)) {
       const int kb0 = t.ks * p.kb_per_split;
       const int nkb = min(p.num_kb, kb0 + p.kb_per_split) - kb0;
-      if (t.n == 0) {
+      if (PE_EARLY_WEIGHTS && t.n == 0) {
         const uint64_t pol_w = policy_evict_first();
         pre = min(nkb, p.stages);
         for (int s = 0; s < pre; ++s) {
@@ -714,6 +723,12 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   // split K across a cluster when one wave of plain tiles leaves SMs idle: the
   // splits of a tile must all be resident at once, their partial tile must fit
   // in the stage ring, and at least 4 k-blocks go to each split
+  // Partial sums pay for wide token tiles (their consumer adds a few splits);
+  // narrow decode tiles split many ways and reduce in a cluster instead
+  // (measured, step at B=1: 297 us with the cluster reduction, 305 us with 13
+  // partial tiles per projection; at B=64 the partial sums save 20 us).
+  partial = partial && pl.BN > kNarrowBN;
+  pl.partial = partial ? 1 : 0;
   int s = 1;
   if (allow_split && base < num_sms && partial) {
     // each split stores its own partial sum: as many as fill the CTA slots

@@ -45,6 +45,7 @@ struct TcPlan {
   int atoms;  // 64-element K atoms per stage
   int acc_bufs;  // TMEM accumulator buffers (2 = the next tile's MMA overlaps the epilogue)
   int ctas_per_sm;  // resident CTAs per SM the plan is sized for
+  int partial;      // K splits store partial sums (else they reduce in a cluster)
   size_t smem_bytes;
   // unsplit plans with several rounds of tiles: the first main_tiles run
   // persistent, the rest as clusters of tail_splits CTAs splitting K

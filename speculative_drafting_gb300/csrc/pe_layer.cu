@@ -22,7 +22,21 @@ namespace pe {
 // bf16 pair (out_lo = bf16(y - out)), and the fp32 value of what was stored
 // (out + out_lo, or y); sum_out receives x.  The row stays in registers between
 // the sum of squares and the output pass (up to kRowCache float4 per thread).
-constexpr int kRowCache = 8;
+constexpr int kRowCache = 4;
+
+template <typename T>
+PE_DEV void load_gain4(const T* g, int i, float* out) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) out[k] = Elem<T>::to_f(g[4 * i + k]);
+}
+template <>
+PE_DEV void load_gain4<bf16>(const bf16* g, int i, float* out) {
+  const uint2 u = reinterpret_cast<const uint2*>(g)[i];  // four bf16 in 8 bytes
+  out[0] = __uint_as_float(u.x << 16);
+  out[1] = __uint_as_float(u.x & 0xffff0000u);
+  out[2] = __uint_as_float(u.y << 16);
+  out[3] = __uint_as_float(u.y & 0xffff0000u);
+}
 
 template <typename T>
 __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
@@ -35,8 +49,12 @@ __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
 #pragma unroll
   for (int c = 0; c < kRowCache; ++c) {
     const int i = threadIdx.x + c * blockDim.x;
+    if (a.apply_norm && i < v4) {
+      load_gain4<T>(gam, i, gc[c]);
+    } else {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) gc[c][k] = (a.apply_norm && i < v4) ? Elem<T>::to_f(gam[4 * i + k]) : 1.f;
+      for (int k = 0; k < 4; ++k) gc[c][k] = 1.f;
+    }
   }
   pdl_wait();
   const int row = blockIdx.x;
@@ -44,18 +62,21 @@ __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
   if (a.n_rows_dev) n = min(max(*a.n_rows_dev, 0), a.rows_cap);
   if (row >= n) return;
   const size_t ro = static_cast<size_t>(row) * a.ld_x;
+  const float4* x0 = reinterpret_cast<const float4*>(a.x + ro);
+  const float4* res =
+      a.resid ? reinterpret_cast<const float4*>(a.resid + static_cast<size_t>(row) * a.ld_resid)
+              : nullptr;
   auto load = [&](int i) {
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < a.n_parts; ++k) {
+    float4 s = x0[i];
+    for (int k = 1; k < a.n_parts; ++k) {
       const float4 p = reinterpret_cast<const float4*>(a.x + k * a.part_stride + ro)[i];
       s.x += p.x;
       s.y += p.y;
       s.z += p.z;
       s.w += p.w;
     }
-    if (a.resid) {
-      const float4 r =
-          reinterpret_cast<const float4*>(a.resid + static_cast<size_t>(row) * a.ld_resid)[i];
+    if (res) {
+      const float4 r = res[i];
       s.x += r.x;
       s.y += r.y;
       s.z += r.z;
@@ -116,9 +137,8 @@ __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
   for (int i = threadIdx.x + kRowCache * blockDim.x; i < v4; i += blockDim.x) {
     // rows wider than the register cache: the sum again (sum_out is rewritten
     // with the same value)
-    float g[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) g[k] = a.apply_norm ? Elem<T>::to_f(gam[4 * i + k]) : 1.f;
+    float g[4] = {1.f, 1.f, 1.f, 1.f};
+    if (a.apply_norm) load_gain4<T>(gam, i, g);
     emit(i, load(i), g);
   }
 }
