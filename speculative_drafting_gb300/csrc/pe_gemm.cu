@@ -56,14 +56,25 @@ constexpr bool kPackedWeights = PE_PACKED_WEIGHTS != 0;
 // (measured: LM head at B=1 259 us instead of 303 us).  Wide tiles keep one atom
 // so that enough stages stay in flight.
 constexpr int kNarrowBN = 64;
+// Token tiles up to kOccBN wide run several CTAs per SM (see below), and no
+// token tile is wider than kMaxBN.  Wide tiles gain from it too (measured, LM
+// head at B=64, 448 tokens: 636 us with one CTA per SM, 535 us with two).
+#ifndef PE_OCC_BN
+#define PE_OCC_BN 256
+#endif
+#ifndef PE_MAX_BN
+#define PE_MAX_BN 256
+#endif
+constexpr int kOccBN = PE_OCC_BN;
+constexpr int kMaxBN = PE_MAX_BN;
 // Narrow token tiles run several CTAs per SM, each with its share of the SM's
 // shared memory: one CTA's loads keep only part of the SM's share of DRAM
 // bandwidth busy, whatever its ring depth (measured, LM head of 201088 x 2880 at
 // 8 tokens: 5 or 3 stages per CTA both 275 us; two CTAs of 3 stages 196 us,
-// three of 3 one-atom stages 188 us).  A long stream of tiles takes three per
-// SM; shorter GEMMs (split over K in clusters) do better with two.
+// three of 3 one-atom stages 188 us).  Up to three per SM, fewer where two
+// stages of a wide tile do not fit a third of the SM's shared memory.
 #ifndef PE_NARROW_CTAS_PER_SM
-#define PE_NARROW_CTAS_PER_SM 2
+#define PE_NARROW_CTAS_PER_SM 3
 #endif
 #ifndef PE_STREAM_CTAS_PER_SM
 #define PE_STREAM_CTAS_PER_SM 3
@@ -673,8 +684,8 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   pl.bpair = bpair;
   const int nA = dual ? 2 : 1;
   const int nB = bpair ? 2 : 1;
-  // token tile: at most 256 rows, and narrow enough that three stages fit
-  int nt = (pl.N_cap + 255) / 256;
+  // token tile: at most kMaxBN rows, and narrow enough that three stages fit
+  int nt = (pl.N_cap + kMaxBN - 1) / kMaxBN;
   size_t stage_bytes = 0;
   for (;; ++nt) {
     int bn = (pl.N_cap + nt - 1) / nt;
@@ -692,21 +703,24 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   // least two full rounds of tiles takes the most
   int occ = 1;
   size_t budget = kSmemBudget;
-  if (pl.BN <= kNarrowBN) {
+  if (pl.BN <= kOccBN) {
     const int want = pl.m_tiles * pl.n_tiles >= 2 * kStreamCtasPerSm * num_sms ? kStreamCtasPerSm
                                                                                 : kNarrowCtasPerSm;
-    const size_t b = tc_max_dyn_smem(want) - 1024;
-    int atoms = pl.atoms;
-    size_t sb = stage_bytes;
-    while (atoms > 1 && b / sb < 2) {
-      atoms /= 2;
-      sb = (static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128 * nB) * atoms;
-    }
-    if (want > 1 && b / sb >= 2) {
-      occ = want;
-      budget = b;
-      pl.atoms = atoms;
-      stage_bytes = sb;
+    // the most CTAs per SM (down from `want`) that still get two stages each
+    for (int o = want; o >= 2 && occ == 1; --o) {
+      const size_t b = tc_max_dyn_smem(o) - 1024;
+      int atoms = pl.atoms;
+      size_t sb = stage_bytes;
+      while (atoms > 1 && b / sb < 2) {
+        atoms /= 2;
+        sb = (static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128 * nB) * atoms;
+      }
+      if (b / sb >= 2) {
+        occ = o;
+        budget = b;
+        pl.atoms = atoms;
+        stage_bytes = sb;
+      }
     }
   }
   pl.num_kb = (K + kBK * pl.atoms - 1) / (kBK * pl.atoms);
