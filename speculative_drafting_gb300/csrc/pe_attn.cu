@@ -297,16 +297,34 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
         split_bf16x2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
         split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
         split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+        if constexpr (HD == 64) {
+          // all V fragments of the 16 keys first, then the high parts into every
+          // accumulator, then the low parts: an accumulator's two updates are
+          // eight MMAs apart instead of back to back
+          uint32_t bv[HD / 8][2];
 #pragma unroll
-        for (int nd = 0; nd < HD / 8; nd += 2) {
-          const int mat = lane >> 3;
-          const int key = kofs + kk * 16 + (mat & 1) * 8 + (lane & 7);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(kv_addr(vb, key, nd + (mat >> 1)), b0, b1, b2, b3);
-          mma_bf16_16816(o[nd], ph, b0, b1);
-          mma_bf16_16816(o[nd], pl, b0, b1);
-          mma_bf16_16816(o[nd + 1], ph, b2, b3);
-          mma_bf16_16816(o[nd + 1], pl, b2, b3);
+          for (int nd = 0; nd < HD / 8; nd += 2) {
+            const int mat = lane >> 3;
+            const int key = kofs + kk * 16 + (mat & 1) * 8 + (lane & 7);
+            ldmatrix_x4_trans(kv_addr(vb, key, nd + (mat >> 1)), bv[nd][0], bv[nd][1],
+                              bv[nd + 1][0], bv[nd + 1][1]);
+          }
+#pragma unroll
+          for (int nd = 0; nd < HD / 8; ++nd) mma_bf16_16816(o[nd], ph, bv[nd][0], bv[nd][1]);
+#pragma unroll
+          for (int nd = 0; nd < HD / 8; ++nd) mma_bf16_16816(o[nd], pl, bv[nd][0], bv[nd][1]);
+        } else {
+#pragma unroll
+          for (int nd = 0; nd < HD / 8; nd += 2) {
+            const int mat = lane >> 3;
+            const int key = kofs + kk * 16 + (mat & 1) * 8 + (lane & 7);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(kv_addr(vb, key, nd + (mat >> 1)), b0, b1, b2, b3);
+            mma_bf16_16816(o[nd], ph, b0, b1);
+            mma_bf16_16816(o[nd + 1], ph, b2, b3);
+            mma_bf16_16816(o[nd], pl, b0, b1);
+            mma_bf16_16816(o[nd + 1], pl, b2, b3);
+          }
         }
       }
       __syncwarp();
