@@ -136,13 +136,16 @@ PE_DEV void epi_store_elem(const Epilogue& e, int f, int t, float v, float v2) {
   }
 }
 
+// Max of a 64-bit key over the warp (all lanes active): the largest high word,
+// then the largest low word among the lanes that hold it -- the same order as
+// comparing the whole keys, in two warp reductions instead of five shuffles.
 PE_DEV unsigned long long warp_max_u64(unsigned long long k) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
-    k = other > k ? other : k;
-  }
-  return k;
+  const uint32_t hi = static_cast<uint32_t>(k >> 32), lo = static_cast<uint32_t>(k);
+  uint32_t mh, ml;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(mh) : "r"(hi));
+  const uint32_t cand = hi == mh ? lo : 0u;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(ml) : "r"(cand));
+  return (static_cast<unsigned long long>(mh) << 32) | ml;
 }
 
 // Epilogue of 16 token columns j0..j0+15 for feature f (this thread's TMEM lane).
