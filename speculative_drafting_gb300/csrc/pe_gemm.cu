@@ -149,10 +149,11 @@ PE_DEV unsigned long long warp_max_u64(unsigned long long k) {
 }
 
 // Epilogue of 16 token columns j0..j0+15 for feature f (this thread's TMEM lane).
-// Called by all 128 epilogue threads together (ARGMAX uses named barrier 1).
+// ARGMAX: each warp reduces its 32 features per column, lane i keeps column i's
+// key, and the warp folds its 16 keys into the row maxima with one atomicMax
+// each (no barrier across the epilogue warps).
 PE_DEV void tc_epilogue16(const TcArgs& p, const Epilogue& e, int f, int j0, const float* v,
-                          const float* v2, int n_rows, unsigned long long (*red)[16], int ew,
-                          int et) {
+                          const float* v2, int n_rows) {
   const bool fok = f < p.M;
   if (e.mode != EPI_ARGMAX) {
     if (!fok) return;
@@ -166,19 +167,14 @@ PE_DEV void tc_epilogue16(const TcArgs& p, const Epilogue& e, int f, int j0, con
     for (int i = 0; i < 16; ++i)
       if (j0 + i < n_rows) e.logits[static_cast<size_t>(j0 + i) * e.ld_logits + f] = v[i];
   }
+  const int lane = threadIdx.x & 31;
+  unsigned long long mine = 0ull;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const unsigned long long k = warp_max_u64(fok ? argmax_key(v[i], f) : 0ull);
-    if ((threadIdx.x & 31) == 0) red[ew][i] = k;
+    if (lane == i) mine = k;
   }
-  named_bar_sync(1, 128);
-  if (et < 16 && j0 + et < n_rows) {
-    unsigned long long k = red[0][et];
-#pragma unroll
-    for (int w = 1; w < 4; ++w) k = red[w][et] > k ? red[w][et] : k;
-    if (k) atomicMax(&e.amax[j0 + et], k);
-  }
-  named_bar_sync(1, 128);
+  if (lane < 16 && j0 + lane < n_rows && mine) atomicMax(&e.amax[j0 + lane], mine);
 }
 
 // ------------------------------------------------------------------ tcgen05 kernel
@@ -254,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, n_rows_sh;
-  __shared__ unsigned long long red_sh[4][16];
+  __shared__ unsigned long long red_sh[4];
   __shared__ int ep_ok[2][4];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -490,7 +486,6 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
     // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
     const int q = warp & 3;
     const int ew = warp - 2;
-    const int et = threadIdx.x - 64;
     const int fl = q * 32 + lane;  // this thread's feature within the tile
     uint32_t acc_phase[2] = {0u, 0u};
     int cnt = 0;
@@ -528,7 +523,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
             tc_fence_before();
             mbar_arrive(&tempty_bar[b]);
           }
-          tc_epilogue16(p, ep, f, jt + c, v, p.dual ? v2 : nullptr, n_rows, red_sh, ew, et);
+          tc_epilogue16(p, ep, f, jt + c, v, p.dual ? v2 : nullptr, n_rows);
         }
       } else {
         // park the partial tile: part[a][j][fl] (consecutive features, conflict-free)
@@ -589,11 +584,11 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
             if (p.epi.logits && f < p.M)
               p.epi.logits[static_cast<size_t>(jt + j) * p.epi.ld_logits + f] = v;
             const unsigned long long k = warp_max_u64(f < p.M ? argmax_key(v, f) : 0ull);
-            if (lane == 0) red_sh[ew][0] = k;
+            if (lane == 0) red_sh[ew] = k;
             named_bar_sync(1, 128);
             if (et == 0) {
-              unsigned long long kk = red_sh[0][0];
-              for (int w2 = 1; w2 < 4; ++w2) kk = red_sh[w2][0] > kk ? red_sh[w2][0] : kk;
+              unsigned long long kk = red_sh[0];
+              for (int w2 = 1; w2 < 4; ++w2) kk = red_sh[w2] > kk ? red_sh[w2] : kk;
               if (kk) atomicMax(&p.epi.amax[jt + j], kk);
             }
             named_bar_sync(1, 128);
