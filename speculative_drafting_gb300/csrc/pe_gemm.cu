@@ -66,6 +66,12 @@ constexpr int kNarrowBN = 64;
 #define PE_MAX_BN 256
 #endif
 constexpr int kOccBN = PE_OCC_BN;
+// Token-tile width: the widest (up to kMaxBN) whose two ring stages fit a
+// two-CTA share of an SM (1), or whose three stages fit one CTA (0).  Measured:
+// step at B=64 1207 -> 1168 us (the bf16-pair and dual GEMMs get two CTAs).
+#ifndef PE_BN_FOR_OCC2
+#define PE_BN_FOR_OCC2 1
+#endif
 constexpr int kMaxBN = PE_MAX_BN;
 // Narrow token tiles run several CTAs per SM, each with its share of the SM's
 // shared memory: one CTA's loads keep only part of the SM's share of DRAM
@@ -692,7 +698,12 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
     pl.atoms = pl.BN <= kNarrowBN ? 2 : 1;
     stage_bytes = (static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128 * nB) *
                   pl.atoms;
+#if PE_BN_FOR_OCC2
+    // wide enough, but two stages fit a two-CTA share of the SM
+    if ((kSmemPerSm / 2 - kCtaSmemOverhead) / stage_bytes >= 2 || pl.BN <= 64) break;
+#else
     if (kSmemBudget / stage_bytes >= 3 || pl.BN <= 64) break;
+#endif
   }
   pl.n_tiles = (pl.N_cap + pl.BN - 1) / pl.BN;
   pl.m_tiles = (M + kBM - 1) / kBM;
