@@ -28,11 +28,23 @@ enum {
                                  schedule with its tail split */
   PE_PROJ_PAIR = 0x200,       /* bf16 only: X holds n rows of high parts followed
                                  by n rows of low parts; the operand is hi + lo */
-  PE_PROJ_PARTIAL = 0x400     /* not with PE_PROJ_SWIGLU: each K split stores its
+  PE_PROJ_PARTIAL = 0x400,    /* not with PE_PROJ_SWIGLU: each K split stores its
                                  partial sum, out = float [16][n][M] (split k at
                                  out + k*n*M; tiles past the split count are left
                                  as they were); the result is their sum */
+  PE_PROJ_TWO_SM = 0x800,     /* bf16 only: run the 2-SM schedule (clusters of two
+                                 CTAs issuing M = 256 MMAs) whatever the size,
+                                 for token tiles of 16 rows or more; never splits K */
+  PE_PROJ_ONE_SM = 0x1000,    /* bf16 only: never the 2-SM schedule */
+  PE_PROJ_ARGMAX = 0x2000     /* PE_PROJ_LM only: the LM head with its argmax
+                                 epilogue, as pe_argmax runs it: out = float
+                                 logits [n][V]; the argmax of each row (int32 [n])
+                                 is written to the workspace at byte offset
+                                 PE_PROJ_ARGMAX_TOKENS_OFFSET(n) */
 };
+
+/* where PE_PROJ_ARGMAX leaves the row maxima' indices in the workspace */
+#define PE_PROJ_ARGMAX_TOKENS_OFFSET(n) (256u + (((size_t)(n) * 8u + 255u) / 256u) * 256u)
 
 /* Workspace bytes pe_test_projection needs for n_rows rows (0 on bad input). */
 size_t pe_test_projection_workspace(const pe_handle* h, int which, int n_rows);

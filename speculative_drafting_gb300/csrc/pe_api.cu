@@ -50,9 +50,10 @@ GemmShape gemm_shape(const pe_handle* h, int id) {
 }
 
 TcPlan plan_of(const pe_handle* h, int id, int N, bool bpair, bool allow_split = true,
-               bool partial = false) {
+               bool partial = false, int two_sm = -1) {
   const GemmShape s = gemm_shape(h, id);
-  return plan_gemm_tc(s.M, s.K, N, s.dual, bpair ? 1 : 0, h->num_sms, allow_split, partial);
+  return plan_gemm_tc(s.M, s.K, N, s.dual, bpair ? 1 : 0, h->num_sms, allow_split, partial,
+                      two_sm);
 }
 
 // The projections whose K splits store partial sums (EPI_PARTIAL_F32) for the
@@ -100,8 +101,8 @@ struct Layout {
   // a / a_lo / a_f: MLP operand pair and its fp32 value; h / h_lo: SwiGLU
   // product pair; part: the split partial sums of fc, QKV, O and down (one at
   // a time: each is read by the next kernel before the next projection stores);
-  // amax: argmax keys
-  size_t status, x, u, u_lo, q_s, x_s, attn, r, a, a_lo, a_f, h, h_lo, part, amax, attn_part;
+  // amax: argmax keys; tok: the test hook's argmax indices
+  size_t status, x, u, u_lo, q_s, x_s, attn, r, a, a_lo, a_f, h, h_lo, part, amax, attn_part, tok;
   size_t total;
 };
 
@@ -163,7 +164,9 @@ Layout layout_argmax(const pe_handle* h, int n_rows) {
 }
 
 // Workspace of one projection (test hook) over n_rows rows.
-Layout layout_projection(const pe_handle* h, int which, int n_rows) {
+// The test hook's workspace: the status word; with the argmax epilogue, the
+// row keys and the row maxima's indices (at PE_PROJ_ARGMAX_TOKENS_OFFSET).
+Layout layout_projection(const pe_handle* h, int which, int n_rows, bool argmax = false) {
   Layout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -172,8 +175,12 @@ Layout layout_projection(const pe_handle* h, int which, int n_rows) {
     return o;
   };
   L.status = take(256);
+  if (argmax) {
+    L.amax = take(static_cast<size_t>(n_rows) * sizeof(unsigned long long));
+    L.tok = take(static_cast<size_t>(n_rows) * sizeof(int32_t));
+  }
+  (void)h;
   (void)which;
-  (void)n_rows;
   L.total = off;
   return L;
 }
@@ -198,7 +205,7 @@ int check_meta(const pe_meta* m) {
 // epi.mode EPI_PARTIAL_F32: *n_parts receives the number of partial tiles stored.
 int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
              const int* n_rows_dev, const Epilogue& epi, void* ws, const Layout& L,
-             cudaStream_t st, bool allow_split = true, int* n_parts = nullptr) {
+             cudaStream_t st, bool allow_split = true, int* n_parts = nullptr, int two_sm = -1) {
   const GemmShape s = gemm_shape(h, id);
   const bool partial = epi.mode == EPI_PARTIAL_F32;
   if (n_parts) *n_parts = 1;
@@ -210,7 +217,7 @@ int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
     return launch_gemm_f32(static_cast<const float*>(W), static_cast<const float*>(W2),
                            static_cast<const float*>(X), s.M, s.K, N_cap, n_rows_dev, epi, st);
   }
-  const TcPlan p = plan_of(h, id, N_cap, X_lo != nullptr, allow_split, partial);
+  const TcPlan p = plan_of(h, id, N_cap, X_lo != nullptr, allow_split, partial, two_sm);
   if (n_parts) *n_parts = p.partial ? p.k_splits : 1;
   Epilogue ep = epi;
   if (partial && !p.partial) ep.mode = EPI_STORE_F32;  // the splits reduce in a cluster
@@ -592,9 +599,11 @@ int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, fl
 }
 
 size_t pe_test_projection_workspace(const pe_handle* h, int which, int n_rows) {
-  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR | PE_PROJ_PARTIAL);
+  const bool argmax = (which & PE_PROJ_ARGMAX) != 0;
+  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR | PE_PROJ_PARTIAL | PE_PROJ_TWO_SM |
+             PE_PROJ_ONE_SM | PE_PROJ_ARGMAX);
   if (!h || which < 0 || which >= G_COUNT || n_rows < 1) return 0;
-  return layout_projection(h, which, n_rows).total;
+  return layout_projection(h, which, n_rows, argmax).total;
 }
 
 int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void* out, void* ws,
@@ -602,16 +611,34 @@ int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void*
   const bool persistent = (which & PE_PROJ_PERSISTENT) != 0;
   const bool pair = (which & PE_PROJ_PAIR) != 0;
   const bool partial = (which & PE_PROJ_PARTIAL) != 0;
-  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR | PE_PROJ_PARTIAL);
+  const bool argmax = (which & PE_PROJ_ARGMAX) != 0;
+  if ((which & PE_PROJ_TWO_SM) && (which & PE_PROJ_ONE_SM)) return PE_ERR_ARG;
+  const int two_sm = (which & PE_PROJ_TWO_SM) ? 1 : (which & PE_PROJ_ONE_SM) ? 0 : -1;
+  which &= ~(PE_PROJ_PERSISTENT | PE_PROJ_PAIR | PE_PROJ_PARTIAL | PE_PROJ_TWO_SM |
+             PE_PROJ_ONE_SM | PE_PROJ_ARGMAX);
   if (partial && which == G_GATEUP) return PE_ERR_ARG;
+  if (argmax && (which != G_LM || partial || pair)) return PE_ERR_ARG;
   if (!h || !h->has_layer || which < 0 || which >= G_COUNT || n_rows < 1 || !X || !out || !ws)
     return PE_ERR_ARG;
   if (!aligned16(X) || !aligned16(ws)) return PE_ERR_ARG;
   if (pair && !is_bf16(h)) return PE_ERR_UNSUPPORTED;
-  const Layout L = layout_projection(h, which, n_rows);
+  const Layout L = layout_projection(h, which, n_rows, argmax);
   if (ws_bytes < L.total) return PE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const GemmShape s = gemm_shape(h, which);
+  if (argmax) {
+    unsigned long long* keys = at<unsigned long long>(ws, L.amax);
+    if (launch_zero_keys(keys, n_rows, st) != PE_OK) return PE_ERR_CUDA;
+    Epilogue e;
+    e.mode = EPI_ARGMAX;
+    e.amax = keys;
+    e.logits = static_cast<float*>(out);
+    e.ld_logits = s.M;
+    const int rc = run_gemm(h, which, X, nullptr, n_rows, nullptr, e, ws, L, st, !persistent,
+                            nullptr, two_sm);
+    if (rc != PE_OK) return rc;
+    return launch_argmax_finalize(keys, n_rows, at<int32_t>(ws, L.tok), st);
+  }
   Epilogue e;
   e.mode = which == G_GATEUP ? EPI_SWIGLU : partial ? EPI_PARTIAL_F32 : EPI_STORE_F32;
   e.out = out;
@@ -621,7 +648,8 @@ int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void*
       pair ? static_cast<const void*>(static_cast<const bf16_t*>(X) +
                                       static_cast<size_t>(n_rows) * s.K)
            : nullptr;
-  return run_gemm(h, which, X, X_lo, n_rows, nullptr, e, ws, L, st, !persistent);
+  return run_gemm(h, which, X, X_lo, n_rows, nullptr, e, ws, L, st, !persistent, nullptr,
+                  two_sm);
 }
 
 int pe_read_status(const pe_handle* h, void* ws, uint32_t* status, int clear, void* stream) {

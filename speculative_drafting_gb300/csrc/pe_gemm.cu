@@ -85,6 +85,16 @@ constexpr int kMaxBN = PE_MAX_BN;
 #ifndef PE_STREAM_CTAS_PER_SM
 #define PE_STREAM_CTAS_PER_SM 3
 #endif
+// Wide token tiles streamed over at least two rounds of weight-tile pairs run
+// as 2-SM pairs (1) or one CTA per tile, two CTAs per SM (0).  Measured, LM
+// head of 201088 x 2880 at 448 tokens: 723 us as pairs, 459 us one-SM; of
+// 128256 x 4096 at 256 tokens: 362 us against 258 us.  One thread issuing
+// tcgen05.mma keeps an SM's tensor pipe only about half busy, whatever the
+// instruction's M, so two issuing CTAs per SM beat one pair per two SMs.
+#ifndef PE_TWO_SM
+#define PE_TWO_SM 0
+#endif
+constexpr bool kTwoSm = PE_TWO_SM != 0;
 constexpr int kNarrowCtasPerSm = PE_NARROW_CTAS_PER_SM;
 constexpr int kStreamCtasPerSm = PE_STREAM_CTAS_PER_SM;
 // shared memory of an SM that its CTAs can have (228 KB less 1 KB)
@@ -154,10 +164,20 @@ PE_DEV unsigned long long warp_max_u64(unsigned long long k) {
   return (static_cast<unsigned long long>(mh) << 32) | ml;
 }
 
+// Largest value over the warp (all lanes active); NaN if any lane holds NaN.
+PE_DEV float warp_max_f32(float v) {
+  float m;
+  asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+  return m;
+}
+
 // Epilogue of 16 token columns j0..j0+15 for feature f (this thread's TMEM lane).
-// ARGMAX: each warp reduces its 32 features per column, lane i keeps column i's
-// key, and the warp folds its 16 keys into the row maxima with one atomicMax
-// each (no barrier across the epilogue warps).
+// ARGMAX: per column the warp takes the largest of its 32 features' values in
+// one reduction and the first lane holding it from a ballot; lane i keeps
+// column i's value and lane, builds its key, and the warp folds its 16 keys
+// into the row maxima with one atomicMax each (no barrier across the epilogue
+// warps).  Equal values resolve to the lowest feature, NaN counts as the
+// largest (argmax_key orders the maxima of different warps the same way).
 PE_DEV void tc_epilogue16(const TcArgs& p, const Epilogue& e, int f, int j0, const float* v,
                           const float* v2, int n_rows) {
   const bool fok = f < p.M;
@@ -174,13 +194,22 @@ PE_DEV void tc_epilogue16(const TcArgs& p, const Epilogue& e, int f, int j0, con
       if (j0 + i < n_rows) e.logits[static_cast<size_t>(j0 + i) * e.ld_logits + f] = v[i];
   }
   const int lane = threadIdx.x & 31;
-  unsigned long long mine = 0ull;
+  float best = 0.f;
+  uint32_t holders = 0u;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const unsigned long long k = warp_max_u64(fok ? argmax_key(v[i], f) : 0ull);
-    if (lane == i) mine = k;
+    const float x = fok ? v[i] : -INFINITY;
+    const float m = warp_max_f32(x);
+    const uint32_t hit = __ballot_sync(0xffffffffu, fok && (m != m ? x != x : x == m));
+    if (lane == i) {
+      best = m;
+      holders = hit;
+    }
   }
-  if (lane < 16 && j0 + lane < n_rows && mine) atomicMax(&e.amax[j0 + lane], mine);
+  if (lane < 16 && j0 + lane < n_rows && holders) {
+    const int first = __ffs(static_cast<int>(holders)) - 1;
+    atomicMax(&e.amax[j0 + lane], argmax_key(best, static_cast<uint32_t>(f - lane + first)));
+  }
 }
 
 // ------------------------------------------------------------------ tcgen05 kernel
@@ -618,6 +647,297 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
   }
 }
 
+// ------------------------------------------------------------------ tcgen05 kernel, 2-SM pairs
+//
+// Wide token tiles over many weight tiles (the LM head of a batch): a cluster
+// of two CTAs on two SMs runs M = 256 MMAs, so each MMA instruction does twice
+// the work and each SM stages only half of the token tile.  Pair tile
+// (mp, n) covers weight tiles 2mp (rank 0) and 2mp + 1 (rank 1) and token
+// tile n; each rank loads its weight box and token rows n*BN + rank*BN/2 ..
+// + BN/2 into its own ring, and its TMEM lanes hold its own weight tile's
+// accumulator (all BN token columns).  Roles per CTA, as in the 1-SM kernel:
+// warp 0 lane 0 loads; on rank 0 warp 1 lane 0 issues the MMAs and commits to
+// the stage and accumulator barriers of both CTAs; on rank 1 warp 1 lane 0
+// reports each stage of its ring as landed to rank 0's full barrier (its own
+// loads complete on its own barriers, so each CTA only ever waits for copies
+// into its own shared memory); warps 2-5 run the same epilogue on their own
+// accumulator and report it drained to rank 0.  Clusters take pair tiles
+// c, c + clusters, ... (persistent).
+
+PE_DEV bool next_pair_tile(const TcArgs& p, int it, uint32_t rank, TileRef& t) {
+  const int clusters = static_cast<int>(gridDim.x >> 1);
+  const int local = static_cast<int>(blockIdx.x >> 1) + it * clusters;
+  if (local >= p.tile_count) return false;
+  const int tile = p.tile_base + local;
+  t.ks = 0;
+  t.n = tile % p.n_tiles;
+  t.m = 2 * (tile / p.n_tiles) + static_cast<int>(rank);
+  return true;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mapA,
+                        const __grid_constant__ CUtensorMap mapA2,
+                        const __grid_constant__ CUtensorMap mapB,
+                        const __grid_constant__ CUtensorMap mapB2, const TcArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh, n_rows_sh;
+  __shared__ int ep_ok[2][4];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int nA = p.dual ? 2 : 1;
+  const int nB = p.bpair ? 2 : 1;
+  const int hn = p.BN / 2;  // token rows of the tile in this CTA's ring
+  const uint32_t bh_bytes = static_cast<uint32_t>(hn) * 128u;
+  const uint32_t stage_bytes = kABytes * nA + bh_bytes * nB;
+  const int nbuf = p.acc_bufs;
+  const uint32_t buf_cols = static_cast<uint32_t>(p.BN * nA);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      // rank 0: its own loads' arrival and rank 1's report for the same stage
+      mbar_init(&full_bar[s], rank == 0 ? 2 : 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 8);  // the 4 epilogue warps of both CTAs
+    }
+    mbar_init(&final_bar, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&mapA);
+    if (p.dual) prefetch_tmap(&mapA2);
+    prefetch_tmap(&mapB);
+    if (p.bpair) prefetch_tmap(&mapB2);
+    // the weights do not depend on the previous kernel: pull the first
+    // k-blocks of the first tile into L2 while it finishes
+    TileRef t;
+    if (next_pair_tile(p, 0, rank, t)) {
+      for (int kb = 0; kb < min(p.num_kb, kPrefetchKb); ++kb) {
+        int cx, cy;
+        weight_box(p, t.m, kb * kBK, cx, cy);
+        tma_prefetch_l2_2d(&mapA, cx, cy);
+        if (p.dual) tma_prefetch_l2_2d(&mapA2, cx, cy);
+      }
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_base_sh, p.tmem_cols);
+    tmem_relinquish_pair();
+  }
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    int n = p.N_cap;
+    if (p.n_rows_dev) {
+      const int v = *p.n_rows_dev;
+      n = v < 0 ? 0 : (v < n ? v : n);
+    }
+    n_rows_sh = n;
+  }
+  // both CTAs' barriers are initialised and their TMEM allocated before
+  // either touches the other's
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();
+  tc_fence_after();
+
+  const uint32_t tmem_base = tmem_base_sh;
+  const int n_rows = n_rows_sh;
+  volatile int* abort_flag = &abort_sh;
+  auto fail = [&]() {
+    abort_sh = 1;
+    set_status(p.status, PE_ST_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs, into their own ring)
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      TileRef t;
+      bool ok = true;
+      for (int it = 0; ok && next_pair_tile(p, it, rank, t) && !*abort_flag; ++it) {
+        if (tile_skipped(p, t, it, n_rows)) continue;
+        const int y = t.n * p.BN + static_cast<int>(rank) * hn;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
+          uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes;
+          int cx, cy;
+          weight_box(p, t.m, kb * kBK, cx, cy);
+          tma_load_2d(sa, &mapA, &full_bar[stage], cx, cy, pol_w);
+          if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], cx, cy, pol_w);
+          tma_load_2d(sa + kABytes * nA, &mapB, &full_bar[stage], kb * kBK, y, pol_x);
+          if (p.bpair)
+            tma_load_2d(sa + kABytes * nA + bh_bytes, &mapB2, &full_bar[stage], kb * kBK, y, pol_x);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let this CTA's copies in flight land before its shared memory goes
+        // away (on rank 0 the wait may also run out for want of rank 1's
+        // report: it is bounded)
+        for (int s = 0; s < p.stages; ++s)
+          if (armed & (1u << s)) {
+            int dummy = 0;
+            mbar_wait(&full_bar[s], (armed_parity >> s) & 1u, &dummy);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer of the pair
+      const uint32_t idesc = idesc_bf16_f32(2 * kBM, p.BN);
+      int stage = 0, cnt = 0;
+      uint32_t phase = 0, acc_phase[2] = {0u, 0u};
+      TileRef t;
+      for (int it = 0; next_pair_tile(p, it, rank, t) && !*abort_flag; ++it) {
+        if (tile_skipped(p, t, it, n_rows)) continue;
+        const int b = cnt % nbuf;
+        ++cnt;
+        if (!mbar_wait_cluster(&tempty_bar[b], acc_phase[b] ^ 1u, abort_flag)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(b) * buf_cols;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait_cluster(&full_bar[stage], phase, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
+          const uint64_t adesc = sw128_kmajor_desc(sa);
+          const uint64_t a2desc = sw128_kmajor_desc(sa + kABytes);
+          const uint64_t bdesc = sw128_kmajor_desc(sa + kABytes * nA);
+          const uint64_t b2desc = sw128_kmajor_desc(sa + kABytes * nA + bh_bytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            umma_bf16_pair(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, acc);
+            if (p.bpair) umma_bf16_pair(d0, adesc + 2 * kk, b2desc + 2 * kk, idesc, 1u);
+            if (p.dual) {
+              const uint32_t d1 = d0 + static_cast<uint32_t>(p.BN);
+              umma_bf16_pair(d1, a2desc + 2 * kk, bdesc + 2 * kk, idesc, acc);
+              if (p.bpair) umma_bf16_pair(d1, a2desc + 2 * kk, b2desc + 2 * kk, idesc, 1u);
+            }
+          }
+          umma_commit_pair_both(&empty_bar[stage]);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_both(&tfull_bar[b]);
+        acc_phase[b] ^= 1u;
+      }
+      // every MMA issued by this thread has finished before either CTA
+      // releases its TMEM or leaves
+      umma_commit_pair_local(&final_bar);
+      int dummy = 0;
+      mbar_wait(&final_bar, 0, &dummy);
+    } else if (lane == 0) {
+      // ---------------- rank 1: report each landed stage to rank 0
+      const uint32_t full0 = cluster_addr_of(&full_bar[0], 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      TileRef t;
+      bool ok = true;
+      for (int it = 0; ok && next_pair_tile(p, it, rank, t) && !*abort_flag; ++it) {
+        if (tile_skipped(p, t, it, n_rows)) continue;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(full0 + static_cast<uint32_t>(stage) * 8u);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    const int fl = q * 32 + lane;
+    const uint32_t tempty0 = cluster_addr_of(&tempty_bar[0], 0);
+    uint32_t acc_phase[2] = {0u, 0u};
+    int cnt = 0;
+    TileRef t;
+    for (int it = 0; next_pair_tile(p, it, rank, t) && !*abort_flag; ++it) {
+      if (tile_skipped(p, t, it, n_rows)) continue;
+      const int b = cnt % nbuf;
+      const int par = cnt & 1;
+      ++cnt;
+      const bool ok = mbar_wait(&tfull_bar[b], acc_phase[b], abort_flag);
+      if (lane == 0) ep_ok[par][ew] = ok ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!(ep_ok[par][0] && ep_ok[par][1] && ep_ok[par][2] && ep_ok[par][3])) {
+        fail();
+        break;
+      }
+      acc_phase[b] ^= 1u;
+      tc_fence_after();
+      const int f = t.m * kBM + fl;
+      const int jt = t.n * p.BN;
+      const uint32_t tl = tmem_base + static_cast<uint32_t>(b) * buf_cols +
+                          (static_cast<uint32_t>(q * 32) << 16);
+      for (int c = 0; c < p.BN; c += 16) {
+        float v[16], v2[16];
+        tmem_ld16(tl + c, v);
+        if (p.dual) tmem_ld16(tl + p.BN + c, v2);
+        if (c + 16 >= p.BN) {
+          // last TMEM read of this buffer: the warp hands it back to rank 0
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(b) * 8u);
+        }
+        tc_epilogue16(p, p.epi, f, jt + c, v, p.dual ? v2 : nullptr, n_rows);
+      }
+    }
+  }
+
+  // no CTA releases TMEM or leaves while the other may still use its
+  // barriers, shared memory or accumulator
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, p.tmem_cols);
+  }
+}
+
 // ------------------------------------------------------------------ host: plan + launch
 
 static_assert(kNarrowCtasPerSm >= 1 && kNarrowCtasPerSm <= 3, "CTAs per SM");
@@ -678,8 +998,45 @@ static int max_active_clusters(int occ, int cs, size_t smem) {
   return n * occ;
 }
 
+static cudaError_t tc_pair_prepare() {
+  const cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBudget + 1024));
+  cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
+// Clusters of two pair-kernel CTAs with `smem` bytes each resident at once.
+static int max_pair_clusters(size_t smem) {
+  static std::mutex mu;
+  static std::map<size_t, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(smem);
+  if (it != cache.end()) return it->second;
+  tc_pair_prepare();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 64);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)gemm_tc_pair_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[smem] = n;
+  return n;
+}
+
 TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split,
-                    bool partial) {
+                    bool partial, int two_sm) {
   TcPlan pl{};
   pl.M = M;
   pl.K = K;
@@ -707,6 +1064,37 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   }
   pl.n_tiles = (pl.N_cap + pl.BN - 1) / pl.BN;
   pl.m_tiles = (M + kBM - 1) / kBM;
+  {
+    // 2-SM pairs: the MMA of one thread does twice the work, and an SM stages
+    // half of the token tile, so a deeper ring fits (measured, LM head of
+    // 201088 x 2880 at 448 tokens: see the kernel's comment)
+    const int pair_tiles = (pl.m_tiles + 1) / 2 * pl.n_tiles;
+    const bool use2 = two_sm > 0 ? pl.BN >= 32
+                                 : two_sm < 0 && kTwoSm && pl.BN > kNarrowBN &&
+                                       pair_tiles >= 2 * (num_sms / 2);
+    if (use2) {
+      pl.cta2 = 1;
+      pl.atoms = 1;
+      pl.ctas_per_sm = 1;
+      pl.partial = 0;
+      pl.num_kb = (K + kBK - 1) / kBK;
+      const size_t sb = static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN / 2) * 128 * nB;
+      pl.stages = std::max(2, std::min(kMaxStages, static_cast<int>(kSmemBudget / sb)));
+      pl.smem_bytes = pl.stages * sb + 1024;
+      pl.k_splits = 1;
+      pl.kb_per_split = pl.num_kb;
+      pl.acc_bufs = 2 * pl.BN * nA <= 512 ? 2 : 1;
+      uint32_t c = 32;
+      while (c < static_cast<uint32_t>(pl.acc_bufs * pl.BN * nA)) c <<= 1;
+      pl.tmem_cols = static_cast<int>(c);
+      const int clusters = max_pair_clusters(pl.smem_bytes);
+      pl.grid = 2 * std::max(1, std::min(pair_tiles, clusters));
+      pl.main_tiles = pair_tiles;
+      pl.tail_splits = 1;
+      pl.tail_kb_per_split = pl.num_kb;
+      return pl;
+    }
+  }
   // CTAs per SM: narrow tiles share each SM among several CTAs of at least two
   // stages each (fewer atoms per stage where that is what fits); a stream of at
   // least two full rounds of tiles takes the most
@@ -850,12 +1238,61 @@ static int launch_one(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorM
              : PE_ERR_CUDA;
 }
 
+// The 2-SM schedule: clusters of two CTAs over all pair tiles, persistent.
+static int launch_pair(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap* mapA2,
+                       const CUtensorMap& mapB, const CUtensorMap& mapB2, const int* n_rows_dev,
+                       const Epilogue& epi, uint32_t* status, cudaStream_t st) {
+  TcArgs a{};
+  a.M = pl.M;
+  a.K = pl.K;
+  a.N_cap = pl.N_cap;
+  a.dual = pl.dual;
+  a.bpair = pl.bpair;
+  a.tile_base = 0;
+  a.tile_count = pl.main_tiles;
+  a.BN = pl.BN;
+  a.n_tiles = pl.n_tiles;
+  a.m_tiles = pl.m_tiles;
+  a.k_splits = 1;
+  a.packed = kPackedWeights ? 1 : 0;
+  a.k_atoms = (pl.K + kBK - 1) / kBK;
+  a.kb_per_split = pl.num_kb;
+  a.num_kb = pl.num_kb;
+  a.atoms = 1;
+  a.stages = pl.stages;
+  a.acc_bufs = pl.acc_bufs;
+  a.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
+  a.n_rows_dev = n_rows_dev;
+  a.epi = epi;
+  a.status = status;
+  if (epi.mode == EPI_PARTIAL_F32) return PE_ERR_ARG;  // pairs never split K
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = pl.smem_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, *mapA, pl.dual ? *mapA2 : *mapA, mapB,
+                            mapB2, a) == cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
+}
+
 int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap* mapA2,
                    const void* X, const void* X_lo, const int* n_rows_dev, const Epilogue& epi,
                    uint32_t* status, cudaStream_t st) {
   if (pl.dual && !mapA2) return PE_ERR_ARG;
   if (pl.bpair && !X_lo) return PE_ERR_ARG;
-  const uint32_t b_box = static_cast<uint32_t>(pl.BN);
+  // a pair stages half of the token tile in each CTA
+  const uint32_t b_box = static_cast<uint32_t>(pl.cta2 ? pl.BN / 2 : pl.BN);
   CUtensorMap mapB, mapB2;
   if (!encode_tmap_bf16(&mapB, X, static_cast<uint64_t>(pl.N_cap), static_cast<uint64_t>(pl.K),
                         b_box))
@@ -869,6 +1306,10 @@ int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap*
   }
   // one attribute value per instance for every launch, so kernels captured
   // into a graph stay launchable whatever order they replay in
+  if (pl.cta2) {
+    if (tc_pair_prepare() != cudaSuccess) return PE_ERR_CUDA;
+    return launch_pair(pl, mapA, mapA2, mapB, mapB2, n_rows_dev, epi, status, st);
+  }
   if (tc_prepare(pl.ctas_per_sm) != cudaSuccess) return PE_ERR_CUDA;
   const int base = pl.m_tiles * pl.n_tiles;
   if (pl.k_splits > 1)
