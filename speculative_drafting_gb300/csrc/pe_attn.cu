@@ -119,6 +119,9 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
   const int P0 = L - a.K;  // position of the first draft query (the NTP row)
   const int t0 = split * a.split_len;
   const int t1 = min(L, t0 + a.split_len);
+  // a split past the request's keys: nothing to write, the combine stops
+  // before it (a cluster's CTAs all take part in its merge)
+  if (!a.cluster && split > 0 && t0 >= L) return;
   const int n_chunks = t1 > t0 ? (t1 - t0 + kKC - 1) / kKC : 0;
   const size_t n_samp = static_cast<size_t>(a.B) * a.K;
   volatile int* abort_flag = &abort_sh;
@@ -491,47 +494,64 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
   cluster_sync_all();
 }
 
-// out[s][h*hd + d] = sum_j 2^(m_j - M) o_j[d] / sum_j 2^(m_j - M) l_j.
-// Warp 0 turns the (m_j, l_j) of the splits into weights once; then every
-// thread sums its dimensions over the splits.
-template <typename T>
-__global__ void attn_combine_kernel(const AttnArgs a) {
-  __shared__ float w_sh[kMaxSplits];
-  __shared__ float inv_sh;
+// out[s][h*hd + d] = sum_j 2^(m_j - M) o_j[d] / sum_j 2^(m_j - M) l_j over the
+// splits j that hold keys of the request (j * split_len < L; the CTAs of the
+// others return at once and leave no partial).  One warp per (sample row,
+// query head): each lane owns hd/32 consecutive dimensions; the splits' loads
+// are independent, their sum runs in split order.
+template <typename T, int HD>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
+  constexpr int V = HD / 32;
   pdl_trigger();
   pdl_wait();
-  const size_t sh = blockIdx.x;  // (sample, head)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t n_sh = static_cast<size_t>(a.B) * a.K * a.H;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float M = -INFINITY;
-    for (int j = lane; j < a.n_splits; j += 32) M = fmaxf(M, a.part_ml[(j * n_sh + sh) * 2]);
-    M = warp_max(M);
-    float den = 0.f;
-    for (int j = lane; j < a.n_splits; j += 32) {
-      const float m = a.part_ml[(j * n_sh + sh) * 2];
-      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      w_sh[j] = w;
-      den += w * a.part_ml[(j * n_sh + sh) * 2 + 1];
-    }
-    den = warp_sum(den);
-    if (lane == 0) inv_sh = den > 0.f ? 1.f / den : 0.f;
+  const size_t sh = static_cast<size_t>(blockIdx.x) * 4 + warp;  // (sample, head)
+  if (sh >= n_sh) return;
+  const int r = static_cast<int>(sh / (static_cast<size_t>(a.K) * a.H));
+  const int L = min(max(a.seq_len[r], 0), a.max_blocks * a.bs);
+  const int n = max(1, min(a.n_splits, (L + a.split_len - 1) / a.split_len));
+  auto ml = [&](int j) { return a.part_ml + (static_cast<size_t>(j) * n_sh + sh) * 2; };
+  float M = -INFINITY;
+  for (int j = lane; j < n; j += 32) M = fmaxf(M, ml(j)[0]);
+  M = warp_max(M);
+  float den = 0.f;
+  for (int j = lane; j < n; j += 32) {
+    const float m = ml(j)[0];
+    den += (m == -INFINITY ? 0.f : exp2f(m - M)) * ml(j)[1];
   }
-  __syncthreads();
-  const float inv = inv_sh;
-  for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {
-    // eight independent accumulators keep eight split loads in flight
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int j = 0;
-    for (; j + 8 <= a.n_splits; j += 8) {
+  den = warp_sum(den);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  float acc[V];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        acc[u] += w_sh[j + u] * a.part_o[((j + u) * n_sh + sh) * a.hd + d];
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    float w = 0.f;
+    if (j0 + lane < n) {
+      const float m = ml(j0 + lane)[0];
+      w = m == -INFINITY ? 0.f : exp2f(m - M);
     }
-    for (; j < a.n_splits; ++j) acc[0] += w_sh[j] * a.part_o[(j * n_sh + sh) * a.hd + d];
-    const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-    static_cast<T*>(a.out)[sh * a.hd + d] = Elem<T>::from_f(sum * inv);
+    const int cnt = min(32, n - j0);
+#pragma unroll 4
+    for (int u = 0; u < cnt; ++u) {
+      const float wu = __shfl_sync(0xffffffffu, w, u);
+      const float* po = a.part_o + (static_cast<size_t>(j0 + u) * n_sh + sh) * HD + lane * V;
+      if constexpr (V == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(po);
+        acc[0] += wu * x.x;
+        acc[1] += wu * x.y;
+        acc[2] += wu * x.z;
+        acc[3] += wu * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(po);
+        acc[0] += wu * x.x;
+        acc[1] += wu * x.y;
+      }
+    }
   }
+  T* out = static_cast<T*>(a.out) + sh * HD + lane * V;
+#pragma unroll
+  for (int i = 0; i < V; ++i) out[i] = Elem<T>::from_f(acc[i] * inv);
 }
 
 // fp32: one CTA (4 warps) per (sample row, query head)
@@ -713,8 +733,9 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
   AttnArgs ag = a;
   ag.cluster = 0;
   if (launch_pdl(kern, grid, block, smem, st, kmap, vmap, ag) != cudaSuccess) return PE_ERR_CUDA;
-  return launch_pdl(attn_combine_kernel<bf16>, dim3(a.B * a.K * a.H), dim3(std::min(a.hd, 128)), 0,
-                    st, ag) == cudaSuccess
+  const dim3 cgrid(static_cast<unsigned>((static_cast<size_t>(a.B) * a.K * a.H + 3) / 4));
+  return launch_pdl(a.hd == 64 ? attn_combine_kernel<bf16, 64> : attn_combine_kernel<bf16, 128>,
+                    cgrid, dim3(128), 0, st, ag) == cudaSuccess
              ? PE_OK
              : PE_ERR_CUDA;
 }

@@ -23,6 +23,9 @@ CASES = [
     ("small_postnorm_hd128", {"post_norm": False, "accepted": (0, 2, 0, 8)}),
     ("small_prenorm", {"K": 1}),
     ("small_prenorm", {"batch": 12, "n_prev": 6, "ctx": ("uniform", 0, 700), "seed": 3}),
+    # enough requests that attention splits merge through global memory: the
+    # combine stops at each request's own last split
+    ("small_prenorm", {"batch": 160, "n_prev": 6, "ctx": ("uniform", 0, 700), "seed": 5}),
 ]
 
 
