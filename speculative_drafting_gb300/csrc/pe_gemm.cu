@@ -100,8 +100,14 @@ constexpr int kStreamCtasPerSm = PE_STREAM_CTAS_PER_SM;
 // shared memory of an SM that its CTAs can have (228 KB less 1 KB)
 constexpr size_t kSmemPerSm = 227 * 1024;
 // per CTA beside its ring: the system's 1 KB, the static barriers and
-// reduction buffers (under 1 KB), the ring's 1 KB alignment slack, and a margin
+// reduction buffers (under 1 KB), the ring's 1 KB alignment slack, and a
+// margin; the vector-store instances also hold the epilogue warps' store
+// scratch (8.25 KB)
 constexpr size_t kCtaSmemOverhead = 5 * 1024;
+constexpr size_t kEpiScratchBytes = 9 * 1024;
+constexpr size_t cta_smem_overhead(bool vec) {
+  return vec ? kCtaSmemOverhead + kEpiScratchBytes : kCtaSmemOverhead;
+}
 constexpr int kTcThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;
 
@@ -212,6 +218,113 @@ PE_DEV void tc_epilogue16(const TcArgs& p, const Epilogue& e, int f, int j0, con
   }
 }
 
+// Stores of a warp's 32 features x 16 token columns (j0..j0+15) with 4
+// consecutive features per lane and instruction: the block passes through the
+// warp's shared scratch w ([16][33] floats, padded rows: no bank conflicts), so
+// each store instruction writes four token rows of 128 contiguous bytes rather
+// than one.  (Measured, B=64 step: the partial-sum tiles of fc, QKV, O and down
+// stored one float per lane: 1146 us; this way: 1091 us.)
+constexpr int kEpiScratch = 16 * 33;  // floats per epilogue warp
+
+// Whether the stores of epilogue `e` can go 4 features at a time: rows of a
+// multiple of 4 elements and 16-byte aligned bases.
+PE_DEV bool epi_vec_ok(const TcArgs& p, const Epilogue& e) {
+  auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  if (e.mode == EPI_ARGMAX || (p.M & 3) || (e.ld_out & 3) || !al(e.out)) return false;
+  if (e.mode == EPI_RESID_F32 && ((e.ld_resid & 3) || !al(e.resid))) return false;
+  if (e.mode == EPI_SWIGLU_PAIR && !al(e.out2)) return false;
+  return true;
+}
+
+// Four outputs of token row t, features fb..fb+3, from accumulator values x (and
+// y, the second accumulator of the dual modes).
+PE_DEV void epi_store4(const Epilogue& e, int t, int fb, const float* x, const float* y) {
+  const size_t o = static_cast<size_t>(t) * e.ld_out + fb;
+  switch (e.mode) {
+    case EPI_STORE_F32:
+    case EPI_PARTIAL_F32:  // (out already points at this split's partial tile)
+      *reinterpret_cast<float4*>(static_cast<float*>(e.out) + o) =
+          make_float4(x[0], x[1], x[2], x[3]);
+      break;
+    case EPI_RESID_F32: {
+      const float4 r =
+          *reinterpret_cast<const float4*>(e.resid + static_cast<size_t>(t) * e.ld_resid + fb);
+      *reinterpret_cast<float4*>(static_cast<float*>(e.out) + o) =
+          make_float4(x[0] + r.x, x[1] + r.y, x[2] + r.z, x[3] + r.w);
+      break;
+    }
+    case EPI_STORE:
+      *reinterpret_cast<uint2*>(static_cast<bf16*>(e.out) + o) =
+          make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+      break;
+    case EPI_SWIGLU: {
+      float h[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) h[k] = x[k] / (1.0f + expf(-x[k])) * y[k];
+      *reinterpret_cast<uint2*>(static_cast<bf16*>(e.out) + o) =
+          make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+      break;
+    }
+    case EPI_SWIGLU_PAIR: {
+      float h[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) h[k] = x[k] / (1.0f + expf(-x[k])) * y[k];
+      uint32_t hi01, lo01, hi23, lo23;
+      split_bf16x2(h[0], h[1], hi01, lo01);
+      split_bf16x2(h[2], h[3], hi23, lo23);
+      *reinterpret_cast<uint2*>(static_cast<bf16*>(e.out) + o) = make_uint2(hi01, hi23);
+      *reinterpret_cast<uint2*>(static_cast<bf16*>(e.out2) + o) = make_uint2(lo01, lo23);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+// f0: the warp's first feature; v (and v2 for dual modes): this lane's 16
+// accumulator columns for feature f0 + lane.
+PE_DEV void tc_store16_vec(const TcArgs& p, const Epilogue& e, int f0, int j0, const float* v,
+                           const float* v2, int n_rows, float* w) {
+  const int lane = threadIdx.x & 31;
+  const int fq = (lane & 7) * 4;  // this lane's 4 features ...
+  const int tr = lane >> 3;       // ... of token rows tr, tr + 4, tr + 8, tr + 12
+  const int fb = f0 + fq;
+  const bool live = fb < p.M;     // M is a multiple of 4: all four features or none
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i * 33 + lane] = v[i];
+  __syncwarp();
+  if (!v2) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      float x[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) x[k] = w[(tr + 4 * s) * 33 + fq + k];
+      const int t = j0 + tr + 4 * s;
+      if (live && t < n_rows) epi_store4(e, t, fb, x, nullptr);
+    }
+    __syncwarp();
+    return;
+  }
+  float a[4][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[s][k] = w[(tr + 4 * s) * 33 + fq + k];
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i * 33 + lane] = v2[i];
+  __syncwarp();
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    float y[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = w[(tr + 4 * s) * 33 + fq + k];
+    const int t = j0 + tr + 4 * s;
+    if (live && t < n_rows) epi_store4(e, t, fb, a[s], y);
+  }
+  __syncwarp();
+}
+
 // ------------------------------------------------------------------ tcgen05 kernel
 //
 // Two schedules share the kernel:
@@ -274,7 +387,11 @@ PE_DEV bool tile_skipped(const TcArgs& p, const TileRef& t, int it, int n_rows) 
 
 // OCC: CTAs per SM the instance is launched for (each instance keeps its own
 // fixed shared-memory limit, so graph replays of either stay launchable).
-template <int OCC>
+// VEC: the instance for token tiles of 32 rows or more at up to two CTAs per
+// SM, whose stores go 4 features at a time through a shared scratch (the
+// argmax epilogue and decode tiles of 16 rows keep the scalar instance:
+// measured, LM head at B=64 458 us in it, 477 us in a shared one).
+template <int OCC, bool VEC>
 __global__ void __launch_bounds__(kTcThreads, OCC)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
                    const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapB2,
@@ -287,6 +404,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
   __shared__ int abort_sh, n_rows_sh;
   __shared__ unsigned long long red_sh[4];
   __shared__ int ep_ok[2][4];
+  __shared__ float epi_sh[VEC ? 4 : 1][VEC ? kEpiScratch : 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -549,6 +667,7 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
         Epilogue ep = p.epi;
         if (ep.mode == EPI_PARTIAL_F32)
           ep.out = static_cast<float*>(ep.out) + static_cast<size_t>(t.ks) * ep.part_stride;
+        const bool vec = VEC && epi_vec_ok(p, ep);
         for (int c = 0; c < p.BN; c += 16) {
           float v[16], v2[16];
           tmem_ld16(tl + c, v);
@@ -557,6 +676,13 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
             // last TMEM read of this buffer: hand it back before the stores
             tc_fence_before();
             mbar_arrive(&tempty_bar[b]);
+          }
+          if constexpr (VEC) {
+            if (vec) {
+              tc_store16_vec(p, ep, f - lane, jt + c, v, p.dual ? v2 : nullptr, n_rows,
+                             epi_sh[ew]);
+              continue;
+            }
           }
           tc_epilogue16(p, ep, f, jt + c, v, p.dual ? v2 : nullptr, n_rows);
         }
@@ -687,6 +813,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, n_rows_sh;
   __shared__ int ep_ok[2][4];
+  __shared__ float epi_sh[4][kEpiScratch];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -891,6 +1018,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int ew = warp - 2;
     const int fl = q * 32 + lane;
     const uint32_t tempty0 = cluster_addr_of(&tempty_bar[0], 0);
+    const bool vec = epi_vec_ok(p, p.epi);
     uint32_t acc_phase[2] = {0u, 0u};
     int cnt = 0;
     TileRef t;
@@ -922,7 +1050,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(b) * 8u);
         }
-        tc_epilogue16(p, p.epi, f, jt + c, v, p.dual ? v2 : nullptr, n_rows);
+        if (vec)
+          tc_store16_vec(p, p.epi, f - lane, jt + c, v, p.dual ? v2 : nullptr, n_rows, epi_sh[ew]);
+        else
+          tc_epilogue16(p, p.epi, f, jt + c, v, p.dual ? v2 : nullptr, n_rows);
       }
     }
   }
@@ -942,27 +1073,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 static_assert(kNarrowCtasPerSm >= 1 && kNarrowCtasPerSm <= 3, "CTAs per SM");
 static_assert(kStreamCtasPerSm >= 1 && kStreamCtasPerSm <= 3, "CTAs per SM");
-using TcKernelFn = decltype(&gemm_tc_kernel<1>);
+using TcKernelFn = decltype(&gemm_tc_kernel<1, false>);
 
-// The instance for `occ` CTAs per SM.
-static TcKernelFn tc_kernel(int occ) {
-  return occ >= 3 ? gemm_tc_kernel<3> : occ == 2 ? gemm_tc_kernel<2> : gemm_tc_kernel<1>;
+// The instance for `occ` CTAs per SM, with vector stores or not (these exist
+// for up to two CTAs per SM).
+static TcKernelFn tc_kernel(int occ, bool vec) {
+  if (vec && occ <= 2) return occ == 2 ? gemm_tc_kernel<2, true> : gemm_tc_kernel<1, true>;
+  return occ >= 3 ? gemm_tc_kernel<3, false>
+                  : occ == 2 ? gemm_tc_kernel<2, false> : gemm_tc_kernel<1, false>;
 }
 
 // Dynamic shared memory limit of an instance: its largest ring plus the 1 KB
 // alignment slack.  The limit, not a launch's own size, decides how many CTAs
 // of the function the SM takes, so it is what makes `occ` CTAs fit.
-static size_t tc_max_dyn_smem(int occ) {
-  return occ > 1 ? kSmemPerSm / occ - kCtaSmemOverhead + 1024 : kSmemBudget + 1024;
+static size_t tc_max_dyn_smem(int occ, bool vec) {
+  return occ > 1 ? kSmemPerSm / occ - cta_smem_overhead(vec) + 1024 : kSmemBudget + 1024;
 }
 
-// Set an instance's attributes: the same values at every launch.
+// Set the attributes of the `occ` instances: the same values at every launch.
 static cudaError_t tc_prepare(int occ) {
-  const TcKernelFn k = tc_kernel(occ);
-  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(tc_max_dyn_smem(occ)));
-  cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
-                       cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = cudaSuccess;
+  for (const bool vec : {false, true}) {
+    if (vec && occ > 2) continue;
+    const TcKernelFn k = tc_kernel(occ, vec);
+    const cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(tc_max_dyn_smem(occ, vec)));
+    if (r != cudaSuccess) e = r;
+    cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+  }
   return e;
 }
 
@@ -990,7 +1129,7 @@ static int max_active_clusters(int occ, int cs, size_t smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, (void*)tc_kernel(occ), &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)tc_kernel(occ, false), &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -1057,7 +1196,7 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
                   pl.atoms;
 #if PE_BN_FOR_OCC2
     // wide enough, but two stages fit a two-CTA share of the SM
-    if ((kSmemPerSm / 2 - kCtaSmemOverhead) / stage_bytes >= 2 || pl.BN <= 64) break;
+    if ((kSmemPerSm / 2 - cta_smem_overhead(true)) / stage_bytes >= 2 || pl.BN <= 64) break;
 #else
     if (kSmemBudget / stage_bytes >= 3 || pl.BN <= 64) break;
 #endif
@@ -1098,6 +1237,11 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   // CTAs per SM: narrow tiles share each SM among several CTAs of at least two
   // stages each (fewer atoms per stage where that is what fits); a stream of at
   // least two full rounds of tiles takes the most
+  // token tiles of 32 rows or more take the vector-store instances (their
+  // scratch comes out of the ring's share) where they run at most two CTAs per
+  // SM; decode tiles of 16 rows keep the ring (measured, B=1 step: 3 us more
+  // with one stage less for gate/up)
+  const bool wide = pl.BN >= 32;
   int occ = 1;
   size_t budget = kSmemBudget;
   if (pl.BN <= kOccBN) {
@@ -1105,7 +1249,7 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
                                                                                 : kNarrowCtasPerSm;
     // the most CTAs per SM (down from `want`) that still get two stages each
     for (int o = want; o >= 2 && occ == 1; --o) {
-      const size_t b = tc_max_dyn_smem(o) - 1024;
+      const size_t b = tc_max_dyn_smem(o, wide && o <= 2) - 1024;
       int atoms = pl.atoms;
       size_t sb = stage_bytes;
       while (atoms > 1 && b / sb < 2) {
@@ -1128,6 +1272,7 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
   // does run two such CTAs side by side: the fit is the arithmetic above, and
   // no CTA outside a cluster waits for another, so it is only a speed matter)
   pl.ctas_per_sm = occ;
+  pl.vec = wide && occ <= 2 ? 1 : 0;
   // the resident CTAs of one wave; every "SM" count below is in these slots
   num_sms *= occ;
   const int base = pl.m_tiles * pl.n_tiles;
@@ -1231,7 +1376,11 @@ static int launch_one(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorM
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = (k_splits > 1 && epi.mode != EPI_PARTIAL_F32) ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, tc_kernel(pl.ctas_per_sm), *mapA, pl.dual ? *mapA2 : *mapA, mapB,
+  // the vector-store instance for the stores of a wide tile; the argmax
+  // epilogue and cluster-reduced splits take the scalar one
+  const bool vec = pl.vec && epi.mode != EPI_ARGMAX && cfg.numAttrs == 1;
+  return cudaLaunchKernelEx(&cfg, tc_kernel(pl.ctas_per_sm, vec), *mapA,
+                            pl.dual ? *mapA2 : *mapA, mapB,
                             mapB2, a) ==
                  cudaSuccess
              ? PE_OK

@@ -47,6 +47,7 @@ struct TcPlan {
   int ctas_per_sm;  // resident CTAs per SM the plan is sized for
   int partial;      // K splits store partial sums (else they reduce in a cluster)
   int cta2;         // 2-SM pairs: clusters of two CTAs run M = 256 MMAs over pair tiles
+  int vec;          // wide tiles: the instance whose stores go 4 features at a time
   size_t smem_bytes;
   // unsplit plans with several rounds of tiles: the first main_tiles run
   // persistent, the rest as clusters of tail_splits CTAs splitting K
