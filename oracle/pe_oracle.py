@@ -19,7 +19,9 @@ Sources (the pages this restates):
           learn": section 2 (EAGLE-3 feeds the fused target hidden states through
           an fc projection into one pre-norm decoder layer), section 4.1 (RMS is
           ||x||_2 / sqrt(d)), Observation 2 (an RMSNorm on each captured target
-          stream before the fc), abstract and section 1 (post-norm drafter).
+          stream before the fc), abstract and section 1 (post-norm drafter);
+          section 2 also states verification: the target scores the drafts in
+          one pass and keeps the longest prefix it accepts (verify_greedy).
   [RFC]   "[RFC]: Add random anchor for p-eagle first position": the P-EAGLE
           drafter is one transformer layer fed by three auxiliary verifier hidden
           streams.
@@ -458,3 +460,53 @@ def prepare_inputs(dims, w, batch):
     E = embed_rows(meta, lambda t: decode(w["emb"][t], dt), decode(w["emb_mask"], dt))
     A = drafter_input(G, E, decode(w["gamma_stream"], dt), dims.eps, dt)
     return meta, G, E, A
+
+
+# ---------------------------------------------------------------------------
+# greedy verification (closes the loop into the next step's accepted counts
+# and bonus tokens)
+
+
+def target_argmax(logits):
+    """Greedy token of each verify row: the index of the largest logit, lowest
+    index on ties, a NaN counting as larger than every number (numpy's argmax
+    rule: the first NaN wins).  -0.0 and +0.0 are equal.  Logits are decoded to
+    fp64 first, which is exact for fp32 and bf16 inputs."""
+    return np.argmax(np.asarray(logits, dtype=np.float64), axis=-1).astype(np.int32)
+
+
+def verify_greedy(qsl, tok, logits):
+    """Greedy verification of a ragged verify batch.
+
+    "Attention Drift", section 2 (preliminaries): the target scores the drafted
+    tokens in one forward pass and keeps the longest prefix its own
+    distribution accepts.  The drafts here are greedy, so the target's
+    distribution is read at temperature 0 and acceptance is exact agreement
+    with the target's greedy token.
+
+    Request r owns verify rows qsl[r] .. qsl[r+1]-1 (n_r of them).  Row 0 of a
+    request carries the last committed token, row j >= 1 carries draft j, and
+    logits[row] are the target's logits after that row's token.  So draft j is
+    accepted when it equals the target's greedy token of row j-1 and every
+    earlier draft was accepted; the bonus (correction) token is the target's
+    greedy token right after the accepted prefix.
+
+    Returns (target_tok[T_in] i32, accepted[B] i32, bonus[B] i32).  An empty
+    request (n_r = 0) gets accepted 0 and bonus -1.
+    """
+    qsl = np.asarray(qsl, dtype=np.int64)
+    tok = np.asarray(tok, dtype=np.int64)
+    B = len(qsl) - 1
+    target = target_argmax(logits) if len(tok) else np.zeros(0, np.int32)
+    accepted = np.zeros(B, dtype=np.int32)
+    bonus = np.full(B, -1, dtype=np.int32)
+    for r in range(B):
+        q0, n = int(qsl[r]), int(qsl[r + 1] - qsl[r])
+        if n <= 0:
+            continue
+        a = 0
+        while a + 1 < n and tok[q0 + a + 1] == target[q0 + a]:
+            a += 1
+        accepted[r] = a
+        bonus[r] = target[q0 + a]
+    return target, accepted, bonus

@@ -46,6 +46,8 @@ NAME_INDEX = {
     "w_lm": 11,
     "k_cache": 12,
     "v_cache": 13,
+    "verify_logits": 14,
+    "verify_plan": 15,
 }
 
 
@@ -319,3 +321,107 @@ def make_kv_cache(wl: Workload, num_blocks: int) -> tuple:
     shp = (num_blocks, dm.n_kv_heads, dm.block_size, dm.head_dim)
     return (draw(wl.seed, "k_cache", shp, 1.0, dm.dtype),
             draw(wl.seed, "v_cache", shp, 1.0, dm.dtype))
+
+
+# ---------------------------------------------------------------------------
+# greedy verification batches
+
+
+@dataclasses.dataclass(frozen=True)
+class VerifyWorkload:
+    """A verify batch: the target's logits over every verify row of a ragged
+    batch, plus the row tokens (the last committed token, then the drafts)."""
+
+    name: str
+    batch: int
+    # verify rows per request (n_r = K + 1 for K drafts); an int or a tuple
+    n_rows: object
+    vocab: int
+    dtype: str = "f32"  # logits dtype: "f32" or "bf16"
+    # fraction of rows whose greatest logit is planted at two indices
+    tie_frac: float = 0.0
+    seed: int = 0
+    description: str = ""
+
+    def n_rows_list(self):
+        if isinstance(self.n_rows, int):
+            return [self.n_rows] * self.batch
+        assert len(self.n_rows) == self.batch
+        return list(self.n_rows)
+
+
+VERIFY_WORKLOADS = {
+    # K = 7 drafts per request (8 verify rows) against a GPT-OSS-20B-sized vocabulary
+    "verify_b64_k7": VerifyWorkload(
+        name="verify_b64_k7", batch=64, n_rows=8, vocab=201088, dtype="f32", tie_frac=0.05,
+        description="greedy verification of K=7 drafts, B=64, V=201088, fp32 logits"),
+    "verify_b64_k7_bf16": VerifyWorkload(
+        name="verify_b64_k7_bf16", batch=64, n_rows=8, vocab=201088, dtype="bf16",
+        tie_frac=0.05,
+        description="greedy verification of K=7 drafts, B=64, V=201088, bf16 logits"),
+    "verify_b1_k7": VerifyWorkload(
+        name="verify_b1_k7", batch=1, n_rows=8, vocab=201088, dtype="f32", tie_frac=0.0,
+        description="greedy verification of K=7 drafts, B=1, V=201088, fp32 logits"),
+    # small ragged cases: rows of 1001 fp32 / 777 bf16 logits start off the
+    # 16-byte grid, one request has no drafts
+    "verify_small": VerifyWorkload(
+        name="verify_small", batch=5, n_rows=(8, 1, 3, 8, 2), vocab=1001, dtype="f32",
+        tie_frac=0.3, description="small ragged verify batch, V=1001, fp32 logits"),
+    "verify_small_bf16": VerifyWorkload(
+        name="verify_small_bf16", batch=4, n_rows=(9, 2, 1, 5), vocab=777, dtype="bf16",
+        tie_frac=0.3, description="small ragged verify batch, V=777, bf16 logits"),
+}
+
+# every drawn logit lies in [-LOGIT_CLIP, LOGIT_CLIP]; the planted greatest
+# logit of a row is PLANTED_MAX, exact in fp32 and bf16
+LOGIT_CLIP = 8.0
+PLANTED_MAX = 9.0
+
+
+def get_verify(name: str, **overrides) -> VerifyWorkload:
+    wl = VERIFY_WORKLOADS[name]
+    return dataclasses.replace(wl, **overrides) if overrides else wl
+
+
+def make_verify_batch(wl: VerifyWorkload) -> dict:
+    """Host arrays of one verify batch, with the target's greedy tokens and the
+    accepted counts planted by construction.
+
+    Logits are N(0, 1) clipped to [-8, 8]; each row's greatest logit (9.0) is
+    planted at a uniform index g (and, in a tie_frac share of rows, also at a
+    second, larger index, so the lowest-index rule picks g).  Per request a
+    planted count a* ~ U[0, n_r - 1]: drafts 1..a* copy the planted tokens of
+    the rows before them, draft a*+1 differs from its row's planted token, and
+    the other tokens are uniform.
+
+    Returns qsl[B+1] i32, tok[T_in] i32, logits[T_in][V] (f32, or bf16 bits),
+    planted_target[T_in] i32, planted_accepted[B] i32, T_in, B, V.
+    """
+    n_rows = np.array(wl.n_rows_list(), dtype=np.int64)
+    B, V = wl.batch, wl.vocab
+    qsl = np.zeros(B + 1, dtype=np.int32)
+    qsl[1:] = np.cumsum(n_rows)
+    T_in = int(qsl[-1])
+    g = _seq(wl.seed, "verify_plan", 0)
+    logits = normal_f32(wl.seed, "verify_logits", T_in * V).reshape(T_in, V)
+    np.clip(logits, -LOGIT_CLIP, LOGIT_CLIP, out=logits)
+    target = g.integers(0, V, size=T_in).astype(np.int32)
+    tie = g.random(T_in) < wl.tie_frac
+    rows = np.arange(T_in)
+    logits[rows, target] = PLANTED_MAX
+    for i in np.nonzero(tie & (target < V - 1))[0]:
+        logits[i, g.integers(int(target[i]) + 1, V)] = PLANTED_MAX
+    tok = g.integers(0, V, size=T_in).astype(np.int32)
+    accepted = np.zeros(B, dtype=np.int32)
+    for r in range(B):
+        q0, n = int(qsl[r]), int(n_rows[r])
+        if n == 0:
+            continue
+        a = int(g.integers(0, n))
+        accepted[r] = a
+        tok[q0 + 1: q0 + 1 + a] = target[q0: q0 + a]
+        if a + 1 < n:
+            tok[q0 + a + 1] = (int(target[q0 + a]) + 1 + int(g.integers(0, V - 1))) % V
+    out = f32_to_bf16_bits(logits) if wl.dtype == "bf16" else logits
+    return dict(qsl=qsl, tok=tok, logits=out, planted_target=target,
+                planted_accepted=accepted, T_in=T_in, B=B, V=V)
