@@ -9,6 +9,9 @@ kernel time comes from a loop of the LM head's own graph right after.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
+A verify_* workload times pe_verify_greedy (the greedy verification that yields
+the next step's accepted counts and bonus tokens) instead of the draft step.
+
 Prints one JSON line.  --impl reference times the CPU oracle (the only
 reference this build has) on a bounded sample of the same workload.
 """
@@ -443,9 +446,188 @@ def graph_kernel_nodes(graph):
         return None
 
 
+# ----------------------------------------------------------------------------- verification
+
+
+VERIFY_METRIC = "greedy verification latency (us); HBM GB/s %peak"
+
+
+def verify_oracle_sample(wl, b, budget_s):
+    """Time the oracle's verification (as it stands) on whole batches until the
+    budget is spent.  Returns (us per batch, sample text, threads)."""
+    from oracle import pe_oracle as O
+
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        O.verify_greedy(b["qsl"], b["tok"], O.decode(b["logits"], wl.dtype))
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sample = f"{done} whole batch(es) of {wl.name} ({b['T_in']} rows x {wl.vocab} logits), {dt:.1f} s"
+    return dt / done * 1e6, sample, 1
+
+
+def run_verify(args, rank, world, local):
+    """pe_verify_greedy over one seeded verify batch per rank.  Inputs sit in HBM;
+    L2 is flushed (a 256 MB write, then a read of it) before every timed call, and
+    each call is timed alone with CUDA events on its stream."""
+    import torch
+
+    from speculative_drafting_gb300 import binding, build
+
+    wl = W.get_verify(args.workload)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        b = W.make_verify_batch(wl)
+        per, sample, threads = [], "", 1
+        t_all = time.perf_counter()
+        for _ in range(max(1, args.steps)):
+            us, sample, threads = verify_oracle_sample(wl, b, budget_s=5.0)
+            per.append(us)
+            if time.perf_counter() - t_all > 150:
+                break
+        us = statistics.median(per)
+        print(json.dumps({
+            "impl": "reference", "metric": VERIFY_METRIC, "value": us, "unit": "us",
+            "n_gpus": args.gpus, "steps": len(per), "warmup": 0, "ms_per_step": us / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "global_batch": wl.batch,
+                                            "description": wl.description},
+            "cpu_baseline": {"value": us, "unit": "us", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    b = W.make_verify_batch(W.get_verify(args.workload, seed=wl.seed + rank))
+    B, T_in, V = b["B"], b["T_in"], b["V"]
+    esize = 2 if wl.dtype == "bf16" else 4
+    code = binding.PE_DTYPE_BF16 if wl.dtype == "bf16" else binding.PE_DTYPE_F32
+    lg_host = torch.from_numpy(b["logits"].view(np.int16) if wl.dtype == "bf16" else b["logits"])
+    d = {"qsl": torch.from_numpy(b["qsl"]).cuda(), "tok": torch.from_numpy(b["tok"]).cuda(),
+         "logits": lg_host.cuda()}
+    target = torch.empty(T_in, dtype=torch.int32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    bon = torch.empty(B, dtype=torch.int32, device="cuda")
+    ws = binding.verify_workspace(T_in, V)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def call():
+        binding.verify_greedy(B, T_in, d["qsl"], d["tok"], d["logits"], V, code, target, acc, bon,
+                              ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    stream.synchronize()
+    st, _ = binding.read_status_ws(ws, stream=stream)
+    if st:
+        raise RuntimeError(f"device status {st:#x} on the verify batch")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call()
+    def flush_l2():
+        # write a buffer twice the size of L2, then read it back: the read evicts
+        # the dirty lines, so no write-back lands inside the timed call
+        flush.zero_()
+        flush.max()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            flush_l2()
+            g.replay()
+    stream.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush_l2()
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    call_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    if world > 1:
+        t = torch.tensor([call_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        call_ms = float(t.item())
+    # end to end: pinned host logits and tokens in, target tokens and counts out
+    h_in = {"qsl": torch.from_numpy(b["qsl"]).pin_memory(),
+            "tok": torch.from_numpy(b["tok"]).pin_memory(), "logits": lg_host.pin_memory()}
+    h_out = [torch.empty(T_in, dtype=torch.int32).pin_memory(),
+             torch.empty(B, dtype=torch.int32).pin_memory(),
+             torch.empty(B, dtype=torch.int32).pin_memory()]
+    n_e2e = max(5, args.steps // 4)
+    with torch.cuda.stream(stream):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            for k, t in h_in.items():
+                d[k].copy_(t, non_blocking=True)
+            g.replay()
+            for hst, dev in zip(h_out, (target, acc, bon)):
+                hst.copy_(dev, non_blocking=True)
+        a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / n_e2e
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    if rank == 0:
+        peaks, src = measured_peaks()
+        alg = T_in * V * esize + T_in * 4 * 2 + (B + 1) * 4 + 2 * B * 4
+        achieved = alg / (call_ms / 1e3) / 1e9
+        cpu = None
+        if not args.no_cpu_baseline:
+            us, sample, threads = verify_oracle_sample(wl, b, budget_s=10.0)
+            cpu = {"value": us, "unit": "us", "cores": threads, "kind": "oracle", "sample": sample}
+        print(json.dumps({
+            "metric": VERIFY_METRIC, "value": call_ms * 1e3, "unit": "us", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": call_ms,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if wl.dtype == "f32" else "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "global_batch": B * world, "rows": T_in, "vocab": V,
+                       "description": wl.description, "cuda_graph": True,
+                       "l2": "flushed before every timed call (256 MB write, then a 256 MB "
+                             "read, so no dirty line is written back inside the call)",
+                       "parallelism": f"replica x{world} (independent batches per GPU)"},
+            "clocks": clk,
+            "e2e": {"value": e2e_ms * 1e3, "unit": "us", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps,
+            "roofline": {"kernel": "verify_partial_kernel + verify_accept_kernel (whole call)",
+                         "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": src, "algorithmic_bytes": alg,
+                         "avg_launch_us": call_ms * 1e3},
+            "cpu_baseline": cpu}), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.workload in W.VERIFY_WORKLOADS:
+        run_verify(args, rank, world, local)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

@@ -22,6 +22,8 @@
  *                      the context plus earlier draft positions, SwiGLU MLP,
  *                      pre-norm or post-norm residuals) and the final norm.
  *   pe_argmax          the LM head fused with a per-row greedy argmax.
+ *   pe_verify_greedy   the target's greedy verification of the drafts, which
+ *                      yields the next step's accepted counts and bonus tokens.
  *
  * Conventions for every call
  *   - All tensor arguments are DEVICE pointers owned by the caller; the library
@@ -74,6 +76,9 @@ extern "C" {
                                      [0, num_blocks) or negative position: slot -1,
                                      the key is skipped by attention */
 #define PE_ST_TOKEN_RANGE 0x4u    /* token id outside [0, V): embedding row 0 is used */
+#define PE_ST_ROWS_RANGE 0x8u     /* pe_verify_greedy: qsl is not a non-decreasing run
+                                     from 0 to T_in; each request is clamped to
+                                     the rows in range */
 #define PE_ST_TIMEOUT 0x10u       /* a bounded wait inside a kernel expired */
 
 /* padding slot of rejected rows ("KV cache and CUDA graphs") */
@@ -232,9 +237,42 @@ int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, fl
 int pe_argmax_noalloc(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens,
                       float* logits, void* stream);
 
+/* Greedy verification of the drafts: the step that produces the next
+ * pe_prepare_inputs' accepted counts and bonus tokens.  "Attention Drift",
+ * section 2 (preliminaries): the target scores the drafted tokens in one forward
+ * pass and keeps the longest prefix it accepts; with greedy drafts that is
+ * exact agreement with the target's greedy token.  Needs no handle.
+ *   qsl[B+1]       int32 row offsets of the verify batch: request r owns rows
+ *                  qsl[r] .. qsl[r+1]-1 (n_r >= 0 rows); qsl[0] = 0, qsl[B] = T_in
+ *   tok[T_in]      int32 token of each verify row: row 0 of a request holds the
+ *                  last committed token, row j >= 1 its draft j
+ *   logits         [T_in][vocab] the target's logits after each row's token,
+ *                  float (PE_DTYPE_F32) or bf16 bits (PE_DTYPE_BF16); rows need
+ *                  no particular alignment beyond the element size
+ *   target_tok[T_in] out: greedy token of each row (largest logit, lowest index
+ *                  on ties, -0 equal to +0, a NaN above every number)
+ *   accepted[B]    out: a_r = the largest m <= n_r - 1 with tok[qsl[r]+j] ==
+ *                  target_tok[qsl[r]+j-1] for every j = 1..m
+ *   bonus[B]       out: target_tok[qsl[r] + a_r] (the correction or next token);
+ *                  a request with no rows gets accepted 0 and bonus -1
+ *   ws             device workspace of pe_verify_workspace_bytes(T_in, vocab)
+ *                  bytes or more, 256-byte aligned; its first word is the status
+ *                  word (read with pe_read_status, handle NULL allowed)
+ * The logits are read once (the call is bound by their bytes).  A qsl that is
+ * not a non-decreasing run from 0 to T_in sets PE_ST_ROWS_RANGE and each request
+ * is clamped to the rows in range; rows outside every request get no target
+ * token.  PE_ERR_ARG: negative sizes, null pointers, logits not aligned to the
+ * element size, ws misaligned or too small, B = 0 with T_in > 0. */
+size_t pe_verify_workspace_bytes(int max_rows_in, int vocab);
+int pe_verify_greedy(int B, int T_in, const int32_t* qsl, const int32_t* tok,
+                     const void* logits, int vocab, int dtype, int32_t* target_tok,
+                     int32_t* accepted, int32_t* bonus, void* ws, size_t ws_bytes,
+                     void* stream);
+
 /* Copy the device status word from ws into *status (synchronises `stream`);
  * clear it when `clear` is non-zero.  Returns PE_OK when no bit is set,
- * PE_ERR_TIMEOUT when PE_ST_TIMEOUT is set, else PE_ERR_DEVICE_INPUT. */
+ * PE_ERR_TIMEOUT when PE_ST_TIMEOUT is set, else PE_ERR_DEVICE_INPUT.  h may be
+ * NULL (the word lives in ws; pe_verify_greedy has no handle). */
 int pe_read_status(const pe_handle* h, void* ws, uint32_t* status, int clear, void* stream);
 
 /* Static text for a return code. */

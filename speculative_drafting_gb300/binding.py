@@ -23,6 +23,7 @@ PE_ERR_TIMEOUT = 5
 PE_ST_ACCEPTED_RANGE = 0x1
 PE_ST_BLOCK_RANGE = 0x2
 PE_ST_TOKEN_RANGE = 0x4
+PE_ST_ROWS_RANGE = 0x8
 PE_ST_TIMEOUT = 0x10
 PE_DTYPE_F32 = 0
 PE_DTYPE_BF16 = 1
@@ -102,6 +103,11 @@ def load(path: str | None = None):
     lib.pe_test_projection_workspace.restype = _sz
     lib.pe_test_projection.argtypes = [_vp, _i32, _vp, _i32, _vp, _vp, _sz, _vp]
     lib.pe_test_projection.restype = _i32
+    lib.pe_verify_workspace_bytes.argtypes = [_i32, _i32]
+    lib.pe_verify_workspace_bytes.restype = _sz
+    lib.pe_verify_greedy.argtypes = [_i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp,
+                                     _sz, _vp]
+    lib.pe_verify_greedy.restype = _i32
     _lib = lib
     return lib
 
@@ -252,3 +258,39 @@ class Drafter:
         if rc not in (PE_OK, PE_ERR_DEVICE_INPUT, PE_ERR_TIMEOUT):
             raise PeError(rc, "pe_read_status")
         return int(v.value), rc
+
+
+# ----------------------------------------------------------------------------- verification
+
+
+def verify_workspace_bytes(max_rows_in: int, vocab: int) -> int:
+    n = int(load().pe_verify_workspace_bytes(int(max_rows_in), int(vocab)))
+    if n == 0:
+        raise PeError(PE_ERR_ARG, "pe_verify_workspace_bytes")
+    return n
+
+
+def verify_workspace(max_rows_in: int, vocab: int, device="cuda"):
+    """A device workspace for pe_verify_greedy (torch allocates it 256-byte aligned)."""
+    import torch
+
+    return torch.zeros(verify_workspace_bytes(max_rows_in, vocab), dtype=torch.uint8,
+                       device=device)
+
+
+def verify_greedy(B, T_in, qsl, tok, logits, vocab, dtype, target_tok, accepted, bonus, ws,
+                  stream=None):
+    """pe_verify_greedy on device tensors; dtype is PE_DTYPE_F32 or PE_DTYPE_BF16."""
+    rc = load().pe_verify_greedy(int(B), int(T_in), _ptr(qsl), _ptr(tok), _ptr(logits),
+                                 int(vocab), int(dtype), _ptr(target_tok), _ptr(accepted),
+                                 _ptr(bonus), _ptr(ws), int(ws.numel()), _stream(stream))
+    _check(rc, "pe_verify_greedy")
+
+
+def read_status_ws(ws, clear=True, stream=None):
+    """pe_read_status without a handle (the verification call has none)."""
+    v = ctypes.c_uint32(0)
+    rc = load().pe_read_status(None, _ptr(ws), ctypes.byref(v), int(clear), _stream(stream))
+    if rc not in (PE_OK, PE_ERR_DEVICE_INPUT, PE_ERR_TIMEOUT):
+        raise PeError(rc, "pe_read_status")
+    return int(v.value), rc

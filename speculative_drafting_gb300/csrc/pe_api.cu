@@ -653,7 +653,8 @@ int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void*
 }
 
 int pe_read_status(const pe_handle* h, void* ws, uint32_t* status, int clear, void* stream) {
-  if (!h || !ws || !status) return PE_ERR_ARG;
+  (void)h;  // the word lives in ws; handle-free calls pass NULL
+  if (!ws || !status) return PE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t v = 0;
   if (cudaMemcpyAsync(&v, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)

@@ -149,12 +149,28 @@ PE_DEV uint32_t smem_u32(const void* p) {
 // Orderable key of (value, index) for a max-reduction that prefers the lowest
 // index among equal values: high word = float bits mapped to an unsigned order,
 // low word = ~index.
-PE_DEV unsigned long long argmax_key(float v, uint32_t idx) {
+PE_DEV uint32_t argmax_order(float v) {
   // -0 counts as +0 and every NaN as the largest value, so that equal values
   // resolve to the lowest index whichever kernel compares them
   uint32_t u = v == 0.f ? 0u : (v != v ? 0x7fffffffu : __float_as_uint(v));
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (static_cast<unsigned long long>(u) << 32) | static_cast<unsigned long long>(~idx);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+PE_DEV unsigned long long argmax_key(float v, uint32_t idx) {
+  return (static_cast<unsigned long long>(argmax_order(v)) << 32) |
+         static_cast<unsigned long long>(~idx);
+}
+
+// Max of a 64-bit key over the warp (all lanes active): the largest high word,
+// then the largest low word among the lanes that hold it -- the same order as
+// comparing the whole keys, in two warp reductions instead of five shuffles.
+PE_DEV unsigned long long warp_max_u64(unsigned long long k) {
+  const uint32_t hi = static_cast<uint32_t>(k >> 32), lo = static_cast<uint32_t>(k);
+  uint32_t mh, ml;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(mh) : "r"(hi));
+  const uint32_t cand = hi == mh ? lo : 0u;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(ml) : "r"(cand));
+  return (static_cast<unsigned long long>(mh) << 32) | ml;
 }
 
 // ---------------------------------------------------------------- mbarrier

@@ -158,18 +158,6 @@ PE_DEV void epi_store_elem(const Epilogue& e, int f, int t, float v, float v2) {
   }
 }
 
-// Max of a 64-bit key over the warp (all lanes active): the largest high word,
-// then the largest low word among the lanes that hold it -- the same order as
-// comparing the whole keys, in two warp reductions instead of five shuffles.
-PE_DEV unsigned long long warp_max_u64(unsigned long long k) {
-  const uint32_t hi = static_cast<uint32_t>(k >> 32), lo = static_cast<uint32_t>(k);
-  uint32_t mh, ml;
-  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(mh) : "r"(hi));
-  const uint32_t cand = hi == mh ? lo : 0u;
-  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(ml) : "r"(cand));
-  return (static_cast<unsigned long long>(mh) << 32) | ml;
-}
-
 // Largest value over the warp (all lanes active); NaN if any lane holds NaN.
 PE_DEV float warp_max_f32(float v) {
   float m;

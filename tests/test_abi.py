@@ -57,3 +57,20 @@ def test_host_argument_checks(lib):
     assert lib.pe_prepare_inputs(None, 1, 1, *([None] * 6), 1, 1, None, None, None, None, None, None,
                                  0, None) == binding.PE_ERR_ARG
     assert lib.pe_argmax(None, None, 1, None, None, None, 0, None) == binding.PE_ERR_ARG
+
+
+def test_verify_host_checks(lib):
+    # 256-byte header, then one 8-byte key per (row, 1024-element chunk)
+    assert lib.pe_verify_workspace_bytes(512, 201088) == 256 + 512 * 197 * 8
+    assert lib.pe_verify_workspace_bytes(-1, 10) == 0
+    assert lib.pe_verify_workspace_bytes(1, 0) == 0
+    call = lib.pe_verify_greedy
+    # an empty batch is a no-op; a bad dtype or null outputs are refused on the host
+    assert call(0, 0, *([None] * 3), 10, binding.PE_DTYPE_F32, *([None] * 4), 0, None) == binding.PE_OK
+    assert call(1, 1, *([None] * 3), 10, 7, *([None] * 4), 0, None) == binding.PE_ERR_UNSUPPORTED
+    assert call(1, 1, *([None] * 3), 10, binding.PE_DTYPE_F32, *([None] * 4), 0, None) == \
+        binding.PE_ERR_ARG
+    assert call(0, 3, *([None] * 3), 10, binding.PE_DTYPE_F32, *([None] * 4), 0, None) == \
+        binding.PE_ERR_ARG
+    assert call(-1, 0, *([None] * 3), 10, binding.PE_DTYPE_F32, *([None] * 4), 0, None) == \
+        binding.PE_ERR_ARG
