@@ -38,6 +38,8 @@ Readings where the pages are silent (each one is listed in the design notes):
   * RMSNorm(x) = x * gamma / sqrt(mean(x^2) + eps).
   * RoPE: rotate-half pairing (i, i + hd/2), inverse frequency theta^(-2i/hd).
   * Attention scale 1/sqrt(hd); query head h reads KV head floor(h / (H/G)).
+  * Optional per-head sink logits (float32 in both modes): one more logit in
+    each head's softmax with a zero value row.
   * Pre-norm layer: u = RMSNorm(x; gamma_in); a = x + O(attn);
     y = a + MLP(RMSNorm(a; gamma_post)); z = RMSNorm(y; gamma_final).
     Post-norm layer: u = x; a = RMSNorm(x + O(attn); gamma_post);
@@ -293,12 +295,20 @@ def softmax(s):
     return e / e.sum()
 
 
-def attend(q, K_seq, V_seq):
+def attend(q, K_seq, V_seq, sink=None):
     """One query head over keys 0..n-1: softmax(K q / sqrt(hd)) weighted sum of V.
 
-    q is [hd]; K_seq and V_seq are [n][hd]."""
+    q is [hd]; K_seq and V_seq are [n][hd].  sink (optional): the head's learned
+    sink logit ("Attention Drift", section 3, the GPT-oss attention: a per-head
+    bias logit in the softmax denominator, an explicit option to attend to
+    nothing).  It joins the softmax as one more logit whose value row is zero,
+    so the weights of the real keys sum to less than one."""
     hd = q.shape[-1]
-    p = softmax(K_seq @ q / np.sqrt(hd))
+    s = K_seq @ q / np.sqrt(hd)
+    if sink is None:
+        p = softmax(s)
+    else:
+        p = softmax(np.append(s, float(sink)))[:-1]
     return p @ V_seq
 
 
@@ -421,12 +431,14 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
         s_loc = np.arange(len(rows) - K, len(rows))
         assert (rows[s_loc] == meta["sample_idx"][r * K:(r + 1) * K]).all()
         group = H // G_
+        sinks = w.get("attn_sink")
         attn = np.empty((K, H, hd))
         for kk, i in enumerate(s_loc):
             n_keys = int(pos[i]) + 1      # causal: the full context plus earlier draft rows
             for h in range(H):
                 g = h // group
-                attn[kk, h] = attend(q[i, h], Kseq[:n_keys, g], Vseq[:n_keys, g])
+                attn[kk, h] = attend(q[i, h], Kseq[:n_keys, g], Vseq[:n_keys, g],
+                                     None if sinks is None else float(sinks[h]))
         attn = R(attn.reshape(K, H * hd))
         xs = x[s_loc]
         o_proj = linear(attn, P["w_o"])

@@ -48,6 +48,7 @@ NAME_INDEX = {
     "v_cache": 13,
     "verify_logits": 14,
     "verify_plan": 15,
+    "attn_sink": 16,
 }
 
 
@@ -95,6 +96,8 @@ class Workload:
     permute_blocks: bool = True
     spare_blocks: int = 0
     has_drafter: bool = True
+    # per-head attention sink logits (GPT-oss attention), N(0, 1), float32
+    sinks: bool = False
     description: str = ""
 
     def n_prev_list(self):
@@ -290,7 +293,7 @@ def make_weights(wl: Workload, only=None) -> dict:
     emb[V][d], emb_mask[d], h_shared[d], gamma_stream[3][d], w_fc[d][4d],
     gamma_in[d], w_qkv[(H+2G)hd][d] (q heads, then k heads, then v heads),
     w_o[d][H hd], gamma_post[d], w_gate[I][d], w_up[I][d], w_down[d][I],
-    gamma_final[d], w_lm[V][d]."""
+    gamma_final[d], w_lm[V][d]; with sinks, attn_sink[H] (float32 in both modes)."""
     dm, s, dt = wl.dims, wl.weight_std, wl.dims.dtype
     d, I, V = dm.d, dm.inter, dm.vocab
     shapes = {
@@ -312,6 +315,8 @@ def make_weights(wl: Workload, only=None) -> dict:
     if wl.has_drafter:
         for gname in ("gamma_in", "gamma_post", "gamma_final"):
             w[gname] = ones((d,))
+        if wl.sinks:
+            w["attn_sink"] = normal_f32(wl.seed, "attn_sink", dm.n_heads)
     return w
 
 
