@@ -112,7 +112,8 @@ typedef struct pe_dims {
  * (w_fc, w_qkv, w_o, gamma_post, w_gate, w_up, w_down, gamma_final, w_lm, and
  * gamma_in for a pre-norm layer) come all together or all NULL: with none, the
  * handle serves pe_prepare_inputs only and the layer's calls (pe_draft_step,
- * pe_argmax, pe_argmax_noalloc) return PE_ERR_ARG.  Some but not all: PE_ERR_ARG. */
+ * pe_argmax, pe_argmax_noalloc) return PE_ERR_ARG.  Some but not all: PE_ERR_ARG.
+ * attn_sink is optional either way. */
 typedef struct pe_weights {
   const void* emb;          /* [V][d] token embedding */
   const void* emb_mask;     /* [d] learned emb(mask) for the MASK slots */
@@ -131,6 +132,11 @@ typedef struct pe_weights {
   const void* gamma_final;  /* [d] pre-norm: final norm; post-norm: norm after the
                                MLP residual */
   const void* w_lm;         /* [V][d] LM head */
+  const void* attn_sink;    /* [H] float (in both dtypes), nullable: per-head sink
+                               logit of the GPT-oss attention ("Attention Drift",
+                               section 3: a learned bias logit in each head's
+                               softmax denominator).  It joins the softmax as one
+                               more logit with a zero value row.  NULL: no sink */
 } pe_weights;
 
 /* Drafter-batch metadata: caller-owned device buffers written by

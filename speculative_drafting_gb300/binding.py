@@ -47,7 +47,7 @@ class PeDims(ctypes.Structure):
 
 
 WEIGHT_FIELDS = ["emb", "emb_mask", "h_shared", "gamma_stream", "w_fc", "gamma_in", "w_qkv", "w_o",
-                 "gamma_post", "w_gate", "w_up", "w_down", "gamma_final", "w_lm"]
+                 "gamma_post", "w_gate", "w_up", "w_down", "gamma_final", "w_lm", "attn_sink"]
 
 
 class PeWeights(ctypes.Structure):

@@ -549,6 +549,7 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
                                         al256(static_cast<size_t>(aa.n_splits) * NS * d.n_heads *
                                               d.head_dim * sizeof(float)));
   aa.out = attn;
+  aa.sink = static_cast<const float*>(h->w.attn_sink);
   aa.status = status;
   if ((rc = launch_attention(aa, dt, st)) != PE_OK) return rc;
   // O projection (partial sums)

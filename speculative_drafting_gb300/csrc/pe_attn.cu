@@ -15,6 +15,11 @@
 // otherwise the partials go to global memory and a combine kernel merges them.
 //
 // fp32: one CTA per (sample row, query head), SIMT dot products, online softmax.
+//
+// Optional per-head sink logits (the GPT-oss attention, "Attention Drift",
+// section 3: a learned bias logit in each head's softmax denominator) enter
+// where the partials are normalised: the sink joins the running maximum and adds
+// its exponential to the denominator, with a zero value row.
 #include <algorithm>
 #include <cmath>
 
@@ -440,7 +445,8 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
   // ---------------- merge of the splits inside the cluster
   // Every split's partial sits at the start of its ring: o [row][HD] (fp32,
   // unnormalised), then (m, l) per row.  CTA `rank` merges rows rank, rank + S,
-  // ...: out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j.
+  // ...: out = sum_j 2^(m_j - M) o_j / (sum_j 2^(m_j - M) l_j + 2^(sink - M)), where
+  // the optional sink term has a zero value row and M also covers it.
   cluster_sync_all();
   {
     const int S = static_cast<int>(gridDim.x);
@@ -458,9 +464,12 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
         mj = ld_dsmem_f32(ml_base + static_cast<uint32_t>(rr * 2) * 4u, lane);
         lj = ld_dsmem_f32(ml_base + static_cast<uint32_t>(rr * 2 + 1) * 4u, lane);
       }
-      const float M = warp_max(mj);
+      const int head = g * HG + rr % HG;
+      // a sink logit (exp2 domain) joins the maximum and the denominator
+      const float sk = a.sink ? a.sink[head] * kLog2e : -INFINITY;
+      const float M = fmaxf(warp_max(mj), sk);
       const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-      const float den = warp_sum(wj * lj);
+      const float den = warp_sum(wj * lj) + (sk == -INFINITY ? 0.f : exp2f(sk - M));
       const float inv = den > 0.f ? 1.f / den : 0.f;
       float acc[DPL];
 #pragma unroll
@@ -484,7 +493,6 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
         }
       }
       const size_t samp = static_cast<size_t>(r) * a.K + rr / HG;
-      const int head = g * HG + rr % HG;
       bf16* out = static_cast<bf16*>(a.out) + (samp * a.H + head) * HD;
 #pragma unroll
       for (int q = 0; q < DPL; ++q) out[lane + 32 * q] = __float2bfloat16_rn(acc[q] * inv);
@@ -494,8 +502,8 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
   cluster_sync_all();
 }
 
-// out[s][h*hd + d] = sum_j 2^(m_j - M) o_j[d] / sum_j 2^(m_j - M) l_j over the
-// splits j that hold keys of the request (j * split_len < L; the CTAs of the
+// out[s][h*hd + d] = sum_j 2^(m_j - M) o_j[d] / (sum_j 2^(m_j - M) l_j + 2^(sink_h - M))
+// (the sink term only with sink logits) over the splits j that hold keys of the request (j * split_len < L; the CTAs of the
 // others return at once and leave no partial).  One warp per (sample row,
 // query head): each lane owns hd/32 consecutive dimensions; the splits' loads
 // are independent, their sum runs in split order.
@@ -514,13 +522,15 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
   auto ml = [&](int j) { return a.part_ml + (static_cast<size_t>(j) * n_sh + sh) * 2; };
   float M = -INFINITY;
   for (int j = lane; j < n; j += 32) M = fmaxf(M, ml(j)[0]);
-  M = warp_max(M);
+  // a sink logit (exp2 domain) joins the maximum and the denominator
+  const float sk = a.sink ? a.sink[sh % a.H] * kLog2e : -INFINITY;
+  M = fmaxf(warp_max(M), sk);
   float den = 0.f;
   for (int j = lane; j < n; j += 32) {
     const float m = ml(j)[0];
     den += (m == -INFINITY ? 0.f : exp2f(m - M)) * ml(j)[1];
   }
-  den = warp_sum(den);
+  den = warp_sum(den) + (sk == -INFINITY ? 0.f : exp2f(sk - M));
   const float inv = den > 0.f ? 1.f / den : 0.f;
   float acc[V];
 #pragma unroll
@@ -607,9 +617,11 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
   for (int i = 0; i < 4; ++i)
     if (lane + 32 * i < a.hd) wacc[warp][lane + 32 * i] = acc[i];
   __syncthreads();
-  float M = -INFINITY;
+  // a sink logit joins the maximum and the denominator (its value row is zero)
+  const float sk = a.sink ? a.sink[h] : -INFINITY;
+  float M = sk;
   for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w]);
-  float den = 0.f;
+  float den = sk == -INFINITY ? 0.f : expf(sk - M);
   for (int w = 0; w < 4; ++w)
     if (wm[w] != -INFINITY) den += expf(wm[w] - M) * wl[w];
   for (int d = threadIdx.x; d < a.hd; d += blockDim.x) {

@@ -121,6 +121,7 @@ struct AttnArgs {
   float* part_o;   // [n_splits][B*K][H][hd]     (bf16 path)
   float* part_ml;  // [n_splits][B*K][H][2]      (bf16 path)
   void* out;       // [B*K][H*hd]
+  const float* sink;  // [H] per-head sink logit (natural units), nullable
   uint32_t* status;
 };
 int attention_split_count(int B, int G, int max_blocks, int bs, int num_sms);

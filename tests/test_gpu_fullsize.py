@@ -14,16 +14,18 @@ from parity import check_close_bf16, check_logits_and_draft, check_meta, cuda_or
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    ("gptoss_b1_k7", [0]),
-    ("gptoss_b64_k7_postnorm", [0, 37, 63]),
-    ("llama8b_b32_k8_32k", [5, 31]),
+    ("gptoss_b1_k7", [0], {}),
+    ("gptoss_b64_k7_postnorm", [0, 37, 63], {}),
+    ("llama8b_b32_k8_32k", [5, 31], {}),
+    # the GPT-oss attention with per-head sink logits
+    ("gptoss_b64_k7_postnorm", [11, 50], {"sinks": True}),
 ]
 
 
-@pytest.mark.parametrize("name,sample", CASES)
-def test_full_size_step(name, sample):
+@pytest.mark.parametrize("name,sample,over", CASES)
+def test_full_size_step(name, sample, over):
     torch = cuda_or_skip()
-    wl, b, w, kc, vc, r = setup(name)
+    wl, b, w, kc, vc, r = setup(name, **over)
     r.run()
     torch.cuda.synchronize()
     st, rc = r.status()

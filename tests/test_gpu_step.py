@@ -26,6 +26,14 @@ CASES = [
     # enough requests that attention splits merge through global memory: the
     # combine stops at each request's own last split
     ("small_prenorm", {"batch": 160, "n_prev": 6, "ctx": ("uniform", 0, 700), "seed": 5}),
+    # per-head sink logits (GPT-oss attention) on every normalisation path: the
+    # fp32 kernel, the in-cluster merge and the global combine
+    ("tiny_fp32", {"sinks": True}),
+    ("small_prenorm", {"sinks": True}),
+    ("small_postnorm_hd128", {"sinks": True}),
+    ("small_prenorm", {"batch": 12, "n_prev": 6, "ctx": ("uniform", 0, 700), "seed": 3, "sinks": True}),
+    ("small_prenorm", {"batch": 160, "n_prev": 6, "ctx": ("uniform", 0, 700), "seed": 5,
+                       "sinks": True}),
 ]
 
 
