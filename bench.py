@@ -71,24 +71,33 @@ def measured_peaks():
 # ----------------------------------------------------------------------------- algorithmic bytes
 
 
-PROFILED_LM = {"gptoss_b1_k7": "lm_head_gemm_gptoss_b1_k7.md",
-               "gptoss_b64_k7_postnorm": "lm_head_gemm_gptoss_b64_k7.md"}
+# workload -> (committed ncu summary, key of the dominant kernel's DRAM bytes per launch)
+PROFILED = {"gptoss_b1_k7": ("lm_head_gemm_gptoss_b1_k7.md", "traffic_bytes_per_step"),
+            "gptoss_b64_k7_postnorm": ("lm_head_gemm_gptoss_b64_k7.md", "traffic_bytes_per_step"),
+            "verify_b64_k7": ("verify_greedy_b64_k7.md", "traffic_bytes_per_launch_f32"),
+            "verify_b64_k7_bf16": ("verify_greedy_b64_k7.md", "traffic_bytes_per_launch_bf16")}
+
+
+def sources_digest(files):
+    """sha256 over the sha256 digests of the listed files (paths from the repo root)."""
+    digests = "".join(hashlib.sha256(open(os.path.join(ROOT, f), "rb").read()).hexdigest()
+                      for f in files)
+    return hashlib.sha256(digests.encode()).hexdigest()
 
 
 def profiled_traffic(workload):
-    """DRAM bytes (read + write) of the LM head per step from the committed ncu
-    summary, while the GEMM sources are the ones it was captured with; else None."""
-    if workload not in PROFILED_LM:
+    """DRAM bytes (read + write) of the dominant kernel per launch from the committed
+    ncu summary, while its sources are the ones it was captured with; else None."""
+    if workload not in PROFILED:
         return None
+    fname, key = PROFILED[workload]
     try:
-        text = open(os.path.join(ROOT, "profiles", PROFILED_LM[workload])).read()
-        vals = dict(re.findall(r"^\s*(traffic_bytes_per_step|source_sha256|sources):\s*(\S.*)$",
+        text = open(os.path.join(ROOT, "profiles", fname)).read()
+        vals = dict(re.findall(r"^\s*(traffic_bytes_per_\w+|source_sha256|sources):\s*(\S.*)$",
                                text, re.M))
-        digests = "".join(hashlib.sha256(open(os.path.join(ROOT, f), "rb").read()).hexdigest()
-                          for f in vals["sources"].split())
-        if hashlib.sha256(digests.encode()).hexdigest() != vals["source_sha256"].strip():
+        if sources_digest(vals["sources"].split()) != vals["source_sha256"].strip():
             return None
-        return int(vals["traffic_bytes_per_step"])
+        return int(vals[key])
     except (OSError, KeyError, ValueError):
         return None
 
@@ -613,7 +622,8 @@ def run_verify(args, rank, world, local):
             "gpu_launches": 2 * args.steps,
             "roofline": {"kernel": "verify_partial_kernel + verify_accept_kernel (whole call)",
                          "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic(wl.name),
                          "peak_source": src, "algorithmic_bytes": alg,
                          "avg_launch_us": call_ms * 1e3},
             "cpu_baseline": cpu}), flush=True)
