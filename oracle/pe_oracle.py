@@ -342,6 +342,10 @@ class _Params:
             self._cache[name] = decode(self._w[name], self._dt)
         return self._cache[name]
 
+    def raw(self, name):
+        """A parameter as stored, or None when absent (the optional sink logits)."""
+        return self._w.get(name)
+
     def emb_row(self, t):
         return decode(self._w["emb"][t], self._dt)
 
@@ -372,16 +376,28 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
 
     dims: object with d, n_heads, n_kv_heads, head_dim, inter, vocab, K,
           block_size, mask_id, post_norm, dtype, eps, rope_theta.
-    w:    parameters as stored (float32 arrays, or bf16 bit patterns).
+    w:    parameters as stored (float32 arrays, or bf16 bit patterns).  With
+          dims.n_layers = N > 1, w["layers"] holds N - 1 dicts of the later
+          layers' parameters (gamma_in, w_qkv, w_o, gamma_post, w_gate, w_up,
+          w_down, gamma_final, optional attn_sink); the top-level ones are layer 1's.
     batch: qsl, prev_tok, prev_pos, accepted, bonus, block_table, H_tgt.
-    k_cache, v_cache: paged caches [num_blocks][G][bs][hd] as stored, before the
-          step; they are read, never modified.
+    k_cache, v_cache: paged caches [num_blocks][G][bs][hd] (one layer) or
+          [N][num_blocks][G][bs][hd], as stored, before the step; they are read,
+          never modified.
     requests: indices of the requests to run the layer for (default: all);
           metadata is always built for the whole batch.
 
     Returns {"meta": ..., "req": {r: per-request results}} where a request's
-    results hold, over its valid rows in order: rows, A, x, u, k, v, slot; and
-    over its K sample rows: q, attn, a, z, logits, draft.
+    results hold, over its valid rows in order: rows, A, x, u, k, v, slot (u, k
+    and v of the first layer) and k_layers, v_layers (every layer's); and over
+    its K sample rows: q, attn, a (the last layer's), z, logits, draft.
+
+    Layers ("P-EAGLE: parallel speculative decoding in vLLM", Parallel drafting:
+    all positions pass through the N layers and the LM head).  Pre-norm: layer l
+    maps x_l to x_{l+1} = a + MLP(RMSNorm(a)) with a = x_l + O(attn); the final
+    norm (the last layer's gamma_final) gives z.  Post-norm: x_{l+1} =
+    RMSNorm(a + MLP(a); gamma_final_l) with a = RMSNorm(x_l + O(attn)); the last
+    layer's output is z.  Each layer has its own KV cache.
     """
     dt = dims.dtype
     R = _rounder(dt)
@@ -398,6 +414,9 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
     h_shared = P["h_shared"]
     emb_mask = P["emb_mask"]
     gam_s = P["gamma_stream"]
+    n_layers = max(1, int(getattr(dims, "n_layers", 1)))
+    layer_params = [P] + [_Params(lw, dt) for lw in w.get("layers", [])[: n_layers - 1]]
+    assert len(layer_params) == n_layers, "w['layers'] holds the layers after the first"
     out = {"meta": meta, "req": {}}
     for r in requests:
         v0, v1 = int(meta["valid_qsl"][r]), int(meta["valid_qsl"][r + 1])
@@ -409,50 +428,67 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
         Erows = np.stack([emb_mask if meta["is_masked"][o] else P.emb_row(int(meta["tok"][o]))
                           for o in rows])
         A = drafter_input(Grows, Erows, gam_s, dims.eps, dt)
-        # (4) fc, input norm, QKV with RoPE, KV write
+        # (4) fc, then the decoder layers.  Every layer but the last runs over all
+        # the request's valid rows (the next layer's keys and values need them);
+        # the last runs its attention, O and MLP over the K sample rows only
+        # (the other rows' outputs are dead).
         x = linear(A, P["w_fc"])
-        u = R2(x) if dims.post_norm else R2(rmsnorm(x, P["gamma_in"], dims.eps))
-        qkv = linear(u, P["w_qkv"])
-        pos = meta["pos"][rows]
-        q = qkv[:, : H * hd].reshape(-1, H, hd)
-        k = qkv[:, H * hd: (H + G_) * hd].reshape(-1, G_, hd)
-        v = qkv[:, (H + G_) * hd:].reshape(-1, G_, hd)
-        q = R(rope(q, pos, dims.rope_theta))
-        k = R(rope(k, pos, dims.rope_theta))
-        v = R(v)
-        # the request's cache after this step's writes, as a position-indexed sequence
         L = int(meta["seq_len"][r])
-        Kseq = request_kv_sequence(k_cache, batch["block_table"], r, L, dims.block_size, dt)
-        Vseq = request_kv_sequence(v_cache, batch["block_table"], r, L, dims.block_size, dt)
-        for i, p in enumerate(pos):
-            Kseq[int(p)] = k[i]
-            Vseq[int(p)] = v[i]
+        pos = meta["pos"][rows]
         # sample rows are the last K valid rows of the request (NTP row, MASK rows)
         s_loc = np.arange(len(rows) - K, len(rows))
         assert (rows[s_loc] == meta["sample_idx"][r * K:(r + 1) * K]).all()
         group = H // G_
-        sinks = w.get("attn_sink")
-        attn = np.empty((K, H, hd))
-        for kk, i in enumerate(s_loc):
-            n_keys = int(pos[i]) + 1      # causal: the full context plus earlier draft rows
-            for h in range(H):
-                g = h // group
-                attn[kk, h] = attend(q[i, h], Kseq[:n_keys, g], Vseq[:n_keys, g],
-                                     None if sinks is None else float(sinks[h]))
-        attn = R(attn.reshape(K, H * hd))
-        xs = x[s_loc]
-        o_proj = linear(attn, P["w_o"])
-        if dims.post_norm:
-            a = R2(rmsnorm(xs + o_proj, P["gamma_post"], dims.eps))
-            y = a + swiglu_mlp(a, P["w_gate"], P["w_up"], P["w_down"], R2)
-            z = R(rmsnorm(y, P["gamma_final"], dims.eps))
-        else:
-            a = xs + o_proj
-            m = R2(rmsnorm(a, P["gamma_post"], dims.eps))
-            y = a + swiglu_mlp(m, P["w_gate"], P["w_up"], P["w_down"], R2)
-            z = R(rmsnorm(y, P["gamma_final"], dims.eps))
-        res = dict(rows=rows, A=A, x=x, u=u, k=k, v=v, slot=meta["slot"][rows],
-                   q=q[s_loc], attn=attn, a=a, z=z)
+        h_in = x
+        k_layers, v_layers = [], []
+        for li, Pl in enumerate(layer_params):
+            last = li == n_layers - 1
+            u = R2(h_in) if dims.post_norm else R2(rmsnorm(h_in, Pl["gamma_in"], dims.eps))
+            if li == 0:
+                u0 = u
+            qkv = linear(u, Pl["w_qkv"])
+            q = qkv[:, : H * hd].reshape(-1, H, hd)
+            k = qkv[:, H * hd: (H + G_) * hd].reshape(-1, G_, hd)
+            v = qkv[:, (H + G_) * hd:].reshape(-1, G_, hd)
+            q = R(rope(q, pos, dims.rope_theta))
+            k = R(rope(k, pos, dims.rope_theta))
+            v = R(v)
+            k_layers.append(k)
+            v_layers.append(v)
+            # this layer's cache after this step's writes, as a position-indexed sequence
+            kc_l = k_cache if n_layers == 1 else k_cache[li]
+            vc_l = v_cache if n_layers == 1 else v_cache[li]
+            Kseq = request_kv_sequence(kc_l, batch["block_table"], r, L, dims.block_size, dt)
+            Vseq = request_kv_sequence(vc_l, batch["block_table"], r, L, dims.block_size, dt)
+            for i, p in enumerate(pos):
+                Kseq[int(p)] = k[i]
+                Vseq[int(p)] = v[i]
+            sinks = Pl.raw("attn_sink")
+            att_rows = s_loc if last else np.arange(len(rows))
+            attn = np.empty((len(att_rows), H, hd))
+            for kk, i in enumerate(att_rows):
+                n_keys = int(pos[i]) + 1      # causal: the full context plus earlier rows
+                for h in range(H):
+                    g = h // group
+                    attn[kk, h] = attend(q[i, h], Kseq[:n_keys, g], Vseq[:n_keys, g],
+                                         None if sinks is None else float(sinks[h]))
+            attn = R(attn.reshape(len(att_rows), H * hd))
+            xs = h_in[att_rows]
+            o_proj = linear(attn, Pl["w_o"])
+            if dims.post_norm:
+                a = R2(rmsnorm(xs + o_proj, Pl["gamma_post"], dims.eps))
+                y = a + swiglu_mlp(a, Pl["w_gate"], Pl["w_up"], Pl["w_down"], R2)
+                # a post-norm layer's output is normalised (the last one's is z)
+                h_out = rmsnorm(y, Pl["gamma_final"], dims.eps)
+            else:
+                a = xs + o_proj
+                m = R2(rmsnorm(a, Pl["gamma_post"], dims.eps))
+                y = a + swiglu_mlp(m, Pl["w_gate"], Pl["w_up"], Pl["w_down"], R2)
+                h_out = y if not last else rmsnorm(y, Pl["gamma_final"], dims.eps)
+            h_in = h_out
+        z = R(h_in)
+        res = dict(rows=rows, A=A, x=x, u=u0, k=k_layers[0], v=v_layers[0], slot=meta["slot"][rows],
+                   q=q[s_loc], attn=attn, a=a, z=z, k_layers=k_layers, v_layers=v_layers)
         if want_logits:
             logits = P.lm_logits(z)
             res["logits"] = logits

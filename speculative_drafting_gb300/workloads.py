@@ -70,6 +70,7 @@ class Dims:
     eps: float = 1e-6
     rope_theta: float = 10000.0
     n_streams: int = 3
+    n_layers: int = 1
 
     @property
     def qkv_rows(self) -> int:
@@ -172,8 +173,10 @@ def get(name: str, **overrides) -> Workload:
 # random streams
 
 
-def _seq(seed: int, name: str, chunk: int) -> np.random.Generator:
-    ss = np.random.SeedSequence(seed, spawn_key=(NAME_INDEX[name], chunk))
+def _seq(seed: int, name: str, chunk: int, layer: int = 0) -> np.random.Generator:
+    # a later layer's tensor of the same name draws from its own stream
+    key = (NAME_INDEX[name], chunk) if layer == 0 else (NAME_INDEX[name], chunk, layer)
+    ss = np.random.SeedSequence(seed, spawn_key=key)
     return np.random.Generator(np.random.PCG64(ss))
 
 
@@ -181,14 +184,14 @@ def _threads() -> int:
     return max(1, min(32, os.cpu_count() or 1))
 
 
-def normal_f32(seed: int, name: str, n: int, std: float = 1.0, out=None) -> np.ndarray:
+def normal_f32(seed: int, name: str, n: int, std: float = 1.0, out=None, layer: int = 0) -> np.ndarray:
     """n float32 draws from N(0, std^2), chunked as described in the module doc."""
     out = np.empty(n, dtype=np.float32) if out is None else out
     n_chunks = (n + CHUNK - 1) // CHUNK
 
     def fill(c):
         lo, hi = c * CHUNK, min(n, (c + 1) * CHUNK)
-        g = _seq(seed, name, c)
+        g = _seq(seed, name, c, layer)
         g.standard_normal(hi - lo, dtype=np.float32, out=out[lo:hi])
         if std != 1.0:
             out[lo:hi] *= np.float32(std)
@@ -225,10 +228,10 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return out
 
 
-def draw(seed: int, name: str, shape, std: float, dtype: str) -> np.ndarray:
+def draw(seed: int, name: str, shape, std: float, dtype: str, layer: int = 0) -> np.ndarray:
     """A tensor of N(0, std^2) values in the workload dtype (f32, or bf16 bits)."""
     n = int(np.prod(shape))
-    v = normal_f32(seed, name, n, std)
+    v = normal_f32(seed, name, n, std, layer=layer)
     if dtype == "bf16":
         return f32_to_bf16_bits(v).reshape(shape)
     return v.reshape(shape)
@@ -293,7 +296,9 @@ def make_weights(wl: Workload, only=None) -> dict:
     emb[V][d], emb_mask[d], h_shared[d], gamma_stream[3][d], w_fc[d][4d],
     gamma_in[d], w_qkv[(H+2G)hd][d] (q heads, then k heads, then v heads),
     w_o[d][H hd], gamma_post[d], w_gate[I][d], w_up[I][d], w_down[d][I],
-    gamma_final[d], w_lm[V][d]; with sinks, attn_sink[H] (float32 in both modes)."""
+    gamma_final[d], w_lm[V][d]; with sinks, attn_sink[H] (float32 in both modes).
+    With n_layers = N > 1, "layers" lists N - 1 dicts of the later layers' w_qkv,
+    w_o, w_gate, w_up, w_down, gains (and sinks)."""
     dm, s, dt = wl.dims, wl.weight_std, wl.dims.dtype
     d, I, V = dm.d, dm.inter, dm.vocab
     shapes = {
@@ -317,15 +322,30 @@ def make_weights(wl: Workload, only=None) -> dict:
             w[gname] = ones((d,))
         if wl.sinks:
             w["attn_sink"] = normal_f32(wl.seed, "attn_sink", dm.n_heads)
+        # layers 2..N: the same recipe, each from its own streams
+        if dm.n_layers > 1:
+            w["layers"] = []
+            for li in range(1, dm.n_layers):
+                lw = {name: draw(wl.seed, name, shapes[name], s, dt, layer=li)
+                      for name in ("w_qkv", "w_o", "w_gate", "w_up", "w_down")}
+                for gname in ("gamma_in", "gamma_post", "gamma_final"):
+                    lw[gname] = ones((d,))
+                if wl.sinks:
+                    lw["attn_sink"] = normal_f32(wl.seed, "attn_sink", dm.n_heads, layer=li)
+                w["layers"].append(lw)
     return w
 
 
 def make_kv_cache(wl: Workload, num_blocks: int) -> tuple:
-    """Paged K and V caches [num_blocks][G][bs][hd], prior contents N(0, 1)."""
+    """Paged K and V caches [num_blocks][G][bs][hd] (one layer) or
+    [N][num_blocks][G][bs][hd] (N layers), prior contents N(0, 1)."""
     dm = wl.dims
     shp = (num_blocks, dm.n_kv_heads, dm.block_size, dm.head_dim)
-    return (draw(wl.seed, "k_cache", shp, 1.0, dm.dtype),
-            draw(wl.seed, "v_cache", shp, 1.0, dm.dtype))
+    if dm.n_layers <= 1:
+        return (draw(wl.seed, "k_cache", shp, 1.0, dm.dtype),
+                draw(wl.seed, "v_cache", shp, 1.0, dm.dtype))
+    return tuple(np.stack([draw(wl.seed, name, shp, 1.0, dm.dtype, layer=li)
+                           for li in range(dm.n_layers)]) for name in ("k_cache", "v_cache"))
 
 
 # ---------------------------------------------------------------------------
