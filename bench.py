@@ -108,16 +108,17 @@ def lm_head_bytes(dm, n_rows):
 
 
 def step_bytes(dm, batch):
-    """Bytes the whole step must move: every weight once, the KV it reads and writes,
-    the captured hidden states and the embedding rows."""
+    """Bytes the whole step must move: every weight once, the KV it reads and writes
+    (in every layer), the captured hidden states and the embedding rows."""
     d, I, V = dm.d, dm.inter, dm.vocab
-    w = (4 * d * d + dm.qkv_rows * d + d * dm.n_heads * dm.head_dim + 3 * I * d + V * d) * 2
+    n_l = max(1, getattr(dm, "n_layers", 1))
+    w = (4 * d * d + n_l * (dm.qkv_rows * d + d * dm.n_heads * dm.head_dim + 3 * I * d) + V * d) * 2
     B, K = batch["B"], dm.K
     acc = batch["accepted"]
     pos0 = batch["prev_pos"][batch["qsl"][:-1] + acc]
-    kv_read = int(np.sum(pos0 + K)) * dm.n_kv_heads * dm.head_dim * 2 * 2
+    kv_read = n_l * int(np.sum(pos0 + K)) * dm.n_kv_heads * dm.head_dim * 2 * 2
     n_valid = int(np.sum(acc + K))
-    kv_write = n_valid * dm.n_kv_heads * dm.head_dim * 2 * 2
+    kv_write = n_l * n_valid * dm.n_kv_heads * dm.head_dim * 2 * 2
     hid = batch["T_in"] * 3 * d * 2 + n_valid * d * 2
     return w + kv_read + kv_write + hid
 

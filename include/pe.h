@@ -77,8 +77,10 @@ extern "C" {
                                      the key is skipped by attention */
 #define PE_ST_TOKEN_RANGE 0x4u    /* token id outside [0, V): embedding row 0 is used */
 #define PE_ST_ROWS_RANGE 0x8u     /* pe_verify_greedy: qsl is not a non-decreasing run
-                                     from 0 to T_in; each request is clamped to
-                                     the rows in range */
+                                     from 0 to T_in (each request is clamped to
+                                     the rows in range); pe_draft_step with
+                                     several layers: a request has more
+                                     non-rejected rows than the layers carry */
 #define PE_ST_TIMEOUT 0x10u       /* a bounded wait inside a kernel expired */
 
 /* padding slot of rejected rows ("KV cache and CUDA graphs") */
@@ -105,7 +107,27 @@ typedef struct pe_dims {
   int32_t dtype;      /* PE_DTYPE_F32 or PE_DTYPE_BF16 */
   float eps;          /* RMSNorm epsilon */
   float rope_theta;   /* RoPE base */
+  int32_t n_layers;   /* N decoder layers, 1..PE_MAX_LAYERS (0 is read as 1) */
 } pe_dims;
+
+/* Most decoder layers a handle takes. */
+#define PE_MAX_LAYERS 16
+
+/* Parameters of decoder layers 2..N (device pointers, borrowed like pe_weights;
+ * the same shapes and meanings as the layer fields of pe_weights, which hold
+ * layer 1).  gamma_final: post-norm, the norm after this layer's MLP residual;
+ * pre-norm, only the last layer's is used, as the final norm. */
+typedef struct pe_layer_weights {
+  const void* gamma_in;     /* [d] pre-norm only */
+  const void* w_qkv;        /* [(H+2G)*hd][d] */
+  const void* w_o;          /* [d][H*hd] */
+  const void* gamma_post;   /* [d] */
+  const void* w_gate;       /* [I][d] */
+  const void* w_up;         /* [I][d] */
+  const void* w_down;       /* [d][I] */
+  const void* gamma_final;  /* [d] */
+  const void* attn_sink;    /* [H] float, nullable */
+} pe_layer_weights;
 
 /* Drafter parameters: device pointers, borrowed for the handle's lifetime.
  * emb, emb_mask, h_shared and gamma_stream are required.  The layer's parameters
@@ -137,6 +159,8 @@ typedef struct pe_weights {
                                section 3: a learned bias logit in each head's
                                softmax denominator).  It joins the softmax as one
                                more logit with a zero value row.  NULL: no sink */
+  const pe_layer_weights* more_layers; /* HOST array of n_layers - 1 entries (layers
+                               2..N; read by pe_create only), NULL for one layer */
 } pe_weights;
 
 /* Drafter-batch metadata: caller-owned device buffers written by
@@ -206,9 +230,16 @@ int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl,
 
 /* Step (4): the drafter layer for the batch prepared by pe_prepare_inputs.
  *   A         [T_out][4d] drafter input from pe_prepare_inputs (A_out)
- *   k_cache, v_cache  [num_blocks][G][block_size][hd] paged KV caches; this
- *             step's non-rejected rows are written at meta->slot (never at -1),
- *             then attention reads them back
+ *   k_cache, v_cache  [n_layers][num_blocks][G][block_size][hd] paged KV
+ *             caches, one per layer, back to back; this step's non-rejected rows
+ *             are written at meta->slot (never at -1) in every layer, then
+ *             attention reads them back
+ * With n_layers > 1 every layer but the last runs over all non-rejected rows
+ * ("Parallel drafting": all positions pass through the N layers), laid out per
+ * request in R = min(2K, 128 / (H/G)) rows (2K in fp32 mode), right-aligned.  A
+ * request whose a_r + K non-rejected rows exceed R (a prefill-sized request)
+ * sets PE_ST_ROWS_RANGE and its drafts are not valid; steady-state steps
+ * (n_r <= K + 1 verify rows) always fit.
  *   z_out     [B*K][d] normalised final hidden state of the K sample rows of each
  *             request (row r*K + k predicts draft token k+1 of request r)
  * block_table / max_blocks / num_blocks as passed to pe_prepare_inputs. */

@@ -51,7 +51,8 @@ Readings where the pages are silent (each one is listed in the design notes):
         after RoPE (the cache dtype), the attention output, z;
       - carried as a bf16 pair hi + lo (hi = bf16(v), lo = bf16(v - hi), about
         16 significant bits): the projection operands u (QKV input), the MLP
-        input (a post-norm, m pre-norm) and the SwiGLU product h;
+        input (a post-norm, m pre-norm), the SwiGLU product h, and with several
+        post-norm layers each layer's output passed to the next;
       - not rounded (fp32 on the GPU): the fc output x and the residual sums.
     Logits stay unrounded.  fp32 mode rounds nothing (fp64 throughout).
 
@@ -478,8 +479,11 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
             if dims.post_norm:
                 a = R2(rmsnorm(xs + o_proj, Pl["gamma_post"], dims.eps))
                 y = a + swiglu_mlp(a, Pl["w_gate"], Pl["w_up"], Pl["w_down"], R2)
-                # a post-norm layer's output is normalised (the last one's is z)
+                # a post-norm layer's output is normalised (the last one's is z);
+                # passed on to the next layer, it is carried as a bf16 pair
                 h_out = rmsnorm(y, Pl["gamma_final"], dims.eps)
+                if not last:
+                    h_out = R2(h_out)
             else:
                 a = xs + o_proj
                 m = R2(rmsnorm(a, Pl["gamma_post"], dims.eps))

@@ -43,15 +43,22 @@ class PeDims(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("vocab", ctypes.c_int32), ("K", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("mask_id", ctypes.c_int32), ("post_norm", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("n_layers", ctypes.c_int32)]
 
 
 WEIGHT_FIELDS = ["emb", "emb_mask", "h_shared", "gamma_stream", "w_fc", "gamma_in", "w_qkv", "w_o",
                  "gamma_post", "w_gate", "w_up", "w_down", "gamma_final", "w_lm", "attn_sink"]
+LAYER_FIELDS = ["gamma_in", "w_qkv", "w_o", "gamma_post", "w_gate", "w_up", "w_down", "gamma_final",
+                "attn_sink"]
+
+
+class PeLayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in LAYER_FIELDS]
 
 
 class PeWeights(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS] + \
+        [("more_layers", ctypes.POINTER(PeLayerWeights))]
 
 
 META_FIELDS = ["out_qsl", "tok", "pos", "is_rejected", "is_masked", "hidden_src", "slot",
@@ -145,7 +152,7 @@ def make_dims(dm) -> PeDims:
                   head_dim=dm.head_dim, inter=dm.inter, vocab=dm.vocab, K=dm.K,
                   block_size=dm.block_size, mask_id=dm.mask_id, post_norm=int(bool(dm.post_norm)),
                   dtype=PE_DTYPE_BF16 if dm.dtype == "bf16" else PE_DTYPE_F32,
-                  eps=dm.eps, rope_theta=dm.rope_theta)
+                  eps=dm.eps, rope_theta=dm.rope_theta, n_layers=getattr(dm, "n_layers", 1))
 
 
 class Meta:
@@ -186,6 +193,14 @@ class Drafter:
         self.weights = weights  # keep the tensors alive for the handle's lifetime
         cw = PeWeights(**{k: (weights[k].data_ptr() if weights.get(k) is not None else None)
                           for k in WEIGHT_FIELDS})
+        more = weights.get("layers") or []
+        if more:
+            # host array of the later layers' device pointers (read by pe_create)
+            arr = (PeLayerWeights * len(more))()
+            for i, lw in enumerate(more):
+                for k in LAYER_FIELDS:
+                    setattr(arr[i], k, lw[k].data_ptr() if lw.get(k) is not None else None)
+            cw.more_layers = arr
         h = ctypes.c_void_p()
         self.cdims = make_dims(dims)
         _check(self.lib.pe_create(ctypes.byref(self.cdims), ctypes.byref(cw), ctypes.byref(h)), "pe_create")

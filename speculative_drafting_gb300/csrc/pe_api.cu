@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "pe_internal.h"
 #include "pe_prep.h"
@@ -15,14 +16,23 @@
 
 using namespace pe;
 
+// Decoder layers 2..N: their parameters and the tensor maps of their packed
+// projection weights (layer 1's live in pe_weights and the handle's own maps).
+struct LayerSlot {
+  pe_layer_weights w;
+  CUtensorMap m_qkv, m_o, m_gate, m_up, m_down;
+};
+
 struct pe_handle {
   pe_dims d;
   pe_weights w;
   int num_sms;
   CUtensorMap m_fc, m_qkv, m_o, m_gate, m_up, m_down, m_lm;
   double inv_freq[64];
-  void* packed;  // owned: tile-packed copies of the seven projection weights (bf16)
+  void* packed;  // owned: tile-packed copies of the projection weights (bf16)
   bool has_layer;  // false: metadata / drafter-input handle without layer weights
+  int n_layers;
+  LayerSlot more[PE_MAX_LAYERS - 1];  // layers 2..n_layers
 };
 
 namespace {
@@ -80,6 +90,17 @@ size_t partial_bytes_bound(const pe_handle* h, int id, int N_max) {
   return best;
 }
 
+// Rows per request that the attention, O and MLP steps carry: the K sample rows
+// with one layer; with several, every non-rejected row (a_r + K <= 2K for n_r <=
+// K + 1), right-aligned, as many as one attention tile of the bf16 kernel holds.
+int layer_rows(const pe_handle* h) {
+  const pe_dims& d = h->d;
+  if (h->n_layers <= 1) return d.K;
+  int R = 2 * d.K;
+  if (is_bf16(h)) R = std::min(R, 128 / (d.n_heads / d.n_kv_heads));
+  return R;
+}
+
 // Attention split partials, bounded over every batch size <= B (the split count
 // rises as the batch shrinks).
 size_t attn_scratch_bound(const pe_handle* h, int B, int max_blocks) {
@@ -90,7 +111,7 @@ size_t attn_scratch_bound(const pe_handle* h, int B, int max_blocks) {
   // bounds every narrower call; the batch size is walked
   for (int b = 1; b <= B; ++b) {
     const int ns = attention_split_count(b, d.n_kv_heads, max_blocks, d.block_size, h->num_sms);
-    best = std::max(best, attention_scratch_bytes(b, d.K, d.n_heads, d.head_dim, ns));
+    best = std::max(best, attention_scratch_bytes(b, layer_rows(h), d.n_heads, d.head_dim, ns));
   }
   return best;
 }
@@ -103,6 +124,8 @@ struct Layout {
   // a time: each is read by the next kernel before the next projection stores);
   // amax: argmax keys; tok: the test hook's argmax indices
   size_t status, x, u, u_lo, q_s, x_s, attn, r, a, a_lo, a_f, h, h_lo, part, amax, attn_part, tok;
+  // several layers: a later layer's input, fp32 (xl) and as its QKV operand (ul, ul_lo)
+  size_t xl, ul, ul_lo;
   size_t total;
 };
 
@@ -113,9 +136,10 @@ Layout layout_of(const pe_handle* h, int B, int T_in, int max_blocks) {
   const pe_dims& d = h->d;
   const size_t e = esize(h);
   const int T_out = T_in + B * (d.K - 1);
-  const int NS = B * d.K;
+  const int NS = B * layer_rows(h);
   const int Hd = d.n_heads * d.head_dim;
   const int QKV = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
+  const bool layers = h->n_layers > 1;
   Layout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -138,9 +162,14 @@ Layout layout_of(const pe_handle* h, int B, int T_in, int max_blocks) {
   L.h = take(static_cast<size_t>(NS) * d.inter * f4);
   L.h_lo = take(static_cast<size_t>(NS) * d.inter * e);
   L.part = take(std::max(std::max(partial_bytes_bound(h, G_FC, T_out),
-                                  partial_bytes_bound(h, G_QKV, T_out)),
+                                  partial_bytes_bound(h, G_QKV, layers ? std::max(T_out, NS) : T_out)),
                          std::max(partial_bytes_bound(h, G_O, NS),
                                   partial_bytes_bound(h, G_DOWN, NS))));
+  if (layers) {
+    L.xl = take(static_cast<size_t>(NS) * d.d * f4);
+    L.ul = take(static_cast<size_t>(NS) * d.d * f4);
+    L.ul_lo = take(static_cast<size_t>(NS) * d.d * e);
+  }
   (void)QKV;
   L.amax = take(static_cast<size_t>(NS) * sizeof(unsigned long long));
   L.attn_part = take(attn_scratch_bound(h, B, max_blocks));
@@ -205,15 +234,20 @@ int check_meta(const pe_meta* m) {
 // epi.mode EPI_PARTIAL_F32: *n_parts receives the number of partial tiles stored.
 int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
              const int* n_rows_dev, const Epilogue& epi, void* ws, const Layout& L,
-             cudaStream_t st, bool allow_split = true, int* n_parts = nullptr, int two_sm = -1) {
+             cudaStream_t st, bool allow_split = true, int* n_parts = nullptr, int two_sm = -1,
+             int layer = 0) {
   const GemmShape s = gemm_shape(h, id);
   const bool partial = epi.mode == EPI_PARTIAL_F32;
   if (n_parts) *n_parts = 1;
+  // layers 2..N: their own projection weights (fc and the LM head are shared)
+  const LayerSlot* ls = layer > 0 && id != G_FC && id != G_LM ? &h->more[layer - 1] : nullptr;
   if (!is_bf16(h)) {
     const pe_weights& w = h->w;
-    const void* W = id == G_FC ? w.w_fc : id == G_QKV ? w.w_qkv : id == G_O ? w.w_o
-                  : id == G_GATEUP ? w.w_gate : id == G_DOWN ? w.w_down : w.w_lm;
-    const void* W2 = id == G_GATEUP ? w.w_up : nullptr;
+    const void* W = id == G_FC ? w.w_fc : id == G_QKV ? (ls ? ls->w.w_qkv : w.w_qkv)
+                  : id == G_O ? (ls ? ls->w.w_o : w.w_o)
+                  : id == G_GATEUP ? (ls ? ls->w.w_gate : w.w_gate)
+                  : id == G_DOWN ? (ls ? ls->w.w_down : w.w_down) : w.w_lm;
+    const void* W2 = id == G_GATEUP ? (ls ? ls->w.w_up : w.w_up) : nullptr;
     return launch_gemm_f32(static_cast<const float*>(W), static_cast<const float*>(W2),
                            static_cast<const float*>(X), s.M, s.K, N_cap, n_rows_dev, epi, st);
   }
@@ -221,9 +255,11 @@ int run_gemm(pe_handle* h, int id, const void* X, const void* X_lo, int N_cap,
   if (n_parts) *n_parts = p.partial ? p.k_splits : 1;
   Epilogue ep = epi;
   if (partial && !p.partial) ep.mode = EPI_STORE_F32;  // the splits reduce in a cluster
-  const CUtensorMap* mA = id == G_FC ? &h->m_fc : id == G_QKV ? &h->m_qkv : id == G_O ? &h->m_o
-                        : id == G_GATEUP ? &h->m_gate : id == G_DOWN ? &h->m_down : &h->m_lm;
-  const CUtensorMap* mA2 = id == G_GATEUP ? &h->m_up : nullptr;
+  const CUtensorMap* mA = id == G_FC ? &h->m_fc : id == G_QKV ? (ls ? &ls->m_qkv : &h->m_qkv)
+                        : id == G_O ? (ls ? &ls->m_o : &h->m_o)
+                        : id == G_GATEUP ? (ls ? &ls->m_gate : &h->m_gate)
+                        : id == G_DOWN ? (ls ? &ls->m_down : &h->m_down) : &h->m_lm;
+  const CUtensorMap* mA2 = id == G_GATEUP ? (ls ? &ls->m_up : &h->m_up) : nullptr;
   return launch_gemm_tc(p, mA, mA2, X, X_lo, n_rows_dev, ep, at<uint32_t>(ws, L.status), st);
 }
 
@@ -261,12 +297,31 @@ int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out) {
   if (n_layer != 0 && n_layer != n_all) return PE_ERR_ARG;
   const bool has_layer = n_layer == n_all;
   if (has_layer && !d.post_norm && (!w->gamma_in || !aligned16(w->gamma_in))) return PE_ERR_ARG;
+  if (w->attn_sink && !aligned16(w->attn_sink)) return PE_ERR_ARG;
+  // layers 2..N: every projection and gain (gamma_in pre-norm only), sinks optional
+  const int n_layers = d.n_layers <= 0 ? 1 : d.n_layers;
+  if (n_layers > PE_MAX_LAYERS) return PE_ERR_UNSUPPORTED;
+  if (n_layers > 1) {
+    if (!has_layer || !w->more_layers) return PE_ERR_ARG;
+    for (int l = 0; l < n_layers - 1; ++l) {
+      const pe_layer_weights& m = w->more_layers[l];
+      const void* need[] = {m.w_qkv, m.w_o, m.gamma_post, m.w_gate, m.w_up, m.w_down,
+                            m.gamma_final, d.post_norm ? m.w_qkv : m.gamma_in};
+      for (const void* p : need)
+        if (!p || !aligned16(p)) return PE_ERR_ARG;
+      if (m.attn_sink && !aligned16(m.attn_sink)) return PE_ERR_ARG;
+    }
+  }
   pe_handle* h = new (std::nothrow) pe_handle;
   if (!h) return PE_ERR_ARG;
   std::memset(h, 0, sizeof(*h));
   h->d = d;
+  h->d.n_layers = n_layers;
   h->w = *w;
+  h->w.more_layers = nullptr;  // the host array is read here only
   h->has_layer = has_layer;
+  h->n_layers = n_layers;
+  for (int l = 0; l < n_layers - 1; ++l) h->more[l].w = w->more_layers[l];
   h->num_sms = num_sms_of_current_device();
   if (h->num_sms <= 0) {
     delete h;
@@ -278,27 +333,38 @@ int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out) {
   if (bf && has_layer) {
     const int QKV = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
     const int HD = d.n_heads * d.head_dim;
-    struct {
+    struct Mat {
       CUtensorMap* map;
       const void* W;
       int M, K;
-    } mats[] = {{&h->m_fc, w->w_fc, d.d, 4 * d.d},     {&h->m_qkv, w->w_qkv, QKV, d.d},
-                {&h->m_o, w->w_o, d.d, HD},             {&h->m_gate, w->w_gate, d.inter, d.d},
-                {&h->m_up, w->w_up, d.inter, d.d},      {&h->m_down, w->w_down, d.d, d.inter},
-                {&h->m_lm, w->w_lm, d.vocab, d.d}};
+    };
+    std::vector<Mat> mats = {{&h->m_fc, w->w_fc, d.d, 4 * d.d},     {&h->m_qkv, w->w_qkv, QKV, d.d},
+                             {&h->m_o, w->w_o, d.d, HD},             {&h->m_gate, w->w_gate, d.inter, d.d},
+                             {&h->m_up, w->w_up, d.inter, d.d},      {&h->m_down, w->w_down, d.d, d.inter},
+                             {&h->m_lm, w->w_lm, d.vocab, d.d}};
+    for (int l = 0; l < n_layers - 1; ++l) {
+      LayerSlot& ls = h->more[l];
+      mats.push_back({&ls.m_qkv, ls.w.w_qkv, QKV, d.d});
+      mats.push_back({&ls.m_o, ls.w.w_o, d.d, HD});
+      mats.push_back({&ls.m_gate, ls.w.w_gate, d.inter, d.d});
+      mats.push_back({&ls.m_up, ls.w.w_up, d.inter, d.d});
+      mats.push_back({&ls.m_down, ls.w.w_down, d.d, d.inter});
+    }
+    const int n_mats = static_cast<int>(mats.size());
     bool ok = true;
     if (gemm_weights_packed()) {
       // one allocation, each copy 256-byte aligned; packed on a private stream
       // once every earlier write of the weights, on any stream, has finished
-      size_t off[7], total = 0;
-      for (int i = 0; i < 7; ++i) {
+      std::vector<size_t> off(n_mats);
+      size_t total = 0;
+      for (int i = 0; i < n_mats; ++i) {
         off[i] = total;
         total += al256(packed_weight_bytes(mats[i].M, mats[i].K));
       }
       cudaStream_t s = nullptr;
       ok = cudaDeviceSynchronize() == cudaSuccess && cudaMalloc(&h->packed, total) == cudaSuccess &&
            cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess;
-      for (int i = 0; ok && i < 7; ++i) {
+      for (int i = 0; ok && i < n_mats; ++i) {
         void* P = static_cast<char*>(h->packed) + off[i];
         ok = pack_weight(mats[i].W, mats[i].M, mats[i].K, P, s) == PE_OK &&
              encode_packed_weight_map(mats[i].map, P, mats[i].M, mats[i].K);
@@ -496,6 +562,143 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
   if ((rc = norm(part, np, e.part_stride, nullptr, x, h->w.gamma_in, d.post_norm ? 0 : 1, u, u_lo,
                  nullptr, T_out, meta->n_valid)) != PE_OK)
     return rc;
+  if (h->n_layers > 1) {
+    // ---------------- several layers: every layer runs over all non-rejected
+    // rows of each request, right-aligned in R rows (padding rows above them)
+    const int R = layer_rows(h);
+    const int NR = B * R;
+    float* xl = at<float>(ws, L.xl);
+    void* ul = at<void>(ws, L.ul);
+    bf16_t* ul_lo = bf ? at<bf16_t>(ws, L.ul_lo) : nullptr;
+    const size_t layer_elems =
+        static_cast<size_t>(num_blocks) * d.n_kv_heads * d.block_size * d.head_dim;
+    // rows no non-rejected row maps to keep finite values in the first layer
+    if (cudaMemsetAsync(q_s, 0, static_cast<size_t>(NR) * Hd * esize(h), st) != cudaSuccess ||
+        cudaMemsetAsync(x_s, 0, static_cast<size_t>(NR) * d.d * sizeof(float), st) != cudaSuccess)
+      return PE_ERR_CUDA;
+    for (int l = 0; l < h->n_layers; ++l) {
+      const bool first = l == 0, last = l == h->n_layers - 1;
+      const pe_layer_weights* lw = first ? nullptr : &h->more[l - 1].w;
+      const void* g_post = first ? h->w.gamma_post : lw->gamma_post;
+      const void* g_final = first ? h->w.gamma_final : lw->gamma_final;
+      const float* sink = static_cast<const float*>(first ? h->w.attn_sink : lw->attn_sink);
+      void* kc = static_cast<char*>(k_cache) + l * layer_elems * esize(h);
+      void* vc = static_cast<char*>(v_cache) + l * layer_elems * esize(h);
+      // QKV: the first layer over the non-rejected rows in order, later layers
+      // over the right-aligned rows (partial sums; RoPE adds them)
+      e = partial_epi(first ? T_out : NR, QKV);
+      if ((rc = first ? run_gemm(h, G_QKV, u, u_lo, T_out, meta->n_valid, e, ws, L, st, true, &np)
+                      : run_gemm(h, G_QKV, ul, ul_lo, NR, nullptr, e, ws, L, st, true, &np, -1, l)) !=
+          PE_OK)
+        return rc;
+      RopeArgs ra{};
+      ra.T_out = T_out;
+      ra.B = B;
+      ra.K = R;
+      ra.H = d.n_heads;
+      ra.G = d.n_kv_heads;
+      ra.hd = d.head_dim;
+      ra.d = d.d;
+      ra.bs = d.block_size;
+      ra.num_blocks = num_blocks;
+      ra.qkv = part;
+      ra.n_parts = np;
+      ra.part_stride = e.part_stride;
+      ra.x = x;
+      ra.n_valid = meta->n_valid;
+      ra.valid_rows = meta->valid_rows;
+      ra.valid_qsl = meta->valid_qsl;
+      ra.pos = meta->pos;
+      ra.slot = meta->slot;
+      ra.k_cache = kc;
+      ra.v_cache = vc;
+      ra.q_s = q_s;
+      ra.x_s = first ? x_s : nullptr;  // later layers' residual is already xl
+      ra.padded_in = first ? 0 : 1;
+      ra.must_fit = 1;
+      std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
+      ra.status = status;
+      if ((rc = launch_rope_kv(ra, dt, st)) != PE_OK) return rc;
+      AttnArgs aa{};
+      aa.B = B;
+      aa.K = R;
+      aa.H = d.n_heads;
+      aa.G = d.n_kv_heads;
+      aa.hd = d.head_dim;
+      aa.bs = d.block_size;
+      aa.max_blocks = max_blocks;
+      aa.num_blocks = num_blocks;
+      plan_attention(B, d.n_kv_heads, R, d.n_heads, d.head_dim, max_blocks, d.block_size,
+                     h->num_sms, aa.n_splits, aa.split_len, aa.cluster);
+      aa.q = q_s;
+      aa.k_cache = kc;
+      aa.v_cache = vc;
+      aa.block_table = block_table;
+      aa.seq_len = meta->seq_len;
+      aa.part_o = at<float>(ws, L.attn_part);
+      aa.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + L.attn_part +
+                                            al256(static_cast<size_t>(aa.n_splits) * NR *
+                                                  d.n_heads * d.head_dim * sizeof(float)));
+      aa.out = attn;
+      aa.sink = sink;
+      aa.k_min = d.K;
+      aa.status = status;
+      if ((rc = launch_attention(aa, dt, st)) != PE_OK) return rc;
+      e = partial_epi(NR, d.d);
+      if ((rc = run_gemm(h, G_O, attn, nullptr, NR, nullptr, e, ws, L, st, true, &np, -1, l)) !=
+          PE_OK)
+        return rc;
+      const float* resid = first ? x_s : xl;
+      if ((rc = norm(part, np, e.part_stride, resid, d.post_norm ? nullptr : r, g_post, 1, a, a_lo,
+                     d.post_norm ? a_f : nullptr, NR, nullptr)) != PE_OK)
+        return rc;
+      const float* mlp_resid = d.post_norm ? (bf ? a_f : static_cast<const float*>(a)) : r;
+      e = Epilogue();
+      e.mode = bf ? EPI_SWIGLU_PAIR : EPI_SWIGLU;
+      e.out = hm;
+      e.out2 = h_lo;
+      e.ld_out = d.inter;
+      if ((rc = run_gemm(h, G_GATEUP, a, a_lo, NR, nullptr, e, ws, L, st, true, nullptr, -1, l)) !=
+          PE_OK)
+        return rc;
+      e = partial_epi(NR, d.d);
+      if ((rc = run_gemm(h, G_DOWN, hm, h_lo, NR, nullptr, e, ws, L, st, true, &np, -1, l)) != PE_OK)
+        return rc;
+      if (last) {
+        // z: the final norm (pre-norm: the last layer's gamma_final) of the
+        // sample rows, the last K of each request's R rows
+        RowNormArgs n{};
+        n.x = part;
+        n.ld_x = d.d;
+        n.n_parts = np;
+        n.part_stride = e.part_stride;
+        n.resid = mlp_resid;
+        n.ld_resid = d.d;
+        n.gamma = g_final;
+        n.apply_norm = 1;
+        n.out = z_out;
+        n.ld_out = d.d;
+        n.d = d.d;
+        n.eps = d.eps;
+        n.rows_cap = NS;
+        n.in_group = R;
+        n.out_group = d.K;
+        return launch_rownorm(n, dt, st);
+      }
+      // the next layer's input: pre-norm y = residual + MLP (fp32) and its
+      // QKV operand RMSNorm(y; gamma_in of the next layer); post-norm
+      // RMSNorm(a + MLP; gamma_final), a bf16 pair that is also the residual
+      if (d.post_norm) {
+        rc = norm(part, np, e.part_stride, mlp_resid, nullptr, g_final, 1, ul, ul_lo, xl, NR,
+                  nullptr);
+      } else {
+        rc = norm(part, np, e.part_stride, mlp_resid, xl, h->more[l].w.gamma_in, 1, ul, ul_lo,
+                  nullptr, NR, nullptr);
+      }
+      if (rc != PE_OK) return rc;
+    }
+    return PE_OK;
+  }
   // QKV (partial sums; RoPE adds them)
   e = partial_epi(T_out, QKV);
   if ((rc = run_gemm(h, G_QKV, u, u_lo, T_out, meta->n_valid, e, ws, L, st, true, &np)) != PE_OK)
@@ -550,6 +753,7 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
                                               d.head_dim * sizeof(float)));
   aa.out = attn;
   aa.sink = static_cast<const float*>(h->w.attn_sink);
+  aa.k_min = d.K;
   aa.status = status;
   if ((rc = launch_attention(aa, dt, st)) != PE_OK) return rc;
   // O projection (partial sums)

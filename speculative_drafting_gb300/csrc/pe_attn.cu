@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
 
   int L = a.seq_len[r];
   const int Lmax = a.max_blocks * a.bs;
-  if (L > Lmax || L < a.K) {
+  if (L > Lmax || L < a.k_min) {
     if (threadIdx.x == 0) set_status(a.status, PE_ST_BLOCK_RANGE);
     L = min(max(L, 0), Lmax);
   }
@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int L = a.seq_len[r];
   const int Lmax = a.max_blocks * a.bs;
-  if (L > Lmax || L < a.K) {
+  if (L > Lmax || L < a.k_min) {
     if (threadIdx.x == 0) set_status(a.status, PE_ST_BLOCK_RANGE);
     L = min(max(L, 0), Lmax);
   }

@@ -61,10 +61,14 @@ __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
   int n = a.rows_cap;
   if (a.n_rows_dev) n = min(max(*a.n_rows_dev, 0), a.rows_cap);
   if (row >= n) return;
-  const size_t ro = static_cast<size_t>(row) * a.ld_x;
+  // input row: the same, or the row-th sample row of a right-aligned layout
+  const int irow = a.in_group > 0 ? (row / a.out_group) * a.in_group +
+                                        (a.in_group - a.out_group) + row % a.out_group
+                                  : row;
+  const size_t ro = static_cast<size_t>(irow) * a.ld_x;
   const float4* x0 = reinterpret_cast<const float4*>(a.x + ro);
   const float4* res =
-      a.resid ? reinterpret_cast<const float4*>(a.resid + static_cast<size_t>(row) * a.ld_resid)
+      a.resid ? reinterpret_cast<const float4*>(a.resid + static_cast<size_t>(irow) * a.ld_resid)
               : nullptr;
   auto load = [&](int i) {
     float4 s = x0[i];
@@ -167,29 +171,48 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
   __shared__ int samp_sh;
   pdl_trigger();
   pdl_wait();
-  const int v = blockIdx.x;
-  const int nv = min(max(*a.n_valid, 0), a.T_out);
-  if (v >= nv) return;
+  const int half = a.hd / 2;
+  int v;  // the non-rejected row this CTA rotates
+  if (a.padded_in) {
+    // right-aligned rows: row blockIdx.x = r * K + k of request r
+    const int r = blockIdx.x / a.K, k = blockIdx.x - r * a.K;
+    v = a.valid_qsl[r + 1] - a.K + k;
+    if (v < a.valid_qsl[r]) {
+      // padding row: a zero query (its output is never used), no KV
+      T* q = static_cast<T*>(a.q_s) + static_cast<size_t>(blockIdx.x) * a.H * a.hd;
+      const int tid = blockIdx.y * blockDim.x + threadIdx.x;
+      for (int e = tid; e < a.H * a.hd; e += gridDim.y * blockDim.x) q[e] = Elem<T>::from_f(0.f);
+      return;
+    }
+  } else {
+    v = blockIdx.x;
+    const int nv = min(max(*a.n_valid, 0), a.T_out);
+    if (v >= nv) return;
+  }
   const int o = a.valid_rows[v];
   if (o < 0 || o >= a.T_out) {
     if (threadIdx.x == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
     return;
   }
-  const int half = a.hd / 2;
   const int64_t p = a.pos[o];
   const int64_t slot = a.slot[o];
   if (threadIdx.x == 0) {
-    // request of row v: largest r with valid_qsl[r] <= v
-    int lo = 0, hi = a.B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.valid_qsl[mid] <= v)
-        lo = mid;
-      else
-        hi = mid - 1;
+    if (a.padded_in) {
+      samp_sh = blockIdx.x;
+    } else {
+      // request of row v: largest r with valid_qsl[r] <= v
+      int lo = 0, hi = a.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.valid_qsl[mid] <= v)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      const int k = v - (a.valid_qsl[lo + 1] - a.K);
+      samp_sh = (k >= 0 && k < a.K) ? lo * a.K + k : -1;
+      if (k < 0 && a.must_fit && blockIdx.y == 0) set_status(a.status, PE_ST_ROWS_RANGE);
     }
-    const int k = v - (a.valid_qsl[lo + 1] - a.K);
-    samp_sh = (k >= 0 && k < a.K) ? lo * a.K + k : -1;
   }
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
     const double ang = static_cast<double>(p) * a.inv_freq[i];
@@ -206,7 +229,7 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
   const int tid = blockIdx.y * blockDim.x + threadIdx.x;  // thread within the row
   const int nthr = gridDim.y * blockDim.x;
   // element x of this row of the QKV projection: the sum of its partial tiles
-  const float* row0 = a.qkv + static_cast<size_t>(v) * QKV;
+  const float* row0 = a.qkv + static_cast<size_t>(a.padded_in ? blockIdx.x : v) * QKV;
   auto qkv_at = [&](int x) {
     float acc = 0.f;
     for (int k = 0; k < a.n_parts; ++k) acc += row0[k * a.part_stride + x];
@@ -241,7 +264,7 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
       vc[i] = Elem<T>::from_f(qkv_at((a.H + a.G) * a.hd + e));
     }
   }
-  if (s_idx >= 0) {
+  if (s_idx >= 0 && a.x_s) {
     // the fc output of the sample rows is the attention residual (fp32)
     const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(v) * a.d);
     float4* dst = reinterpret_cast<float4*>(a.x_s + static_cast<size_t>(s_idx) * a.d);
@@ -250,11 +273,12 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
 }
 
 int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st) {
-  if (a.T_out <= 0) return PE_OK;
+  const int rows = a.padded_in ? a.B * a.K : a.T_out;
+  if (rows <= 0) return PE_OK;
   const cudaError_t e =
       dtype == PE_DTYPE_BF16
-          ? launch_pdl(rope_kv_kernel<bf16>, dim3(a.T_out, kRopeCtasPerRow), dim3(256), 0, st, a)
-          : launch_pdl(rope_kv_kernel<float>, dim3(a.T_out, kRopeCtasPerRow), dim3(256), 0, st, a);
+          ? launch_pdl(rope_kv_kernel<bf16>, dim3(rows, kRopeCtasPerRow), dim3(256), 0, st, a)
+          : launch_pdl(rope_kv_kernel<float>, dim3(rows, kRopeCtasPerRow), dim3(256), 0, st, a);
   return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 

@@ -80,6 +80,10 @@ struct RowNormArgs {
   float eps;
   int rows_cap;
   const int* n_rows_dev;
+  // in_group > 0: output row i reads input row (i / out_group) * in_group +
+  // (in_group - out_group) + i % out_group, i.e. the last out_group of each
+  // group of in_group input rows (the sample rows of a right-aligned layout)
+  int in_group, out_group;
 };
 int launch_rownorm(const RowNormArgs& a, int dtype, cudaStream_t st);
 
@@ -99,8 +103,16 @@ struct RopeArgs {
   void* k_cache;
   void* v_cache;
   void* q_s;    // [B*K][H][hd] queries of the sample rows
-  float* x_s;  // [B*K][d] fc output of the sample rows (residual, fp32)
+  float* x_s;  // [B*K][d] fc output of the sample rows (residual, fp32); nullable
   double inv_freq[64];
+  // 0: qkv rows are the non-rejected rows in valid_rows order (K is then the
+  // number of rows per request that q_s / x_s keep, right-aligned);
+  // 1: qkv rows are already in that right-aligned layout, B*K rows (rows of a
+  // request before its first non-rejected row are padding: q = 0, no KV write)
+  int padded_in;
+  // padded_in 0: a non-rejected row left out of the K kept rows of its request
+  // sets PE_ST_ROWS_RANGE (several layers need every row)
+  int must_fit;
   uint32_t* status;
 };
 int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st);
@@ -122,6 +134,7 @@ struct AttnArgs {
   float* part_ml;  // [n_splits][B*K][H][2]      (bf16 path)
   void* out;       // [B*K][H*hd]
   const float* sink;  // [H] per-head sink logit (natural units), nullable
+  int k_min;          // seq_len below this is an input error (the draft depth K)
   uint32_t* status;
 };
 int attention_split_count(int B, int G, int max_blocks, int bs, int num_sms);

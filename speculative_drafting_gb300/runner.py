@@ -45,7 +45,10 @@ class StepRunner:
         self.num_blocks = int(batch["num_blocks"])
         K = wl.dims.K
         self.T_out = self.T_in + self.B * (K - 1)
-        self.w = {k: to_device(v, dt, device) for k, v in weights.items()}
+        self.w = {k: to_device(v, dt, device) for k, v in weights.items() if k != "layers"}
+        if weights.get("layers"):
+            self.w["layers"] = [{k: to_device(v, dt, device) for k, v in lw.items()}
+                                for lw in weights["layers"]]
         self.inp = {k: to_device(batch[k], dt, device) for k in
                     ("qsl", "prev_tok", "prev_pos", "accepted", "bonus", "block_table", "H_tgt")}
         self.drafter = binding.Drafter(wl.dims, self.w) if wl.has_drafter else None

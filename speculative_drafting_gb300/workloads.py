@@ -135,6 +135,16 @@ WORKLOADS = {
         name="gptoss_b64_k7_postnorm", dims=_gpt_oss_dims(post_norm=True), batch=64,
         n_prev=8, ctx=("uniform", 512, 8192),
         description="GPT-OSS-20B-shaped drafter, bf16, B=64, K=7, ctx U[512,8192], post-norm"),
+    # four decoder layers (every layer but the last over all non-rejected rows)
+    "gptoss_b1_k7_4layers": Workload(
+        name="gptoss_b1_k7_4layers", dims=dataclasses.replace(_gpt_oss_dims(), n_layers=4),
+        batch=1, n_prev=8, ctx=(2048,),
+        description="GPT-OSS-20B-shaped 4-layer drafter, bf16, B=1, K=7, context 2048"),
+    "gptoss_b64_k7_postnorm_4layers": Workload(
+        name="gptoss_b64_k7_postnorm_4layers",
+        dims=dataclasses.replace(_gpt_oss_dims(post_norm=True), n_layers=4), batch=64,
+        n_prev=8, ctx=("uniform", 512, 8192),
+        description="GPT-OSS-20B-shaped 4-layer drafter, bf16, B=64, K=7, ctx U[512,8192], post-norm"),
     "llama8b_b32_k8_32k": Workload(
         name="llama8b_b32_k8_32k",
         dims=Dims(d=4096, n_heads=32, n_kv_heads=8, head_dim=128, inter=14336,

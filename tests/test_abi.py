@@ -74,3 +74,21 @@ def test_verify_host_checks(lib):
         binding.PE_ERR_ARG
     assert call(-1, 0, *([None] * 3), 10, binding.PE_DTYPE_F32, *([None] * 4), 0, None) == \
         binding.PE_ERR_ARG
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """The ctypes structs the binding marshals have the header's sizes."""
+    gxx = shutil.which("g++") or shutil.which("gcc")
+    if gxx is None:
+        pytest.skip("needs a host C++ compiler")
+    src = tmp_path / "sizes.cc"
+    src.write_text('#include <cstdio>\n#include "pe.h"\nint main(){std::printf("%zu %zu %zu %zu",'
+                   ' sizeof(pe_dims), sizeof(pe_weights), sizeof(pe_layer_weights), sizeof(pe_meta));}\n')
+    exe = tmp_path / "sizes"
+    import subprocess
+
+    subprocess.run([gxx, "-x", "c++", "-I", __import__("os").path.dirname(binding.HEADER), str(src),
+                    "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got == [ctypes.sizeof(binding.PeDims), ctypes.sizeof(binding.PeWeights),
+                   ctypes.sizeof(binding.PeLayerWeights), ctypes.sizeof(binding.PeMeta)]
