@@ -135,6 +135,12 @@ WORKLOADS = {
         name="gptoss_b64_k7_postnorm", dims=_gpt_oss_dims(post_norm=True), batch=64,
         n_prev=8, ctx=("uniform", 512, 8192),
         description="GPT-OSS-20B-shaped drafter, bf16, B=64, K=7, ctx U[512,8192], post-norm"),
+    # the GPT-oss attention: per-head sink logits
+    "gptoss_b64_k7_postnorm_sinks": Workload(
+        name="gptoss_b64_k7_postnorm_sinks", dims=_gpt_oss_dims(post_norm=True), batch=64,
+        n_prev=8, ctx=("uniform", 512, 8192), sinks=True,
+        description="GPT-OSS-20B-shaped drafter with attention sinks, bf16, B=64, K=7, "
+                    "ctx U[512,8192], post-norm"),
     # four decoder layers (every layer but the last over all non-rejected rows)
     "gptoss_b1_k7_4layers": Workload(
         name="gptoss_b1_k7_4layers", dims=dataclasses.replace(_gpt_oss_dims(), n_layers=4),
