@@ -255,17 +255,36 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
       }
       // mask (range, invalid blocks, causal limit), online softmax
       const int kbase = t0 + c * kKC + kofs;
+      // this warp's keys of the chunk are all in range, in valid blocks and at or
+      // before position P0, which every query row sees: no per-key mask (the
+      // same for the whole warp)
+      constexpr uint32_t kGroupBits = (1u << (KEYS / 16)) - 1u;
+      const bool interior = kbase + KEYS <= t1 && kbase + KEYS - 1 <= P0 &&
+                            ((mask >> (kofs >> 4)) & kGroupBits) == kGroupBits;
       float mx_a = -INFINITY, mx_b = -INFINITY;
+      if (interior) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = kbase + nt * 8 + tq * 2 + e;
-          const bool ok = t < t1 && ((mask >> ((kofs + nt * 8) >> 4)) & 1u);
-          s[nt][e] = (ok && t <= lim_a) ? s[nt][e] * sc : -INFINITY;
-          s[nt][2 + e] = (ok && t <= lim_b) ? s[nt][2 + e] * sc : -INFINITY;
-          mx_a = fmaxf(mx_a, s[nt][e]);
-          mx_b = fmaxf(mx_b, s[nt][2 + e]);
+          for (int e = 0; e < 2; ++e) {
+            s[nt][e] *= sc;
+            s[nt][2 + e] *= sc;
+            mx_a = fmaxf(mx_a, s[nt][e]);
+            mx_b = fmaxf(mx_b, s[nt][2 + e]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int t = kbase + nt * 8 + tq * 2 + e;
+            const bool ok = t < t1 && ((mask >> ((kofs + nt * 8) >> 4)) & 1u);
+            s[nt][e] = (ok && t <= lim_a) ? s[nt][e] * sc : -INFINITY;
+            s[nt][2 + e] = (ok && t <= lim_b) ? s[nt][2 + e] * sc : -INFINITY;
+            mx_a = fmaxf(mx_a, s[nt][e]);
+            mx_b = fmaxf(mx_b, s[nt][2 + e]);
+          }
         }
       }
       mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
