@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import os
@@ -58,6 +59,33 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+# ----------------------------------------------------------------------------- ranks
+# Several GPUs run independent replicas: each rank drafts (or verifies) its own
+# seeded batch, no data crosses ranks, and the job's time is the slowest rank's.
+
+
+def rank_workload(wl, rank):
+    """The workload of one rank: the same recipe, its own seed."""
+    return dataclasses.replace(wl, seed=wl.seed + rank)
+
+
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x, on every rank (a no-op for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms):
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
 
 
 def measured_peaks():
@@ -247,7 +275,7 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     wl = W.get(args.workload)
-    wl_rank = W.get(args.workload, seed=wl.seed + rank)  # each rank drafts its own batch
+    wl_rank = rank_workload(wl, rank)  # each rank drafts its own batch
     batch = W.make_batch(wl_rank)
     w = W.make_weights(wl)
     kc, vc = W.make_kv_cache(wl_rank, batch["num_blocks"])
@@ -325,10 +353,7 @@ def run_ours(args, rank, world, local):
             ev[i][1].record(stream)
     torch.cuda.synchronize()
     lm_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    if world > 1:
-        t = torch.tensor([step_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, world, "cuda")
 
     # eager (no graph) step time, for reference
     with torch.cuda.stream(stream):
@@ -371,10 +396,7 @@ def run_ours(args, rank, world, local):
         a1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a0.elapsed_time(a1) / n_e2e
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
     st, _ = r.status()
     if st:
         raise RuntimeError(f"device status {st:#x} after timing")
@@ -395,7 +417,7 @@ def run_ours(args, rank, world, local):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}
     total_tokens = n_rows * world
-    value = total_tokens / (step_ms / 1e3)
+    value = job_throughput(n_rows, world, step_ms)
     line = None
     if rank == 0:
         cpu = None
@@ -518,7 +540,7 @@ def run_verify(args, rank, world, local):
         build.build()
     if world > 1:
         torch.distributed.barrier()
-    b = W.make_verify_batch(W.get_verify(args.workload, seed=wl.seed + rank))
+    b = W.make_verify_batch(rank_workload(wl, rank))
     B, T_in, V = b["B"], b["T_in"], b["V"]
     esize = 2 if wl.dtype == "bf16" else 4
     code = binding.PE_DTYPE_BF16 if wl.dtype == "bf16" else binding.PE_DTYPE_F32
@@ -574,10 +596,7 @@ def run_verify(args, rank, world, local):
     torch.cuda.synchronize()
     clk = clocks.stop()
     call_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
-    if world > 1:
-        t = torch.tensor([call_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        call_ms = float(t.item())
+    call_ms = max_over_ranks(call_ms, world, "cuda")
     # end to end: pinned host logits and tokens in, target tokens and counts out
     h_in = {"qsl": torch.from_numpy(b["qsl"]).pin_memory(),
             "tok": torch.from_numpy(b["tok"]).pin_memory(), "logits": lg_host.pin_memory()}
