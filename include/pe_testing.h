@@ -1,5 +1,6 @@
 /*
- * pe_testing.h -- unit-test hook of libpe: one drafter projection in isolation.
+ * pe_testing.h -- unit-test hooks of libpe: one drafter projection in isolation,
+ * and the bounded device wait run out on purpose.
  *
  * Not part of the parallel-draft step.  It runs exactly the kernel the step runs
  * for one of the drafter's projections (tcgen05 GEMM for bf16, SIMT GEMM for
@@ -54,6 +55,14 @@ size_t pe_test_projection_workspace(const pe_handle* h, int which, int n_rows);
  * failure.  The status word is the first 4 bytes of ws (pe_read_status). */
 int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void* out, void* ws,
                        size_t ws_bytes, void* stream);
+
+/* Failure-detection check: one kernel whose bounded device wait (the mbarrier
+ * wait every kernel of the step uses, limit 2 s) waits on a barrier that nothing
+ * ever arrives on.  When the limit runs out the kernel ORs PE_ST_TIMEOUT into the
+ * status word (the first 4 bytes of ws, at least 256 bytes, 16-byte aligned) and
+ * returns; nothing faults and the context stays usable.  The caller clears the
+ * word first (pe_read_status with clear set). */
+int pe_test_bounded_wait(void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

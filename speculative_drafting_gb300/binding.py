@@ -110,6 +110,8 @@ def load(path: str | None = None):
     lib.pe_test_projection_workspace.restype = _sz
     lib.pe_test_projection.argtypes = [_vp, _i32, _vp, _i32, _vp, _vp, _sz, _vp]
     lib.pe_test_projection.restype = _i32
+    lib.pe_test_bounded_wait.argtypes = [_vp, _sz, _vp]
+    lib.pe_test_bounded_wait.restype = _i32
     lib.pe_verify_workspace_bytes.argtypes = [_i32, _i32]
     lib.pe_verify_workspace_bytes.restype = _sz
     lib.pe_verify_greedy.argtypes = [_i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp,

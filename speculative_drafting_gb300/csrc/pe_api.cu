@@ -408,6 +408,7 @@ int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl, const i
                       const int32_t* block_table, int max_blocks, int num_blocks,
                       const void* H_tgt, const pe_meta* meta, void* G_out, void* E_out,
                       void* A_out, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("pe_prepare_inputs");
   if (!h || B < 1 || T_in < B || max_blocks < 1 || num_blocks < 1 || !qsl || !prev_tok ||
       !prev_pos || !accepted || !bonus || !block_table || !H_tgt || !ws)
     return PE_ERR_ARG;
@@ -486,6 +487,7 @@ int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl, const i
 int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void* A,
                   const int32_t* block_table, int max_blocks, int num_blocks, void* k_cache,
                   void* v_cache, void* z_out, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("pe_draft_step");
   if (!h || !h->has_layer || B < 1 || T_in < B || max_blocks < 1 || num_blocks < 1 || !A ||
       !block_table || !k_cache || !v_cache || !z_out || !ws)
     return PE_ERR_ARG;
@@ -786,6 +788,7 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
 
 int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, float* logits,
               void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("pe_argmax");
   if (!h || !h->has_layer || !z || n_rows < 1 || !draft_tokens || !ws) return PE_ERR_ARG;
   if (!aligned16(z) || !aligned16(ws)) return PE_ERR_ARG;
   const Layout L = layout_argmax(h, n_rows);
@@ -801,6 +804,11 @@ int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, fl
   int rc = run_gemm(h, G_LM, z, nullptr, n_rows, nullptr, e, ws, L, st);
   if (rc != PE_OK) return rc;
   return launch_argmax_finalize(keys, n_rows, draft_tokens, st);
+}
+
+int pe_test_bounded_wait(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < 256 || !aligned16(ws)) return PE_ERR_ARG;
+  return launch_bounded_wait(static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream));
 }
 
 size_t pe_test_projection_workspace(const pe_handle* h, int which, int n_rows) {

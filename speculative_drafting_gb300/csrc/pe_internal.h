@@ -8,7 +8,32 @@
 
 #include "pe.h"
 
+#if __has_include(<nvtx3/nvToolsExt.h>)
+#include <nvtx3/nvToolsExt.h>
+#define PE_HAVE_NVTX 1
+#endif
+
 namespace pe {
+
+// An NVTX range over the enqueue of one C-ABI call, so that a profiler can pick
+// out a call's kernels (ncu --nvtx --nvtx-include "pe_argmax/").  Without a tool
+// attached the push and pop do nothing.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) {
+#ifdef PE_HAVE_NVTX
+    nvtxRangePushA(name);
+#else
+    (void)name;
+#endif
+  }
+  ~NvtxRange() {
+#ifdef PE_HAVE_NVTX
+    nvtxRangePop();
+#endif
+  }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ------------------------------------------------------------------ GEMM epilogues
 // Every drafter projection is D[t][f] = sum_k X[t][k] * W[f][k] (X: token rows,

@@ -320,4 +320,26 @@ int launch_argmax_finalize(const unsigned long long* keys, int n, int32_t* out, 
              : PE_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ bounded-wait check
+
+// One thread waits, through the bounded mbarrier wait every kernel here uses, on
+// a barrier nothing ever arrives on.  The wait gives up after its limit; the
+// kernel records PE_ST_TIMEOUT and returns, leaving the context usable.
+__global__ void __launch_bounds__(32) bounded_wait_kernel(uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_sh;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0u, &abort_sh)) set_status(status, PE_ST_TIMEOUT);
+}
+
+int launch_bounded_wait(uint32_t* status, cudaStream_t st) {
+  bounded_wait_kernel<<<1, 32, 0, st>>>(status);
+  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+}
+
 }  // namespace pe

@@ -149,4 +149,8 @@ int launch_zero_keys(unsigned long long* keys, int n, cudaStream_t st);
 // keys -> ids
 int launch_argmax_finalize(const unsigned long long* keys, int n, int32_t* out, cudaStream_t st);
 
+// ---------------------------------------------------------------- bounded-wait check
+// one kernel whose bounded wait can never be satisfied: it records PE_ST_TIMEOUT
+int launch_bounded_wait(uint32_t* status, cudaStream_t st);
+
 }  // namespace pe

@@ -245,6 +245,7 @@ extern "C" int pe_verify_greedy(int B, int T_in, const int32_t* qsl, const int32
                                 const void* logits, int vocab, int dtype, int32_t* target_tok,
                                 int32_t* accepted, int32_t* bonus, void* ws, size_t ws_bytes,
                                 void* stream) {
+  NvtxRange nvtx("pe_verify_greedy");
   if (B < 0 || T_in < 0 || vocab < 1) return PE_ERR_ARG;
   if (dtype != PE_DTYPE_F32 && dtype != PE_DTYPE_BF16) return PE_ERR_UNSUPPORTED;
   if (B == 0) return T_in == 0 ? PE_OK : PE_ERR_ARG;
