@@ -60,6 +60,14 @@ __host__ __device__ inline AttnShape attn_shape(int rows) {
   return s;
 }
 
+// 2^x by the hardware approximation (ex2.approx.ftz: results below the normal
+// range flush to 0, weights far below the rounding of any sum they join).
+PE_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // One CTA per (key split, KV head, request).  The producer warp walks the
 // split's 64-key chunks: per 16-key group it looks the block up once and loads
 // the K and V rows of this KV head with TMA (128-byte swizzle, 64 elements of
@@ -292,8 +300,8 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
       mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
       mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
       const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-      const float al_a = (mn_a == -INFINITY) ? 1.f : exp2f(m_a - mn_a);
-      const float al_b = (mn_b == -INFINITY) ? 1.f : exp2f(m_b - mn_b);
+      const float al_a = (mn_a == -INFINITY) ? 1.f : ex2_approx(m_a - mn_a);
+      const float al_b = (mn_b == -INFINITY) ? 1.f : ex2_approx(m_b - mn_b);
       m_a = mn_a;
       m_b = mn_b;
       float ps_a = 0.f, ps_b = 0.f;
@@ -301,8 +309,8 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
       for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          s[nt][e] = (mn_a == -INFINITY) ? 0.f : exp2f(s[nt][e] - mn_a);
-          s[nt][2 + e] = (mn_b == -INFINITY) ? 0.f : exp2f(s[nt][2 + e] - mn_b);
+          s[nt][e] = (mn_a == -INFINITY) ? 0.f : ex2_approx(s[nt][e] - mn_a);
+          s[nt][2 + e] = (mn_b == -INFINITY) ? 0.f : ex2_approx(s[nt][2 + e] - mn_b);
           ps_a += s[nt][e];
           ps_b += s[nt][2 + e];
         }
