@@ -196,22 +196,28 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
   }
   const int64_t p = a.pos[o];
   const int64_t slot = a.slot[o];
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
     if (a.padded_in) {
-      samp_sh = blockIdx.x;
+      if (threadIdx.x == 0) samp_sh = blockIdx.x;
     } else {
-      // request of row v: largest r with valid_qsl[r] <= v
-      int lo = 0, hi = a.B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.valid_qsl[mid] <= v)
-          lo = mid;
-        else
-          hi = mid - 1;
+      // request of row v: the requests whose first non-rejected row is at or
+      // before v, less one (valid_qsl rises strictly: each request keeps at
+      // least K rows).  The warp compares 32 offsets per round with one ballot;
+      // the rounds' loads are independent, so a batch costs one or two load
+      // latencies instead of a binary search's log2(B) dependent loads.
+      const int lane = threadIdx.x;
+      int cnt = 0;
+#pragma unroll 4
+      for (int base = 0; base < a.B; base += 32) {
+        const int i = base + lane;
+        cnt += __popc(__ballot_sync(0xffffffffu, i < a.B && a.valid_qsl[i] <= v));
       }
-      const int k = v - (a.valid_qsl[lo + 1] - a.K);
-      samp_sh = (k >= 0 && k < a.K) ? lo * a.K + k : -1;
-      if (k < 0 && a.must_fit && blockIdx.y == 0) set_status(a.status, PE_ST_ROWS_RANGE);
+      if (lane == 0) {
+        const int r = cnt - 1;
+        const int k = v - (a.valid_qsl[r + 1] - a.K);
+        samp_sh = (k >= 0 && k < a.K) ? r * a.K + k : -1;
+        if (k < 0 && a.must_fit && blockIdx.y == 0) set_status(a.status, PE_ST_ROWS_RANGE);
+      }
     }
   }
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
