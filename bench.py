@@ -13,7 +13,7 @@ A verify_* workload times pe_verify_greedy (the greedy verification that yields
 the next step's accepted counts and bonus tokens) instead of the draft step.
 
 Prints one JSON line.  --impl reference times the CPU oracle (the only
-reference this build has) on a bounded sample of the same workload.
+reference there is) on a bounded sample of the same workload.
 """
 
 from __future__ import annotations
