@@ -19,6 +19,7 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     ("tiny_fp32", {"n_layers": 2}),
+    ("tiny_fp32", {"n_layers": 2, "K": 1, "n_prev": 2}),  # n_r = K + 1 verify rows
     ("tiny_fp32", {"n_layers": 3, "post_norm": True, "sinks": True}),
     ("small_prenorm", {"n_layers": 3}),
     ("small_postnorm_hd128", {"n_layers": 2}),

@@ -144,3 +144,35 @@ def test_bad_qsl_is_clamped_and_reported():
     assert a[1] == 0 and bo[1] == -1
     ref2 = _oracle(np.array([0, 9], np.int32), tok[3:], lg[3:], "f32")
     assert a[2] == ref2[1][0] and bo[2] == ref2[2][0]
+
+
+def test_verify_replays_in_a_cuda_graph():
+    """Captured once, replayed: the same results on every replay (the call holds
+    no host state and allocates nothing)."""
+    torch = cuda_or_skip()
+    built()
+    wl = W.get_verify("verify_small")
+    b = W.make_verify_batch(wl)
+    d = {k: torch.from_numpy(b[k]).cuda() for k in ("qsl", "tok", "logits")}
+    target = torch.empty(b["T_in"], dtype=torch.int32, device="cuda")
+    acc = torch.empty(b["B"], dtype=torch.int32, device="cuda")
+    bon = torch.empty(b["B"], dtype=torch.int32, device="cuda")
+    ws = binding.verify_workspace(b["T_in"], b["V"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        binding.verify_greedy(b["B"], b["T_in"], d["qsl"], d["tok"], d["logits"], b["V"],
+                              binding.PE_DTYPE_F32, target, acc, bon, ws, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        binding.verify_greedy(b["B"], b["T_in"], d["qsl"], d["tok"], d["logits"], b["V"],
+                              binding.PE_DTYPE_F32, target, acc, bon, ws, stream=s)
+    ref = _oracle(b["qsl"], b["tok"], b["logits"], "f32")
+    for _ in range(3):
+        target.fill_(-9)
+        acc.fill_(-9)
+        bon.fill_(-9)
+        g.replay()
+        torch.cuda.synchronize()
+        for got, want in zip((target, acc, bon), ref):
+            np.testing.assert_array_equal(host(got), want)
