@@ -95,6 +95,11 @@ constexpr int kMaxBN = PE_MAX_BN;
 #define PE_TWO_SM 0
 #endif
 constexpr bool kTwoSm = PE_TWO_SM != 0;
+// 2-SM pairs: two pairs per SM pair (one TMEM accumulator each) where they fit
+#ifndef PE_PAIR_TWO_PER_SM
+#define PE_PAIR_TWO_PER_SM 1
+#endif
+constexpr bool kPairTwoPerSm = PE_PAIR_TWO_PER_SM != 0;
 constexpr int kNarrowCtasPerSm = PE_NARROW_CTAS_PER_SM;
 constexpr int kStreamCtasPerSm = PE_STREAM_CTAS_PER_SM;
 // shared memory of an SM that its CTAs can have (228 KB less 1 KB)
@@ -789,7 +794,8 @@ PE_DEV bool next_pair_tile(const TcArgs& p, int it, uint32_t rank, TileRef& t) {
   return true;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int OCC>
+__global__ void __launch_bounds__(kTcThreads, OCC)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mapA,
                         const __grid_constant__ CUtensorMap mapA2,
                         const __grid_constant__ CUtensorMap mapB,
@@ -1125,23 +1131,36 @@ static int max_active_clusters(int occ, int cs, size_t smem) {
   return n * occ;
 }
 
-static cudaError_t tc_pair_prepare() {
-  const cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel,
+using TcPairKernelFn = decltype(&gemm_tc_pair_kernel<1>);
+
+// The pair instance for one or two pair CTAs per SM.
+static TcPairKernelFn tc_pair_kernel(int occ) {
+  return occ >= 2 ? gemm_tc_pair_kernel<2> : gemm_tc_pair_kernel<1>;
+}
+
+// Dynamic shared memory limit of a pair instance (as tc_max_dyn_smem: the limit
+// decides how many CTAs the SM takes).
+static size_t tc_pair_max_dyn_smem(int occ) {
+  return occ >= 2 ? kSmemPerSm / 2 - cta_smem_overhead(true) + 1024 : kSmemBudget + 1024;
+}
+
+static cudaError_t tc_pair_prepare(int occ) {
+  const cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel(occ),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBudget + 1024));
-  cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             static_cast<int>(tc_pair_max_dyn_smem(occ)));
+  cudaFuncSetAttribute(tc_pair_kernel(occ), cudaFuncAttributePreferredSharedMemoryCarveout,
                        cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
 // Clusters of two pair-kernel CTAs with `smem` bytes each resident at once.
-static int max_pair_clusters(size_t smem) {
+static int max_pair_clusters(size_t smem, int occ) {
   static std::mutex mu;
-  static std::map<size_t, int> cache;
+  static std::map<std::pair<size_t, int>, int> cache;
   std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find(smem);
+  auto it = cache.find({smem, occ});
   if (it != cache.end()) return it->second;
-  tc_pair_prepare();
+  tc_pair_prepare(occ);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 64);
   cfg.blockDim = dim3(kTcThreads);
@@ -1154,11 +1173,11 @@ static int max_pair_clusters(size_t smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, (void*)gemm_tc_pair_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)tc_pair_kernel(occ), &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
-  cache[smem] = n;
+  cache[{smem, occ}] = n;
   return n;
 }
 
@@ -1202,19 +1221,27 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
     if (use2) {
       pl.cta2 = 1;
       pl.atoms = 1;
-      pl.ctas_per_sm = 1;
       pl.partial = 0;
       pl.num_kb = (K + kBK - 1) / kBK;
       const size_t sb = static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN / 2) * 128 * nB;
-      pl.stages = std::max(2, std::min(kMaxStages, static_cast<int>(kSmemBudget / sb)));
+      // two pairs per SM pair when one accumulator of each fits half the TMEM
+      // and two stages fit half the shared memory: one pair's epilogue then
+      // runs beside the other's MMAs
+      const size_t half = tc_pair_max_dyn_smem(2) - 1024;
+      const bool two = kPairTwoPerSm && pl.BN * nA <= 256 && half / sb >= 2;
+      pl.ctas_per_sm = two ? 2 : 1;
+      pl.stages = two ? std::min(kMaxStages, static_cast<int>(half / sb))
+                      : std::max(2, std::min(kMaxStages, static_cast<int>(kSmemBudget / sb)));
       pl.smem_bytes = pl.stages * sb + 1024;
       pl.k_splits = 1;
       pl.kb_per_split = pl.num_kb;
-      pl.acc_bufs = 2 * pl.BN * nA <= 512 ? 2 : 1;
+      pl.acc_bufs = two ? 1 : (2 * pl.BN * nA <= 512 ? 2 : 1);
       uint32_t c = 32;
       while (c < static_cast<uint32_t>(pl.acc_bufs * pl.BN * nA)) c <<= 1;
       pl.tmem_cols = static_cast<int>(c);
-      const int clusters = max_pair_clusters(pl.smem_bytes);
+      // two pairs on each SM pair: as many clusters as SMs (the occupancy
+      // query does not see the TMEM share, the arithmetic above does)
+      const int clusters = two ? num_sms : max_pair_clusters(pl.smem_bytes, 1);
       pl.grid = 2 * std::max(1, std::min(pair_tiles, clusters));
       pl.main_tiles = pair_tiles;
       pl.tail_splits = 1;
@@ -1417,7 +1444,7 @@ static int launch_pair(const TcPlan& pl, const CUtensorMap* mapA, const CUtensor
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, *mapA, pl.dual ? *mapA2 : *mapA, mapB,
+  return cudaLaunchKernelEx(&cfg, tc_pair_kernel(pl.ctas_per_sm), *mapA, pl.dual ? *mapA2 : *mapA, mapB,
                             mapB2, a) == cudaSuccess
              ? PE_OK
              : PE_ERR_CUDA;
@@ -1444,7 +1471,7 @@ int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap*
   // one attribute value per instance for every launch, so kernels captured
   // into a graph stay launchable whatever order they replay in
   if (pl.cta2) {
-    if (tc_pair_prepare() != cudaSuccess) return PE_ERR_CUDA;
+    if (tc_pair_prepare(pl.ctas_per_sm) != cudaSuccess) return PE_ERR_CUDA;
     return launch_pair(pl, mapA, mapA2, mapB, mapB2, n_rows_dev, epi, status, st);
   }
   if (tc_prepare(pl.ctas_per_sm) != cudaSuccess) return PE_ERR_CUDA;
