@@ -310,21 +310,36 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
 // A[v] = [RMSNorm(G0) g0, RMSNorm(G1) g1, RMSNorm(G2) g2, E] for non-rejected row
 // v (output row valid_rows[v]), straight from H_tgt / h_shared / the embedding.
 // blockIdx.x = v, blockIdx.y = segment (0..2 streams, 3 embedding).
+// Vectors of a stream segment each thread keeps in registers (rows of up to
+// 4 * 128 * 8 bf16 = 4096 elements; longer rows read the rest twice).
+constexpr int kInputVecs = 4;
+
 template <typename T>
 __global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
   __shared__ float red[32];
-  pdl_trigger();
-  pdl_wait();
   constexpr int V = Elem<T>::kVec;
   const int v = blockIdx.x, seg = blockIdx.y;
+  const int vd = a.d / V;
+  const int tid = threadIdx.x;
+  // the gains are weights, independent of the kernels before: read them first
+  uint4 g[kInputVecs];
+  if (seg < 3) {
+    const uint4* gam = static_cast<const uint4*>(a.gamma_stream) + static_cast<size_t>(seg) * vd;
+#pragma unroll
+    for (int c = 0; c < kInputVecs; ++c) {
+      const int i = tid + c * 128;
+      if (i < vd) g[c] = gam[i];
+    }
+  }
+  pdl_trigger();
+  pdl_wait();
   const int nv = min(max(*a.n_valid, 0), a.T_out);
   if (v >= nv) return;
   const int o = a.valid_rows[v];
   if (o < 0 || o >= a.T_out) {
-    if (threadIdx.x == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
+    if (tid == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
     return;
   }
-  const int vd = a.d / V;
   uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.A) + static_cast<size_t>(v) * 4 * a.d +
                                         static_cast<size_t>(seg) * a.d);
   if (seg == 3) {
@@ -334,12 +349,12 @@ __global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
     } else {
       int t = a.tok[o];
       if (t < 0 || t >= a.vocab) {
-        if (threadIdx.x == 0) set_status(a.status, PE_ST_TOKEN_RANGE);
+        if (tid == 0) set_status(a.status, PE_ST_TOKEN_RANGE);
         t = 0;
       }
       src = static_cast<const uint4*>(a.emb) + static_cast<size_t>(t) * vd;
     }
-    for (int i = threadIdx.x; i < vd; i += blockDim.x) out[i] = src[i];
+    for (int i = tid; i < vd; i += blockDim.x) out[i] = src[i];
     return;
   }
   const int hsrc = a.hidden_src[o];
@@ -349,11 +364,29 @@ __global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
   } else if (hsrc < a.T_in) {
     src = static_cast<const uint4*>(a.H_tgt) + (static_cast<size_t>(hsrc) * 3 + seg) * vd;
   } else {
-    if (threadIdx.x == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
+    if (tid == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
     src = static_cast<const uint4*>(a.h_shared);
   }
+  // the row's vectors i = tid, tid + 128, ...: the first kInputVecs stay in
+  // registers (all loads in flight together), in the same summation order as a
+  // plain loop over i
+  uint4 x[kInputVecs];
+#pragma unroll
+  for (int c = 0; c < kInputVecs; ++c) {
+    const int i = tid + c * 128;
+    if (i < vd) x[c] = src[i];
+  }
   float ss = 0.f;
-  for (int i = threadIdx.x; i < vd; i += blockDim.x) {
+#pragma unroll
+  for (int c = 0; c < kInputVecs; ++c) {
+    if (tid + c * 128 < vd) {
+      float f[V];
+      unpack16<T>(x[c], f);
+#pragma unroll
+      for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
+    }
+  }
+  for (int i = tid + kInputVecs * 128; i < vd; i += 128) {
     float f[V];
     unpack16<T>(src[i], f);
 #pragma unroll
@@ -361,13 +394,25 @@ __global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
   }
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / static_cast<float>(a.d) + a.eps);
-  const uint4* gam = static_cast<const uint4*>(a.gamma_stream) + static_cast<size_t>(seg) * vd;
-  for (int i = threadIdx.x; i < vd; i += blockDim.x) {
-    float f[V], g[V];
-    unpack16<T>(src[i], f);
-    unpack16<T>(gam[i], g);
 #pragma unroll
-    for (int k = 0; k < V; ++k) f[k] = f[k] * inv * g[k];
+  for (int c = 0; c < kInputVecs; ++c) {
+    const int i = tid + c * 128;
+    if (i < vd) {
+      float f[V], gf[V];
+      unpack16<T>(x[c], f);
+      unpack16<T>(g[c], gf);
+#pragma unroll
+      for (int k = 0; k < V; ++k) f[k] = f[k] * inv * gf[k];
+      out[i] = pack16<T>(f);
+    }
+  }
+  const uint4* gam = static_cast<const uint4*>(a.gamma_stream) + static_cast<size_t>(seg) * vd;
+  for (int i = tid + kInputVecs * 128; i < vd; i += 128) {
+    float f[V], gf[V];
+    unpack16<T>(src[i], f);
+    unpack16<T>(gam[i], gf);
+#pragma unroll
+    for (int k = 0; k < V; ++k) f[k] = f[k] * inv * gf[k];
     out[i] = pack16<T>(f);
   }
 }
