@@ -93,3 +93,28 @@ def test_preparation_only_handle_refuses_layer_calls():
     torch.cuda.synchronize()
     st, _ = r.status()
     assert st == 0
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_metadata_random_batches(seed):
+    """Random ragged batches (1-40 requests, K 1-9, 1..K+3 verify rows each,
+    contexts 0-300 across block boundaries, block sizes 1, 4 and 16): every
+    metadata tensor bit-exact against the oracle, A within one bf16 step."""
+    torch = cuda_or_skip()
+    g = np.random.default_rng(1000 + seed)
+    B = int(g.integers(1, 41))
+    K = int(g.integers(1, 10))
+    n_prev = tuple(int(x) for x in g.integers(1, K + 4, size=B))
+    ctx = tuple(int(x) for x in g.integers(0, 301, size=B))
+    bs = int(g.choice([1, 4, 16]))
+    wl, b, w, kc, vc, r = setup("tiny_fp32", want_logits=False, kv=False, batch=B, n_prev=n_prev,
+                                ctx=ctx, K=K, block_size=bs, seed=seed, has_drafter=False)
+    r.prepare()
+    torch.cuda.synchronize()
+    st, _ = r.status()
+    assert st == 0, hex(st)
+    meta, G, E, A = O.prepare_inputs(wl.dims, w, b)
+    check_meta(r, meta)
+    nv = meta["n_valid"]
+    np.testing.assert_allclose(f64(host(r.A)[:nv], "f32"), A[meta["valid_rows"][:nv]], rtol=2e-6,
+                               atol=1e-7)
