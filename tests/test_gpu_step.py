@@ -102,3 +102,33 @@ def test_step_is_repeatable_and_graph_capturable():
     torch.cuda.synchronize()
     np.testing.assert_array_equal(host(r.logits), first)
     assert r.status()[0] == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_steps(seed):
+    """Random small steps (bf16, d=320, hd 64): batch 1-24, K 1-8, ragged verify
+    rows, contexts 0-600, pre- or post-norm, with or without sinks, one or two
+    layers: metadata bit-exact, z and logits within the step's tolerances."""
+    torch = cuda_or_skip()
+    g = np.random.default_rng(500 + seed)
+    B = int(g.integers(1, 25))
+    K = int(g.integers(1, 9))
+    layers = int(g.integers(1, 3))
+    top = K + 1 if layers > 1 else K + 3   # several layers: steady-state rows
+    over = dict(batch=B, K=K, n_layers=layers, seed=seed,
+                n_prev=tuple(int(x) for x in g.integers(1, top + 1, size=B)),
+                ctx=tuple(int(x) for x in g.integers(0, 601, size=B)),
+                post_norm=bool(g.integers(0, 2)), sinks=bool(g.integers(0, 2)))
+    wl, b, w, kc, vc, r = setup("small_prenorm", **over)
+    r.run()
+    torch.cuda.synchronize()
+    st, _ = r.status()
+    assert st == 0, hex(st)
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    check_meta(r, res["meta"])
+    z = f64(host(r.z), "bf16")
+    logits, draft = host(r.logits), host(r.draft)
+    for rr, out in res["req"].items():
+        sl = slice(rr * K, (rr + 1) * K)
+        assert np.abs(z[sl] - out["z"]).max() <= 0.05
+        check_logits_and_draft("bf16", logits[sl], draft[sl], out["logits"], where=f"request {rr}")
