@@ -49,6 +49,8 @@ NAME_INDEX = {
     "verify_logits": 14,
     "verify_plan": 15,
     "attn_sink": 16,
+    "cod_spans": 17,
+    "cod_draws": 18,
 }
 
 
@@ -466,3 +468,94 @@ def make_verify_batch(wl: VerifyWorkload) -> dict:
     out = f32_to_bf16_bits(logits) if wl.dtype == "bf16" else logits
     return dict(qsl=qsl, tok=tok, logits=out, planted_target=target,
                 planted_accepted=accepted, T_in=T_in, B=B, V=V)
+
+
+# ---------------------------------------------------------------------------
+# COD training indices ("[RFC]: Add random anchor for p-eagle first position")
+
+
+@dataclasses.dataclass(frozen=True)
+class CodWorkload:
+    """A batch of training sequences for the COD index and mask generator.
+
+    Each sequence alternates spans with loss_mask 0 (prompt turns) and 1
+    (response turns), so a large share of positions carries no loss, as the
+    page's motivation says.  n_depth COD depths (depth 0 = every anchor),
+    retain = the share of a depth's chains that reach the next (the page's
+    "drop rate"), max_anchors = cap on depth-0 anchors (0 = no cap)."""
+
+    name: str
+    batch: int
+    seq_len: object          # int or tuple of per-sequence lengths
+    s_max: int               # row stride of the per-sequence arrays
+    n_depth: int
+    retain: float
+    max_anchors: int
+    prompt_span: tuple = (64, 512)
+    response_span: tuple = (128, 1024)
+    seed: int = 0
+    description: str = ""
+
+    def lens(self):
+        if isinstance(self.seq_len, int):
+            return [self.seq_len] * self.batch
+        assert len(self.seq_len) == self.batch
+        return list(self.seq_len)
+
+
+COD_WORKLOADS = {
+    # the page's 8K runs: max_anchors = 1024, drop rate 0.5, depths d0..d7
+    "cod_s8192_a1024": CodWorkload(
+        name="cod_s8192_a1024", batch=16, seq_len=8192, s_max=8192, n_depth=8, retain=0.5,
+        max_anchors=1024,
+        description="COD indices + asymmetric mask, 16 sequences x 8192, max_anchors 1024, "
+                    "retain 0.5, 8 depths"),
+    # the uncapped baseline of the page's 4K runs: every loss position is an anchor
+    "cod_s4096_nocap": CodWorkload(
+        name="cod_s4096_nocap", batch=8, seq_len=4096, s_max=4096, n_depth=5, retain=0.7,
+        max_anchors=0,
+        description="COD indices + asymmetric mask, 8 sequences x 4096, no anchor cap, "
+                    "retain 0.7, 5 depths"),
+    # small ragged cases: an empty sequence, a one-token one, lengths off every tile
+    "cod_small": CodWorkload(
+        name="cod_small", batch=6, seq_len=(3001, 0, 1, 777, 2048, 1500), s_max=3072, n_depth=8,
+        retain=0.5, max_anchors=256, prompt_span=(16, 200), response_span=(32, 400),
+        description="small ragged COD batch, max_anchors 256, retain 0.5, 8 depths"),
+    "cod_tiny": CodWorkload(
+        name="cod_tiny", batch=4, seq_len=(37, 64, 5, 50), s_max=64, n_depth=4, retain=0.7,
+        max_anchors=8, prompt_span=(2, 9), response_span=(3, 12),
+        description="tiny COD batch, max_anchors 8, retain 0.7, 4 depths"),
+}
+
+
+def get_cod(name: str, **overrides) -> CodWorkload:
+    wl = COD_WORKLOADS[name]
+    return dataclasses.replace(wl, **overrides) if overrides else wl
+
+
+def make_cod_batch(wl: CodWorkload) -> dict:
+    """Host arrays of one COD batch.
+
+    loss_mask[B][s_max] u8: per sequence, spans alternate prompt (0) and response
+    (1), lengths uniform in prompt_span / response_span, starting with a prompt
+    span; positions past the sequence's length are 0.  u_anchor[B][s_max] and
+    u_keep[B][n_depth-1][s_max]: float32 uniform in [0, 1) (the method's random
+    draws).  seq_len[B] i32."""
+    B, S, D = wl.batch, wl.s_max, wl.n_depth
+    lens = np.array(wl.lens(), dtype=np.int32)
+    assert lens.max(initial=0) <= S
+    g = _seq(wl.seed, "cod_spans", 0)
+    loss_mask = np.zeros((B, S), dtype=np.uint8)
+    for b in range(B):
+        pos, on = 0, 0
+        while pos < lens[b]:
+            lo, hi = wl.response_span if on else wl.prompt_span
+            n = int(g.integers(lo, hi + 1))
+            loss_mask[b, pos:min(pos + n, lens[b])] = on
+            pos += n
+            on ^= 1
+    d = _seq(wl.seed, "cod_draws", 0)
+    u_anchor = d.random((B, S), dtype=np.float32)
+    u_keep = d.random((B, max(D - 1, 0), S), dtype=np.float32)
+    return dict(seq_len=lens, loss_mask=loss_mask, u_anchor=u_anchor, u_keep=u_keep,
+                B=B, S_max=S, n_depth=D, retain=wl.retain, max_anchors=wl.max_anchors)
