@@ -81,7 +81,9 @@ def cod_sizes(levels, L):
 
 def cod_rows(levels):
     """(anchor, depth) of each query row, depth-major."""
-    a = np.concatenate([x for x in levels]) if levels else np.zeros(0, np.int64)
+    if not levels:  # one depth only: no deeper tokens
+        return np.zeros(0, np.int64), np.zeros(0, np.int64)
+    a = np.concatenate(levels)
     k = np.concatenate([np.full(len(x), d, np.int64) for d, x in enumerate(levels)])
     return a.astype(np.int64), k
 

@@ -209,3 +209,12 @@ def test_workload_batches_are_seeded_and_shaped():
         for r, L in enumerate(b["seq_len"]):
             assert not b["loss_mask"][r, L:].any()
         assert (b["u_anchor"] >= 0).all() and (b["u_anchor"] < 1).all()
+
+
+def test_one_depth_mask_is_causal_over_the_anchors():
+    # D = 1: no deeper tokens, so the keys are the sequence and row a sees 0..a
+    lm = np.array([0, 1, 1, 0, 1], np.uint8)
+    lv = C.cod_sample_indices(lm, 1, 0.5, 0, np.zeros(5, np.float32), [])
+    m = C.cod_mask(lv, 5)
+    assert m.shape == (3, 5)
+    np.testing.assert_array_equal(m, [[1, 1, 0, 0, 0], [1, 1, 1, 0, 0], [1, 1, 1, 1, 1]])
