@@ -674,11 +674,200 @@ def run_verify(args, rank, world, local):
         torch.distributed.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- COD training indices
+
+
+COD_METRIC = "COD index lists + asymmetric mask per batch (us); HBM GB/s %peak of the mask write"
+
+
+def cod_oracle_sample(wl, b, budget_s):
+    """Time the oracle's index lists and dense mask (as they stand), one sequence
+    at a time, until the budget is spent; scale to the whole batch.  Returns
+    (us per batch, sample text, threads)."""
+    from oracle import pe_cod as C
+
+    t0 = time.perf_counter()
+    done = 0
+    while done < b["B"]:
+        L = int(b["seq_len"][done])
+        lv = C.cod_sample_indices(b["loss_mask"][done, :L], b["n_depth"], b["retain"],
+                                  b["max_anchors"], b["u_anchor"][done, :L], b["u_keep"][done, :, :L])
+        C.cod_mask(lv, L)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sample = f"{done} of {b['B']} sequences of {wl.name}, {dt:.1f} s, scaled to the batch"
+    return dt / done * b["B"] * 1e6, sample, 1
+
+
+def run_cod(args, rank, world, local):
+    """pe_cod_sample_indices + pe_cod_mask over one seeded batch of sequences per
+    rank.  L2 is flushed before every timed call; the whole pair is one graph, and
+    the mask call alone is a second graph, timed in its own loop for the
+    roofline line."""
+    import torch
+
+    from speculative_drafting_gb300 import build, runner
+
+    wl = W.get_cod(args.workload)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        b = W.make_cod_batch(wl)
+        per, sample, threads = [], "", 1
+        t_all = time.perf_counter()
+        for _ in range(max(1, args.steps)):
+            us, sample, threads = cod_oracle_sample(wl, b, budget_s=5.0)
+            per.append(us)
+            if time.perf_counter() - t_all > 150:
+                break
+        us = statistics.median(per)
+        print(json.dumps({
+            "impl": "reference", "metric": COD_METRIC, "value": us, "unit": "us",
+            "n_gpus": args.gpus, "steps": len(per), "warmup": 0, "ms_per_step": us / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic", "config": {"workload": wl.name, "global_batch": wl.batch,
+                                            "description": wl.description},
+            "cpu_baseline": {"value": us, "unit": "us", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    b = W.make_cod_batch(rank_workload(wl, rank))
+    r = runner.CodRunner(b)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            r.run(stream=stream)
+    stream.synchronize()
+    st, _ = r.status()
+    if st:
+        raise RuntimeError(f"device status {st:#x} on the COD batch")
+    g_all, g_mask = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=stream):
+        r.run(stream=stream)
+    with torch.cuda.graph(g_mask, stream=stream):
+        r.build_mask(stream=stream)
+
+    def flush_l2():
+        flush.zero_()
+        flush.max()
+
+    def timed(graph, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                flush_l2()
+                ev[i][0].record(stream)
+                graph.replay()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            flush_l2()
+            g_all.replay()
+    stream.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    call_ms = timed(g_all, args.steps)
+    mask_ms = timed(g_mask, args.steps)
+    clk = clocks.stop()
+    call_ms = max_over_ranks(call_ms, world, "cuda")
+    # end to end: pinned host inputs in, the lists, counts and masks out
+    h_in = {k: torch.from_numpy(np.ascontiguousarray(b[k])).pin_memory()
+            for k in ("seq_len", "loss_mask", "u_anchor", "u_keep")}
+    counts = r.counts.cpu().numpy()
+    lens = np.clip(b["seq_len"], 0, b["S_max"])
+    Q = counts.sum(1)
+    KV = lens + Q - counts[:, 0]
+    width = (KV + 15) // 16 * 16
+    h_mask = torch.empty(r.mask.numel(), dtype=torch.uint8).pin_memory()
+    h_idx = torch.empty(r.idx.shape, dtype=torch.int32).pin_memory()
+    h_cnt = torch.empty(r.counts.shape, dtype=torch.int32).pin_memory()
+    n_e2e = max(3, args.steps // 8)
+    with torch.cuda.stream(stream):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            for k, t in h_in.items():
+                r.inp[k].copy_(t, non_blocking=True)
+            g_all.replay()
+            h_idx.copy_(r.idx, non_blocking=True)
+            h_cnt.copy_(r.counts, non_blocking=True)
+            # each sequence's written rows (Q_b rows of its block)
+            for s in range(r.B):
+                nb = int(Q[s]) * r.ld
+                if nb:
+                    lo = s * r.mask_stride
+                    h_mask[lo:lo + nb].copy_(r.mask[lo:lo + nb], non_blocking=True)
+        a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / n_e2e
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h_mask = int((Q * r.ld).sum())
+    d2h = d2h_mask + h_idx.numel() * 4 + h_cnt.numel() * 4
+    if rank == 0:
+        peaks, src = measured_peaks()
+        mask_bytes = int((Q * width).sum())
+        # the mask kernel also reads each row's anchor and its chain places
+        alg = mask_bytes + int(Q.sum()) * 4 + int((counts[:, 1:].sum(1)).sum()) * 4
+        achieved = alg / (mask_ms / 1e3) / 1e9
+        cpu = None
+        if not args.no_cpu_baseline:
+            us, sample, threads = cod_oracle_sample(wl, b, budget_s=10.0)
+            cpu = {"value": us, "unit": "us", "cores": threads, "kind": "oracle", "sample": sample}
+        print(json.dumps({
+            "metric": COD_METRIC, "value": call_ms * 1e3, "unit": "us", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": call_ms,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "global_batch": r.B * world, "seq_len": r.S,
+                       "n_depth": r.D, "retain": r.retain, "max_anchors": r.max_anchors,
+                       "mask_rows": int(Q.sum()), "mask_bytes": mask_bytes,
+                       "description": wl.description, "cuda_graph": True,
+                       "l2": "flushed before every timed call (256 MB write, then a 256 MB "
+                             "read, so no dirty line is written back inside the call)",
+                       "parallelism": f"replica x{world} (independent batches per GPU)"},
+            "clocks": clk,
+            "e2e": {"value": e2e_ms * 1e3, "unit": "us", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps,
+            "roofline": {"kernel": "cod_mask_kernel", "bound": "hbm", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(wl.name),
+                         "peak_source": src, "algorithmic_bytes": alg,
+                         "avg_launch_us": mask_ms * 1e3},
+            "index_kernel_us": (call_ms - mask_ms) * 1e3,
+            "cpu_baseline": cpu}), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.workload in W.VERIFY_WORKLOADS:
         run_verify(args, rank, world, local)
+        return
+    if args.workload in W.COD_WORKLOADS:
+        run_cod(args, rank, world, local)
         return
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -24,6 +24,10 @@
  *   pe_argmax          the LM head fused with a per-row greedy argmax.
  *   pe_verify_greedy   the target's greedy verification of the drafts, which
  *                      yields the next step's accepted counts and bonus tokens.
+ *   pe_cod_sample_indices, pe_cod_mask
+ *                      the training side's COD index lists and asymmetric
+ *                      attention mask ("[RFC]: Add random anchor for p-eagle
+ *                      first position").
  *
  * Conventions for every call
  *   - All tensor arguments are DEVICE pointers owned by the caller; the library
@@ -82,6 +86,12 @@ extern "C" {
                                      several layers: a request has more
                                      non-rejected rows than the layers carry */
 #define PE_ST_TIMEOUT 0x10u       /* a bounded wait inside a kernel expired */
+#define PE_ST_CAPACITY 0x20u      /* COD calls: a sequence length outside [0, S_max]
+                                     (clamped), a mask larger than its row capacity
+                                     or row stride (rows / columns past it are not
+                                     written), or index lists the mask call cannot
+                                     have been given by pe_cod_sample_indices
+                                     (those rows are skipped) */
 
 /* padding slot of rejected rows ("KV cache and CUDA graphs") */
 #define PE_PADDING_SLOT_ID (-1)
@@ -305,6 +315,75 @@ int pe_verify_greedy(int B, int T_in, const int32_t* qsl, const int32_t* tok,
                      const void* logits, int vocab, int dtype, int32_t* target_tok,
                      int32_t* accepted, int32_t* bonus, void* ws, size_t ws_bytes,
                      void* stream);
+
+/* ---------------------------------------------------------------- COD training indices
+ * "[RFC]: Add random anchor for p-eagle first position": the training-side
+ * index lists of COD sampling and the asymmetric attention mask built on them.
+ * For a batch of B sequences (sequence b has seq_len[b] <= S_max tokens; every
+ * per-sequence array has row stride S_max):
+ *   depth 0 (anchors)  the positions with loss_mask != 0; when max_anchors > 0
+ *                      and there are more of them, the max_anchors with the
+ *                      smallest (u_anchor, position) keys, i.e. a uniform random
+ *                      subset for uniform draws
+ *   depth k (1..D-1)   the anchors of depth k-1 with u_keep[k-1][a] < retain
+ *                      and a + k < seq_len (each chain continues on its own
+ *                      draw; the page's "drop rate" is this retained share)
+ * Query rows of the mask: the COD tokens, depth-major (depth 0's anchors, then
+ * depth 1's, ...), anchors ascending within a depth; row (a, k) stands at
+ * position a + k.  Key columns: the seq_len original positions, then the depth
+ * >= 1 tokens in the same order.  Row (a, k) may attend original position j iff
+ * j <= a, and chain token (a', k') iff a' == a and k' <= k (the reply's "Depth >
+ * 0 attention": the original sequence up to the anchor plus its own chain).
+ * Sizes: Q = sum_k counts[k] rows, KV = seq_len + Q - counts[0] columns.
+ *
+ * The random draws are inputs: float in [0, 1) (negative or NaN draws are
+ * outside the contract).  Both calls are asynchronous on `stream` and capturable. */
+#define PE_COD_MAX_DEPTH 16
+
+/* Workspace for both COD calls: 256 + B * (n_depth - 1) * S_max * 4 bytes (the
+ * status word, then each chain member's place in its depth's list, which
+ * pe_cod_sample_indices writes and pe_cod_mask reads).  0 for invalid sizes. */
+size_t pe_cod_workspace_bytes(int B, int S_max, int n_depth);
+
+/* COD index lists.
+ *   seq_len[B]            int32 sequence lengths (outside [0, S_max]: clamped,
+ *                         PE_ST_CAPACITY)
+ *   loss_mask[B][S_max]   uint8, non-zero = the position carries a loss
+ *   n_depth               D, 1..PE_COD_MAX_DEPTH
+ *   retain                share of a depth's chains kept for the next depth
+ *   max_anchors           cap on depth-0 anchors per sequence, 0 = no cap
+ *   u_anchor[B][S_max]    float draws of the anchor subset
+ *   u_keep[B][D-1][S_max] float draws of the chain continuations (NULL if D = 1)
+ *   idx[B][D][S_max]      out: idx[b][k][0..counts[b][k]) = depth k's anchor
+ *                         positions, ascending; the rest of each row is not written
+ *   counts[B][D]          out: list lengths
+ *   ws                    pe_cod_workspace_bytes(B, S_max, D) bytes or more,
+ *                         256-byte aligned; the call clears its status word
+ * PE_ERR_ARG: negative sizes, D outside 1..16, NaN retain, negative cap, null
+ * or misaligned pointers, ws too small.  PE_ERR_UNSUPPORTED: B > 65535. */
+int pe_cod_sample_indices(int B, int S_max, const int32_t* seq_len, const uint8_t* loss_mask,
+                          int n_depth, float retain, int max_anchors, const float* u_anchor,
+                          const float* u_keep, int32_t* idx, int32_t* counts, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* The asymmetric mask of each sequence, from the lists of pe_cod_sample_indices
+ * (same B, S_max, seq_len, D and ws).
+ *   mask                  uint8, sequence b's mask at mask + b * mask_stride:
+ *                         row q at + q * ld, 1 = may attend, 0 = masked.  Rows
+ *                         0..Q-1 are written, each up to the next multiple of 16
+ *                         bytes past its KV columns (the extra bytes 0); rows >= Q
+ *                         and columns beyond are left untouched.
+ *   q_cap                 rows each sequence's block holds (>= Q; D * the anchor
+ *                         count is always enough)
+ *   ld                    row stride in bytes, a multiple of 16, >= KV rounded up
+ *                         to 16 (S_max + (D-1) * anchors is always enough)
+ *   mask_stride           bytes between sequences, a multiple of 16, >= q_cap * ld
+ * A mask larger than q_cap or ld sets PE_ST_CAPACITY and writes what fits.  The
+ * status word is not cleared (read it after both calls).  PE_ERR_ARG: as above,
+ * plus a misaligned mask, ld or mask_stride. */
+int pe_cod_mask(int B, int S_max, const int32_t* seq_len, int n_depth, const int32_t* idx,
+                const int32_t* counts, uint8_t* mask, int64_t q_cap, int64_t ld,
+                int64_t mask_stride, void* ws, size_t ws_bytes, void* stream);
 
 /* Copy the device status word from ws into *status (synchronises `stream`);
  * clear it when `clear` is non-zero.  Returns PE_OK when no bit is set,

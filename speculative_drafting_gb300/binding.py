@@ -25,6 +25,8 @@ PE_ST_BLOCK_RANGE = 0x2
 PE_ST_TOKEN_RANGE = 0x4
 PE_ST_ROWS_RANGE = 0x8
 PE_ST_TIMEOUT = 0x10
+PE_ST_CAPACITY = 0x20
+PE_COD_MAX_DEPTH = 16
 PE_DTYPE_F32 = 0
 PE_DTYPE_BF16 = 1
 
@@ -117,6 +119,14 @@ def load(path: str | None = None):
     lib.pe_verify_greedy.argtypes = [_i32, _i32, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp,
                                      _sz, _vp]
     lib.pe_verify_greedy.restype = _i32
+    lib.pe_cod_workspace_bytes.argtypes = [_i32, _i32, _i32]
+    lib.pe_cod_workspace_bytes.restype = _sz
+    lib.pe_cod_sample_indices.argtypes = [_i32, _i32, _vp, _vp, _i32, ctypes.c_float, _i32, _vp,
+                                          _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.pe_cod_sample_indices.restype = _i32
+    lib.pe_cod_mask.argtypes = [_i32, _i32, _vp, _i32, _vp, _vp, _vp, ctypes.c_int64,
+                                ctypes.c_int64, ctypes.c_int64, _vp, _sz, _vp]
+    lib.pe_cod_mask.restype = _i32
     _lib = lib
     return lib
 
@@ -311,3 +321,38 @@ def read_status_ws(ws, clear=True, stream=None):
     if rc not in (PE_OK, PE_ERR_DEVICE_INPUT, PE_ERR_TIMEOUT):
         raise PeError(rc, "pe_read_status")
     return int(v.value), rc
+
+
+# ----------------------------------------------------------------------------- COD training indices
+
+
+def cod_workspace_bytes(B: int, S_max: int, n_depth: int) -> int:
+    n = int(load().pe_cod_workspace_bytes(int(B), int(S_max), int(n_depth)))
+    if n == 0:
+        raise PeError(PE_ERR_ARG, "pe_cod_workspace_bytes")
+    return n
+
+
+def cod_workspace(B: int, S_max: int, n_depth: int, device="cuda"):
+    """A device workspace for the two COD calls (torch allocates it 256-byte aligned)."""
+    import torch
+
+    return torch.zeros(cod_workspace_bytes(B, S_max, n_depth), dtype=torch.uint8, device=device)
+
+
+def cod_sample_indices(B, S_max, seq_len, loss_mask, n_depth, retain, max_anchors, u_anchor, u_keep,
+                       idx, counts, ws, stream=None):
+    """pe_cod_sample_indices on device tensors."""
+    rc = load().pe_cod_sample_indices(int(B), int(S_max), _ptr(seq_len), _ptr(loss_mask),
+                                      int(n_depth), float(retain), int(max_anchors), _ptr(u_anchor),
+                                      _ptr(u_keep), _ptr(idx), _ptr(counts), _ptr(ws),
+                                      int(ws.numel()), _stream(stream))
+    _check(rc, "pe_cod_sample_indices")
+
+
+def cod_mask(B, S_max, seq_len, n_depth, idx, counts, mask, q_cap, ld, mask_stride, ws, stream=None):
+    """pe_cod_mask on device tensors; mask is a uint8 buffer of B * mask_stride bytes."""
+    rc = load().pe_cod_mask(int(B), int(S_max), _ptr(seq_len), int(n_depth), _ptr(idx), _ptr(counts),
+                            _ptr(mask), int(q_cap), int(ld), int(mask_stride), _ptr(ws),
+                            int(ws.numel()), _stream(stream))
+    _check(rc, "pe_cod_mask")

@@ -1,0 +1,353 @@
+// COD training indices and the asymmetric attention mask.
+//
+// "[RFC]: Add random anchor for p-eagle first position": COD sampling starts a
+// chain at every loss position (with max_anchors, at a uniform random subset of
+// them) and keeps a share of each depth's chains for the next depth; the mask's
+// queries are the COD tokens, its keys the original sequence plus the deeper COD
+// tokens.  The reply's "Depth > 0 attention": a deeper query sees the original
+// sequence (up to its anchor), not only its own chain.
+//
+// Two kernels, chained by programmatic launch:
+//   cod_index_kernel  one CTA per sequence.  Counts the loss positions; when the
+//                     cap binds, a three-pass radix select (11 + 11 + 10 bits)
+//                     over the candidates' random keys finds the cap-th
+//                     smallest (u, position) key.  One pass over the positions,
+//                     1024 at a time, then walks each chain's draws to its depth
+//                     and writes every depth's list with one ballot and one warp
+//                     scan per depth, plus each chain member's place in its
+//                     depth's list (the mask kernel's column lookup).
+//                     Latency-bound.
+//   cod_mask_kernel   one warp per query row (anchor a, depth k): columns 0..a of
+//                     the original sequence and the row's own chain columns at
+//                     depths 1..k are 1, every other column below the row's key
+//                     count 0, written with 16-byte stores.  Bound by the mask's
+//                     bytes (HBM).
+#include "pe_common.cuh"
+#include "pe_internal.h"
+
+namespace pe {
+namespace {
+
+constexpr int kIdxThreads = 1024;
+constexpr int kIdxWarps = kIdxThreads / 32;
+constexpr int kMaskThreads = 256;
+constexpr int kMaskWarps = kMaskThreads / 32;
+constexpr int kWsHeader = 256;  // status word, then the place table
+constexpr int kMaxD = PE_COD_MAX_DEPTH;
+
+PE_DEV int warp_inclusive_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+PE_DEV int clamp_len(int L, int S_max) { return L < 0 ? 0 : (L > S_max ? S_max : L); }
+
+// place[b][k-1][a] = index of anchor a in depth k's list (k >= 1; written for
+// chain members only).  counts[b][k] = |I_k|; idx[b][k][j] = I_k[j], ascending.
+__global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
+    int S_max, const int32_t* __restrict__ seq_len, const uint8_t* __restrict__ loss_mask, int D,
+    float rho, int A, const float* __restrict__ u_anchor, const float* __restrict__ u_keep,
+    int32_t* __restrict__ idx, int32_t* __restrict__ counts, int32_t* __restrict__ place,
+    uint32_t* status) {
+  __shared__ int hist[2048];
+  __shared__ int red[kIdxWarps];
+  __shared__ int wofs[kMaxD][kIdxWarps];
+  __shared__ int base[kMaxD];
+  __shared__ int tot[kMaxD];
+  __shared__ int pick[2];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();
+  const int L_in = seq_len[b];
+  const int L = clamp_len(L_in, S_max);
+  if (L != L_in && tid == 0) set_status(status, PE_ST_CAPACITY);
+  const size_t row = static_cast<size_t>(b) * S_max;
+  const uint8_t* lm = loss_mask + row;
+  const uint32_t* ua = reinterpret_cast<const uint32_t*>(u_anchor) + row;
+  const float* uk = D > 1 ? u_keep + static_cast<size_t>(b) * (D - 1) * S_max : nullptr;
+
+  // ---- depth 0: the anchors.  With a binding cap, the cap smallest keys
+  // (u bits, position) among the loss positions; u >= 0, so the bits order as
+  // the values.
+  bool capped = false;
+  uint32_t thr = 0;
+  int need_eq = 0;  // keys equal to thr taken, lowest positions first
+  if (A > 0) {
+    int c = 0;
+    for (int i = tid; i < L; i += kIdxThreads) c += lm[i] != 0;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (lane == 0) red[warp] = c;
+    __syncthreads();
+    int n = 0;
+    for (int w = 0; w < kIdxWarps; ++w) n += red[w];
+    capped = n > A;
+    if (capped) {
+      uint32_t prefix = 0, pmask = 0;
+      int rank = A;  // 1-based rank of the wanted key among those matching prefix
+      for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = pass == 2 ? 1024 : 2048;
+        for (int j = tid; j < nb; j += kIdxThreads) hist[j] = 0;
+        __syncthreads();
+        for (int i = tid; i < L; i += kIdxThreads) {
+          if (lm[i]) {
+            const uint32_t k = ua[i];
+            if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & (nb - 1)], 1);
+          }
+        }
+        __syncthreads();
+        if (warp == 0) {
+          // lane l sums bins [l*per, (l+1)*per); the lane whose range holds the
+          // rank walks its bins
+          const int per = nb / 32;
+          int s = 0;
+          for (int j = 0; j < per; ++j) s += hist[lane * per + j];
+          const int inc = warp_inclusive_scan(s);
+          const int exc = inc - s;
+          if (exc < rank && rank <= inc) {
+            int r = rank - exc, d = lane * per;
+            const int end = d + per - 1;
+            while (d < end && hist[d] < r) {
+              r -= hist[d];
+              ++d;
+            }
+            pick[0] = d;
+            pick[1] = r;
+          }
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(pick[0]) << shift;
+        pmask |= static_cast<uint32_t>(nb - 1) << shift;
+        rank = pick[1];
+        __syncthreads();
+      }
+      thr = prefix;
+      need_eq = rank;
+    }
+  }
+
+  // ---- every depth's list, 1024 positions at a time
+  if (tid < kMaxD) base[tid] = 0;
+  __syncthreads();
+  int eq_seen = 0;  // keys equal to thr met so far (same on every thread)
+  for (int c0 = 0; c0 < L; c0 += kIdxThreads) {
+    const int i = c0 + tid;
+    const bool cand = i < L && lm[i] != 0;
+    bool sel = cand;
+    if (capped) {
+      const uint32_t k = cand ? ua[i] : 0u;
+      const bool eq = cand && k == thr;
+      const unsigned be = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) red[warp] = __popc(be);
+      __syncthreads();
+      int before = eq_seen, all = 0;
+      for (int w = 0; w < kIdxWarps; ++w) {
+        const int v = red[w];
+        before += w < warp ? v : 0;
+        all += v;
+      }
+      before += __popc(be & ((1u << lane) - 1u));
+      sel = cand && (k < thr || (eq && before < need_eq));
+      eq_seen += all;
+      __syncthreads();
+    }
+    // the chain's depth: each further depth needs its draw below rho and its
+    // position a + k inside the sequence
+    int len = 0;
+    if (sel) {
+      len = 1;
+      while (len < D && i + len < L && uk[static_cast<size_t>(len - 1) * S_max + i] < rho) ++len;
+    }
+    unsigned bal[kMaxD];
+#pragma unroll
+    for (int k = 0; k < kMaxD; ++k) {
+      bal[k] = __ballot_sync(0xffffffffu, len > k);
+      if (k < D && lane == 0) wofs[k][warp] = __popc(bal[k]);
+    }
+    __syncthreads();
+    if (warp < D) {
+      const int v = wofs[warp][lane];
+      const int inc = warp_inclusive_scan(v);
+      wofs[warp][lane] = inc - v;
+      if (lane == 31) tot[warp] = inc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kMaxD; ++k) {
+      if (k < D && len > k) {
+        const int pos = base[k] + wofs[k][warp] + __popc(bal[k] & ((1u << lane) - 1u));
+        idx[(static_cast<size_t>(b) * D + k) * S_max + pos] = i;
+        if (k > 0) place[(static_cast<size_t>(b) * (D - 1) + (k - 1)) * S_max + i] = pos;
+      }
+    }
+    __syncthreads();
+    if (tid < D) base[tid] += tot[tid];
+    __syncthreads();
+  }
+  if (tid < D) counts[b * D + tid] = base[tid];
+}
+
+// Row q of sequence b (depth-major): anchor a, depth k.  The mask row holds the
+// key columns 0..KV-1 (the L original positions, then the depth >= 1 tokens in
+// depth-major order) and is written up to the next multiple of 16 bytes.
+__global__ void __launch_bounds__(kMaskThreads) cod_mask_kernel(
+    int S_max, const int32_t* __restrict__ seq_len, int D, const int32_t* __restrict__ idx,
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ place, uint8_t* __restrict__ mask,
+    long long q_cap, long long ld, long long mstride, uint32_t* status) {
+  __shared__ int qoff[kMaxD + 1];
+  __shared__ int spc[kMaskWarps][kMaxD];
+  const int b = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_trigger();
+  pdl_wait();
+  const int L_in = seq_len[b];
+  const int L = clamp_len(L_in, S_max);
+  if (threadIdx.x == 0) {
+    uint32_t bad = L != L_in ? PE_ST_CAPACITY : 0u;
+    int s = 0;
+    for (int k = 0; k < D; ++k) {
+      int n = counts[b * D + k];
+      if (n < 0 || n > L) {
+        bad |= PE_ST_CAPACITY;
+        n = n < 0 ? 0 : L;
+      }
+      qoff[k] = s;
+      s += n;
+    }
+    qoff[D] = s;
+    if (bad && blockIdx.x == 0) set_status(status, bad);
+  }
+  __syncthreads();
+  const long long Q = qoff[D];
+  const long long n0 = qoff[1];
+  const long long KV = L + Q - n0;
+  long long rows = Q, width = (KV + 15) / 16 * 16;
+  if (rows > q_cap || width > ld) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, PE_ST_CAPACITY);
+    rows = rows < q_cap ? rows : q_cap;
+    width = width < ld ? width : ld;
+  }
+  uint8_t* mb = mask + static_cast<long long>(b) * mstride;
+  const int32_t* ib = idx + static_cast<size_t>(b) * D * S_max;
+  const int32_t* pb = D > 1 ? place + static_cast<size_t>(b) * (D - 1) * S_max : nullptr;
+  const long long nvec = width / 16;
+  for (long long q = static_cast<long long>(blockIdx.x) * kMaskWarps + warp; q < rows;
+       q += static_cast<long long>(gridDim.x) * kMaskWarps) {
+    int k = 0;
+    while (k + 1 < D && qoff[k + 1] <= q) ++k;
+    const int a = ib[static_cast<size_t>(k) * S_max + (q - qoff[k])];
+    if (a < 0 || a >= L) {  // not a list this kernel's sibling wrote
+      if (lane == 0) set_status(status, PE_ST_CAPACITY);
+      continue;
+    }
+    // the row's own chain token at depth j (1..k) is key column
+    // L + (qoff[j] - n0) + its place in depth j's list
+    if (lane >= 1 && lane <= k) {
+      const int p = pb[static_cast<size_t>(lane - 1) * S_max + a];
+      const bool ok = p >= 0 && p < qoff[lane + 1] - qoff[lane];
+      if (!ok) set_status(status, PE_ST_CAPACITY);
+      spc[warp][lane] = ok ? static_cast<int>(L + (qoff[lane] - n0) + p) : -1;
+    }
+    __syncwarp();
+    uint8_t* rowp = mb + q * ld;
+    for (long long v = lane; v < nvec; v += 32) {
+      const long long c0 = v * 16;
+      uint32_t w[4];
+      if (c0 + 15 <= a) {
+        w[0] = w[1] = w[2] = w[3] = 0x01010101u;
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t x = 0;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (c0 + 4 * h + t <= a) x |= 1u << (8 * t);
+          w[h] = x;
+        }
+        if (c0 + 16 > L) {
+          for (int j = 1; j <= k; ++j) {
+            const long long s = spc[warp][j] - c0;
+            if (s >= 0 && s < 16) w[s >> 2] |= 1u << (8 * (s & 3));
+          }
+        }
+      }
+      *reinterpret_cast<uint4*>(rowp + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+}  // namespace pe
+
+using namespace pe;
+
+extern "C" size_t pe_cod_workspace_bytes(int B, int S_max, int n_depth) {
+  if (B < 0 || S_max < 0 || n_depth < 1 || n_depth > PE_COD_MAX_DEPTH) return 0;
+  return static_cast<size_t>(kWsHeader) +
+         static_cast<size_t>(B) * static_cast<size_t>(n_depth - 1) * static_cast<size_t>(S_max) *
+             sizeof(int32_t);
+}
+
+static int cod_common_args(int B, int S_max, int n_depth, const void* seq_len, void* ws,
+                           size_t ws_bytes) {
+  if (B < 0 || S_max < 0 || n_depth < 1 || n_depth > PE_COD_MAX_DEPTH) return PE_ERR_ARG;
+  if (B > 65535) return PE_ERR_UNSUPPORTED;
+  if (!ws || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return PE_ERR_ARG;
+  if (ws_bytes < pe_cod_workspace_bytes(B, S_max, n_depth)) return PE_ERR_ARG;
+  if (B > 0 && !seq_len) return PE_ERR_ARG;
+  return PE_OK;
+}
+
+extern "C" int pe_cod_sample_indices(int B, int S_max, const int32_t* seq_len,
+                                     const uint8_t* loss_mask, int n_depth, float retain,
+                                     int max_anchors, const float* u_anchor, const float* u_keep,
+                                     int32_t* idx, int32_t* counts, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  NvtxRange nvtx("pe_cod_sample_indices");
+  const int e = cod_common_args(B, S_max, n_depth, seq_len, ws, ws_bytes);
+  if (e != PE_OK) return e;
+  if (!(retain == retain) || max_anchors < 0) return PE_ERR_ARG;
+  if (B > 0 && (!counts || (S_max > 0 && (!loss_mask || !u_anchor || !idx ||
+                                          (n_depth > 1 && !u_keep)))))
+    return PE_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(u_anchor) % 4 != 0 || reinterpret_cast<uintptr_t>(u_keep) % 4 != 0)
+    return PE_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* status = static_cast<uint32_t*>(ws);
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return PE_ERR_CUDA;
+  if (B == 0) return PE_OK;
+  int32_t* place = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kWsHeader);
+  return launch_pdl(cod_index_kernel, dim3(B), dim3(kIdxThreads), 0, st, S_max, seq_len,
+                    loss_mask, n_depth, retain, max_anchors, u_anchor, u_keep, idx, counts, place,
+                    status) == cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
+}
+
+extern "C" int pe_cod_mask(int B, int S_max, const int32_t* seq_len, int n_depth,
+                           const int32_t* idx, const int32_t* counts, uint8_t* mask, int64_t q_cap,
+                           int64_t ld, int64_t mask_stride, void* ws, size_t ws_bytes,
+                           void* stream) {
+  NvtxRange nvtx("pe_cod_mask");
+  const int e = cod_common_args(B, S_max, n_depth, seq_len, ws, ws_bytes);
+  if (e != PE_OK) return e;
+  if (q_cap < 0 || ld < 16 || ld % 16 != 0 || mask_stride % 16 != 0) return PE_ERR_ARG;
+  if (q_cap > INT64_MAX / ld || (q_cap > 0 && mask_stride < q_cap * ld)) return PE_ERR_ARG;
+  if (B > 0 && (!counts || !idx || !mask)) return PE_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(mask) % 16 != 0) return PE_ERR_ARG;
+  if (B == 0 || q_cap == 0) return PE_OK;
+  const int sms = num_sms_of_current_device();
+  const int gx = (4 * sms + B - 1) / B;
+  const int32_t* place = reinterpret_cast<const int32_t*>(static_cast<const char*>(ws) + kWsHeader);
+  return launch_pdl(cod_mask_kernel, dim3(gx < 1 ? 1 : gx, B), dim3(kMaskThreads), 0,
+                    static_cast<cudaStream_t>(stream), S_max, seq_len, n_depth, idx, counts, place,
+                    mask, static_cast<long long>(q_cap), static_cast<long long>(ld),
+                    static_cast<long long>(mask_stride), static_cast<uint32_t*>(ws)) == cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
+}

@@ -93,3 +93,55 @@ class StepRunner:
 
     def status(self, clear=True):
         return self.drafter.read_status(self.ws, clear=clear)
+
+
+def cod_capacity(S_max: int, n_depth: int, max_anchors: int):
+    """(q_cap, ld) that hold any COD mask of a sequence of at most S_max tokens:
+    at most n_depth * anchors rows and S_max + (n_depth - 1) * anchors columns,
+    anchors = max_anchors (or S_max without a cap)."""
+    anchors = min(max_anchors, S_max) if max_anchors > 0 else S_max
+    q_cap = max(1, n_depth * anchors)
+    ld = max(16, (S_max + (n_depth - 1) * anchors + 15) // 16 * 16)
+    return q_cap, ld
+
+
+class CodRunner:
+    """One COD batch resident on the device: the index call, then the mask call."""
+
+    def __init__(self, batch: dict, device="cuda", q_cap=None, ld=None, guard=0):
+        import torch
+
+        self.B, self.S, self.D = int(batch["B"]), int(batch["S_max"]), int(batch["n_depth"])
+        self.retain, self.max_anchors = float(batch["retain"]), int(batch["max_anchors"])
+        self.inp = {k: torch.from_numpy(np.ascontiguousarray(batch[k])).to(device)
+                    for k in ("seq_len", "loss_mask", "u_anchor", "u_keep")}
+        cq, cl = cod_capacity(self.S, self.D, self.max_anchors)
+        self.q_cap = cq if q_cap is None else int(q_cap)
+        self.ld = cl if ld is None else int(ld)
+        self.mask_stride = self.q_cap * self.ld
+        self.idx = torch.full((self.B, self.D, self.S), -1, dtype=torch.int32, device=device)
+        self.counts = torch.full((self.B, self.D), -1, dtype=torch.int32, device=device)
+        # `guard` extra bytes after the last sequence's block (tests check them)
+        self.mask = torch.zeros(self.B * self.mask_stride + guard, dtype=torch.uint8, device=device)
+        self.ws = binding.cod_workspace(self.B, self.S, self.D, device)
+
+    def sample(self, stream=None):
+        i = self.inp
+        binding.cod_sample_indices(self.B, self.S, i["seq_len"], i["loss_mask"], self.D, self.retain,
+                                   self.max_anchors, i["u_anchor"], i["u_keep"] if self.D > 1 else None,
+                                   self.idx, self.counts, self.ws, stream=stream)
+
+    def build_mask(self, stream=None):
+        binding.cod_mask(self.B, self.S, self.inp["seq_len"], self.D, self.idx, self.counts, self.mask,
+                         self.q_cap, self.ld, self.mask_stride, self.ws, stream=stream)
+
+    def run(self, stream=None):
+        self.sample(stream)
+        self.build_mask(stream)
+
+    def status(self, clear=True):
+        return binding.read_status_ws(self.ws, clear=clear)
+
+    def mask_of(self, b):
+        """Sequence b's mask block as a [q_cap][ld] uint8 view."""
+        return self.mask[b * self.mask_stride:(b + 1) * self.mask_stride].view(self.q_cap, self.ld)

@@ -92,3 +92,33 @@ def test_struct_layouts_match_the_header(tmp_path):
     got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     assert got == [ctypes.sizeof(binding.PeDims), ctypes.sizeof(binding.PeWeights),
                    ctypes.sizeof(binding.PeLayerWeights), ctypes.sizeof(binding.PeMeta)]
+
+
+def test_cod_host_checks(lib):
+    # 256-byte header, then one int32 place per (sequence, depth >= 1, position)
+    assert lib.pe_cod_workspace_bytes(16, 8192, 8) == 256 + 16 * 7 * 8192 * 4
+    assert lib.pe_cod_workspace_bytes(4, 100, 1) == 256
+    for bad in ((-1, 10, 2), (1, -1, 2), (1, 10, 0), (1, 10, binding.PE_COD_MAX_DEPTH + 1)):
+        assert lib.pe_cod_workspace_bytes(*bad) == 0
+    # fake, never dereferenced addresses: every case fails on the host
+    ws, p = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 21)
+    big = 1 << 30
+    sample = lib.pe_cod_sample_indices
+    assert sample(1, 10, p, p, 0, 0.5, 0, p, p, p, p, ws, big, None) == binding.PE_ERR_ARG    # D = 0
+    assert sample(1, 10, p, p, 17, 0.5, 0, p, p, p, p, ws, big, None) == binding.PE_ERR_ARG   # D > 16
+    assert sample(1, 10, p, p, 4, float("nan"), 0, p, p, p, p, ws, big, None) == binding.PE_ERR_ARG
+    assert sample(1, 10, p, p, 4, 0.5, -1, p, p, p, p, ws, big, None) == binding.PE_ERR_ARG  # cap < 0
+    assert sample(1, 10, p, p, 4, 0.5, 0, p, None, p, p, ws, big, None) == binding.PE_ERR_ARG  # no u_keep
+    assert sample(1, 10, p, p, 4, 0.5, 0, p, p, p, p, None, big, None) == binding.PE_ERR_ARG   # no ws
+    assert sample(1, 10, p, p, 4, 0.5, 0, p, p, p, p, ctypes.c_void_p((1 << 20) + 16), big, None) == \
+        binding.PE_ERR_ARG                                                                     # ws misaligned
+    assert sample(2, 10, p, p, 4, 0.5, 0, p, p, p, p, ws, 256, None) == binding.PE_ERR_ARG     # ws too small
+    assert sample(70000, 1, p, p, 1, 0.5, 0, p, p, p, p, ws, big, None) == binding.PE_ERR_UNSUPPORTED
+    mask = lib.pe_cod_mask
+    assert mask(1, 10, p, 4, p, p, p, 8, 15, 1 << 12, ws, big, None) == binding.PE_ERR_ARG     # ld % 16
+    assert mask(1, 10, p, 4, p, p, p, 8, 0, 1 << 12, ws, big, None) == binding.PE_ERR_ARG      # ld = 0
+    assert mask(1, 10, p, 4, p, p, p, 8, 32, 200, ws, big, None) == binding.PE_ERR_ARG         # stride < q_cap * ld
+    assert mask(1, 10, p, 4, p, p, p, 8, 32, 264, ws, big, None) == binding.PE_ERR_ARG         # stride % 16
+    assert mask(1, 10, p, 4, p, p, ctypes.c_void_p((1 << 21) + 8), 8, 32, 256, ws, big, None) == \
+        binding.PE_ERR_ARG                                                                     # mask misaligned
+    assert mask(1, 10, p, 4, p, p, p, 1 << 62, 32, 1 << 12, ws, big, None) == binding.PE_ERR_ARG  # overflow
