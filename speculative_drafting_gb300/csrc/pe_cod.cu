@@ -49,6 +49,8 @@ PE_DEV int clamp_len(int L, int S_max) { return L < 0 ? 0 : (L > S_max ? S_max :
 
 // place[b][k-1][a] = index of anchor a in depth k's list (k >= 1; written for
 // chain members only).  counts[b][k] = |I_k|; idx[b][k][j] = I_k[j], ascending.
+// MAXD >= D bounds the unrolled per-depth loops.
+template <int MAXD>
 __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
     int S_max, const int32_t* __restrict__ seq_len, const uint8_t* __restrict__ loss_mask, int D,
     float rho, int A, const float* __restrict__ u_anchor, const float* __restrict__ u_keep,
@@ -56,9 +58,9 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
     uint32_t* status) {
   __shared__ int hist[2048];
   __shared__ int red[kIdxWarps];
-  __shared__ int wofs[kMaxD][kIdxWarps];
-  __shared__ int base[kMaxD];
-  __shared__ int tot[kMaxD];
+  __shared__ int wofs[MAXD][kIdxWarps];
+  __shared__ int base[MAXD];
+  __shared__ int tot[MAXD];
   __shared__ int pick[2];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
   int need_eq = 0;  // keys equal to thr taken, lowest positions first
   if (A > 0) {
     int c = 0;
+#pragma unroll 4
     for (int i = tid; i < L; i += kIdxThreads) c += lm[i] != 0;
     c = __reduce_add_sync(0xffffffffu, c);
     if (lane == 0) red[warp] = c;
@@ -94,6 +97,7 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
         const int nb = pass == 2 ? 1024 : 2048;
         for (int j = tid; j < nb; j += kIdxThreads) hist[j] = 0;
         __syncthreads();
+#pragma unroll 4
         for (int i = tid; i < L; i += kIdxThreads) {
           if (lm[i]) {
             const uint32_t k = ua[i];
@@ -132,7 +136,7 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
   }
 
   // ---- every depth's list, 1024 positions at a time
-  if (tid < kMaxD) base[tid] = 0;
+  if (tid < MAXD) base[tid] = 0;
   __syncthreads();
   int eq_seen = 0;  // keys equal to thr met so far (same on every thread)
   for (int c0 = 0; c0 < L; c0 += kIdxThreads) {
@@ -145,29 +149,34 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
       const unsigned be = __ballot_sync(0xffffffffu, eq);
       if (lane == 0) red[warp] = __popc(be);
       __syncthreads();
-      int before = eq_seen, all = 0;
-      for (int w = 0; w < kIdxWarps; ++w) {
-        const int v = red[w];
-        before += w < warp ? v : 0;
-        all += v;
-      }
-      before += __popc(be & ((1u << lane) - 1u));
+      // equal keys in the warps before this one, and in the whole chunk
+      const int wv = red[lane];
+      const int winc = warp_inclusive_scan(wv);
+      const int before = eq_seen + __shfl_sync(0xffffffffu, winc - wv, warp) +
+                         __popc(be & ((1u << lane) - 1u));
+      const int all = __shfl_sync(0xffffffffu, winc, 31);
       sel = cand && (k < thr || (eq && before < need_eq));
       eq_seen += all;
       __syncthreads();
     }
     // the chain's depth: each further depth needs its draw below rho and its
-    // position a + k inside the sequence
+    // position a + k inside the sequence.  The draws are loaded together (one
+    // memory latency per chunk, not one per depth).
     int len = 0;
     if (sel) {
-      len = 1;
-      while (len < D && i + len < L && uk[static_cast<size_t>(len - 1) * S_max + i] < rho) ++len;
-    }
-    unsigned bal[kMaxD];
+      float uu[MAXD > 1 ? MAXD - 1 : 1];
 #pragma unroll
-    for (int k = 0; k < kMaxD; ++k) {
-      bal[k] = __ballot_sync(0xffffffffu, len > k);
-      if (k < D && lane == 0) wofs[k][warp] = __popc(bal[k]);
+      for (int k = 0; k < MAXD - 1; ++k)
+        uu[k] = (k < D - 1 && i + k + 1 < L) ? uk[static_cast<size_t>(k) * S_max + i] : 0.f;
+      len = 1;
+#pragma unroll
+      for (int k = 0; k < MAXD - 1; ++k)
+        if (len == k + 1 && k < D - 1 && i + k + 1 < L && uu[k] < rho) len = k + 2;
+    }
+#pragma unroll
+    for (int k = 0; k < MAXD; ++k) {
+      const unsigned bk = __ballot_sync(0xffffffffu, len > k);
+      if (k < D && lane == 0) wofs[k][warp] = __popc(bk);
     }
     __syncthreads();
     if (warp < D) {
@@ -178,9 +187,10 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
     }
     __syncthreads();
 #pragma unroll
-    for (int k = 0; k < kMaxD; ++k) {
+    for (int k = 0; k < MAXD; ++k) {
+      const unsigned bk = __ballot_sync(0xffffffffu, len > k);
       if (k < D && len > k) {
-        const int pos = base[k] + wofs[k][warp] + __popc(bal[k] & ((1u << lane) - 1u));
+        const int pos = base[k] + wofs[k][warp] + __popc(bk & ((1u << lane) - 1u));
         idx[(static_cast<size_t>(b) * D + k) * S_max + pos] = i;
         if (k > 0) place[(static_cast<size_t>(b) * (D - 1) + (k - 1)) * S_max + i] = pos;
       }
@@ -235,11 +245,20 @@ __global__ void __launch_bounds__(kMaskThreads) cod_mask_kernel(
   const int32_t* ib = idx + static_cast<size_t>(b) * D * S_max;
   const int32_t* pb = D > 1 ? place + static_cast<size_t>(b) * (D - 1) * S_max : nullptr;
   const long long nvec = width / 16;
-  for (long long q = static_cast<long long>(blockIdx.x) * kMaskWarps + warp; q < rows;
-       q += static_cast<long long>(gridDim.x) * kMaskWarps) {
-    int k = 0;
+  const long long stride = static_cast<long long>(gridDim.x) * kMaskWarps;
+  // row q's anchor (and its depth) is loaded one row ahead, so its latency
+  // overlaps the previous row's stores
+  auto anchor_of = [&](long long q, int& k) {
+    k = 0;
     while (k + 1 < D && qoff[k + 1] <= q) ++k;
-    const int a = ib[static_cast<size_t>(k) * S_max + (q - qoff[k])];
+    return ib[static_cast<size_t>(k) * S_max + (q - qoff[k])];
+  };
+  long long q = static_cast<long long>(blockIdx.x) * kMaskWarps + warp;
+  int k_next = 0;
+  int a_next = q < rows ? anchor_of(q, k_next) : 0;
+  for (; q < rows; q += stride) {
+    const int k = k_next, a = a_next;
+    if (q + stride < rows) a_next = anchor_of(q + stride, k_next);
     if (a < 0 || a >= L) {  // not a list this kernel's sibling wrote
       if (lane == 0) set_status(status, PE_ST_CAPACITY);
       continue;
@@ -322,11 +341,14 @@ extern "C" int pe_cod_sample_indices(int B, int S_max, const int32_t* seq_len,
   if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return PE_ERR_CUDA;
   if (B == 0) return PE_OK;
   int32_t* place = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kWsHeader);
-  return launch_pdl(cod_index_kernel, dim3(B), dim3(kIdxThreads), 0, st, S_max, seq_len,
-                    loss_mask, n_depth, retain, max_anchors, u_anchor, u_keep, idx, counts, place,
-                    status) == cudaSuccess
-             ? PE_OK
-             : PE_ERR_CUDA;
+  auto go = [&](auto kernel) {
+    return launch_pdl(kernel, dim3(B), dim3(kIdxThreads), 0, st, S_max, seq_len, loss_mask,
+                      n_depth, retain, max_anchors, u_anchor, u_keep, idx, counts, place, status);
+  };
+  const cudaError_t err = n_depth <= 4   ? go(cod_index_kernel<4>)
+                          : n_depth <= 8 ? go(cod_index_kernel<8>)
+                                         : go(cod_index_kernel<kMaxD>);
+  return err == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 
 extern "C" int pe_cod_mask(int B, int S_max, const int32_t* seq_len, int n_depth,
