@@ -276,18 +276,21 @@ __global__ void __launch_bounds__(kMaskThreads) cod_mask_kernel(
     for (long long v = lane; v < nvec; v += 32) {
       const long long c0 = v * 16;
       uint32_t w[4];
-      if (c0 + 15 <= a) {
+      if (c0 + 15 <= a) {  // wholly inside the context the row sees
         w[0] = w[1] = w[2] = w[3] = 0x01010101u;
       } else {
+        w[0] = w[1] = w[2] = w[3] = 0u;
+        if (c0 <= a) {  // the one vector that holds column a
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t x = 0;
+          for (int h = 0; h < 4; ++h) {
+            uint32_t x = 0;
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            if (c0 + 4 * h + t <= a) x |= 1u << (8 * t);
-          w[h] = x;
+            for (int t = 0; t < 4; ++t)
+              if (c0 + 4 * h + t <= a) x |= 1u << (8 * t);
+            w[h] = x;
+          }
         }
-        if (c0 + 16 > L) {
+        if (c0 + 16 > L) {  // reaches the chain tokens' columns
           for (int j = 1; j <= k; ++j) {
             const long long s = spc[warp][j] - c0;
             if (s >= 0 && s < 16) w[s >> 2] |= 1u << (8 * (s & 3));
