@@ -103,7 +103,8 @@ def measured_peaks():
 PROFILED = {"gptoss_b1_k7": ("lm_head_gemm_gptoss_b1_k7.md", "traffic_bytes_per_step"),
             "gptoss_b64_k7_postnorm": ("lm_head_gemm_gptoss_b64_k7.md", "traffic_bytes_per_step"),
             "verify_b64_k7": ("verify_greedy_b64_k7.md", "traffic_bytes_per_launch_f32"),
-            "verify_b64_k7_bf16": ("verify_greedy_b64_k7.md", "traffic_bytes_per_launch_bf16")}
+            "verify_b64_k7_bf16": ("verify_greedy_b64_k7.md", "traffic_bytes_per_launch_bf16"),
+            "cod_s8192_a1024": ("cod_index_mask_s8192_a1024.md", "traffic_bytes_per_launch")}
 
 
 def sources_digest(files):
