@@ -99,10 +99,10 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
         __syncthreads();
 #pragma unroll 4
         for (int i = tid; i < L; i += kIdxThreads) {
-          if (lm[i]) {
-            const uint32_t k = ua[i];
-            if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & (nb - 1)], 1);
-          }
+          // both loads issue together (the key does not wait for the mask byte)
+          const uint8_t m = lm[i];
+          const uint32_t k = ua[i];
+          if (m && (k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & (nb - 1)], 1);
         }
         __syncthreads();
         if (warp == 0) {
@@ -141,10 +141,19 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
   int eq_seen = 0;  // keys equal to thr met so far (same on every thread)
   for (int c0 = 0; c0 < L; c0 += kIdxThreads) {
     const int i = c0 + tid;
-    const bool cand = i < L && lm[i] != 0;
+    // the position's mask byte, key and chain draws are loaded together: one
+    // memory latency per chunk
+    const bool in = i < L;
+    const uint8_t m = in ? lm[i] : 0;
+    const uint32_t key = (capped && in) ? ua[i] : 0u;
+    float uu[MAXD > 1 ? MAXD - 1 : 1];
+#pragma unroll
+    for (int k = 0; k < MAXD - 1; ++k)
+      uu[k] = (k < D - 1 && i + k + 1 < L) ? uk[static_cast<size_t>(k) * S_max + i] : 0.f;
+    const bool cand = m != 0;
     bool sel = cand;
     if (capped) {
-      const uint32_t k = cand ? ua[i] : 0u;
+      const uint32_t k = cand ? key : 0u;
       const bool eq = cand && k == thr;
       const unsigned be = __ballot_sync(0xffffffffu, eq);
       if (lane == 0) red[warp] = __popc(be);
@@ -160,14 +169,9 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
       __syncthreads();
     }
     // the chain's depth: each further depth needs its draw below rho and its
-    // position a + k inside the sequence.  The draws are loaded together (one
-    // memory latency per chunk, not one per depth).
+    // position a + k inside the sequence
     int len = 0;
     if (sel) {
-      float uu[MAXD > 1 ? MAXD - 1 : 1];
-#pragma unroll
-      for (int k = 0; k < MAXD - 1; ++k)
-        uu[k] = (k < D - 1 && i + k + 1 < L) ? uk[static_cast<size_t>(k) * S_max + i] : 0.f;
       len = 1;
 #pragma unroll
       for (int k = 0; k < MAXD - 1; ++k)
