@@ -1,7 +1,7 @@
 """The multi-GPU benchmark path on CPU: two gloo ranks (world_size 2).
 
-Several GPUs run independent replicas of the step: each rank drafts its own
-seeded batch, nothing crosses ranks on the data path, the job's time is the
+Several GPUs run independent replicas of the step: each rank drafts (verifies,
+or builds the COD lists of) its own seeded batch, nothing crosses ranks on the data path, the job's time is the
 slowest rank's and its throughput the units of all ranks over that time.  The
 host logic that does this (bench.py: rank_workload, max_over_ranks,
 job_throughput) runs here on CPU tensors over gloo.
@@ -44,14 +44,17 @@ def _worker(rank, world, port, out_dir):
         vwl = bench.rank_workload(W.get_verify("verify_small"), rank)
         vb = W.make_verify_batch(vwl)
         vdigest = hashlib.sha256(vb["logits"].tobytes()).hexdigest()
+        cb = W.make_cod_batch(bench.rank_workload(W.get_cod("cod_tiny"), rank))
+        cdigest = hashlib.sha256(cb["u_anchor"].tobytes() + cb["loss_mask"].tobytes()).hexdigest()
         digests = [None] * world
-        dist.all_gather_object(digests, (digest, vdigest))
+        dist.all_gather_object(digests, (digest, vdigest, cdigest))
         # the job's time is the slowest rank's, on every rank
         local_ms = 1.5 + rank  # rank 1 is the slow one
         job_ms = bench.max_over_ranks(local_ms, world, "cpu")
         value = bench.job_throughput(wl.batch * wl.dims.K, world, job_ms)
         with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
-            f.write(f"{job_ms} {value} {digests[0][0]} {digests[1][0]} {digests[0][1]} {digests[1][1]}\n")
+            f.write(f"{job_ms} {value} {digests[0][0]} {digests[1][0]} {digests[0][1]} {digests[1][1]} "
+                    f"{digests[0][2]} {digests[1][2]}\n")
     finally:
         dist.destroy_process_group()
 
@@ -60,10 +63,10 @@ def test_two_gloo_ranks(tmp_path):
     world = 2
     mp.spawn(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
     rows = [open(tmp_path / f"rank{r}.txt").read().split() for r in range(world)]
-    for job_ms, value, d0, d1, v0, v1 in rows:
+    for job_ms, value, d0, d1, v0, v1, c0, c1 in rows:
         assert float(job_ms) == 2.5                      # the slower rank's time
         assert np.isclose(float(value), 2 * 2 * 4 / 2.5e-3)  # 2 ranks x B=2 x K=4 tokens
-        assert d0 != d1 and v0 != v1                     # distinct batches per rank
+        assert d0 != d1 and v0 != v1 and c0 != c1        # distinct batches per rank
     assert rows[0] == rows[1]
 
 
