@@ -218,3 +218,21 @@ def test_one_depth_mask_is_causal_over_the_anchors():
     m = C.cod_mask(lv, 5)
     assert m.shape == (3, 5)
     np.testing.assert_array_equal(m, [[1, 1, 0, 0, 0], [1, 1, 1, 0, 0], [1, 1, 1, 1, 1]])
+
+
+def test_capacity_bound_holds_for_every_mask():
+    # the library's sizing helper: q_cap and ld hold any mask of the batch
+    from speculative_drafting_gb300 import runner
+
+    for name in W.COD_WORKLOADS:
+        for over in ({}, {"retain": 1.0}, {"max_anchors": 0, "retain": 1.0}):
+            wl = W.get_cod(name, **over)
+            if wl.s_max > 4096 and over:
+                continue
+            b = W.make_cod_batch(wl)
+            q_cap, ld = runner.cod_capacity(b["S_max"], b["n_depth"], b["max_anchors"])
+            assert ld % 16 == 0
+            for lv, L in zip(C.cod_batch(b["seq_len"], b["loss_mask"], b["n_depth"], b["retain"],
+                                         b["max_anchors"], b["u_anchor"], b["u_keep"]), b["seq_len"]):
+                Q, KV = C.cod_sizes(lv, int(L))
+                assert Q <= q_cap and (KV + 15) // 16 * 16 <= ld
