@@ -10,7 +10,10 @@ kernel time comes from a loop of the LM head's own graph right after.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 A verify_* workload times pe_verify_greedy (the greedy verification that yields
-the next step's accepted counts and bonus tokens) instead of the draft step.
+the next step's accepted counts and bonus tokens) instead of the draft step.  A
+cod_* workload times pe_cod_sample_indices + pe_cod_mask (the training side's
+COD index lists and asymmetric mask); its roofline line is the mask kernel, and
+index_kernel_us is the whole call less the mask call timed alone.
 
 Prints one JSON line.  --impl reference times the CPU oracle (the only
 reference there is) on a bounded sample of the same workload.
