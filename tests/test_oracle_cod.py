@@ -236,3 +236,66 @@ def test_capacity_bound_holds_for_every_mask():
                                          b["max_anchors"], b["u_anchor"], b["u_keep"]), b["seq_len"]):
                 Q, KV = C.cod_sizes(lv, int(L))
                 assert Q <= q_cap and (KV + 15) // 16 * 16 <= ld
+
+
+# ---- planted mistakes: each one, put into the oracle, fails a pin above
+
+_orig_mask = C.cod_mask
+
+
+def _mask_context_before_anchor(levels, L):
+    m = _orig_mask(levels, L)
+    qa, _ = C.cod_rows(levels)
+    m[np.arange(len(qa)), qa] = False           # the row no longer sees its own anchor
+    return m
+
+
+def _mask_chain_strictly_earlier(levels, L):
+    qa, qk = C.cod_rows(levels)
+    ca, ck = C.cod_rows(levels[1:])
+    m = _orig_mask(levels, L)
+    for q in range(len(qa)):
+        m[q, L:] = (ca == qa[q]) & (ck + 1 < qk[q])  # drops the row's own token
+    return m
+
+
+_orig_sample = C.cod_sample_indices
+
+
+def _sample_bound_off_by_one(loss_mask, n_depth, retain, max_anchors, u_anchor, u_keep):
+    lv = _orig_sample(loss_mask, n_depth, 1.0, 0, u_anchor, u_keep)
+    return lv if retain != 1.0 or max_anchors else [
+        np.array([a for a in np.nonzero(np.asarray(loss_mask))[0] if a + k <= len(loss_mask)])
+        for k in range(n_depth)]
+
+
+def _sample_ties_to_higher_position(loss_mask, n_depth, retain, max_anchors, u_anchor, u_keep):
+    L = len(loss_mask)
+    cand = np.nonzero(np.asarray(loss_mask) != 0)[0]
+    if max_anchors > 0 and len(cand) > max_anchors:
+        order = np.lexsort((-cand, np.asarray(u_anchor, np.float32)[cand]))
+        cand = np.sort(cand[order[:max_anchors]])
+    return [cand.astype(np.int64)] + _orig_sample(np.isin(np.arange(L), cand), n_depth, retain, 0,
+                                                  u_anchor, u_keep)[1:]
+
+
+@pytest.mark.parametrize("mutant,pin", [
+    (_mask_context_before_anchor, lambda: test_mask_row_and_column_sums(0)),
+    (_mask_chain_strictly_earlier, lambda: test_mask_row_and_column_sums(0)),
+    (_mask_context_before_anchor, lambda: test_mask_is_the_draft_steps_visibility(0)),
+    (_mask_chain_strictly_earlier, lambda: test_mask_is_the_draft_steps_visibility(0)),
+])
+def test_pins_catch_planted_mask_mistakes(monkeypatch, mutant, pin):
+    monkeypatch.setattr(C, "cod_mask", mutant)
+    with pytest.raises(AssertionError):
+        pin()
+
+
+@pytest.mark.parametrize("mutant,pin", [
+    (_sample_bound_off_by_one, test_full_retain_no_cap_is_every_position_in_range),
+    (_sample_ties_to_higher_position, test_selected_anchors_precede_the_rest_in_draw_order),
+])
+def test_pins_catch_planted_sampling_mistakes(monkeypatch, mutant, pin):
+    monkeypatch.setattr(C, "cod_sample_indices", mutant)
+    with pytest.raises(AssertionError):
+        pin()
