@@ -1,4 +1,4 @@
-// COD training indices and the asymmetric attention mask.
+// COD training indices (the mask built on them is in pe_cod_mask.cu).
 //
 // "[RFC]: Add random anchor for p-eagle first position": COD sampling starts a
 // chain at every loss position (with max_anchors, at a uniform random subset of
@@ -7,7 +7,8 @@
 // tokens.  The reply's "Depth > 0 attention": a deeper query sees the original
 // sequence (up to its anchor), not only its own chain.
 //
-// Two kernels, chained by programmatic launch:
+// The index call's kernel (the mask call's kernel follows it by programmatic
+// launch):
 //   cod_index_kernel  one CTA per sequence.  Counts the loss positions; when the
 //                     cap binds, a three-pass radix select (11 + 11 + 10 bits)
 //                     over the candidates' random keys finds the cap-th
@@ -17,23 +18,13 @@
 //                     scan per depth, plus each chain member's place in its
 //                     depth's list (the mask kernel's column lookup).
 //                     Latency-bound.
-//   cod_mask_kernel   one warp per query row (anchor a, depth k): columns 0..a of
-//                     the original sequence and the row's own chain columns at
-//                     depths 1..k are 1, every other column below the row's key
-//                     count 0, written with 16-byte stores.  Bound by the mask's
-//                     bytes (HBM).
-#include "pe_common.cuh"
-#include "pe_internal.h"
+#include "pe_cod_internal.h"
 
 namespace pe {
 namespace {
 
 constexpr int kIdxThreads = 1024;
 constexpr int kIdxWarps = kIdxThreads / 32;
-constexpr int kMaskThreads = 256;
-constexpr int kMaskWarps = kMaskThreads / 32;
-constexpr int kWsHeader = 256;  // status word, then the place table
-constexpr int kMaxD = PE_COD_MAX_DEPTH;
 
 PE_DEV int warp_inclusive_scan(int v) {
   const int lane = threadIdx.x & 31;
@@ -44,8 +35,6 @@ PE_DEV int warp_inclusive_scan(int v) {
   }
   return v;
 }
-
-PE_DEV int clamp_len(int L, int S_max) { return L < 0 ? 0 : (L > S_max ? S_max : L); }
 
 // place[b][k-1][a] = index of anchor a in depth k's list (k >= 1; written for
 // chain members only).  counts[b][k] = |I_k|; idx[b][k][j] = I_k[j], ascending.
@@ -206,120 +195,12 @@ __global__ void __launch_bounds__(kIdxThreads) cod_index_kernel(
   if (tid < D) counts[b * D + tid] = base[tid];
 }
 
-// Row q of sequence b (depth-major): anchor a, depth k.  The mask row holds the
-// key columns 0..KV-1 (the L original positions, then the depth >= 1 tokens in
-// depth-major order) and is written up to the next multiple of 16 bytes.
-__global__ void __launch_bounds__(kMaskThreads) cod_mask_kernel(
-    int S_max, const int32_t* __restrict__ seq_len, int D, const int32_t* __restrict__ idx,
-    const int32_t* __restrict__ counts, const int32_t* __restrict__ place, uint8_t* __restrict__ mask,
-    long long q_cap, long long ld, long long mstride, uint32_t* status) {
-  __shared__ int qoff[kMaxD + 1];
-  __shared__ int spc[kMaskWarps][kMaxD];
-  const int b = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  pdl_trigger();
-  pdl_wait();
-  const int L_in = seq_len[b];
-  const int L = clamp_len(L_in, S_max);
-  if (threadIdx.x == 0) {
-    uint32_t bad = L != L_in ? PE_ST_CAPACITY : 0u;
-    int s = 0;
-    for (int k = 0; k < D; ++k) {
-      int n = counts[b * D + k];
-      if (n < 0 || n > L) {
-        bad |= PE_ST_CAPACITY;
-        n = n < 0 ? 0 : L;
-      }
-      qoff[k] = s;
-      s += n;
-    }
-    qoff[D] = s;
-    if (bad && blockIdx.x == 0) set_status(status, bad);
-  }
-  __syncthreads();
-  const long long Q = qoff[D];
-  const long long n0 = qoff[1];
-  const long long KV = L + Q - n0;
-  long long rows = Q, width = (KV + 15) / 16 * 16;
-  if (rows > q_cap || width > ld) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, PE_ST_CAPACITY);
-    rows = rows < q_cap ? rows : q_cap;
-    width = width < ld ? width : ld;
-  }
-  uint8_t* mb = mask + static_cast<long long>(b) * mstride;
-  const int32_t* ib = idx + static_cast<size_t>(b) * D * S_max;
-  const int32_t* pb = D > 1 ? place + static_cast<size_t>(b) * (D - 1) * S_max : nullptr;
-  const long long nvec = width / 16;
-  const long long stride = static_cast<long long>(gridDim.x) * kMaskWarps;
-  // row q's anchor (and its depth) is loaded one row ahead, so its latency
-  // overlaps the previous row's stores
-  auto anchor_of = [&](long long q, int& k) {
-    k = 0;
-    while (k + 1 < D && qoff[k + 1] <= q) ++k;
-    return ib[static_cast<size_t>(k) * S_max + (q - qoff[k])];
-  };
-  long long q = static_cast<long long>(blockIdx.x) * kMaskWarps + warp;
-  int k_next = 0;
-  int a_next = q < rows ? anchor_of(q, k_next) : 0;
-  for (; q < rows; q += stride) {
-    const int k = k_next, a = a_next;
-    if (q + stride < rows) a_next = anchor_of(q + stride, k_next);
-    if (a < 0 || a >= L) {  // not a list this kernel's sibling wrote
-      if (lane == 0) set_status(status, PE_ST_CAPACITY);
-      continue;
-    }
-    // the row's own chain token at depth j (1..k) is key column
-    // L + (qoff[j] - n0) + its place in depth j's list
-    if (lane >= 1 && lane <= k) {
-      const int p = pb[static_cast<size_t>(lane - 1) * S_max + a];
-      const bool ok = p >= 0 && p < qoff[lane + 1] - qoff[lane];
-      if (!ok) set_status(status, PE_ST_CAPACITY);
-      spc[warp][lane] = ok ? static_cast<int>(L + (qoff[lane] - n0) + p) : -1;
-    }
-    __syncwarp();
-    uint8_t* rowp = mb + q * ld;
-    for (long long v = lane; v < nvec; v += 32) {
-      const long long c0 = v * 16;
-      uint32_t w[4];
-      if (c0 + 15 <= a) {  // wholly inside the context the row sees
-        w[0] = w[1] = w[2] = w[3] = 0x01010101u;
-      } else {
-        w[0] = w[1] = w[2] = w[3] = 0u;
-        if (c0 <= a) {  // the one vector that holds column a
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            uint32_t x = 0;
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-              if (c0 + 4 * h + t <= a) x |= 1u << (8 * t);
-            w[h] = x;
-          }
-        }
-        if (c0 + 16 > L) {  // reaches the chain tokens' columns
-          for (int j = 1; j <= k; ++j) {
-            const long long s = spc[warp][j] - c0;
-            if (s >= 0 && s < 16) w[s >> 2] |= 1u << (8 * (s & 3));
-          }
-        }
-      }
-      *reinterpret_cast<uint4*>(rowp + c0) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    __syncwarp();
-  }
-}
-
 }  // namespace
 }  // namespace pe
 
 using namespace pe;
 
-extern "C" size_t pe_cod_workspace_bytes(int B, int S_max, int n_depth) {
-  if (B < 0 || S_max < 0 || n_depth < 1 || n_depth > PE_COD_MAX_DEPTH) return 0;
-  return static_cast<size_t>(kWsHeader) +
-         static_cast<size_t>(B) * static_cast<size_t>(n_depth - 1) * static_cast<size_t>(S_max) *
-             sizeof(int32_t);
-}
-
-static int cod_common_args(int B, int S_max, int n_depth, const void* seq_len, void* ws,
+int cod_common_args(int B, int S_max, int n_depth, const void* seq_len, void* ws,
                            size_t ws_bytes) {
   if (B < 0 || S_max < 0 || n_depth < 1 || n_depth > PE_COD_MAX_DEPTH) return PE_ERR_ARG;
   if (B > 65535) return PE_ERR_UNSUPPORTED;
@@ -327,6 +208,14 @@ static int cod_common_args(int B, int S_max, int n_depth, const void* seq_len, v
   if (ws_bytes < pe_cod_workspace_bytes(B, S_max, n_depth)) return PE_ERR_ARG;
   if (B > 0 && !seq_len) return PE_ERR_ARG;
   return PE_OK;
+}
+
+
+extern "C" size_t pe_cod_workspace_bytes(int B, int S_max, int n_depth) {
+  if (B < 0 || S_max < 0 || n_depth < 1 || n_depth > PE_COD_MAX_DEPTH) return 0;
+  return static_cast<size_t>(kWsHeader) +
+         static_cast<size_t>(B) * static_cast<size_t>(n_depth - 1) * static_cast<size_t>(S_max) *
+             sizeof(int32_t);
 }
 
 extern "C" int pe_cod_sample_indices(int B, int S_max, const int32_t* seq_len,
@@ -356,27 +245,4 @@ extern "C" int pe_cod_sample_indices(int B, int S_max, const int32_t* seq_len,
                           : n_depth <= 8 ? go(cod_index_kernel<8>)
                                          : go(cod_index_kernel<kMaxD>);
   return err == cudaSuccess ? PE_OK : PE_ERR_CUDA;
-}
-
-extern "C" int pe_cod_mask(int B, int S_max, const int32_t* seq_len, int n_depth,
-                           const int32_t* idx, const int32_t* counts, uint8_t* mask, int64_t q_cap,
-                           int64_t ld, int64_t mask_stride, void* ws, size_t ws_bytes,
-                           void* stream) {
-  NvtxRange nvtx("pe_cod_mask");
-  const int e = cod_common_args(B, S_max, n_depth, seq_len, ws, ws_bytes);
-  if (e != PE_OK) return e;
-  if (q_cap < 0 || ld < 16 || ld % 16 != 0 || mask_stride % 16 != 0) return PE_ERR_ARG;
-  if (q_cap > INT64_MAX / ld || (q_cap > 0 && mask_stride < q_cap * ld)) return PE_ERR_ARG;
-  if (B > 0 && (!counts || !idx || !mask)) return PE_ERR_ARG;
-  if (reinterpret_cast<uintptr_t>(mask) % 16 != 0) return PE_ERR_ARG;
-  if (B == 0 || q_cap == 0) return PE_OK;
-  const int sms = num_sms_of_current_device();
-  const int gx = (4 * sms + B - 1) / B;
-  const int32_t* place = reinterpret_cast<const int32_t*>(static_cast<const char*>(ws) + kWsHeader);
-  return launch_pdl(cod_mask_kernel, dim3(gx < 1 ? 1 : gx, B), dim3(kMaskThreads), 0,
-                    static_cast<cudaStream_t>(stream), S_max, seq_len, n_depth, idx, counts, place,
-                    mask, static_cast<long long>(q_cap), static_cast<long long>(ld),
-                    static_cast<long long>(mask_stride), static_cast<uint32_t*>(ws)) == cudaSuccess
-             ? PE_OK
-             : PE_ERR_CUDA;
 }
