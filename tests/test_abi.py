@@ -122,3 +122,10 @@ def test_cod_host_checks(lib):
     assert mask(1, 10, p, 4, p, p, ctypes.c_void_p((1 << 21) + 8), 8, 32, 256, ws, big, None) == \
         binding.PE_ERR_ARG                                                                     # mask misaligned
     assert mask(1, 10, p, 4, p, p, p, 1 << 62, 32, 1 << 12, ws, big, None) == binding.PE_ERR_ARG  # overflow
+
+
+def test_cod_mask_empty_calls_are_no_ops(lib):
+    # B = 0 or q_cap = 0: nothing to write, answered on the host (no device call)
+    ws, p = ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 21)
+    assert lib.pe_cod_mask(0, 10, None, 4, None, None, None, 8, 32, 256, ws, 1 << 30, None) == binding.PE_OK
+    assert lib.pe_cod_mask(2, 10, p, 4, p, p, p, 0, 32, 0, ws, 1 << 30, None) == binding.PE_OK
