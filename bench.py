@@ -264,6 +264,40 @@ def run_reference(args, rank, world):
 # ----------------------------------------------------------------------------- our arm
 
 
+def warm_up_eager(r, stream, n=3):
+    """n eager steps on `stream` (the step's first calls, before any capture)."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            r.run(stream=stream)
+    stream.synchronize()
+
+
+def capture_step_graph(r, stream):
+    """The timed graph of one step: pe_prepare_inputs -> pe_draft_step ->
+    pe_argmax exactly as the benchmark replays it (no logits store unless the
+    runner asks for logits), captured on `stream`.  Every kernel boundary keeps
+    its programmatic launch.  Returns (graph, kernel nodes in it)."""
+    import torch
+
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)  # kept to count its kernel nodes
+    except TypeError:
+        g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        r.prepare(stream=stream)
+        r.step(stream=stream)
+        r.argmax(stream=stream)
+    n = graph_kernel_nodes(g)
+    if hasattr(g, "instantiate"):
+        try:
+            g.instantiate()
+        except RuntimeError:
+            pass
+    return g, n
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -292,31 +326,14 @@ def run_ours(args, rank, world, local):
     n_rows = B * K
     stream = torch.cuda.Stream()
     # eager warm-up, then capture
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            r.run(stream=stream)
-    stream.synchronize()
+    warm_up_eager(r, stream)
     st, _ = r.status()
     if st:
         raise RuntimeError(f"device status {st:#x} on the benchmark batch")
-    # the whole step (prepare + drafter layer + LM head and argmax) is one graph,
-    # so every kernel boundary keeps its programmatic launch; the LM head alone
-    # is a second graph, timed in its own loop for the roofline line
-    try:
-        g_step = torch.cuda.CUDAGraph(keep_graph=True)  # kept to count its kernel nodes
-    except TypeError:
-        g_step = torch.cuda.CUDAGraph()
+    # the whole step is one graph; the LM head alone is a second graph, timed in
+    # its own loop for the roofline line
+    g_step, launches_per_step = capture_step_graph(r, stream)
     g_lm = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_step, stream=stream):
-        r.prepare(stream=stream)
-        r.step(stream=stream)
-        r.argmax(stream=stream)
-    launches_per_step = graph_kernel_nodes(g_step)
-    if hasattr(g_step, "instantiate"):
-        try:
-            g_step.instantiate()
-        except RuntimeError:
-            pass
     with torch.cuda.graph(g_lm, stream=stream):
         r.argmax(stream=stream)
 

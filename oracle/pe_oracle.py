@@ -46,15 +46,14 @@ Readings where the pages are silent (each one is listed in the design notes):
     z = RMSNorm(a + MLP(a); gamma_final), no further norm.
   * MLP is SwiGLU: down(silu(gate(m)) * up(m)), silu(t) = t / (1 + e^-t).
   * Greedy draft: argmax of the logits, lowest index on ties.
-  * bf16 mode (weights, KV cache and tensor-core operands in bf16):
-      - rounded to bf16 (nearest, ties to even): the drafter input A, q/k/v
-        after RoPE (the cache dtype), the attention output, z;
-      - carried as a bf16 pair hi + lo (hi = bf16(v), lo = bf16(v - hi), about
-        16 significant bits): the projection operands u (QKV input), the MLP
-        input (a post-norm, m pre-norm), the SwiGLU product h, and with several
-        post-norm layers each layer's output passed to the next;
-      - not rounded (fp32 on the GPU): the fc output x and the residual sums.
-    Logits stay unrounded.  fp32 mode rounds nothing (fp64 throughout).
+  * bf16 mode (weights and the KV cache in bf16): a value is rounded to bf16
+    (nearest, ties to even) only where the step stores it as a bf16 tensor:
+    the drafter input A, q/k/v after RoPE (the cache dtype), the attention
+    output and z.  Every other intermediate (the fc output x, the QKV operand u,
+    the MLP input, the SwiGLU product, the residual sums, a layer's output
+    passed to the next) is kept exact (fp64): the reading is that nothing is
+    rounded where the pages fix no storage type.  Logits stay unrounded.  fp32
+    mode rounds nothing (fp64 throughout).
 
 Pins: every function here is checked in tests/test_oracle_*.py against closed
 forms, brute force or invariants the pages fix.  The end-to-end logits beyond
@@ -99,18 +98,13 @@ def decode(arr, dtype):
     return np.asarray(arr, dtype=np.float64)
 
 
-def bf16_pair_round(x):
-    """Value of a bf16 pair hi + lo holding x: hi = bf16(x), lo = bf16(x - hi)."""
-    hi = bf16_round(x)
-    return hi + bf16_round(np.asarray(x, dtype=np.float64) - hi)
-
-
 def _rounder(dtype):
     return bf16_round if dtype == "bf16" else (lambda v: np.asarray(v, dtype=np.float64))
 
 
-def _pair_rounder(dtype):
-    return bf16_pair_round if dtype == "bf16" else (lambda v: np.asarray(v, dtype=np.float64))
+def _exact(v):
+    """An intermediate the step does not store as a bf16 tensor: kept in fp64."""
+    return np.asarray(v, dtype=np.float64)
 
 
 # ---------------------------------------------------------------------------
@@ -317,9 +311,9 @@ def silu(t):
     return t / (1.0 + np.exp(-t))
 
 
-def swiglu_mlp(m, w_gate, w_up, w_down, R):
-    """down(silu(gate(m)) * up(m)); the product h is stored through R."""
-    h = R(silu(linear(m, w_gate)) * linear(m, w_up))
+def swiglu_mlp(m, w_gate, w_up, w_down):
+    """down(silu(gate(m)) * up(m))."""
+    h = silu(linear(m, w_gate)) * linear(m, w_up)
     return linear(h, w_down)
 
 
@@ -360,6 +354,63 @@ class _Params:
         return out
 
 
+def decoder_layer(dims, Pl, h_in, pos, att_rows, Kseq, Vseq, R, last):
+    """One decoder layer over a request's rows.
+
+    h_in: the layer's input rows [n][d] (fp64); pos: their positions.  Kseq,
+    Vseq: the layer's cache of the request as position-indexed [L][G][hd]
+    sequences, before this step; every row's k and v are written into them at
+    its position ("KV cache and CUDA graphs": the cache is read after this
+    step's writes).  att_rows: the rows whose attention, O and MLP are needed
+    (all of them, or the sample rows of the last layer).  R: the rounding of
+    the tensors the step stores in bf16.  [Drift] section 2: the EAGLE-3 drafter
+    layer is a pre-norm decoder layer; abstract and section 1: the post-norm
+    variant normalises after each residual.
+
+    Returns u, q (all rows), k, v, attn, a (att_rows), y (the MLP residual sum),
+    out (the layer's output: the next layer's input, or before z for the last
+    layer: RMSNorm(y; gamma_final)) and hidden (the drafter's output hidden
+    state: pre-norm y, post-norm the normalised output; both unrounded).
+    """
+    H, G_, hd = dims.n_heads, dims.n_kv_heads, dims.head_dim
+    group = H // G_
+    u = _exact(h_in) if dims.post_norm else rmsnorm(h_in, Pl["gamma_in"], dims.eps)
+    qkv = linear(u, Pl["w_qkv"])
+    q = qkv[:, : H * hd].reshape(-1, H, hd)
+    k = qkv[:, H * hd: (H + G_) * hd].reshape(-1, G_, hd)
+    v = qkv[:, (H + G_) * hd:].reshape(-1, G_, hd)
+    q = R(rope(q, pos, dims.rope_theta))
+    k = R(rope(k, pos, dims.rope_theta))
+    v = R(v)
+    for i, p in enumerate(pos):
+        Kseq[int(p)] = k[i]
+        Vseq[int(p)] = v[i]
+    sinks = Pl.raw("attn_sink")
+    attn = np.empty((len(att_rows), H, hd))
+    for kk, i in enumerate(att_rows):
+        n_keys = int(pos[i]) + 1      # causal: the full context plus earlier rows
+        for h in range(H):
+            g = h // group
+            attn[kk, h] = attend(q[i, h], Kseq[:n_keys, g], Vseq[:n_keys, g],
+                                 None if sinks is None else float(sinks[h]))
+    attn = R(attn.reshape(len(att_rows), H * hd))
+    xs = h_in[att_rows]
+    o_proj = linear(attn, Pl["w_o"])
+    if dims.post_norm:
+        a = rmsnorm(xs + o_proj, Pl["gamma_post"], dims.eps)
+        y = a + swiglu_mlp(a, Pl["w_gate"], Pl["w_up"], Pl["w_down"])
+        # a post-norm layer's output is normalised (the last one's is z)
+        out = rmsnorm(y, Pl["gamma_final"], dims.eps)
+        hidden = out
+    else:
+        a = xs + o_proj
+        m = rmsnorm(a, Pl["gamma_post"], dims.eps)
+        y = a + swiglu_mlp(m, Pl["w_gate"], Pl["w_up"], Pl["w_down"])
+        out = y if not last else rmsnorm(y, Pl["gamma_final"], dims.eps)
+        hidden = y
+    return dict(u=u, q=q, k=k, v=v, attn=attn, a=a, y=y, out=out, hidden=hidden)
+
+
 def request_kv_sequence(cache, block_table, r, n_pos, block_size, dtype):
     """The first n_pos cache positions of request r as [n_pos][G][hd] fp64,
     read through its block table (cache is [num_blocks][G][bs][hd])."""
@@ -372,7 +423,8 @@ def request_kv_sequence(cache, block_table, r, n_pos, block_size, dtype):
     return decode(seq, dtype)
 
 
-def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_logits=True):
+def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_logits=True,
+               round_stores=True):
     """One parallel-draft step.
 
     dims: object with d, n_heads, n_kv_heads, head_dim, inter, vocab, K,
@@ -387,6 +439,9 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
           never modified.
     requests: indices of the requests to run the layer for (default: all);
           metadata is always built for the whole batch.
+    round_stores: in bf16 mode, round the tensors the step stores in bf16 (A,
+          q/k/v, the attention output, z).  False computes the plain fp64
+          definition on the same stored inputs (nothing rounded at all).
 
     Returns {"meta": ..., "req": {r: per-request results}} where a request's
     results hold, over its valid rows in order: rows, A, x, u, k, v, slot (u, k
@@ -401,8 +456,7 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
     layer's output is z.  Each layer has its own KV cache.
     """
     dt = dims.dtype
-    R = _rounder(dt)
-    R2 = _pair_rounder(dt)
+    R = _rounder(dt) if round_stores else _exact
     P = _Params(w, dt)
     K, H, G_, hd = dims.K, dims.n_heads, dims.n_kv_heads, dims.head_dim
     meta = prepare_metadata(batch["qsl"], batch["prev_tok"], batch["prev_pos"],
@@ -428,7 +482,7 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
                           for o in rows])
         Erows = np.stack([emb_mask if meta["is_masked"][o] else P.emb_row(int(meta["tok"][o]))
                           for o in rows])
-        A = drafter_input(Grows, Erows, gam_s, dims.eps, dt)
+        A = drafter_input(Grows, Erows, gam_s, dims.eps, dt if round_stores else "f32")
         # (4) fc, then the decoder layers.  Every layer but the last runs over all
         # the request's valid rows (the next layer's keys and values need them);
         # the last runs its attention, O and MLP over the K sample rows only
@@ -439,60 +493,27 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
         # sample rows are the last K valid rows of the request (NTP row, MASK rows)
         s_loc = np.arange(len(rows) - K, len(rows))
         assert (rows[s_loc] == meta["sample_idx"][r * K:(r + 1) * K]).all()
-        group = H // G_
         h_in = x
         k_layers, v_layers = [], []
         for li, Pl in enumerate(layer_params):
             last = li == n_layers - 1
-            u = R2(h_in) if dims.post_norm else R2(rmsnorm(h_in, Pl["gamma_in"], dims.eps))
-            if li == 0:
-                u0 = u
-            qkv = linear(u, Pl["w_qkv"])
-            q = qkv[:, : H * hd].reshape(-1, H, hd)
-            k = qkv[:, H * hd: (H + G_) * hd].reshape(-1, G_, hd)
-            v = qkv[:, (H + G_) * hd:].reshape(-1, G_, hd)
-            q = R(rope(q, pos, dims.rope_theta))
-            k = R(rope(k, pos, dims.rope_theta))
-            v = R(v)
-            k_layers.append(k)
-            v_layers.append(v)
-            # this layer's cache after this step's writes, as a position-indexed sequence
+            # this layer's cache before this step, as a position-indexed sequence
             kc_l = k_cache if n_layers == 1 else k_cache[li]
             vc_l = v_cache if n_layers == 1 else v_cache[li]
             Kseq = request_kv_sequence(kc_l, batch["block_table"], r, L, dims.block_size, dt)
             Vseq = request_kv_sequence(vc_l, batch["block_table"], r, L, dims.block_size, dt)
-            for i, p in enumerate(pos):
-                Kseq[int(p)] = k[i]
-                Vseq[int(p)] = v[i]
-            sinks = Pl.raw("attn_sink")
             att_rows = s_loc if last else np.arange(len(rows))
-            attn = np.empty((len(att_rows), H, hd))
-            for kk, i in enumerate(att_rows):
-                n_keys = int(pos[i]) + 1      # causal: the full context plus earlier rows
-                for h in range(H):
-                    g = h // group
-                    attn[kk, h] = attend(q[i, h], Kseq[:n_keys, g], Vseq[:n_keys, g],
-                                         None if sinks is None else float(sinks[h]))
-            attn = R(attn.reshape(len(att_rows), H * hd))
-            xs = h_in[att_rows]
-            o_proj = linear(attn, Pl["w_o"])
-            if dims.post_norm:
-                a = R2(rmsnorm(xs + o_proj, Pl["gamma_post"], dims.eps))
-                y = a + swiglu_mlp(a, Pl["w_gate"], Pl["w_up"], Pl["w_down"], R2)
-                # a post-norm layer's output is normalised (the last one's is z);
-                # passed on to the next layer, it is carried as a bf16 pair
-                h_out = rmsnorm(y, Pl["gamma_final"], dims.eps)
-                if not last:
-                    h_out = R2(h_out)
-            else:
-                a = xs + o_proj
-                m = R2(rmsnorm(a, Pl["gamma_post"], dims.eps))
-                y = a + swiglu_mlp(m, Pl["w_gate"], Pl["w_up"], Pl["w_down"], R2)
-                h_out = y if not last else rmsnorm(y, Pl["gamma_final"], dims.eps)
-            h_in = h_out
+            ly = decoder_layer(dims, Pl, h_in, pos, att_rows, Kseq, Vseq, R, last)
+            if li == 0:
+                u0 = ly["u"]
+            k_layers.append(ly["k"])
+            v_layers.append(ly["v"])
+            q, attn, a = ly["q"], ly["attn"], ly["a"]
+            h_in = ly["out"]
         z = R(h_in)
         res = dict(rows=rows, A=A, x=x, u=u0, k=k_layers[0], v=v_layers[0], slot=meta["slot"][rows],
-                   q=q[s_loc], attn=attn, a=a, z=z, k_layers=k_layers, v_layers=v_layers)
+                   q=q[s_loc], attn=attn, a=a, z=z, h=ly["hidden"], k_layers=k_layers,
+                   v_layers=v_layers)
         if want_logits:
             logits = P.lm_logits(z)
             res["logits"] = logits

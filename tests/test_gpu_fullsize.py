@@ -9,7 +9,8 @@ import numpy as np
 import pytest
 
 from oracle import pe_oracle as O
-from parity import check_close_bf16, check_logits_and_draft, check_meta, cuda_or_skip, f64, host, setup
+from parity import (check_close_bf16, check_logits_and_draft, check_meta, check_z, cuda_or_skip, f64,
+                    host, setup)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +47,7 @@ def test_full_size_step(name, sample, over):
     for rr in sample:
         out = res["req"][rr]
         sl = slice(rr * K, (rr + 1) * K)
-        assert np.abs(z[sl] - out["z"]).max() <= 0.05
+        check_z(dm.dtype, z[sl], out["z"], where=f"request {rr}")
         check_logits_and_draft(dm.dtype, host(logits[sl]), draft[sl], out["logits"], where=f"request {rr}")
         slots = torch.from_numpy(out["slot"]).to("cuda")
         got_k = f64(host(r.k_cache[slots // bs, :, slots % bs, :]), dm.dtype)

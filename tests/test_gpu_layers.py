@@ -12,7 +12,8 @@ import numpy as np
 import pytest
 
 from oracle import pe_oracle as O
-from parity import check_close_bf16, check_logits_and_draft, check_meta, cuda_or_skip, f64, host, setup
+from parity import (check_close_bf16, check_logits_and_draft, check_meta, check_z, cuda_or_skip, f64,
+                    host, setup)
 from speculative_drafting_gb300 import binding
 
 pytestmark = pytest.mark.gpu
@@ -71,10 +72,7 @@ def test_layers_match_oracle(name, over):
     draft = host(r.draft)
     for rr, out in res["req"].items():
         sl = slice(rr * K, (rr + 1) * K)
-        if dt == "bf16":
-            assert np.abs(z[sl] - out["z"]).max() <= 0.05
-        else:
-            np.testing.assert_allclose(z[sl], out["z"], rtol=1e-5, atol=1e-5)
+        check_z(dt, z[sl], out["z"], where=f"request {rr}")
         check_logits_and_draft(dt, logits[sl], draft[sl], out["logits"], where=f"request {rr}")
     _check_layers_kv(wl, kc, vc, r, res)
 
@@ -117,6 +115,6 @@ def test_full_size_two_layers():
     for rr in sample:
         sl = slice(rr * K, (rr + 1) * K)
         out = res["req"][rr]
-        assert np.abs(z[sl] - out["z"]).max() <= 0.05
+        check_z("bf16", z[sl], out["z"], where=f"request {rr}")
         check_logits_and_draft("bf16", host(r.logits[sl]), draft[sl], out["logits"],
                                where=f"request {rr}")

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 from oracle import pe_oracle as O
-from parity import built, check_logits_and_draft, check_meta, cuda_or_skip, f64, host
+from parity import built, check_logits_and_draft, check_meta, check_z, cuda_or_skip, f64, host
 from speculative_drafting_gb300 import binding, runner, workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -62,5 +62,5 @@ def test_verify_then_draft(name, logit_dtype):
     z = f64(host(r.z), dt)
     for rr, out in res["req"].items():
         sl = slice(rr * K, (rr + 1) * K)
-        assert np.abs(z[sl] - out["z"]).max() <= 0.05
+        check_z(dt, z[sl], out["z"], where=f"request {rr}")
         check_logits_and_draft(dt, logits[sl], draft[sl], out["logits"], where=f"request {rr}")

@@ -8,8 +8,8 @@ import numpy as np
 import pytest
 
 from oracle import pe_oracle as O
-from parity import (LOGIT_TOL, check_close_bf16, check_logits_and_draft, check_meta, cuda_or_skip, f64,
-                    host, setup)
+from parity import (LOGIT_TOL, check_close_bf16, check_logits_and_draft, check_meta, check_z,
+                    cuda_or_skip, f64, host, setup)
 
 pytestmark = pytest.mark.gpu
 
@@ -78,10 +78,7 @@ def test_step_matches_oracle(name, over):
     draft = host(r.draft)
     for rr, out in res["req"].items():
         sl = slice(rr * K, (rr + 1) * K)
-        if dt == "bf16":
-            assert np.abs(z[sl] - out["z"]).max() <= 0.05
-        else:
-            np.testing.assert_allclose(z[sl], out["z"], rtol=1e-5, atol=1e-5)
+        check_z(dt, z[sl], out["z"], where=f"request {rr}")
         check_logits_and_draft(dt, logits[sl], draft[sl], out["logits"], where=f"request {rr}")
     _check_kv(wl, b, kc, vc, r, res)
 
@@ -130,5 +127,5 @@ def test_random_steps(seed):
     logits, draft = host(r.logits), host(r.draft)
     for rr, out in res["req"].items():
         sl = slice(rr * K, (rr + 1) * K)
-        assert np.abs(z[sl] - out["z"]).max() <= 0.05
+        check_z("bf16", z[sl], out["z"], where=f"request {rr}")
         check_logits_and_draft("bf16", logits[sl], draft[sl], out["logits"], where=f"request {rr}")

@@ -12,7 +12,9 @@
 * Batch order and physical block numbering do not matter.
 * The per-stream RMSNorm of "Attention Drift" (Observation 2) makes the step
   invariant to the scale of each captured stream.
-* In bf16 mode every stored intermediate is a bf16 value.
+* In bf16 mode the tensors the step stores in bf16 are bf16 values, nothing
+  else is rounded, and the logits stay within the step's 2e-2 tolerance of the
+  unrounded fp64 definition.
 """
 
 import dataclasses
@@ -238,25 +240,69 @@ def test_per_stream_scale_invariance():
         np.testing.assert_allclose(res2["req"][r]["logits"], res["req"][r]["logits"], rtol=0, atol=1e-6)
 
 
-def test_bf16_mode_stores_bf16_values_and_tracks_fp64():
-    wl, b, w, kc, vc = _setup("small_prenorm")
-    res = O.draft_step(wl.dims, w, b, kc, vc)
-    # the same data with no rounding anywhere
-    w64 = {k: O.bf16_decode(v).astype(np.float32) for k, v in w.items()}
-    b64 = dict(b)
-    b64["H_tgt"] = O.bf16_decode(b["H_tgt"]).astype(np.float32)
-    dm64 = dataclasses.replace(wl.dims, dtype="f32")
-    res64 = O.draft_step(dm64, w64, b64, O.bf16_decode(kc).astype(np.float32),
-                         O.bf16_decode(vc).astype(np.float32))
-    for r in range(wl.batch):
-        rr = res["req"][r]
+# The step's bf16 logit tolerance: the bf16 oracle (rounding only the tensors the
+# step stores in bf16) must itself stay within it of the plain fp64 definition.
+BF16_LOGIT_TOL = 2e-2
+
+
+def _bf16_tracks_fp64(wl, w, b, kc, vc, requests=None):
+    """Max |logit| difference between the bf16 oracle and the unrounded fp64
+    definition on the same stored inputs; also checks what is rounded."""
+    res = O.draft_step(wl.dims, w, b, kc, vc, requests=requests)
+    res64 = O.draft_step(wl.dims, w, b, kc, vc, requests=requests, round_stores=False)
+    worst = 0.0
+    for r, rr in res["req"].items():
+        # stored tensors are bf16 values ...
         for key in ("A", "k", "v", "q", "attn", "z"):
             assert np.array_equal(O.bf16_round(rr[key]), rr[key]), key
-        # the projection operands are bf16 pairs: not bf16 values, but pair values
-        assert not np.array_equal(O.bf16_round(rr["u"]), rr["u"])
-        assert np.array_equal(O.bf16_pair_round(rr["u"]), rr["u"])
-        diff = np.abs(rr["logits"] - res64["req"][r]["logits"]).max()
-        assert diff < 0.05, diff
+        # ... the fc output, the QKV operand and the MLP input are not rounded
+        for key in ("x", "u", "a"):
+            assert not np.array_equal(O.bf16_round(rr[key]), rr[key]), key
+        r64 = res64["req"][r]
+        for key in ("A", "z"):
+            assert not np.array_equal(O.bf16_round(r64[key]), r64[key]), key
+        worst = max(worst, float(np.abs(rr["logits"] - r64["logits"]).max()))
+    return worst
+
+
+@pytest.mark.parametrize("name,over", [
+    ("small_prenorm", {}),
+    ("small_prenorm", {"post_norm": True}),
+    ("small_postnorm_hd128", {}),
+    ("small_postnorm_hd128", {"post_norm": False}),
+    ("small_prenorm", {"n_layers": 3}),
+    ("small_prenorm", {"n_layers": 2, "post_norm": True, "sinks": True}),
+])
+def test_bf16_mode_stores_bf16_values_and_tracks_fp64(name, over):
+    wl, b, w, kc, vc = _setup(name, **over)
+    diff = _bf16_tracks_fp64(wl, w, b, kc, vc)
+    print(f"{name} {over}: bf16 oracle vs fp64 logits max-abs {diff:.3g}")
+    assert diff <= BF16_LOGIT_TOL, diff
+
+
+# At the full sizes the six bf16 stores themselves (A, q, k, v, the attention
+# output and z, which the kernels store in bf16 too) move the logits by up to
+# about the step's tolerance from exact arithmetic: at GPT-OSS B=64 post-norm,
+# rounding only A moves them by 0.014, only q 0.009, only k 0.007, only z 0.009,
+# only the attention output or v 0.004, all six 0.020.  Both sides round at the
+# same points, so the kernel-vs-oracle logits stay far inside 2e-2 (0.002-0.008
+# measured); this pin bounds the oracle's own drift from the definition.
+FULL_SIZE_TRACK_TOL = 2.5e-2
+
+
+@pytest.mark.parametrize("name,requests,over", [
+    ("gptoss_b1_k7", None, {}),
+    ("gptoss_b64_k7_postnorm", (0, 31, 63), {}),
+    # the Llama-8B shape at a 2048-token context (the 32K cache takes minutes to draw)
+    ("llama8b_b32_k8_32k", (0, 17), {"ctx": (2048,) * 32}),
+])
+def test_bf16_oracle_tracks_fp64_at_full_size(name, requests, over):
+    """The bf16 oracle against the unrounded definition at the full model sizes
+    (sampled requests)."""
+    wl, b, w, kc, vc = _setup(name, **over)
+    diff = _bf16_tracks_fp64(wl, w, b, kc, vc, requests=requests)
+    print(f"{name}: bf16 oracle vs fp64 logits max-abs {diff:.3g}")
+    assert diff <= FULL_SIZE_TRACK_TOL, diff
 
 
 def test_table1_stream_rms_equalised_by_per_stream_norm():
