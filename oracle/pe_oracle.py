@@ -522,6 +522,73 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
     return out
 
 
+def draft_autoregressive(dims, w, batch, k_cache, v_cache, requests=None, round_stores=True):
+    """The autoregressive EAGLE-3 drafting that the parallel step replaces: K
+    sequential passes of the same one-layer drafter, one draft token per pass.
+
+    [vLLM] "Solving the autoregressive drafting bottleneck": K draft tokens cost
+    K sequential forward passes of the drafter.  [Drift] section 3 and section
+    4.1 (Table 1, Observation 3): once drafting starts, the drafter consumes its
+    own hidden state instead of the target's.
+
+      pass 1      the parallel step with K = 1: the request's non-rejected rows,
+                  the NTP row (bonus token, target hidden state) as the one
+                  sample row; it drafts t_1.
+      pass k > 1  one row per request at position prev_pos[a_r] + k - 1 (the
+                  position of P-EAGLE's MASK row k - 1): the drafter's hidden
+                  state from pass k - 1 fills the three stream slots (where the
+                  parallel step puts h_shared) and the embedding of t_{k-1} the
+                  token slot; it drafts t_k.
+    The hidden state passed on is the layer's output before the LM head's norm:
+    y for a pre-norm layer, the normalised output for a post-norm layer (both
+    unrounded).  Every pass writes its rows' KV and attends to the cache after
+    its own write.  One decoder layer (dims.n_layers == 1).
+
+    Returns {"meta": pass 1's metadata, "req": {r: dict(draft [K], logits [K][V],
+    z [K][d], hidden [K][d], pos [K])}}.
+    """
+    assert max(1, int(getattr(dims, "n_layers", 1))) == 1, "one decoder layer"
+    import dataclasses
+
+    dt = dims.dtype
+    R = _rounder(dt) if round_stores else _exact
+    P = _Params(w, dt)
+    K = dims.K
+    d1 = dataclasses.replace(dims, K=1)
+    first = draft_step(d1, w, batch, k_cache, v_cache, requests=requests, round_stores=round_stores)
+    meta = first["meta"]
+    gam_s = P["gamma_stream"]
+    out = {"meta": meta, "req": {}}
+    for r, r1 in first["req"].items():
+        # the cache after pass 1: prior context plus the non-rejected rows' writes
+        P0 = int(meta["pos"][meta["sample_idx"][r]])
+        L = P0 + K
+        Kseq = request_kv_sequence(k_cache, batch["block_table"], r, L, dims.block_size, dt)
+        Vseq = request_kv_sequence(v_cache, batch["block_table"], r, L, dims.block_size, dt)
+        for i, o in enumerate(r1["rows"]):
+            Kseq[int(meta["pos"][o])] = r1["k"][i]
+            Vseq[int(meta["pos"][o])] = r1["v"][i]
+        drafts, logits, zs, hs, poss = [int(r1["draft"][0])], [r1["logits"][0]], [r1["z"][0]], \
+            [r1["h"][0]], [P0]
+        for k in range(2, K + 1):
+            p = P0 + k - 1
+            G = np.broadcast_to(hs[-1], (dims.n_streams, dims.d))[None]
+            A = drafter_input(G, P.emb_row(drafts[-1])[None], gam_s, dims.eps,
+                              dt if round_stores else "f32")
+            x = linear(A, P["w_fc"])
+            ly = decoder_layer(dims, P, x, np.array([p]), np.array([0]), Kseq, Vseq, R, True)
+            z = R(ly["out"])
+            lg = P.lm_logits(z)
+            drafts.append(int(argmax_lowest(lg)[0]))
+            logits.append(lg[0])
+            zs.append(z[0])
+            hs.append(ly["hidden"][0])
+            poss.append(p)
+        out["req"][r] = dict(draft=np.array(drafts, np.int32), logits=np.stack(logits),
+                             z=np.stack(zs), hidden=np.stack(hs), pos=np.array(poss, np.int64))
+    return out
+
+
 def prepare_inputs(dims, w, batch):
     """Steps (1)-(3) over every output row: metadata, G, E and A (all T_out rows)."""
     dt = dims.dtype
