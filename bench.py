@@ -5,7 +5,11 @@ One step = the whole hot path over one synthetic batch: pe_prepare_inputs
 attention, final norm) -> pe_argmax (LM head + greedy argmax).  The step is
 captured as one CUDA graph (the way a serving engine runs the drafter) and
 timed with CUDA events on its stream, max over ranks.  The roofline line's
-kernel time comes from a loop of the LM head's own graph right after.
+kernel time comes from a loop of the LM head's own graph right after.  The
+default line also carries, on one GPU, an "autoregressive" block (the same
+batch drafted by the K-pass autoregressive baseline and by the parallel step,
+at K = 7 and K = 3) and a "batched" block (the concurrency-64 post-norm
+configuration, step and LM-head roofline); --no-extra leaves them out.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -54,6 +58,8 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the batched-step and autoregressive comparison blocks")
     return p.parse_args()
 
 
@@ -392,6 +398,8 @@ def run_ours(args, rank, world, local):
 
     # end to end through the C-ABI with host buffers: H2D of the step inputs from
     # pinned memory (one packed copy), the step, D2H of the draft tokens, every step
+    # Each step ends with the host waiting for its drafts (what a scheduler pays
+    # before it can use them), so the host clock times the loop.
     out_host = torch.empty(n_rows, dtype=torch.int32).pin_memory()
     h2d = stage_host.numel()
     d2h = out_host.numel() * 4
@@ -401,16 +409,15 @@ def run_ours(args, rank, world, local):
             stage_dev.copy_(stage_host, non_blocking=True)
             one_step()
             out_host.copy_(r.draft, non_blocking=True)
-        stream.synchronize()
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
+            stream.synchronize()
+        t0 = time.perf_counter()
         for _ in range(n_e2e):
             stage_dev.copy_(stage_host, non_blocking=True)
             one_step()
             out_host.copy_(r.draft, non_blocking=True)
-        a1.record(stream)
+            stream.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
     torch.cuda.synchronize()
-    e2e_ms = a0.elapsed_time(a1) / n_e2e
     e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
     st, _ = r.status()
     if st:
@@ -464,10 +471,124 @@ def run_ours(args, rank, world, local):
                          "avg_launch_us": lm_avg_s * 1e6},
             "cpu_baseline": cpu,
         }
+        if world == 1 and not args.no_extra and wl.name == DEFAULT_WORKLOAD:
+            line["autoregressive"] = autoregressive_block(wl, w, args.steps, stream)
+            line["batched"] = batched_block("gptoss_b64_k7_postnorm", w, args.steps, stream, peaks,
+                                            src)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
+
+
+def time_replays(g, stream, steps, warmup=3):
+    """Device time (ms) per replay of graph g over `steps` back-to-back replays."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        a1.record(stream)
+    torch.cuda.synchronize()
+    return a0.elapsed_time(a1) / steps
+
+
+def autoregressive_block(wl, w, steps, stream):
+    """The pages' comparison on this GPU ("P-EAGLE: parallel speculative decoding
+    in vLLM", Solving the autoregressive drafting bottleneck, Performance
+    benchmarks: K drafts cost K sequential passes; the autoregressive drafter
+    peaks at K = 3, P-EAGLE at K = 7): the same batch drafted by the parallel
+    step (one pass) and by pe_draft_autoregressive (K passes), each one CUDA
+    graph, at K = 7 and K = 3 (K + 1 verify rows per request)."""
+    import torch
+
+    from speculative_drafting_gb300 import runner
+
+    out = {}
+    for K in (7, 3):
+        wk = W.get(wl.name, K=K, n_prev=K + 1)
+        batch = W.make_batch(wk)
+        kc, vc = W.make_kv_cache(wk, batch["num_blocks"])
+        r = runner.StepRunner(wk, batch, w, kc, vc)
+        warm_up_eager(r, stream)
+        g_par, n_par = capture_step_graph(r, stream)
+        par_ms = time_replays(g_par, stream, steps)
+        ws = r.drafter.autoregressive_workspace(r.B, r.T_in, r.inp["block_table"].shape[1])
+        draft = torch.empty(r.B, K, dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                r.autoregressive(draft, ws, stream=stream)
+        stream.synchronize()
+        st, _ = r.drafter.read_status(ws)
+        if st:
+            raise RuntimeError(f"device status {st:#x} in the autoregressive drafting")
+        try:
+            g_ar = torch.cuda.CUDAGraph(keep_graph=True)
+        except TypeError:
+            g_ar = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_ar, stream=stream):
+            r.autoregressive(draft, ws, stream=stream)
+        n_ar = graph_kernel_nodes(g_ar)
+        if hasattr(g_ar, "instantiate"):
+            try:
+                g_ar.instantiate()
+            except RuntimeError:
+                pass
+        ar_ms = time_replays(g_ar, stream, max(10, steps // 4))
+        n_tok = r.B * K
+        out[f"k{K}"] = {"workload": f"{wl.name} with K={K}", "parallel_step_us": par_ms * 1e3,
+                        "parallel_kernels": n_par, "autoregressive_us": ar_ms * 1e3,
+                        "autoregressive_kernels": n_ar,
+                        "parallel_draft_tokens_per_s": n_tok / (par_ms / 1e3),
+                        "autoregressive_draft_tokens_per_s": n_tok / (ar_ms / 1e3),
+                        "speedup": ar_ms / par_ms}
+        del r
+    return out
+
+
+def batched_block(name, w, steps, stream, peaks, src):
+    """The concurrency-64 configuration ("P-EAGLE: parallel speculative decoding
+    in vLLM", Performance benchmarks, c = 64), timed in the same process with the
+    same method as the headline line: step graph, LM head graph, clocks."""
+    import torch
+
+    from speculative_drafting_gb300 import runner
+
+    wl = W.get(name)
+    batch = W.make_batch(wl)
+    kc, vc = W.make_kv_cache(wl, batch["num_blocks"])
+    r = runner.StepRunner(wl, batch, w, kc, vc)
+    warm_up_eager(r, stream)
+    st, _ = r.status()
+    if st:
+        raise RuntimeError(f"device status {st:#x} on the batched batch")
+    g, n = capture_step_graph(r, stream)
+    g_lm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_lm, stream=stream):
+        r.argmax(stream=stream)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    step_ms = time_replays(g, stream, steps)
+    lm_ms = time_replays(g_lm, stream, steps)
+    clk = clocks.stop()
+    dm = wl.dims
+    n_rows = batch["B"] * dm.K
+    flops = 2.0 * dm.vocab * dm.d * n_rows
+    ach = flops / (lm_ms / 1e3) / 1e12
+    return {"workload": name, "description": wl.description, "global_batch": batch["B"],
+            "step_us": step_ms * 1e3, "draft_tokens_per_s": n_rows / (step_ms / 1e3),
+            "gpu_launches_per_step": n,
+            "roofline": {"kernel": "gemm_tc_kernel (LM head + argmax epilogue)", "bound": "tensor",
+                         "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": ach / peaks["bf16_tflops"], "algorithmic_flops": flops,
+                         "avg_launch_us": lm_ms * 1e3, "peak_source": src,
+                         "traffic": profiled_traffic(name)},
+            "clocks": clk}
 
 
 STEP_INPUTS = ("qsl", "prev_tok", "prev_pos", "accepted", "bonus", "block_table", "H_tgt")

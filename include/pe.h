@@ -24,6 +24,9 @@
  *   pe_argmax          the LM head fused with a per-row greedy argmax.
  *   pe_verify_greedy   the target's greedy verification of the drafts, which
  *                      yields the next step's accepted counts and bonus tokens.
+ *   pe_draft_autoregressive
+ *                      the K-pass autoregressive drafting the parallel step
+ *                      replaces, on the same kernels (the baseline).
  *   pe_cod_sample_indices, pe_cod_mask
  *                      the training side's COD index lists and asymmetric
  *                      attention mask ("[RFC]: Add random anchor for p-eagle
@@ -32,15 +35,18 @@
  * Conventions for every call
  *   - All tensor arguments are DEVICE pointers owned by the caller; the library
  *     never frees or keeps them past the call (weights excepted: pe_create
- *     borrows them for the handle's lifetime; for bf16 it reads the seven
- *     projection matrices once, into its own tile-packed copy, so later
- *     writes to those seven are not seen).  Layouts are dense row-major.
+ *     borrows them for the handle's lifetime; a bf16 handle's GEMMs read the
+ *     projection matrices from the caller's tile-packed copy that
+ *     pe_pack_weights fills, so later writes to the row-major matrices are not
+ *     seen until they are packed again).  Layouts are dense row-major.  No
+ *     call allocates device memory.
  *   - Floating tensors have the handle's dtype: float (PE_DTYPE_F32) or bf16
  *     bit patterns (PE_DTYPE_BF16), except where a signature says float.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Every call only enqueues work on it: no allocation, no host
- *     synchronisation, no stream creation, so a step can be captured in a CUDA
- *     graph.  Host-side sizes (B, T_in, ...) are baked into a capture.
+ *     synchronisation (pe_read_status excepted), no stream creation, so a step
+ *     can be captured in a CUDA graph.  Host-side sizes (B, T_in, ...) are
+ *     baked into a capture.
  *   - `ws` is a caller-allocated device workspace of at least
  *     pe_workspace_bytes() bytes, 256-byte aligned.  One workspace must not be
  *     used by two calls that may run concurrently.
@@ -171,6 +177,11 @@ typedef struct pe_weights {
                                more logit with a zero value row.  NULL: no sink */
   const pe_layer_weights* more_layers; /* HOST array of n_layers - 1 entries (layers
                                2..N; read by pe_create only), NULL for one layer */
+  const void* packed;       /* bf16 handles with a layer: the tile-packed copy of the
+                               projection matrices (pe_pack_weights), caller-owned,
+                               256-byte aligned, borrowed for the handle's lifetime;
+                               unused (may be NULL) in fp32 mode */
+  size_t packed_bytes;      /* its size, at least pe_packed_weights_bytes(dims) */
 } pe_weights;
 
 /* Drafter-batch metadata: caller-owned device buffers written by
@@ -197,18 +208,36 @@ typedef struct pe_meta {
 
 typedef struct pe_handle pe_handle;
 
+/* Bytes of the tile-packed copy of a bf16 drafter's projection matrices: w_fc,
+ * w_qkv, w_o, w_gate, w_up, w_down and w_lm, then w_qkv, w_o, w_gate, w_up and
+ * w_down of each later layer, one after another, each starting 256-byte
+ * aligned; a matrix [M][K] is stored in blocks of 128 rows x 64 columns, each
+ * one contiguous 16 KB run, blocks ordered by column within a row of blocks,
+ * zero-padded to whole blocks.  0 for fp32 dims (the fp32 kernels read the
+ * row-major matrices) or dims pe_create would refuse. */
+size_t pe_packed_weights_bytes(const pe_dims* dims);
+
+/* Fill `packed` (device, caller-owned, packed_bytes >= pe_packed_weights_bytes,
+ * 256-byte aligned) with the tile-packed copy of w's projection matrices
+ * (w_fc, w_qkv, w_o, w_gate, w_up, w_down, w_lm and more_layers' five; the
+ * other fields are not read).  Asynchronous on `stream`: the copy must be
+ * complete before a handle over it runs (same stream, or synchronise).  Packing
+ * again after the caller changes its matrices updates every handle that
+ * borrows the buffer.  PE_ERR_UNSUPPORTED for fp32 or unsupported dims;
+ * PE_ERR_ARG for null or misaligned pointers or a buffer too small. */
+int pe_pack_weights(const pe_dims* dims, const pe_weights* w, void* packed, size_t packed_bytes,
+                    void* stream);
+
 /* Create a handle for one drafter.  Validates dims (PE_ERR_UNSUPPORTED) and
- * pointers (PE_ERR_ARG), selects the kernels and encodes the TMA descriptors of
- * the weight matrices.  bf16: allocates device memory for a copy of w_fc,
- * w_qkv, w_o, w_gate, w_up, w_down and w_lm in tile order (blocks of 128 rows x
- * 64 columns, each one contiguous 16 KB run, zero-padded to whole blocks), then
- * synchronises the device and fills it; pe_destroy frees it.  This is the only
- * call that allocates device memory or synchronises.  Uses the current CUDA
- * device; *out is NULL on error (PE_ERR_CUDA: allocation or packing failed). */
+ * pointers (PE_ERR_ARG: a bf16 handle with a layer also needs w->packed, filled
+ * by pe_pack_weights), selects the kernels and encodes the TMA descriptors of
+ * the packed weight matrices.  Allocates no device memory and does not
+ * synchronise; the handle is a host object.  Uses the current CUDA device;
+ * *out is NULL on error. */
 int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out);
 
-/* Destroy a handle (NULL is ignored): frees its packed weight copy, never the
- * caller's weights.  No work that uses the handle may still be in flight. */
+/* Destroy a handle (NULL is ignored).  It never frees the caller's weights or
+ * packed copy.  No work that uses the handle may still be in flight. */
 void pe_destroy(pe_handle* h);
 
 /* Workspace bytes that cover every call with at most max_batch requests,
@@ -264,22 +293,65 @@ int pe_draft_step(pe_handle* h, int B, int T_in, const pe_meta* meta, const void
 int pe_argmax(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens, float* logits,
               void* ws, size_t ws_bytes, void* stream);
 
+/* The autoregressive drafting that the parallel step replaces, on the same
+ * kernels: K sequential passes of the one-layer drafter, one draft token per
+ * pass ("P-EAGLE: parallel speculative decoding in vLLM", Solving the
+ * autoregressive drafting bottleneck: K drafts cost K sequential forward
+ * passes; "Attention Drift", sections 3 and 4.1: after the first step the
+ * drafter consumes its own hidden state).
+ *   pass 1      the parallel step with one draft row per request: metadata,
+ *               drafter input, layer and LM head over the non-rejected rows of
+ *               the verify batch, the NTP row (bonus token, target hidden state)
+ *               drafting token 1;
+ *   pass k > 1  one row per request at position prev_pos[a_r] + k - 1 (where
+ *               the parallel step puts MASK row k - 1), its three stream slots
+ *               filled with the drafter's own hidden state of pass k - 1 (y of a
+ *               pre-norm layer, the normalised output of a post-norm layer, both
+ *               fp32) and its token slot with the embedding of draft k - 1.
+ * Every pass writes its rows' KV (k_cache, v_cache as for pe_draft_step, the
+ * slots of the parallel step's non-rejected rows) and attends to the cache
+ * after its own write.
+ * Inputs as for pe_prepare_inputs (no metadata buffers: they live in ws).
+ *   draft_tokens [B][K] int32 out: draft k of request r at r * K + k - 1
+ *   logits       [B][K][V] float, nullable: each pass's fp32 logits
+ *   hidden_out   [B][K][d] float, nullable: the hidden state each pass hands
+ *                to the next (the drafter output "Attention Drift" Table 1
+ *                tracks per speculative step)
+ *   ws           pe_autoregressive_workspace_bytes(...) bytes or more, 256-byte
+ *                aligned; its status word is cleared first (pe_read_status)
+ * One decoder layer only: a handle with n_layers > 1 returns
+ * PE_ERR_UNSUPPORTED.  PE_ERR_ARG as for pe_prepare_inputs / pe_draft_step.
+ * All K passes are enqueued on `stream` (3 + 14 K kernels in bf16 mode); no host
+ * round trip between passes: each pass reads the previous pass's draft and
+ * hidden state on the device. */
+size_t pe_autoregressive_workspace_bytes(const pe_handle* h, int max_batch, int max_rows_in,
+                                         int max_blocks_per_seq);
+int pe_draft_autoregressive(pe_handle* h, int B, int T_in, const int32_t* qsl,
+                            const int32_t* prev_tok, const int64_t* prev_pos,
+                            const int32_t* accepted, const int32_t* bonus,
+                            const int32_t* block_table, int max_blocks, int num_blocks,
+                            const void* H_tgt, void* k_cache, void* v_cache, int32_t* draft_tokens,
+                            float* logits, float* hidden_out, void* ws, size_t ws_bytes,
+                            void* stream);
+
 /* Allocation-free pe_argmax.  The pages have no counterpart: this is an
  * interface addition for callers that cannot allocate device memory at all,
  * such as a serving engine that has already reserved every byte for weights and
- * KV cache and hands a plugin only a stream, code that runs while another
- * component is capturing a CUDA graph (a cudaMalloc there would break the
- * capture), or a runtime bound to a fixed memory plan.
+ * KV cache and hands a plugin only a stream, or a runtime bound to a fixed
+ * memory plan.
  * Same arguments and results as pe_argmax, without the workspace: its scratch
  * (one 64-bit argmax key per row) lives in a static device array of
  * PE_NOALLOC_MAX_ROWS entries (32 KiB) that every GPU loading this library holds
  * until the process exits.  n_rows above PE_NOALLOC_MAX_ROWS returns PE_ERR_ARG.
- * The call performs no cudaMalloc / cudaFree; it never splits the LM head over
- * K (no partial sums to keep).  The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress) with that device current, so make it
- * before any stream capture.  All calls on a device share the array: each call
- * clears the keys it uses, and calls that overlap on the GPU race.  No status
- * word is kept, so device-side problems are not reported. */
+ * The call performs no cudaMalloc / cudaFree and runs pe_argmax's LM-head plan
+ * (its K splits add their partial tiles inside a thread-block cluster, with no
+ * global scratch).  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current and caches it for the
+ * process (one context per device: do not call it again on a device after a
+ * cudaDeviceReset); make that first call before any stream capture.  All calls
+ * on a device share the array: each call clears the keys it uses, and calls
+ * that overlap on the GPU race.  No status word is kept, so device-side problems
+ * are not reported. */
 #define PE_NOALLOC_MAX_ROWS 4096
 int pe_argmax_noalloc(pe_handle* h, const void* z, int n_rows, int32_t* draft_tokens,
                       float* logits, void* stream);

@@ -33,10 +33,6 @@ enum {
                                  partial sum, out = float [16][n][M] (split k at
                                  out + k*n*M; tiles past the split count are left
                                  as they were); the result is their sum */
-  PE_PROJ_TWO_SM = 0x800,     /* bf16 only: run the 2-SM schedule (clusters of two
-                                 CTAs issuing M = 256 MMAs) whatever the size,
-                                 for token tiles of 16 rows or more; never splits K */
-  PE_PROJ_ONE_SM = 0x1000,    /* bf16 only: never the 2-SM schedule */
   PE_PROJ_ARGMAX = 0x2000     /* PE_PROJ_LM only: the LM head with its argmax
                                  epilogue, as pe_argmax runs it: out = float
                                  logits [n][V]; the argmax of each row (int32 [n])

@@ -411,6 +411,12 @@ def decoder_layer(dims, Pl, h_in, pos, att_rows, Kseq, Vseq, R, last):
     return dict(u=u, q=q, k=k, v=v, attn=attn, a=a, y=y, out=out, hidden=hidden)
 
 
+def params(w, dtype):
+    """fp64 views of stored drafter parameters (decoded on first use), the form
+    autoregressive_pass takes."""
+    return _Params(w, dtype)
+
+
 def request_kv_sequence(cache, block_table, r, n_pos, block_size, dtype):
     """The first n_pos cache positions of request r as [n_pos][G][hd] fp64,
     read through its block table (cache is [num_blocks][G][bs][hd])."""
@@ -522,6 +528,26 @@ def draft_step(dims, w, batch, k_cache=None, v_cache=None, requests=None, want_l
     return out
 
 
+def autoregressive_pass(dims, P, hidden_prev, token_prev, p, Kseq, Vseq, round_stores=True):
+    """One pass k >= 2 of the autoregressive drafting for one request: the row at
+    position p whose three stream slots hold hidden_prev (the drafter's hidden
+    state of the pass before, [d]) and whose token is token_prev.  Its k and v
+    are written into the request's cache sequences Kseq / Vseq at p (the cache
+    the pass attends to after its write).  P: the parameters (_Params).
+    Returns z, logits, draft, hidden (the state passed to the next pass), k, v."""
+    dt = dims.dtype
+    R = _rounder(dt) if round_stores else _exact
+    G = np.broadcast_to(np.asarray(hidden_prev, np.float64), (dims.n_streams, dims.d))[None]
+    A = drafter_input(G, P.emb_row(int(token_prev))[None], P["gamma_stream"], dims.eps,
+                      dt if round_stores else "f32")
+    x = linear(A, P["w_fc"])
+    ly = decoder_layer(dims, P, x, np.array([p]), np.array([0]), Kseq, Vseq, R, True)
+    z = R(ly["out"])
+    lg = P.lm_logits(z)
+    return dict(z=z[0], logits=lg[0], draft=int(argmax_lowest(lg)[0]), hidden=ly["hidden"][0],
+                k=ly["k"][0], v=ly["v"][0])
+
+
 def draft_autoregressive(dims, w, batch, k_cache, v_cache, requests=None, round_stores=True):
     """The autoregressive EAGLE-3 drafting that the parallel step replaces: K
     sequential passes of the same one-layer drafter, one draft token per pass.
@@ -545,19 +571,18 @@ def draft_autoregressive(dims, w, batch, k_cache, v_cache, requests=None, round_
     its own write.  One decoder layer (dims.n_layers == 1).
 
     Returns {"meta": pass 1's metadata, "req": {r: dict(draft [K], logits [K][V],
-    z [K][d], hidden [K][d], pos [K])}}.
+    z [K][d], hidden [K][d], pos [K], first (pass 1's draft_step results),
+    k_pass / v_pass [K-1][G][hd] (the KV passes 2..K write))}}.
     """
     assert max(1, int(getattr(dims, "n_layers", 1))) == 1, "one decoder layer"
     import dataclasses
 
     dt = dims.dtype
-    R = _rounder(dt) if round_stores else _exact
     P = _Params(w, dt)
     K = dims.K
     d1 = dataclasses.replace(dims, K=1)
     first = draft_step(d1, w, batch, k_cache, v_cache, requests=requests, round_stores=round_stores)
     meta = first["meta"]
-    gam_s = P["gamma_stream"]
     out = {"meta": meta, "req": {}}
     for r, r1 in first["req"].items():
         # the cache after pass 1: prior context plus the non-rejected rows' writes
@@ -570,22 +595,21 @@ def draft_autoregressive(dims, w, batch, k_cache, v_cache, requests=None, round_
             Vseq[int(meta["pos"][o])] = r1["v"][i]
         drafts, logits, zs, hs, poss = [int(r1["draft"][0])], [r1["logits"][0]], [r1["z"][0]], \
             [r1["h"][0]], [P0]
+        ks, vs = [], []
         for k in range(2, K + 1):
             p = P0 + k - 1
-            G = np.broadcast_to(hs[-1], (dims.n_streams, dims.d))[None]
-            A = drafter_input(G, P.emb_row(drafts[-1])[None], gam_s, dims.eps,
-                              dt if round_stores else "f32")
-            x = linear(A, P["w_fc"])
-            ly = decoder_layer(dims, P, x, np.array([p]), np.array([0]), Kseq, Vseq, R, True)
-            z = R(ly["out"])
-            lg = P.lm_logits(z)
-            drafts.append(int(argmax_lowest(lg)[0]))
-            logits.append(lg[0])
-            zs.append(z[0])
-            hs.append(ly["hidden"][0])
+            one = autoregressive_pass(dims, P, hs[-1], drafts[-1], p, Kseq, Vseq, round_stores)
+            drafts.append(one["draft"])
+            logits.append(one["logits"])
+            zs.append(one["z"])
+            hs.append(one["hidden"])
             poss.append(p)
+            ks.append(one["k"])
+            vs.append(one["v"])
         out["req"][r] = dict(draft=np.array(drafts, np.int32), logits=np.stack(logits),
-                             z=np.stack(zs), hidden=np.stack(hs), pos=np.array(poss, np.int64))
+                             z=np.stack(zs), hidden=np.stack(hs), pos=np.array(poss, np.int64),
+                             first=r1, k_pass=np.array(ks).reshape(-1, dims.n_kv_heads, dims.head_dim),
+                             v_pass=np.array(vs).reshape(-1, dims.n_kv_heads, dims.head_dim))
     return out
 
 

@@ -60,7 +60,8 @@ class PeLayerWeights(ctypes.Structure):
 
 class PeWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS] + \
-        [("more_layers", ctypes.POINTER(PeLayerWeights))]
+        [("more_layers", ctypes.POINTER(PeLayerWeights)), ("packed", ctypes.c_void_p),
+         ("packed_bytes", ctypes.c_size_t)]
 
 
 META_FIELDS = ["out_qsl", "tok", "pos", "is_rejected", "is_masked", "hidden_src", "slot",
@@ -92,6 +93,10 @@ def load(path: str | None = None):
     lib.pe_create.restype = _i32
     lib.pe_destroy.argtypes = [_vp]
     lib.pe_destroy.restype = None
+    lib.pe_packed_weights_bytes.argtypes = [ctypes.POINTER(PeDims)]
+    lib.pe_packed_weights_bytes.restype = _sz
+    lib.pe_pack_weights.argtypes = [ctypes.POINTER(PeDims), ctypes.POINTER(PeWeights), _vp, _sz, _vp]
+    lib.pe_pack_weights.restype = _i32
     lib.pe_workspace_bytes.argtypes = [_vp, _i32, _i32, _i32]
     lib.pe_workspace_bytes.restype = _sz
     lib.pe_prepare_inputs.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp,
@@ -106,6 +111,11 @@ def load(path: str | None = None):
     lib.pe_read_status.restype = _i32
     lib.pe_status_string.argtypes = [_i32]
     lib.pe_status_string.restype = ctypes.c_char_p
+    lib.pe_autoregressive_workspace_bytes.argtypes = [_vp, _i32, _i32, _i32]
+    lib.pe_autoregressive_workspace_bytes.restype = _sz
+    lib.pe_draft_autoregressive.argtypes = [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                            _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.pe_draft_autoregressive.restype = _i32
     lib.pe_argmax_noalloc.argtypes = [_vp, _vp, _i32, _vp, _vp, _vp]
     lib.pe_argmax_noalloc.restype = _i32
     lib.pe_test_projection_workspace.argtypes = [_vp, _i32, _i32]
@@ -197,9 +207,13 @@ class Meta:
 
 
 class Drafter:
-    """One drafter handle: ``pe_create`` over device weight tensors (borrowed)."""
+    """One drafter handle: ``pe_create`` over device weight tensors (borrowed).
+    A bf16 drafter's projection matrices are first tile-packed (pe_pack_weights)
+    into a buffer this object owns and the handle borrows."""
 
-    def __init__(self, dims, weights: dict):
+    def __init__(self, dims, weights: dict, stream=None):
+        import torch
+
         self.lib = load()
         self.dims = dims
         self.weights = weights  # keep the tensors alive for the handle's lifetime
@@ -213,10 +227,28 @@ class Drafter:
                 for k in LAYER_FIELDS:
                     setattr(arr[i], k, lw[k].data_ptr() if lw.get(k) is not None else None)
             cw.more_layers = arr
+        self.cw = cw
         h = ctypes.c_void_p()
         self.cdims = make_dims(dims)
+        self.packed = None
+        n = int(self.lib.pe_packed_weights_bytes(ctypes.byref(self.cdims)))
+        if n and weights.get("w_fc") is not None:
+            dev = weights["w_fc"].device
+            self.packed = torch.empty(n, dtype=torch.uint8, device=dev)
+            self.pack(stream)
+            # the handle may be used on any stream: let the packing finish first
+            (stream or torch.cuda.current_stream()).synchronize()
+            cw.packed = self.packed.data_ptr()
+            cw.packed_bytes = n
         _check(self.lib.pe_create(ctypes.byref(self.cdims), ctypes.byref(cw), ctypes.byref(h)), "pe_create")
         self.h = h
+
+    def pack(self, stream=None, weights=None):
+        """pe_pack_weights into this drafter's packed buffer (from `weights`, a
+        PeWeights, when given: the tests pack other matrices into it)."""
+        _check(self.lib.pe_pack_weights(ctypes.byref(self.cdims), ctypes.byref(weights or self.cw),
+                                        _ptr(self.packed), self.packed.numel(), _stream(stream)),
+               "pe_pack_weights")
 
     def close(self):
         if self.h:
@@ -259,6 +291,27 @@ class Drafter:
         rc = self.lib.pe_argmax(self.h, _ptr(z), n_rows, _ptr(draft_tokens), _ptr(logits), _ptr(ws),
                                 ws.numel(), _stream(stream))
         _check(rc, "pe_argmax")
+
+    def autoregressive_workspace(self, max_batch: int, max_rows_in: int, max_blocks: int,
+                                 device="cuda"):
+        import torch
+
+        n = int(self.lib.pe_autoregressive_workspace_bytes(self.h, max_batch, max_rows_in,
+                                                           max_blocks))
+        if n == 0:
+            raise PeError(PE_ERR_ARG, "pe_autoregressive_workspace_bytes")
+        return torch.zeros(n, dtype=torch.uint8, device=device)
+
+    def draft_autoregressive(self, B, T_in, qsl, prev_tok, prev_pos, accepted, bonus, block_table,
+                             num_blocks, H_tgt, k_cache, v_cache, draft_tokens, ws, logits=None,
+                             hidden=None, stream=None):
+        """pe_draft_autoregressive: K sequential one-token passes (the baseline)."""
+        rc = self.lib.pe_draft_autoregressive(
+            self.h, B, T_in, _ptr(qsl), _ptr(prev_tok), _ptr(prev_pos), _ptr(accepted), _ptr(bonus),
+            _ptr(block_table), block_table.shape[1], num_blocks, _ptr(H_tgt), _ptr(k_cache),
+            _ptr(v_cache), _ptr(draft_tokens), _ptr(logits), _ptr(hidden), _ptr(ws), ws.numel(),
+            _stream(stream))
+        _check(rc, "pe_draft_autoregressive")
 
     def argmax_noalloc(self, z, n_rows, draft_tokens, logits=None, stream=None):
         """pe_argmax without a workspace (its scratch is a static device array)."""

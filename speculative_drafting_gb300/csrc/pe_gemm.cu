@@ -34,74 +34,35 @@ constexpr size_t kSmemBudget = 212 * 1024;  // dynamic shared memory for the sta
 // 4: 303 us, 2: 301 us, none: 306 us).
 constexpr int kPrefetchKb = 2;
 constexpr int kMaxClusterSplits = 8;        // portable cluster size
-#ifndef PE_MAX_PARTIAL_SPLITS
-#define PE_MAX_PARTIAL_SPLITS 16
-#endif
-constexpr int kMaxPartialSplits = PE_MAX_PARTIAL_SPLITS;  // splits storing their own partials
-// Weight boxes of the first stages issued before the dependency wait (1), or
-// only the first k-blocks pulled into L2 (0).  Measured slightly slower at
-// every workload (2-6 us per step), so off.
-#ifndef PE_EARLY_WEIGHTS
-#define PE_EARLY_WEIGHTS 0
-#endif
+constexpr int kMaxPartialSplits = 16;       // splits storing their own partials
 static_assert(kMaxPartialSplits <= 16, "the projection test hook holds 16 partial tiles");
-// Weights in tile order (one contiguous 16 KB block per weight box) or row-major
-// (measured, LM head at B=1 with two CTAs per SM: 188 us packed, 192 us not).
-#ifndef PE_PACKED_WEIGHTS
-#define PE_PACKED_WEIGHTS 1
-#endif
-constexpr bool kPackedWeights = PE_PACKED_WEIGHTS != 0;
-// Narrow token tiles stream weights: two 64-element K atoms per stage put the
-// two 128-byte halves of each weight row's 256 bytes on the bus back to back
-// (measured: LM head at B=1 259 us instead of 303 us).  Wide tiles keep one atom
-// so that enough stages stay in flight.
+// Weights are read in tile order (one contiguous 16 KB block per weight box;
+// measured, LM head at B=1 with two CTAs per SM: 188 us packed, 192 us
+// row-major).  Narrow token tiles stream weights: two 64-element K atoms per
+// stage put the two 128-byte halves of each weight row's 256 bytes on the bus
+// back to back (measured: LM head at B=1 259 us instead of 303 us).  Wide tiles
+// keep one atom so that enough stages stay in flight.
 constexpr int kNarrowBN = 64;
 // Token tiles up to kOccBN wide run several CTAs per SM (see below), and no
 // token tile is wider than kMaxBN.  Wide tiles gain from it too (measured, LM
-// head at B=64, 448 tokens: 636 us with one CTA per SM, 535 us with two).
-#ifndef PE_OCC_BN
-#define PE_OCC_BN 256
-#endif
-#ifndef PE_MAX_BN
-#define PE_MAX_BN 256
-#endif
-constexpr int kOccBN = PE_OCC_BN;
-// Token-tile width: the widest (up to kMaxBN) whose two ring stages fit a
-// two-CTA share of an SM (1), or whose three stages fit one CTA (0).  Measured:
-// step at B=64 1207 -> 1168 us (the bf16-pair and dual GEMMs get two CTAs).
-#ifndef PE_BN_FOR_OCC2
-#define PE_BN_FOR_OCC2 1
-#endif
-constexpr int kMaxBN = PE_MAX_BN;
+// head at B=64, 448 tokens: 636 us with one CTA per SM, 535 us with two).  The
+// token-tile width is the widest (up to kMaxBN) whose two ring stages fit a
+// two-CTA share of an SM (measured: step at B=64 1207 -> 1168 us, the bf16-pair
+// and dual GEMMs get two CTAs).
+constexpr int kOccBN = 256;
+constexpr int kMaxBN = 256;
 // Narrow token tiles run several CTAs per SM, each with its share of the SM's
 // shared memory: one CTA's loads keep only part of the SM's share of DRAM
 // bandwidth busy, whatever its ring depth (measured, LM head of 201088 x 2880 at
 // 8 tokens: 5 or 3 stages per CTA both 275 us; two CTAs of 3 stages 196 us,
 // three of 3 one-atom stages 188 us).  Up to three per SM, fewer where two
-// stages of a wide tile do not fit a third of the SM's shared memory.
-#ifndef PE_NARROW_CTAS_PER_SM
-#define PE_NARROW_CTAS_PER_SM 3
-#endif
-#ifndef PE_STREAM_CTAS_PER_SM
-#define PE_STREAM_CTAS_PER_SM 3
-#endif
-// Wide token tiles streamed over at least two rounds of weight-tile pairs run
-// as 2-SM pairs (1) or one CTA per tile, two CTAs per SM (0).  Measured, LM
-// head of 201088 x 2880 at 448 tokens: 723 us as pairs, 459 us one-SM; of
-// 128256 x 4096 at 256 tokens: 362 us against 258 us.  One thread issuing
-// tcgen05.mma keeps an SM's tensor pipe only about half busy, whatever the
-// instruction's M, so two issuing CTAs per SM beat one pair per two SMs.
-#ifndef PE_TWO_SM
-#define PE_TWO_SM 0
-#endif
-constexpr bool kTwoSm = PE_TWO_SM != 0;
-// 2-SM pairs: two pairs per SM pair (one TMEM accumulator each) where they fit
-#ifndef PE_PAIR_TWO_PER_SM
-#define PE_PAIR_TWO_PER_SM 1
-#endif
-constexpr bool kPairTwoPerSm = PE_PAIR_TWO_PER_SM != 0;
-constexpr int kNarrowCtasPerSm = PE_NARROW_CTAS_PER_SM;
-constexpr int kStreamCtasPerSm = PE_STREAM_CTAS_PER_SM;
+// stages of a wide tile do not fit a third of the SM's shared memory.  (A 2-SM
+// pair schedule, M = 256 MMAs over clusters of two CTAs, measured slower: LM
+// head of 201088 x 2880 at 448 tokens 723 us as pairs, 459 us one-SM; one thread
+// issuing tcgen05.mma keeps an SM's tensor pipe only about half busy whatever
+// the instruction's M, so two issuing CTAs per SM beat one pair per two SMs.)
+constexpr int kNarrowCtasPerSm = 3;
+constexpr int kStreamCtasPerSm = 3;
 // shared memory of an SM that its CTAs can have (228 KB less 1 KB)
 constexpr size_t kSmemPerSm = 227 * 1024;
 // per CTA beside its ring: the system's 1 KB, the static barriers and
@@ -121,8 +82,7 @@ struct TcArgs {
   int tile_base, tile_count;  // the (m, n) tiles of this launch
   int BN, n_tiles, m_tiles, k_splits, kb_per_split, num_kb, stages, acc_bufs;
   int atoms;  // 64-element K atoms per stage (a k-block is atoms * 64 elements)
-  int packed;   // weights tile-packed: box (m, atom) at row (m * k_atoms + atom) * 128
-  int k_atoms;  // 64-element atoms per weight row (packed)
+  int k_atoms;  // 64-element atoms per weight row: box (m, atom) at row (m * k_atoms + atom) * 128
   uint32_t tmem_cols;
   const int* n_rows_dev;
   Epilogue epi;
@@ -339,14 +299,9 @@ struct TileRef {
 // (a multiple of 64).  Packed weights: past K the box lies beyond the last
 // block, so TMA fills it with zeros as it does past K of a row-major weight.
 PE_DEV void weight_box(const TcArgs& p, int m, int x, int& cx, int& cy) {
-  if (p.packed) {
-    const int a = x / kBK;
-    cx = 0;
-    cy = (a < p.k_atoms ? m * p.k_atoms + a : p.m_tiles * p.k_atoms) * kBM;
-  } else {
-    cx = x;
-    cy = m * kBM;
-  }
+  const int a = x / kBK;
+  cx = 0;
+  cy = (a < p.k_atoms ? m * p.k_atoms + a : p.m_tiles * p.k_atoms) * kBM;
 }
 
 // The tile a CTA works on at its it-th turn; false when it has no more.
@@ -371,8 +326,8 @@ PE_DEV bool next_tile(const TcArgs& p, int it, TileRef& t) {
 }
 
 // A tile whose token rows all lie past the live row count is skipped, except a
-// CTA's first tile when it is the token tile 0: its weights start loading
-// before the row count is known, so every role works through it (its epilogue
+// CTA's first tile when it is the token tile 0 (only an empty batch makes that
+// one dead: every role then works through it the same way, and its epilogue
 // stores nothing past the live rows).
 PE_DEV bool tile_skipped(const TcArgs& p, const TileRef& t, int it, int n_rows) {
   return t.n * p.BN >= n_rows && !(it == 0 && t.n == 0);
@@ -426,45 +381,28 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
     abort_sh = 0;
     fence_barrier_init();
   }
-  // weight boxes of the first tile's first stages, already loading (thread 0)
-  int pre = 0;
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&mapA);
     if (p.dual) prefetch_tmap(&mapA2);
     prefetch_tmap(&mapB);
     if (p.bpair) prefetch_tmap(&mapB2);
-    // The weights do not depend on the previous kernel.  Token tile 0: load the
-    // weight boxes of the first stages into the ring now, while that kernel
-    // finishes (the token boxes follow after the dependency wait).  Otherwise
-    // pull the first k-blocks into L2.
+    // The weights do not depend on the previous kernel: pull the first tile's
+    // first k-blocks into L2 while that kernel finishes.  (Loading the first
+    // stages' weight boxes straight into the ring before the dependency wait
+    // measured 2-6 us slower per step at every workload.)
     TileRef t;
     if (next_tile(p, 0, t)) {
       const int kb0 = t.ks * p.kb_per_split;
       const int nkb = min(p.num_kb, kb0 + p.kb_per_split) - kb0;
-      if (PE_EARLY_WEIGHTS && t.n == 0) {
-        const uint64_t pol_w = policy_evict_first();
-        pre = min(nkb, p.stages);
-        for (int s = 0; s < pre; ++s) {
-          mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-          for (int at = 0; at < p.atoms; ++at) {
-            uint8_t* sa = smem + static_cast<size_t>(s) * stage_bytes + at * atom_bytes;
-            int cx, cy;
-            weight_box(p, t.m, (kb0 + s) * kbk + at * kBK, cx, cy);
-            tma_load_2d(sa, &mapA, &full_bar[s], cx, cy, pol_w);
-            if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[s], cx, cy, pol_w);
-          }
+      const int kb1 = min(kb0 + nkb, kb0 + kPrefetchKb / p.atoms);
+      for (int kb = kb0; kb < kb1; ++kb)
+        for (int at = 0; at < p.atoms; ++at) {
+          if (kb * kbk + at * kBK >= p.K) break;
+          int cx, cy;
+          weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
+          tma_prefetch_l2_2d(&mapA, cx, cy);
+          if (p.dual) tma_prefetch_l2_2d(&mapA2, cx, cy);
         }
-      } else {
-        const int kb1 = min(kb0 + nkb, kb0 + kPrefetchKb / p.atoms);
-        for (int kb = kb0; kb < kb1; ++kb)
-          for (int at = 0; at < p.atoms; ++at) {
-            if (kb * kbk + at * kBK >= p.K) break;
-            int cx, cy;
-            weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
-            tma_prefetch_l2_2d(&mapA, cx, cy);
-            if (p.dual) tma_prefetch_l2_2d(&mapA2, cx, cy);
-          }
-      }
     }
   }
   if (warp == 1) {
@@ -504,10 +442,8 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
       const uint64_t pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      // per stage: ever armed / parity of the last arm; stages 0..pre-1 were
-      // armed (phase 0) with their weight boxes before the dependency wait
-      uint32_t armed = (1u << pre) - 1u, armed_parity = 0;
-      uint32_t pending_b = armed;  // ... whose token boxes are still to be issued
+      // per stage: ever armed / parity of the last arm
+      uint32_t armed = 0u, armed_parity = 0;
       auto issue_b = [&](int s, int kb, int tn) {
         for (int at = 0; at < p.atoms; ++at) {
           uint8_t* sa = smem + static_cast<size_t>(s) * stage_bytes + at * atom_bytes;
@@ -523,29 +459,23 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
         const int kb0 = t.ks * p.kb_per_split;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (it == 0 && kb - kb0 < pre) {
-            // weights already on their way into this stage
-            issue_b(stage, kb, t.n);
-            pending_b &= ~(1u << stage);
-          } else {
-            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
-              fail();
-              break;
-            }
-            mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
-            // the atoms of one row follow each other in memory: their boxes go
-            // out back to back, A first (the weights dominate the traffic)
-            for (int at = 0; at < p.atoms; ++at) {
-              uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes;
-              int cx, cy;
-              weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
-              tma_load_2d(sa, &mapA, &full_bar[stage], cx, cy, pol_w);
-              if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], cx, cy, pol_w);
-            }
-            issue_b(stage, kb, t.n);
-            armed |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            fail();
+            break;
           }
+          mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
+          // the atoms of one row follow each other in memory: their boxes go
+          // out back to back, A first (the weights dominate the traffic)
+          for (int at = 0; at < p.atoms; ++at) {
+            uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes + at * atom_bytes;
+            int cx, cy;
+            weight_box(p, t.m, kb * kbk + at * kBK, cx, cy);
+            tma_load_2d(sa, &mapA, &full_bar[stage], cx, cy, pol_w);
+            if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], cx, cy, pol_w);
+          }
+          issue_b(stage, kb, t.n);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
@@ -553,11 +483,6 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
         }
       }
       if (*abort_flag) {
-        // stages armed before the wait but left without their token boxes get
-        // them now, so that their barriers complete
-        if (pending_b && next_tile(p, 0, t))
-          for (int s = 0; s < p.stages; ++s)
-            if (pending_b & (1u << s)) issue_b(s, t.ks * p.kb_per_split + s, t.n);
         // let copies already in flight land before the CTA's shared memory goes away
         for (int s = 0; s < p.stages; ++s)
           if (armed & (1u << s)) {
@@ -766,303 +691,6 @@ __global__ void __launch_bounds__(kTcThreads, OCC)
   }
 }
 
-// ------------------------------------------------------------------ tcgen05 kernel, 2-SM pairs
-//
-// Wide token tiles over many weight tiles (the LM head of a batch): a cluster
-// of two CTAs on two SMs runs M = 256 MMAs, so each MMA instruction does twice
-// the work and each SM stages only half of the token tile.  Pair tile
-// (mp, n) covers weight tiles 2mp (rank 0) and 2mp + 1 (rank 1) and token
-// tile n; each rank loads its weight box and token rows n*BN + rank*BN/2 ..
-// + BN/2 into its own ring, and its TMEM lanes hold its own weight tile's
-// accumulator (all BN token columns).  Roles per CTA, as in the 1-SM kernel:
-// warp 0 lane 0 loads; on rank 0 warp 1 lane 0 issues the MMAs and commits to
-// the stage and accumulator barriers of both CTAs; on rank 1 warp 1 lane 0
-// reports each stage of its ring as landed to rank 0's full barrier (its own
-// loads complete on its own barriers, so each CTA only ever waits for copies
-// into its own shared memory); warps 2-5 run the same epilogue on their own
-// accumulator and report it drained to rank 0.  Clusters take pair tiles
-// c, c + clusters, ... (persistent).
-
-PE_DEV bool next_pair_tile(const TcArgs& p, int it, uint32_t rank, TileRef& t) {
-  const int clusters = static_cast<int>(gridDim.x >> 1);
-  const int local = static_cast<int>(blockIdx.x >> 1) + it * clusters;
-  if (local >= p.tile_count) return false;
-  const int tile = p.tile_base + local;
-  t.ks = 0;
-  t.n = tile % p.n_tiles;
-  t.m = 2 * (tile / p.n_tiles) + static_cast<int>(rank);
-  return true;
-}
-
-template <int OCC>
-__global__ void __launch_bounds__(kTcThreads, OCC)
-    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap mapA,
-                        const __grid_constant__ CUtensorMap mapA2,
-                        const __grid_constant__ CUtensorMap mapB,
-                        const __grid_constant__ CUtensorMap mapB2, const TcArgs p) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_sh, n_rows_sh;
-  __shared__ int ep_ok[2][4];
-  __shared__ float epi_sh[4][kEpiScratch];
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int nA = p.dual ? 2 : 1;
-  const int nB = p.bpair ? 2 : 1;
-  const int hn = p.BN / 2;  // token rows of the tile in this CTA's ring
-  const uint32_t bh_bytes = static_cast<uint32_t>(hn) * 128u;
-  const uint32_t stage_bytes = kABytes * nA + bh_bytes * nB;
-  const int nbuf = p.acc_bufs;
-  const uint32_t buf_cols = static_cast<uint32_t>(p.BN * nA);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      // rank 0: its own loads' arrival and rank 1's report for the same stage
-      mbar_init(&full_bar[s], rank == 0 ? 2 : 1);
-      mbar_init(&empty_bar[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], 8);  // the 4 epilogue warps of both CTAs
-    }
-    mbar_init(&final_bar, 1);
-    abort_sh = 0;
-    fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&mapA);
-    if (p.dual) prefetch_tmap(&mapA2);
-    prefetch_tmap(&mapB);
-    if (p.bpair) prefetch_tmap(&mapB2);
-    // the weights do not depend on the previous kernel: pull the first
-    // k-blocks of the first tile into L2 while it finishes
-    TileRef t;
-    if (next_pair_tile(p, 0, rank, t)) {
-      for (int kb = 0; kb < min(p.num_kb, kPrefetchKb); ++kb) {
-        int cx, cy;
-        weight_box(p, t.m, kb * kBK, cx, cy);
-        tma_prefetch_l2_2d(&mapA, cx, cy);
-        if (p.dual) tma_prefetch_l2_2d(&mapA2, cx, cy);
-      }
-    }
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(&tmem_base_sh, p.tmem_cols);
-    tmem_relinquish_pair();
-  }
-  pdl_trigger();
-  pdl_wait();
-  if (threadIdx.x == 0) {
-    int n = p.N_cap;
-    if (p.n_rows_dev) {
-      const int v = *p.n_rows_dev;
-      n = v < 0 ? 0 : (v < n ? v : n);
-    }
-    n_rows_sh = n;
-  }
-  // both CTAs' barriers are initialised and their TMEM allocated before
-  // either touches the other's
-  tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();
-  tc_fence_after();
-
-  const uint32_t tmem_base = tmem_base_sh;
-  const int n_rows = n_rows_sh;
-  volatile int* abort_flag = &abort_sh;
-  auto fail = [&]() {
-    abort_sh = 1;
-    set_status(p.status, PE_ST_TIMEOUT);
-  };
-
-  if (warp == 0) {
-    // ---------------- TMA producer (both CTAs, into their own ring)
-    if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_parity = 0;
-      TileRef t;
-      bool ok = true;
-      for (int it = 0; ok && next_pair_tile(p, it, rank, t) && !*abort_flag; ++it) {
-        if (tile_skipped(p, t, it, n_rows)) continue;
-        const int y = t.n * p.BN + static_cast<int>(rank) * hn;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full_bar[stage], stage_bytes);
-          uint8_t* sa = smem + static_cast<size_t>(stage) * stage_bytes;
-          int cx, cy;
-          weight_box(p, t.m, kb * kBK, cx, cy);
-          tma_load_2d(sa, &mapA, &full_bar[stage], cx, cy, pol_w);
-          if (p.dual) tma_load_2d(sa + kABytes, &mapA2, &full_bar[stage], cx, cy, pol_w);
-          tma_load_2d(sa + kABytes * nA, &mapB, &full_bar[stage], kb * kBK, y, pol_x);
-          if (p.bpair)
-            tma_load_2d(sa + kABytes * nA + bh_bytes, &mapB2, &full_bar[stage], kb * kBK, y, pol_x);
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (*abort_flag) {
-        // let this CTA's copies in flight land before its shared memory goes
-        // away (on rank 0 the wait may also run out for want of rank 1's
-        // report: it is bounded)
-        for (int s = 0; s < p.stages; ++s)
-          if (armed & (1u << s)) {
-            int dummy = 0;
-            mbar_wait(&full_bar[s], (armed_parity >> s) & 1u, &dummy);
-          }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
-      // ---------------- MMA issuer of the pair
-      const uint32_t idesc = idesc_bf16_f32(2 * kBM, p.BN);
-      int stage = 0, cnt = 0;
-      uint32_t phase = 0, acc_phase[2] = {0u, 0u};
-      TileRef t;
-      for (int it = 0; next_pair_tile(p, it, rank, t) && !*abort_flag; ++it) {
-        if (tile_skipped(p, t, it, n_rows)) continue;
-        const int b = cnt % nbuf;
-        ++cnt;
-        if (!mbar_wait_cluster(&tempty_bar[b], acc_phase[b] ^ 1u, abort_flag)) {
-          fail();
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + static_cast<uint32_t>(b) * buf_cols;
-        bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait_cluster(&full_bar[stage], phase, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + static_cast<size_t>(stage) * stage_bytes);
-          const uint64_t adesc = sw128_kmajor_desc(sa);
-          const uint64_t a2desc = sw128_kmajor_desc(sa + kABytes);
-          const uint64_t bdesc = sw128_kmajor_desc(sa + kABytes * nA);
-          const uint64_t b2desc = sw128_kmajor_desc(sa + kABytes * nA + bh_bytes);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            umma_bf16_pair(d0, adesc + 2 * kk, bdesc + 2 * kk, idesc, acc);
-            if (p.bpair) umma_bf16_pair(d0, adesc + 2 * kk, b2desc + 2 * kk, idesc, 1u);
-            if (p.dual) {
-              const uint32_t d1 = d0 + static_cast<uint32_t>(p.BN);
-              umma_bf16_pair(d1, a2desc + 2 * kk, bdesc + 2 * kk, idesc, acc);
-              if (p.bpair) umma_bf16_pair(d1, a2desc + 2 * kk, b2desc + 2 * kk, idesc, 1u);
-            }
-          }
-          umma_commit_pair_both(&empty_bar[stage]);
-          if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit_pair_both(&tfull_bar[b]);
-        acc_phase[b] ^= 1u;
-      }
-      // every MMA issued by this thread has finished before either CTA
-      // releases its TMEM or leaves
-      umma_commit_pair_local(&final_bar);
-      int dummy = 0;
-      mbar_wait(&final_bar, 0, &dummy);
-    } else if (lane == 0) {
-      // ---------------- rank 1: report each landed stage to rank 0
-      const uint32_t full0 = cluster_addr_of(&full_bar[0], 0);
-      int stage = 0;
-      uint32_t phase = 0;
-      TileRef t;
-      bool ok = true;
-      for (int it = 0; ok && next_pair_tile(p, it, rank, t) && !*abort_flag; ++it) {
-        if (tile_skipped(p, t, it, n_rows)) continue;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          mbar_arrive_cluster(full0 + static_cast<uint32_t>(stage) * 8u);
-          if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    }
-  } else {
-    // ---------------- epilogue warps 2..5: TMEM lane quarter = warp % 4
-    const int q = warp & 3;
-    const int ew = warp - 2;
-    const int fl = q * 32 + lane;
-    const uint32_t tempty0 = cluster_addr_of(&tempty_bar[0], 0);
-    const bool vec = epi_vec_ok(p, p.epi);
-    uint32_t acc_phase[2] = {0u, 0u};
-    int cnt = 0;
-    TileRef t;
-    for (int it = 0; next_pair_tile(p, it, rank, t) && !*abort_flag; ++it) {
-      if (tile_skipped(p, t, it, n_rows)) continue;
-      const int b = cnt % nbuf;
-      const int par = cnt & 1;
-      ++cnt;
-      const bool ok = mbar_wait(&tfull_bar[b], acc_phase[b], abort_flag);
-      if (lane == 0) ep_ok[par][ew] = ok ? 1 : 0;
-      named_bar_sync(1, 128);
-      if (!(ep_ok[par][0] && ep_ok[par][1] && ep_ok[par][2] && ep_ok[par][3])) {
-        fail();
-        break;
-      }
-      acc_phase[b] ^= 1u;
-      tc_fence_after();
-      const int f = t.m * kBM + fl;
-      const int jt = t.n * p.BN;
-      const uint32_t tl = tmem_base + static_cast<uint32_t>(b) * buf_cols +
-                          (static_cast<uint32_t>(q * 32) << 16);
-      for (int c = 0; c < p.BN; c += 16) {
-        float v[16], v2[16];
-        tmem_ld16(tl + c, v);
-        if (p.dual) tmem_ld16(tl + p.BN + c, v2);
-        if (c + 16 >= p.BN) {
-          // last TMEM read of this buffer: the warp hands it back to rank 0
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(b) * 8u);
-        }
-        if (vec)
-          tc_store16_vec(p, p.epi, f - lane, jt + c, v, p.dual ? v2 : nullptr, n_rows, epi_sh[ew]);
-        else
-          tc_epilogue16(p, p.epi, f, jt + c, v, p.dual ? v2 : nullptr, n_rows);
-      }
-    }
-  }
-
-  // no CTA releases TMEM or leaves while the other may still use its
-  // barriers, shared memory or accumulator
-  tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, p.tmem_cols);
-  }
-}
-
 // ------------------------------------------------------------------ host: plan + launch
 
 static_assert(kNarrowCtasPerSm >= 1 && kNarrowCtasPerSm <= 3, "CTAs per SM");
@@ -1131,58 +759,8 @@ static int max_active_clusters(int occ, int cs, size_t smem) {
   return n * occ;
 }
 
-using TcPairKernelFn = decltype(&gemm_tc_pair_kernel<1>);
-
-// The pair instance for one or two pair CTAs per SM.
-static TcPairKernelFn tc_pair_kernel(int occ) {
-  return occ >= 2 ? gemm_tc_pair_kernel<2> : gemm_tc_pair_kernel<1>;
-}
-
-// Dynamic shared memory limit of a pair instance (as tc_max_dyn_smem: the limit
-// decides how many CTAs the SM takes).
-static size_t tc_pair_max_dyn_smem(int occ) {
-  return occ >= 2 ? kSmemPerSm / 2 - cta_smem_overhead(true) + 1024 : kSmemBudget + 1024;
-}
-
-static cudaError_t tc_pair_prepare(int occ) {
-  const cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel(occ),
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(tc_pair_max_dyn_smem(occ)));
-  cudaFuncSetAttribute(tc_pair_kernel(occ), cudaFuncAttributePreferredSharedMemoryCarveout,
-                       cudaSharedmemCarveoutMaxShared);
-  return e;
-}
-
-// Clusters of two pair-kernel CTAs with `smem` bytes each resident at once.
-static int max_pair_clusters(size_t smem, int occ) {
-  static std::mutex mu;
-  static std::map<std::pair<size_t, int>, int> cache;
-  std::lock_guard<std::mutex> lock(mu);
-  auto it = cache.find({smem, occ});
-  if (it != cache.end()) return it->second;
-  tc_pair_prepare(occ);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * 64);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, (void*)tc_pair_kernel(occ), &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    n = 0;
-  }
-  cache[{smem, occ}] = n;
-  return n;
-}
-
 TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split,
-                    bool partial, int two_sm) {
+                    bool partial) {
   TcPlan pl{};
   pl.M = M;
   pl.K = K;
@@ -1201,54 +779,11 @@ TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, b
     pl.atoms = pl.BN <= kNarrowBN ? 2 : 1;
     stage_bytes = (static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN) * 128 * nB) *
                   pl.atoms;
-#if PE_BN_FOR_OCC2
     // wide enough, but two stages fit a two-CTA share of the SM
     if ((kSmemPerSm / 2 - cta_smem_overhead(true)) / stage_bytes >= 2 || pl.BN <= 64) break;
-#else
-    if (kSmemBudget / stage_bytes >= 3 || pl.BN <= 64) break;
-#endif
   }
   pl.n_tiles = (pl.N_cap + pl.BN - 1) / pl.BN;
   pl.m_tiles = (M + kBM - 1) / kBM;
-  {
-    // 2-SM pairs: the MMA of one thread does twice the work, and an SM stages
-    // half of the token tile, so a deeper ring fits (measured, LM head of
-    // 201088 x 2880 at 448 tokens: see the kernel's comment)
-    const int pair_tiles = (pl.m_tiles + 1) / 2 * pl.n_tiles;
-    const bool use2 = two_sm > 0 ? pl.BN >= 32
-                                 : two_sm < 0 && kTwoSm && pl.BN > kNarrowBN &&
-                                       pair_tiles >= 2 * (num_sms / 2);
-    if (use2) {
-      pl.cta2 = 1;
-      pl.atoms = 1;
-      pl.partial = 0;
-      pl.num_kb = (K + kBK - 1) / kBK;
-      const size_t sb = static_cast<size_t>(kABytes) * nA + static_cast<size_t>(pl.BN / 2) * 128 * nB;
-      // two pairs per SM pair when one accumulator of each fits half the TMEM
-      // and two stages fit half the shared memory: one pair's epilogue then
-      // runs beside the other's MMAs
-      const size_t half = tc_pair_max_dyn_smem(2) - 1024;
-      const bool two = kPairTwoPerSm && pl.BN * nA <= 256 && half / sb >= 2;
-      pl.ctas_per_sm = two ? 2 : 1;
-      pl.stages = two ? std::min(kMaxStages, static_cast<int>(half / sb))
-                      : std::max(2, std::min(kMaxStages, static_cast<int>(kSmemBudget / sb)));
-      pl.smem_bytes = pl.stages * sb + 1024;
-      pl.k_splits = 1;
-      pl.kb_per_split = pl.num_kb;
-      pl.acc_bufs = two ? 1 : (2 * pl.BN * nA <= 512 ? 2 : 1);
-      uint32_t c = 32;
-      while (c < static_cast<uint32_t>(pl.acc_bufs * pl.BN * nA)) c <<= 1;
-      pl.tmem_cols = static_cast<int>(c);
-      // two pairs on each SM pair: as many clusters as SMs (the occupancy
-      // query does not see the TMEM share, the arithmetic above does)
-      const int clusters = two ? num_sms : max_pair_clusters(pl.smem_bytes, 1);
-      pl.grid = 2 * std::max(1, std::min(pair_tiles, clusters));
-      pl.main_tiles = pair_tiles;
-      pl.tail_splits = 1;
-      pl.tail_kb_per_split = pl.num_kb;
-      return pl;
-    }
-  }
   // CTAs per SM: narrow tiles share each SM among several CTAs of at least two
   // stages each (fewer atoms per stage where that is what fits); a stream of at
   // least two full rounds of tiles takes the most
@@ -1366,7 +901,6 @@ static int launch_one(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorM
   a.n_tiles = pl.n_tiles;
   a.m_tiles = pl.m_tiles;
   a.k_splits = k_splits;
-  a.packed = kPackedWeights ? 1 : 0;
   a.k_atoms = (pl.K + kBK - 1) / kBK;
   a.kb_per_split = kb_per_split;
   a.num_kb = pl.num_kb;
@@ -1402,61 +936,12 @@ static int launch_one(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorM
              : PE_ERR_CUDA;
 }
 
-// The 2-SM schedule: clusters of two CTAs over all pair tiles, persistent.
-static int launch_pair(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap* mapA2,
-                       const CUtensorMap& mapB, const CUtensorMap& mapB2, const int* n_rows_dev,
-                       const Epilogue& epi, uint32_t* status, cudaStream_t st) {
-  TcArgs a{};
-  a.M = pl.M;
-  a.K = pl.K;
-  a.N_cap = pl.N_cap;
-  a.dual = pl.dual;
-  a.bpair = pl.bpair;
-  a.tile_base = 0;
-  a.tile_count = pl.main_tiles;
-  a.BN = pl.BN;
-  a.n_tiles = pl.n_tiles;
-  a.m_tiles = pl.m_tiles;
-  a.k_splits = 1;
-  a.packed = kPackedWeights ? 1 : 0;
-  a.k_atoms = (pl.K + kBK - 1) / kBK;
-  a.kb_per_split = pl.num_kb;
-  a.num_kb = pl.num_kb;
-  a.atoms = 1;
-  a.stages = pl.stages;
-  a.acc_bufs = pl.acc_bufs;
-  a.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
-  a.n_rows_dev = n_rows_dev;
-  a.epi = epi;
-  a.status = status;
-  if (epi.mode == EPI_PARTIAL_F32) return PE_ERR_ARG;  // pairs never split K
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.grid);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = pl.smem_bytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, tc_pair_kernel(pl.ctas_per_sm), *mapA, pl.dual ? *mapA2 : *mapA, mapB,
-                            mapB2, a) == cudaSuccess
-             ? PE_OK
-             : PE_ERR_CUDA;
-}
-
 int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap* mapA2,
                    const void* X, const void* X_lo, const int* n_rows_dev, const Epilogue& epi,
                    uint32_t* status, cudaStream_t st) {
   if (pl.dual && !mapA2) return PE_ERR_ARG;
   if (pl.bpair && !X_lo) return PE_ERR_ARG;
-  // a pair stages half of the token tile in each CTA
-  const uint32_t b_box = static_cast<uint32_t>(pl.cta2 ? pl.BN / 2 : pl.BN);
+  const uint32_t b_box = static_cast<uint32_t>(pl.BN);
   CUtensorMap mapB, mapB2;
   if (!encode_tmap_bf16(&mapB, X, static_cast<uint64_t>(pl.N_cap), static_cast<uint64_t>(pl.K),
                         b_box))
@@ -1470,10 +955,6 @@ int launch_gemm_tc(const TcPlan& pl, const CUtensorMap* mapA, const CUtensorMap*
   }
   // one attribute value per instance for every launch, so kernels captured
   // into a graph stay launchable whatever order they replay in
-  if (pl.cta2) {
-    if (tc_pair_prepare(pl.ctas_per_sm) != cudaSuccess) return PE_ERR_CUDA;
-    return launch_pair(pl, mapA, mapA2, mapB, mapB2, n_rows_dev, epi, status, st);
-  }
   if (tc_prepare(pl.ctas_per_sm) != cudaSuccess) return PE_ERR_CUDA;
   const int base = pl.m_tiles * pl.n_tiles;
   if (pl.k_splits > 1)
@@ -1650,7 +1131,6 @@ bool encode_packed_weight_map(CUtensorMap* map, const void* P, int M, int K) {
   return encode_tmap_bf16(map, P, rows, 64, static_cast<uint32_t>(kBM));
 }
 
-bool gemm_weights_packed() { return kPackedWeights; }
 
 int num_sms_of_current_device() {
   int dev = 0, n = 0;

@@ -71,7 +71,6 @@ struct TcPlan {
   int acc_bufs;  // TMEM accumulator buffers (2 = the next tile's MMA overlaps the epilogue)
   int ctas_per_sm;  // resident CTAs per SM the plan is sized for
   int partial;      // K splits store partial sums (else they reduce in a cluster)
-  int cta2;         // 2-SM pairs: clusters of two CTAs run M = 256 MMAs over pair tiles
   int vec;          // wide tiles: the instance whose stores go 4 features at a time
   size_t smem_bytes;
   // unsplit plans with several rounds of tiles: the first main_tiles run
@@ -81,12 +80,10 @@ struct TcPlan {
 
 // partial: the epilogue is EPI_PARTIAL_F32, so splits of K need no cluster (each
 // stores its own partial) and the split count is free of cluster limits.
-// two_sm: 2-SM pairs where they pay (-1: wide token tiles over at least two
-// rounds of pair tiles), always (1, any token tile of 16 rows or more) or never (0).
 // dual: two weight matrices (gate and up) with two accumulators.  bpair: the
 // token rows come as a bf16 pair (hi, lo) whose products add into one accumulator.
 TcPlan plan_gemm_tc(int M, int K, int N_cap, int dual, int bpair, int num_sms, bool allow_split,
-                    bool partial = false, int two_sm = -1);
+                    bool partial = false);
 
 // mapA / mapA2: weight tensor maps (box 64 x 128, 128-byte swizzle).  X: token
 // rows [N_cap][K] bf16 (row stride K).  n_rows_dev: live token rows on device
@@ -117,8 +114,6 @@ size_t packed_weight_bytes(int M, int K);
 int pack_weight(const void* W, int M, int K, void* P, cudaStream_t st);
 // tensor map over a packed weight: [m_tiles * k_atoms * 128 rows][64], box 128 x 64
 bool encode_packed_weight_map(CUtensorMap* map, const void* P, int M, int K);
-// whether the GEMM takes its weights packed (the handle packs them when true)
-bool gemm_weights_packed();
 
 int num_sms_of_current_device();
 

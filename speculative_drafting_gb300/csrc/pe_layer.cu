@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
         }
       }
       if (a.out_f32) a.out_f32[oo + c] = stored;
+      if (a.norm_out) a.norm_out[oo + c] = y;
     }
   };
 #pragma unroll
@@ -309,19 +310,21 @@ int launch_zero_keys(unsigned long long* keys, int n, cudaStream_t st) {
 
 
 __global__ void argmax_finalize_kernel(const unsigned long long* __restrict__ keys, int n,
-                                       int32_t* __restrict__ out) {
+                                       int32_t* __restrict__ out, int stride) {
   pdl_trigger();
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const unsigned long long k = keys[i];
-  out[i] = k ? static_cast<int32_t>(~static_cast<uint32_t>(k & 0xffffffffull)) : 0;
+  out[static_cast<size_t>(i) * stride] =
+      k ? static_cast<int32_t>(~static_cast<uint32_t>(k & 0xffffffffull)) : 0;
 }
 
-int launch_argmax_finalize(const unsigned long long* keys, int n, int32_t* out, cudaStream_t st) {
+int launch_argmax_finalize(const unsigned long long* keys, int n, int32_t* out, cudaStream_t st,
+                           int stride) {
   if (n <= 0) return PE_OK;
-  return launch_pdl(argmax_finalize_kernel, dim3((n + 255) / 256), dim3(256), 0, st, keys, n, out) ==
-                 cudaSuccess
+  return launch_pdl(argmax_finalize_kernel, dim3((n + 255) / 256), dim3(256), 0, st, keys, n, out,
+                    stride) == cudaSuccess
              ? PE_OK
              : PE_ERR_CUDA;
 }

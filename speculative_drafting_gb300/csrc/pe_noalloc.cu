@@ -3,11 +3,10 @@
 // pe_argmax needs a caller-allocated workspace for its per-row argmax keys and
 // status word.  Some callers cannot provide one: a serving engine that has
 // already reserved all device memory for weights and KV cache and hands a
-// plugin only a stream; code that runs while another component captures a CUDA
-// graph, where a cudaMalloc would break the capture; runtimes bound to a fixed
-// memory plan they cannot grow.  pe_argmax_noalloc runs the same LM-head kernel
-// and argmax finalisation with that scratch in a file-scope __device__ array
-// instead, so it allocates nothing.
+// plugin only a stream, or a runtime bound to a fixed memory plan it cannot
+// grow.  pe_argmax_noalloc runs the same LM-head plan and argmax finalisation
+// with that scratch in a file-scope __device__ array instead, so it allocates
+// nothing.
 //
 // The array is global state: every GPU that loads this library holds it
 // (PE_NOALLOC_MAX_ROWS 64-bit keys, 32 KiB) until the process exits.  Every call
@@ -30,7 +29,10 @@ void* g_addr[kMaxDevices] = {};
 
 // Device address of the scratch array for the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached.  The cache assumes one CUDA
+// context per device for the life of the process: after a cudaDeviceReset the
+// cached address would be stale, so a caller that resets a device must not
+// call this entry point on it again.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PE_ERR_CUDA;
@@ -65,8 +67,9 @@ extern "C" int pe_argmax_noalloc(pe_handle* h, const void* z, int n_rows, int32_
   e.logits = logits;
   e.ld_logits = d.vocab;
   if (d.dtype == PE_DTYPE_BF16) {
-    // no split over K: a split would need partial sums the array does not hold
-    const TcPlan p = plan_gemm_tc(d.vocab, d.d, n_rows, 0, 0, handle_num_sms(h), false);
+    // the plan pe_argmax takes: K splits, where the plan makes any, add their
+    // partial tiles inside a thread-block cluster, so they need no global scratch
+    const TcPlan p = plan_gemm_tc(d.vocab, d.d, n_rows, 0, 0, handle_num_sms(h), true);
     rc = launch_gemm_tc(p, handle_lm_map(h), nullptr, z, nullptr, nullptr, e, nullptr, st);
   } else {
     rc = launch_gemm_f32(static_cast<const float*>(handle_w_lm(h)), nullptr,

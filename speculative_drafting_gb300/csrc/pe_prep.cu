@@ -435,6 +435,90 @@ int launch_gather(const GatherArgs& a, int dtype, int num_sms, cudaStream_t st) 
                                 : launch_gather_t<float>(a, num_sms, st);
 }
 
+// ------------------------------------------------------------------ autoregressive pass input
+// Grid (B, 4): CTA (r, s) writes segment s of request r's row; CTA (r, 0) also
+// writes the row's metadata.  The three stream segments normalise the same fp32
+// hidden state (each with its own gain), as the parallel step does with
+// h_shared in a MASK row.
+template <typename T>
+__global__ void __launch_bounds__(128) ar_input_kernel(ArInputArgs a) {
+  __shared__ float red[32];
+  constexpr int V = Elem<T>::kVec;
+  const int r = blockIdx.x, seg = blockIdx.y;
+  const int vd = a.d / V;
+  const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  int t = a.drafts[static_cast<size_t>(r) * a.K + (a.k - 2)];
+  const bool t_ok = t >= 0 && t < a.vocab;
+  if (!t_ok) t = 0;
+  if (seg == 0 && tid == 0) {
+    pe_meta& m = a.meta;
+    const int64_t p = a.pos1[a.sample1[r]] + (a.k - 1);
+    int64_t slot = PE_PADDING_SLOT_ID;
+    const int64_t bi = p >= 0 ? p / a.bs : -1;
+    if (bi >= 0 && bi < a.max_blocks) {
+      const int blk = a.block_table[static_cast<size_t>(r) * a.max_blocks + bi];
+      if (blk >= 0 && blk < a.num_blocks) slot = static_cast<int64_t>(blk) * a.bs + p % a.bs;
+    }
+    if (slot < 0) set_status(a.status, PE_ST_BLOCK_RANGE);
+    if (!t_ok) set_status(a.status, PE_ST_TOKEN_RANGE);
+    m.tok[r] = t;
+    m.pos[r] = p;
+    m.slot[r] = slot;
+    m.is_rejected[r] = 0;
+    m.is_masked[r] = 0;
+    m.hidden_src[r] = -1;
+    m.valid_rows[r] = r;
+    m.sample_idx[r] = r;
+    m.seq_len[r] = static_cast<int32_t>(p + 1);
+    m.out_qsl[r] = r;
+    m.valid_qsl[r] = r;
+    if (r == a.B - 1) {
+      m.out_qsl[a.B] = a.B;
+      m.valid_qsl[a.B] = a.B;
+      *m.n_valid = a.B;
+    }
+  }
+  uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.A) + static_cast<size_t>(r) * 4 * a.d +
+                                        static_cast<size_t>(seg) * a.d);
+  if (seg == 3) {
+    const uint4* src = static_cast<const uint4*>(a.emb) + static_cast<size_t>(t) * vd;
+    for (int i = tid; i < vd; i += blockDim.x) out[i] = src[i];
+    return;
+  }
+  const float* h = a.hidden + static_cast<size_t>(r) * a.d;
+  float ss = 0.f;
+  for (int i = tid; i < a.d / 4; i += blockDim.x) {
+    const float4 f = reinterpret_cast<const float4*>(h)[i];
+    ss = fmaf(f.x, f.x, ss);
+    ss = fmaf(f.y, f.y, ss);
+    ss = fmaf(f.z, f.z, ss);
+    ss = fmaf(f.w, f.w, ss);
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(a.d) + a.eps);
+  const uint4* gam = static_cast<const uint4*>(a.gamma_stream) + static_cast<size_t>(seg) * vd;
+  for (int i = tid; i < vd; i += blockDim.x) {
+    float f[V], gf[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) f[k] = h[i * V + k];
+    unpack16<T>(gam[i], gf);
+#pragma unroll
+    for (int k = 0; k < V; ++k) f[k] = f[k] * inv * gf[k];
+    out[i] = pack16<T>(f);
+  }
+}
+
+int launch_ar_input(const ArInputArgs& a, int dtype, cudaStream_t st) {
+  if (a.B <= 0) return PE_OK;
+  dim3 grid(a.B, 4);
+  const cudaError_t e = dtype == PE_DTYPE_BF16
+                            ? launch_pdl(ar_input_kernel<bf16>, grid, dim3(128), 0, st, a)
+                            : launch_pdl(ar_input_kernel<float>, grid, dim3(128), 0, st, a);
+  return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
+}
+
 int launch_input(const InputArgs& a, int dtype, cudaStream_t st) {
   if (a.T_out <= 0) return PE_OK;
   dim3 grid(a.T_out, 4);

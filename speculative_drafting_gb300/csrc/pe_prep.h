@@ -58,6 +58,30 @@ struct InputArgs {
 };
 int launch_input(const InputArgs& a, int dtype, cudaStream_t st);
 
+// ---------------------------------------------------------------- autoregressive pass input
+// Pass k >= 2 of the autoregressive K-pass drafting: one row per request at
+// position pos0[r] + k - 1, where pos0[r] = pos1[sample1[r]] is the NTP row's
+// position of pass 1.  Its drafter input is [RMSNorm(h)*g0, RMSNorm(h)*g1,
+// RMSNorm(h)*g2, emb(t)] with h = hidden[r] (the drafter's own hidden state of
+// the previous pass, fp32) and t = drafts[r * K + k - 2]; its metadata (one
+// non-rejected row per request, which is also its sample row) goes into meta.
+struct ArInputArgs {
+  int B, K, k, d, vocab, bs, max_blocks, num_blocks;
+  float eps;
+  const int64_t* pos1;       // pass 1's row positions
+  const int32_t* sample1;    // pass 1's sample row of each request (the NTP row)
+  const int32_t* drafts;     // [B][K] draft tokens of the passes so far
+  const float* hidden;       // [B][d]
+  const int32_t* block_table;
+  const void* emb;
+  const void* gamma_stream;
+  pe_meta meta;              // out: B rows (tok, pos, slot, valid_qsl, valid_rows,
+                             // n_valid, sample_idx, seq_len, out_qsl, flags)
+  void* A;                   // out: [B][4d]
+  uint32_t* status;
+};
+int launch_ar_input(const ArInputArgs& a, int dtype, cudaStream_t st);
+
 // ---------------------------------------------------------------- row RMSNorm
 // y[i] = x[i] * gamma / sqrt(mean(x[i]^2) + eps) (apply_norm) or x[i], for rows
 // i < n_rows, where x = (sum of n_parts partial tiles, in order) + resid, stored
@@ -71,6 +95,7 @@ struct RowNormArgs {
   const float* resid;  // nullable, [rows][ld_resid]
   int ld_resid;
   float* sum_out;  // nullable, [rows][ld_x]
+  float* norm_out; // nullable, [rows][ld_out]: the normalised value before rounding
   const void* gamma;
   int apply_norm;
   void* out;
@@ -146,8 +171,9 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st);
 // ---------------------------------------------------------------- argmax keys
 // keys[0..n) = 0 (a kernel, so the LM head that follows can start early)
 int launch_zero_keys(unsigned long long* keys, int n, cudaStream_t st);
-// keys -> ids
-int launch_argmax_finalize(const unsigned long long* keys, int n, int32_t* out, cudaStream_t st);
+// keys -> ids: out[i * stride] for i < n
+int launch_argmax_finalize(const unsigned long long* keys, int n, int32_t* out, cudaStream_t st,
+                           int stride = 1);
 
 // ---------------------------------------------------------------- bounded-wait check
 // one kernel whose bounded wait can never be satisfied: it records PE_ST_TIMEOUT

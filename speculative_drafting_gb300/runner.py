@@ -91,6 +91,16 @@ class StepRunner:
         self.step(stream)
         self.argmax(stream)
 
+    def autoregressive(self, draft, ws, logits=None, hidden=None, stream=None):
+        """The K-pass autoregressive drafting of the same batch (the baseline):
+        draft [B][K] int32, ws from Drafter.autoregressive_workspace; optional
+        logits [B][K][V] and per-pass hidden states [B][K][d] (fp32)."""
+        i = self.inp
+        self.drafter.draft_autoregressive(self.B, self.T_in, i["qsl"], i["prev_tok"], i["prev_pos"],
+                                          i["accepted"], i["bonus"], i["block_table"],
+                                          self.num_blocks, i["H_tgt"], self.k_cache, self.v_cache,
+                                          draft, ws, logits=logits, hidden=hidden, stream=stream)
+
     def status(self, clear=True):
         return self.drafter.read_status(self.ws, clear=clear)
 

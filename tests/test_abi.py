@@ -59,6 +59,51 @@ def test_host_argument_checks(lib):
     assert lib.pe_argmax(None, None, 1, None, None, None, 0, None) == binding.PE_ERR_ARG
 
 
+def test_packed_weights_host_checks(lib):
+    """The tile-packed weight copy: its size from the dims alone, and a bf16
+    handle with a layer refused without it (answered on the host)."""
+    gpt = binding.PeDims(d=2880, n_streams=3, n_heads=64, n_kv_heads=8, head_dim=64, inter=7680,
+                         vocab=201088, K=7, block_size=16, mask_id=0, post_norm=0,
+                         dtype=binding.PE_DTYPE_BF16, eps=1e-6, rope_theta=1e4, n_layers=1)
+
+    def packed(M, K):  # blocks of 128 rows x 64 columns of 2-byte elements, 256-aligned
+        b = -(-M // 128) * -(-K // 64) * 128 * 64 * 2
+        return -(-b // 256) * 256
+
+    d, H, G, hd, I, V = 2880, 64, 8, 64, 7680, 201088
+    one = (packed(d, 4 * d) + packed((H + 2 * G) * hd, d) + packed(d, H * hd) + 2 * packed(I, d)
+           + packed(d, I) + packed(V, d))
+    assert lib.pe_packed_weights_bytes(ctypes.byref(gpt)) == one
+    four = binding.PeDims.from_buffer_copy(gpt)
+    four.n_layers = 4
+    per_layer = packed((H + 2 * G) * hd, d) + packed(d, H * hd) + 2 * packed(I, d) + packed(d, I)
+    assert lib.pe_packed_weights_bytes(ctypes.byref(four)) == one + 3 * per_layer
+    f32 = binding.PeDims.from_buffer_copy(gpt)
+    f32.dtype = binding.PE_DTYPE_F32
+    assert lib.pe_packed_weights_bytes(ctypes.byref(f32)) == 0
+    assert lib.pe_packed_weights_bytes(None) == 0
+    # fake, never dereferenced device addresses: every case fails on the host
+    fake = [ctypes.c_void_p((1 << 30) + 256 * i) for i in range(len(binding.WEIGHT_FIELDS))]
+    w = binding.PeWeights(**{k: fake[i] for i, k in enumerate(binding.WEIGHT_FIELDS)})
+    w.attn_sink = None
+    h = ctypes.c_void_p()
+    assert lib.pe_create(ctypes.byref(gpt), ctypes.byref(w), ctypes.byref(h)) == binding.PE_ERR_ARG
+    w.packed, w.packed_bytes = ctypes.c_void_p(1 << 40), one - 1          # too small
+    assert lib.pe_create(ctypes.byref(gpt), ctypes.byref(w), ctypes.byref(h)) == binding.PE_ERR_ARG
+    w.packed, w.packed_bytes = ctypes.c_void_p((1 << 40) + 128), one      # misaligned
+    assert lib.pe_create(ctypes.byref(gpt), ctypes.byref(w), ctypes.byref(h)) == binding.PE_ERR_ARG
+    assert not h.value
+    pack = lib.pe_pack_weights
+    assert pack(ctypes.byref(f32), ctypes.byref(w), ctypes.c_void_p(1 << 40), one, None) == \
+        binding.PE_ERR_UNSUPPORTED
+    assert pack(ctypes.byref(gpt), ctypes.byref(w), None, one, None) == binding.PE_ERR_ARG
+    assert pack(ctypes.byref(gpt), ctypes.byref(w), ctypes.c_void_p(1 << 40), one - 1, None) == \
+        binding.PE_ERR_ARG
+    w.w_lm = None
+    assert pack(ctypes.byref(gpt), ctypes.byref(w), ctypes.c_void_p(1 << 40), one, None) == \
+        binding.PE_ERR_ARG
+
+
 def test_verify_host_checks(lib):
     # 256-byte header, then one 8-byte key per (row, 1024-element chunk)
     assert lib.pe_verify_workspace_bytes(512, 201088) == 256 + 512 * 197 * 8

@@ -150,69 +150,25 @@ def test_projection_partial_sums(name, which, n, pair):
     assert np.all(err <= tol), f"max err {err.max():.3g}"
 
 
-TWO_SM, ONE_SM, ARGMAX = 0x800, 0x1000, 0x2000  # pe_testing.h
-
-
-@pytest.mark.parametrize("name", ["small_prenorm", "small_postnorm_hd128"])
-@pytest.mark.parametrize("which", list(PROJ))
-@pytest.mark.parametrize("n", [32, 100, 300, 448, 513])
-@pytest.mark.parametrize("pair", [False, True])
-def test_projection_two_sm(name, which, n, pair):
-    """The 2-SM schedule (clusters of two CTAs, M = 256 MMAs, each CTA staging
-    half of the token tile): odd weight-tile counts leave rank 1 of the last
-    pair past the weights; ragged token tiles; dual (SwiGLU) and bf16-pair
-    operands."""
-    torch = cuda_or_skip()
-    wl, b, w, kc, vc, r = setup(name, want_logits=False, kv=False)
-    M, Kd, wname = _shape(wl.dims, which)
-    from speculative_drafting_gb300.workloads import f32_to_bf16_bits
-    g = np.random.default_rng(n * 43 + PROJ[which] + 5 * pair)
-    X = g.standard_normal((n, Kd)).astype(np.float32)
-    hi = f32_to_bf16_bits(X)
-    x64 = f64(hi, "bf16")
-    Xh = hi
-    if pair:
-        lo = f32_to_bf16_bits((X.astype(np.float64) - x64).astype(np.float32))
-        x64 = x64 + f64(lo, "bf16")
-        Xh = np.concatenate([hi, lo], axis=0)
-    Xd = runner.to_device(Xh, "bf16")
-    out_dt = torch.bfloat16 if which == "swiglu" else torch.float32
-    out = torch.full((n, M), float("nan"), dtype=out_dt, device="cuda")
-    ws = r.drafter.test_projection(PROJ[which] | TWO_SM | (PAIR if pair else 0), Xd, n, out)
-    torch.cuda.synchronize()
-    st, _ = r.drafter.read_status(ws)
-    assert st == 0, hex(st)
-    if which == "swiglu":
-        ref = O.bf16_round(O.silu(O.linear(x64, f64(w["w_gate"], "bf16"))) *
-                           O.linear(x64, f64(w["w_up"], "bf16")))
-        got = f64(host(out), "bf16")
-        tol = 2 ** -7 * np.abs(ref) + 1e-6
-    else:
-        ref = O.linear(x64, f64(w[wname], "bf16"))
-        got = host(out).astype(np.float64)
-        tol = 1e-5 * np.sqrt(Kd) * 0.02 * 4 + 1e-5 * np.abs(ref)
-    assert np.all(np.isfinite(got))
-    err = np.abs(got - ref)
-    assert np.all(err <= tol), f"max err {err.max():.3g}"
+ARGMAX = 0x2000  # pe_testing.h
 
 
 @pytest.mark.parametrize("name", ["small_prenorm", "small_postnorm_hd128"])
 @pytest.mark.parametrize("n", [1, 7, 100, 300, 448, 513])
-@pytest.mark.parametrize("sched", [ONE_SM, TWO_SM])
-def test_lm_head_argmax_schedules(name, n, sched):
-    """The LM head with its argmax epilogue on either schedule: the logits match
-    the float64 product, each row's index is the first maximum of the logits the
-    kernel produced, and it is the float64 argmax wherever the top two logits
-    are apart by more than the accumulation error."""
+def test_lm_head_argmax(name, n):
+    """The LM head with its argmax epilogue: the logits match the float64
+    product, each row's index is the first maximum of the logits the kernel
+    produced, and it is the float64 argmax wherever the top two logits are apart
+    by more than the accumulation error."""
     torch = cuda_or_skip()
     wl, b, w, kc, vc, r = setup(name, want_logits=False, kv=False)
     M, Kd, wname = _shape(wl.dims, "lm")
     from speculative_drafting_gb300.workloads import f32_to_bf16_bits
-    g = np.random.default_rng(n * 47 + sched)
+    g = np.random.default_rng(n * 47)
     hi = f32_to_bf16_bits(g.standard_normal((n, Kd)).astype(np.float32))
     Xd = runner.to_device(hi, "bf16")
     out = torch.full((n, M), float("nan"), dtype=torch.float32, device="cuda")
-    ws = r.drafter.test_projection(PROJ["lm"] | ARGMAX | sched, Xd, n, out)
+    ws = r.drafter.test_projection(PROJ["lm"] | ARGMAX, Xd, n, out)
     torch.cuda.synchronize()
     st, _ = r.drafter.read_status(ws)
     assert st == 0, hex(st)
@@ -226,3 +182,37 @@ def test_lm_head_argmax_schedules(name, n, sched):
     top2 = np.sort(ref, axis=1)[:, -2:]
     clear = top2[:, 1] - top2[:, 0] > 2 * tol.max()
     np.testing.assert_array_equal(tok[clear], ref.argmax(axis=1)[clear])
+
+
+def test_gemms_read_the_callers_packed_copy():
+    """A bf16 handle's GEMMs read the caller's tile-packed buffer: packing the
+    negated matrices into it (pe_pack_weights, no new handle) negates every
+    projection, and writing the row-major matrices afterwards changes nothing."""
+    torch = cuda_or_skip()
+    import ctypes
+
+    from speculative_drafting_gb300 import binding
+    wl, b, w, kc, vc, r = setup("small_prenorm", want_logits=False, kv=False)
+    dm = wl.dims
+    n = 40
+    from speculative_drafting_gb300.workloads import f32_to_bf16_bits
+    X = runner.to_device(f32_to_bf16_bits(
+        np.random.default_rng(3).standard_normal((n, 4 * dm.d)).astype(np.float32)), "bf16")
+    out = torch.empty(n, dm.d, dtype=torch.float32, device="cuda")
+    r.drafter.test_projection(PROJ["fc"], X, n, out)
+    torch.cuda.synchronize()
+    first = out.clone()
+    neg = {k: -t for k, t in r.w.items() if k.startswith("w_")}
+    cw = binding.PeWeights.from_buffer_copy(r.drafter.cw)
+    for k, t in neg.items():
+        setattr(cw, k, t.data_ptr())
+    r.drafter.pack(weights=cw)
+    torch.cuda.synchronize()
+    r.drafter.test_projection(PROJ["fc"], X, n, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, -first)
+    # the row-major matrices are not what the kernels read
+    r.w["w_fc"].zero_()
+    r.drafter.test_projection(PROJ["fc"], X, n, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, -first)
