@@ -929,6 +929,15 @@ int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl, const i
     ia.gamma_stream = h->w.gamma_stream;
     ia.A = A_out;
     ia.status = status;
+    // small batches: the input kernel indexes its rows itself and runs beside
+    // the metadata kernel (no gather kernel between them)
+    ia.self_index = (B <= kSelfIndexMaxBatch && !(G_out || E_out)) ? 1 : 0;
+    ia.B = B;
+    ia.K = d.K;
+    ia.qsl = qsl;
+    ia.prev_tok = prev_tok;
+    ia.accepted = accepted;
+    ia.bonus = bonus;
     rc = launch_input(ia, d.dtype, st);
     if (rc != PE_OK) return rc;
   }

@@ -33,7 +33,11 @@ constexpr size_t kSmemBudget = 212 * 1024;  // dynamic shared memory for the sta
 // and deep prefetches delayed them (measured, step at B=1: 16 k-blocks 328 us,
 // 4: 303 us, 2: 301 us, none: 306 us).
 constexpr int kPrefetchKb = 2;
-constexpr int kMaxClusterSplits = 8;        // portable cluster size
+// K splits of one tile that reduce in a cluster: up to 16 (a non-portable
+// cluster size, allowed per kernel).  Decode-sized projections have few weight
+// tiles (fc, O and down of the GPT-OSS shape: 23) and need many splits each to
+// give every SM several CTAs' worth of weight stream.
+constexpr int kMaxClusterSplits = 16;
 constexpr int kMaxPartialSplits = 16;       // splits storing their own partials
 static_assert(kMaxPartialSplits <= 16, "the projection test hook holds 16 partial tiles");
 // Weights are read in tile order (one contiguous 16 KB block per weight box;
@@ -718,8 +722,10 @@ static cudaError_t tc_prepare(int occ) {
   for (const bool vec : {false, true}) {
     if (vec && occ > 2) continue;
     const TcKernelFn k = tc_kernel(occ, vec);
-    const cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(tc_max_dyn_smem(occ, vec)));
+    cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(tc_max_dyn_smem(occ, vec)));
+    if (r != cudaSuccess) e = r;
+    r = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (r != cudaSuccess) e = r;
     cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                          cudaSharedmemCarveoutMaxShared);

@@ -67,8 +67,11 @@ __global__ void __launch_bounds__(256) meta_kernel(const MetaArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nw = blockDim.x >> 5;
   const int r_begin = blockIdx.x * nw, r_end = min(a.B, r_begin + nw);
-  pdl_trigger();
+  // the batch's inputs may come from the kernel before (the verification):
+  // wait for it, and only then let the next kernel start, so that it may read
+  // the same inputs without waiting for this kernel
   pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     carry_o = 0;
     carry_v = 0;
@@ -314,6 +317,65 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
 // 4 * 128 * 8 bf16 = 4096 elements; longer rows read the rest twice).
 constexpr int kInputVecs = 4;
 
+// Warp 0 of an input CTA: the request, hidden source and token of non-rejected
+// row v, from the verify batch itself.  The per-request counts take the metadata
+// kernel's clamps (request_counts), so row v is the one that kernel lists at
+// valid_rows[v]: request r's copied rows 0..a_r, then its K-1 MASK rows.
+// out[0] = 1 when v exists; out[1] = hidden source (-1: h_shared), out[2] =
+// token, out[3] = 1 for a MASK row.
+PE_DEV void locate_valid_row(const InputArgs& a, int v, int* out) {
+  const int lane = threadIdx.x & 31;
+  int base = 0, found = 0, hsrc = -1, tok = 0, masked = 1;
+  for (int r0 = 0; r0 < a.B; r0 += 32) {
+    const int r = r0 + lane;
+    int q0 = 0, n = 0, acc = 0, c = 0;
+    if (r < a.B) {
+      q0 = a.qsl[r];
+      int q1 = a.qsl[r + 1];
+      if (q0 < 0 || q1 > a.T_in || q1 < q0) {
+        q0 = min(max(q0, 0), a.T_in);
+        q1 = min(max(q1, q0), a.T_in);
+      }
+      n = q1 - q0;
+      acc = a.accepted[r];
+      if (n < 1 || acc < 0 || acc > n - 1) acc = min(max(acc, 0), max(n - 1, 0));
+      c = (n >= 1 ? acc + 1 : 0) + a.K - 1;
+    }
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    const int start = base + incl - c;
+    const bool hit = r < a.B && v >= start && v < start + c;
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (hit) {
+      const int j = v - start;
+      if (n >= 1 && j <= acc) {
+        hsrc = q0 + j;
+        tok = (j == acc || j == n - 1) ? a.bonus[r] : a.prev_tok[q0 + j + 1];
+        masked = 0;
+      }
+    }
+    if (m) {
+      const int src = __ffs(static_cast<int>(m)) - 1;
+      hsrc = __shfl_sync(0xffffffffu, hsrc, src);
+      tok = __shfl_sync(0xffffffffu, tok, src);
+      masked = __shfl_sync(0xffffffffu, masked, src);
+      found = 1;
+      break;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    out[0] = found && v < a.T_out;
+    out[1] = hsrc;
+    out[2] = tok;
+    out[3] = masked;
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
   __shared__ float red[32];
@@ -332,22 +394,41 @@ __global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
     }
   }
   pdl_trigger();
-  pdl_wait();
-  const int nv = min(max(*a.n_valid, 0), a.T_out);
-  if (v >= nv) return;
-  const int o = a.valid_rows[v];
-  if (o < 0 || o >= a.T_out) {
-    if (tid == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
-    return;
+  int hsrc, tok, masked;
+  if (a.self_index) {
+    // the metadata kernel let this kernel start after its own dependency wait:
+    // the verify batch is final, and its outputs are not needed
+    __shared__ int row_sh[4];
+    if (tid < 32) locate_valid_row(a, v, row_sh);
+    __syncthreads();
+    if (!row_sh[0]) {
+      pdl_wait();
+      return;
+    }
+    hsrc = row_sh[1];
+    tok = row_sh[2];
+    masked = row_sh[3];
+  } else {
+    pdl_wait();
+    const int nv = min(max(*a.n_valid, 0), a.T_out);
+    if (v >= nv) return;
+    const int o = a.valid_rows[v];
+    if (o < 0 || o >= a.T_out) {
+      if (tid == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
+      return;
+    }
+    hsrc = a.hidden_src[o];
+    tok = a.tok[o];
+    masked = a.is_masked[o];
   }
   uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.A) + static_cast<size_t>(v) * 4 * a.d +
                                         static_cast<size_t>(seg) * a.d);
   if (seg == 3) {
     const uint4* src;
-    if (a.is_masked[o]) {
+    if (masked) {
       src = static_cast<const uint4*>(a.emb_mask);
     } else {
-      int t = a.tok[o];
+      int t = tok;
       if (t < 0 || t >= a.vocab) {
         if (tid == 0) set_status(a.status, PE_ST_TOKEN_RANGE);
         t = 0;
@@ -355,9 +436,11 @@ __global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
       src = static_cast<const uint4*>(a.emb) + static_cast<size_t>(t) * vd;
     }
     for (int i = tid; i < vd; i += blockDim.x) out[i] = src[i];
+    // (self-indexed) this kernel completes only after the metadata kernel, so
+    // the kernels after it see both
+    if (a.self_index) pdl_wait();
     return;
   }
-  const int hsrc = a.hidden_src[o];
   const uint4* src;
   if (hsrc < 0) {
     src = static_cast<const uint4*>(a.h_shared);
@@ -415,6 +498,7 @@ __global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
     for (int k = 0; k < V; ++k) f[k] = f[k] * inv * gf[k];
     out[i] = pack16<T>(f);
   }
+  if (a.self_index) pdl_wait();
 }
 
 template <typename T>

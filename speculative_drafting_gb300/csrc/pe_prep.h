@@ -22,6 +22,8 @@ struct MetaLaunch {
   uint32_t* status;
 };
 int launch_meta(const MetaLaunch& L, cudaStream_t st);
+// Largest batch for which the drafter-input kernel indexes its rows itself.
+constexpr int kSelfIndexMaxBatch = 256;
 
 // ---------------------------------------------------------------- (2) hidden-state map
 struct GatherArgs {
@@ -43,6 +45,16 @@ int launch_gather(const GatherArgs& a, int dtype, int num_sms, cudaStream_t st);
 struct InputArgs {
   int T_out, T_in, d, vocab;
   float eps;
+  // self_index: each CTA finds its row's request, hidden source and token from
+  // the verify batch itself (B, K, qsl, prev_tok, accepted, bonus), with the
+  // same clamps as the metadata kernel, instead of waiting for that kernel's
+  // outputs; the two kernels then run side by side.  Small batches only (every
+  // CTA scans all B requests).
+  int self_index, B, K;
+  const int32_t* qsl;
+  const int32_t* prev_tok;
+  const int32_t* accepted;
+  const int32_t* bonus;
   const int32_t* n_valid;
   const int32_t* valid_rows;
   const int32_t* hidden_src;
