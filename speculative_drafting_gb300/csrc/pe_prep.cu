@@ -312,10 +312,14 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
 
 // A[v] = [RMSNorm(G0) g0, RMSNorm(G1) g1, RMSNorm(G2) g2, E] for non-rejected row
 // v (output row valid_rows[v]), straight from H_tgt / h_shared / the embedding.
-// blockIdx.x = v, blockIdx.y = segment (0..2 streams, 3 embedding).
-// Vectors of a stream segment each thread keeps in registers (rows of up to
-// 4 * 128 * 8 bf16 = 4096 elements; longer rows read the rest twice).
-constexpr int kInputVecs = 4;
+// One CTA of 8 warps per row: warps 2s and 2s+1 write segment s (0..2 the
+// streams, 3 the embedding), so a row's four segments load together and a
+// wave of CTAs covers hundreds of rows.  Each thread keeps up to kInputVecs
+// vectors of its segment in registers (segments of up to 8 * 64 * 8 = 4096 bf16
+// elements; longer ones read the rest twice).
+constexpr int kInputVecs = 8;
+constexpr int kInputThreads = 256;
+constexpr int kSegThreads = 64;
 
 // Warp 0 of an input CTA: the request, hidden source and token of non-rejected
 // row v, from the verify batch itself.  The per-request counts take the metadata
@@ -377,127 +381,137 @@ PE_DEV void locate_valid_row(const InputArgs& a, int v, int* out) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(128) input_kernel(InputArgs a) {
-  __shared__ float red[32];
+__global__ void __launch_bounds__(kInputThreads) input_kernel(InputArgs a) {
+  __shared__ float red[4][2];
+  __shared__ int row_sh[4];
   constexpr int V = Elem<T>::kVec;
-  const int v = blockIdx.x, seg = blockIdx.y;
+  const int v = blockIdx.x;
   const int vd = a.d / V;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seg = warp >> 1;
+  const int st = tid & (kSegThreads - 1);  // thread within the segment
   // the gains are weights, independent of the kernels before: read them first
   uint4 g[kInputVecs];
+  const uint4* gam = static_cast<const uint4*>(a.gamma_stream) + static_cast<size_t>(seg) * vd;
   if (seg < 3) {
-    const uint4* gam = static_cast<const uint4*>(a.gamma_stream) + static_cast<size_t>(seg) * vd;
 #pragma unroll
     for (int c = 0; c < kInputVecs; ++c) {
-      const int i = tid + c * 128;
+      const int i = st + c * kSegThreads;
       if (i < vd) g[c] = gam[i];
     }
   }
   pdl_trigger();
-  int hsrc, tok, masked;
   if (a.self_index) {
     // the metadata kernel let this kernel start after its own dependency wait:
     // the verify batch is final, and its outputs are not needed
-    __shared__ int row_sh[4];
-    if (tid < 32) locate_valid_row(a, v, row_sh);
-    __syncthreads();
-    if (!row_sh[0]) {
-      pdl_wait();
-      return;
-    }
-    hsrc = row_sh[1];
-    tok = row_sh[2];
-    masked = row_sh[3];
-  } else {
+    if (warp == 0) locate_valid_row(a, v, row_sh);
+  } else if (tid == 0) {
     pdl_wait();
     const int nv = min(max(*a.n_valid, 0), a.T_out);
-    if (v >= nv) return;
-    const int o = a.valid_rows[v];
-    if (o < 0 || o >= a.T_out) {
-      if (tid == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
-      return;
+    int ok = v < nv;
+    int o = ok ? a.valid_rows[v] : -1;
+    if (ok && (o < 0 || o >= a.T_out)) {
+      set_status(a.status, PE_ST_ACCEPTED_RANGE);
+      ok = 0;
     }
-    hsrc = a.hidden_src[o];
-    tok = a.tok[o];
-    masked = a.is_masked[o];
+    row_sh[0] = ok;
+    if (ok) {
+      row_sh[1] = a.hidden_src[o];
+      row_sh[2] = a.tok[o];
+      row_sh[3] = a.is_masked[o];
+    }
   }
+  __syncthreads();
+  if (!row_sh[0]) {
+    if (a.self_index) pdl_wait();
+    return;
+  }
+  const int hsrc = row_sh[1], tok = row_sh[2], masked = row_sh[3];
   uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.A) + static_cast<size_t>(v) * 4 * a.d +
                                         static_cast<size_t>(seg) * a.d);
+  const uint4* src;
   if (seg == 3) {
-    const uint4* src;
     if (masked) {
       src = static_cast<const uint4*>(a.emb_mask);
     } else {
       int t = tok;
       if (t < 0 || t >= a.vocab) {
-        if (tid == 0) set_status(a.status, PE_ST_TOKEN_RANGE);
+        if (st == 0) set_status(a.status, PE_ST_TOKEN_RANGE);
         t = 0;
       }
       src = static_cast<const uint4*>(a.emb) + static_cast<size_t>(t) * vd;
     }
-    for (int i = tid; i < vd; i += blockDim.x) out[i] = src[i];
-    // (self-indexed) this kernel completes only after the metadata kernel, so
-    // the kernels after it see both
-    if (a.self_index) pdl_wait();
-    return;
-  }
-  const uint4* src;
-  if (hsrc < 0) {
+  } else if (hsrc < 0) {
     src = static_cast<const uint4*>(a.h_shared);
   } else if (hsrc < a.T_in) {
     src = static_cast<const uint4*>(a.H_tgt) + (static_cast<size_t>(hsrc) * 3 + seg) * vd;
   } else {
-    if (tid == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
+    if (st == 0) set_status(a.status, PE_ST_ACCEPTED_RANGE);
     src = static_cast<const uint4*>(a.h_shared);
   }
-  // the row's vectors i = tid, tid + 128, ...: the first kInputVecs stay in
-  // registers (all loads in flight together), in the same summation order as a
-  // plain loop over i
+  // the segment's vectors i = st, st + 64, ...: the first kInputVecs stay in
+  // registers (all loads in flight together), summed in that order
   uint4 x[kInputVecs];
 #pragma unroll
   for (int c = 0; c < kInputVecs; ++c) {
-    const int i = tid + c * 128;
+    const int i = st + c * kSegThreads;
     if (i < vd) x[c] = src[i];
   }
   float ss = 0.f;
+  if (seg < 3) {
 #pragma unroll
-  for (int c = 0; c < kInputVecs; ++c) {
-    if (tid + c * 128 < vd) {
+    for (int c = 0; c < kInputVecs; ++c) {
+      if (st + c * kSegThreads < vd) {
+        float f[V];
+        unpack16<T>(x[c], f);
+#pragma unroll
+        for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
+      }
+    }
+    for (int i = st + kInputVecs * kSegThreads; i < vd; i += kSegThreads) {
       float f[V];
-      unpack16<T>(x[c], f);
+      unpack16<T>(src[i], f);
 #pragma unroll
       for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
     }
   }
-  for (int i = tid + kInputVecs * 128; i < vd; i += 128) {
-    float f[V];
-    unpack16<T>(src[i], f);
+  // the segment's sum of squares: its two warps, then across them
+  ss = warp_sum(ss);
+  if (lane == 0) red[seg][warp & 1] = ss;
+  __syncthreads();
+  if (seg == 3) {
+    // the embedding row (or emb(mask)) is copied as it is
 #pragma unroll
-    for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
-  }
-  ss = block_sum(ss, red);
-  const float inv = 1.0f / sqrtf(ss / static_cast<float>(a.d) + a.eps);
+    for (int c = 0; c < kInputVecs; ++c) {
+      const int i = st + c * kSegThreads;
+      if (i < vd) out[i] = x[c];
+    }
+    for (int i = st + kInputVecs * kSegThreads; i < vd; i += kSegThreads) out[i] = src[i];
+  } else {
+    const float inv = 1.0f / sqrtf((red[seg][0] + red[seg][1]) / static_cast<float>(a.d) + a.eps);
 #pragma unroll
-  for (int c = 0; c < kInputVecs; ++c) {
-    const int i = tid + c * 128;
-    if (i < vd) {
+    for (int c = 0; c < kInputVecs; ++c) {
+      const int i = st + c * kSegThreads;
+      if (i < vd) {
+        float f[V], gf[V];
+        unpack16<T>(x[c], f);
+        unpack16<T>(g[c], gf);
+#pragma unroll
+        for (int k = 0; k < V; ++k) f[k] = f[k] * inv * gf[k];
+        out[i] = pack16<T>(f);
+      }
+    }
+    for (int i = st + kInputVecs * kSegThreads; i < vd; i += kSegThreads) {
       float f[V], gf[V];
-      unpack16<T>(x[c], f);
-      unpack16<T>(g[c], gf);
+      unpack16<T>(src[i], f);
+      unpack16<T>(gam[i], gf);
 #pragma unroll
       for (int k = 0; k < V; ++k) f[k] = f[k] * inv * gf[k];
       out[i] = pack16<T>(f);
     }
   }
-  const uint4* gam = static_cast<const uint4*>(a.gamma_stream) + static_cast<size_t>(seg) * vd;
-  for (int i = tid + kInputVecs * 128; i < vd; i += 128) {
-    float f[V], gf[V];
-    unpack16<T>(src[i], f);
-    unpack16<T>(gam[i], gf);
-#pragma unroll
-    for (int k = 0; k < V; ++k) f[k] = f[k] * inv * gf[k];
-    out[i] = pack16<T>(f);
-  }
+  // (self-indexed) this kernel completes only after the metadata kernel, so
+  // the kernels after it see both
   if (a.self_index) pdl_wait();
 }
 
@@ -605,10 +619,10 @@ int launch_ar_input(const ArInputArgs& a, int dtype, cudaStream_t st) {
 
 int launch_input(const InputArgs& a, int dtype, cudaStream_t st) {
   if (a.T_out <= 0) return PE_OK;
-  dim3 grid(a.T_out, 4);
+  dim3 grid(a.T_out);
   const cudaError_t e = dtype == PE_DTYPE_BF16
-                            ? launch_pdl(input_kernel<bf16>, grid, dim3(128), 0, st, a)
-                            : launch_pdl(input_kernel<float>, grid, dim3(128), 0, st, a);
+                            ? launch_pdl(input_kernel<bf16>, grid, dim3(kInputThreads), 0, st, a)
+                            : launch_pdl(input_kernel<float>, grid, dim3(kInputThreads), 0, st, a);
   return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 
