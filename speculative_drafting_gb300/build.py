@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libpe.so")
 
 SOURCES = ["pe_api.cu", "pe_gemm.cu", "pe_prep.cu", "pe_layer.cu", "pe_attn.cu", "pe_noalloc.cu",
-           "pe_verify.cu", "pe_cod.cu", "pe_cod_mask.cu"]
+           "pe_verify.cu", "pe_cod.cu", "pe_cod_mask.cu", "pe_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-I", INCLUDE, "-I", CSRC]

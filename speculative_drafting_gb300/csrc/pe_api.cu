@@ -172,8 +172,13 @@ struct Layout {
   size_t status, x, u, u_lo, q_s, x_s, attn, r, a, a_lo, a_f, h, h_lo, part, amax, attn_part, tok;
   // several layers: a later layer's input, fp32 (xl) and as its QKV operand (ul, ul_lo)
   size_t xl, ul, ul_lo;
+  size_t dec;  // persistent decode layer: partial tiles and operands
   size_t total;
 };
+
+// Barrier words of the persistent decode layer: in the workspace header, after
+// the status word (the header's 256 bytes are cleared together).
+constexpr size_t kBarrierWordsOffset = 64;
 
 // Workspace layout of a step with B requests, T_in verify rows and block tables
 // of max_blocks entries.  Each region is sized by a bound that only grows with
@@ -220,9 +225,10 @@ Layout layout_of(const pe_handle* h, int B, int T_in, int max_blocks, int K_draf
     L.ul = take(static_cast<size_t>(NS) * d.d * f4);
     L.ul_lo = take(static_cast<size_t>(NS) * d.d * e);
   }
-  (void)QKV;
   L.amax = take(static_cast<size_t>(NS) * sizeof(unsigned long long));
   L.attn_part = take(attn_scratch_bound(h, B, max_blocks, rows));
+  if (is_bf16(h) && h->n_layers <= 1 && decode_layer_fits(d.d, QKV, d.inter, h->num_sms))
+    L.dec = take(decode_scratch_bytes(d.d, QKV, d.inter, h->num_sms));
   L.total = off;
   return L;
 }
@@ -415,6 +421,95 @@ int fc_step(const StepCtx& c, int T_out, const pe_meta* meta, const void* A) {
                    h->d.post_norm ? 0 : 1, c.u, c.u_lo, nullptr, T_out, meta->n_valid);
 }
 
+// The attention of the step's sample rows (Kd per request) over the paged cache.
+int attention_step(const StepCtx& c, int Kd, int B, const pe_meta* meta, const int32_t* block_table,
+                   int max_blocks, int num_blocks, void* k_cache, void* v_cache) {
+  pe_handle* h = c.h;
+  const pe_dims& d = h->d;
+  const int NS = B * Kd;
+  AttnArgs aa{};
+  aa.B = B;
+  aa.K = Kd;
+  aa.H = d.n_heads;
+  aa.G = d.n_kv_heads;
+  aa.hd = d.head_dim;
+  aa.bs = d.block_size;
+  aa.max_blocks = max_blocks;
+  aa.num_blocks = num_blocks;
+  plan_attention(B, d.n_kv_heads, Kd, d.n_heads, d.head_dim, max_blocks, d.block_size, h->num_sms,
+                 aa.n_splits, aa.split_len, aa.cluster);
+  aa.q = c.q_s;
+  aa.k_cache = k_cache;
+  aa.v_cache = v_cache;
+  aa.block_table = block_table;
+  aa.seq_len = meta->seq_len;
+  aa.part_o = at<float>(c.ws, c.L->attn_part);
+  aa.part_ml = reinterpret_cast<float*>(static_cast<char*>(c.ws) + c.L->attn_part +
+                                        al256(static_cast<size_t>(aa.n_splits) * NS * d.n_heads *
+                                              d.head_dim * sizeof(float)));
+  aa.out = c.attn;
+  aa.sink = static_cast<const float*>(h->w.attn_sink);
+  aa.k_min = Kd;
+  aa.status = c.status;
+  return launch_attention(aa, c.dt, c.st);
+}
+
+// A decode-sized one-layer step (at most 16 token rows and 16 sample rows):
+// fc, QKV and RoPE/KV write in one persistent kernel, attention, then O,
+// gate/up, down and the final norm in a second (pe_decode.cu).
+int decode_layer_step(const StepCtx& c, int Kd, int B, int T_in, const pe_meta* meta,
+                      const void* A, const int32_t* block_table, int max_blocks, int num_blocks,
+                      void* k_cache, void* v_cache, void* z_out, float* hidden_out) {
+  pe_handle* h = c.h;
+  const pe_dims& d = h->d;
+  DecodeLaunch dl{};
+  dl.d = d.d;
+  dl.H = d.n_heads;
+  dl.G = d.n_kv_heads;
+  dl.hd = d.head_dim;
+  dl.inter = d.inter;
+  dl.K = Kd;
+  dl.B = B;
+  dl.T_out = T_in + B * (Kd - 1);
+  dl.bs = d.block_size;
+  dl.num_blocks = num_blocks;
+  dl.post_norm = d.post_norm;
+  dl.num_sms = h->num_sms;
+  dl.eps = d.eps;
+  std::memcpy(dl.inv_freq, h->inv_freq, sizeof(dl.inv_freq));
+  dl.m_fc = &h->m_fc;
+  dl.m_qkv = &h->m_qkv;
+  dl.m_o = &h->m_o;
+  dl.m_gate = &h->m_gate;
+  dl.m_up = &h->m_up;
+  dl.m_down = &h->m_down;
+  dl.A = A;
+  dl.n_valid = meta->n_valid;
+  dl.valid_rows = meta->valid_rows;
+  dl.valid_qsl = meta->valid_qsl;
+  dl.pos = meta->pos;
+  dl.slot = meta->slot;
+  dl.gamma_in = h->w.gamma_in;
+  dl.gamma_post = h->w.gamma_post;
+  dl.gamma_final = h->w.gamma_final;
+  dl.q_s = c.q_s;
+  dl.k_cache = k_cache;
+  dl.v_cache = v_cache;
+  dl.x_s = c.x_s;
+  dl.attn = c.attn;
+  dl.z = z_out;
+  dl.hidden_out = hidden_out;
+  dl.scratch = at<void>(c.ws, c.L->dec);
+  dl.bar = at<uint32_t>(c.ws, c.L->status + kBarrierWordsOffset);
+  dl.status = c.status;
+  int rc;
+  if ((rc = launch_decode_layer(dl, 1, c.st)) != PE_OK) return rc;
+  if ((rc = attention_step(c, Kd, B, meta, block_table, max_blocks, num_blocks, k_cache,
+                           v_cache)) != PE_OK)
+    return rc;
+  return launch_decode_layer(dl, 2, c.st);
+}
+
 // The one-layer drafter over a batch of Kd draft rows per request (the handle's
 // K for the parallel step, 1 for a pass of the autoregressive drafting): fc,
 // QKV, RoPE + KV write, attention of the sample rows, O, MLP and the final norm
@@ -430,6 +525,9 @@ int one_layer_step(const StepCtx& c, int Kd, int B, int T_in, const pe_meta* met
   const int NS = B * Kd;
   const int QKV = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim;
   int rc, np = 1;
+  if (c.bf && T_out <= kDecodeRows && NS <= kDecodeRows && c.L->dec)
+    return decode_layer_step(c, Kd, B, T_in, meta, A, block_table, max_blocks, num_blocks,
+                             k_cache, v_cache, z_out, hidden_out);
   if ((rc = fc_step(c, T_out, meta, A)) != PE_OK) return rc;
   // QKV (partial sums; RoPE adds them)
   Epilogue e = partial_epi(c, T_out, QKV);
@@ -870,7 +968,8 @@ int pe_prepare_inputs(pe_handle* h, int B, int T_in, const int32_t* qsl, const i
   const pe_dims& d = h->d;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* status = at<uint32_t>(ws, 0);
-  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return PE_ERR_CUDA;
+  // the status word and the decode layer's barrier words
+  if (cudaMemsetAsync(status, 0, 256, st) != cudaSuccess) return PE_ERR_CUDA;
   MetaLaunch ml;
   ml.B = B;
   ml.T_in = T_in;
@@ -989,7 +1088,7 @@ int pe_draft_autoregressive(pe_handle* h, int B, int T_in, const int32_t* qsl,
   if (ws_bytes < AL.total) return PE_ERR_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const StepCtx c = make_ctx(h, AL.layer, ws, st);
-  if (cudaMemsetAsync(c.status, 0, sizeof(uint32_t), st) != cudaSuccess) return PE_ERR_CUDA;
+  if (cudaMemsetAsync(c.status, 0, 256, st) != cudaSuccess) return PE_ERR_CUDA;
   const pe_meta m1 = meta_at(ws, AL.m1);
   const pe_meta m2 = meta_at(ws, AL.m2);
   void* A = at<void>(ws, AL.A);
@@ -1170,7 +1269,7 @@ int pe_read_status(const pe_handle* h, void* ws, uint32_t* status, int clear, vo
   if (cudaMemcpyAsync(&v, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return PE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return PE_ERR_CUDA;
-  if (clear && cudaMemsetAsync(ws, 0, sizeof(uint32_t), st) != cudaSuccess) return PE_ERR_CUDA;
+  if (clear && cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return PE_ERR_CUDA;
   *status = v;
   if (v & PE_ST_TIMEOUT) return PE_ERR_TIMEOUT;
   return v ? PE_ERR_DEVICE_INPUT : PE_OK;

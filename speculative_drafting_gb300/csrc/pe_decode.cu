@@ -1,0 +1,822 @@
+// The decoder layer of a decode-sized step as two persistent kernels.
+//
+// With at most 16 token rows every projection of the layer streams its weight
+// matrix from DRAM.  Run as separate kernels (fc, row norm, QKV, RoPE, O, row
+// norm, gate/up, down, final norm) each boundary costs a launch, a pipeline
+// fill and a drain, and the DRAM stream stops in between.  Here one launch
+// covers fc -> QKV -> RoPE/KV write and a second covers O -> gate/up -> down
+// -> final norm (attention runs between them as its own kernel):
+//
+//   * Every CTA (2 per SM, all resident) owns at most one work item of each
+//     projection: one 128-row weight tile and one share of its reduction
+//     dimension.  It stores the partial product of its share (fp32); the
+//     elementwise stage after the projection adds the shares in order.
+//   * Stages hand off through grid barriers in global memory (arrival counts,
+//     bounded waits).  A projection's weight boxes depend on nothing, so the
+//     TMA warp issues its first ring stages before it waits for the barrier that
+//     releases the token operand: the next projection's weights stream while the
+//     stage before it finishes.
+//   * A row norm before a projection needs the whole row's sum of squares.  The
+//     elementwise stage writes the un-normalised operand (x * gamma, as a bf16
+//     pair) and per-chunk sums of squares; the stage after the projection scales
+//     each row by 1/rms (the projection is linear in its operand).
+//
+// Warp roles: warp 0 issues TMA, one thread of warp 1 issues tcgen05.mma into
+// TMEM (128 x 16 fp32 accumulator), warps 2-5 read the accumulator, store the
+// partial tile, and run the elementwise stages.  Every wait is bounded: a wait
+// that runs out sets PE_ST_TIMEOUT and a global abort word, and every CTA
+// leaves.
+#include <algorithm>
+#include <cstring>
+
+#include "pe_common.cuh"
+#include "pe_internal.h"
+#include "pe_prep.h"
+
+namespace pe {
+
+namespace {
+
+constexpr int kThreads = 192;
+// The grid barriers need every CTA of the grid resident at once.  Three CTAs
+// fit an SM, but the grid takes two per SM: with every slot needed, a single
+// SM slot held up elsewhere once in a while left the last CTA unscheduled and
+// the others waiting at the first barrier until the bounded wait ran out
+// (measured: a few of 60 replays of a 7-pass autoregressive graph).
+constexpr int kCtasPerSm = 2;
+constexpr int kBM = 128;                          // weight rows per tile (MMA M)
+constexpr int kBK = 64;                           // reduction elements per k-block
+constexpr int kSlots = 3;                         // ring stages
+constexpr uint32_t kABytes = kBM * kBK * 2;       // 16 KB weight box
+constexpr uint32_t kBBytes = kDecodeRows * 128;   // 2 KB token box (16 rows)
+constexpr uint32_t kSlotBytes = kABytes + 2 * kBBytes;
+constexpr size_t kSmemBytes = kSlots * kSlotBytes + 1024;
+constexpr int kChunk = 128;                       // features per elementwise unit
+constexpr int kMaxGemm = 3;
+constexpr uint32_t kTmemCols = 32;
+
+// Barrier words (uint32) in the workspace header, after the status word.
+enum : int {
+  BW_PART1 = 0,     // part 1: 0 fc done, 1 operand written, 2 QKV done, 3 CTAs done
+  BW_PART2 = 4,     // part 2: 4 O done, 5 operand, 6 gate/up, 7 SwiGLU, 8 down, 9 y, 10 done
+  BW_EPOCH1 = 12,   // completed launches of part 1 / part 2
+  BW_EPOCH2 = 13,
+  BW_ABORT = 14,    // set by a CTA whose wait ran out: every other CTA leaves
+  BW_COUNT = 16,
+};
+
+struct DecGemm {
+  int M, K, num_kb, kbps, splits, m_tiles, n_mats, bpair, items;
+  float* out;       // partial tiles: out[((mat * splits + ks) * 16 + t) * M + f]
+};
+
+struct DecParams {
+  CUtensorMap mapA[kMaxGemm][2];  // packed weights of each projection (two for gate/up)
+  CUtensorMap mapB[kMaxGemm][2];  // token operand (hi, lo; lo = hi when not a pair)
+  DecGemm g[kMaxGemm];
+  int n_gemm;
+  int d, H, G, hd, inter, K, B, bs, num_blocks, post_norm;
+  float eps;
+  int rows_cap;            // token rows: T_out (part 1) or B*K (part 2)
+  const int* n_rows_dev;   // part 1: live rows (n_valid); part 2: NULL
+  const int32_t* valid_rows;
+  const int32_t* valid_qsl;
+  const int64_t* pos;
+  const int64_t* slot;
+  float* x_s;              // [B*K][d] residual rows of the sample rows
+  bf16* op_hi;             // projection operand pair [16][d]
+  bf16* op_lo;
+  bf16* h_hi;              // SwiGLU product pair [16][I]
+  bf16* h_lo;
+  float* r;                // [16][d] attention residual sum
+  float* y;                // [16][d] MLP residual sum
+  float* ss;               // [16][64] sums of squares per (row, 128-feature chunk)
+  float* ss2;              // [16][64] (final norm)
+  const bf16* gamma_a;     // part 1: gamma_in; part 2: gamma_post
+  const bf16* gamma_b;     // part 2: gamma_final
+  bf16* q_s;
+  bf16* k_cache;
+  bf16* v_cache;
+  bf16* z;                 // [B*K][d]
+  float* hidden_out;       // [B*K][d], nullable: the state handed to the next pass
+  uint32_t* bar;           // BW_COUNT barrier words
+  uint32_t* status;
+  double inv_freq[64];
+};
+
+PE_DEV uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until barrier word w has reached `target` arrivals (wrap-safe compare).
+// Bounded; gives up early when another CTA has aborted.
+PE_DEV bool grid_wait(const DecParams& p, int w, uint32_t target) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (static_cast<int32_t>(ld_acquire(p.bar + w) - target) >= 0) return true;
+    if ((i & 63u) == 63u) {
+      if (ld_acquire(p.bar + BW_ABORT)) return false;
+      if (globaltimer() - t0 > kWaitNs) return false;
+    }
+  }
+}
+
+PE_DEV void grid_arrive(const DecParams& p, int w) {
+  __threadfence();
+  atomicAdd(p.bar + w, 1u);
+}
+
+// A wait that ran out: the status bit, the abort word every CTA polls, and the
+// first place that gave up (header word 15: part << 16 | where << 8 | block, in
+// words 32.. the block, the barrier word, its count and the target).
+PE_DEV void abort_all(const DecParams& p, int part, int where, uint32_t word = 0,
+                      uint32_t target = 0) {
+  set_status(p.status, PE_ST_TIMEOUT);
+  if (atomicCAS(p.bar + 15, 0u, 1u + ((part << 16) | (where << 8))) == 0u) {
+    p.bar[16] = blockIdx.x;
+    p.bar[17] = word;
+    p.bar[18] = word < 16 ? p.bar[word] : 0u;
+    p.bar[19] = target;
+  }
+  atomicExch(p.bar + BW_ABORT, 1u);
+}
+
+// Generic-proxy writes of other CTAs (seen through an acquire) before this
+// thread's TMA (async-proxy) reads of the same global memory.
+PE_DEV void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// The packed weight box of tile row m at k-block kb (beyond K: past the last
+// block, which TMA fills with zeros).
+PE_DEV void weight_box(const DecGemm& g, int m, int kb, int& cx, int& cy) {
+  const int k_atoms = (g.K + kBK - 1) / kBK;
+  cx = 0;
+  cy = (kb < k_atoms ? m * k_atoms + kb : g.m_tiles * k_atoms) * kBM;
+}
+
+struct Item {
+  int mat, m, ks, kb0, kb1;
+};
+
+PE_DEV bool item_of(const DecGemm& g, int it, Item& out) {
+  if (it >= g.items) return false;
+  const int per_mat = g.m_tiles * g.splits;
+  out.mat = it / per_mat;
+  const int rem = it - out.mat * per_mat;
+  out.m = rem / g.splits;
+  out.ks = rem - out.m * g.splits;
+  out.kb0 = out.ks * g.kbps;
+  out.kb1 = min(g.num_kb, out.kb0 + g.kbps);
+  return out.kb0 < out.kb1;
+}
+
+// Sum of the partial tiles of projection g (matrix `mat`) at (row t, feature f).
+PE_DEV float sum_parts(const DecGemm& g, int mat, int t, int f) {
+  const float* p = g.out + (static_cast<size_t>(mat) * g.splits * kDecodeRows + t) * g.M + f;
+  const size_t stride = static_cast<size_t>(kDecodeRows) * g.M;
+  float acc = 0.f;
+  for (int k = 0; k < g.splits; ++k) acc += p[k * stride];
+  return acc;
+}
+
+// 1 / rms of row t from its per-chunk sums of squares (one warp, all lanes get it).
+PE_DEV float row_inv_rms(const float* ss, int t, int d, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int nc = (d + kChunk - 1) / kChunk;
+  float s = 0.f;
+  for (int c = lane; c < nc; c += 32) s += ss[t * 64 + c];
+  s = warp_sum(s);
+  return 1.0f / sqrtf(s / static_cast<float>(d) + eps);
+}
+
+// The sample row (r * K + k) non-rejected row v is, or -1: one of the last K
+// non-rejected rows of its request.
+PE_DEV int sample_of(const DecParams& p, int v) {
+  for (int r = 0; r < p.B; ++r) {
+    const int v0 = p.valid_qsl[r], v1 = p.valid_qsl[r + 1];
+    if (v >= v0 && v < v1) {
+      const int k = v - (v1 - p.K);
+      return k >= 0 && k < p.K ? r * p.K + k : -1;
+    }
+  }
+  return -1;
+}
+
+PE_DEV void store_pair(bf16* hi, bf16* lo, size_t i, float v) {
+  const bf16 h = __float2bfloat16_rn(v);
+  hi[i] = h;
+  lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+// Sum of x over the 128 elementwise threads (4 warps); `red` holds 4 floats.
+PE_DEV float sum128(float x, float* red) {
+  const int ew = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31;
+  x = warp_sum(x);
+  named_bar_sync(2, 128);
+  if (lane == 0) red[ew] = x;
+  named_bar_sync(2, 128);
+  return red[0] + red[1] + red[2] + red[3];
+}
+
+// ---------------------------------------------------------------- elementwise stages
+
+// Part 1, after fc: x = the fc shares' sum for non-rejected row v; the QKV
+// operand (x * gamma_in pre-norm, x post-norm) as a bf16 pair; x of the sample
+// rows (the attention residual); per-chunk sums of squares of x (pre-norm).
+PE_DEV void stage_after_fc(const DecParams& p, int n_rows, float* red) {
+  const int j = threadIdx.x - 64;
+  const int nc = (p.d + kChunk - 1) / kChunk;
+  for (int u = blockIdx.x; u < n_rows * nc; u += gridDim.x) {
+    const int v = u / nc, c = u - v * nc;
+    const int f = c * kChunk + j;
+    float x = 0.f;
+    if (f < p.d) {
+      x = sum_parts(p.g[0], 0, v, f);
+      const float opv = p.post_norm ? x : x * __bfloat162float(p.gamma_a[f]);
+      store_pair(p.op_hi, p.op_lo, static_cast<size_t>(v) * p.d + f, opv);
+      const int s = sample_of(p, v);
+      if (s >= 0) p.x_s[static_cast<size_t>(s) * p.d + f] = x;
+    }
+    if (!p.post_norm) {
+      const float t = sum128(x * x, red);
+      if (j == 0) p.ss[v * 64 + c] = t;
+    }
+  }
+}
+
+// Part 1, after QKV: one warp per (non-rejected row, head): the QKV shares'
+// sum, scaled by the row's 1/rms (pre-norm), RoPE on q and k, q of the sample
+// rows, k and v at the row's cache slot.
+PE_DEV void stage_rope(const DecParams& p, int n_rows) {
+  const int lane = threadIdx.x & 31;
+  const int ew = (threadIdx.x >> 5) - 2;
+  const int heads = p.H + 2 * p.G;
+  const int half = p.hd / 2;
+  for (int u = blockIdx.x * 4 + ew; u < n_rows * heads; u += gridDim.x * 4) {
+    const int v = u / heads, hh = u - v * heads;
+    const float sc = p.post_norm ? 1.f : row_inv_rms(p.ss, v, p.d, p.eps);
+    const int o = p.valid_rows[v];
+    const int64_t pos = p.pos[o];
+    const int64_t slot = p.slot[o];
+    const bool slot_ok = slot >= 0 && slot < static_cast<int64_t>(p.num_blocks) * p.bs;
+    if (!slot_ok && slot != PE_PADDING_SLOT_ID && lane == 0 && hh == 0)
+      set_status(p.status, PE_ST_BLOCK_RANGE);
+    const int64_t blk = slot_ok ? slot / p.bs : 0, off = slot_ok ? slot % p.bs : 0;
+    const int s = hh < p.H ? sample_of(p, v) : -1;
+    for (int i = lane; i < half; i += 32) {
+      const int e1 = hh * p.hd + i, e2 = e1 + half;
+      const float x1 = sc * sum_parts(p.g[1], 0, v, e1);
+      const float x2 = sc * sum_parts(p.g[1], 0, v, e2);
+      if (hh >= p.H + p.G) {  // v: no rotation
+        if (slot_ok) {
+          bf16* vc = p.v_cache + ((blk * p.G + (hh - p.H - p.G)) * p.bs + off) * p.hd;
+          vc[i] = __float2bfloat16_rn(x1);
+          vc[i + half] = __float2bfloat16_rn(x2);
+        }
+        continue;
+      }
+      const double ang = static_cast<double>(pos) * p.inv_freq[i];
+      const double two_pi = 6.283185307179586476925286766559;
+      const double red = ang - two_pi * rint(ang / two_pi);
+      float sn, cs;
+      sincosf(static_cast<float>(red), &sn, &cs);
+      const float y1 = x1 * cs - x2 * sn;
+      const float y2 = x2 * cs + x1 * sn;
+      if (hh < p.H) {
+        if (s >= 0) {
+          bf16* q = p.q_s + (static_cast<size_t>(s) * p.H + hh) * p.hd;
+          q[i] = __float2bfloat16_rn(y1);
+          q[i + half] = __float2bfloat16_rn(y2);
+        }
+      } else if (slot_ok) {
+        bf16* kc = p.k_cache + ((blk * p.G + (hh - p.H)) * p.bs + off) * p.hd;
+        kc[i] = __float2bfloat16_rn(y1);
+        kc[i + half] = __float2bfloat16_rn(y2);
+      }
+    }
+  }
+}
+
+// Part 2, after O: r = x_s + the O shares' sum; the MLP operand r * gamma_post
+// as a bf16 pair; per-chunk sums of squares of r.
+PE_DEV void stage_after_o(const DecParams& p, float* red) {
+  const int j = threadIdx.x - 64;
+  const int nc = (p.d + kChunk - 1) / kChunk;
+  for (int u = blockIdx.x; u < p.rows_cap * nc; u += gridDim.x) {
+    const int s = u / nc, c = u - s * nc;
+    const int f = c * kChunk + j;
+    float rv = 0.f;
+    if (f < p.d) {
+      const size_t i = static_cast<size_t>(s) * p.d + f;
+      rv = p.x_s[i] + sum_parts(p.g[0], 0, s, f);
+      p.r[i] = rv;
+      store_pair(p.op_hi, p.op_lo, i, rv * __bfloat162float(p.gamma_a[f]));
+    }
+    const float t = sum128(rv * rv, red);
+    if (j == 0) p.ss[s * 64 + c] = t;
+  }
+}
+
+// Part 2, after gate/up: h = silu(g) * u with g, u the shares' sums scaled by
+// the row's 1/rms (the MLP input is RMSNorm(r) * gamma_post), as a bf16 pair.
+PE_DEV void stage_swiglu(const DecParams& p) {
+  const int j = threadIdx.x - 64;
+  const int nc = (p.inter + kChunk - 1) / kChunk;
+  for (int u = blockIdx.x; u < p.rows_cap * nc; u += gridDim.x) {
+    const int s = u / nc, c = u - s * nc;
+    const int f = c * kChunk + j;
+    const float sc = row_inv_rms(p.ss, s, p.d, p.eps);
+    if (f < p.inter) {
+      const float gv = sc * sum_parts(p.g[1], 0, s, f);
+      const float uv = sc * sum_parts(p.g[1], 1, s, f);
+      store_pair(p.h_hi, p.h_lo, static_cast<size_t>(s) * p.inter + f,
+                 gv / (1.0f + expf(-gv)) * uv);
+    }
+  }
+}
+
+// Part 2, after down: y = residual + the down shares' sum (residual: r
+// pre-norm; RMSNorm(r) * gamma_post post-norm); per-chunk sums of squares of y.
+PE_DEV void stage_after_down(const DecParams& p, float* red) {
+  const int j = threadIdx.x - 64;
+  const int nc = (p.d + kChunk - 1) / kChunk;
+  for (int u = blockIdx.x; u < p.rows_cap * nc; u += gridDim.x) {
+    const int s = u / nc, c = u - s * nc;
+    const int f = c * kChunk + j;
+    const float sc = p.post_norm ? row_inv_rms(p.ss, s, p.d, p.eps) : 1.f;
+    float yv = 0.f;
+    if (f < p.d) {
+      const size_t i = static_cast<size_t>(s) * p.d + f;
+      const float res = p.post_norm ? sc * p.r[i] * __bfloat162float(p.gamma_a[f]) : p.r[i];
+      yv = res + sum_parts(p.g[2], 0, s, f);
+      p.y[i] = yv;
+    }
+    const float t = sum128(yv * yv, red);
+    if (j == 0) p.ss2[s * 64 + c] = t;
+  }
+}
+
+// Part 2, last: z = RMSNorm(y) * gamma_final (bf16) and the hidden state handed
+// on (y pre-norm, the normalised value post-norm).
+PE_DEV void stage_final(const DecParams& p) {
+  const int j = threadIdx.x - 64;
+  const int nc = (p.d + kChunk - 1) / kChunk;
+  for (int u = blockIdx.x; u < p.rows_cap * nc; u += gridDim.x) {
+    const int s = u / nc, c = u - s * nc;
+    const int f = c * kChunk + j;
+    const float sc = row_inv_rms(p.ss2, s, p.d, p.eps);
+    if (f < p.d) {
+      const size_t i = static_cast<size_t>(s) * p.d + f;
+      const float zf = p.y[i] * sc * __bfloat162float(p.gamma_b[f]);
+      p.z[i] = __float2bfloat16_rn(zf);
+      if (p.hidden_out) p.hidden_out[i] = p.post_norm ? zf : p.y[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- the kernel
+
+// PART 1: fc, [after fc], QKV, [RoPE].  PART 2: O, [after O], gate/up,
+// [SwiGLU], down, [after down], [final].  The barrier word after GEMM stage
+// `gs` (its partial tiles stored) and after each elementwise stage.
+template <int PART>
+__global__ void __launch_bounds__(kThreads, 3) decode_layer_kernel(const __grid_constant__ DecParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kSlots], empty_bar[kSlots], tfull_bar, tempty_bar,
+      final_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh, ok_sh;
+  __shared__ float red_sh[4];
+  __shared__ uint32_t epoch_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int wbase = PART == 1 ? BW_PART1 : BW_PART2;
+  const int wepoch = PART == 1 ? BW_EPOCH1 : BW_EPOCH2;
+  // barrier word that releases GEMM stage gs's token operand (-1: the kernel before)
+  auto ready_word = [&](int gs) { return gs == 0 ? -1 : wbase + 2 * gs - 1; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&tfull_bar, 1);
+    mbar_init(&tempty_bar, 128);
+    mbar_init(&final_bar, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+  volatile int* abort_flag = &abort_sh;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int slot = 0;
+      uint32_t phase = 0, armed = 0u, armed_parity = 0u;
+      uint32_t target = 0;
+      bool have_target = false, ok = true;
+      for (int gs = 0; gs < p.n_gemm && ok; ++gs) {
+        const DecGemm& g = p.g[gs];
+        Item it;
+        const bool mine = item_of(g, blockIdx.x, it);
+        const CUtensorMap* mA = &p.mapA[gs][mine ? it.mat : 0];
+        const uint32_t bytes = kABytes + kBBytes * (g.bpair ? 2u : 1u);
+        int pre_slot[kSlots];
+        int pre = 0;
+        if (mine) {
+          prefetch_tmap(mA);
+          // the weight boxes of the first ring stages go out before the wait
+          const int want = min(it.kb1 - it.kb0, kSlots);
+          for (int j = 0; j < want; ++j) {
+            if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag)) {
+              ok = false;
+              if (!*abort_flag) abort_all(p, PART, 10 + gs);
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[slot], bytes);
+            int cx, cy;
+            weight_box(g, it.m, it.kb0 + j, cx, cy);
+            tma_load_2d(smem + static_cast<size_t>(slot) * kSlotBytes, mA, &full_bar[slot], cx, cy,
+                        pol_w);
+            armed |= 1u << slot;
+            armed_parity = (armed_parity & ~(1u << slot)) | (phase << slot);
+            pre_slot[pre++] = slot;
+            if (++slot == kSlots) {
+              slot = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        // the token operand: written by the kernel before, or the stage before
+        if (!have_target) {
+          pdl_wait();
+          target = (ld_acquire(p.bar + wepoch) + 1u) * gridDim.x;
+          have_target = true;
+        }
+        if (ok && ready_word(gs) >= 0) {
+          if (!grid_wait(p, ready_word(gs), target)) {
+            ok = false;
+            abort_all(p, PART, 1 + gs, ready_word(gs), target);
+          } else {
+            fence_proxy_async_global();
+          }
+        }
+        if (!ok) {
+          // the stages armed above still get their token boxes, so they complete
+          for (int j = 0; j < pre && mine; ++j) {
+            uint8_t* sb = smem + static_cast<size_t>(pre_slot[j]) * kSlotBytes + kABytes;
+            tma_load_2d(sb, &p.mapB[gs][0], &full_bar[pre_slot[j]], (it.kb0 + j) * kBK, 0, pol_x);
+            if (g.bpair)
+              tma_load_2d(sb + kBBytes, &p.mapB[gs][1], &full_bar[pre_slot[j]], (it.kb0 + j) * kBK,
+                          0, pol_x);
+          }
+          break;
+        }
+        if (!mine) continue;
+        for (int j = 0; j < pre; ++j) {
+          uint8_t* sb = smem + static_cast<size_t>(pre_slot[j]) * kSlotBytes + kABytes;
+          tma_load_2d(sb, &p.mapB[gs][0], &full_bar[pre_slot[j]], (it.kb0 + j) * kBK, 0, pol_x);
+          if (g.bpair)
+            tma_load_2d(sb + kBBytes, &p.mapB[gs][1], &full_bar[pre_slot[j]], (it.kb0 + j) * kBK, 0,
+                        pol_x);
+        }
+        for (int kb = it.kb0 + pre; kb < it.kb1; ++kb) {
+          if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag)) {
+            ok = false;
+            if (!*abort_flag) abort_all(p, PART, 20 + gs);
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[slot], bytes);
+          uint8_t* sa = smem + static_cast<size_t>(slot) * kSlotBytes;
+          int cx, cy;
+          weight_box(g, it.m, kb, cx, cy);
+          tma_load_2d(sa, mA, &full_bar[slot], cx, cy, pol_w);
+          tma_load_2d(sa + kABytes, &p.mapB[gs][0], &full_bar[slot], kb * kBK, 0, pol_x);
+          if (g.bpair) tma_load_2d(sa + kABytes + kBBytes, &p.mapB[gs][1], &full_bar[slot], kb * kBK, 0, pol_x);
+          armed |= 1u << slot;
+          armed_parity = (armed_parity & ~(1u << slot)) | (phase << slot);
+          if (++slot == kSlots) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) abort_sh = 1;
+      if (*abort_flag) {
+        // copies already in flight land before the CTA's shared memory goes away
+        for (int s = 0; s < kSlots; ++s)
+          if (armed & (1u << s)) {
+            int dummy = 0;
+            mbar_wait(&full_bar[s], (armed_parity >> s) & 1u, &dummy);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, kDecodeRows);
+      int slot = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int gs = 0; gs < p.n_gemm && ok && !*abort_flag; ++gs) {
+        const DecGemm& g = p.g[gs];
+        Item it;
+        if (!item_of(g, blockIdx.x, it)) continue;
+        if (!mbar_wait(&tempty_bar, acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          if (!*abort_flag) abort_all(p, PART, 30 + gs);
+          break;
+        }
+        tc_fence_after();
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (!mbar_wait(&full_bar[slot], phase, abort_flag)) {
+            ok = false;
+            if (!*abort_flag) abort_all(p, PART, 40 + gs);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + static_cast<size_t>(slot) * kSlotBytes);
+          const uint64_t adesc = sw128_kmajor_desc(sa);
+          const uint64_t bdesc = sw128_kmajor_desc(sa + kABytes);
+          const uint64_t b2desc = sw128_kmajor_desc(sa + kABytes + kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t acc = (kb > it.kb0 || kk > 0) ? 1u : 0u;
+            umma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, acc);
+            if (g.bpair) umma_bf16(tmem_base, adesc + 2 * kk, b2desc + 2 * kk, idesc, 1u);
+          }
+          umma_commit(&empty_bar[slot]);
+          if (++slot == kSlots) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar);
+        acc_phase ^= 1u;
+      }
+      if (!ok) abort_sh = 1;
+      umma_commit(&final_bar);
+      int dummy = 0;
+      mbar_wait(&final_bar, 0, &dummy);
+    }
+  } else {
+    // ---------------- warps 2-5: partial tiles and the elementwise stages
+    const int q = warp & 3;
+    const int fl = q * 32 + lane;
+    const int j = threadIdx.x - 64;
+    pdl_wait();
+    if (j == 0) epoch_sh = (ld_acquire(p.bar + wepoch) + 1u) * gridDim.x;
+    named_bar_sync(1, 128);
+    const uint32_t target = epoch_sh;
+    int n_rows = p.rows_cap;
+    if (p.n_rows_dev) n_rows = min(max(*p.n_rows_dev, 0), p.rows_cap);
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    // every CTA arrives at every barrier word, in order, once
+    auto gemm_epilogue = [&](int gs) {
+      const DecGemm& g = p.g[gs];
+      Item it;
+      if (item_of(g, blockIdx.x, it)) {
+        const bool got = mbar_wait(&tfull_bar, acc_phase, abort_flag);
+        if (j == 0) ok_sh = 1;
+        named_bar_sync(1, 128);
+        if (!got) {
+          ok_sh = 0;
+          if (j == 0 && !*abort_flag) abort_all(p, PART, 50 + gs);
+        }
+        named_bar_sync(1, 128);
+        if (!ok_sh) return false;
+        acc_phase ^= 1u;
+        tc_fence_after();
+        float v[16];
+        tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16), v);
+        tc_fence_before();
+        mbar_arrive(&tempty_bar);
+        const int f = it.m * kBM + fl;
+        if (f < g.M) {
+          float* out = g.out + (static_cast<size_t>(it.mat) * g.splits + it.ks) * kDecodeRows * g.M + f;
+#pragma unroll
+          for (int t = 0; t < kDecodeRows; ++t)
+            if (t < n_rows) out[static_cast<size_t>(t) * g.M] = v[t];
+        }
+      }
+      return true;
+    };
+    auto barrier = [&](int w, bool wait_next) {
+      // arrive at w; then (wait_next) wait for every CTA's arrival at w
+      named_bar_sync(1, 128);
+      if (j == 0) {
+        grid_arrive(p, w);
+        ok_sh = wait_next ? (grid_wait(p, w, target) ? 1 : 0) : 1;
+        if (!ok_sh) abort_all(p, PART, 60, w, target);
+      }
+      named_bar_sync(1, 128);
+      return ok_sh != 0;
+    };
+    if (PART == 1) {
+      ok = gemm_epilogue(0) && barrier(wbase + 0, true);
+      if (ok) stage_after_fc(p, n_rows, red_sh);
+      ok = ok && barrier(wbase + 1, false);
+      ok = ok && gemm_epilogue(1) && barrier(wbase + 2, true);
+      if (ok) stage_rope(p, n_rows);
+    } else {
+      ok = gemm_epilogue(0) && barrier(wbase + 0, true);
+      if (ok) stage_after_o(p, red_sh);
+      ok = ok && barrier(wbase + 1, false);
+      ok = ok && gemm_epilogue(1) && barrier(wbase + 2, true);
+      if (ok) stage_swiglu(p);
+      ok = ok && barrier(wbase + 3, false);
+      ok = ok && gemm_epilogue(2) && barrier(wbase + 4, true);
+      if (ok) stage_after_down(p, red_sh);
+      ok = ok && barrier(wbase + 5, true);
+      if (ok) stage_final(p);
+    }
+    if (!ok && j == 0) abort_sh = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+  // the last CTA to finish counts the launch (every CTA has read the count by now)
+  if (threadIdx.x == 64) {
+    const int wdone = PART == 1 ? BW_PART1 + 3 : BW_PART2 + 6;
+    __threadfence();
+    const uint32_t prev = atomicAdd(p.bar + wdone, 1u);
+    if (prev + 1u == epoch_sh) atomicAdd(p.bar + wepoch, 1u);
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host
+
+size_t decode_scratch_bytes(int d, int qkv, int inter, int num_sms) {
+  // partial tiles: the largest projection's shares over every CTA of the grid
+  const size_t grid = static_cast<size_t>(num_sms) * kCtasPerSm;
+  const size_t rows = kDecodeRows;
+  const int widest = std::max(std::max(d, qkv), inter);
+  const size_t parts = grid * rows * kBM * sizeof(float) + rows * widest * sizeof(float) * 2;
+  auto a256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  return a256(parts) +                                          // partial tiles
+         2 * a256(rows * std::max(d, inter) * 2) +              // operand pair
+         2 * a256(rows * inter * 2) +                           // SwiGLU pair
+         2 * a256(rows * d * sizeof(float)) +                   // r, y
+         2 * a256(rows * 64 * sizeof(float));                   // sums of squares
+}
+
+bool decode_layer_fits(int d, int qkv, int inter, int num_sms) {
+  const int grid = num_sms * kCtasPerSm;
+  auto tiles = [](int m) { return (m + kBM - 1) / kBM; };
+  // every projection's weight tiles fit the grid; a row's chunk sums fit 64 slots
+  return num_sms > 0 && tiles(d) <= grid && tiles(qkv) <= grid && 2 * tiles(inter) <= grid &&
+         (d + kChunk - 1) / kChunk <= 64;
+}
+
+// Split a projection [M][K] (n_mats matrices) so that every CTA of the grid
+// has at most one item.
+static DecGemm plan_dec_gemm(int M, int K, int n_mats, int bpair, int grid, float* out) {
+  DecGemm g{};
+  g.M = M;
+  g.K = K;
+  g.n_mats = n_mats;
+  g.bpair = bpair;
+  g.m_tiles = (M + kBM - 1) / kBM;
+  g.num_kb = (K + kBK - 1) / kBK;
+  int s = std::max(1, grid / (n_mats * g.m_tiles));
+  s = std::min(s, g.num_kb);
+  g.kbps = (g.num_kb + s - 1) / s;
+  g.splits = (g.num_kb + g.kbps - 1) / g.kbps;
+  g.items = n_mats * g.m_tiles * g.splits;
+  g.out = out;
+  return g;
+}
+
+int launch_decode_layer(const DecodeLaunch& L, int part, cudaStream_t st) {
+  const int grid = L.num_sms * kCtasPerSm;
+  DecParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int Hd = L.H * L.hd;
+  const int QKV = (L.H + 2 * L.G) * L.hd;
+  auto a256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  char* base = static_cast<char*>(L.scratch);
+  const size_t rows = kDecodeRows;
+  const int widest = std::max(std::max(L.d, QKV), L.inter);
+  size_t off = 0;
+  float* part_buf = reinterpret_cast<float*>(base + off);
+  off += a256(static_cast<size_t>(grid) * rows * kBM * sizeof(float) +
+              rows * widest * sizeof(float) * 2);
+  bf16* op_hi = reinterpret_cast<bf16*>(base + off);
+  off += a256(rows * std::max(L.d, L.inter) * 2);
+  bf16* op_lo = reinterpret_cast<bf16*>(base + off);
+  off += a256(rows * std::max(L.d, L.inter) * 2);
+  bf16* h_hi = reinterpret_cast<bf16*>(base + off);
+  off += a256(rows * L.inter * 2);
+  bf16* h_lo = reinterpret_cast<bf16*>(base + off);
+  off += a256(rows * L.inter * 2);
+  float* r = reinterpret_cast<float*>(base + off);
+  off += a256(rows * L.d * sizeof(float));
+  float* y = reinterpret_cast<float*>(base + off);
+  off += a256(rows * L.d * sizeof(float));
+  float* ss = reinterpret_cast<float*>(base + off);
+  off += a256(rows * 64 * sizeof(float));
+  float* ss2 = reinterpret_cast<float*>(base + off);
+
+  p.d = L.d;
+  p.H = L.H;
+  p.G = L.G;
+  p.hd = L.hd;
+  p.inter = L.inter;
+  p.K = L.K;
+  p.B = L.B;
+  p.bs = L.bs;
+  p.num_blocks = L.num_blocks;
+  p.post_norm = L.post_norm;
+  p.eps = L.eps;
+  p.x_s = L.x_s;
+  p.op_hi = op_hi;
+  p.op_lo = op_lo;
+  p.h_hi = h_hi;
+  p.h_lo = h_lo;
+  p.r = r;
+  p.y = y;
+  p.ss = ss;
+  p.ss2 = ss2;
+  p.bar = L.bar;
+  p.status = L.status;
+  std::memcpy(p.inv_freq, L.inv_freq, sizeof(p.inv_freq));
+  auto map_x = [&](CUtensorMap* m, const void* X, int rows_cap, int cols) {
+    return encode_tmap_bf16(m, X, static_cast<uint64_t>(rows_cap), static_cast<uint64_t>(cols),
+                            kDecodeRows);
+  };
+  bool ok = true;
+  if (part == 1) {
+    p.rows_cap = L.T_out;
+    p.n_rows_dev = L.n_valid;
+    p.valid_rows = L.valid_rows;
+    p.valid_qsl = L.valid_qsl;
+    p.pos = L.pos;
+    p.slot = L.slot;
+    p.gamma_a = static_cast<const bf16*>(L.gamma_in);
+    p.q_s = static_cast<bf16*>(L.q_s);
+    p.k_cache = static_cast<bf16*>(L.k_cache);
+    p.v_cache = static_cast<bf16*>(L.v_cache);
+    p.n_gemm = 2;
+    p.g[0] = plan_dec_gemm(L.d, 4 * L.d, 1, 0, grid, part_buf);
+    p.g[1] = plan_dec_gemm(QKV, L.d, 1, 1, grid, part_buf);
+    p.mapA[0][0] = *L.m_fc;
+    p.mapA[1][0] = *L.m_qkv;
+    ok = map_x(&p.mapB[0][0], L.A, L.T_out, 4 * L.d) && map_x(&p.mapB[1][0], op_hi, L.T_out, L.d) &&
+         map_x(&p.mapB[1][1], op_lo, L.T_out, L.d);
+    p.mapB[0][1] = p.mapB[0][0];
+  } else {
+    const int NS = L.B * L.K;
+    p.rows_cap = NS;
+    p.gamma_a = static_cast<const bf16*>(L.gamma_post);
+    p.gamma_b = static_cast<const bf16*>(L.gamma_final);
+    p.z = static_cast<bf16*>(L.z);
+    p.hidden_out = L.hidden_out;
+    p.n_gemm = 3;
+    p.g[0] = plan_dec_gemm(L.d, Hd, 1, 0, grid, part_buf);
+    p.g[1] = plan_dec_gemm(L.inter, L.d, 2, 1, grid, part_buf);
+    p.g[2] = plan_dec_gemm(L.d, L.inter, 1, 1, grid, part_buf);
+    p.mapA[0][0] = *L.m_o;
+    p.mapA[1][0] = *L.m_gate;
+    p.mapA[1][1] = *L.m_up;
+    p.mapA[2][0] = *L.m_down;
+    ok = map_x(&p.mapB[0][0], L.attn, NS, Hd) && map_x(&p.mapB[1][0], op_hi, NS, L.d) &&
+         map_x(&p.mapB[1][1], op_lo, NS, L.d) && map_x(&p.mapB[2][0], h_hi, NS, L.inter) &&
+         map_x(&p.mapB[2][1], h_lo, NS, L.inter);
+    p.mapB[0][1] = p.mapB[0][0];
+  }
+  if (!ok) return PE_ERR_CUDA;
+  auto kern = part == 1 ? decode_layer_kernel<1> : decode_layer_kernel<2>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes)) != cudaSuccess)
+    return PE_ERR_CUDA;
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, p) == cudaSuccess
+             ? PE_OK
+             : PE_ERR_CUDA;
+}
+
+}  // namespace pe

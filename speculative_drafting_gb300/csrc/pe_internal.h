@@ -115,6 +115,48 @@ int pack_weight(const void* W, int M, int K, void* P, cudaStream_t st);
 // tensor map over a packed weight: [m_tiles * k_atoms * 128 rows][64], box 128 x 64
 bool encode_packed_weight_map(CUtensorMap* map, const void* P, int M, int K);
 
+// ------------------------------------------------------------------ persistent decode layer
+// A one-layer bf16 step whose token rows (T_out, and B*K sample rows) fit in
+// one 16-row tile runs its layer as two persistent kernels around attention
+// (pe_decode.cu).
+constexpr int kDecodeRows = 16;
+
+struct DecodeLaunch {
+  int d, H, G, hd, inter, K, B, T_out, bs, num_blocks, post_norm, num_sms;
+  float eps;
+  double inv_freq[64];
+  const CUtensorMap* m_fc;
+  const CUtensorMap* m_qkv;
+  const CUtensorMap* m_o;
+  const CUtensorMap* m_gate;
+  const CUtensorMap* m_up;
+  const CUtensorMap* m_down;
+  const void* A;           // part 1 token rows [T_out][4d]
+  const int* n_valid;
+  const int32_t* valid_rows;
+  const int32_t* valid_qsl;
+  const int64_t* pos;
+  const int64_t* slot;
+  const void* gamma_in;
+  const void* gamma_post;
+  const void* gamma_final;
+  void* q_s;               // [B*K][H][hd]
+  void* k_cache;
+  void* v_cache;
+  float* x_s;              // [B*K][d]
+  const void* attn;        // part 2 token rows [B*K][H*hd]
+  void* z;                 // [B*K][d]
+  float* hidden_out;       // nullable
+  void* scratch;           // decode_scratch_bytes
+  uint32_t* bar;           // 16 barrier words, zero on first use
+  uint32_t* status;
+};
+size_t decode_scratch_bytes(int d, int qkv, int inter, int num_sms);
+// whether the decode layer handles these dimensions on this device
+bool decode_layer_fits(int d, int qkv, int inter, int num_sms);
+// part 1: fc, QKV, RoPE + KV write; part 2: O, gate/up, down, final norm
+int launch_decode_layer(const DecodeLaunch& L, int part, cudaStream_t st);
+
 int num_sms_of_current_device();
 
 // Read-only views of a handle (defined beside the handle).

@@ -34,6 +34,15 @@ CASES = [
     ("small_prenorm", {"batch": 12, "n_prev": 6, "ctx": ("uniform", 0, 700), "seed": 3, "sinks": True}),
     ("small_prenorm", {"batch": 160, "n_prev": 6, "ctx": ("uniform", 0, 700), "seed": 5,
                        "sinks": True}),
+    # decode-sized steps (at most 16 token rows and 16 sample rows): the layer
+    # runs as the two persistent kernels
+    ("small_prenorm", {"batch": 2, "n_prev": 4, "K": 4, "ctx": (37, 150)}),
+    ("small_prenorm", {"batch": 1, "n_prev": 8, "K": 7, "ctx": (300,)}),
+    ("small_prenorm", {"batch": 2, "n_prev": (5, 2), "K": 4, "accepted": (4, 0), "ctx": (60, 9),
+                       "sinks": True}),
+    ("small_postnorm_hd128", {"batch": 2, "n_prev": (3, 1), "K": 5, "ctx": (17, 100)}),
+    ("small_postnorm_hd128", {"batch": 1, "n_prev": 9, "K": 8, "ctx": (0,), "post_norm": False}),
+    ("small_prenorm", {"batch": 16, "n_prev": 1, "K": 1, "ctx": ("uniform", 0, 400), "seed": 7}),
 ]
 
 
