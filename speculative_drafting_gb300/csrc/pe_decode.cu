@@ -46,11 +46,19 @@ constexpr int kThreads = 192;
 constexpr int kCtasPerSm = 2;
 constexpr int kBM = 128;                          // weight rows per tile (MMA M)
 constexpr int kBK = 64;                           // reduction elements per k-block
-constexpr int kSlots = 3;                         // ring stages
+// Ring stages: the first ones of each projection are issued before the wait for
+// its token operand, so a deeper ring keeps more of the next weights in flight
+// across a stage boundary (two CTAs of five 20 KB stages fit an SM).
+constexpr int kSlots = 5;
 constexpr uint32_t kABytes = kBM * kBK * 2;       // 16 KB weight box
 constexpr uint32_t kBBytes = kDecodeRows * 128;   // 2 KB token box (16 rows)
 constexpr uint32_t kSlotBytes = kABytes + 2 * kBBytes;
 constexpr size_t kSmemBytes = kSlots * kSlotBytes + 1024;
+// kCtasPerSm CTAs fit an SM's 228 KB of shared memory: the ring, under 1 KB of
+// static shared memory and the 1 KB the system reserves per CTA.  (The
+// occupancy query answers 1 for tcgen05 kernels like this one whatever their
+// size, so the fit is this arithmetic.)
+static_assert(kCtasPerSm * (kSmemBytes + 2048) <= 228 * 1024, "decode CTAs must fit an SM");
 constexpr int kChunk = 128;                       // features per elementwise unit
 constexpr int kMaxGemm = 3;
 constexpr uint32_t kTmemCols = 32;
@@ -173,36 +181,62 @@ PE_DEV bool item_of(const DecGemm& g, int it, Item& out) {
   return out.kb0 < out.kb1;
 }
 
-// Sum of the partial tiles of projection g (matrix `mat`) at (row t, feature f).
-PE_DEV float sum_parts(const DecGemm& g, int mat, int t, int f) {
-  const float* p = g.out + (static_cast<size_t>(mat) * g.splits * kDecodeRows + t) * g.M + f;
+// Sums of the partial tiles of projection g (matrix `mat`) at row t for N
+// features f[i] (f[i] < 0: none, 0 returned; a feature of matrix 1 may also be
+// given as f + splits * 16 * M with mat = 0).  The shares are added in split
+// order; the loads of W shares of every feature are issued together.
+template <int N, int W>
+PE_DEV void sum_parts(const DecGemm& g, int mat, int t, const int (&f)[N], float (&out)[N]) {
+  const float* p = g.out + (static_cast<size_t>(mat) * g.splits * kDecodeRows + t) * g.M;
   const size_t stride = static_cast<size_t>(kDecodeRows) * g.M;
-  float acc = 0.f;
-  for (int k = 0; k < g.splits; ++k) acc += p[k * stride];
-  return acc;
+#pragma unroll
+  for (int i = 0; i < N; ++i) out[i] = 0.f;
+  for (int k0 = 0; k0 < g.splits; k0 += W) {
+    float v[N][W];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+#pragma unroll
+      for (int k = 0; k < W; ++k)
+        v[i][k] = (f[i] >= 0 && k0 + k < g.splits) ? p[(k0 + k) * stride + f[i]] : 0.f;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+#pragma unroll
+      for (int k = 0; k < W; ++k)
+        if (k0 + k < g.splits) out[i] += v[i][k];
+  }
 }
 
-// 1 / rms of row t from its per-chunk sums of squares (one warp, all lanes get it).
-PE_DEV float row_inv_rms(const float* ss, int t, int d, float eps) {
+// Row norms in two steps, so that the loads go out beside the others: this
+// lane's share of row t's per-chunk sums of squares (chunks lane and lane + 32),
+// then 1 / rms from the warp's shares.
+PE_DEV float ss_share(const float* ss, int t, int nc) {
   const int lane = threadIdx.x & 31;
-  const int nc = (d + kChunk - 1) / kChunk;
   float s = 0.f;
-  for (int c = lane; c < nc; c += 32) s += ss[t * 64 + c];
-  s = warp_sum(s);
+  if (lane < nc) s += ss[t * 64 + lane];
+  if (lane + 32 < nc) s += ss[t * 64 + lane + 32];
+  return s;
+}
+
+PE_DEV float inv_rms(float share, int d, float eps) {
+  const float s = warp_sum(share);
   return 1.0f / sqrtf(s / static_cast<float>(d) + eps);
 }
 
 // The sample row (r * K + k) non-rejected row v is, or -1: one of the last K
-// non-rejected rows of its request.
+// non-rejected rows of its request.  One warp-wide lookup (B <= 32); every lane
+// of the warp calls it with the same v.
 PE_DEV int sample_of(const DecParams& p, int v) {
-  for (int r = 0; r < p.B; ++r) {
-    const int v0 = p.valid_qsl[r], v1 = p.valid_qsl[r + 1];
-    if (v >= v0 && v < v1) {
-      const int k = v - (v1 - p.K);
-      return k >= 0 && k < p.K ? r * p.K + k : -1;
-    }
+  const int lane = threadIdx.x & 31;
+  int v0 = 0, v1 = 0;
+  if (lane < p.B) {
+    v0 = p.valid_qsl[lane];
+    v1 = p.valid_qsl[lane + 1];
   }
-  return -1;
+  const uint32_t hit = __ballot_sync(0xffffffffu, lane < p.B && v >= v0 && v < v1);
+  if (!hit) return -1;
+  const int r = __ffs(static_cast<int>(hit)) - 1;
+  const int k = v - (__shfl_sync(0xffffffffu, v1, r) - p.K);
+  return k >= 0 && k < p.K ? r * p.K + k : -1;
 }
 
 PE_DEV void store_pair(bf16* hi, bf16* lo, size_t i, float v) {
@@ -211,65 +245,115 @@ PE_DEV void store_pair(bf16* hi, bf16* lo, size_t i, float v) {
   lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
-// Sum of x over the 128 elementwise threads (4 warps); `red` holds 4 floats.
-PE_DEV float sum128(float x, float* red) {
+// Sums of x[i] over the 128 elementwise threads (4 warps); `red` holds 4 * N floats.
+template <int N>
+PE_DEV void sum128(float (&x)[N], float* red) {
   const int ew = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31;
-  x = warp_sum(x);
+#pragma unroll
+  for (int i = 0; i < N; ++i) x[i] = warp_sum(x[i]);
   named_bar_sync(2, 128);
-  if (lane == 0) red[ew] = x;
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < N; ++i) red[i * 4 + ew] = x[i];
   named_bar_sync(2, 128);
-  return red[0] + red[1] + red[2] + red[3];
+#pragma unroll
+  for (int i = 0; i < N; ++i) x[i] = red[i * 4] + red[i * 4 + 1] + red[i * 4 + 2] + red[i * 4 + 3];
 }
 
 // ---------------------------------------------------------------- elementwise stages
+//
+// The units of a stage are (row, group of up to kMaxCG consecutive 128-feature
+// chunks): groups wide enough that the units fit one round of the grid, each
+// thread one feature of every chunk of its unit, all loads issued together.
+constexpr int kMaxCG = 2;
+
+PE_DEV int chunks_per_unit(int rows, int nc) {
+  const int cg = (rows * nc + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  return min(max(cg, 1), kMaxCG);
+}
+
+// Features of unit chunk group c0 .. c0 + cg - 1 for this thread (j), -1 past
+// the group or past M.
+PE_DEV void unit_features(int c0, int cg, int M, int (&f)[kMaxCG]) {
+  const int j = threadIdx.x - 64;
+#pragma unroll
+  for (int i = 0; i < kMaxCG; ++i) {
+    const int ff = (c0 + i) * kChunk + j;
+    f[i] = (i < cg && ff < M) ? ff : -1;
+  }
+}
 
 // Part 1, after fc: x = the fc shares' sum for non-rejected row v; the QKV
 // operand (x * gamma_in pre-norm, x post-norm) as a bf16 pair; x of the sample
 // rows (the attention residual); per-chunk sums of squares of x (pre-norm).
 PE_DEV void stage_after_fc(const DecParams& p, int n_rows, float* red) {
-  const int j = threadIdx.x - 64;
   const int nc = (p.d + kChunk - 1) / kChunk;
-  for (int u = blockIdx.x; u < n_rows * nc; u += gridDim.x) {
-    const int v = u / nc, c = u - v * nc;
-    const int f = c * kChunk + j;
-    float x = 0.f;
-    if (f < p.d) {
-      x = sum_parts(p.g[0], 0, v, f);
-      const float opv = p.post_norm ? x : x * __bfloat162float(p.gamma_a[f]);
-      store_pair(p.op_hi, p.op_lo, static_cast<size_t>(v) * p.d + f, opv);
-      const int s = sample_of(p, v);
-      if (s >= 0) p.x_s[static_cast<size_t>(s) * p.d + f] = x;
+  const int cg = chunks_per_unit(n_rows, nc);
+  const int ngr = (nc + cg - 1) / cg;
+  for (int u = blockIdx.x; u < n_rows * ngr; u += gridDim.x) {
+    const int v = u / ngr, c0 = (u - v * ngr) * cg;
+    int f[kMaxCG];
+    unit_features(c0, cg, p.d, f);
+    float x[kMaxCG], sq[kMaxCG];
+    sum_parts<kMaxCG, 16>(p.g[0], 0, v, f, x);
+    const int s = sample_of(p, v);
+#pragma unroll
+    for (int i = 0; i < kMaxCG; ++i) {
+      sq[i] = 0.f;
+      if (f[i] < 0) continue;
+      const float opv = p.post_norm ? x[i] : x[i] * __bfloat162float(p.gamma_a[f[i]]);
+      store_pair(p.op_hi, p.op_lo, static_cast<size_t>(v) * p.d + f[i], opv);
+      if (s >= 0) p.x_s[static_cast<size_t>(s) * p.d + f[i]] = x[i];
+      sq[i] = x[i] * x[i];
     }
     if (!p.post_norm) {
-      const float t = sum128(x * x, red);
-      if (j == 0) p.ss[v * 64 + c] = t;
+      sum128(sq, red);
+      if (threadIdx.x == 64)
+#pragma unroll
+        for (int i = 0; i < kMaxCG; ++i)
+          if (i < cg && c0 + i < nc) p.ss[v * 64 + c0 + i] = sq[i];
     }
   }
 }
 
 // Part 1, after QKV: one warp per (non-rejected row, head): the QKV shares'
 // sum, scaled by the row's 1/rms (pre-norm), RoPE on q and k, q of the sample
-// rows, k and v at the row's cache slot.
+// rows, k and v at the row's cache slot.  Lane l rotates the pairs (i, i + hd/2)
+// for i = l and l + 32 (hd <= 128).
 PE_DEV void stage_rope(const DecParams& p, int n_rows) {
   const int lane = threadIdx.x & 31;
   const int ew = (threadIdx.x >> 5) - 2;
   const int heads = p.H + 2 * p.G;
   const int half = p.hd / 2;
+  const int nc = (p.d + kChunk - 1) / kChunk;
+  constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
+  constexpr double kTwoPi = 6.283185307179586476925286766559;
   for (int u = blockIdx.x * 4 + ew; u < n_rows * heads; u += gridDim.x * 4) {
     const int v = u / heads, hh = u - v * heads;
-    const float sc = p.post_norm ? 1.f : row_inv_rms(p.ss, v, p.d, p.eps);
-    const int o = p.valid_rows[v];
+    const int o = p.valid_rows[v];  // (its pos and slot are read below)
+    const float share = p.post_norm ? 0.f : ss_share(p.ss, v, nc);
+    int f[4];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int i = lane + 32 * q;
+      f[2 * q] = i < half ? hh * p.hd + i : -1;
+      f[2 * q + 1] = i < half ? hh * p.hd + i + half : -1;
+    }
+    float x[4];
+    sum_parts<4, 8>(p.g[1], 0, v, f, x);
+    const int s = hh < p.H ? sample_of(p, v) : -1;
     const int64_t pos = p.pos[o];
     const int64_t slot = p.slot[o];
+    const float sc = p.post_norm ? 1.f : inv_rms(share, p.d, p.eps);
     const bool slot_ok = slot >= 0 && slot < static_cast<int64_t>(p.num_blocks) * p.bs;
     if (!slot_ok && slot != PE_PADDING_SLOT_ID && lane == 0 && hh == 0)
       set_status(p.status, PE_ST_BLOCK_RANGE);
     const int64_t blk = slot_ok ? slot / p.bs : 0, off = slot_ok ? slot % p.bs : 0;
-    const int s = hh < p.H ? sample_of(p, v) : -1;
-    for (int i = lane; i < half; i += 32) {
-      const int e1 = hh * p.hd + i, e2 = e1 + half;
-      const float x1 = sc * sum_parts(p.g[1], 0, v, e1);
-      const float x2 = sc * sum_parts(p.g[1], 0, v, e2);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int i = lane + 32 * q;
+      if (i >= half) continue;
+      const float x1 = sc * x[2 * q], x2 = sc * x[2 * q + 1];
       if (hh >= p.H + p.G) {  // v: no rotation
         if (slot_ok) {
           bf16* vc = p.v_cache + ((blk * p.G + (hh - p.H - p.G)) * p.bs + off) * p.hd;
@@ -279,17 +363,16 @@ PE_DEV void stage_rope(const DecParams& p, int n_rows) {
         continue;
       }
       const double ang = static_cast<double>(pos) * p.inv_freq[i];
-      const double two_pi = 6.283185307179586476925286766559;
-      const double red = ang - two_pi * rint(ang / two_pi);
+      const double red = ang - kTwoPi * rint(ang * kInvTwoPi);
       float sn, cs;
       sincosf(static_cast<float>(red), &sn, &cs);
       const float y1 = x1 * cs - x2 * sn;
       const float y2 = x2 * cs + x1 * sn;
       if (hh < p.H) {
         if (s >= 0) {
-          bf16* q = p.q_s + (static_cast<size_t>(s) * p.H + hh) * p.hd;
-          q[i] = __float2bfloat16_rn(y1);
-          q[i + half] = __float2bfloat16_rn(y2);
+          bf16* qd = p.q_s + (static_cast<size_t>(s) * p.H + hh) * p.hd;
+          qd[i] = __float2bfloat16_rn(y1);
+          qd[i + half] = __float2bfloat16_rn(y2);
         }
       } else if (slot_ok) {
         bf16* kc = p.k_cache + ((blk * p.G + (hh - p.H)) * p.bs + off) * p.hd;
@@ -303,36 +386,64 @@ PE_DEV void stage_rope(const DecParams& p, int n_rows) {
 // Part 2, after O: r = x_s + the O shares' sum; the MLP operand r * gamma_post
 // as a bf16 pair; per-chunk sums of squares of r.
 PE_DEV void stage_after_o(const DecParams& p, float* red) {
-  const int j = threadIdx.x - 64;
   const int nc = (p.d + kChunk - 1) / kChunk;
-  for (int u = blockIdx.x; u < p.rows_cap * nc; u += gridDim.x) {
-    const int s = u / nc, c = u - s * nc;
-    const int f = c * kChunk + j;
-    float rv = 0.f;
-    if (f < p.d) {
-      const size_t i = static_cast<size_t>(s) * p.d + f;
-      rv = p.x_s[i] + sum_parts(p.g[0], 0, s, f);
-      p.r[i] = rv;
-      store_pair(p.op_hi, p.op_lo, i, rv * __bfloat162float(p.gamma_a[f]));
+  const int cg = chunks_per_unit(p.rows_cap, nc);
+  const int ngr = (nc + cg - 1) / cg;
+  for (int u = blockIdx.x; u < p.rows_cap * ngr; u += gridDim.x) {
+    const int s = u / ngr, c0 = (u - s * ngr) * cg;
+    int f[kMaxCG];
+    unit_features(c0, cg, p.d, f);
+    float xs[kMaxCG], x[kMaxCG];
+#pragma unroll
+    for (int i = 0; i < kMaxCG; ++i)
+      xs[i] = f[i] >= 0 ? p.x_s[static_cast<size_t>(s) * p.d + f[i]] : 0.f;
+    sum_parts<kMaxCG, 16>(p.g[0], 0, s, f, x);
+#pragma unroll
+    for (int i = 0; i < kMaxCG; ++i) {
+      float rv = 0.f;
+      if (f[i] >= 0) {
+        const size_t k = static_cast<size_t>(s) * p.d + f[i];
+        rv = xs[i] + x[i];
+        p.r[k] = rv;
+        store_pair(p.op_hi, p.op_lo, k, rv * __bfloat162float(p.gamma_a[f[i]]));
+      }
+      x[i] = rv * rv;
     }
-    const float t = sum128(rv * rv, red);
-    if (j == 0) p.ss[s * 64 + c] = t;
+    sum128(x, red);
+    if (threadIdx.x == 64)
+#pragma unroll
+      for (int i = 0; i < kMaxCG; ++i)
+        if (i < cg && c0 + i < nc) p.ss[s * 64 + c0 + i] = x[i];
   }
 }
 
 // Part 2, after gate/up: h = silu(g) * u with g, u the shares' sums scaled by
 // the row's 1/rms (the MLP input is RMSNorm(r) * gamma_post), as a bf16 pair.
 PE_DEV void stage_swiglu(const DecParams& p) {
-  const int j = threadIdx.x - 64;
   const int nc = (p.inter + kChunk - 1) / kChunk;
-  for (int u = blockIdx.x; u < p.rows_cap * nc; u += gridDim.x) {
-    const int s = u / nc, c = u - s * nc;
-    const int f = c * kChunk + j;
-    const float sc = row_inv_rms(p.ss, s, p.d, p.eps);
-    if (f < p.inter) {
-      const float gv = sc * sum_parts(p.g[1], 0, s, f);
-      const float uv = sc * sum_parts(p.g[1], 1, s, f);
-      store_pair(p.h_hi, p.h_lo, static_cast<size_t>(s) * p.inter + f,
+  const int ncd = (p.d + kChunk - 1) / kChunk;
+  const int cg = chunks_per_unit(p.rows_cap, nc);
+  const int ngr = (nc + cg - 1) / cg;
+  const int up = p.g[1].splits * kDecodeRows * p.g[1].M;  // matrix 1 as a feature offset
+  for (int u = blockIdx.x; u < p.rows_cap * ngr; u += gridDim.x) {
+    const int s = u / ngr, c0 = (u - s * ngr) * cg;
+    const float share = ss_share(p.ss, s, ncd);
+    int f[kMaxCG], fgu[2 * kMaxCG];
+    unit_features(c0, cg, p.inter, f);
+#pragma unroll
+    for (int i = 0; i < kMaxCG; ++i) {
+      fgu[i] = f[i];
+      fgu[kMaxCG + i] = f[i] >= 0 ? f[i] + up : -1;
+    }
+    float x[2 * kMaxCG];
+    sum_parts<2 * kMaxCG, 8>(p.g[1], 0, s, fgu, x);
+    const float sc = inv_rms(share, p.d, p.eps);
+#pragma unroll
+    for (int i = 0; i < kMaxCG; ++i) {
+      if (f[i] < 0) continue;
+      const float gv = sc * x[i];
+      const float uv = sc * x[kMaxCG + i];
+      store_pair(p.h_hi, p.h_lo, static_cast<size_t>(s) * p.inter + f[i],
                  gv / (1.0f + expf(-gv)) * uv);
     }
   }
@@ -341,38 +452,62 @@ PE_DEV void stage_swiglu(const DecParams& p) {
 // Part 2, after down: y = residual + the down shares' sum (residual: r
 // pre-norm; RMSNorm(r) * gamma_post post-norm); per-chunk sums of squares of y.
 PE_DEV void stage_after_down(const DecParams& p, float* red) {
-  const int j = threadIdx.x - 64;
   const int nc = (p.d + kChunk - 1) / kChunk;
-  for (int u = blockIdx.x; u < p.rows_cap * nc; u += gridDim.x) {
-    const int s = u / nc, c = u - s * nc;
-    const int f = c * kChunk + j;
-    const float sc = p.post_norm ? row_inv_rms(p.ss, s, p.d, p.eps) : 1.f;
-    float yv = 0.f;
-    if (f < p.d) {
-      const size_t i = static_cast<size_t>(s) * p.d + f;
-      const float res = p.post_norm ? sc * p.r[i] * __bfloat162float(p.gamma_a[f]) : p.r[i];
-      yv = res + sum_parts(p.g[2], 0, s, f);
-      p.y[i] = yv;
+  const int cg = chunks_per_unit(p.rows_cap, nc);
+  const int ngr = (nc + cg - 1) / cg;
+  for (int u = blockIdx.x; u < p.rows_cap * ngr; u += gridDim.x) {
+    const int s = u / ngr, c0 = (u - s * ngr) * cg;
+    const float share = p.post_norm ? ss_share(p.ss, s, nc) : 0.f;
+    int f[kMaxCG];
+    unit_features(c0, cg, p.d, f);
+    float rr[kMaxCG], x[kMaxCG];
+#pragma unroll
+    for (int i = 0; i < kMaxCG; ++i)
+      rr[i] = f[i] >= 0 ? p.r[static_cast<size_t>(s) * p.d + f[i]] : 0.f;
+    sum_parts<kMaxCG, 16>(p.g[2], 0, s, f, x);
+    const float sc = p.post_norm ? inv_rms(share, p.d, p.eps) : 1.f;
+#pragma unroll
+    for (int i = 0; i < kMaxCG; ++i) {
+      float yv = 0.f;
+      if (f[i] >= 0) {
+        const size_t k = static_cast<size_t>(s) * p.d + f[i];
+        const float res = p.post_norm ? sc * rr[i] * __bfloat162float(p.gamma_a[f[i]]) : rr[i];
+        yv = res + x[i];
+        p.y[k] = yv;
+      }
+      x[i] = yv * yv;
     }
-    const float t = sum128(yv * yv, red);
-    if (j == 0) p.ss2[s * 64 + c] = t;
+    sum128(x, red);
+    if (threadIdx.x == 64)
+#pragma unroll
+      for (int i = 0; i < kMaxCG; ++i)
+        if (i < cg && c0 + i < nc) p.ss2[s * 64 + c0 + i] = x[i];
   }
 }
 
 // Part 2, last: z = RMSNorm(y) * gamma_final (bf16) and the hidden state handed
 // on (y pre-norm, the normalised value post-norm).
 PE_DEV void stage_final(const DecParams& p) {
-  const int j = threadIdx.x - 64;
   const int nc = (p.d + kChunk - 1) / kChunk;
-  for (int u = blockIdx.x; u < p.rows_cap * nc; u += gridDim.x) {
-    const int s = u / nc, c = u - s * nc;
-    const int f = c * kChunk + j;
-    const float sc = row_inv_rms(p.ss2, s, p.d, p.eps);
-    if (f < p.d) {
-      const size_t i = static_cast<size_t>(s) * p.d + f;
-      const float zf = p.y[i] * sc * __bfloat162float(p.gamma_b[f]);
-      p.z[i] = __float2bfloat16_rn(zf);
-      if (p.hidden_out) p.hidden_out[i] = p.post_norm ? zf : p.y[i];
+  const int cg = chunks_per_unit(p.rows_cap, nc);
+  const int ngr = (nc + cg - 1) / cg;
+  for (int u = blockIdx.x; u < p.rows_cap * ngr; u += gridDim.x) {
+    const int s = u / ngr, c0 = (u - s * ngr) * cg;
+    const float share = ss_share(p.ss2, s, nc);
+    int f[kMaxCG];
+    unit_features(c0, cg, p.d, f);
+    float yv[kMaxCG];
+#pragma unroll
+    for (int i = 0; i < kMaxCG; ++i)
+      yv[i] = f[i] >= 0 ? p.y[static_cast<size_t>(s) * p.d + f[i]] : 0.f;
+    const float sc = inv_rms(share, p.d, p.eps);
+#pragma unroll
+    for (int i = 0; i < kMaxCG; ++i) {
+      if (f[i] < 0) continue;
+      const size_t k = static_cast<size_t>(s) * p.d + f[i];
+      const float zf = yv[i] * sc * __bfloat162float(p.gamma_b[f[i]]);
+      p.z[k] = __float2bfloat16_rn(zf);
+      if (p.hidden_out) p.hidden_out[k] = p.post_norm ? zf : yv[i];
     }
   }
 }
@@ -383,13 +518,13 @@ PE_DEV void stage_final(const DecParams& p) {
 // [SwiGLU], down, [after down], [final].  The barrier word after GEMM stage
 // `gs` (its partial tiles stored) and after each elementwise stage.
 template <int PART>
-__global__ void __launch_bounds__(kThreads, 3) decode_layer_kernel(const __grid_constant__ DecParams p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_layer_kernel(const __grid_constant__ DecParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kSlots], empty_bar[kSlots], tfull_bar, tempty_bar,
       final_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, ok_sh;
-  __shared__ float red_sh[4];
+  __shared__ float red_sh[4 * kMaxCG];
   __shared__ uint32_t epoch_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -814,6 +949,7 @@ int launch_decode_layer(const DecodeLaunch& L, int part, cudaStream_t st) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemBytes)) != cudaSuccess)
     return PE_ERR_CUDA;
+
   return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, p) == cudaSuccess
              ? PE_OK
              : PE_ERR_CUDA;
