@@ -30,7 +30,7 @@ struct pe_handle {
   pe_weights w;
   int num_sms;
   CUtensorMap m_fc, m_qkv, m_o, m_gate, m_up, m_down, m_lm;
-  double inv_freq[64];
+  uint64_t rope_turn[64];  // RoPE frequencies as fractions of a turn (rope_cos_sin)
   bool has_layer;  // false: metadata / drafter-input handle without layer weights
   int n_layers;
   LayerSlot more[PE_MAX_LAYERS - 1];  // layers 2..n_layers
@@ -476,7 +476,7 @@ int decode_layer_step(const StepCtx& c, int Kd, int B, int T_in, const pe_meta* 
   dl.post_norm = d.post_norm;
   dl.num_sms = h->num_sms;
   dl.eps = d.eps;
-  std::memcpy(dl.inv_freq, h->inv_freq, sizeof(dl.inv_freq));
+  std::memcpy(dl.rope_turn, h->rope_turn, sizeof(dl.rope_turn));
   dl.m_fc = &h->m_fc;
   dl.m_qkv = &h->m_qkv;
   dl.m_o = &h->m_o;
@@ -558,7 +558,7 @@ int one_layer_step(const StepCtx& c, int Kd, int B, int T_in, const pe_meta* met
   ra.v_cache = v_cache;
   ra.q_s = c.q_s;
   ra.x_s = c.x_s;
-  std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
+  std::memcpy(ra.rope_turn, h->rope_turn, sizeof(ra.rope_turn));
   ra.status = c.status;
   if ((rc = launch_rope_kv(ra, c.dt, c.st)) != PE_OK) return rc;
   // paged attention of the sample rows
@@ -686,7 +686,7 @@ int layers_step(const StepCtx& c, int B, int T_in, const pe_meta* meta, const vo
     ra.x_s = first ? c.x_s : nullptr;  // later layers' residual is already xl
     ra.padded_in = first ? 0 : 1;
     ra.must_fit = 1;
-    std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
+    std::memcpy(ra.rope_turn, h->rope_turn, sizeof(ra.rope_turn));
     ra.status = c.status;
     if ((rc = launch_rope_kv(ra, c.dt, c.st)) != PE_OK) return rc;
     AttnArgs aa{};
@@ -894,9 +894,14 @@ int pe_create(const pe_dims* dims, const pe_weights* w, pe_handle** out) {
     delete h;
     return PE_ERR_CUDA;
   }
-  for (int i = 0; i < d.head_dim / 2; ++i)
-    h->inv_freq[i] = std::pow(static_cast<double>(d.rope_theta),
-                              -2.0 * static_cast<double>(i) / static_cast<double>(d.head_dim));
+  // RoPE frequency i, theta^(-2i/hd) radians per position, as the fraction of a
+  // turn per position in 64-bit fixed point (below 1/(2 pi) of a turn: no whole turns)
+  for (int i = 0; i < d.head_dim / 2; ++i) {
+    const double inv_freq = std::pow(static_cast<double>(d.rope_theta),
+                                     -2.0 * static_cast<double>(i) / static_cast<double>(d.head_dim));
+    const double turn = inv_freq / 6.283185307179586476925286766559;
+    h->rope_turn[i] = static_cast<uint64_t>(std::ldexp(turn - std::floor(turn), 64));
+  }
   if (bf && has_layer) {
     std::vector<CUtensorMap*> maps = {&h->m_fc, &h->m_qkv, &h->m_o,   &h->m_gate,
                                       &h->m_up, &h->m_down, &h->m_lm};

@@ -107,6 +107,17 @@ inline cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, siz
 
 // ---------------------------------------------------------------- small utilities
 
+// cos and sin of the RoPE angle pos * inv_freq.  turn = inv_freq / (2 pi) as a
+// 64-bit fixed-point fraction of a turn (host side); pos * turn mod 2^64 is the
+// angle's fraction of a turn, reduced exactly by the integer wrap however large
+// pos is.  Its top 32 bits, read as a signed fraction in [-1/2, 1/2), go to
+// sincospif.  No double-precision arithmetic on the device.
+PE_DEV void rope_cos_sin(int64_t pos, uint64_t turn, float& c, float& s) {
+  const uint64_t ph = static_cast<uint64_t>(pos) * turn;
+  const int32_t top = static_cast<int32_t>(ph >> 32);
+  sincospif(__int2float_rn(top) * 0x1p-31f, &s, &c);
+}
+
 PE_DEV void set_status(uint32_t* st, uint32_t bits) {
   if (st) atomicOr(st, bits);
 }
@@ -279,58 +290,6 @@ PE_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 PE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 PE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// ---------------------------------------------------------------- tcgen05, CTA pairs
-//
-// A cluster of two CTAs on two SMs runs M = 256 MMAs together: each CTA keeps
-// 128 rows of A and half of the N rows of B in its own shared memory (at the
-// same offsets in both) and its own 128 TMEM lanes of the accumulator; rank 0
-// issues the MMAs.  Every tcgen05 instruction of such a kernel names
-// cta_group::2.
-
-// Allocation in both CTAs at once: one whole warp of each CTA executes it.
-PE_DEV void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(dst)),
-               "r"(ncols)
-               : "memory");
-}
-PE_DEV void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-PE_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-// D[tmem of both CTAs] (+)= A * B^T over the pair (M = 256), issued by rank 0.
-PE_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on the barrier at `bar`'s offset in both CTAs of the pair once every
-// tcgen05 operation issued so far by this thread is done.
-PE_DEV void umma_commit_pair_both(uint64_t* bar) {
-  const uint16_t both = 3;
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(both)
-      : "memory");
-}
-// ... on this CTA's own barrier only.
-PE_DEV void umma_commit_pair_local(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
 // Shared-memory matrix descriptor of a K-major bf16 tile stored with the
 // 128-byte swizzle (rows of 64 elements = 128 bytes, 8-row atoms of 1024 bytes).
 // Fields: start address >> 4 (bits 0-13), leading-dimension offset (16-29,
@@ -403,47 +362,6 @@ PE_DEV uint32_t cluster_ctarank() {
 PE_DEV void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
-}
-
-// Address, in the cluster's shared window, of the variable at `p`'s offset in
-// CTA `rank` of the cluster.
-PE_DEV uint32_t cluster_addr_of(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-
-// Arrive on an mbarrier of any CTA of the cluster, releasing this thread's
-// earlier writes to the cluster.
-PE_DEV void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                   bar_cluster_addr)
-               : "memory");
-}
-
-// mbar_wait for barriers that other CTAs of the cluster arrive on: acquires
-// what they released.
-PE_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-PE_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitNs) return false;
-    }
-  }
 }
 
 // Load a float from the shared memory of CTA `rank` of this cluster, at the

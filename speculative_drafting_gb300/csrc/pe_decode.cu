@@ -109,7 +109,7 @@ struct DecParams {
   float* hidden_out;       // [B*K][d], nullable: the state handed to the next pass
   uint32_t* bar;           // BW_COUNT barrier words
   uint32_t* status;
-  double inv_freq[64];
+  uint64_t rope_turn[64];
 };
 
 PE_DEV uint32_t ld_acquire(const uint32_t* p) {
@@ -286,7 +286,7 @@ PE_DEV void unit_features(int c0, int cg, int M, int (&f)[kMaxCG]) {
 // Part 1, after fc: x = the fc shares' sum for non-rejected row v; the QKV
 // operand (x * gamma_in pre-norm, x post-norm) as a bf16 pair; x of the sample
 // rows (the attention residual); per-chunk sums of squares of x (pre-norm).
-PE_DEV void stage_after_fc(const DecParams& p, int n_rows, float* red) {
+PE_DEV void stage_after_fc(const DecParams& p, int n_rows, float* red, int s_first) {
   const int nc = (p.d + kChunk - 1) / kChunk;
   const int cg = chunks_per_unit(n_rows, nc);
   const int ngr = (nc + cg - 1) / cg;
@@ -296,7 +296,7 @@ PE_DEV void stage_after_fc(const DecParams& p, int n_rows, float* red) {
     unit_features(c0, cg, p.d, f);
     float x[kMaxCG], sq[kMaxCG];
     sum_parts<kMaxCG, 16>(p.g[0], 0, v, f, x);
-    const int s = sample_of(p, v);
+    const int s = u == static_cast<int>(blockIdx.x) ? s_first : sample_of(p, v);
 #pragma unroll
     for (int i = 0; i < kMaxCG; ++i) {
       sq[i] = 0.f;
@@ -316,21 +316,46 @@ PE_DEV void stage_after_fc(const DecParams& p, int n_rows, float* red) {
   }
 }
 
+// The metadata of a warp's first RoPE unit (row v, head hh): the row's index in
+// the step's row arrays, its position and cache slot, and its sample row (q
+// heads).  Loaded while fc streams, so the RoPE stage waits only for its sums.
+struct RopeMeta {
+  int u, o, s;
+  int64_t pos, slot;
+};
+
+PE_DEV RopeMeta rope_meta(const DecParams& p, int n_rows) {
+  const int heads = p.H + 2 * p.G;
+  RopeMeta m;
+  m.u = blockIdx.x * 4 + ((threadIdx.x >> 5) - 2);
+  m.o = 0;
+  m.s = -1;
+  m.pos = 0;
+  m.slot = PE_PADDING_SLOT_ID;
+  if (m.u < n_rows * heads) {
+    const int v = m.u / heads, hh = m.u - (m.u / heads) * heads;
+    m.o = p.valid_rows[v];
+    m.s = hh < p.H ? sample_of(p, v) : -1;
+    m.pos = p.pos[m.o];
+    m.slot = p.slot[m.o];
+  }
+  return m;
+}
+
 // Part 1, after QKV: one warp per (non-rejected row, head): the QKV shares'
 // sum, scaled by the row's 1/rms (pre-norm), RoPE on q and k, q of the sample
 // rows, k and v at the row's cache slot.  Lane l rotates the pairs (i, i + hd/2)
 // for i = l and l + 32 (hd <= 128).
-PE_DEV void stage_rope(const DecParams& p, int n_rows) {
+PE_DEV void stage_rope(const DecParams& p, int n_rows, const RopeMeta& first) {
   const int lane = threadIdx.x & 31;
   const int ew = (threadIdx.x >> 5) - 2;
   const int heads = p.H + 2 * p.G;
   const int half = p.hd / 2;
   const int nc = (p.d + kChunk - 1) / kChunk;
-  constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
-  constexpr double kTwoPi = 6.283185307179586476925286766559;
   for (int u = blockIdx.x * 4 + ew; u < n_rows * heads; u += gridDim.x * 4) {
     const int v = u / heads, hh = u - v * heads;
-    const int o = p.valid_rows[v];  // (its pos and slot are read below)
+    const bool pre = u == first.u;
+    const int o = pre ? first.o : p.valid_rows[v];
     const float share = p.post_norm ? 0.f : ss_share(p.ss, v, nc);
     int f[4];
 #pragma unroll
@@ -341,9 +366,9 @@ PE_DEV void stage_rope(const DecParams& p, int n_rows) {
     }
     float x[4];
     sum_parts<4, 8>(p.g[1], 0, v, f, x);
-    const int s = hh < p.H ? sample_of(p, v) : -1;
-    const int64_t pos = p.pos[o];
-    const int64_t slot = p.slot[o];
+    const int s = pre ? first.s : (hh < p.H ? sample_of(p, v) : -1);
+    const int64_t pos = pre ? first.pos : p.pos[o];
+    const int64_t slot = pre ? first.slot : p.slot[o];
     const float sc = p.post_norm ? 1.f : inv_rms(share, p.d, p.eps);
     const bool slot_ok = slot >= 0 && slot < static_cast<int64_t>(p.num_blocks) * p.bs;
     if (!slot_ok && slot != PE_PADDING_SLOT_ID && lane == 0 && hh == 0)
@@ -362,10 +387,8 @@ PE_DEV void stage_rope(const DecParams& p, int n_rows) {
         }
         continue;
       }
-      const double ang = static_cast<double>(pos) * p.inv_freq[i];
-      const double red = ang - kTwoPi * rint(ang * kInvTwoPi);
       float sn, cs;
-      sincosf(static_cast<float>(red), &sn, &cs);
+      rope_cos_sin(pos, p.rope_turn[i], cs, sn);
       const float y1 = x1 * cs - x2 * sn;
       const float y2 = x2 * cs + x1 * sn;
       if (hh < p.H) {
@@ -766,11 +789,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_layer_kernel(cons
       return ok_sh != 0;
     };
     if (PART == 1) {
+      // the row metadata of this CTA's first units, read while fc streams
+      const RopeMeta rmeta = rope_meta(p, n_rows);
+      int s_first = -1;
+      {
+        const int nc = (p.d + kChunk - 1) / kChunk;
+        const int cg = chunks_per_unit(n_rows, nc);
+        const int ngr = (nc + cg - 1) / cg;
+        if (static_cast<int>(blockIdx.x) < n_rows * ngr) s_first = sample_of(p, blockIdx.x / ngr);
+      }
       ok = gemm_epilogue(0) && barrier(wbase + 0, true);
-      if (ok) stage_after_fc(p, n_rows, red_sh);
+      if (ok) stage_after_fc(p, n_rows, red_sh, s_first);
       ok = ok && barrier(wbase + 1, false);
       ok = ok && gemm_epilogue(1) && barrier(wbase + 2, true);
-      if (ok) stage_rope(p, n_rows);
+      if (ok) stage_rope(p, n_rows, rmeta);
     } else {
       ok = gemm_epilogue(0) && barrier(wbase + 0, true);
       if (ok) stage_after_o(p, red_sh);
@@ -899,7 +931,7 @@ int launch_decode_layer(const DecodeLaunch& L, int part, cudaStream_t st) {
   p.ss2 = ss2;
   p.bar = L.bar;
   p.status = L.status;
-  std::memcpy(p.inv_freq, L.inv_freq, sizeof(p.inv_freq));
+  std::memcpy(p.rope_turn, L.rope_turn, sizeof(p.rope_turn));
   auto map_x = [&](CUtensorMap* m, const void* X, int rows_cap, int cols) {
     return encode_tmap_bf16(m, X, static_cast<uint64_t>(rows_cap), static_cast<uint64_t>(cols),
                             kDecodeRows);

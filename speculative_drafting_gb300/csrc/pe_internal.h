@@ -124,7 +124,7 @@ constexpr int kDecodeRows = 16;
 struct DecodeLaunch {
   int d, H, G, hd, inter, K, B, T_out, bs, num_blocks, post_norm, num_sms;
   float eps;
-  double inv_freq[64];
+  uint64_t rope_turn[64];
   const CUtensorMap* m_fc;
   const CUtensorMap* m_qkv;
   const CUtensorMap* m_o;

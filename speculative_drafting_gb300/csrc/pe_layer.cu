@@ -222,11 +222,8 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
     }
   }
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    const double ang = static_cast<double>(p) * a.inv_freq[i];
-    const double two_pi = 6.283185307179586476925286766559;
-    const double red = ang - two_pi * rint(ang / two_pi);
     float s, c;
-    sincosf(static_cast<float>(red), &s, &c);
+    rope_cos_sin(p, a.rope_turn[i], c, s);
     cs[i] = c;
     sn[i] = s;
   }

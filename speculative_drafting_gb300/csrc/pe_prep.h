@@ -141,7 +141,7 @@ struct RopeArgs {
   void* v_cache;
   void* q_s;    // [B*K][H][hd] queries of the sample rows
   float* x_s;  // [B*K][d] fc output of the sample rows (residual, fp32); nullable
-  double inv_freq[64];
+  uint64_t rope_turn[64];  // fractions of a turn per position (rope_cos_sin)
   // 0: qkv rows are the non-rejected rows in valid_rows order (K is then the
   // number of rows per request that q_s / x_s keep, right-aligned);
   // 1: qkv rows are already in that right-aligned layout, B*K rows (rows of a
