@@ -318,10 +318,13 @@ PE_DEV void stage_after_fc(const DecParams& p, int n_rows, float* red, int s_fir
 
 // The metadata of a warp's first RoPE unit (row v, head hh): the row's index in
 // the step's row arrays, its position and cache slot, and its sample row (q
-// heads).  Loaded while fc streams, so the RoPE stage waits only for its sums.
+// heads); and this lane's two RoPE frequencies (a per-lane index into the
+// kernel parameters reads the constant bank lane by lane).  Loaded while fc
+// streams, so the RoPE stage waits only for its sums.
 struct RopeMeta {
   int u, o, s;
   int64_t pos, slot;
+  uint64_t turn[2];
 };
 
 PE_DEV RopeMeta rope_meta(const DecParams& p, int n_rows) {
@@ -332,6 +335,9 @@ PE_DEV RopeMeta rope_meta(const DecParams& p, int n_rows) {
   m.s = -1;
   m.pos = 0;
   m.slot = PE_PADDING_SLOT_ID;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) m.turn[q] = lane + 32 * q < p.hd / 2 ? p.rope_turn[lane + 32 * q] : 0ull;
   if (m.u < n_rows * heads) {
     const int v = m.u / heads, hh = m.u - (m.u / heads) * heads;
     m.o = p.valid_rows[v];
@@ -388,7 +394,7 @@ PE_DEV void stage_rope(const DecParams& p, int n_rows, const RopeMeta& first) {
         continue;
       }
       float sn, cs;
-      rope_cos_sin(pos, p.rope_turn[i], cs, sn);
+      rope_cos_sin(pos, first.turn[q], cs, sn);
       const float y1 = x1 * cs - x2 * sn;
       const float y2 = x2 * cs + x1 * sn;
       if (hh < p.H) {
