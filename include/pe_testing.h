@@ -60,6 +60,14 @@ int pe_test_projection(pe_handle* h, int which, const void* X, int n_rows, void*
  * word first (pe_read_status with clear set). */
 int pe_test_bounded_wait(void* ws, size_t ws_bytes, void* stream);
 
+/* Failure-detection check of the persistent decode layer (a bf16 one-layer step
+ * of at most 16 rows): the byte of the step workspace that holds the count of
+ * the layer's first kernel's completed launches within the step (uint32, zeroed
+ * by pe_prepare_inputs).  A test that sets it far ahead after pe_prepare_inputs
+ * makes that kernel's first grid barrier unreachable: its bounded wait runs out
+ * (2 s), PE_ST_TIMEOUT goes into the status word and every CTA leaves. */
+#define PE_TEST_DECODE_EPOCH_BYTE 112u
+
 #ifdef __cplusplus
 }
 #endif

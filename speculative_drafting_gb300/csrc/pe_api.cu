@@ -179,6 +179,8 @@ struct Layout {
 // Barrier words of the persistent decode layer: in the workspace header, after
 // the status word (the header's 256 bytes are cleared together).
 constexpr size_t kBarrierWordsOffset = 64;
+// the first kernel's launch count is barrier word 12 (pe_decode.cu)
+static_assert(kBarrierWordsOffset + 4 * 12 == PE_TEST_DECODE_EPOCH_BYTE, "decode epoch word");
 
 // Workspace layout of a step with B requests, T_in verify rows and block tables
 // of max_blocks entries.  Each region is sized by a bound that only grows with

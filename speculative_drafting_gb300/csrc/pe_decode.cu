@@ -72,6 +72,7 @@ enum : int {
   BW_ABORT = 14,    // set by a CTA whose wait ran out: every other CTA leaves
   BW_COUNT = 16,
 };
+static_assert(BW_EPOCH1 == 12, "PE_TEST_DECODE_EPOCH_BYTE names word 12 of the header");
 
 struct DecGemm {
   int M, K, num_kb, kbps, splits, m_tiles, n_mats, bpair, items;

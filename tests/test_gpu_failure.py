@@ -10,6 +10,7 @@ other requests of the batch (nothing mixes rows of different requests).
 """
 
 import ctypes
+import re
 import time
 
 import numpy as np
@@ -45,6 +46,39 @@ def test_wait_runs_out_and_the_context_survives():
     for rr, out in res["req"].items():
         sl = slice(rr * K, (rr + 1) * K)
         check_logits_and_draft("f32", logits[sl], draft[sl], out["logits"], where=f"request {rr}")
+
+
+def test_decode_layer_barrier_runs_out_and_the_context_survives():
+    """The persistent decode layer's grid barriers are bounded waits too: with the
+    first kernel's launch count set far ahead of its arrival counters, its first
+    barrier can never complete.  The wait runs out, every CTA of both layer
+    kernels leaves, the status says so, and after clearing the workspace header
+    the next step matches the oracle."""
+    torch = cuda_or_skip()
+    wl, b, w, kc, vc, r = setup("small_prenorm", batch=1, n_prev=8, K=7, ctx=(300,))
+    text = open(binding.TESTING_HEADER).read()
+    off = int(re.search(r"#define\s+PE_TEST_DECODE_EPOCH_BYTE\s+(\d+)u", text).group(1))
+    r.prepare()
+    torch.cuda.synchronize()
+    r.ws[off:off + 4].view(torch.int32).fill_(1 << 20)
+    t0 = time.perf_counter()
+    r.step()
+    r.argmax()
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    st, code = r.status(clear=True)
+    assert st & binding.PE_ST_TIMEOUT and code == binding.PE_ERR_TIMEOUT
+    assert 1.5 < waited < 30.0  # the 2 s limit, not a hang
+    # the same workspace, cleared: a whole step matches the oracle
+    r.run()
+    torch.cuda.synchronize()
+    assert r.status()[0] == 0
+    res = O.draft_step(wl.dims, w, b, kc, vc)
+    K = wl.dims.K
+    logits, draft = host(r.logits), host(r.draft)
+    for rr, out in res["req"].items():
+        sl = slice(rr * K, (rr + 1) * K)
+        check_logits_and_draft("bf16", logits[sl], draft[sl], out["logits"], where=f"request {rr}")
 
 
 def test_nan_hidden_states_stay_in_their_request():
