@@ -138,3 +138,36 @@ def test_random_steps(seed):
         sl = slice(rr * K, (rr + 1) * K)
         check_z("bf16", z[sl], out["z"], where=f"request {rr}")
         check_logits_and_draft("bf16", logits[sl], draft[sl], out["logits"], where=f"request {rr}")
+
+
+def test_bad_context_block_at_a_batch_of_several_waves():
+    """A context block id out of range in one request of a batch large enough that
+    attention runs as the persistent tensor-core kernel (160 requests x 2 KV heads):
+    the status word flags it, the step completes, the keys of that block are
+    skipped, and every other request still matches the oracle."""
+    torch = cuda_or_skip()
+    from speculative_drafting_gb300 import binding as Bnd
+
+    wl, b, w, kc, vc, r = setup("small_prenorm", batch=160, n_prev=6,
+                                ctx=("uniform", 100, 700), seed=11)
+    bad = 37
+    bs = wl.dims.block_size
+    assert int(b["ctx"][bad]) >= 3 * bs
+    # block 1 of the request holds context keys only: no row of this step writes
+    # there, so the attention is the one kernel that reads it
+    r.inp["block_table"][bad, 1] = int(b["num_blocks"]) + 5
+    r.run()
+    torch.cuda.synchronize()
+    st, rc = r.status()
+    assert st & Bnd.PE_ST_BLOCK_RANGE, hex(st)
+    assert not st & Bnd.PE_ST_TIMEOUT, hex(st)
+    assert rc == Bnd.PE_ERR_DEVICE_INPUT
+    K = wl.dims.K
+    logits, draft = host(r.logits), host(r.draft)
+    others = [0, 1, bad - 1, bad + 1, 100, 159]
+    res = O.draft_step(wl.dims, w, b, kc, vc, requests=others)
+    for rr in others:
+        sl = slice(rr * K, (rr + 1) * K)
+        check_logits_and_draft("bf16", logits[sl], draft[sl], res["req"][rr]["logits"],
+                               where=f"request {rr}")
+    assert ((draft[bad * K:(bad + 1) * K] >= 0) & (draft[bad * K:(bad + 1) * K] < wl.dims.vocab)).all()
