@@ -567,8 +567,10 @@ constexpr uint32_t kTcQCol = 192;       // Q (two bf16 per column), buffer b at 
 constexpr int kTcRows = 64;             // query rows per unit, at most
 constexpr int kTcUq = 4;                // ring of claimed unit ids
 constexpr float kTcRescale = 8.f;
-// dynamic + static shared memory + the 1 KB the system reserves, twice per SM
-static_assert(2 * (kTcSmem + 2048) <= 228 * 1024, "two tcgen05 attention CTAs per SM");
+constexpr int kTcOrdMax = 1024;         // requests whose units are claimed longest first
+// dynamic + static shared memory (the claim order, 8 bytes per request, and
+// the rest) + the 1 KB the system reserves, twice per SM
+static_assert(2 * (kTcSmem + 8 * kTcOrdMax + 2048) <= 228 * 1024, "two tcgen05 attention CTAs per SM");
 static_assert(2 * kTcTmemCols <= 512, "two tcgen05 attention CTAs per SM (tensor memory)");
 static_assert(kTcRows * 64 * 4 <= kTcRowBytes, "a unit's o rows fit the P tile");
 static_assert(kTcQCol + 64 <= kTcTmemCols, "both Q buffers fit the tensor memory");
@@ -703,18 +705,24 @@ PE_DEV TcUnit tc_unit_of(const AttnArgs& a, int4 e) {
   return x;
 }
 
-PE_DEV TcUnit tc_unit(const AttnArgs& a, int u) {
+PE_DEV TcUnit tc_unit_jrg(const AttnArgs& a, int j, int r, int g) {
   TcUnit x;
-  const int BG = a.B * a.G;
-  x.j = u / BG;
-  const int rem = u - x.j * BG;
-  x.r = rem / a.G;
-  x.g = rem - x.r * a.G;
-  x.L = min(max(a.seq_len[x.r], 0), a.max_blocks * a.bs);
+  x.j = j;
+  x.r = r;
+  x.g = g;
+  x.L = min(max(a.seq_len[r], 0), a.max_blocks * a.bs);
   x.t0 = x.j * a.split_len;
   x.t1 = min(x.L, x.t0 + a.split_len);
   x.n = x.t1 > x.t0 ? (x.t1 - x.t0 + kKC - 1) / kKC : 0;
   return x;
+}
+
+// Unit u in split-major order.
+PE_DEV TcUnit tc_unit(const AttnArgs& a, int u) {
+  const int BG = a.B * a.G;
+  const int j = u / BG;
+  const int rem = u - j * BG;
+  return tc_unit_jrg(a, j, rem / a.G, rem % a.G);
 }
 
 __global__ void __launch_bounds__(192, 2)
@@ -727,6 +735,11 @@ __global__ void __launch_bounds__(192, 2)
   __shared__ int4 meta_sh[kTcStages];  // per stage: unit (-1: end of the stream), chunk, chunks, group mask
   __shared__ int4 uq_sh[kTcUq];        // claimed units' fields, in this CTA's order (tc_unit_of)
   __shared__ float xl_sh[kTcRows];     // the low lanes' sums of weights, at a unit's end
+  // the claim order (producer warp): full splits per request as a prefix, the
+  // requests ordered by the chunks of their last split, and its bucket offsets
+  __shared__ int ord_full[kTcOrdMax + 1];
+  __shared__ int ord_part[kTcOrdMax];
+  __shared__ int ord_start[34];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
   uint8_t* ring = reinterpret_cast<uint8_t*>(
@@ -801,6 +814,71 @@ __global__ void __launch_bounds__(192, 2)
     uint32_t phase = 0;
     uint32_t armed = 0u, armed_parity = 0u;  // per stage: ever filled / parity of its last fill
     bool go = true;
+    // The claim order, longest units first (as dealt by a shared counter, the
+    // last units decide when the grid ends): every split of split_len keys,
+    // request-major, then each request's last, shorter split by its chunks,
+    // most first and in request order among equals, an empty context's empty
+    // split last.  Every CTA builds the same order from the request lengths.
+    // Larger batches take the splits split-major.
+    const bool lpt = a.B <= kTcOrdMax;
+    int n_full = 0, n_live = 0;  // units of full splits; units with keys or an empty context
+    // -> the bucket of request r's last split: its chunks (1..32), 0 for an
+    // empty context, -1 for none; nf = its full splits
+    auto req_class = [&](int r, int& nf) -> int {
+      const int L = min(max(a.seq_len[r], 0), Lmax);
+      nf = min(L / a.split_len, a.n_splits);
+      const int rem = L - nf * a.split_len;
+      if (rem > 0) return min((rem + kKC - 1) / kKC, 32);
+      return L == 0 ? 0 : -1;
+    };
+    if (lpt) {
+      for (int i = lane; i < 34; i += 32) ord_start[i] = 0;
+      if (lane == 0) ord_full[0] = 0;
+      __syncwarp();
+      int base = 0;
+      for (int r0 = 0; r0 < a.B; r0 += 32) {
+        const int r = r0 + lane;
+        int nf = 0, bk = -1;
+        if (r < a.B) bk = req_class(r, nf);
+        int incl = nf;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += t;
+        }
+        if (r < a.B) ord_full[r + 1] = base + incl;
+        if (bk >= 0) atomicAdd(&ord_start[bk], 1);
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        int acc = 0;
+        for (int bkt = 32; bkt >= 0; --bkt) {
+          const int c = ord_start[bkt];
+          ord_start[bkt] = acc;
+          acc += c;
+        }
+        ord_start[33] = acc;
+      }
+      __syncwarp();
+      n_full = base * a.G;
+      n_live = n_full + ord_start[33] * a.G;
+      // each request's place in its bucket, in request order
+      for (int r0 = 0; r0 < a.B; r0 += 32) {
+        const int r = r0 + lane;
+        int nf = 0, bk = -1;
+        if (r < a.B) bk = req_class(r, nf);
+        const unsigned same = __match_any_sync(0xffffffffu, bk);
+        const int s0 = bk >= 0 ? ord_start[bk] : 0;
+        __syncwarp();
+        const unsigned below = same & ((1u << lane) - 1u);
+        if (bk >= 0) {
+          ord_part[s0 + __popc(below)] = r;
+          if (below == 0) ord_start[bk] = s0 + __popc(same);
+        }
+        __syncwarp();
+      }
+    }
     // the next unit with keys (x = -1: none left); an empty context's first
     // split leaves its empty partial here, and splits past a request's keys none
     auto claim = [&]() -> int4 {
@@ -808,13 +886,37 @@ __global__ void __launch_bounds__(192, 2)
         int u = 0;
         if (lane == 0) u = static_cast<int>(atomicAdd(a.sched, 1u));
         u = __shfl_sync(0xffffffffu, u, 0);
-        if (u >= U) return make_int4(-1, 0, 0, 0);
-        const TcUnit x = tc_unit(a, u);
+        TcUnit x;
+        if (lpt) {
+          if (u >= n_live) return make_int4(-1, 0, 0, 0);
+          if (u < n_full) {
+            // full split j of request r: ord_full[r] <= u / G < ord_full[r + 1]
+            const int up = u / a.G;
+            int lo = 0, hi = a.B;
+            while (hi - lo > 1) {
+              const int mid = (lo + hi) >> 1;
+              if (ord_full[mid] <= up)
+                lo = mid;
+              else
+                hi = mid;
+            }
+            x = tc_unit_jrg(a, up - ord_full[lo], lo, u - up * a.G);
+          } else {
+            const int v = u - n_full;
+            const int pos = v / a.G;
+            const int r = ord_part[pos];
+            const int L = min(max(a.seq_len[r], 0), Lmax);
+            x = tc_unit_jrg(a, min(L / a.split_len, a.n_splits - 1), r, v - pos * a.G);
+          }
+        } else {
+          if (u >= U) return make_int4(-1, 0, 0, 0);
+          x = tc_unit(a, u);
+          if (x.j > 0 && x.t0 >= x.L) continue;
+        }
         if (lane == 0) {
           const int Lr = a.seq_len[x.r];
           if (Lr > Lmax || Lr < a.k_min) set_status(a.status, PE_ST_BLOCK_RANGE);
         }
-        if (x.j > 0 && x.t0 >= x.L) continue;
         if (x.n == 0) {
           for (int rr = 0; rr < rows; ++rr) {
             const size_t idx =
