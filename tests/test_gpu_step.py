@@ -171,3 +171,27 @@ def test_bad_context_block_at_a_batch_of_several_waves():
         check_logits_and_draft("bf16", logits[sl], draft[sl], res["req"][rr]["logits"],
                                where=f"request {rr}")
     assert ((draft[bad * K:(bad + 1) * K] >= 0) & (draft[bad * K:(bad + 1) * K] < wl.dims.vocab)).all()
+
+
+def test_batch_past_the_longest_first_order():
+    """1100 requests: more than the persistent attention orders longest first, so
+    its units go out split-major.  Metadata bit-exact; a sample of requests (the
+    first, the last and some between) matches the oracle."""
+    torch = cuda_or_skip()
+    wl, b, w, kc, vc, r = setup("small_prenorm", batch=1100, n_prev=2, ctx=("uniform", 0, 120),
+                                seed=13)
+    r.run()
+    torch.cuda.synchronize()
+    st, _ = r.status()
+    assert st == 0, hex(st)
+    K = wl.dims.K
+    sample = [0, 1, 517, 1024, 1098, 1099]
+    res = O.draft_step(wl.dims, w, b, kc, vc, requests=sample)
+    check_meta(r, res["meta"])
+    logits, draft = host(r.logits), host(r.draft)
+    z = f64(host(r.z), "bf16")
+    for rr in sample:
+        sl = slice(rr * K, (rr + 1) * K)
+        check_z("bf16", z[sl], res["req"][rr]["z"], where=f"request {rr}")
+        check_logits_and_draft("bf16", logits[sl], draft[sl], res["req"][rr]["logits"],
+                               where=f"request {rr}")
