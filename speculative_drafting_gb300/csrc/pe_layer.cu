@@ -160,11 +160,20 @@ int launch_rownorm(const RowNormArgs& a, int dtype, cudaStream_t st) {
 
 // ------------------------------------------------------------------ RoPE + KV write
 
-// CTAs (v, y): non-rejected row v, the y-th of kRopeCtasPerRow slices of its
-// heads (every element sums the QKV partial tiles, so a row is spread over
-// several CTAs).  The row is a sample row when it is one of the last K
+// CTAs (v, y): non-rejected row v, the y-th of gridDim.y slices of its heads
+// (every element sums the QKV partial tiles, so a few rows are spread over
+// several CTAs each).  The row is a sample row when it is one of the last K
 // non-rejected rows of its request (NTP row + MASK rows).
-constexpr int kRopeCtasPerRow = 8;
+constexpr int kRopeCtasPerRow = 8;  // at most
+// CTAs per row: as many as one wave of 8 CTAs per SM holds for all rows (a row
+// has only (H + 2G) hd / 2 rotations: a CTA's fixed chain of dependent loads,
+// not its elements, sets its time), at least 1, at most kRopeCtasPerRow
+int rope_ctas_per_row(int rows) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return std::max(1, std::min(kRopeCtasPerRow, 8 * std::max(sms, 1) / rows));
+}
 
 template <typename T>
 __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
@@ -279,10 +288,11 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
 int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st) {
   const int rows = a.padded_in ? a.B * a.K : a.T_out;
   if (rows <= 0) return PE_OK;
+  const dim3 grid(rows, rope_ctas_per_row(rows));
   const cudaError_t e =
       dtype == PE_DTYPE_BF16
-          ? launch_pdl(rope_kv_kernel<bf16>, dim3(rows, kRopeCtasPerRow), dim3(256), 0, st, a)
-          : launch_pdl(rope_kv_kernel<float>, dim3(rows, kRopeCtasPerRow), dim3(256), 0, st, a);
+          ? launch_pdl(rope_kv_kernel<bf16>, grid, dim3(256), 0, st, a)
+          : launch_pdl(rope_kv_kernel<float>, grid, dim3(256), 0, st, a);
   return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 
