@@ -38,6 +38,12 @@ PE_DEV void load_gain4<bf16>(const bf16* g, int i, float* out) {
   out[3] = __uint_as_float(u.y & 0xffff0000u);
 }
 
+// two 16-bit values as one word (the first in the low half)
+PE_DEV uint32_t pack2(bf16 a, bf16 b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
   __shared__ float red[32];
@@ -113,25 +119,50 @@ __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
   }
   T* out = static_cast<T*>(a.out);
   const size_t oo = static_cast<size_t>(row) * a.ld_out;
+  // four consecutive outputs at once: one 8-byte (bf16) or 16-byte store per
+  // output tensor where the row stride allows (ld_out % 4 == 0, checked on the
+  // host), else one store per element
   auto emit = [&](int i, const float4& f4, const float* g) {
     const float f[4] = {f4.x, f4.y, f4.z, f4.w};
+    float y[4], st[4];
+    T hi[4];
+    bf16 lo[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int c = 4 * i + k;
-      const float y = a.apply_norm ? f[k] * inv * g[k] : f[k];
-      float stored = y;
+      y[k] = a.apply_norm ? f[k] * inv * g[k] : f[k];
+      st[k] = y[k];
       if (out) {
-        const T hi = Elem<T>::from_f(y);
-        out[oo + c] = hi;
-        stored = Elem<T>::to_f(hi);
+        hi[k] = Elem<T>::from_f(y[k]);
+        st[k] = Elem<T>::to_f(hi[k]);
         if (a.out_lo) {
-          const bf16 lo = __float2bfloat16_rn(y - stored);
-          a.out_lo[oo + c] = lo;
-          stored += __bfloat162float(lo);
+          lo[k] = __float2bfloat16_rn(y[k] - st[k]);
+          st[k] += __bfloat162float(lo[k]);
         }
       }
-      if (a.out_f32) a.out_f32[oo + c] = stored;
-      if (a.norm_out) a.norm_out[oo + c] = y;
+    }
+    const size_t c0 = oo + 4 * static_cast<size_t>(i);
+    if (a.vec4) {
+      if (out) {
+        if constexpr (sizeof(T) == 2) {
+          *reinterpret_cast<uint2*>(out + c0) = make_uint2(pack2(hi[0], hi[1]), pack2(hi[2], hi[3]));
+        } else {
+          *reinterpret_cast<float4*>(out + c0) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+        }
+        if (a.out_lo)
+          *reinterpret_cast<uint2*>(a.out_lo + c0) = make_uint2(pack2(lo[0], lo[1]), pack2(lo[2], lo[3]));
+      }
+      if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + c0) = make_float4(st[0], st[1], st[2], st[3]);
+      if (a.norm_out) *reinterpret_cast<float4*>(a.norm_out + c0) = make_float4(y[0], y[1], y[2], y[3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (out) {
+          out[c0 + k] = hi[k];
+          if (a.out_lo) a.out_lo[c0 + k] = lo[k];
+        }
+        if (a.out_f32) a.out_f32[c0 + k] = st[k];
+        if (a.norm_out) a.norm_out[c0 + k] = y[k];
+      }
     }
   };
 #pragma unroll
@@ -148,8 +179,13 @@ __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
   }
 }
 
-int launch_rownorm(const RowNormArgs& a, int dtype, cudaStream_t st) {
-  if (a.rows_cap <= 0) return PE_OK;
+int launch_rownorm(const RowNormArgs& a_in, int dtype, cudaStream_t st) {
+  if (a_in.rows_cap <= 0) return PE_OK;
+  RowNormArgs a = a_in;
+  // vector stores: every output row starts 16-byte aligned
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  a.vec4 = (a.ld_out % 4 == 0) && (!a.out || al16(a.out)) && (!a.out_lo || al16(a.out_lo)) &&
+           (!a.out_f32 || al16(a.out_f32)) && (!a.norm_out || al16(a.norm_out));
   const int threads = a.d >= 2048 ? 256 : 128;
   const cudaError_t e =
       dtype == PE_DTYPE_BF16

@@ -121,6 +121,7 @@ struct RowNormArgs {
   // (in_group - out_group) + i % out_group, i.e. the last out_group of each
   // group of in_group input rows (the sample rows of a right-aligned layout)
   int in_group, out_group;
+  int vec4;  // set by launch_rownorm: four outputs per store
 };
 int launch_rownorm(const RowNormArgs& a, int dtype, cudaStream_t st);
 
