@@ -44,6 +44,20 @@ PE_DEV uint32_t pack2(bf16 a, bf16 b) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
+// four consecutive values (rounded to T) with one store: 8 bytes for bf16,
+// 16 for fp32
+template <typename T>
+PE_DEV void store4(T* p, const float* v);
+template <>
+PE_DEV void store4<bf16>(bf16* p, const float* v) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack2(__float2bfloat16_rn(v[0]), __float2bfloat16_rn(v[1])),
+                                            pack2(__float2bfloat16_rn(v[2]), __float2bfloat16_rn(v[3])));
+}
+template <>
+PE_DEV void store4<float>(float* p, const float* v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) rownorm_kernel(RowNormArgs a) {
   __shared__ float red[32];
@@ -288,6 +302,55 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
   if (!slot_ok && slot != PE_PADDING_SLOT_ID && threadIdx.x == 0)
     set_status(a.status, PE_ST_BLOCK_RANGE);
   const int64_t blk = slot_ok ? slot / a.bs : 0, off = slot_ok ? slot % a.bs : 0;
+  if (a.vec4) {
+    // four consecutive elements at once (16-byte partial loads, 8- or 16-byte
+    // stores; the host checked the strides and alignments)
+    auto qkv_at4 = [&](int x, float* f) {
+      float4 acc = *reinterpret_cast<const float4*>(row0 + x);
+      for (int k = 1; k < a.n_parts; ++k) {
+        const float4 p = *reinterpret_cast<const float4*>(row0 + k * a.part_stride + x);
+        acc.x += p.x;
+        acc.y += p.y;
+        acc.z += p.z;
+        acc.w += p.w;
+      }
+      f[0] = acc.x;
+      f[1] = acc.y;
+      f[2] = acc.z;
+      f[3] = acc.w;
+    };
+    const int q4 = half / 4;
+    for (int e = tid; e < (a.H + a.G) * q4; e += nthr) {
+      const int hh = e / q4, i0 = (e - hh * q4) * 4;
+      float x1[4], x2[4], y1[4], y2[4];
+      qkv_at4(hh * a.hd + i0, x1);
+      qkv_at4(hh * a.hd + i0 + half, x2);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        y1[k] = x1[k] * cs[i0 + k] - x2[k] * sn[i0 + k];
+        y2[k] = x2[k] * cs[i0 + k] + x1[k] * sn[i0 + k];
+      }
+      T* dst = nullptr;
+      if (hh < a.H) {
+        if (s_idx >= 0) dst = static_cast<T*>(a.q_s) + (static_cast<size_t>(s_idx) * a.H + hh) * a.hd;
+      } else if (slot_ok) {
+        dst = static_cast<T*>(a.k_cache) + ((blk * a.G + (hh - a.H)) * a.bs + off) * a.hd;
+      }
+      if (dst) {
+        store4<T>(dst + i0, y1);
+        store4<T>(dst + i0 + half, y2);
+      }
+    }
+    if (slot_ok) {
+      const int v4 = a.hd / 4;
+      for (int e = tid; e < a.G * v4; e += nthr) {
+        const int g = e / v4, i0 = (e - g * v4) * 4;
+        float f[4];
+        qkv_at4((a.H + a.G) * a.hd + g * a.hd + i0, f);
+        store4<T>(static_cast<T*>(a.v_cache) + ((blk * a.G + g) * a.bs + off) * a.hd + i0, f);
+      }
+    }
+  } else {
   // rotated q (sample rows) and k (all rows)
   for (int e = tid; e < (a.H + a.G) * half; e += nthr) {
     const int hh = e / half, i = e - hh * half;
@@ -313,6 +376,7 @@ __global__ void __launch_bounds__(256) rope_kv_kernel(const RopeArgs a) {
       vc[i] = Elem<T>::from_f(qkv_at((a.H + a.G) * a.hd + e));
     }
   }
+  }
   if (s_idx >= 0 && a.x_s) {
     // the fc output of the sample rows is the attention residual (fp32)
     const float4* src = reinterpret_cast<const float4*>(a.x + static_cast<size_t>(v) * a.d);
@@ -325,10 +389,18 @@ int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st) {
   const int rows = a.padded_in ? a.B * a.K : a.T_out;
   if (rows <= 0) return PE_OK;
   const dim3 grid(rows, rope_ctas_per_row(rows));
+  RopeArgs av = a;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  const size_t esz = dtype == PE_DTYPE_BF16 ? 2 : 4;
+  // 16-byte partial loads need every row and part to start 16-byte aligned;
+  // 4-element stores need hd % 8 == 0 (so half % 4 == 0) and aligned rows
+  av.vec4 = a.hd % 8 == 0 && (static_cast<size_t>(a.H + 2 * a.G) * a.hd) % 4 == 0 &&
+            a.part_stride % 4 == 0 && al16(a.qkv) && al16(a.q_s) && al16(a.k_cache) &&
+            al16(a.v_cache) && (static_cast<size_t>(a.hd) * esz) % 8 == 0;
   const cudaError_t e =
       dtype == PE_DTYPE_BF16
-          ? launch_pdl(rope_kv_kernel<bf16>, grid, dim3(256), 0, st, a)
-          : launch_pdl(rope_kv_kernel<float>, grid, dim3(256), 0, st, a);
+          ? launch_pdl(rope_kv_kernel<bf16>, grid, dim3(256), 0, st, av)
+          : launch_pdl(rope_kv_kernel<float>, grid, dim3(256), 0, st, av);
   return e == cudaSuccess ? PE_OK : PE_ERR_CUDA;
 }
 

@@ -152,6 +152,7 @@ struct RopeArgs {
   // sets PE_ST_ROWS_RANGE (several layers need every row)
   int must_fit;
   uint32_t* status;
+  int vec4;  // set by launch_rope_kv: four elements per load and store
 };
 int launch_rope_kv(const RopeArgs& a, int dtype, cudaStream_t st);
 
