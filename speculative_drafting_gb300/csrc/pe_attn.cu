@@ -1451,8 +1451,22 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
     }
   }
   T* out = static_cast<T*>(a.out) + sh * HD + lane * V;
+  if constexpr (sizeof(T) == 2) {
+    // the lane's V = 2 or 4 bf16 outputs with one 4- or 8-byte store
+    uint32_t w[V / 2];
 #pragma unroll
-  for (int i = 0; i < V; ++i) out[i] = Elem<T>::from_f(acc[i] * inv);
+    for (int i = 0; i < V / 2; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    if constexpr (V == 2)
+      *reinterpret_cast<uint32_t*>(out) = w[0];
+    else
+      *reinterpret_cast<uint2*>(out) = make_uint2(w[0], w[1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) out[i] = Elem<T>::from_f(acc[i] * inv);
+  }
 }
 
 // fp32: one CTA (4 warps) per (sample row, query head)
