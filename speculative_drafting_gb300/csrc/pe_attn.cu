@@ -533,16 +533,16 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
 // ---------------------------------------------------------------- tcgen05 attention (hd = 64)
 // For hd = 64 and query tiles of at most 64 rows (K x H/G), both products run on
 // the tensor cores (tcgen05) with fp32 accumulators in tensor memory:
-//   S = Q K^T (M = 128, N = 64 keys, K = 64 dims): rows 0..63 of the A operand
-//             are the query rows, rows 64..127 the same rows again;
+//   S = Q K^T (M = 128, N = 64 keys, K = 64 dims): Q is read from tensor memory,
+//             its rows 0..63 the query rows, rows 64..127 the same rows again;
 //   O += P V  (M = 128, N = 64 dims, K = 64 keys): rows 0..63 of P hold the high
 //             bf16 part of the softmax weights, rows 64..127 the low part (the
 //             hi + lo pair, about 16 significant bits), so one MMA covers both
 //             halves and a query row's output is O[r] + O[r + 64].
 // The kernel is persistent: two CTAs per SM take work units (key split j, KV head
-// g, request r), split-major, from a counter in global memory, and stream one
-// unit's 64-key chunks after the other through the same pipeline, so the ring
-// stays full across unit boundaries.  Each unit leaves the same partial as the
+// g, request r) from a counter in global memory, longest first (the claim order
+// below), and stream one unit's 64-key chunks after the other through the same
+// pipeline, so the ring stays full across unit boundaries.  Each unit leaves the same partial as the
 // mma.sync kernel's CTAs (unnormalised o, then m and l in the exp2 domain) for
 // the combine kernel.  Warp 0 claims units and streams K and V with TMA (every
 // ring stage carries its unit, its chunk index and its group mask); one thread
