@@ -181,11 +181,6 @@ struct Layout {
 constexpr size_t kBarrierWordsOffset = 64;
 // the first kernel's launch count is barrier word 12 (pe_decode.cu)
 static_assert(kBarrierWordsOffset + 4 * 12 == PE_TEST_DECODE_EPOCH_BYTE, "decode epoch word");
-// The attention's work-unit counter: two words in the header, after the decode
-// layer's barrier and diagnostic words (20 words from kBarrierWordsOffset).
-constexpr size_t kAttnSchedWord = 48;
-static_assert(kBarrierWordsOffset / 4 + 20 <= kAttnSchedWord && kAttnSchedWord + 2 <= 256 / 4,
-              "attention counter inside the header, clear of the decode layer's words");
 
 // Workspace layout of a step with B requests, T_in verify rows and block tables
 // of max_blocks entries.  Each region is sized by a bound that only grows with
@@ -458,7 +453,6 @@ int attention_step(const StepCtx& c, int Kd, int B, const pe_meta* meta, const i
   aa.sink = static_cast<const float*>(h->w.attn_sink);
   aa.k_min = Kd;
   aa.status = c.status;
-  aa.sched = c.status + kAttnSchedWord;
   return launch_attention(aa, c.dt, c.st);
 }
 
@@ -594,7 +588,6 @@ int one_layer_step(const StepCtx& c, int Kd, int B, int T_in, const pe_meta* met
   aa.sink = static_cast<const float*>(h->w.attn_sink);
   aa.k_min = Kd;
   aa.status = c.status;
-  aa.sched = c.status + kAttnSchedWord;
   if ((rc = launch_attention(aa, c.dt, c.st)) != PE_OK) return rc;
   // O projection (partial sums)
   e = partial_epi(c, NS, d.d);
@@ -722,7 +715,6 @@ int layers_step(const StepCtx& c, int B, int T_in, const pe_meta* meta, const vo
     aa.sink = sink;
     aa.k_min = d.K;
     aa.status = c.status;
-    aa.sched = c.status + kAttnSchedWord;
     if ((rc = launch_attention(aa, c.dt, c.st)) != PE_OK) return rc;
     e = partial_epi(c, NR, d.d);
     if ((rc = run_gemm(h, G_O, c.attn, nullptr, NR, nullptr, e, c.ws, L, c.st, true, &np, l)) !=

@@ -22,7 +22,6 @@
 // its exponential to the denominator, with a zero value row.
 #include <algorithm>
 #include <cmath>
-#include <type_traits>
 
 #include "pe_common.cuh"
 #include "pe_prep.h"
@@ -530,869 +529,6 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
   cluster_sync_all();
 }
 
-// ---------------------------------------------------------------- tcgen05 attention (hd = 64)
-// For hd = 64 and query tiles of at most 64 rows (K x H/G), both products run on
-// the tensor cores (tcgen05) with fp32 accumulators in tensor memory:
-//   S = Q K^T (M = 128, N = 64 keys, K = 64 dims): Q is read from tensor memory,
-//             its rows 0..63 the query rows, rows 64..127 the same rows again;
-//   O += P V  (M = 128, N = 64 dims, K = 64 keys): rows 0..63 of P hold the high
-//             bf16 part of the softmax weights, rows 64..127 the low part (the
-//             hi + lo pair, about 16 significant bits), so one MMA covers both
-//             halves and a query row's output is O[r] + O[r + 64].
-// The kernel is persistent: two CTAs per SM take work units (key split j, KV head
-// g, request r) from a counter in global memory, longest first (the claim order
-// below), and stream one unit's 64-key chunks after the other through the same
-// pipeline, so the ring stays full across unit boundaries.  Each unit leaves the same partial as the
-// mma.sync kernel's CTAs (unnormalised o, then m and l in the exp2 domain) for
-// the combine kernel.  Warp 0 claims units and streams K and V with TMA (every
-// ring stage carries its unit, its chunk index and its group mask); one thread
-// of warp 1 issues the MMAs; each thread of warps 2..5 owns one TMEM lane R.
-// Lanes r and r + 64 hold the same score row: both take its maximum over the
-// chunk's 64 keys, each takes the exponentials of half the keys (lane r the first
-// 32, lane r + 64 the last 32) and writes their hi and lo weights into the P
-// tile.  O accumulates in tensor memory over a unit's chunks; a row's reference
-// maximum moves only when a score exceeds it by more than kTcRescale (weights up
-// to 2^kTcRescale), and then each of its two lanes rescales its O row in place
-// between two P V products.  Q sits in tensor memory, double-buffered by unit:
-// the next unit's rows are copied into a staging tile (cp.async) when a unit
-// starts and moved into tensor memory after its first chunk.
-constexpr int kTcStages = 4;
-constexpr int kTcTile = kKC * 64 * 2;   // one K (or V) chunk: 64 keys x 64 dims bf16
-constexpr int kTcStage = 2 * kTcTile;   // K then V
-constexpr int kTcRowBytes = 128 * 128;  // 128 rows x 128 bytes: the P tile, the Q staging tile
-constexpr int kTcSmem = kTcStages * kTcStage + 2 * kTcRowBytes + 1024;
-constexpr uint32_t kTcTmemCols = 256;   // S0, S1, O: 64 fp32 columns each; Q0, Q1: 32 each
-constexpr uint32_t kTcOCol = 128;
-constexpr uint32_t kTcQCol = 192;       // Q (two bf16 per column), buffer b at + 32 b
-constexpr int kTcRows = 64;             // query rows per unit, at most
-constexpr int kTcUq = 4;                // ring of claimed unit ids
-constexpr float kTcRescale = 8.f;
-constexpr int kTcOrdMax = 1024;         // requests whose units are claimed longest first
-// dynamic + static shared memory (the claim order, 8 bytes per request, and
-// the rest) + the 1 KB the system reserves, twice per SM
-static_assert(2 * (kTcSmem + 8 * kTcOrdMax + 2048) <= 228 * 1024, "two tcgen05 attention CTAs per SM");
-static_assert(2 * kTcTmemCols <= 512, "two tcgen05 attention CTAs per SM (tensor memory)");
-static_assert(kTcRows * 64 * 4 <= kTcRowBytes, "a unit's o rows fit the P tile");
-static_assert(kTcQCol + 64 <= kTcTmemCols, "both Q buffers fit the tensor memory");
-
-// Shared-memory descriptor of an MN-major bf16 tile with the 128-byte swizzle:
-// 128-byte rows of 64 consecutive N elements, one row per K index, 8-row atoms
-// of 1024 bytes.  A 64-wide N is one atom wide, so the only stride the MMA
-// walks is the 1024 bytes between the atoms of 8 K rows; both offset fields
-// hold it.
-PE_DEV uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1024 >> 4) << 16;
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
-}
-
-// max(a, b, c) in one instruction
-PE_DEV float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, A read from tensor memory (one row per
-// lane, two bf16 per 32-bit column, K-major), issued by one thread.
-PE_DEV void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Has the phase of parity `parity` completed?  (No waiting.)
-PE_DEV bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// N consecutive 32-bit columns of this thread's TMEM lane (32x32b shape, thread
-// t of the warp reads or writes lane taddr.lane + t), waited for in the same
-// statement so that no use of the registers can move above the wait.
-PE_DEV void tmem_ld64(uint32_t taddr, float* v) {
-  uint32_t r[64];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
-PE_DEV void tmem_st32(uint32_t taddr, const float* v) {
-  uint32_t r[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
-      "tcgen05.wait::st.sync.aligned;\n"
-      :
-      : "r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-PE_DEV void tmem_st64(uint32_t taddr, const float* v) {
-  uint32_t r[64];
-#pragma unroll
-  for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(v[i]);
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};\n\t"
-      "tcgen05.wait::st.sync.aligned;\n"
-      :
-      : "r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]),
-        "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]),
-        "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]),
-        "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]),
-        "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
-      : "memory");
-}
-
-
-// A work unit of the tcgen05 attention: key split j of request r, KV head g.
-// Units are numbered split-major: u = (j B + r) G + g.
-struct TcUnit {
-  int r, g, j;
-  int L;       // the request's keys (clamped to its block table)
-  int t0, t1;  // the split's keys [t0, t1)
-  int n;       // 64-key chunks
-};
-
-// A unit's fields as the producer hands them to the softmax warps:
-// (u, r, g | j << 16, L); u = -1: no unit left.
-PE_DEV TcUnit tc_unit_of(const AttnArgs& a, int4 e) {
-  TcUnit x;
-  x.r = e.y;
-  x.g = e.z & 0xffff;
-  x.j = e.z >> 16;
-  x.L = e.w;
-  x.t0 = x.j * a.split_len;
-  x.t1 = min(x.L, x.t0 + a.split_len);
-  x.n = x.t1 > x.t0 ? (x.t1 - x.t0 + kKC - 1) / kKC : 0;
-  return x;
-}
-
-PE_DEV TcUnit tc_unit_jrg(const AttnArgs& a, int j, int r, int g) {
-  TcUnit x;
-  x.j = j;
-  x.r = r;
-  x.g = g;
-  x.L = min(max(a.seq_len[r], 0), a.max_blocks * a.bs);
-  x.t0 = x.j * a.split_len;
-  x.t1 = min(x.L, x.t0 + a.split_len);
-  x.n = x.t1 > x.t0 ? (x.t1 - x.t0 + kKC - 1) / kKC : 0;
-  return x;
-}
-
-// Unit u in split-major order.
-PE_DEV TcUnit tc_unit(const AttnArgs& a, int u) {
-  const int BG = a.B * a.G;
-  const int j = u / BG;
-  const int rem = u - j * BG;
-  return tc_unit_jrg(a, j, rem / a.G, rem % a.G);
-}
-
-__global__ void __launch_bounds__(192, 2)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                   const AttnArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kTcStages], empty_bar[kTcStages];
-  __shared__ __align__(8) uint64_t s_full[2], q_full[2], uq_full[kTcUq], uq_empty[kTcUq];
-  __shared__ __align__(8) uint64_t p_full, o_done, x_full, x_empty, done_bar;
-  __shared__ int4 meta_sh[kTcStages];  // per stage: unit (-1: end of the stream), chunk, chunks, group mask
-  __shared__ int4 uq_sh[kTcUq];        // claimed units' fields, in this CTA's order (tc_unit_of)
-  __shared__ float xl_sh[kTcRows];     // the low lanes' sums of weights, at a unit's end
-  // the claim order (producer warp): full splits per request as a prefix, the
-  // requests ordered by the chunks of their last split, and its bucket offsets
-  __shared__ int ord_full[kTcOrdMax + 1];
-  __shared__ int ord_part[kTcOrdMax];
-  __shared__ int ord_start[34];
-  __shared__ uint32_t tmem_sh;
-  __shared__ int abort_sh;
-  uint8_t* ring = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  // P tile, [128 rows][64 keys] bf16, K-major with the 128-byte swizzle; at a
-  // unit's end it carries the low lanes' O rows to the high lanes
-  uint8_t* pbuf = ring + kTcStages * kTcStage;
-  uint8_t* qst = pbuf + kTcRowBytes;  // the next unit's Q rows, [128][128 bytes], swizzled
-
-  const int HG = a.H / a.G;
-  const int rows = a.K * HG;
-  const int U = a.n_splits * a.G * a.B;
-  const int Lmax = a.max_blocks * a.bs;
-  const size_t n_samp = static_cast<size_t>(a.B) * a.K;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // stale shared memory must be finite: a masked key still multiplies its V row by 0
-  for (int i = threadIdx.x; i < kTcStages * kTcStage / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(ring)[i] = make_uint4(0, 0, 0, 0);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&q_full[b], 128);
-    }
-    for (int i = 0; i < kTcUq; ++i) {
-      mbar_init(&uq_full[i], 1);
-      mbar_init(&uq_empty[i], 128);
-    }
-    mbar_init(&p_full, 128);
-    mbar_init(&o_done, 1);
-    mbar_init(&x_full, kTcRows);
-    mbar_init(&x_empty, kTcRows);
-    mbar_init(&done_bar, 1);
-    abort_sh = 0;
-    fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&kmap);
-    prefetch_tmap(&vmap);
-  }
-  // tensor memory before the next kernel may start: its CTAs then find this
-  // grid's allocations in place and wait for them, never the other way round
-  if (warp == 1) {
-    tmem_alloc(&tmem_sh, kTcTmemCols);
-    tmem_relinquish();
-  }
-  pdl_trigger();
-  pdl_wait();
-  fence_proxy_async();  // the zeroed ring is visible to the TMA writes that follow
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_sh;
-  volatile int* abort_flag = &abort_sh;
-  auto fail = [&]() {
-    abort_sh = 1;
-    set_status(a.status, PE_ST_TIMEOUT);
-  };
-
-  if (warp == 0) {
-    // ---------------- producer warp.  It claims each unit one ahead of the one
-    // it streams (while the ring is full), reads the block ids of the next
-    // 8-chunk window one window ahead (across unit boundaries too), and issues
-    // the TMA loads of each chunk into the ring.
-    constexpr int GROUP_BYTES = 16 * 128;  // one box: 16 keys x 64 dims
-    constexpr int kPast = -0x7fffffff - 1;  // a group past the split's keys
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t armed = 0u, armed_parity = 0u;  // per stage: ever filled / parity of its last fill
-    bool go = true;
-    // The claim order, longest units first (as dealt by a shared counter, the
-    // last units decide when the grid ends): every split of split_len keys,
-    // request-major, then each request's last, shorter split by its chunks,
-    // most first and in request order among equals, an empty context's empty
-    // split last.  Every CTA builds the same order from the request lengths.
-    // Larger batches take the splits split-major.
-    const bool lpt = a.B <= kTcOrdMax;
-    int n_full = 0, n_live = 0;  // units of full splits; units with keys or an empty context
-    // -> the bucket of request r's last split: its chunks (1..32), 0 for an
-    // empty context, -1 for none; nf = its full splits
-    auto req_class = [&](int r, int& nf) -> int {
-      const int L = min(max(a.seq_len[r], 0), Lmax);
-      nf = min(L / a.split_len, a.n_splits);
-      const int rem = L - nf * a.split_len;
-      if (rem > 0) return min((rem + kKC - 1) / kKC, 32);
-      return L == 0 ? 0 : -1;
-    };
-    if (lpt) {
-      for (int i = lane; i < 34; i += 32) ord_start[i] = 0;
-      if (lane == 0) ord_full[0] = 0;
-      __syncwarp();
-      int base = 0;
-      for (int r0 = 0; r0 < a.B; r0 += 32) {
-        const int r = r0 + lane;
-        int nf = 0, bk = -1;
-        if (r < a.B) bk = req_class(r, nf);
-        int incl = nf;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int t = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += t;
-        }
-        if (r < a.B) ord_full[r + 1] = base + incl;
-        if (bk >= 0) atomicAdd(&ord_start[bk], 1);
-        base += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      __syncwarp();
-      if (lane == 0) {
-        int acc = 0;
-        for (int bkt = 32; bkt >= 0; --bkt) {
-          const int c = ord_start[bkt];
-          ord_start[bkt] = acc;
-          acc += c;
-        }
-        ord_start[33] = acc;
-      }
-      __syncwarp();
-      n_full = base * a.G;
-      n_live = n_full + ord_start[33] * a.G;
-      // each request's place in its bucket, in request order
-      for (int r0 = 0; r0 < a.B; r0 += 32) {
-        const int r = r0 + lane;
-        int nf = 0, bk = -1;
-        if (r < a.B) bk = req_class(r, nf);
-        const unsigned same = __match_any_sync(0xffffffffu, bk);
-        const int s0 = bk >= 0 ? ord_start[bk] : 0;
-        __syncwarp();
-        const unsigned below = same & ((1u << lane) - 1u);
-        if (bk >= 0) {
-          ord_part[s0 + __popc(below)] = r;
-          if (below == 0) ord_start[bk] = s0 + __popc(same);
-        }
-        __syncwarp();
-      }
-    }
-    // the next unit with keys (x = -1: none left); an empty context's first
-    // split leaves its empty partial here, and splits past a request's keys none
-    auto claim = [&]() -> int4 {
-      for (;;) {
-        int u = 0;
-        if (lane == 0) u = static_cast<int>(atomicAdd(a.sched, 1u));
-        u = __shfl_sync(0xffffffffu, u, 0);
-        TcUnit x;
-        if (lpt) {
-          if (u >= n_live) return make_int4(-1, 0, 0, 0);
-          if (u < n_full) {
-            // full split j of request r: ord_full[r] <= u / G < ord_full[r + 1]
-            const int up = u / a.G;
-            int lo = 0, hi = a.B;
-            while (hi - lo > 1) {
-              const int mid = (lo + hi) >> 1;
-              if (ord_full[mid] <= up)
-                lo = mid;
-              else
-                hi = mid;
-            }
-            x = tc_unit_jrg(a, up - ord_full[lo], lo, u - up * a.G);
-          } else {
-            const int v = u - n_full;
-            const int pos = v / a.G;
-            const int r = ord_part[pos];
-            const int L = min(max(a.seq_len[r], 0), Lmax);
-            x = tc_unit_jrg(a, min(L / a.split_len, a.n_splits - 1), r, v - pos * a.G);
-          }
-        } else {
-          if (u >= U) return make_int4(-1, 0, 0, 0);
-          x = tc_unit(a, u);
-          if (x.j > 0 && x.t0 >= x.L) continue;
-        }
-        if (lane == 0) {
-          const int Lr = a.seq_len[x.r];
-          if (Lr > Lmax || Lr < a.k_min) set_status(a.status, PE_ST_BLOCK_RANGE);
-        }
-        if (x.n == 0) {
-          for (int rr = 0; rr < rows; ++rr) {
-            const size_t idx =
-                (static_cast<size_t>(x.j) * n_samp + static_cast<size_t>(x.r) * a.K + rr / HG) * a.H +
-                x.g * HG + rr % HG;
-            a.part_o[idx * 64 + lane] = 0.f;
-            a.part_o[idx * 64 + 32 + lane] = 0.f;
-            if (lane == 0) {
-              a.part_ml[idx * 2] = -INFINITY;
-              a.part_ml[idx * 2 + 1] = 0.f;
-            }
-          }
-          continue;
-        }
-        return make_int4(u, x.r, x.g | (x.j << 16), x.L);
-      }
-    };
-    // unit number k of this CTA's sequence, for the softmax warps
-    auto publish = [&](int k, int4 e) -> bool {
-      const int sl = k % kTcUq;
-      int ok = 1;
-      if (lane == 0) {
-        if (k >= kTcUq && !mbar_wait(&uq_empty[sl], (k / kTcUq - 1) & 1, abort_flag)) {
-          ok = 0;
-        } else {
-          uq_sh[sl] = e;
-          mbar_arrive(&uq_full[sl]);
-        }
-      }
-      return __shfl_sync(0xffffffffu, ok, 0) != 0;
-    };
-    // block id of this lane's 16-key group of window cbw of unit y (the load's
-    // value is used one window later)
-    auto load_blk = [&](const TcUnit& y, int cbw) -> int {
-      const int t = y.t0 + (cbw * 4 + lane) * 16;
-      return t < y.t1 ? a.block_table[static_cast<size_t>(y.r) * a.max_blocks + t / a.bs] : kPast;
-    };
-    // -> cache row of the group's first key, -1 = none
-    auto to_row = [&](const TcUnit& y, int cbw, int blk) -> int {
-      if (blk == kPast) return -1;
-      if (blk < 0 || blk >= a.num_blocks) {
-        set_status(a.status, PE_ST_BLOCK_RANGE);
-        return -1;
-      }
-      const int t = y.t0 + (cbw * 4 + lane) * 16;
-      return (blk * a.G + y.g) * a.bs + t % a.bs;
-    };
-    int4 ec = claim();  // the unit being streamed
-    go = publish(0, ec);
-    int4 en = make_int4(-1, 0, 0, 0);  // the one after it
-    if (go && ec.x >= 0) {
-      en = claim();
-      go = publish(1, en);
-    }
-    int k = 0;
-    TcUnit x = tc_unit_of(a, ec);
-    int cb = 0;
-    int blk = (go && ec.x >= 0) ? load_blk(x, 0) : kPast;
-    while (go && ec.x >= 0) {
-      // the next window: this unit's next 8 chunks, or the next unit's first
-      const bool same = cb + 8 < x.n;
-      const TcUnit xn = same ? x : tc_unit_of(a, en);
-      const int cbn = same ? cb + 8 : 0;
-      const int blk_next = (same || en.x >= 0) ? load_blk(xn, cbn) : kPast;
-      const int rowv = to_row(x, cb, blk);
-      const int c_end = min(x.n, cb + 8);
-      for (int c = cb; c < c_end; ++c) {
-        int row[4];
-        uint32_t mask = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          row[q] = __shfl_sync(0xffffffffu, rowv, (c - cb) * 4 + q);
-          if (row[q] >= 0) mask |= 1u << q;
-        }
-        int ok = 1;
-        if (lane == 0) {
-          if (*abort_flag || !mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
-            ok = 0;
-          } else {
-            meta_sh[stage] = make_int4(ec.x, c, x.n, static_cast<int>(mask));
-            mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(__popc(mask)) * 2u * GROUP_BYTES);
-            uint8_t* kd = ring + stage * kTcStage;
-            for (int q = 0; q < 4; ++q) {
-              if (!(mask & (1u << q))) continue;
-              tma_load_2d(kd + q * GROUP_BYTES, &kmap, &full_bar[stage], 0, row[q], policy_evict_first());
-              tma_load_2d(kd + kTcTile + q * GROUP_BYTES, &vmap, &full_bar[stage], 0, row[q],
-                          policy_evict_first());
-            }
-            armed |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          go = false;
-          break;
-        }
-        if (++stage == kTcStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!go) break;
-      if (same) {
-        cb += 8;
-      } else {
-        // on to the next unit; the one after it is claimed now, with the ring full
-        ++k;
-        ec = en;
-        x = xn;
-        cb = 0;
-        if (ec.x >= 0) {
-          en = claim();
-          if (!publish(k + 1, en)) {
-            go = false;
-            break;
-          }
-        }
-      }
-      blk = blk_next;
-    }
-    // the end of the stream: a stage without keys
-    if (lane == 0) {
-      if (go && mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
-        meta_sh[stage] = make_int4(-1, 0, 0, 0);
-        mbar_arrive(&full_bar[stage]);
-      } else {
-        fail();
-        // let copies already in flight land before the CTA's shared memory goes away
-        for (int s = 0; s < kTcStages; ++s)
-          if (armed & (1u << s)) {
-            int dummy = 0;
-            mbar_wait(&full_bar[s], (armed_parity >> s) & 1u, &dummy);
-          }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---------------- MMA issuer.  Chunk c's S goes out as soon as its keys (and,
-    // for a unit's first chunk, its Q) are there, if the softmax is done with the
-    // S buffer (it has written P of chunk c - 2); P V of chunk c once P is
-    // written.  The thread blocks in the barrier waits (no spinning beside the
-    // softmax warps).
-    if (lane == 0) {
-      const uint32_t idesc_s = idesc_bf16_f32(128, 64);
-      const uint32_t idesc_o = idesc_bf16_f32(128, 64) | (1u << 16);  // B = V, MN-major
-      const uint64_t pdesc = sw128_kmajor_desc(smem_u32(pbuf));
-      int ns = 0;    // chunks whose S has been issued
-      int kq = -1;   // unit of the Q those S products use
-      bool end = false;
-      // S of chunk ns if its inputs are there (block: wait for them); false
-      // only for a wait that gave up
-      auto try_s = [&](bool block) -> bool {
-        const int stage = ns % kTcStages;
-        const uint32_t par = (ns / kTcStages) & 1;
-        if (block) {
-          if (!mbar_wait(&full_bar[stage], par, abort_flag)) return false;
-        } else if (!mbar_test(&full_bar[stage], par)) {
-          return true;
-        }
-        const int4 md = meta_sh[stage];
-        if (md.x < 0) {
-          end = true;
-          return true;
-        }
-        if (md.y == 0) {
-          const int q = kq + 1;
-          if (block) {
-            if (!mbar_wait(&q_full[q & 1], (q >> 1) & 1, abort_flag)) return false;
-          } else if (!mbar_test(&q_full[q & 1], (q >> 1) & 1)) {
-            return true;
-          }
-          kq = q;
-        }
-        tc_fence_after();
-        const uint64_t kdesc = sw128_kmajor_desc(smem_u32(ring + stage * kTcStage));
-        // 16 dims per MMA: 8 columns of Q, 32 bytes along a K row
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16_ta(tmem + (ns & 1) * 64, tmem + kTcQCol + 32 * (kq & 1) + 8 * kk, kdesc + 2 * kk,
-                       idesc_s, kk > 0 ? 1u : 0u);
-        umma_commit(&s_full[ns & 1]);
-        ++ns;
-        return true;
-      };
-      bool ok = try_s(true);
-      for (int c = 0; ok && c < ns; ++c) {
-        if (!end && ns == c + 1 && !(ok = try_s(false))) break;
-        if (!mbar_wait(&p_full, c & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int stage = c % kTcStages;
-        const int4 md = meta_sh[stage];
-        const uint64_t vdesc = sw128_mnmajor_desc(smem_u32(ring + stage * kTcStage + kTcTile));
-        // 16 keys per MMA: 32 bytes along a P row, 16 V rows of 128 bytes; a
-        // unit's first chunk starts O afresh
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + kTcOCol, pdesc + 2 * kk, vdesc + 128 * kk, idesc_o, (md.y > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&o_done);
-        umma_commit(&empty_bar[stage]);
-        if (!end && ns == c + 1) ok = try_s(true);
-      }
-      if (!ok) fail();
-      // every MMA done before the tensor memory is freed
-      umma_commit(&done_bar);
-      int dummy = 0;
-      mbar_wait(&done_bar, 0, &dummy);
-    }
-    __syncwarp();
-  } else {
-    // ---------------- softmax warps: thread = TMEM lane R
-    const int qd = warp & 3;
-    const int R = qd * 32 + lane;
-    const int qr = R & (kTcRows - 1);  // query row
-    const int half = R >> 6;           // 0: high parts of P and O, keys 0..31; 1: low parts, keys 32..63
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(qd * 32) << 16);
-    const int swz = qr & 7;
-    const uint32_t off_hi = static_cast<uint32_t>((qr >> 3) * 1024 + swz * 128);  // P row qr
-    const uint32_t off_lo = off_hi + 8 * 1024;                                   // P row qr + 64
-    uint8_t* qst_row = qst + R * 128;
-    const float sc = kLog2e / sqrtf(64.f);
-    // this lane's row of Q for unit x (rows past the query tile are zero)
-    auto q_src = [&](const TcUnit& x) -> const uint4* {
-      return reinterpret_cast<const uint4*>(
-          static_cast<const bf16*>(a.q) +
-          ((static_cast<size_t>(x.r) * a.K + qr / HG) * a.H + x.g * HG + qr % HG) * 64);
-    };
-    auto q_to_tmem = [&](const uint4* v, int buf) {
-      float qw[32];
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        qw[4 * ch] = __uint_as_float(v[ch].x);
-        qw[4 * ch + 1] = __uint_as_float(v[ch].y);
-        qw[4 * ch + 2] = __uint_as_float(v[ch].z);
-        qw[4 * ch + 3] = __uint_as_float(v[ch].w);
-      }
-      tmem_st32(t_lane + kTcQCol + 32 * buf, qw);
-      tc_fence_before();
-      mbar_arrive(&q_full[buf]);
-    };
-    bool ok = true;
-    int k = 0;  // this CTA's unit number
-    {
-      // unit 0's Q (its entry is released when the unit starts)
-      const bool got = mbar_wait(&uq_full[0], 0, abort_flag);
-      if (!__all_sync(0xffffffffu, got)) {
-        fail();
-        ok = false;
-      } else {
-        const int4 e0 = uq_sh[0];
-        if (e0.x >= 0) {
-          uint4 v[8];
-          const TcUnit x0 = tc_unit_of(a, e0);
-          const uint4* src = q_src(x0);
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) v[ch] = qr < rows ? src[ch] : make_uint4(0, 0, 0, 0);
-          q_to_tmem(v, 0);
-        }
-      }
-    }
-    TcUnit x{};
-    int P0 = 0, lim = 0;
-    float m = -INFINITY, l = 0.f;
-    bool q_pending = false, x_pending = false;
-    int kx = 0;  // the unit whose pair exchange is pending
-    for (int c = 0; ok; ++c) {
-      const int stage = c % kTcStages;
-      const bool got_f = mbar_wait(&full_bar[stage], (c / kTcStages) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, got_f)) {
-        fail();
-        break;
-      }
-      const int4 md = meta_sh[stage];
-      if (md.x < 0) break;  // the end of the stream
-      if (md.y == 0) {
-        // unit k starts: its keys and causal limits (its entry was waited for
-        // when unit k - 1 started); the next unit's Q rows go into the staging
-        // tile while this unit's first chunk is processed
-        x = tc_unit_of(a, uq_sh[k % kTcUq]);
-        P0 = x.L - a.K;
-        lim = P0 + (qr < rows ? qr / HG : 0);
-        m = -INFINITY;
-        l = 0.f;
-        const int sl = (k + 1) % kTcUq;
-        const bool got_u = mbar_wait(&uq_full[sl], ((k + 1) / kTcUq) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, got_u)) {
-          fail();
-          break;
-        }
-        const int4 en = uq_sh[sl];
-        mbar_arrive(&uq_empty[k % kTcUq]);
-        if (en.x >= 0) {
-          const TcUnit xn = tc_unit_of(a, en);
-          const uint4* src = qr < rows ? q_src(xn) : static_cast<const uint4*>(a.q);
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            cp_async16(smem_u32(qst_row + ((ch ^ (R & 7)) << 4)), src + (qr < rows ? ch : 0), qr < rows);
-          cp_async_commit();
-          q_pending = true;
-        }
-      }
-      const bool got_s = mbar_wait(&s_full[c & 1], (c >> 1) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, got_s)) {
-        fail();
-        break;
-      }
-      tc_fence_after();
-      const uint32_t mask = static_cast<uint32_t>(md.w);
-      const int kbase = x.t0 + md.y * kKC;
-      // every key in range, in a valid block and at or before P0 (seen by all rows)
-      const bool interior = kbase + kKC <= x.t1 && kbase + kKC - 1 <= P0 && mask == 0xFu;
-      const uint32_t scol = static_cast<uint32_t>((c & 1) * 64);
-      float sv[64];  // the chunk's 64 scores of this row
-      tmem_ld64(t_lane + scol, sv);
-      if (!interior) {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int t = kbase + j;
-          sv[j] = (t < x.t1 && ((mask >> (j >> 4)) & 1u) && t <= lim) ? sv[j] : -INFINITY;
-        }
-      }
-      // the maximum of all 64: a tree of three-input maxima
-      float mr;
-      {
-        float z[22], w[8];
-#pragma unroll
-        for (int i = 0; i < 21; ++i) z[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
-        z[21] = sv[63];
-#pragma unroll
-        for (int i = 0; i < 7; ++i) w[i] = fmax3(z[3 * i], z[3 * i + 1], z[3 * i + 2]);
-        w[7] = z[21];
-        mr = fmax3(fmax3(w[0], w[1], w[2]), fmax3(w[3], w[4], w[5]), fmaxf(w[6], w[7]));
-      }
-      const float mx = mr * sc;  // in the exp2 domain (sc > 0)
-      const bool move = mx > m + kTcRescale;
-      const float mn = move ? mx : m;
-      const float al = move ? ex2_approx(m - mn) : 1.f;
-      // with no valid key so far every score of the chunk is -inf: any finite
-      // reference gives the weights 0
-      const float mref = (mn == -INFINITY) ? 0.f : mn;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t hw[16], lw[16];
-      // this lane's 32 keys (a constant offset into sv, so sv stays in registers)
-      auto weights = [&](auto first) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = ex2_approx(fmaf(sv[decltype(first)::value + j], sc, -mref));
-          const float p1 = ex2_approx(fmaf(sv[decltype(first)::value + j + 1], sc, -mref));
-          ps[(j >> 1) & 3] += p0 + p1;
-          split_bf16x2(p0, p1, hw[j >> 1], lw[j >> 1]);
-        }
-      };
-      if (half)
-        weights(std::integral_constant<int, 32>{});
-      else
-        weights(std::integral_constant<int, 0>{});
-      // the P tile is free once P V of chunk c - 1 has completed and (after a
-      // unit's end) the high lanes have read the exchange; a moved reference
-      // maximum then rescales O (within a unit)
-      if (c >= 1) {
-        const bool got_o = mbar_wait(&o_done, (c - 1) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, got_o)) {
-          fail();
-          break;
-        }
-        tc_fence_after();
-      }
-      if (x_pending) {
-        const bool got_x = mbar_wait(&x_empty, kx & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, got_x)) {
-          fail();
-          break;
-        }
-        x_pending = false;
-      }
-      if (md.y > 0 && __any_sync(0xffffffffu, move)) {
-        float ov[64];
-        tmem_ld64(t_lane + kTcOCol, ov);
-#pragma unroll
-        for (int j = 0; j < 64; ++j) ov[j] *= al;
-        tmem_st64(t_lane + kTcOCol, ov);
-      }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t col = static_cast<uint32_t>(((half * 4 + kk) ^ swz) << 4);
-        *reinterpret_cast<uint4*>(pbuf + off_hi + col) =
-            make_uint4(hw[4 * kk], hw[4 * kk + 1], hw[4 * kk + 2], hw[4 * kk + 3]);
-        *reinterpret_cast<uint4*>(pbuf + off_lo + col) =
-            make_uint4(lw[4 * kk], lw[4 * kk + 1], lw[4 * kk + 2], lw[4 * kk + 3]);
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      mbar_arrive(&p_full);
-      l = l * al + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      m = mn;
-      if (q_pending) {
-        // the next unit's Q into its tensor-memory buffer (its S products wait
-        // for it; the buffer's previous unit has no S product left)
-        cp_async_wait<0>();
-        uint4 v[8];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) v[ch] = *reinterpret_cast<const uint4*>(qst_row + ((ch ^ (R & 7)) << 4));
-        q_to_tmem(v, (k + 1) & 1);
-        q_pending = false;
-      }
-      if (md.y == md.z - 1) {
-        // unit k ends: its O rows, the two halves of the pair added, and its
-        // partial for the combine kernel
-        const bool got_o = mbar_wait(&o_done, c & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, got_o)) {
-          fail();
-          break;
-        }
-        tc_fence_after();
-        float o[64];
-        tmem_ld64(t_lane + kTcOCol, o);
-        float* xo = reinterpret_cast<float*>(pbuf) + qr * 64;
-        if (half) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            reinterpret_cast<float4*>(xo)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-          xl_sh[qr] = l;
-          mbar_arrive(&x_full);
-        } else {
-          const bool got_x = mbar_wait(&x_full, k & 1, abort_flag);
-          if (!__all_sync(0xffffffffu, got_x)) {
-            fail();
-            break;
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float4 xv = reinterpret_cast<const float4*>(xo)[j];
-            o[4 * j] += xv.x;
-            o[4 * j + 1] += xv.y;
-            o[4 * j + 2] += xv.z;
-            o[4 * j + 3] += xv.w;
-          }
-          const float lt = l + xl_sh[qr];
-          mbar_arrive(&x_empty);
-          if (qr < rows) {
-            const size_t idx =
-                (static_cast<size_t>(x.j) * n_samp + static_cast<size_t>(x.r) * a.K + qr / HG) * a.H +
-                x.g * HG + qr % HG;
-            float4* dst = reinterpret_cast<float4*>(a.part_o + idx * 64);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-            a.part_ml[idx * 2] = m;
-            a.part_ml[idx * 2 + 1] = lt;
-          }
-        }
-        x_pending = true;
-        kx = k;
-        ++k;
-      }
-    }
-    tc_fence_before();
-  }
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, kTcTmemCols);
-  }
-  // the last CTA to finish leaves the unit counter at zero for the next launch
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
-      a.sched[0] = 0u;
-      a.sched[1] = 0u;
-      __threadfence();
-    }
-  }
-}
-
 // out[s][h*hd + d] = sum_j 2^(m_j - M) o_j[d] / (sum_j 2^(m_j - M) l_j + 2^(sink_h - M))
 // (the sink term only with sink logits) over the splits j that hold keys of the request (j * split_len < L; the CTAs of the
 // others return at once and leave no partial).  One warp per (sample row,
@@ -1616,17 +752,6 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
                ? PE_OK
                : PE_ERR_CUDA;
   };
-  if (a.hd == 64 && rows <= kTcRows && waves && !a.cluster && a.sched) {
-    // several waves of units: the persistent tensor-core kernel, two CTAs per SM
-    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    const long units = static_cast<long>(a.n_splits) * a.G * a.B;
-    const unsigned ctas = static_cast<unsigned>(std::min<long>(2L * sms, units));
-    if (launch_pdl(attn_tc_kernel, dim3(ctas), dim3(192), kTcSmem, st, kmap, vmap, a) != cudaSuccess)
-      return PE_ERR_CUDA;
-    return combine(a);
-  }
   if (a.hd == 64) {
     // the register-capped instance (two CTAs per SM) for several waves
     kern = sh.kg == 2 ? (waves ? attn_tma_kernel<64, 2, 2> : attn_tma_kernel<64, 2, 1>)

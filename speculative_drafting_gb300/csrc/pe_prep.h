@@ -175,10 +175,6 @@ struct AttnArgs {
   const float* sink;  // [H] per-head sink logit (natural units), nullable
   int k_min;          // seq_len below this is an input error (the draft depth K)
   uint32_t* status;
-  // two words of device memory, zero before the first launch (the persistent
-  // tensor-core kernel hands out its work units with the first and leaves both
-  // at zero when it ends); null: that kernel is not used
-  uint32_t* sched;
 };
 int attention_split_count(int B, int G, int max_blocks, int bs, int num_sms);
 void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, int num_sms,

@@ -141,10 +141,10 @@ def test_random_steps(seed):
 
 
 def test_bad_context_block_at_a_batch_of_several_waves():
-    """A context block id out of range in one request of a batch large enough that
-    attention runs as the persistent tensor-core kernel (160 requests x 2 KV heads):
-    the status word flags it, the step completes, the keys of that block are
-    skipped, and every other request still matches the oracle."""
+    """A context block id out of range in one request of a batch whose attention
+    grid runs several waves (160 requests x 2 KV heads, partials merged by the
+    combine kernel): the status word flags it, the step completes, the keys of
+    that block are skipped, and every other request still matches the oracle."""
     torch = cuda_or_skip()
     from speculative_drafting_gb300 import binding as Bnd
 
@@ -173,9 +173,9 @@ def test_bad_context_block_at_a_batch_of_several_waves():
     assert ((draft[bad * K:(bad + 1) * K] >= 0) & (draft[bad * K:(bad + 1) * K] < wl.dims.vocab)).all()
 
 
-def test_batch_past_the_longest_first_order():
-    """1100 requests: more than the persistent attention orders longest first, so
-    its units go out split-major.  Metadata bit-exact; a sample of requests (the
+def test_batch_of_1100_requests():
+    """1100 requests (past the drafter-input kernel's self-indexing limit, an
+    attention grid of many waves).  Metadata bit-exact; a sample of requests (the
     first, the last and some between) matches the oracle."""
     torch = cuda_or_skip()
     wl, b, w, kc, vc, r = setup("small_prenorm", batch=1100, n_prev=2, ctx=("uniform", 0, 120),
