@@ -95,7 +95,6 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
-  const int split = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
   const int HG = a.H / a.G;
   const int rows = a.K * HG;
   const AttnShape sh = attn_shape(rows);
@@ -122,6 +121,28 @@ __global__ void __launch_bounds__(32 * (kMaxComputeWarps + 1), MINB)
   pdl_wait();
   fence_proxy_async();  // the zeroed ring is visible to the TMA writes that follow
   __syncthreads();
+
+  // this CTA's unit: (split, KV head, request) from the grid, or entry
+  // blockIdx.x of the longest-first order (attn_order_kernel); past its end the
+  // CTA has nothing to do
+  int split = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+  if (a.order) {
+    const int n = a.order[0].x;
+    const int idx = static_cast<int>(blockIdx.x);
+    if (n >= 0) {
+      if (idx >= n) return;
+      const int2 e = a.order[1 + idx];
+      r = e.x;
+      split = e.y / a.G;
+      g = e.y - split * a.G;
+    } else {
+      // split-major by index (batches too large to order)
+      const int BG = a.B * a.G;
+      split = idx / BG;
+      r = (idx - split * BG) / a.G;
+      g = idx - split * BG - r * a.G;
+    }
+  }
 
   int L = a.seq_len[r];
   const int Lmax = a.max_blocks * a.bs;
@@ -711,13 +732,114 @@ void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, 
   if (n_splits < 1) n_splits = 1;
 }
 
+// The order in which a grid of several waves takes its units (split j, KV head
+// g, request r), longest first: the hardware starts CTAs in index order as SMs
+// free up, and the last units to start decide when the grid ends.  Every full
+// split (split_len keys) comes first, in the grid's order (request, KV head,
+// split); then each request's last,
+// shorter split by its 64-key chunks, most first and in request order among
+// equals; an empty context's first split last.  Splits past a request's keys
+// are left out.  order[0].x = the number of entries (-1: more than kOrdMax
+// requests, the grid takes its units split-major by index); order[1 + i] =
+// (r, j G + g).  One warp.
+constexpr int kOrdMax = 1024;
+__global__ void __launch_bounds__(32) attn_order_kernel(const AttnArgs a, int2* order) {
+  __shared__ int full_pre[kOrdMax + 1];  // full splits of the requests before r
+  __shared__ int bstart[34];             // bucket offsets (33 buckets: 0..32 chunks)
+  pdl_trigger();
+  pdl_wait();  // the lengths come from the metadata kernel; the last grid has read order
+  const int lane = threadIdx.x;
+  if (a.B > kOrdMax) {
+    if (lane == 0) order[0] = make_int2(-1, 0);
+    return;
+  }
+  const int Lmax = a.max_blocks * a.bs;
+  // -> the bucket of request r's last split (its chunks, 1..32; 0: an empty
+  // context; -1: none), nf = its full splits
+  auto req_class = [&](int r, int& nf) -> int {
+    const int L = min(max(a.seq_len[r], 0), Lmax);
+    nf = min(L / a.split_len, a.n_splits);
+    const int rem = L - nf * a.split_len;
+    if (rem > 0) return min((rem + kKC - 1) / kKC, 32);
+    return L == 0 ? 0 : -1;
+  };
+  for (int i = lane; i < 34; i += 32) bstart[i] = 0;
+  if (lane == 0) full_pre[0] = 0;
+  __syncwarp();
+  int base = 0;
+  for (int r0 = 0; r0 < a.B; r0 += 32) {
+    const int r = r0 + lane;
+    int nf = 0, bk = -1;
+    if (r < a.B) bk = req_class(r, nf);
+    int incl = nf;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    if (r < a.B) full_pre[r + 1] = base + incl;
+    if (bk >= 0) atomicAdd(&bstart[bk], 1);
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    int acc = 0;
+    for (int bkt = 32; bkt >= 0; --bkt) {
+      const int c = bstart[bkt];
+      bstart[bkt] = acc;
+      acc += c;
+    }
+    bstart[33] = acc;
+  }
+  __syncwarp();
+  const int n_full = base * a.G;
+  const int n_live = n_full + bstart[33] * a.G;
+  // the full splits in the grid's own order (request, then KV head, then
+  // split): entry u belongs to request r with G full_pre[r] <= u < G full_pre[r + 1]
+  for (int u = lane; u < n_full; u += 32) {
+    int lo = 0, hi = a.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (full_pre[mid] * a.G <= u)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int nf = full_pre[lo + 1] - full_pre[lo];
+    const int loc = u - full_pre[lo] * a.G;
+    const int gg = loc / nf, j = loc - gg * nf;
+    order[1 + u] = make_int2(lo, j * a.G + gg);
+  }
+  // the last splits: each request's place in its bucket, in request order
+  for (int r0 = 0; r0 < a.B; r0 += 32) {
+    const int r = r0 + lane;
+    int nf = 0, bk = -1;
+    if (r < a.B) bk = req_class(r, nf);
+    const unsigned same = __match_any_sync(0xffffffffu, bk);
+    const int s0 = bk >= 0 ? bstart[bk] : 0;
+    __syncwarp();
+    const unsigned below = same & ((1u << lane) - 1u);
+    if (bk >= 0) {
+      const int pos = s0 + __popc(below);
+      const int j = min(nf, a.n_splits - 1);
+      for (int gg = 0; gg < a.G; ++gg) order[1 + n_full + pos * a.G + gg] = make_int2(r, j * a.G + gg);
+      if (below == 0) bstart[bk] = s0 + __popc(same);
+    }
+    __syncwarp();
+  }
+  if (lane == 0) order[0] = make_int2(n_live, 0);
+}
+
 size_t attention_scratch_bytes(int B, int K, int H, int hd, int n_splits) {
   const size_t sh = static_cast<size_t>(n_splits) * B * K * H;
   size_t o = sh * hd * sizeof(float);
   o = (o + 255) / 256 * 256;
   size_t ml = sh * 2 * sizeof(float);
   ml = (ml + 255) / 256 * 256;
-  return o + ml;
+  // the unit order: at most n_splits * B * H units (G <= H), plus the count
+  size_t ord = (static_cast<size_t>(n_splits) * B * H + 1) * sizeof(int2);
+  ord = (ord + 255) / 256 * 256;
+  return o + ml + ord;
 }
 
 int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
@@ -793,7 +915,21 @@ int launch_attention(const AttnArgs& a, int dtype, cudaStream_t st) {
   }
   AttnArgs ag = a;
   ag.cluster = 0;
-  if (launch_pdl(kern, grid, block, smem, st, kmap, vmap, ag) != cudaSuccess) return PE_ERR_CUDA;
+  ag.order = nullptr;
+  dim3 g3 = grid;
+  if (waves && a.hd == 64) {
+    // several waves at head size 64: the units in the longest-first order, one
+    // CTA per entry; the order sits after the partials (attention_scratch_bytes).
+    // Head size 128 keeps the 3-D grid: there the order measured slower (Llama-8B
+    // shape, 32 requests of 32K keys: 1337 -> 1396 us a step)
+    const size_t sh = static_cast<size_t>(a.n_splits) * a.B * a.K * a.H;
+    const size_t ml = (sh * 2 * sizeof(float) + 255) / 256 * 256;
+    ag.order = reinterpret_cast<int2*>(reinterpret_cast<char*>(a.part_ml) + ml);
+    if (launch_pdl(attn_order_kernel, dim3(1), dim3(32), 0, st, ag, ag.order) != cudaSuccess)
+      return PE_ERR_CUDA;
+    g3 = dim3(static_cast<unsigned>(static_cast<size_t>(a.n_splits) * a.G * a.B));
+  }
+  if (launch_pdl(kern, g3, block, smem, st, kmap, vmap, ag) != cudaSuccess) return PE_ERR_CUDA;
   return combine(ag);
 }
 

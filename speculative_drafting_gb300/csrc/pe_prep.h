@@ -175,6 +175,9 @@ struct AttnArgs {
   const float* sink;  // [H] per-head sink logit (natural units), nullable
   int k_min;          // seq_len below this is an input error (the draft depth K)
   uint32_t* status;
+  // set by launch_attention for grids of several waves at head size 64: the longest-first unit
+  // order (scratch after the partials); null: the 3-D grid (split, KV head, request)
+  int2* order;
 };
 int attention_split_count(int B, int G, int max_blocks, int bs, int num_sms);
 void plan_attention(int B, int G, int K, int H, int hd, int max_blocks, int bs, int num_sms,
