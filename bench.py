@@ -237,6 +237,20 @@ def oracle_sample(wl, batch, w, kc, vc, budget_s=20.0):
 # ----------------------------------------------------------------------------- reference arm
 
 
+def warm_up(call, n, limit_s=60.0):
+    """n untimed calls of call() before a reference arm's timed samples (the
+    oracle's first calls pay numpy's and the BLAS library's set-up), at most
+    limit_s in all.  Returns how many ran."""
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(max(0, n)):
+        call()
+        done += 1
+        if time.perf_counter() - t0 > limit_s:
+            break
+    return done
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -244,17 +258,8 @@ def run_reference(args, rank, world):
     batch = W.make_batch(wl)
     w = W.make_weights(wl)
     kc, vc = W.make_kv_cache(wl, batch["num_blocks"])
-    from oracle import pe_oracle as O
-
-    # W untimed warm-up steps, one request each (the first calls pay numpy's and
-    # the BLAS library's set-up), at most a minute in all
-    n_warm = 0
-    t_warm = time.perf_counter()
-    for _ in range(max(0, args.warmup)):
-        O.draft_step(wl.dims, w, batch, kc, vc, requests=[0])
-        n_warm += 1
-        if time.perf_counter() - t_warm > 60:
-            break
+    # a zero budget: one request per warm-up step
+    n_warm = warm_up(lambda: oracle_sample(wl, batch, w, kc, vc, budget_s=0.0), args.warmup)
     # each step: the oracle on whole requests of the workload, bounded in time;
     # the whole run stops after a few minutes
     per = []
@@ -689,6 +694,7 @@ def run_verify(args, rank, world, local):
         if rank != 0:
             return
         b = W.make_verify_batch(wl)
+        n_warm = warm_up(lambda: verify_oracle_sample(wl, b, budget_s=0.0), args.warmup)
         per, sample, threads = [], "", 1
         t_all = time.perf_counter()
         for _ in range(max(1, args.steps)):
@@ -699,7 +705,7 @@ def run_verify(args, rank, world, local):
         us = statistics.median(per)
         print(json.dumps({
             "impl": "reference", "metric": VERIFY_METRIC, "value": us, "unit": "us",
-            "n_gpus": args.gpus, "steps": len(per), "warmup": 0, "ms_per_step": us / 1e3,
+            "n_gpus": args.gpus, "steps": len(per), "warmup": n_warm, "ms_per_step": us / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl.name, "global_batch": wl.batch,
                                             "description": wl.description},
@@ -868,6 +874,7 @@ def run_cod(args, rank, world, local):
         if rank != 0:
             return
         b = W.make_cod_batch(wl)
+        n_warm = warm_up(lambda: cod_oracle_sample(wl, b, budget_s=0.0), args.warmup)
         per, sample, threads = [], "", 1
         t_all = time.perf_counter()
         for _ in range(max(1, args.steps)):
@@ -878,7 +885,7 @@ def run_cod(args, rank, world, local):
         us = statistics.median(per)
         print(json.dumps({
             "impl": "reference", "metric": COD_METRIC, "value": us, "unit": "us",
-            "n_gpus": args.gpus, "steps": len(per), "warmup": 0, "ms_per_step": us / 1e3,
+            "n_gpus": args.gpus, "steps": len(per), "warmup": n_warm, "ms_per_step": us / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
             "data": "synthetic", "config": {"workload": wl.name, "global_batch": wl.batch,
                                             "description": wl.description},
@@ -1055,6 +1062,7 @@ def run_prep_reference(args, rank):
     wl = W.get(args.workload)
     batch = W.make_batch(wl)
     w = W.make_weights(wl)
+    n_warm = warm_up(lambda: prep_oracle_sample(wl, batch, w, budget_s=0.0), args.warmup)
     per, sample, threads = [], "", 1
     t_all = time.perf_counter()
     for _ in range(max(1, args.steps)):
@@ -1065,7 +1073,7 @@ def run_prep_reference(args, rank):
     us = statistics.median(per)
     print(json.dumps({
         "impl": "reference", "metric": PREP_METRIC, "value": us, "unit": "us", "n_gpus": args.gpus,
-        "steps": len(per), "warmup": 0, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "steps": len(per), "warmup": n_warm, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "global_batch": wl.batch, "K": wl.dims.K,
                    "description": wl.description},
